@@ -1,0 +1,88 @@
+"""Seeded synthetic inputs for dense attention (shared by the CUDA path's tests and the oracle's).
+
+This module draws random numbers and rounds them to BF16; it holds none of the
+attention arithmetic. Both the GPU parity tests and the CPU oracle take their
+Q, K, V from here, so the two sides always see bit-identical inputs.
+
+Recipe (the pages' workloads are iid-normal BF16 tensors of shape
+[batch, heads, seq, head_dim], see "Sıfırdan yazılan CUDA attention kerneli...",
+section "Kernel işini nasıl bölümlendiriyor"):
+
+* one ``numpy.random.Generator(PCG64(seed))`` stream per call;
+* float32 standard normals drawn in the order Q, K, V, each as a full
+  ``[B, H, N, d]`` block in C order;
+* Q and K (not V) multiplied by ``qk_mult`` in float32 (the peaked-softmax
+  workload multiplies them by 3);
+* each float32 rounded to BF16 with round-to-nearest-even, done here with
+  integer operations so the result is the same on every host.
+
+numpy's PCG64 stream and its float32 ziggurat normal sampler are
+platform-independent, which keeps inputs identical between an x86 host and an
+Arm GPU host.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+__all__ = [
+    "f32_to_bf16_bits",
+    "bf16_bits_to_f32",
+    "make_qkv",
+    "sample_rows",
+]
+
+
+def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
+    """Round float32 values to BF16 (round to nearest, ties to even); return the uint16 bit patterns.
+
+    Finite inputs only (the generators never produce NaN or Inf).
+    """
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    u = x.view(np.uint32).astype(np.uint64)
+    bias = ((u >> np.uint64(16)) & np.uint64(1)) + np.uint64(0x7FFF)
+    return ((u + bias) >> np.uint64(16)).astype(np.uint16)
+
+
+def bf16_bits_to_f32(b: np.ndarray) -> np.ndarray:
+    """Widen BF16 bit patterns to float32 exactly."""
+    b = np.ascontiguousarray(b, dtype=np.uint16)
+    return (b.astype(np.uint32) << np.uint32(16)).view(np.float32)
+
+
+def make_qkv(B: int, H: int, Nq: int, Nk: int, d: int = 128, seed: int = 0,
+             qk_mult: float = 1.0, dv: int | None = None):
+    """Return (q, k, v) as uint16 BF16 bit arrays of shapes [B,H,Nq,d], [B,H,Nk,d], [B,H,Nk,dv]."""
+    dv = d if dv is None else dv
+    rng = np.random.Generator(np.random.PCG64(seed))
+    q = rng.standard_normal((B, H, Nq, d), dtype=np.float32)
+    k = rng.standard_normal((B, H, Nk, d), dtype=np.float32)
+    v = rng.standard_normal((B, H, Nk, dv), dtype=np.float32)
+    if qk_mult != 1.0:
+        m = np.float32(qk_mult)
+        q = q * m
+        k = k * m
+    return f32_to_bf16_bits(q), f32_to_bf16_bits(k), f32_to_bf16_bits(v)
+
+
+def sample_rows(B: int, H: int, Nq: int, per_head: int = 64, seed_base: int = 1_000_003,
+                extra_head0=(0, 127, 128, -1)) -> np.ndarray:
+    """Seeded sample of query rows, returned as sorted flat indices ``(b*H + h)*Nq + i``.
+
+    For every (b, h) a separate PCG64 stream seeded with ``seed_base + b*H + h``
+    picks ``per_head`` distinct rows. Rows listed in ``extra_head0`` (negative
+    values count from the end) are always added for head (0, 0): they sit on
+    128-row tile boundaries, where indexing mistakes show first.
+    """
+    out = []
+    for bh in range(B * H):
+        rng = np.random.Generator(np.random.PCG64(seed_base + bh))
+        n = min(per_head, Nq)
+        rows = rng.choice(Nq, size=n, replace=False)
+        out.append(bh * Nq + np.asarray(rows, dtype=np.int64))
+    extra = []
+    for r in extra_head0:
+        r = r + Nq if r < 0 else r
+        if 0 <= r < Nq:
+            extra.append(r)
+    out.append(np.asarray(extra, dtype=np.int64))
+    return np.unique(np.concatenate(out))

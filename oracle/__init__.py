@@ -1,0 +1,140 @@
+"""FP64 CPU oracle for dense scaled-dot-product attention -- TEST INFRASTRUCTURE ONLY.
+
+Only the test suite, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this package. The library under test never does, and
+this package imports nothing from it: the two share no code. Inputs are BF16
+bit patterns (uint16 numpy arrays), as produced by the seeded generators.
+
+The arithmetic lives in ``attn_ref.c`` (plain C, double precision, OpenMP over
+query rows); this module compiles it with gcc on first use and marshals numpy
+arrays. See ``attn_ref.c`` for the definition it follows and its citations.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+__all__ = ["build", "Oracle", "default", "attention_rows", "attention", "probs", "max_threads", "LIB_PATH"]
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "attn_ref.c")
+LIB_PATH = os.path.join(_HERE, "libattn_ref.so")
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False, src: str = _SRC, out: str = LIB_PATH) -> str:
+    """Compile attn_ref.c into a shared library (gcc, -O2, OpenMP when available)."""
+    if not force and os.path.exists(out) and os.path.getmtime(out) >= os.path.getmtime(src):
+        return out
+    tmp = out + f".tmp{os.getpid()}"
+    base = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fno-fast-math", src, "-o", tmp, "-lm"]
+    try:
+        subprocess.run(base[:1] + ["-fopenmp"] + base[1:], check=True, capture_output=True, text=True)
+    except subprocess.CalledProcessError:
+        subprocess.run(base, check=True, capture_output=True, text=True)
+    os.replace(tmp, out)
+    return out
+
+
+class Oracle:
+    """The oracle bound to one compiled copy of attn_ref.c (the default one, or a test's own build)."""
+
+    def __init__(self, lib_path: str):
+        lib = ctypes.CDLL(lib_path)
+        i64, dbl, vp = ctypes.c_int64, ctypes.c_double, ctypes.c_void_p
+        lib.attn_ref_rows_f64.argtypes = [vp, vp, vp, i64, i64, i64, i64, i64, dbl, vp, i64, vp, vp, ctypes.c_int]
+        lib.attn_ref_rows_f64.restype = ctypes.c_int
+        lib.attn_ref_probs_f64.argtypes = [vp, vp, i64, i64, i64, i64, dbl, vp]
+        lib.attn_ref_probs_f64.restype = ctypes.c_int
+        lib.attn_ref_max_threads.argtypes = []
+        lib.attn_ref_max_threads.restype = ctypes.c_int
+        self.lib = lib
+        self.path = lib_path
+
+    def max_threads(self) -> int:
+        return self.lib.attn_ref_max_threads()
+
+    def attention_rows(self, q, k, v, scale: float, rows=None, nthreads: int = 0):
+        """O and LSE (float64) for selected query rows.
+
+        q [B,H,Nq,d], k [B,H,Nk,d], v [B,H,Nk,dv] as uint16 BF16 bits. ``rows`` holds
+        flat ids ``(b*H + h)*Nq + i``; None means every row. Returns
+        (o [len(rows), dv], lse [len(rows)]).
+        """
+        q, k, v = _u16(q, 4), _u16(k, 4), _u16(v, 4)
+        B, H, Nq, d = q.shape
+        Nk, dv = k.shape[2], v.shape[3]
+        if k.shape != (B, H, Nk, d) or v.shape[:3] != (B, H, Nk):
+            raise ValueError(f"shape mismatch q{q.shape} k{k.shape} v{v.shape}")
+        if rows is None:
+            rows = np.arange(B * H * Nq, dtype=np.int64)
+        rows = np.ascontiguousarray(rows, dtype=np.int64)
+        o = np.empty((rows.size, dv), dtype=np.float64)
+        lse = np.empty(rows.size, dtype=np.float64)
+        rc = self.lib.attn_ref_rows_f64(_ptr(q), _ptr(k), _ptr(v), B * H, Nq, Nk, d, dv, float(scale),
+                                        _ptr(rows), rows.size, _ptr(o), _ptr(lse), int(nthreads))
+        if rc != 0:
+            raise ValueError(f"attn_ref_rows_f64 failed with status {rc}")
+        return o, lse
+
+    def attention(self, q, k, v, scale: float, nthreads: int = 0):
+        """Full O [B,H,Nq,dv] and LSE [B,H,Nq] in float64."""
+        B, H, Nq, _ = q.shape
+        dv = v.shape[3]
+        o, lse = self.attention_rows(q, k, v, scale, None, nthreads)
+        return o.reshape(B, H, Nq, dv), lse.reshape(B, H, Nq)
+
+    def probs(self, q, k, scale: float):
+        """Full P = softmax_row(scale * Q K^T) as float64 [B,H,Nq,Nk] (small shapes only)."""
+        q, k = _u16(q, 4), _u16(k, 4)
+        B, H, Nq, d = q.shape
+        Nk = k.shape[2]
+        p = np.empty((B, H, Nq, Nk), dtype=np.float64)
+        rc = self.lib.attn_ref_probs_f64(_ptr(q), _ptr(k), B * H, Nq, Nk, d, float(scale), _ptr(p))
+        if rc != 0:
+            raise ValueError(f"attn_ref_probs_f64 failed with status {rc}")
+        return p
+
+
+def default() -> Oracle:
+    """The oracle built from this directory's attn_ref.c (compiled on first use)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            build()
+            _lib = Oracle(LIB_PATH)
+    return _lib
+
+
+def _u16(a: np.ndarray, ndim: int) -> np.ndarray:
+    a = np.ascontiguousarray(a)
+    if a.dtype != np.uint16:
+        raise TypeError(f"expected BF16 bit patterns as uint16, got {a.dtype}")
+    if a.ndim != ndim:
+        raise ValueError(f"expected {ndim} dims, got shape {a.shape}")
+    return a
+
+
+def _ptr(a: np.ndarray):
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+def max_threads() -> int:
+    return default().max_threads()
+
+
+def attention_rows(q, k, v, scale: float, rows=None, nthreads: int = 0):
+    return default().attention_rows(q, k, v, scale, rows, nthreads)
+
+
+def attention(q, k, v, scale: float, nthreads: int = 0):
+    return default().attention(q, k, v, scale, nthreads)
+
+
+def probs(q, k, scale: float):
+    return default().probs(q, k, scale)

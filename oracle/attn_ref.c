@@ -1,0 +1,194 @@
+/*
+ * attn_ref.c -- FP64 CPU oracle for dense scaled-dot-product attention.
+ *
+ * TEST INFRASTRUCTURE ONLY. Nothing in the product path links, loads or calls
+ * this file; only the test suite, the smoke check and the CPU-baseline leg of
+ * the benchmark do. It shares no code, header or constant with the CUDA path.
+ *
+ * What it computes is the plain definition written out, one query row at a time,
+ * with no tiling and no online recurrence:
+ *
+ *   S = scale * Q K^T,   P = softmax_row(S),   O = P V
+ *
+ * ("FlashAttention'ı Anlamak Bölüm 1", section 0.2 Notasyon, with the optional
+ * mask/bias B taken as zero; the scale is the caller's, applied to the scores as
+ * in the "Алгоритм Flash Attention 2" pseudocode of "Flash Attention на 5090 в
+ * CUDA C++"). The same notes (section 0.1) state that FlashAttention reaches this
+ * exact result, only in a different floating-point order, so a tiled GPU kernel
+ * must agree with it up to rounding.
+ *
+ * Per query row i of head (b,h), in double precision from BF16 inputs widened
+ * exactly:
+ *   1. s_j = scale * sum_c q[i,c] * k[j,c]           for every key j
+ *   2. m   = max_j s_j
+ *   3. l   = sum_j exp(s_j - m)
+ *   4. o_c = (sum_j exp(s_j - m) * v[j,c]) / l
+ *   5. lse = m + log(l)     (natural log of sum_j exp(s_j))
+ * Subtracting m leaves P unchanged (the common factor exp(-m) cancels) and keeps
+ * exp() from overflowing; step 5 adds it back.
+ *
+ * The log-sum-exp output is not defined on the pages; it is read here as the
+ * natural logarithm of the softmax denominator in scaled-score units, one value
+ * per query row.
+ *
+ * Parity pins for every function below live in tests/test_oracle.py.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* Status codes of this file (independent of the library's own). */
+#define REF_OK 0
+#define REF_EINVAL (-1)
+#define REF_ENOMEM (-2)
+
+static double bf16_to_f64(uint16_t bits)
+{
+    uint32_t u = ((uint32_t)bits) << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+/* step 1: s_j = scale * (q_i . k_j) for every key j of one head */
+static void row_scores(const uint16_t *qi, const uint16_t *kh, int64_t Nk, int64_t d,
+                       double scale, double *s)
+{
+    for (int64_t j = 0; j < Nk; j++) {
+        const uint16_t *kj = kh + j * d;
+        double acc = 0.0;
+        for (int64_t c = 0; c < d; c++)
+            acc += bf16_to_f64(qi[c]) * bf16_to_f64(kj[c]);
+        s[j] = scale * acc;
+    }
+}
+
+/* step 2: m = max_j s_j */
+static double row_max(const double *s, int64_t Nk)
+{
+    double m = s[0];
+    for (int64_t j = 1; j < Nk; j++)
+        if (s[j] > m) m = s[j];
+    return m;
+}
+
+/* step 3: overwrite s_j with exp(s_j - m) and return their sum l */
+static double row_exp_sum(double *s, int64_t Nk, double m)
+{
+    double l = 0.0;
+    for (int64_t j = 0; j < Nk; j++) {
+        s[j] = exp(s[j] - m);
+        l += s[j];
+    }
+    return l;
+}
+
+/* One query row: writes o[0..dv) and *lse. s is caller scratch of Nk doubles. */
+static void attend_row(const uint16_t *qi, const uint16_t *kh, const uint16_t *vh,
+                       int64_t Nk, int64_t d, int64_t dv, double scale,
+                       double *s, double *o, double *lse)
+{
+    row_scores(qi, kh, Nk, d, scale, s);
+    double m = row_max(s, Nk);
+    double l = row_exp_sum(s, Nk, m);
+    /* step 4: weighted sum of value rows */
+    for (int64_t c = 0; c < dv; c++) {
+        double acc = 0.0;
+        for (int64_t j = 0; j < Nk; j++)
+            acc += s[j] * bf16_to_f64(vh[j * dv + c]);
+        o[c] = acc / l;
+    }
+    /* step 5 */
+    *lse = m + log(l);
+}
+
+/*
+ * attn_ref_rows_f64: O and LSE for a chosen set of query rows.
+ *
+ *   q   [BH, Nq, d]   BF16 bit patterns, C order     (BH = batch * heads)
+ *   k   [BH, Nk, d]
+ *   v   [BH, Nk, dv]
+ *   sel [nsel]        flat row ids bh*Nq + i, each in [0, BH*Nq)
+ *   o   [nsel, dv]    output, float64
+ *   lse [nsel]        output, float64
+ *   nthreads          OpenMP threads (<= 0: the runtime's default)
+ *
+ * Returns REF_OK, REF_EINVAL for a bad size or row id, REF_ENOMEM.
+ */
+int attn_ref_rows_f64(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                      int64_t BH, int64_t Nq, int64_t Nk, int64_t d, int64_t dv,
+                      double scale, const int64_t *sel, int64_t nsel,
+                      double *o, double *lse, int nthreads)
+{
+    if (BH < 0 || Nq < 0 || Nk < 1 || d < 1 || dv < 1 || nsel < 0) return REF_EINVAL;
+    if (nsel == 0) return REF_OK;
+    if (!q || !k || !v || !sel || !o || !lse) return REF_EINVAL;
+    for (int64_t r = 0; r < nsel; r++)
+        if (sel[r] < 0 || sel[r] >= BH * Nq) return REF_EINVAL;
+
+    int failed = 0;
+#ifdef _OPENMP
+    int nt = nthreads > 0 ? nthreads : omp_get_max_threads();
+#pragma omp parallel num_threads(nt)
+#else
+    (void)nthreads;
+#endif
+    {
+        double *s = (double *)malloc((size_t)Nk * sizeof(double));
+        if (!s) {
+#ifdef _OPENMP
+#pragma omp atomic write
+#endif
+            failed = 1;
+        } else {
+#ifdef _OPENMP
+#pragma omp for schedule(dynamic, 1)
+#endif
+            for (int64_t r = 0; r < nsel; r++) {
+                int64_t bh = sel[r] / Nq, i = sel[r] % Nq;
+                attend_row(q + (bh * Nq + i) * d, k + bh * Nk * d, v + bh * Nk * dv,
+                           Nk, d, dv, scale, s, o + r * dv, lse + r);
+            }
+            free(s);
+        }
+    }
+    return failed ? REF_ENOMEM : REF_OK;
+}
+
+/*
+ * attn_ref_probs_f64: the full probability matrix P = softmax_row(scale * Q K^T),
+ * p [BH, Nq, Nk], for small shapes (tests of the row normalisation).
+ */
+int attn_ref_probs_f64(const uint16_t *q, const uint16_t *k,
+                       int64_t BH, int64_t Nq, int64_t Nk, int64_t d,
+                       double scale, double *p)
+{
+    if (BH < 0 || Nq < 0 || Nk < 1 || d < 1) return REF_EINVAL;
+    if (BH * Nq == 0) return REF_OK;
+    if (!q || !k || !p) return REF_EINVAL;
+    for (int64_t bh = 0; bh < BH; bh++) {
+        for (int64_t i = 0; i < Nq; i++) {
+            double *s = p + (bh * Nq + i) * Nk;
+            row_scores(q + (bh * Nq + i) * d, k + bh * Nk * d, Nk, d, scale, s);
+            double m = row_max(s, Nk);
+            double l = row_exp_sum(s, Nk, m);
+            for (int64_t j = 0; j < Nk; j++) s[j] /= l;
+        }
+    }
+    return REF_OK;
+}
+
+/* Number of threads an OpenMP region of this library would use by default. */
+int attn_ref_max_threads(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}

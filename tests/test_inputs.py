@@ -1,0 +1,45 @@
+"""The seeded input generators: BF16 rounding, determinism and row sampling."""
+import numpy as np
+import pytest
+
+from dense_attention_forward_fwd_gb300.inputs import bf16_bits_to_f32, f32_to_bf16_bits, make_qkv, sample_rows
+
+
+def test_bf16_rounding_is_nearest_even():
+    # 1 + 2^-8 is halfway between 1 and 1 + 2^-7: ties go to the even mantissa (1.0)
+    x = np.array([1.0, 1 + 2**-8, 1 + 3 * 2**-8, -(1 + 2**-8), 1 + 2**-8 + 2**-20, 3.0e38], dtype=np.float32)
+    got = bf16_bits_to_f32(f32_to_bf16_bits(x))
+    want = np.array([1.0, 1.0, 1 + 2 * 2**-7, -1.0, 1 + 2**-7, 3.0e38], dtype=np.float32)
+    assert np.allclose(got[:5], want[:5], rtol=0, atol=0)
+    assert abs(got[5] - 3.0e38) / 3.0e38 < 2**-8
+
+
+def test_bf16_rounding_matches_torch():
+    torch = pytest.importorskip("torch")
+    x = np.random.Generator(np.random.PCG64(1)).standard_normal(100000, dtype=np.float32) * 7
+    ours = f32_to_bf16_bits(x)
+    theirs = torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(ours, theirs)
+
+
+def test_make_qkv_is_deterministic_and_ordered():
+    a = make_qkv(1, 2, 3, 5, d=8, seed=3)
+    b = make_qkv(1, 2, 3, 5, d=8, seed=3)
+    for x, y in zip(a, b):
+        assert np.array_equal(x, y)
+    assert a[0].shape == (1, 2, 3, 8) and a[1].shape == (1, 2, 5, 8) and a[2].shape == (1, 2, 5, 8)
+    c = make_qkv(1, 2, 3, 5, d=8, seed=3, qk_mult=3.0)
+    assert np.array_equal(c[2], a[2])  # V is not scaled
+    assert not np.array_equal(c[0], a[0])
+    # Q drawn first: the Q block equals the first draws of the stream
+    g = np.random.Generator(np.random.PCG64(3)).standard_normal((1, 2, 3, 8), dtype=np.float32)
+    assert np.array_equal(a[0], f32_to_bf16_bits(g))
+
+
+def test_sample_rows():
+    r = sample_rows(1, 16, 16384, per_head=64)
+    assert np.all(np.diff(r) > 0)
+    assert {0, 127, 128, 16383}.issubset(set(r.tolist()))
+    per_head = np.bincount(r // 16384, minlength=16)
+    assert np.all(per_head >= 64)
+    assert np.array_equal(r, sample_rows(1, 16, 16384, per_head=64))

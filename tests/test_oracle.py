@@ -1,0 +1,234 @@
+"""Pins for the FP64 oracle against facts fixed by the mathematics, not by the oracle itself.
+
+The definition being pinned is S = scale*QK^T, P = softmax_row(S), O = PV, plus the
+natural log-sum-exp of each score row ("FlashAttention'ı Anlamak Bölüm 1", section 0.2
+Notasyon; "Flash Attention на 5090 в CUDA C++", Алгоритм Flash Attention 2). Each test
+below is chosen so that a plausible slip in the oracle (a dropped scale, a sign flip in
+the exponent, value rows indexed with the key stride, a missing 1/l, a head-stride
+error, a wrong logarithm base) fails at least one of them.
+"""
+import math
+
+import numpy as np
+import pytest
+
+import oracle
+from dense_attention_forward_fwd_gb300.inputs import bf16_bits_to_f32, f32_to_bf16_bits, make_qkv
+
+SCALE = float(np.float32(1 / math.sqrt(128)))
+
+
+def bf16(x):
+    """Exact BF16 bits of values that are representable (asserts no rounding happened)."""
+    x = np.asarray(x, dtype=np.float32)
+    b = f32_to_bf16_bits(x)
+    assert np.array_equal(bf16_bits_to_f32(b), x), "test value not exactly representable in BF16"
+    return b
+
+
+def widen(b):
+    return bf16_bits_to_f32(b).astype(np.float64)
+
+
+# ---- invariants ---------------------------------------------------------------------------
+
+def pin_probability_rows_sum_to_one(orc):
+    q, k, _ = make_qkv(2, 3, 7, 11, d=16, seed=5, qk_mult=2.0)
+    p = orc.probs(q, k, 0.37)
+    assert p.shape == (2, 3, 7, 11)
+    assert np.all(p >= 0)
+    assert np.max(np.abs(p.sum(-1) - 1.0)) < 1e-12
+
+
+def pin_constant_v_returns_that_row(orc):
+    q, k, _ = make_qkv(1, 2, 9, 13, d=32, seed=1)
+    c = np.array([((i % 7) - 3) * 0.25 for i in range(32)], dtype=np.float32)
+    v = np.broadcast_to(bf16(c), (1, 2, 13, 32)).copy()
+    o, _ = orc.attention(q, k, v, SCALE)
+    assert np.max(np.abs(o - c.astype(np.float64))) < 1e-12
+
+
+def pin_zero_query_gives_mean_of_v_and_log_nk(orc):
+    _, k, v = make_qkv(2, 2, 5, 37, d=128, seed=2)
+    q = np.zeros((2, 2, 5, 128), dtype=np.uint16)  # +0.0 in BF16
+    o, lse = orc.attention(q, k, v, SCALE)
+    mean_v = widen(v).mean(axis=2)  # [B,H,dv]
+    assert np.max(np.abs(o - mean_v[:, :, None, :])) < 1e-12
+    assert np.max(np.abs(lse - math.log(37))) < 1e-12
+
+
+def pin_single_key_returns_its_value_and_score(orc):
+    q, k, v = make_qkv(1, 3, 4, 1, d=128, seed=3)
+    o, lse = orc.attention(q, k, v, SCALE)
+    assert np.max(np.abs(o - widen(v)[:, :, 0:1, :])) < 1e-15
+    s = SCALE * np.einsum("bhic,bhc->bhi", widen(q), widen(k)[:, :, 0, :])
+    assert np.max(np.abs(lse - s)) < 1e-12
+
+
+def pin_two_keys_logistic_closed_form(orc):
+    # softmax over two scores is the logistic function of their difference
+    q, k, v = make_qkv(1, 1, 6, 2, d=8, seed=4, qk_mult=3.0)
+    scale = 0.5
+    o, lse = orc.attention(q, k, v, scale)
+    qw, kw, vw = widen(q)[0, 0], widen(k)[0, 0], widen(v)[0, 0]
+    for i in range(6):
+        s0 = scale * float(qw[i] @ kw[0])
+        s1 = scale * float(qw[i] @ kw[1])
+        t = s1 - s0
+        sig = 1.0 / (1.0 + math.exp(-t)) if t >= 0 else math.exp(t) / (1.0 + math.exp(t))
+        want_o = vw[0] + sig * (vw[1] - vw[0])
+        want_lse = max(s0, s1) + math.log1p(math.exp(-abs(t)))
+        assert np.max(np.abs(o[0, 0, i] - want_o)) < 1e-12
+        assert abs(lse[0, 0, i] - want_lse) < 1e-12
+
+
+def pin_key_permutation_invariance(orc):
+    q, k, v = make_qkv(1, 2, 8, 50, d=64, seed=6)
+    perm = np.random.Generator(np.random.PCG64(9)).permutation(50)
+    o1, l1 = orc.attention(q, k, v, SCALE)
+    o2, l2 = orc.attention(q, k[:, :, perm], v[:, :, perm], SCALE)
+    assert np.max(np.abs(o1 - o2)) < 1e-13
+    assert np.max(np.abs(l1 - l2)) < 1e-13
+
+
+def pin_linear_in_v(orc):
+    q, k, _ = make_qkv(1, 1, 5, 20, d=16, seed=7)
+    g = np.random.Generator(np.random.PCG64(10))
+    v1 = g.integers(-8, 9, size=(1, 1, 20, 16)).astype(np.float32)
+    v2 = g.integers(-8, 9, size=(1, 1, 20, 16)).astype(np.float32)
+    o1, _ = orc.attention(q, k, bf16(v1), SCALE)
+    o2, _ = orc.attention(q, k, bf16(v2), SCALE)
+    o3, _ = orc.attention(q, k, bf16(2 * v1 + v2), SCALE)
+    assert np.max(np.abs(o3 - (2 * o1 + o2))) < 1e-12
+
+
+def pin_common_key_shift_moves_only_lse(orc):
+    # K_j -> K_j + u adds scale*q.u to every score of a row: P unchanged, LSE shifted
+    g = np.random.Generator(np.random.PCG64(11))
+    kq = g.integers(-8, 9, size=(1, 1, 30, 8)).astype(np.float32) * 0.25
+    u = g.integers(-8, 9, size=(8,)).astype(np.float32) * 0.25
+    qf = g.integers(-4, 5, size=(1, 1, 6, 8)).astype(np.float32) * 0.5
+    _, _, v = make_qkv(1, 1, 6, 30, d=8, seed=12)
+    o1, l1 = orc.attention(bf16(qf), bf16(kq), v, 0.3)
+    o2, l2 = orc.attention(bf16(qf), bf16(kq + u), v, 0.3)
+    shift = 0.3 * (qf[0, 0].astype(np.float64) @ u.astype(np.float64))
+    assert np.max(np.abs(o1 - o2)) < 1e-12
+    assert np.max(np.abs((l2 - l1)[0, 0] - shift)) < 1e-12
+
+
+def pin_heads_and_batches_are_independent(orc):
+    q, k, v = make_qkv(2, 3, 9, 17, d=32, seed=13)
+    o, lse = orc.attention(q, k, v, SCALE)
+    for b in range(2):
+        for h in range(3):
+            oo, ll = orc.attention(q[b:b + 1, h:h + 1], k[b:b + 1, h:h + 1], v[b:b + 1, h:h + 1], SCALE)
+            assert np.array_equal(oo[0, 0], o[b, h])
+            assert np.array_equal(ll[0, 0], lse[b, h])
+
+
+def pin_scale_zero_is_uniform_and_sign_of_scale_matches_negated_keys(orc):
+    q, k, v = make_qkv(1, 2, 4, 19, d=16, seed=14)
+    o, lse = orc.attention(q, k, v, 0.0)
+    assert np.max(np.abs(o - widen(v).mean(axis=2)[:, :, None, :])) < 1e-12
+    assert np.max(np.abs(lse - math.log(19))) < 1e-12
+    kneg = k ^ np.uint16(0x8000)  # flip the BF16 sign bit
+    o1, l1 = orc.attention(q, k, v, -0.2)
+    o2, l2 = orc.attention(q, kneg, v, 0.2)
+    assert np.max(np.abs(o1 - o2)) < 1e-13 and np.max(np.abs(l1 - l2)) < 1e-13
+
+
+def pin_huge_scores_do_not_overflow(orc):
+    # one key's score is ~1000 above the rest: exp() of raw scores would overflow
+    d = 4
+    qf = np.array([[[[8.0, 0, 0, 0]]]], dtype=np.float32)
+    kf = np.zeros((1, 1, 5, d), dtype=np.float32)
+    kf[0, 0, 3, 0] = 128.0
+    kf[0, 0, 1, 0] = 1.0
+    _, _, v = make_qkv(1, 1, 1, 5, d=d, seed=15)
+    o, lse = orc.attention(bf16(qf), bf16(kf), v, 1.0)
+    assert np.all(np.isfinite(o)) and np.isfinite(lse).all()
+    assert np.max(np.abs(o[0, 0, 0] - widen(v)[0, 0, 3])) < 1e-300 + 1e-15
+    assert abs(lse[0, 0, 0] - 1024.0) < 1e-12
+
+
+def pin_row_subset_matches_full_rows(orc):
+    q, k, v = make_qkv(2, 2, 33, 40, d=128, seed=16)
+    o, lse = orc.attention(q, k, v, SCALE)
+    rows = np.array([0, 5, 32, 33, 70, 131], dtype=np.int64)
+    os_, ls = orc.attention_rows(q, k, v, SCALE, rows)
+    assert np.array_equal(os_, o.reshape(-1, 128)[rows])
+    assert np.array_equal(ls, lse.reshape(-1)[rows])
+
+
+def pin_value_head_dim_may_differ(orc):
+    q, k, v = make_qkv(1, 2, 3, 6, d=4, seed=17, dv=3)
+    o, _ = orc.attention(q, k, v, 0.7)
+    assert o.shape == (1, 2, 3, 3)
+    p = orc.probs(q, k, 0.7)
+    assert np.max(np.abs(o - np.einsum("bhij,bhjc->bhic", p, widen(v)))) < 1e-12
+
+
+def test_rejects_bad_sizes():
+    orc = oracle.default()
+    q, k, v = make_qkv(1, 1, 2, 2, d=4, seed=0)
+    with pytest.raises(ValueError):
+        orc.attention_rows(q, k, v, 1.0, np.array([4], dtype=np.int64))
+    with pytest.raises(TypeError):
+        orc.attention(q.astype(np.float32), k, v, 1.0)
+
+
+# ---- brute force in arbitrary precision -----------------------------------------------------
+
+def _mp_attention(qw, kw, vw, scale):
+    mp = pytest.importorskip("mpmath")
+    mp.mp.dps = 50
+    Nq, Nk, dv = qw.shape[0], kw.shape[0], vw.shape[1]
+    o = np.zeros((Nq, dv))
+    lse = np.zeros(Nq)
+    for i in range(Nq):
+        e = [mp.exp(mp.mpf(scale) * mp.fsum(mp.mpf(float(a)) * mp.mpf(float(b)) for a, b in zip(qw[i], kw[j])))
+             for j in range(Nk)]  # no max subtraction: exact arithmetic needs none
+        den = mp.fsum(e)
+        for c in range(dv):
+            o[i, c] = float(mp.fsum(e[j] * mp.mpf(float(vw[j, c])) for j in range(Nk)) / den)
+        lse[i] = float(mp.log(den))
+    return o, lse
+
+
+BRUTE_CASES = [(1, 1, 1, 1.0, 1.0), (2, 3, 4, 1.0, 0.5), (3, 5, 4, 3.0, SCALE), (5, 2, 128, 1.0, SCALE),
+               (2, 5, 128, 3.0, SCALE), (3, 4, 6, 1.0, 0.8, 5)]
+
+
+def pin_matches_high_precision_brute_force(orc, cases=BRUTE_CASES):
+    for case in cases:
+        Nq, Nk, d, mult, scale = case[:5]
+        dv = case[5] if len(case) > 5 else d
+        q, k, v = make_qkv(2, 2, Nq, Nk, d=d, seed=Nq * 100 + Nk, qk_mult=mult, dv=dv)
+        o, lse = orc.attention(q, k, v, scale)
+        for b in range(2):
+            for h in range(2):
+                wo, wl = _mp_attention(widen(q)[b, h], widen(k)[b, h], widen(v)[b, h], scale)
+                assert np.max(np.abs(o[b, h] - wo)) < 1e-13
+                assert np.max(np.abs(lse[b, h] - wl)) < 1e-12 * max(1.0, np.max(np.abs(wl)))
+
+
+# ---- a library routine as an independent special case ---------------------------------------
+
+def pin_matches_torch_float64_softmax_on_the_256_workload(orc):
+    torch = pytest.importorskip("torch")
+    q, k, v = make_qkv(1, 1, 256, 256, d=128, seed=0)
+    o, lse = orc.attention(q, k, v, SCALE)
+    qt, kt, vt = (torch.from_numpy(widen(x)) for x in (q, k, v))
+    s = (qt @ kt.transpose(-1, -2)) * SCALE
+    ot = torch.softmax(s, dim=-1) @ vt
+    lt = torch.logsumexp(s, dim=-1)
+    assert np.max(np.abs(o - ot.numpy())) < 1e-12
+    assert np.max(np.abs(lse - lt.numpy())) < 1e-12
+
+
+PINS = [v for k_, v in sorted(globals().items()) if k_.startswith("pin_")]
+
+
+@pytest.mark.parametrize("pin", PINS, ids=lambda f: f.__name__[4:])
+def test_oracle_pin(pin):
+    pin(oracle.default())

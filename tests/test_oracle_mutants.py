@@ -1,0 +1,47 @@
+"""The oracle's pins must catch plausible slips: each mutant below plants one in a private
+copy of attn_ref.c (compiled into a temporary directory, on the CPU) and at least one pin
+of tests/test_oracle.py must fail against it. The committed oracle is never modified.
+"""
+import os
+import shutil
+
+import pytest
+
+import oracle
+from test_oracle import PINS
+
+MUTANTS = {
+    "scale dropped": ("s[j] = scale * acc;", "s[j] = acc;"),
+    "exponent sign flipped": ("s[j] = exp(s[j] - m);", "s[j] = exp(m - s[j]);"),
+    "missing 1/l": ("o[c] = acc / l;", "o[c] = acc;"),
+    "max not added back to lse": ("*lse = m + log(l);", "*lse = log(l);"),
+    "log2 instead of ln": ("*lse = m + log(l);", "*lse = m + log2(l);"),
+    "value rows with key stride": ("vh[j * dv + c]", "vh[j * d + c]"),
+    "key head stride uses Nq": ("k + bh * Nk * d, v", "k + bh * Nq * d, v"),
+    "query row stride uses Nk": ("attend_row(q + (bh * Nq + i) * d", "attend_row(q + (bh * Nk + i) * d"),
+    "minimum instead of maximum": ("if (s[j] > m) m = s[j];", "if (s[j] < m) m = s[j];"),
+    "last key dropped from PV": ("for (int64_t j = 0; j < Nk; j++)\n            acc += s[j]",
+                                 "for (int64_t j = 0; j < Nk - 1; j++)\n            acc += s[j]"),
+    "keys used as values": ("bf16_to_f64(vh[j * dv + c])", "bf16_to_f64(kh[j * d + c])"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_some_pin_catches(name, tmp_path):
+    old, new = MUTANTS[name]
+    src = open(os.path.join(os.path.dirname(oracle.__file__), "attn_ref.c")).read()
+    assert src.count(old) == 1, f"mutation site for {name!r} not found exactly once"
+    mut_src = tmp_path / "attn_ref.c"
+    mut_src.write_text(src.replace(old, new))
+    lib = oracle.build(force=True, src=str(mut_src), out=str(tmp_path / "libmut.so"))
+    mutant = oracle.Oracle(lib)
+    caught = []
+    for pin in PINS:
+        try:
+            pin(mutant)
+        except (AssertionError, ValueError, FloatingPointError):
+            caught.append(pin.__name__)
+        except pytest.skip.Exception:
+            pass
+    assert caught, f"no pin caught mutant {name!r}"
+    shutil.rmtree(tmp_path, ignore_errors=True)
