@@ -1,0 +1,364 @@
+#!/usr/bin/env python3
+"""Benchmark of the dense BF16 attention forward (d=128, non-causal) on GB300.
+
+One step = one attn_fwd call over the whole workload (every (b, h) and every query
+tile). Default workload: B=1, H=8, Nq=4096, Nk=8192 (the shape of the RTX 5090 table
+in "Flash Attention на 5090 в CUDA C++"); --workload picks another of the five.
+
+Kernel time: CUDA events around each launch on the launching stream, inputs resident
+in HBM, L2 flushed (a 512 MiB write) before every timed launch. value = total
+4*B*H*Nq*Nk*d FLOPs of all ranks / max-over-ranks time. e2e: the same metric through
+the same C-ABI call, with the host->device copy of Q, K, V from pinned memory and the
+device->host copy of O and LSE inside each timed step.
+
+--impl reference times the FP64 CPU oracle (the plain definition) on host cores, on a
+bounded sample of query rows per step.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from dense_attention_forward_fwd_gb300.configs import WORKLOADS, by_name  # noqa: E402
+
+METRIC = "attention fwd TFLOPS (4·B·H·N²·d) and % of GB300 dense-BF16 tensor peak"
+DEFAULT_WORKLOAD = "rect-4k-8k"
+# The pages' own figure for this shape: the from-scratch v5 kernel on an RTX 5090
+# ("Flash Attention на 5090 в CUDA C++", benchmark table). Another GPU: context only.
+PAGES_TFLOPS = {"rect-4k-8k": 197.74}
+L2_FLUSH_BYTES = 512 << 20
+KERNEL_SRC = os.path.join(ROOT, "dense_attention_forward_fwd_gb300", "csrc", "attn_fwd.cu")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=[w.name for w in WORKLOADS])
+    ap.add_argument("--e2e-steps", type=int, default=50)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0, help="target CPU time of the oracle sample")
+    return ap.parse_args()
+
+
+def dist_env():
+    return int(os.environ.get("RANK", 0)), int(os.environ.get("LOCAL_RANK", 0)), int(os.environ.get("WORLD_SIZE", 1))
+
+
+def kernel_hash() -> str:
+    h = hashlib.sha256()
+    for f in (KERNEL_SRC, os.path.join(ROOT, "include", "attn_fwd.h")):
+        h.update(open(f, "rb").read())
+    return h.hexdigest()[:16]
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            return json.load(f), "measured"
+    return {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}, "fallback"
+
+
+def host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+# ------------------------------------------------------------------ clocks (nvidia-smi) ----
+
+SMI_FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+
+class ClockSampler:
+    def __init__(self, gpu_index: int):
+        self.path = tempfile.mktemp(prefix="clocks_", suffix=".csv")
+        self.proc = None
+        try:
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={SMI_FIELDS}", "--format=csv,noheader,nounits", "-i", str(gpu_index),
+                 "-lms", "50"], stdout=self.fh, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.fh.close()
+
+    def summary(self, t0: float, t1: float):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 10:
+                continue
+            try:
+                ts = time.mktime(time.strptime(parts[0].split(".")[0], "%Y/%m/%d %H:%M:%S"))
+                frac = float("0." + parts[0].split(".")[1]) if "." in parts[0] else 0.0
+                rows.append((ts + frac, float(parts[2]), float(parts[3]), parts[6:10]))
+            except (ValueError, IndexError):
+                continue
+        os.unlink(self.path)
+        inside = [r for r in rows if t0 - 0.05 <= r[0] <= t1 + 0.05]
+        window = "timed"
+        if len(inside) < 2:
+            inside, window = rows, "warmup+timed+after"
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in inside for n, v in zip(names, r[3]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[1] for r in inside), "sm_max_mhz": max(r[2] for r in inside),
+                "reasons": reasons, "samples": len(inside), "window": window}
+
+
+# ------------------------------------------------------------------ reference arm (oracle) ---
+
+def cpu_oracle_sample(w, target_seconds: float, rank_seed: int = 0):
+    """Time the FP64 oracle on a sample of query rows; returns (TFLOPS, rows, seconds, threads)."""
+    import numpy as np
+
+    import oracle
+    from dense_attention_forward_fwd_gb300.inputs import make_qkv
+
+    # K and V of one head are all a row needs; draw the workload's own tensors at full
+    # size only when they are small, else draw one head (same distribution).
+    H1 = w.H if w.B * w.H * w.Nk * w.d <= (1 << 26) else 1
+    q, k, v = make_qkv(1, H1, min(w.Nq, 4096), w.Nk, d=w.d, seed=w.seed + rank_seed, qk_mult=w.qk_mult)
+    threads = oracle.max_threads()
+    flop_row = 4.0 * w.Nk * w.d
+    n_rows_total = q.shape[1] * q.shape[2]
+    probe = min(max(threads, 8), n_rows_total)
+    rows = np.arange(probe, dtype=np.int64)
+    t = time.perf_counter()
+    oracle.attention_rows(q, k, v, w.scale, rows)
+    dt = time.perf_counter() - t
+    n = int(min(n_rows_total, max(probe, target_seconds / max(dt / probe, 1e-9))))
+    rows = np.linspace(0, n_rows_total - 1, n).astype(np.int64)
+    t = time.perf_counter()
+    oracle.attention_rows(q, k, v, w.scale, rows)
+    dt = time.perf_counter() - t
+    return flop_row * n / dt / 1e12, n, dt, threads
+
+
+def run_reference(args, w):
+    rank, _, world = dist_env()
+    if rank != 0:
+        return 0
+    import numpy as np
+
+    import oracle
+    from dense_attention_forward_fwd_gb300.inputs import make_qkv
+
+    steps, warm = args.steps, args.warmup
+    H1 = w.H if w.B * w.H * w.Nk * w.d <= (1 << 26) else 1
+    q, k, v = make_qkv(1, H1, min(w.Nq, 4096), w.Nk, d=w.d, seed=w.seed, qk_mult=w.qk_mult)
+    threads = oracle.max_threads()
+    n_rows_total = q.shape[1] * q.shape[2]
+    flop_row = 4.0 * w.Nk * w.d
+    # size each step so that warmup + steps take about two minutes in all
+    t = time.perf_counter()
+    oracle.attention_rows(q, k, v, w.scale, np.arange(threads, dtype=np.int64))
+    per_row = (time.perf_counter() - t) / threads
+    rows_per_step = int(max(1, min(n_rows_total, 120.0 / (steps + warm) / per_row)))
+    rng = np.random.Generator(np.random.PCG64(1234))
+    for _ in range(warm):
+        oracle.attention_rows(q, k, v, w.scale, rng.choice(n_rows_total, rows_per_step, replace=False))
+    total = 0.0
+    for _ in range(steps):
+        rows = rng.choice(n_rows_total, rows_per_step, replace=False)
+        t = time.perf_counter()
+        oracle.attention_rows(q, k, v, w.scale, rows)
+        total += time.perf_counter() - t
+    ms = total / steps * 1e3
+    tflops = flop_row * rows_per_step / (ms / 1e3) / 1e12
+    sample = f"{rows_per_step} query rows per step of {w.describe()} (full Nk per row), FP64"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": tflops, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": steps, "warmup": warm, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "Nq": w.Nq, "Nk": w.Nk, "d": w.d, "causal": False,
+                   "qk_mult": w.qk_mult},
+        "cpu_baseline": {"value": tflops, "unit": "TFLOP/s", "cores": threads, "kind": "oracle", "sample": sample},
+        "e2e": {"value": tflops, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ------------------------------------------------------------------ our arm ---------------
+
+def run_ours(args, w):
+    import numpy as np
+    import torch
+
+    import dense_attention_forward_fwd_gb300 as attn
+
+    rank, local_rank, world = dist_env()
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+        pg = dist
+    attn.load_library()
+
+    def barrier():
+        if pg is not None:
+            pg.barrier()
+
+    g = torch.Generator(device=dev)
+    g.manual_seed(w.seed + rank)
+    mult = w.qk_mult
+    q = (torch.randn(w.B, w.H, w.Nq, w.d, device=dev, generator=g) * mult).to(torch.bfloat16)
+    k = (torch.randn(w.B, w.H, w.Nk, w.d, device=dev, generator=g) * mult).to(torch.bfloat16)
+    v = torch.randn(w.B, w.H, w.Nk, w.d, device=dev, generator=g).to(torch.bfloat16)
+    o = torch.empty_like(q)
+    lse = torch.empty(w.B, w.H, w.Nq, device=dev, dtype=torch.float32)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, device=dev, dtype=torch.int32)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        attn.attn_fwd(q, k, v, o, lse, w.B, w.H, w.Nq, w.Nk, w.d, w.scale, stream)
+
+    sampler = ClockSampler(local_rank)   # started early: nvidia-smi needs a moment to come up
+    time.sleep(1.0)
+    for _ in range(max(args.warmup, 3)):
+        flush.zero_()
+        step()
+    if attn.attn_fwd_status(stream) != attn.ATTN_OK:
+        raise RuntimeError("kernel reported a timeout during warm-up")
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    barrier()
+    torch.cuda.synchronize()
+    launches0 = attn.attn_fwd_kernel_count()
+    t0 = time.time()
+    for i in range(args.steps):
+        flush.zero_()
+        starts[i].record(stream)
+        step()
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    t1 = time.time()
+    barrier()
+    launches = attn.attn_fwd_kernel_count() - launches0
+    time.sleep(0.2)
+    sampler.stop()
+    clocks = sampler.summary(t0, t1)
+    durs = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    ms = sum(durs) / len(durs)
+    status = attn.attn_fwd_status(stream)
+    if status != attn.ATTN_OK:
+        raise RuntimeError(f"kernel status {attn.attn_status_string(status)}")
+
+    # e2e through host buffers: pinned H2D of Q, K, V; attn_fwd; D2H of O and LSE
+    hq, hk, hv = (t.cpu().pin_memory() for t in (q, k, v))
+    ho, hl = torch.empty_like(o, device="cpu").pin_memory(), torch.empty_like(lse, device="cpu").pin_memory()
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+
+    def e2e_step():
+        dq.copy_(hq, non_blocking=True)
+        dk.copy_(hk, non_blocking=True)
+        dv.copy_(hv, non_blocking=True)
+        attn.attn_fwd(dq, dk, dv, o, lse, w.B, w.H, w.Nq, w.Nk, w.d, w.scale, stream)
+        ho.copy_(o, non_blocking=True)
+        hl.copy_(lse, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    es, ee = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    es.record(stream)
+    for _ in range(args.e2e_steps):
+        e2e_step()
+    ee.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = es.elapsed_time(ee) / args.e2e_steps
+    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv))
+    d2h = ho.numel() * ho.element_size() + hl.numel() * hl.element_size()
+
+    # max over ranks
+    if pg is not None:
+        tt = torch.tensor([ms, e2e_ms], device=dev, dtype=torch.float64)
+        pg.all_reduce(tt, op=pg.ReduceOp.MAX)
+        ms, e2e_ms = float(tt[0]), float(tt[1])
+    total_flops = w.flops * world
+    value = total_flops / (ms * 1e-3) / 1e12
+    e2e_value = total_flops / (e2e_ms * 1e-3) / 1e12
+
+    peaks, peak_src = measured_peaks()
+    peak = float(peaks["bf16_tflops"])
+    achieved = w.flops / (ms * 1e-3) / 1e12   # one launch on one GPU
+    traffic = None
+    if os.path.exists(TRAFFIC_FILE):
+        rec = json.load(open(TRAFFIC_FILE)).get(w.name)
+        if rec and rec.get("kernel_hash") == kernel_hash():
+            traffic = rec.get("bytes_per_launch")
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": (value / PAGES_TFLOPS[w.name]) if w.name in PAGES_TFLOPS else None,
+        "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "Nq": w.Nq, "Nk": w.Nk, "d": w.d, "causal": False,
+                   "qk_mult": w.qk_mult, "inputs": "iid N(0,1) BF16 (Q,K x qk_mult)",
+                   "l2": "flushed (512 MiB write) before every timed launch",
+                   "vs_baseline_ref": "RTX 5090 v5 kernel, same shape (other hardware: context only)"},
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak, "traffic": traffic,
+                     "peak_source": f"{peak_src} bf16_tflops (burst: each launch is timed alone)"},
+        "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches,
+        "clocks": clocks,
+        "kernel_ms_min": min(durs), "kernel_ms_median": statistics.median(durs),
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        tfl, n, dt, thr = cpu_oracle_sample(w, args.cpu_seconds)
+        line["cpu_baseline"] = {"value": tfl, "unit": "TFLOP/s", "cores": thr, "kind": "oracle",
+                                "sample": f"{n} query rows of {w.describe()} (full Nk each), FP64, {dt:.1f} s"}
+    if pg is not None:
+        pg.barrier()
+        pg.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    args = parse()
+    w = by_name(args.workload)
+    if args.impl == "reference":
+        return run_reference(args, w)
+    return run_ours(args, w)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,150 @@
+"""Dense, non-causal BF16 attention forward (head_dim 128) for GB300, sm_103a.
+
+A thin ctypes binding over the C ABI declared in ``include/attn_fwd.h``; every step of
+the computation runs in the CUDA kernels of ``libattn_fwd.so``. The Python side only
+checks that tensors match the sizes it passes and marshals pointers and streams.
+There is no CPU fallback: if the library cannot be built or loaded, calls raise.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import threading
+
+from ._build import LIB_PATH, build_library
+
+__all__ = [
+    "ATTN_OK", "ATTN_ERR_INVALID_ARG", "ATTN_ERR_UNSUPPORTED", "ATTN_ERR_MISALIGNED", "ATTN_ERR_CUDA",
+    "ATTN_ERR_TIMEOUT", "AttnError", "load_library", "attn_fwd", "attn_fwd_status", "attn_status_string",
+    "attn_fwd_set_wait_limit", "attn_fwd_kernel_count", "attention",
+]
+
+ATTN_OK = 0
+ATTN_ERR_INVALID_ARG = -1
+ATTN_ERR_UNSUPPORTED = -2
+ATTN_ERR_MISALIGNED = -3
+ATTN_ERR_CUDA = -4
+ATTN_ERR_TIMEOUT = -5
+
+_lock = threading.Lock()
+_lib = None
+
+
+class AttnError(RuntimeError):
+    def __init__(self, status: int, where: str = "attn_fwd"):
+        self.status = status
+        super().__init__(f"{where} failed: {attn_status_string(status)} ({status})")
+
+
+def load_library(build_if_stale: bool = True) -> ctypes.CDLL:
+    """Load libattn_fwd.so (building it first when it is missing or older than its sources)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = build_library() if build_if_stale else LIB_PATH
+            lib = ctypes.CDLL(path)
+            vp, i32, f32 = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+            lib.attn_fwd.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, f32, vp]
+            lib.attn_fwd.restype = i32
+            lib.attn_fwd_status.argtypes = [vp]
+            lib.attn_fwd_status.restype = i32
+            lib.attn_status_string.argtypes = [i32]
+            lib.attn_status_string.restype = ctypes.c_char_p
+            lib.attn_fwd_set_wait_limit.argtypes = [ctypes.c_ulonglong, i32]
+            lib.attn_fwd_set_wait_limit.restype = i32
+            lib.attn_fwd_kernel_count.argtypes = []
+            lib.attn_fwd_kernel_count.restype = ctypes.c_ulonglong
+            _lib = lib
+    return _lib
+
+
+def _is_tensor(x) -> bool:
+    return hasattr(x, "data_ptr") and hasattr(x, "is_cuda")
+
+
+def _ptr(x, name: str, numel: int | None, dtype_name: str):
+    """Raw device pointer of a torch tensor (checked against the element count) or an int."""
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    if _is_tensor(x):
+        import torch
+        want = {"bf16": torch.bfloat16, "f32": torch.float32}[dtype_name]
+        if not x.is_cuda:
+            raise ValueError(f"{name} must be a CUDA tensor")
+        if x.dtype != want:
+            raise TypeError(f"{name} must be {want}, got {x.dtype}")
+        if not x.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+        if numel is not None and x.numel() != numel:
+            raise ValueError(f"{name} has {x.numel()} elements, the sizes given need {numel}")
+        return x.data_ptr()
+    raise TypeError(f"{name}: expected a torch tensor or an integer device pointer, got {type(x).__name__}")
+
+
+def _stream_handle(stream, *tensors):
+    if stream is None:
+        for t in tensors:
+            if _is_tensor(t):
+                import torch
+                return torch.cuda.current_stream(t.device).cuda_stream
+        return None
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream  # torch.cuda.Stream
+
+
+def attn_fwd(q, k, v, o, lse, B: int, H: int, Nq: int, Nk: int, d: int, scale: float, stream=None) -> None:
+    """Enqueue O = softmax(scale * Q K^T) V and LSE on ``stream`` (see include/attn_fwd.h).
+
+    q, k, v, o: BF16 [B,H,N,d] CUDA tensors (or integer device pointers); lse: FP32 [B,H,Nq].
+    ``stream`` defaults to torch's current stream on the tensors' device. Raises AttnError
+    with the library's status code when the call is rejected.
+    """
+    lib = load_library()
+    args = (
+        _ptr(q, "q", B * H * Nq * d, "bf16"), _ptr(k, "k", B * H * Nk * d, "bf16"),
+        _ptr(v, "v", B * H * Nk * d, "bf16"), _ptr(o, "o", B * H * Nq * d, "bf16"),
+        _ptr(lse, "lse", B * H * Nq, "f32"),
+    )
+    rc = lib.attn_fwd(*args, int(B), int(H), int(Nq), int(Nk), int(d), float(scale),
+                      _stream_handle(stream, q, k, v, o, lse))
+    if rc != ATTN_OK:
+        raise AttnError(rc)
+
+
+def attn_fwd_status(stream=None) -> int:
+    """Synchronise ``stream`` and return (and clear) the device's timeout status."""
+    return load_library().attn_fwd_status(_stream_handle(stream))
+
+
+def attn_status_string(status: int) -> str:
+    return load_library().attn_status_string(int(status)).decode()
+
+
+def attn_fwd_set_wait_limit(cycles: int = 0, withhold_tile: bool = False) -> None:
+    """Test hook: per-wait time limit in SM cycles (0 = default) and the withheld-tile switch."""
+    load_library().attn_fwd_set_wait_limit(int(cycles), 1 if withhold_tile else 0)
+
+
+def attn_fwd_kernel_count() -> int:
+    """Kernel launches made by the library in this process."""
+    return int(load_library().attn_fwd_kernel_count())
+
+
+def attention(q, k, v, scale: float | None = None, stream=None):
+    """Allocate O and LSE with torch and run :func:`attn_fwd` on [B,H,N,128] BF16 CUDA tensors."""
+    import torch
+    if q.dim() != 4 or k.dim() != 4 or v.dim() != 4:
+        raise ValueError("q, k, v must be [B, H, N, d]")
+    B, H, Nq, d = q.shape
+    Nk = k.shape[2]
+    if tuple(k.shape) != (B, H, Nk, d) or tuple(v.shape) != (B, H, Nk, d):
+        raise ValueError(f"shape mismatch: q{tuple(q.shape)} k{tuple(k.shape)} v{tuple(v.shape)}")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device)
+    attn_fwd(q, k, v, o, lse, B, H, Nq, Nk, d, scale, stream)
+    return o, lse

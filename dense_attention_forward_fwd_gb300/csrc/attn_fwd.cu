@@ -1,0 +1,749 @@
+// attn_fwd.cu -- dense, non-causal BF16 attention forward for GB300 (sm_103a).
+//
+// O = softmax(scale * Q K^T) V and the per-row log-sum-exp, head_dim 128, computed
+// FlashAttention-style: each thread block owns output tiles of 128 query rows, loads
+// their Q once and streams 128-key K/V tiles through an online softmax, so S and P
+// stay on chip ("Sıfırdan yazılan CUDA attention kerneli...", section "Kernel işini
+// nasıl bölümlendiriyor"; the running max / running sum / rescale recurrence of
+// "Flash Attention на 5090 в CUDA C++", v1).
+//
+// Blackwell mapping (one block per SM, 12 warps):
+//   warp 0        TMA producer: Q tiles once, then K_j, V_j into a ring of 128B-swizzled
+//                 shared-memory slots guarded by full/empty mbarriers.
+//   warp 1        MMA issuer (one thread): tcgen05.mma S_i = Q_i K_j^T into TMEM, and
+//                 O_i += P_i V_j with P_i read from TMEM; owns the TMEM allocation.
+//   warps 4-7     softmax + epilogue for Q tile 0 (thread = query row = TMEM lane).
+//   warps 8-11    softmax + epilogue for Q tile 1.
+//   warps 2-3     idle.
+// Two Q tiles per block let one tile's softmax run while the tensor core works on
+// the other tile's two GEMMs (the two-query-tile schedule that the FlashAttention-4
+// summary in "Hacker News Digest" describes). TMEM holds S0, S1, O0, O1 (4 x 128
+// columns of FP32); P_i is written as BF16 over the first 64 columns of S_i.
+//
+// The softmax keeps, per row, m (running max of scale*s in log2 units) and l (running
+// sum of 2^(scale*s*log2e - m)). O is accumulated unnormalised and divided by l once
+// at the end ("normalised once the loop ends, then written", same write-up). The
+// running max is only moved when it grows by more than kRescaleLog2 (log2 units): the
+// exponentials are then bounded by 2^kRescaleLog2 and O and l keep sharing one m, so
+// the result is unchanged; skipping the move avoids reading and rewriting O in TMEM.
+//
+// Every wait is bounded (clock64 budget). On expiry a block raises a flag in shared
+// memory, the others stop at their next wait, the producer and the MMA thread wait
+// (bounded) for their own copies and MMAs in flight, TMEM is freed and the block
+// exits; the host learns of it through attn_fwd_status().
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <atomic>
+#include <climits>
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include "attn_fwd.h"
+
+namespace {
+
+// ---------------------------------------------------------------------------------
+// Tiling constants
+// ---------------------------------------------------------------------------------
+constexpr int kD = 128;                        // head dimension
+constexpr int kBM = 128;                       // query rows per Q tile (= TMEM lanes)
+constexpr int kBN = 128;                       // keys per K/V tile
+constexpr int kQTiles = 2;                     // Q tiles per block
+constexpr int kSlots = 4;                      // K/V ring depth, one 128x128 tile per slot
+constexpr int kTileBytes = kBM * kD * 2;       // 32 KB of BF16
+constexpr int kBoxBytes = kTileBytes / 2;      // one TMA box: 64 columns (128 B) x 128 rows
+constexpr int kThreads = 384;
+constexpr int kTmemCols = 512;
+constexpr float kRescaleLog2 = 8.0f;
+constexpr unsigned long long kDefaultWaitLimit = 1ull << 31;
+
+// shared memory map (byte offsets from a 1024-byte aligned base)
+constexpr int kOffQ = 0;
+constexpr int kOffKV = kOffQ + kQTiles * kTileBytes;
+constexpr int kOffBar = kOffKV + kSlots * kTileBytes;
+constexpr int kBarQFull = 0;
+constexpr int kBarKVFull = 1;
+constexpr int kBarKVEmpty = kBarKVFull + kSlots;
+constexpr int kBarSFull = kBarKVEmpty + kSlots;
+constexpr int kBarPFull = kBarSFull + kQTiles;
+constexpr int kBarOFull = kBarPFull + kQTiles;
+constexpr int kBarDrain = kBarOFull + kQTiles;
+constexpr int kNumBars = kBarDrain + 1;
+constexpr int kOffTmemSlot = kOffBar + kNumBars * 8;
+constexpr int kOffAbort = kOffTmemSlot + 4;
+constexpr int kSmemUsed = kOffAbort + 4;
+constexpr int kSmemBytes = kSmemUsed + 1024;   // slack to align the dynamic base to 1024
+
+static_assert(kOffKV % 1024 == 0 && kOffBar % 8 == 0, "swizzle atoms need 1024-byte alignment");
+static_assert(kSmemBytes <= 232448, "exceeds the 227 KB shared memory of one block");
+
+struct Params {
+  uint16_t* o;            // BF16 bits [BH, Nq, 128]
+  float* lse;             // [BH, Nq]
+  int Nq, Nk;
+  int q_groups;           // ceil(Nq / (kQTiles * kBM)): blocks per (b, h)
+  int n_kv;               // ceil(Nk / kBN)
+  int kv_tail;            // valid keys in the last K/V tile, 1..128
+  float scale_log2;       // scale * log2(e)
+  unsigned long long wait_limit;
+  int withhold_tile;      // test hook: never load K/V item 2 (the K tile of step 1)
+};
+
+__device__ unsigned int g_attn_status;   // per device; bit 0 = a wait timed out
+
+// ---------------------------------------------------------------------------------
+// PTX wrappers
+// ---------------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                            int x, int y, int z) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "r"(z)
+      : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+               : "memory");
+}
+
+// D(tmem) (+)= A(smem desc) * B(smem desc)
+__device__ __forceinline__ void mma_ss(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, bool acc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
+      "l"(a), "l"(b), "r"(idesc), "r"(static_cast<uint32_t>(acc))
+      : "memory");
+}
+// D(tmem) (+)= A(tmem) * B(smem desc)
+__device__ __forceinline__ void mma_ts(uint32_t d, uint32_t a, uint64_t b, uint32_t idesc, bool acc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d),
+      "r"(a), "l"(b), "r"(idesc), "r"(static_cast<uint32_t>(acc))
+      : "memory");
+}
+
+// 128 consecutive FP32 columns of this thread's TMEM lane (32x32b shape), waited on.
+__device__ __forceinline__ void tmem_ld128(uint32_t taddr, uint32_t (&x)[128]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x128.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32, %33, %34, %35, %36, %37, %38, %39, %40, %41, %42, %43, %44, %45, %46, %47, %48, %49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, %60, %61, %62, %63, %64, %65, %66, %67, %68, %69, %70, %71, %72, %73, %74, %75, %76, %77, %78, %79, %80, %81, %82, %83, %84, %85, %86, %87, %88, %89, %90, %91, %92, %93, %94, %95, %96, %97, %98, %99, %100, %101, %102, %103, %104, %105, %106, %107, %108, %109, %110, %111, %112, %113, %114, %115, %116, %117, %118, %119, %120, %121, %122, %123, %124, %125, %126, %127}, [%128];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(x[0]), "=r"(x[1]), "=r"(x[2]), "=r"(x[3]), "=r"(x[4]), "=r"(x[5]), "=r"(x[6]), "=r"(x[7]),
+        "=r"(x[8]), "=r"(x[9]), "=r"(x[10]), "=r"(x[11]), "=r"(x[12]), "=r"(x[13]), "=r"(x[14]), "=r"(x[15]),
+        "=r"(x[16]), "=r"(x[17]), "=r"(x[18]), "=r"(x[19]), "=r"(x[20]), "=r"(x[21]), "=r"(x[22]), "=r"(x[23]),
+        "=r"(x[24]), "=r"(x[25]), "=r"(x[26]), "=r"(x[27]), "=r"(x[28]), "=r"(x[29]), "=r"(x[30]), "=r"(x[31]),
+        "=r"(x[32]), "=r"(x[33]), "=r"(x[34]), "=r"(x[35]), "=r"(x[36]), "=r"(x[37]), "=r"(x[38]), "=r"(x[39]),
+        "=r"(x[40]), "=r"(x[41]), "=r"(x[42]), "=r"(x[43]), "=r"(x[44]), "=r"(x[45]), "=r"(x[46]), "=r"(x[47]),
+        "=r"(x[48]), "=r"(x[49]), "=r"(x[50]), "=r"(x[51]), "=r"(x[52]), "=r"(x[53]), "=r"(x[54]), "=r"(x[55]),
+        "=r"(x[56]), "=r"(x[57]), "=r"(x[58]), "=r"(x[59]), "=r"(x[60]), "=r"(x[61]), "=r"(x[62]), "=r"(x[63]),
+        "=r"(x[64]), "=r"(x[65]), "=r"(x[66]), "=r"(x[67]), "=r"(x[68]), "=r"(x[69]), "=r"(x[70]), "=r"(x[71]),
+        "=r"(x[72]), "=r"(x[73]), "=r"(x[74]), "=r"(x[75]), "=r"(x[76]), "=r"(x[77]), "=r"(x[78]), "=r"(x[79]),
+        "=r"(x[80]), "=r"(x[81]), "=r"(x[82]), "=r"(x[83]), "=r"(x[84]), "=r"(x[85]), "=r"(x[86]), "=r"(x[87]),
+        "=r"(x[88]), "=r"(x[89]), "=r"(x[90]), "=r"(x[91]), "=r"(x[92]), "=r"(x[93]), "=r"(x[94]), "=r"(x[95]),
+        "=r"(x[96]), "=r"(x[97]), "=r"(x[98]), "=r"(x[99]), "=r"(x[100]), "=r"(x[101]), "=r"(x[102]), "=r"(x[103]),
+        "=r"(x[104]), "=r"(x[105]), "=r"(x[106]), "=r"(x[107]), "=r"(x[108]), "=r"(x[109]), "=r"(x[110]), "=r"(x[111]),
+        "=r"(x[112]), "=r"(x[113]), "=r"(x[114]), "=r"(x[115]), "=r"(x[116]), "=r"(x[117]), "=r"(x[118]), "=r"(x[119]),
+        "=r"(x[120]), "=r"(x[121]), "=r"(x[122]), "=r"(x[123]), "=r"(x[124]), "=r"(x[125]), "=r"(x[126]), "=r"(x[127])
+      : "r"(taddr)
+      : "memory");
+}
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&x)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(x[0]), "=r"(x[1]), "=r"(x[2]), "=r"(x[3]), "=r"(x[4]), "=r"(x[5]), "=r"(x[6]), "=r"(x[7]),
+        "=r"(x[8]), "=r"(x[9]), "=r"(x[10]), "=r"(x[11]), "=r"(x[12]), "=r"(x[13]), "=r"(x[14]), "=r"(x[15]),
+        "=r"(x[16]), "=r"(x[17]), "=r"(x[18]), "=r"(x[19]), "=r"(x[20]), "=r"(x[21]), "=r"(x[22]), "=r"(x[23]),
+        "=r"(x[24]), "=r"(x[25]), "=r"(x[26]), "=r"(x[27]), "=r"(x[28]), "=r"(x[29]), "=r"(x[30]), "=r"(x[31])
+      : "r"(taddr)
+      : "memory");
+}
+__device__ __forceinline__ void tmem_st64(uint32_t taddr, const uint32_t (&x)[64]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x64.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32, %33, %34, %35, %36, %37, %38, %39, %40, %41, %42, %43, %44, %45, %46, %47, %48, %49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, %60, %61, %62, %63, %64};\n\t"
+      "tcgen05.wait::st.sync.aligned;" ::"r"(taddr),
+      "r"(x[0]), "r"(x[1]), "r"(x[2]), "r"(x[3]), "r"(x[4]), "r"(x[5]), "r"(x[6]), "r"(x[7]),
+        "r"(x[8]), "r"(x[9]), "r"(x[10]), "r"(x[11]), "r"(x[12]), "r"(x[13]), "r"(x[14]), "r"(x[15]),
+        "r"(x[16]), "r"(x[17]), "r"(x[18]), "r"(x[19]), "r"(x[20]), "r"(x[21]), "r"(x[22]), "r"(x[23]),
+        "r"(x[24]), "r"(x[25]), "r"(x[26]), "r"(x[27]), "r"(x[28]), "r"(x[29]), "r"(x[30]), "r"(x[31]),
+        "r"(x[32]), "r"(x[33]), "r"(x[34]), "r"(x[35]), "r"(x[36]), "r"(x[37]), "r"(x[38]), "r"(x[39]),
+        "r"(x[40]), "r"(x[41]), "r"(x[42]), "r"(x[43]), "r"(x[44]), "r"(x[45]), "r"(x[46]), "r"(x[47]),
+        "r"(x[48]), "r"(x[49]), "r"(x[50]), "r"(x[51]), "r"(x[52]), "r"(x[53]), "r"(x[54]), "r"(x[55]),
+        "r"(x[56]), "r"(x[57]), "r"(x[58]), "r"(x[59]), "r"(x[60]), "r"(x[61]), "r"(x[62]), "r"(x[63])
+      : "memory");
+}
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&x)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};\n\t"
+      "tcgen05.wait::st.sync.aligned;" ::"r"(taddr),
+      "r"(x[0]), "r"(x[1]), "r"(x[2]), "r"(x[3]), "r"(x[4]), "r"(x[5]), "r"(x[6]), "r"(x[7]),
+        "r"(x[8]), "r"(x[9]), "r"(x[10]), "r"(x[11]), "r"(x[12]), "r"(x[13]), "r"(x[14]), "r"(x[15]),
+        "r"(x[16]), "r"(x[17]), "r"(x[18]), "r"(x[19]), "r"(x[20]), "r"(x[21]), "r"(x[22]), "r"(x[23]),
+        "r"(x[24]), "r"(x[25]), "r"(x[26]), "r"(x[27]), "r"(x[28]), "r"(x[29]), "r"(x[30]), "r"(x[31])
+      : "memory");
+}
+
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float y;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(y) : "f"(a), "f"(b), "f"(c));
+  return y;
+}
+// (y0, y1) = (x0 * a + b, x1 * a + b) as one packed FP32x2 FMA
+__device__ __forceinline__ void fma2(float& y0, float& y1, float x0, float x1, float a, float b) {
+  asm("{\n\t.reg .b64 x, a, b, y;\n\t"
+      "mov.b64 x, {%2, %3};\n\t"
+      "mov.b64 a, {%4, %4};\n\t"
+      "mov.b64 b, {%5, %5};\n\t"
+      "fma.rn.f32x2 y, x, a, b;\n\t"
+      "mov.b64 {%0, %1}, y;\n\t}"
+      : "=f"(y0), "=f"(y1)
+      : "f"(x0), "f"(x1), "f"(a), "f"(b));
+}
+// (a0, a1) += (x0, x1) as one packed FP32x2 add
+__device__ __forceinline__ void add2(float& a0, float& a1, float x0, float x1) {
+  asm("{\n\t.reg .b64 a, x;\n\t"
+      "mov.b64 a, {%0, %1};\n\t"
+      "mov.b64 x, {%2, %3};\n\t"
+      "add.rn.f32x2 a, a, x;\n\t"
+      "mov.b64 {%0, %1}, a;\n\t}"
+      : "+f"(a0), "+f"(a1)
+      : "f"(x0), "f"(x1));
+}
+// two floats -> packed BF16x2 (round to nearest even), lo in the low half
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// ---------------------------------------------------------------------------------
+// Descriptors (tcgen05 shared-memory matrix descriptor and kind::f16 instruction
+// descriptor, field layouts per the PTX ISA)
+// ---------------------------------------------------------------------------------
+// 128B-swizzled operand: start address, leading/stride byte offsets, descriptor
+// version 1 (bits 46-48), swizzle mode 2 = 128B (bits 61-63).
+__device__ __forceinline__ uint64_t sdesc_sw128(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+  return static_cast<uint64_t>((addr >> 4) & 0x3FFFu) |
+         (static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16) |
+         (static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
+}
+// BF16 x BF16 -> FP32, M = 128, N = 128, A K-major, B K-major (S = Q K^T) or
+// MN-major (O += P V, V stored key-major with d contiguous).
+__host__ __device__ constexpr uint32_t idesc_bf16(bool b_mn_major) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((b_mn_major ? 1u : 0u) << 16) |
+         (static_cast<uint32_t>(kBN >> 3) << 17) | (static_cast<uint32_t>(kBM >> 4) << 24);
+}
+
+// ---------------------------------------------------------------------------------
+// Bounded waits
+// ---------------------------------------------------------------------------------
+struct Ctl {
+  uint32_t bars;                 // shared address of barrier 0
+  volatile uint32_t* abort;      // shared flag: some wait of this block gave up
+  unsigned long long limit;      // clock64 budget per wait
+  __device__ __forceinline__ uint32_t bar(int i) const { return bars + 8u * static_cast<uint32_t>(i); }
+};
+
+// true once the phase with this parity has completed; false on timeout, or (when
+// watch_abort) as soon as another role of the block has given up.
+__device__ __forceinline__ bool wait_phase(const Ctl& c, int idx, uint32_t parity, bool watch_abort) {
+  const uint32_t b = c.bar(idx);
+  if (mbar_try_wait(b, parity)) return true;
+  const long long t0 = clock64();
+  for (;;) {
+    if (mbar_try_wait(b, parity)) return true;
+    if (watch_abort && *c.abort) return false;
+    if (static_cast<unsigned long long>(clock64() - t0) > c.limit) {
+      *c.abort = 1u;
+      atomicOr(&g_attn_status, 1u);
+      return false;
+    }
+  }
+}
+// warp-uniform variant for roles whose next step is a .sync.aligned TMEM access
+__device__ __forceinline__ bool wait_warp(const Ctl& c, int idx, uint32_t parity) {
+  const bool ok = wait_phase(c, idx, parity, true);
+  return __all_sync(0xffffffffu, ok);
+}
+
+// ---------------------------------------------------------------------------------
+// Roles
+// ---------------------------------------------------------------------------------
+__device__ void run_producer(const Ctl& c, uint32_t base, const CUtensorMap* tmQ,
+                             const CUtensorMap* tmK, const CUtensorMap* tmV, const Params& p,
+                             int bh, int q_row0) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tmQ)) : "memory");
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tmK)) : "memory");
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tmV)) : "memory");
+
+  mbar_arrive_expect_tx(c.bar(kBarQFull), kQTiles * kTileBytes);
+  for (int i = 0; i < kQTiles; ++i)
+    for (int h = 0; h < 2; ++h)
+      tma_load_3d(base + kOffQ + i * kTileBytes + h * kBoxBytes, tmQ, c.bar(kBarQFull), h * 64,
+                  q_row0 + i * kBM, bh);
+
+  int last_item[kSlots];
+#pragma unroll
+  for (int s = 0; s < kSlots; ++s) last_item[s] = -1;
+
+  const int items = 2 * p.n_kv;   // K_0, V_0, K_1, V_1, ...
+  for (int it = 0; it < items; ++it) {
+    const int slot = it % kSlots;
+    const int use = it / kSlots;
+    if (use > 0 && !wait_phase(c, kBarKVEmpty + slot, (use - 1) & 1, true)) break;
+    if (p.withhold_tile && it == 2) continue;
+    const uint32_t fb = c.bar(kBarKVFull + slot);
+    mbar_arrive_expect_tx(fb, kTileBytes);
+    const CUtensorMap* m = (it & 1) ? tmV : tmK;
+    const int kv_row = (it >> 1) * kBN;
+    for (int h = 0; h < 2; ++h)
+      tma_load_3d(base + kOffKV + slot * kTileBytes + h * kBoxBytes, m, fb, h * 64, kv_row, bh);
+    last_item[slot] = it;
+  }
+  // Leave no copy in flight into shared memory that the block is about to release
+  // (on the normal path these phases have completed or are about to).
+  wait_phase(c, kBarQFull, 0, false);
+  for (int s = 0; s < kSlots; ++s)
+    if (last_item[s] >= 0) wait_phase(c, kBarKVFull + s, (last_item[s] / kSlots) & 1, false);
+}
+
+__device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint32_t q_smem, uint32_t k_smem) {
+  constexpr uint32_t idesc = idesc_bf16(false);
+#pragma unroll
+  for (int kk = 0; kk < kD / 16; ++kk) {
+    // K-major, 128B swizzle: 16 columns = 32 bytes inside a 128-byte row; the second
+    // 64-column half of the head dimension is the second TMA box.
+    const uint32_t off = static_cast<uint32_t>((kk >> 2) * kBoxBytes + (kk & 3) * 32);
+    mma_ss(d_tmem, sdesc_sw128(q_smem + off, 16, 1024), sdesc_sw128(k_smem + off, 16, 1024), idesc,
+           kk > 0);
+  }
+}
+
+__device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint32_t v_smem, bool acc) {
+  constexpr uint32_t idesc = idesc_bf16(true);
+#pragma unroll
+  for (int kk = 0; kk < kBN / 16; ++kk) {
+    // MN-major, 128B swizzle: 16 keys = 16 rows of 128 bytes; the two 64-column
+    // halves of d sit one box (kBoxBytes) apart, 8-row groups 1024 bytes apart.
+    mma_ts(d_tmem, p_tmem + kk * 8, sdesc_sw128(v_smem + kk * 16 * 128, kBoxBytes, 1024), idesc,
+           acc || kk > 0);
+  }
+}
+
+__device__ void run_mma(const Ctl& c, uint32_t base, uint32_t tmem, const Params& p) {
+  const uint32_t tS[2] = {tmem, tmem + 128};
+  const uint32_t tO[2] = {tmem + 256, tmem + 384};
+  const uint32_t sQ[2] = {base + kOffQ, base + kOffQ + kTileBytes};
+  bool ok = wait_phase(c, kBarQFull, 0, true) && wait_phase(c, kBarKVFull + 0, 0, true);
+  if (ok) {
+    tc_fence_after();
+    const uint32_t sK = base + kOffKV;
+    issue_qk(tS[0], sQ[0], sK);
+    tc_commit(c.bar(kBarSFull + 0));
+    issue_qk(tS[1], sQ[1], sK);
+    tc_commit(c.bar(kBarSFull + 1));
+    tc_commit(c.bar(kBarKVEmpty + 0));
+  }
+  for (int j = 0; ok && j < p.n_kv; ++j) {
+    const int itV = 2 * j + 1, slotV = itV % kSlots;
+    const int itK = 2 * j + 2, slotK = itK % kSlots;
+    const bool more = j + 1 < p.n_kv;
+    const uint32_t sV = base + kOffKV + slotV * kTileBytes;
+    const uint32_t sK = base + kOffKV + slotK * kTileBytes;
+    if (!wait_phase(c, kBarKVFull + slotV, (itV / kSlots) & 1, true)) break;
+    // tile 0: O0 += P0 V_j, then S0 = Q0 K_{j+1}^T
+    if (!wait_phase(c, kBarPFull + 0, j & 1, true)) break;
+    tc_fence_after();
+    issue_pv(tO[0], tS[0], sV, j > 0);
+    if (more) {
+      if (!wait_phase(c, kBarKVFull + slotK, (itK / kSlots) & 1, true)) break;
+      tc_fence_after();
+      issue_qk(tS[0], sQ[0], sK);
+      tc_commit(c.bar(kBarSFull + 0));
+    } else {
+      tc_commit(c.bar(kBarOFull + 0));
+    }
+    // tile 1: O1 += P1 V_j, then S1 = Q1 K_{j+1}^T
+    if (!wait_phase(c, kBarPFull + 1, j & 1, true)) break;
+    tc_fence_after();
+    issue_pv(tO[1], tS[1], sV, j > 0);
+    tc_commit(c.bar(kBarKVEmpty + slotV));
+    if (more) {
+      issue_qk(tS[1], sQ[1], sK);
+      tc_commit(c.bar(kBarSFull + 1));
+      tc_commit(c.bar(kBarKVEmpty + slotK));
+    } else {
+      tc_commit(c.bar(kBarOFull + 1));
+    }
+  }
+  // Every MMA this thread issued must finish before TMEM and shared memory are released.
+  tc_commit(c.bar(kBarDrain));
+  wait_phase(c, kBarDrain, 0, false);
+}
+
+template <bool kPosScale>
+__device__ void run_softmax(const Ctl& c, uint32_t tmem, const Params& p, int tile, int bh, int q_row0) {
+  const int quarter = (threadIdx.x >> 5) & 3;   // TMEM lanes this warp may access
+  const int lane = threadIdx.x & 31;
+  const int r = quarter * 32 + lane;            // query row within the tile
+  const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+  const uint32_t tS = tmem + lane_off + tile * 128;
+  const uint32_t tO = tmem + lane_off + 256 + tile * 128;
+  const float cs = kPosScale ? p.scale_log2 : 1.0f;   // factor still to apply to s
+
+  float m_used = -INFINITY;   // log2 units
+  float l = 0.0f;             // sum of 2^(s*cs - m_used) in FP32
+  float lr = 0.0f;            // the same sum over the BF16-rounded terms
+  bool ok = true;
+  for (int j = 0; j < p.n_kv; ++j) {
+    if (!wait_warp(c, kBarSFull + tile, j & 1)) {
+      ok = false;
+      break;
+    }
+    tc_fence_after();
+    uint32_t x[128];
+    tmem_ld128(tS, x);
+    float s[128];
+#pragma unroll
+    for (int i = 0; i < 128; ++i) s[i] = __uint_as_float(x[i]);
+    if (!kPosScale) {
+#pragma unroll
+      for (int i = 0; i < 128; ++i) s[i] *= p.scale_log2;
+    }
+    if (j == p.n_kv - 1 && p.kv_tail < kBN) {
+      const int valid = p.kv_tail;
+#pragma unroll
+      for (int i = 0; i < 128; ++i) s[i] = (i < valid) ? s[i] : -INFINITY;
+    }
+    // four independent three-input max chains over s[0..127]
+    float mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
+#pragma unroll
+    for (int i = 4; i < 124; i += 8) {
+      mx0 = max3(mx0, s[i + 0], s[i + 1]);
+      mx1 = max3(mx1, s[i + 2], s[i + 3]);
+      mx2 = max3(mx2, s[i + 4], s[i + 5]);
+      mx3 = max3(mx3, s[i + 6], s[i + 7]);
+    }
+    mx0 = max3(mx0, s[124], s[125]);
+    mx1 = max3(mx1, s[126], s[127]);
+    const float m_tile = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * cs;
+    bool rescale = false;
+    float alpha = 1.0f;
+    if (m_tile > m_used + kRescaleLog2) {
+      alpha = ex2(m_used - m_tile);   // 0 on the first tile
+      l *= alpha;
+      lr *= alpha;
+      m_used = m_tile;
+      rescale = j > 0;
+    }
+    // p = 2^(s*cs - m), rounded to BF16 for the P V product. Two row sums: l over the
+    // FP32 p (for the log-sum-exp) and lr over the rounded p, i.e. exactly the weights
+    // the tensor core multiplies V by. O is divided by lr, so it stays a convex
+    // combination of V rows even when the stale running max leaves the dominant p
+    // anywhere in [1, 2^kRescaleLog2] with its BF16 rounding error.
+    const float neg_m = -m_used;
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    float accr[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    uint32_t pk[64];
+#pragma unroll
+    for (int i = 0; i < 64; ++i) {
+      float e0, e1;
+      fma2(e0, e1, s[2 * i], s[2 * i + 1], cs, neg_m);
+      e0 = ex2(e0);
+      e1 = ex2(e1);
+      pk[i] = pack_bf16(e0, e1);
+      add2(acc[2 * (i & 3)], acc[2 * (i & 3) + 1], e0, e1);
+      add2(accr[2 * (i & 3)], accr[2 * (i & 3) + 1], __uint_as_float(pk[i] << 16),
+           __uint_as_float(pk[i] & 0xFFFF0000u));
+    }
+    l += ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
+    lr += ((accr[0] + accr[1]) + (accr[2] + accr[3])) + ((accr[4] + accr[5]) + (accr[6] + accr[7]));
+    tmem_st64(tS, pk);
+    if (__any_sync(0xffffffffu, rescale)) {
+      const float a = rescale ? alpha : 1.0f;
+#pragma unroll 1
+      for (int ch = 0; ch < 4; ++ch) {
+        uint32_t ov[32];
+        tmem_ld32(tO + ch * 32, ov);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * a);
+        tmem_st32(tO + ch * 32, ov);
+      }
+    }
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(c.bar(kBarPFull + tile));
+  }
+
+  if (ok) ok = wait_warp(c, kBarOFull + tile, 0);
+  if (!ok) return;
+  tc_fence_after();
+  const int qrow = q_row0 + tile * kBM + r;
+  const bool live = qrow < p.Nq;
+  const float inv_l = 1.0f / lr;
+  const size_t row_id = static_cast<size_t>(bh) * static_cast<size_t>(p.Nq) + static_cast<size_t>(qrow);
+  uint4* dst = reinterpret_cast<uint4*>(p.o + row_id * kD);
+#pragma unroll 1
+  for (int ch = 0; ch < 4; ++ch) {
+    uint32_t ov[32];
+    tmem_ld32(tO + ch * 32, ov);
+    uint32_t pk[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+      pk[i] = pack_bf16(__uint_as_float(ov[2 * i]) * inv_l, __uint_as_float(ov[2 * i + 1]) * inv_l);
+    if (live) {
+#pragma unroll
+      for (int v = 0; v < 4; ++v)
+        dst[ch * 4 + v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+    }
+  }
+  if (live) p.lse[row_id] = (m_used + log2f(l)) * 0.69314718055994531f;
+}
+
+// ---------------------------------------------------------------------------------
+// Kernel
+// ---------------------------------------------------------------------------------
+template <bool kPosScale>
+__global__ void __launch_bounds__(kThreads, 1)
+    attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                    const __grid_constant__ CUtensorMap tmV, const Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* smem = smem_raw + (base - raw);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int bh = blockIdx.x / p.q_groups;
+  const int q_row0 = (blockIdx.x % p.q_groups) * (kQTiles * kBM);
+
+  Ctl c;
+  c.bars = base + kOffBar;
+  c.abort = reinterpret_cast<volatile uint32_t*>(smem + kOffAbort);
+  c.limit = p.wait_limit;
+
+  if (threadIdx.x == 0) {
+    mbar_init(c.bar(kBarQFull), 1);
+    for (int s = 0; s < kSlots; ++s) {
+      mbar_init(c.bar(kBarKVFull + s), 1);
+      mbar_init(c.bar(kBarKVEmpty + s), 1);
+    }
+    for (int t = 0; t < kQTiles; ++t) {
+      mbar_init(c.bar(kBarSFull + t), 1);
+      mbar_init(c.bar(kBarPFull + t), 4);   // one arrival per softmax warp
+      mbar_init(c.bar(kBarOFull + t), 1);
+    }
+    mbar_init(c.bar(kBarDrain), 1);
+    *c.abort = 0u;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(base + kOffTmemSlot),
+                 "r"(kTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + kOffTmemSlot);
+
+  if (warp == 0) {
+    if (lane == 0) run_producer(c, base, &tmQ, &tmK, &tmV, p, bh, q_row0);
+    __syncwarp();
+  } else if (warp == 1) {
+    if (lane == 0) run_mma(c, base, tmem, p);
+    __syncwarp();
+  } else if (warp >= 4) {
+    run_softmax<kPosScale>(c, tmem, p, (warp >> 2) - 1, bh, q_row0);
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols)
+                 : "memory");
+  }
+}
+
+// ---------------------------------------------------------------------------------
+// Host side
+// ---------------------------------------------------------------------------------
+std::atomic<unsigned long long> g_wait_limit{kDefaultWaitLimit};
+std::atomic<int> g_withhold{0};
+std::atomic<unsigned long long> g_launches{0};
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+PFN_cuTensorMapEncodeTiled_v12000 encoder() {
+  std::call_once(g_encode_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  return g_encode;
+}
+
+// [BH, rows, 128] BF16 viewed as a 3-D tensor (d innermost); box = 64 columns x 128 rows x 1.
+bool make_map(CUtensorMap* map, const void* ptr, int rows, long long bh) {
+  auto enc = encoder();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(kD), static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(bh)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(kD) * 2, static_cast<cuuint64_t>(rows) * kD * 2};
+  cuuint32_t box[3] = {64, static_cast<cuuint32_t>(kBM), 1};
+  cuuint32_t elem[3] = {1, 1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, elem,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+constexpr int kMaxDevices = 64;
+std::atomic<int> g_attr_done[2][kMaxDevices];
+
+template <bool kPos>
+int launch(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, const Params& p, int grid,
+           cudaStream_t stream) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return ATTN_ERR_CUDA;
+  auto kern = attn_fwd_kernel<kPos>;
+  if (dev < 0 || dev >= kMaxDevices || !g_attr_done[kPos][dev].load(std::memory_order_acquire)) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) != cudaSuccess)
+      return ATTN_ERR_CUDA;
+    if (dev >= 0 && dev < kMaxDevices) g_attr_done[kPos][dev].store(1, std::memory_order_release);
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = stream;
+  if (cudaLaunchKernelEx(&cfg, kern, mq, mk, mv, p) != cudaSuccess) return ATTN_ERR_CUDA;
+  g_launches.fetch_add(1, std::memory_order_relaxed);
+  return ATTN_OK;
+}
+
+}  // namespace
+
+extern "C" int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Nq,
+                        int Nk, int d, float scale, void* stream) {
+  if (B < 0 || H < 0 || Nq < 0 || Nk < 0) return ATTN_ERR_INVALID_ARG;
+  if (d != kD) return ATTN_ERR_UNSUPPORTED;
+  if (!std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
+  const long long bh = static_cast<long long>(B) * H;
+  if (bh == 0 || Nq == 0) return ATTN_OK;   // nothing to compute
+  if (Nk == 0) return ATTN_ERR_INVALID_ARG;  // softmax over an empty key set
+  if (!q || !k || !v || !o || !lse) return ATTN_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) | reinterpret_cast<uintptr_t>(v) |
+       reinterpret_cast<uintptr_t>(o)) & 15u)
+    return ATTN_ERR_MISALIGNED;
+  if (reinterpret_cast<uintptr_t>(lse) & 3u) return ATTN_ERR_MISALIGNED;
+  // index ranges: TMA coordinates and the block index are 32-bit
+  const long long q_groups = (static_cast<long long>(Nq) + kQTiles * kBM - 1) / (kQTiles * kBM);
+  if (bh > INT_MAX || bh * q_groups > INT_MAX) return ATTN_ERR_UNSUPPORTED;
+  // element counts must fit a signed 64-bit byte offset
+  const long long max_rows = static_cast<long long>(Nq > Nk ? Nq : Nk);
+  if (bh > (LLONG_MAX / 256) / max_rows) return ATTN_ERR_INVALID_ARG;
+
+  CUtensorMap mq, mk, mv;
+  if (!make_map(&mq, q, Nq, bh) || !make_map(&mk, k, Nk, bh) || !make_map(&mv, v, Nk, bh))
+    return ATTN_ERR_CUDA;
+
+  Params p;
+  p.o = static_cast<uint16_t*>(o);
+  p.lse = lse;
+  p.Nq = Nq;
+  p.Nk = Nk;
+  p.q_groups = static_cast<int>(q_groups);
+  p.n_kv = (Nk + kBN - 1) / kBN;
+  p.kv_tail = Nk - (p.n_kv - 1) * kBN;
+  p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+  p.wait_limit = g_wait_limit.load(std::memory_order_relaxed);
+  p.withhold_tile = g_withhold.load(std::memory_order_relaxed);
+
+  const int grid = static_cast<int>(bh * q_groups);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  return scale > 0.0f ? launch<true>(mq, mk, mv, p, grid, s) : launch<false>(mq, mk, mv, p, grid, s);
+}
+
+extern "C" int attn_fwd_status(void* stream) {
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  unsigned int h = 0;
+  if (cudaMemcpyFromSymbolAsync(&h, g_attn_status, sizeof h, 0, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return ATTN_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return ATTN_ERR_CUDA;
+  if (h == 0) return ATTN_OK;
+  const unsigned int zero = 0;
+  if (cudaMemcpyToSymbolAsync(g_attn_status, &zero, sizeof zero, 0, cudaMemcpyHostToDevice, s) != cudaSuccess ||
+      cudaStreamSynchronize(s) != cudaSuccess)
+    return ATTN_ERR_CUDA;
+  return ATTN_ERR_TIMEOUT;
+}
+
+extern "C" const char* attn_status_string(int status) {
+  switch (status) {
+    case ATTN_OK: return "ATTN_OK";
+    case ATTN_ERR_INVALID_ARG: return "ATTN_ERR_INVALID_ARG";
+    case ATTN_ERR_UNSUPPORTED: return "ATTN_ERR_UNSUPPORTED";
+    case ATTN_ERR_MISALIGNED: return "ATTN_ERR_MISALIGNED";
+    case ATTN_ERR_CUDA: return "ATTN_ERR_CUDA";
+    case ATTN_ERR_TIMEOUT: return "ATTN_ERR_TIMEOUT";
+    default: return "ATTN_ERR_UNKNOWN";
+  }
+}
+
+extern "C" int attn_fwd_set_wait_limit(unsigned long long cycles, int withhold_tile) {
+  g_wait_limit.store(cycles ? cycles : kDefaultWaitLimit, std::memory_order_relaxed);
+  g_withhold.store(withhold_tile ? 1 : 0, std::memory_order_relaxed);
+  return ATTN_OK;
+}
+
+extern "C" unsigned long long attn_fwd_kernel_count(void) { return g_launches.load(std::memory_order_relaxed); }

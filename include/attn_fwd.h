@@ -1,0 +1,113 @@
+/*
+ * attn_fwd.h -- C ABI of the GB300 (sm_103a) dense attention forward library.
+ *
+ * The operation is scaled-dot-product attention for one head at a time,
+ *
+ *     S = scale * Q K^T,   P = softmax_row(S),   O = P V,
+ *
+ * as written in "FlashAttention'ı Anlamak Bölüm 1", section 0.2 Notasyon (with the
+ * optional mask/bias taken as zero), and computed the FlashAttention way: Q, K, V
+ * and O cut into 128x128 tiles, each output tile owned by one thread block, which
+ * loads its Q tile once and streams K/V tile pairs through an online softmax, so
+ * that neither S nor P is ever written to device memory ("Sıfırdan yazılan CUDA
+ * attention kerneli...", section "Kernel işini nasıl bölümlendiriyor"; the online
+ * update of "Flash Attention на 5090 в CUDA C++", v1). The notes state that the
+ * result is exact attention, not an approximation, up to floating-point order.
+ *
+ * Besides O the call writes, per query row, the natural log-sum-exp of its scaled
+ * scores, lse = log(sum_j exp(S_ij)). The pages do not define this output; it is
+ * the softmax denominator in log form, the quantity a backward pass needs.
+ *
+ * Conventions shared by every entry point below:
+ *   - Tensors are dense, C-ordered, [B, H, N, d] (batch, heads, sequence, head dim)
+ *     with d = 128, in device memory reachable from the current CUDA device.
+ *   - BF16 is IEEE-style bfloat16 (1 sign, 8 exponent, 7 mantissa bits), passed as
+ *     raw 16-bit storage (void*).
+ *   - The caller owns every buffer. The library allocates no device memory and
+ *     keeps no pointer after a call returns.
+ *   - Calls are asynchronous: work is enqueued on `stream` (a cudaStream_t; NULL
+ *     means the legacy default stream) and the call returns at once. Only argument
+ *     and launch errors are reported by the return value.
+ *   - No C++ exception crosses this interface. Calls are thread-safe.
+ */
+#ifndef ATTN_FWD_H
+#define ATTN_FWD_H
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Status codes. */
+#define ATTN_OK               0
+#define ATTN_ERR_INVALID_ARG (-1) /* null pointer, negative size, Nk == 0 with rows to compute, non-finite scale, size overflow */
+#define ATTN_ERR_UNSUPPORTED (-2) /* d != 128, or sizes beyond the kernel's index range */
+#define ATTN_ERR_MISALIGNED  (-3) /* q, k, v or o not 16-byte aligned, or lse not 4-byte aligned */
+#define ATTN_ERR_CUDA        (-4) /* a CUDA runtime or driver call failed (no device, launch failure, ...) */
+#define ATTN_ERR_TIMEOUT     (-5) /* a kernel gave up a pipeline wait after its time limit (see attn_fwd_status) */
+
+/*
+ * attn_fwd -- dense, non-causal attention forward.
+ *
+ *   q    device, BF16 [B, H, Nq, d], read
+ *   k    device, BF16 [B, H, Nk, d], read
+ *   v    device, BF16 [B, H, Nk, d], read
+ *   o    device, BF16 [B, H, Nq, d], written: O = softmax(scale * Q K^T) V,
+ *        each element rounded to nearest-even from FP32
+ *   lse  device, FP32 [B, H, Nq],    written: log(sum_j exp(scale * q_i . k_j))
+ *   B, H, Nq, Nk   sizes, >= 0. B*H*Nq == 0 is an empty call: nothing is read or
+ *        written and ATTN_OK is returned. Otherwise Nk must be >= 1. Any Nq and Nk
+ *        are accepted; a sequence that is not a multiple of 128 ends in a partial
+ *        tile that the kernel masks.
+ *   d    head dimension; must be 128.
+ *   scale  any finite float, applied to the scores (1/sqrt(d) for standard attention).
+ *   stream a cudaStream_t, or NULL.
+ *
+ * o must not overlap q, k, v or lse (not checked). The call writes o and lse only.
+ *
+ * Returns ATTN_OK once the kernel is enqueued; ATTN_ERR_INVALID_ARG,
+ * ATTN_ERR_UNSUPPORTED or ATTN_ERR_MISALIGNED without touching the GPU when an
+ * argument is rejected; ATTN_ERR_CUDA when the launch fails.
+ */
+int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+             int B, int H, int Nq, int Nk, int d, float scale, void* stream);
+
+/*
+ * attn_fwd_status -- synchronises `stream`, then reads and clears the device status
+ * word that kernels of this library set when a pipeline wait runs past its time
+ * limit (every wait inside the kernel is bounded; on expiry the block stops its work,
+ * waits for its own copies and matrix operations in flight, frees its tensor memory
+ * and exits, leaving o and lse undefined). The word is per device and shared by all
+ * calls on that device since the last attn_fwd_status.
+ *
+ * Returns ATTN_OK, ATTN_ERR_TIMEOUT, or ATTN_ERR_CUDA if synchronising failed.
+ * No counterpart on the pages: this is the library's error channel.
+ */
+int attn_fwd_status(void* stream);
+
+/*
+ * attn_status_string -- a static, human-readable name for a status code.
+ */
+const char* attn_status_string(int status);
+
+/*
+ * attn_fwd_set_wait_limit -- test hook for the failure path. Sets, process-wide and for
+ * launches enqueued after the call, the time limit of every in-kernel wait in SM clock
+ * cycles (0 restores the default of 2^31 cycles, about one second) and whether launches
+ * withhold one K/V tile load (withhold_tile != 0), so that the consumer's wait for it
+ * runs out and the kernel takes its timeout exit. No GPU fault is involved: the kernel
+ * returns normally and attn_fwd_status reports ATTN_ERR_TIMEOUT. Returns ATTN_OK.
+ * No counterpart on the pages.
+ */
+int attn_fwd_set_wait_limit(unsigned long long cycles, int withhold_tile);
+
+/*
+ * attn_fwd_kernel_count -- number of kernel launches this library has made in this
+ * process (all devices), for launch accounting by callers.
+ */
+unsigned long long attn_fwd_kernel_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ATTN_FWD_H */

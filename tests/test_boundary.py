@@ -1,0 +1,94 @@
+"""The C-ABI library on a host without a GPU: it loads, exports every entry point the
+header declares, and rejects bad arguments before touching the device."""
+import ctypes
+import math
+import os
+import re
+
+import pytest
+
+import dense_attention_forward_fwd_gb300 as attn
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "attn_fwd.h")
+
+
+def declared_functions():
+    text = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?[A-Za-z_][\w\s\*]*?\b(attn_\w+)\s*\(", text, flags=re.M)))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    assert {"attn_fwd", "attn_fwd_status", "attn_status_string", "attn_fwd_set_wait_limit",
+            "attn_fwd_kernel_count"} <= set(names)
+
+
+def test_library_exports_every_declared_symbol():
+    lib = ctypes.CDLL(attn.load_library()._name)
+    for name in declared_functions():
+        assert hasattr(lib, name), f"{name} declared in attn_fwd.h but not exported"
+
+
+def test_status_strings():
+    for code, name in [(0, "ATTN_OK"), (-1, "ATTN_ERR_INVALID_ARG"), (-2, "ATTN_ERR_UNSUPPORTED"),
+                       (-3, "ATTN_ERR_MISALIGNED"), (-4, "ATTN_ERR_CUDA"), (-5, "ATTN_ERR_TIMEOUT")]:
+        assert attn.attn_status_string(code) == name
+    assert attn.attn_status_string(7) == "ATTN_ERR_UNKNOWN"
+
+
+def test_header_codes_match_binding():
+    text = open(HEADER).read()
+    for name in ["ATTN_OK", "ATTN_ERR_INVALID_ARG", "ATTN_ERR_UNSUPPORTED", "ATTN_ERR_MISALIGNED",
+                 "ATTN_ERR_CUDA", "ATTN_ERR_TIMEOUT"]:
+        m = re.search(rf"#define\s+{name}\s+\(?(-?\d+)\)?", text)
+        assert m and int(m.group(1)) == getattr(attn, name)
+
+
+A = 1 << 20  # fake, 16-byte aligned addresses: every call below is rejected before any CUDA call
+
+
+def call(q=A, k=A, v=A, o=A, lse=A, B=1, H=1, Nq=128, Nk=128, d=128, scale=0.125):
+    return attn.load_library().attn_fwd(q, k, v, o, lse, B, H, Nq, Nk, d, scale, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(q=None), attn.ATTN_ERR_INVALID_ARG),
+    (dict(lse=None), attn.ATTN_ERR_INVALID_ARG),
+    (dict(B=-1), attn.ATTN_ERR_INVALID_ARG),
+    (dict(Nk=-3), attn.ATTN_ERR_INVALID_ARG),
+    (dict(Nk=0), attn.ATTN_ERR_INVALID_ARG),
+    (dict(scale=math.inf), attn.ATTN_ERR_INVALID_ARG),
+    (dict(scale=math.nan), attn.ATTN_ERR_INVALID_ARG),
+    (dict(d=64), attn.ATTN_ERR_UNSUPPORTED),
+    (dict(d=256), attn.ATTN_ERR_UNSUPPORTED),
+    (dict(q=A + 8), attn.ATTN_ERR_MISALIGNED),
+    (dict(v=A + 2), attn.ATTN_ERR_MISALIGNED),
+    (dict(o=A + 4), attn.ATTN_ERR_MISALIGNED),
+    (dict(lse=A + 2), attn.ATTN_ERR_MISALIGNED),
+    (dict(B=1 << 16, H=1 << 16), attn.ATTN_ERR_UNSUPPORTED),
+    (dict(B=0, q=None, o=None), attn.ATTN_OK),        # empty batch: nothing read or written
+    (dict(Nq=0, lse=None), attn.ATTN_OK),
+    (dict(H=0, Nk=0), attn.ATTN_OK),
+])
+def test_argument_checks(kw, code):
+    assert call(**kw) == code
+
+
+def test_binding_raises_on_rejected_call():
+    with pytest.raises(attn.AttnError) as e:
+        attn.attn_fwd(A, A, A, A, A, 1, 1, 128, 128, 64, 0.1)
+    assert e.value.status == attn.ATTN_ERR_UNSUPPORTED
+
+
+def test_binding_checks_tensor_sizes():
+    torch = pytest.importorskip("torch")
+    q = torch.zeros(1, 1, 128, 128, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):  # a CPU tensor is refused before any pointer is passed
+        attn.attn_fwd(q, q, q, q, torch.zeros(1, 1, 128), 1, 1, 128, 128, 128, 0.1)
+
+
+def test_no_launch_without_gpu_calls():
+    before = attn.attn_fwd_kernel_count()
+    call(d=64)
+    assert attn.attn_fwd_kernel_count() == before

@@ -1,0 +1,122 @@
+"""Parity of the CUDA path (through the C-ABI) against the FP64 oracle on seeded inputs."""
+import math
+
+import numpy as np
+import pytest
+
+import oracle
+from dense_attention_forward_fwd_gb300.configs import WORKLOADS, by_name
+from dense_attention_forward_fwd_gb300.inputs import bf16_bits_to_f32, f32_to_bf16_bits, make_qkv, sample_rows
+from parity import check_case, compare, run_gpu
+
+pytestmark = pytest.mark.gpu
+
+SCALE = float(np.float32(1 / math.sqrt(128)))
+
+
+# ---- every element, at sizes spanning several tiles and ragged tails --------------------------
+
+@pytest.mark.parametrize("B,H,Nq,Nk", [
+    (1, 1, 256, 256),     # one block, both Q tiles, two K/V tiles
+    (1, 2, 512, 1024),    # several blocks and K/V steps, ring wrap-around
+    (2, 3, 384, 640),     # an odd number of Q tiles: second tile of the last block is empty
+    (1, 2, 300, 200),     # ragged Nq and Nk
+    (1, 1, 1, 1),         # a single query and key
+    (1, 1, 129, 1),
+    (1, 1, 1, 129),
+    (1, 3, 1000, 777),
+    (2, 2, 128, 2176),    # 17 K/V steps
+])
+def test_full_parity_small(gpu_lib, B, H, Nq, Nk):
+    check_case(gpu_lib, B, H, Nq, Nk, seed=B * 1000 + Nq + Nk)
+
+
+def test_full_parity_tiny_256_workload(gpu_lib):
+    w = by_name("tiny-256")
+    rep = check_case(gpu_lib, w.B, w.H, w.Nq, w.Nk, seed=w.seed, scale=w.scale)
+    assert rep.max_abs < 5e-3
+
+
+@pytest.mark.parametrize("seed", [1, 2])
+def test_full_parity_peaked_small(gpu_lib, seed):
+    # scores with std ~9: the running max moves late and the O rescale path runs
+    check_case(gpu_lib, 1, 2, 512, 2048, seed=seed, qk_mult=3.0, ulp_aware=True)
+
+
+# ---- the five workloads at full size, on seeded samples of query rows --------------------------
+
+@pytest.mark.parametrize("name", [w.name for w in WORKLOADS])
+def test_workload_sampled_rows(gpu_lib, name):
+    w = by_name(name)
+    rows = None
+    if w.oracle_rows_per_head is not None:
+        rows = sample_rows(w.B, w.H, w.Nq, per_head=w.oracle_rows_per_head)
+    check_case(gpu_lib, w.B, w.H, w.Nq, w.Nk, seed=w.seed, qk_mult=w.qk_mult, scale=w.scale, rows=rows,
+               ulp_aware=w.qk_mult != 1.0)
+
+
+# ---- the oracle's closed forms, replayed on the GPU -------------------------------------------
+
+def test_zero_query_gives_mean_of_v(gpu_lib):
+    _, k, v = make_qkv(1, 2, 256, 1000, seed=3)
+    q = np.zeros((1, 2, 256, 128), dtype=np.uint16)
+    o, lse = run_gpu(gpu_lib, q, k, v, SCALE)
+    mean_v = bf16_bits_to_f32(v).astype(np.float64).mean(axis=2)
+    compare(o.reshape(-1, 128), lse.reshape(-1), np.repeat(mean_v[0], 256, axis=0),
+            np.full(512, math.log(1000)))
+
+
+def test_constant_v_returns_it(gpu_lib):
+    q, k, _ = make_qkv(1, 1, 256, 384, seed=4, qk_mult=3.0)
+    c = np.array([((i % 9) - 4) * 0.5 for i in range(128)], dtype=np.float32)
+    v = np.broadcast_to(f32_to_bf16_bits(c), (1, 1, 384, 128)).copy()
+    o, _ = run_gpu(gpu_lib, q, k, v, SCALE)
+    assert np.max(np.abs(o - c)) <= 1e-2
+
+
+def test_identical_keys_behave_like_one_key(gpu_lib):
+    q, k1, v1 = make_qkv(1, 1, 256, 1, seed=5)
+    k = np.repeat(k1, 128, axis=2)
+    v = np.repeat(v1, 128, axis=2)
+    o, lse = run_gpu(gpu_lib, q, k, v, SCALE)
+    s = SCALE * (bf16_bits_to_f32(q)[0, 0].astype(np.float64) @ bf16_bits_to_f32(k1)[0, 0, 0].astype(np.float64))
+    compare(o.reshape(-1, 128), lse.reshape(-1),
+            np.repeat(bf16_bits_to_f32(v1)[0, 0].astype(np.float64), 256, axis=0), s + math.log(128))
+
+
+def test_hot_key_in_last_tile_forces_late_rescale(gpu_lib):
+    q, k, v = make_qkv(1, 1, 256, 1024, seed=6)
+    qf = bf16_bits_to_f32(q)
+    kf = bf16_bits_to_f32(k)
+    kf[0, 0, 1000] = qf[0, 0, 0].copy() * 4  # row 0 sees a score far above all others, late
+    kf[0, 0, 1001] = qf[0, 0, 200].copy() * 2
+    k = f32_to_bf16_bits(kf)
+    check_case(gpu_lib, 1, 1, 256, 1024, qkv=(q, k, v), ulp_aware=True)
+
+
+@pytest.mark.parametrize("scale", [0.0, -0.0883883461356163, 0.5, 1e-3])
+def test_other_scales(gpu_lib, scale):
+    check_case(gpu_lib, 1, 2, 256, 384, seed=8, scale=scale, ulp_aware=True)
+
+
+def test_results_are_deterministic(gpu_lib):
+    q, k, v = make_qkv(1, 4, 512, 512, seed=9)
+    o1, l1 = run_gpu(gpu_lib, q, k, v, SCALE)
+    o2, l2 = run_gpu(gpu_lib, q, k, v, SCALE)
+    assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
+
+
+def test_misaligned_device_pointer_rejected(gpu_lib):
+    import torch
+    buf = torch.zeros(1 * 1 * 128 * 128 + 8, dtype=torch.bfloat16, device="cuda")
+    lse = torch.zeros(128, dtype=torch.float32, device="cuda")
+    p = buf.data_ptr()
+    rc = gpu_lib.load_library().attn_fwd(p + 2, p, p, p, lse.data_ptr(), 1, 1, 128, 128, 128, 0.1, None)
+    assert rc == gpu_lib.ATTN_ERR_MISALIGNED
+
+
+def test_launch_counter_counts_launches(gpu_lib):
+    before = gpu_lib.attn_fwd_kernel_count()
+    q, k, v = make_qkv(1, 1, 128, 128, seed=10)
+    run_gpu(gpu_lib, q, k, v, SCALE)
+    assert gpu_lib.attn_fwd_kernel_count() == before + 1
