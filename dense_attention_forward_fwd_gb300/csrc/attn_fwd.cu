@@ -53,7 +53,7 @@ constexpr int kD = 128;                        // head dimension
 constexpr int kBM = 128;                       // query rows per Q tile (= TMEM lanes)
 constexpr int kBN = 128;                       // keys per K/V tile
 constexpr int kQTiles = 2;                     // Q tiles per block
-constexpr int kSlots = 4;                      // K/V ring depth, one 128x128 tile per slot
+constexpr int kSlots = 5;                      // K/V ring depth, one 128x128 tile per slot
 constexpr int kTileBytes = kBM * kD * 2;       // 32 KB of BF16
 constexpr int kBoxBytes = kTileBytes / 2;      // one TMA box: 64 columns (128 B) x 128 rows
 constexpr int kThreads = 384;
@@ -69,8 +69,8 @@ constexpr int kBarQFull = 0;
 constexpr int kBarKVFull = 1;
 constexpr int kBarKVEmpty = kBarKVFull + kSlots;
 constexpr int kBarSFull = kBarKVEmpty + kSlots;
-constexpr int kBarPFull = kBarSFull + kQTiles;
-constexpr int kBarOFull = kBarPFull + kQTiles;
+constexpr int kBarPFull = kBarSFull + kQTiles;    // [tile][half]: one barrier per 64-key half of P
+constexpr int kBarOFull = kBarPFull + 2 * kQTiles;
 constexpr int kBarDrain = kBarOFull + kQTiles;
 constexpr int kNumBars = kBarDrain + 1;
 constexpr int kOffTmemSlot = kOffBar + kNumBars * 8;
@@ -195,6 +195,21 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&x)[32]) {
         "=r"(x[16]), "=r"(x[17]), "=r"(x[18]), "=r"(x[19]), "=r"(x[20]), "=r"(x[21]), "=r"(x[22]), "=r"(x[23]),
         "=r"(x[24]), "=r"(x[25]), "=r"(x[26]), "=r"(x[27]), "=r"(x[28]), "=r"(x[29]), "=r"(x[30]), "=r"(x[31])
       : "r"(taddr)
+      : "memory");
+}
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t (&x)[8]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(x[0]), "=r"(x[1]), "=r"(x[2]), "=r"(x[3]), "=r"(x[4]), "=r"(x[5]), "=r"(x[6]), "=r"(x[7])
+      : "r"(taddr)
+      : "memory");
+}
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&x)[8]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};\n\t"
+      "tcgen05.wait::st.sync.aligned;" ::"r"(taddr),
+      "r"(x[0]), "r"(x[1]), "r"(x[2]), "r"(x[3]), "r"(x[4]), "r"(x[5]), "r"(x[6]), "r"(x[7])
       : "memory");
 }
 __device__ __forceinline__ void tmem_st64(uint32_t taddr, const uint32_t (&x)[64]) {
@@ -363,10 +378,11 @@ __device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint32_t q_smem, uint3
   }
 }
 
-__device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint32_t v_smem, bool acc) {
+// keys [64*half, 64*half + 64) of O += P V
+__device__ __forceinline__ void issue_pv_half(uint32_t d_tmem, uint32_t p_tmem, uint32_t v_smem, int half, bool acc) {
   constexpr uint32_t idesc = idesc_bf16(true);
 #pragma unroll
-  for (int kk = 0; kk < kBN / 16; ++kk) {
+  for (int kk = 4 * half; kk < 4 * half + 4; ++kk) {
     // MN-major, 128B swizzle: 16 keys = 16 rows of 128 bytes; the two 64-column
     // halves of d sit one box (kBoxBytes) apart, 8-row groups 1024 bytes apart.
     mma_ts(d_tmem, p_tmem + kk * 8, sdesc_sw128(v_smem + kk * 16 * 128, kBoxBytes, 1024), idesc,
@@ -398,7 +414,10 @@ __device__ void run_mma(const Ctl& c, uint32_t base, uint32_t tmem, const Params
     // tile 0: O0 += P0 V_j, then S0 = Q0 K_{j+1}^T
     if (!wait_phase(c, kBarPFull + 0, j & 1, true)) break;
     tc_fence_after();
-    issue_pv(tO[0], tS[0], sV, j > 0);
+    issue_pv_half(tO[0], tS[0], sV, 0, j > 0);
+    if (!wait_phase(c, kBarPFull + 1, j & 1, true)) break;
+    tc_fence_after();
+    issue_pv_half(tO[0], tS[0], sV, 1, true);
     if (more) {
       if (!wait_phase(c, kBarKVFull + slotK, (itK / kSlots) & 1, true)) break;
       tc_fence_after();
@@ -408,9 +427,12 @@ __device__ void run_mma(const Ctl& c, uint32_t base, uint32_t tmem, const Params
       tc_commit(c.bar(kBarOFull + 0));
     }
     // tile 1: O1 += P1 V_j, then S1 = Q1 K_{j+1}^T
-    if (!wait_phase(c, kBarPFull + 1, j & 1, true)) break;
+    if (!wait_phase(c, kBarPFull + 2, j & 1, true)) break;
     tc_fence_after();
-    issue_pv(tO[1], tS[1], sV, j > 0);
+    issue_pv_half(tO[1], tS[1], sV, 0, j > 0);
+    if (!wait_phase(c, kBarPFull + 3, j & 1, true)) break;
+    tc_fence_after();
+    issue_pv_half(tO[1], tS[1], sV, 1, true);
     tc_commit(c.bar(kBarKVEmpty + slotV));
     if (more) {
       issue_qk(tS[1], sQ[1], sK);
@@ -437,7 +459,7 @@ __device__ void run_softmax(const Ctl& c, uint32_t tmem, const Params& p, int ti
 
   float m_used = -INFINITY;   // log2 units
   float l = 0.0f;             // sum of 2^(s*cs - m_used) in FP32
-  float lr = 0.0f;            // the same sum over the BF16-rounded terms
+  float corr = 0.0f;          // BF16 rounding error of the largest term of each tile
   bool ok = true;
   for (int j = 0; j < p.n_kv; ++j) {
     if (!wait_warp(c, kBarSFull + tile, j & 1)) {
@@ -459,64 +481,71 @@ __device__ void run_softmax(const Ctl& c, uint32_t tmem, const Params& p, int ti
 #pragma unroll
       for (int i = 0; i < 128; ++i) s[i] = (i < valid) ? s[i] : -INFINITY;
     }
-    // four independent three-input max chains over s[0..127]
-    float mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
+    // row max: eight independent three-input max chains over s[0..127]
+    // (chain t covers s[t], s[t + 8], s[t + 16], ..., s[t + 120])
+    float mx[8];
 #pragma unroll
-    for (int i = 4; i < 124; i += 8) {
-      mx0 = max3(mx0, s[i + 0], s[i + 1]);
-      mx1 = max3(mx1, s[i + 2], s[i + 3]);
-      mx2 = max3(mx2, s[i + 4], s[i + 5]);
-      mx3 = max3(mx3, s[i + 6], s[i + 7]);
+    for (int t = 0; t < 8; ++t) mx[t] = fmaxf(s[t], s[t + 8]);             // s[0..15]
+#pragma unroll
+    for (int i = 16; i < 128; i += 16) {                                    // i = 16, 32, ..., 112
+#pragma unroll
+      for (int t = 0; t < 8; ++t) mx[t] = max3(mx[t], s[i + t], s[i + 8 + t]);  // s[i..i+15]
     }
-    mx0 = max3(mx0, s[124], s[125]);
-    mx1 = max3(mx1, s[126], s[127]);
-    const float m_tile = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * cs;
+    const float m_tile =
+        fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])), fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) * cs;
     bool rescale = false;
     float alpha = 1.0f;
     if (m_tile > m_used + kRescaleLog2) {
       alpha = ex2(m_used - m_tile);   // 0 on the first tile
       l *= alpha;
-      lr *= alpha;
+      corr *= alpha;
       m_used = m_tile;
       rescale = j > 0;
     }
-    // p = 2^(s*cs - m), rounded to BF16 for the P V product. Two row sums: l over the
-    // FP32 p (for the log-sum-exp) and lr over the rounded p, i.e. exactly the weights
-    // the tensor core multiplies V by. O is divided by lr, so it stays a convex
-    // combination of V rows even when the stale running max leaves the dominant p
-    // anywhere in [1, 2^kRescaleLog2] with its BF16 rounding error.
-    const float neg_m = -m_used;
-    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-    float accr[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-    uint32_t pk[64];
-#pragma unroll
-    for (int i = 0; i < 64; ++i) {
-      float e0, e1;
-      fma2(e0, e1, s[2 * i], s[2 * i + 1], cs, neg_m);
-      e0 = ex2(e0);
-      e1 = ex2(e1);
-      pk[i] = pack_bf16(e0, e1);
-      add2(acc[2 * (i & 3)], acc[2 * (i & 3) + 1], e0, e1);
-      add2(accr[2 * (i & 3)], accr[2 * (i & 3) + 1], __uint_as_float(pk[i] << 16),
-           __uint_as_float(pk[i] & 0xFFFF0000u));
-    }
-    l += ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
-    lr += ((accr[0] + accr[1]) + (accr[2] + accr[3])) + ((accr[4] + accr[5]) + (accr[6] + accr[7]));
-    tmem_st64(tS, pk);
+    // O must be rescaled before this step's first P V MMA accumulates into it.
     if (__any_sync(0xffffffffu, rescale)) {
       const float a = rescale ? alpha : 1.0f;
 #pragma unroll 1
-      for (int ch = 0; ch < 4; ++ch) {
-        uint32_t ov[32];
-        tmem_ld32(tO + ch * 32, ov);
+      for (int ch = 0; ch < 16; ++ch) {   // small chunks: s[] is still live here
+        uint32_t ov[8];
+        tmem_ld8(tO + ch * 8, ov);
 #pragma unroll
-        for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * a);
-        tmem_st32(tO + ch * 32, ov);
+        for (int i = 0; i < 8; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * a);
+        tmem_st8(tO + ch * 8, ov);
       }
     }
-    tc_fence_before();
-    __syncwarp();
-    if (lane == 0) mbar_arrive(c.bar(kBarPFull + tile));
+    // The BF16 rounding of P matters most for the tile's largest term, which the stale
+    // running max leaves anywhere in [1, 2^kRescaleLog2]. corr accumulates that term's
+    // rounding error, so that l + corr is the sum of the weights the tensor core
+    // actually applies to V (up to the far smaller errors of the other terms).
+    {
+      const float pm = ex2(m_tile - m_used);
+      corr += __uint_as_float(pack_bf16(pm, 0.0f) << 16) - pm;
+    }
+    // p = 2^(s*cs - m) in two halves of 64 keys; each half is rounded to BF16, stored
+    // over S in TMEM and handed to the MMA warp at once, so the first half of the
+    // P V product runs while the second half is computed.
+    const float neg_m = -m_used;
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+      uint32_t pk[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        const int e = half * 64 + 2 * i;
+        float e0, e1;
+        fma2(e0, e1, s[e], s[e + 1], cs, neg_m);
+        e0 = ex2(e0);
+        e1 = ex2(e1);
+        pk[i] = pack_bf16(e0, e1);
+        add2(acc[2 * (i & 3)], acc[2 * (i & 3) + 1], e0, e1);
+      }
+      tmem_st32(tS + half * 32, pk);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(c.bar(kBarPFull + 2 * tile + half));
+    }
+    l += ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
   }
 
   if (ok) ok = wait_warp(c, kBarOFull + tile, 0);
@@ -524,7 +553,7 @@ __device__ void run_softmax(const Ctl& c, uint32_t tmem, const Params& p, int ti
   tc_fence_after();
   const int qrow = q_row0 + tile * kBM + r;
   const bool live = qrow < p.Nq;
-  const float inv_l = 1.0f / lr;
+  const float inv_l = 1.0f / (l + corr);
   const size_t row_id = static_cast<size_t>(bh) * static_cast<size_t>(p.Nq) + static_cast<size_t>(qrow);
   uint4* dst = reinterpret_cast<uint4*>(p.o + row_id * kD);
 #pragma unroll 1
@@ -574,7 +603,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int t = 0; t < kQTiles; ++t) {
       mbar_init(c.bar(kBarSFull + t), 1);
-      mbar_init(c.bar(kBarPFull + t), 4);   // one arrival per softmax warp
+      mbar_init(c.bar(kBarPFull + 2 * t), 4);       // one arrival per softmax warp
+      mbar_init(c.bar(kBarPFull + 2 * t + 1), 4);
       mbar_init(c.bar(kBarOFull + t), 1);
     }
     mbar_init(c.bar(kBarDrain), 1);
