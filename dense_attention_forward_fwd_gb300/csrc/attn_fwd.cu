@@ -1,15 +1,15 @@
 // attn_fwd.cu -- dense, non-causal BF16 attention forward for GB300 (sm_103a).
 //
 // O = softmax(scale * Q K^T) V and the per-row log-sum-exp, head_dim 128, computed
-// FlashAttention-style: each thread block owns output tiles of 128 query rows, loads
-// their Q once and streams 128-key K/V tiles through an online softmax, so S and P
-// stay on chip ("Sıfırdan yazılan CUDA attention kerneli...", section "Kernel işini
-// nasıl bölümlendiriyor"; the running max / running sum / rescale recurrence of
-// "Flash Attention на 5090 в CUDA C++", v1).
+// FlashAttention-style: Q tiles of 128 query rows are loaded once and 128-key K/V
+// tiles are streamed through an online softmax, so S and P stay on chip ("Sıfırdan
+// yazılan CUDA attention kerneli...", section "Kernel işini nasıl bölümlendiriyor";
+// the running max / running sum / rescale recurrence of "Flash Attention на 5090 в
+// CUDA C++", v1).
 //
-// Blackwell mapping (one block per SM, 12 warps):
-//   warp 0        TMA producer: Q tiles once, then K_j, V_j into a ring of 128B-swizzled
-//                 shared-memory slots guarded by full/empty mbarriers.
+// Blackwell mapping (one persistent block per SM, 12 warps):
+//   warp 0        TMA producer: the two Q tiles of each work segment, then K_j, V_j
+//                 into a ring of 128B-swizzled shared-memory slots (full/empty mbarriers).
 //   warp 1        MMA issuer (one thread): tcgen05.mma S_i = Q_i K_j^T into TMEM, and
 //                 O_i += P_i V_j with P_i read from TMEM; owns the TMEM allocation.
 //   warps 4-7     softmax + epilogue for Q tile 0 (thread = query row = TMEM lane).
@@ -20,12 +20,20 @@
 // summary in "Hacker News Digest" describes). TMEM holds S0, S1, O0, O1 (4 x 128
 // columns of FP32); P_i is written as BF16 over the first 64 columns of S_i.
 //
+// Work is a list of groups (two Q tiles of one (b, h)) times K/V steps. Each block
+// walks a list of segments (group, key-step range): whole groups dealt round-robin in
+// waves (neighbouring blocks share heads, so K/V stay in L2), then, for the last one
+// or two waves' worth of groups, an even split of their key steps over all blocks, so
+// no SM idles at the end. A group split between blocks is finished by whichever block
+// completes its share last: every share leaves its unnormalised O, running max and
+// sums in a workspace, and the last one merges them. No block waits for another.
+//
 // The softmax keeps, per row, m (running max of scale*s in log2 units) and l (running
-// sum of 2^(scale*s*log2e - m)). O is accumulated unnormalised and divided by l once
-// at the end ("normalised once the loop ends, then written", same write-up). The
-// running max is only moved when it grows by more than kRescaleLog2 (log2 units): the
-// exponentials are then bounded by 2^kRescaleLog2 and O and l keep sharing one m, so
-// the result is unchanged; skipping the move avoids reading and rewriting O in TMEM.
+// sum of 2^(scale*s*log2e - m)). O is accumulated unnormalised and divided once at the
+// end ("normalised once the loop ends, then written", same write-up). The running max
+// only moves when it grows by more than kRescaleLog2 (log2 units): the exponentials
+// are then bounded by 2^kRescaleLog2 and O and l keep sharing one m, so the result is
+// unchanged; skipping the move avoids reading and rewriting O in TMEM.
 //
 // Every wait is bounded (clock64 budget). On expiry a block raises a flag in shared
 // memory, the others stop at their next wait, the producer and the MMA thread wait
@@ -40,7 +48,9 @@
 #include <climits>
 #include <cmath>
 #include <cstdint>
+#include <map>
 #include <mutex>
+#include <utility>
 
 #include "attn_fwd.h"
 
@@ -66,12 +76,14 @@ constexpr int kOffQ = 0;
 constexpr int kOffKV = kOffQ + kQTiles * kTileBytes;
 constexpr int kOffBar = kOffKV + kSlots * kTileBytes;
 constexpr int kBarQFull = 0;
-constexpr int kBarKVFull = 1;
+constexpr int kBarQEmpty = 1;                      // the Q tiles may be overwritten
+constexpr int kBarKVFull = 2;
 constexpr int kBarKVEmpty = kBarKVFull + kSlots;
 constexpr int kBarSFull = kBarKVEmpty + kSlots;
-constexpr int kBarPFull = kBarSFull + kQTiles;    // [tile][half]: one barrier per 64-key half of P
+constexpr int kBarPFull = kBarSFull + kQTiles;     // [tile][half]: one barrier per 64-key half of P
 constexpr int kBarOFull = kBarPFull + 2 * kQTiles;
-constexpr int kBarDrain = kBarOFull + kQTiles;
+constexpr int kBarOEmpty = kBarOFull + kQTiles;    // the epilogue has read O_i out of TMEM
+constexpr int kBarDrain = kBarOEmpty + kQTiles;
 constexpr int kNumBars = kBarDrain + 1;
 constexpr int kOffTmemSlot = kOffBar + kNumBars * 8;
 constexpr int kOffAbort = kOffTmemSlot + 4;
@@ -81,17 +93,90 @@ constexpr int kSmemBytes = kSmemUsed + 1024;   // slack to align the dynamic bas
 static_assert(kOffKV % 1024 == 0 && kOffBar % 8 == 0, "swizzle atoms need 1024-byte alignment");
 static_assert(kSmemBytes <= 232448, "exceeds the 227 KB shared memory of one block");
 
+// Workspace of split groups: per block two partial records (its first and its last
+// split segment), each [tile][row][kPartStride] floats: 128 of unnormalised O, then
+// m (log2 units), l, corr and one pad word.
+constexpr int kPartStride = kD + 4;
+constexpr size_t kPartBytesPerBlock = size_t(2) * kQTiles * kBM * kPartStride * sizeof(float);
+constexpr int kMinSegSteps = 8;   // smallest share of a group worth a block of its own
+
 struct Params {
   uint16_t* o;            // BF16 bits [BH, Nq, 128]
   float* lse;             // [BH, Nq]
   int Nq, Nk;
-  int q_groups;           // ceil(Nq / (kQTiles * kBM)): blocks per (b, h)
+  int q_groups;           // ceil(Nq / (kQTiles * kBM)): groups per (b, h)
   int n_kv;               // ceil(Nk / kBN)
   int kv_tail;            // valid keys in the last K/V tile, 1..128
+  int dp_groups;          // groups [0, dp_groups) are processed whole, group g by block g % grid
+  long long sk_steps;     // key steps of groups [dp_groups, n_groups), split evenly over the blocks
+  float* part;            // partial records, kPartBytesPerBlock per block (split groups only)
+  unsigned int* cnt;      // [n_groups - dp_groups][kQTiles][4] epoch-tagged arrival counters
+  unsigned int epoch;     // 1 .. 2^24-1, differs between consecutive launches sharing a workspace
   float scale_log2;       // scale * log2(e)
   unsigned long long wait_limit;
-  int withhold_tile;      // test hook: never load K/V item 2 (the K tile of step 1)
+  int withhold_tile;      // test hook: never load the third K/V item of a block (K of its step 1)
 };
+
+// First key step (counted over the split region) of block c's share.
+__host__ __device__ __forceinline__ long long sk_share_start(long long c, long long sk_steps, long long grid) {
+  return c * sk_steps / grid;
+}
+
+struct Segment {
+  int group;      // b*H*q_groups + h*q_groups + q-group
+  int kv0, kv1;   // key steps [kv0, kv1) of the group
+  int which;      // 0: first segment of this block's split share, 1: its last
+  bool split;     // other blocks hold other key steps of this group
+};
+
+// The segments of one block, in processing order; every role of the block walks the
+// same sequence.
+struct SegIter {
+  int n_kv, dp_groups, grid, next_dp;
+  long long sk_begin, sk_end, sk_pos;
+  __device__ explicit SegIter(const Params& p) {
+    n_kv = p.n_kv;
+    dp_groups = p.dp_groups;
+    grid = static_cast<int>(gridDim.x);
+    next_dp = static_cast<int>(blockIdx.x);
+    sk_begin = sk_share_start(blockIdx.x, p.sk_steps, grid);
+    sk_end = sk_share_start(static_cast<long long>(blockIdx.x) + 1, p.sk_steps, grid);
+    sk_pos = sk_begin;
+  }
+  __device__ bool next(Segment& sg) {
+    if (next_dp < dp_groups) {
+      sg.group = next_dp;
+      sg.kv0 = 0;
+      sg.kv1 = n_kv;
+      sg.which = 0;
+      sg.split = false;
+      next_dp += grid;
+      return true;
+    }
+    if (sk_pos < sk_end) {
+      const long long g_rel = sk_pos / n_kv;
+      const int kv0 = static_cast<int>(sk_pos - g_rel * n_kv);
+      const long long left = sk_end - sk_pos;
+      const int kv1 = left < n_kv - kv0 ? kv0 + static_cast<int>(left) : n_kv;
+      sg.group = dp_groups + static_cast<int>(g_rel);
+      sg.kv0 = kv0;
+      sg.kv1 = kv1;
+      sg.which = sk_pos == sk_begin ? 0 : 1;
+      sg.split = !(kv0 == 0 && kv1 == n_kv);
+      sk_pos = g_rel * n_kv + kv1;
+      return true;
+    }
+    return false;
+  }
+};
+
+// The block whose share contains split-region key step x (every share is non-empty).
+__device__ __forceinline__ int sk_block_of(long long x, long long sk_steps, int grid) {
+  int c = static_cast<int>(x * grid / sk_steps);
+  while (c + 1 < grid && sk_share_start(c + 1, sk_steps, grid) <= x) ++c;
+  while (c > 0 && sk_share_start(c, sk_steps, grid) > x) --c;
+  return c;
+}
 
 __device__ unsigned int g_attn_status;   // per device; bit 0 = a wait timed out
 
@@ -212,20 +297,6 @@ __device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&x)[8])
       "r"(x[0]), "r"(x[1]), "r"(x[2]), "r"(x[3]), "r"(x[4]), "r"(x[5]), "r"(x[6]), "r"(x[7])
       : "memory");
 }
-__device__ __forceinline__ void tmem_st64(uint32_t taddr, const uint32_t (&x)[64]) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x64.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32, %33, %34, %35, %36, %37, %38, %39, %40, %41, %42, %43, %44, %45, %46, %47, %48, %49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, %60, %61, %62, %63, %64};\n\t"
-      "tcgen05.wait::st.sync.aligned;" ::"r"(taddr),
-      "r"(x[0]), "r"(x[1]), "r"(x[2]), "r"(x[3]), "r"(x[4]), "r"(x[5]), "r"(x[6]), "r"(x[7]),
-        "r"(x[8]), "r"(x[9]), "r"(x[10]), "r"(x[11]), "r"(x[12]), "r"(x[13]), "r"(x[14]), "r"(x[15]),
-        "r"(x[16]), "r"(x[17]), "r"(x[18]), "r"(x[19]), "r"(x[20]), "r"(x[21]), "r"(x[22]), "r"(x[23]),
-        "r"(x[24]), "r"(x[25]), "r"(x[26]), "r"(x[27]), "r"(x[28]), "r"(x[29]), "r"(x[30]), "r"(x[31]),
-        "r"(x[32]), "r"(x[33]), "r"(x[34]), "r"(x[35]), "r"(x[36]), "r"(x[37]), "r"(x[38]), "r"(x[39]),
-        "r"(x[40]), "r"(x[41]), "r"(x[42]), "r"(x[43]), "r"(x[44]), "r"(x[45]), "r"(x[46]), "r"(x[47]),
-        "r"(x[48]), "r"(x[49]), "r"(x[50]), "r"(x[51]), "r"(x[52]), "r"(x[53]), "r"(x[54]), "r"(x[55]),
-        "r"(x[56]), "r"(x[57]), "r"(x[58]), "r"(x[59]), "r"(x[60]), "r"(x[61]), "r"(x[62]), "r"(x[63])
-      : "memory");
-}
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&x)[32]) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};\n\t"
@@ -329,39 +400,52 @@ __device__ __forceinline__ bool wait_warp(const Ctl& c, int idx, uint32_t parity
 // Roles
 // ---------------------------------------------------------------------------------
 __device__ void run_producer(const Ctl& c, uint32_t base, const CUtensorMap* tmQ,
-                             const CUtensorMap* tmK, const CUtensorMap* tmV, const Params& p,
-                             int bh, int q_row0) {
+                             const CUtensorMap* tmK, const CUtensorMap* tmV, const Params& p) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tmQ)) : "memory");
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tmK)) : "memory");
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tmV)) : "memory");
-
-  mbar_arrive_expect_tx(c.bar(kBarQFull), kQTiles * kTileBytes);
-  for (int i = 0; i < kQTiles; ++i)
-    for (int h = 0; h < 2; ++h)
-      tma_load_3d(base + kOffQ + i * kTileBytes + h * kBoxBytes, tmQ, c.bar(kBarQFull), h * 64,
-                  q_row0 + i * kBM, bh);
 
   int last_item[kSlots];
 #pragma unroll
   for (int s = 0; s < kSlots; ++s) last_item[s] = -1;
 
-  const int items = 2 * p.n_kv;   // K_0, V_0, K_1, V_1, ...
-  for (int it = 0; it < items; ++it) {
-    const int slot = it % kSlots;
-    const int use = it / kSlots;
-    if (use > 0 && !wait_phase(c, kBarKVEmpty + slot, (use - 1) & 1, true)) break;
-    if (p.withhold_tile && it == 2) continue;
-    const uint32_t fb = c.bar(kBarKVFull + slot);
-    mbar_arrive_expect_tx(fb, kTileBytes);
-    const CUtensorMap* m = (it & 1) ? tmV : tmK;
-    const int kv_row = (it >> 1) * kBN;
-    for (int h = 0; h < 2; ++h)
-      tma_load_3d(base + kOffKV + slot * kTileBytes + h * kBoxBytes, m, fb, h * 64, kv_row, bh);
-    last_item[slot] = it;
+  int it = 0;   // K/V items (K_j, V_j of every step of every segment) issued or skipped
+  int u = 0;    // segments whose Q load was issued
+  bool ok = true;
+  SegIter si(p);
+  Segment sg;
+  while (ok && si.next(sg)) {
+    const int bh = sg.group / p.q_groups;
+    const int q_row0 = (sg.group % p.q_groups) * (kQTiles * kBM);
+    // the previous segment's S MMAs must be done with the Q tiles
+    if (u > 0 && !wait_phase(c, kBarQEmpty, (u - 1) & 1, true)) break;
+    mbar_arrive_expect_tx(c.bar(kBarQFull), kQTiles * kTileBytes);
+    for (int i = 0; i < kQTiles; ++i)
+      for (int h = 0; h < 2; ++h)
+        tma_load_3d(base + kOffQ + i * kTileBytes + h * kBoxBytes, tmQ, c.bar(kBarQFull), h * 64,
+                    q_row0 + i * kBM, bh);
+    ++u;
+    for (int kv = sg.kv0; ok && kv < sg.kv1; ++kv) {
+      for (int kind = 0; kind < 2; ++kind, ++it) {   // K, then V
+        const int slot = it % kSlots;
+        const int use = it / kSlots;
+        if (use > 0 && !wait_phase(c, kBarKVEmpty + slot, (use - 1) & 1, true)) {
+          ok = false;
+          break;
+        }
+        if (p.withhold_tile && it == 2) continue;
+        const uint32_t fb = c.bar(kBarKVFull + slot);
+        mbar_arrive_expect_tx(fb, kTileBytes);
+        const CUtensorMap* m = kind ? tmV : tmK;
+        for (int h = 0; h < 2; ++h)
+          tma_load_3d(base + kOffKV + slot * kTileBytes + h * kBoxBytes, m, fb, h * 64, kv * kBN, bh);
+        last_item[slot] = it;
+      }
+    }
   }
   // Leave no copy in flight into shared memory that the block is about to release
   // (on the normal path these phases have completed or are about to).
-  wait_phase(c, kBarQFull, 0, false);
+  if (u > 0) wait_phase(c, kBarQFull, (u - 1) & 1, false);
   for (int s = 0; s < kSlots; ++s)
     if (last_item[s] >= 0) wait_phase(c, kBarKVFull + s, (last_item[s] / kSlots) & 1, false);
 }
@@ -394,61 +478,153 @@ __device__ void run_mma(const Ctl& c, uint32_t base, uint32_t tmem, const Params
   const uint32_t tS[2] = {tmem, tmem + 128};
   const uint32_t tO[2] = {tmem + 256, tmem + 384};
   const uint32_t sQ[2] = {base + kOffQ, base + kOffQ + kTileBytes};
-  bool ok = wait_phase(c, kBarQFull, 0, true) && wait_phase(c, kBarKVFull + 0, 0, true);
-  if (ok) {
-    tc_fence_after();
-    const uint32_t sK = base + kOffKV;
-    issue_qk(tS[0], sQ[0], sK);
-    tc_commit(c.bar(kBarSFull + 0));
-    issue_qk(tS[1], sQ[1], sK);
-    tc_commit(c.bar(kBarSFull + 1));
-    tc_commit(c.bar(kBarKVEmpty + 0));
-  }
-  for (int j = 0; ok && j < p.n_kv; ++j) {
-    const int itV = 2 * j + 1, slotV = itV % kSlots;
-    const int itK = 2 * j + 2, slotK = itK % kSlots;
-    const bool more = j + 1 < p.n_kv;
-    const uint32_t sV = base + kOffKV + slotV * kTileBytes;
-    const uint32_t sK = base + kOffKV + slotK * kTileBytes;
-    if (!wait_phase(c, kBarKVFull + slotV, (itV / kSlots) & 1, true)) break;
-    // tile 0: O0 += P0 V_j, then S0 = Q0 K_{j+1}^T
-    if (!wait_phase(c, kBarPFull + 0, j & 1, true)) break;
-    tc_fence_after();
-    issue_pv_half(tO[0], tS[0], sV, 0, j > 0);
-    if (!wait_phase(c, kBarPFull + 1, j & 1, true)) break;
-    tc_fence_after();
-    issue_pv_half(tO[0], tS[0], sV, 1, true);
-    if (more) {
-      if (!wait_phase(c, kBarKVFull + slotK, (itK / kSlots) & 1, true)) break;
+  int it = 0;           // K/V items consumed
+  uint32_t gstep = 0;   // K/V steps of all previous segments: phase of s_full / p_full
+  int u = 0;            // segments started
+  bool ok = true;
+  SegIter si(p);
+  Segment sg;
+  while (ok && si.next(sg)) {
+    const int n = sg.kv1 - sg.kv0;
+    {
+      const int slotK = it % kSlots;
+      if (!wait_phase(c, kBarQFull, u & 1, true) ||
+          !wait_phase(c, kBarKVFull + slotK, (it / kSlots) & 1, true))
+        break;
       tc_fence_after();
+      const uint32_t sK = base + kOffKV + slotK * kTileBytes;
       issue_qk(tS[0], sQ[0], sK);
       tc_commit(c.bar(kBarSFull + 0));
-    } else {
-      tc_commit(c.bar(kBarOFull + 0));
-    }
-    // tile 1: O1 += P1 V_j, then S1 = Q1 K_{j+1}^T
-    if (!wait_phase(c, kBarPFull + 2, j & 1, true)) break;
-    tc_fence_after();
-    issue_pv_half(tO[1], tS[1], sV, 0, j > 0);
-    if (!wait_phase(c, kBarPFull + 3, j & 1, true)) break;
-    tc_fence_after();
-    issue_pv_half(tO[1], tS[1], sV, 1, true);
-    tc_commit(c.bar(kBarKVEmpty + slotV));
-    if (more) {
       issue_qk(tS[1], sQ[1], sK);
       tc_commit(c.bar(kBarSFull + 1));
       tc_commit(c.bar(kBarKVEmpty + slotK));
-    } else {
-      tc_commit(c.bar(kBarOFull + 1));
+      if (n == 1) tc_commit(c.bar(kBarQEmpty));   // the segment's last S MMA is issued
     }
+    for (int j = 0; j < n; ++j) {
+      const int itV = it + 2 * j + 1, slotV = itV % kSlots;
+      const int itK = it + 2 * j + 2, slotK = itK % kSlots;
+      const bool more = j + 1 < n;
+      const uint32_t ph = (gstep + static_cast<uint32_t>(j)) & 1u;
+      const uint32_t sV = base + kOffKV + slotV * kTileBytes;
+      const uint32_t sK = base + kOffKV + slotK * kTileBytes;
+      if (!wait_phase(c, kBarKVFull + slotV, (itV / kSlots) & 1, true)) {
+        ok = false;
+        break;
+      }
+      // tile 0: O0 += P0 V_j (the first product of a segment overwrites O0, so the
+      // previous segment's epilogue must have read it out), then S0 = Q0 K_{j+1}^T
+      if ((j == 0 && u > 0 && !wait_phase(c, kBarOEmpty + 0, (u - 1) & 1, true)) ||
+          !wait_phase(c, kBarPFull + 0, ph, true)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      issue_pv_half(tO[0], tS[0], sV, 0, j > 0);
+      if (!wait_phase(c, kBarPFull + 1, ph, true)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      issue_pv_half(tO[0], tS[0], sV, 1, true);
+      if (more) {
+        if (!wait_phase(c, kBarKVFull + slotK, (itK / kSlots) & 1, true)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        issue_qk(tS[0], sQ[0], sK);
+        tc_commit(c.bar(kBarSFull + 0));
+      } else {
+        tc_commit(c.bar(kBarOFull + 0));
+      }
+      // tile 1: O1 += P1 V_j, then S1 = Q1 K_{j+1}^T
+      if ((j == 0 && u > 0 && !wait_phase(c, kBarOEmpty + 1, (u - 1) & 1, true)) ||
+          !wait_phase(c, kBarPFull + 2, ph, true)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      issue_pv_half(tO[1], tS[1], sV, 0, j > 0);
+      if (!wait_phase(c, kBarPFull + 3, ph, true)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      issue_pv_half(tO[1], tS[1], sV, 1, true);
+      tc_commit(c.bar(kBarKVEmpty + slotV));
+      if (more) {
+        issue_qk(tS[1], sQ[1], sK);
+        tc_commit(c.bar(kBarSFull + 1));
+        tc_commit(c.bar(kBarKVEmpty + slotK));
+        if (j + 2 == n) tc_commit(c.bar(kBarQEmpty));   // the segment's last S MMA is issued
+      } else {
+        tc_commit(c.bar(kBarOFull + 1));
+      }
+    }
+    it += 2 * n;
+    gstep += static_cast<uint32_t>(n);
+    ++u;
   }
   // Every MMA this thread issued must finish before TMEM and shared memory are released.
   tc_commit(c.bar(kBarDrain));
   wait_phase(c, kBarDrain, 0, false);
 }
 
+// Merges the partial records of one split group for this thread's query row (the
+// calling warp was the last of the group's shares to finish these 32 rows). With
+// m_s, l_s, corr_s, O_s the running max, sums and unnormalised output of share s and
+// M = max m_s, w_s = 2^(m_s - M): O = sum w_s O_s / sum w_s (l_s + corr_s) and
+// LSE = (M + log2 sum w_s l_s) * ln 2.
+__device__ void merge_split_row(const Params& p, int tile, int r, int c_first, int c_last, long long x0,
+                                uint4* dst, float* lse_out) {
+  const int grid = static_cast<int>(gridDim.x);
+  auto record = [&](int cs) -> const float* {
+    const int which = sk_share_start(cs, p.sk_steps, grid) >= x0 ? 0 : 1;
+    return p.part + ((static_cast<size_t>(cs) * 2 + which) * kQTiles + tile) * kBM * kPartStride +
+           static_cast<size_t>(r) * kPartStride;
+  };
+  float M = -INFINITY;
+  for (int cs = c_first; cs <= c_last; ++cs) M = fmaxf(M, __ldcg(record(cs) + kD));
+  float L = 0.0f, Lr = 0.0f;
+  for (int cs = c_first; cs <= c_last; ++cs) {
+    const float4 st = __ldcg(reinterpret_cast<const float4*>(record(cs) + kD));
+    const float w = ex2(st.x - M);
+    L += st.y * w;
+    Lr += (st.y + st.z) * w;
+  }
+  const float inv = 1.0f / Lr;
+#pragma unroll 1
+  for (int ch = 0; ch < 4; ++ch) {
+    float acc[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) acc[i] = 0.0f;
+    for (int cs = c_first; cs <= c_last; ++cs) {
+      const float* rec = record(cs);
+      const float w = ex2(__ldcg(rec + kD) - M);
+      const float4* src = reinterpret_cast<const float4*>(rec + ch * 32);
+#pragma unroll
+      for (int v = 0; v < 8; ++v) {
+        const float4 o4 = __ldcg(src + v);
+        acc[4 * v + 0] += o4.x * w;
+        acc[4 * v + 1] += o4.y * w;
+        acc[4 * v + 2] += o4.z * w;
+        acc[4 * v + 3] += o4.w * w;
+      }
+    }
+    if (dst != nullptr) {
+#pragma unroll
+      for (int v = 0; v < 4; ++v)
+        dst[ch * 4 + v] = make_uint4(pack_bf16(acc[8 * v + 0] * inv, acc[8 * v + 1] * inv),
+                                     pack_bf16(acc[8 * v + 2] * inv, acc[8 * v + 3] * inv),
+                                     pack_bf16(acc[8 * v + 4] * inv, acc[8 * v + 5] * inv),
+                                     pack_bf16(acc[8 * v + 6] * inv, acc[8 * v + 7] * inv));
+    }
+  }
+  if (lse_out != nullptr) *lse_out = (M + log2f(L)) * 0.69314718055994531f;
+}
+
 template <bool kPosScale>
-__device__ void run_softmax(const Ctl& c, uint32_t tmem, const Params& p, int tile, int bh, int q_row0) {
+__device__ void run_softmax(const Ctl& c, uint32_t tmem, const Params& p, int tile) {
   const int quarter = (threadIdx.x >> 5) & 3;   // TMEM lanes this warp may access
   const int lane = threadIdx.x & 31;
   const int r = quarter * 32 + lane;            // query row within the tile
@@ -457,120 +633,175 @@ __device__ void run_softmax(const Ctl& c, uint32_t tmem, const Params& p, int ti
   const uint32_t tO = tmem + lane_off + 256 + tile * 128;
   const float cs = kPosScale ? p.scale_log2 : 1.0f;   // factor still to apply to s
 
-  float m_used = -INFINITY;   // log2 units
-  float l = 0.0f;             // sum of 2^(s*cs - m_used) in FP32
-  float corr = 0.0f;          // BF16 rounding error of the largest term of each tile
-  bool ok = true;
-  for (int j = 0; j < p.n_kv; ++j) {
-    if (!wait_warp(c, kBarSFull + tile, j & 1)) {
-      ok = false;
-      break;
-    }
-    tc_fence_after();
-    uint32_t x[128];
-    tmem_ld128(tS, x);
-    float s[128];
+  uint32_t gstep = 0;   // K/V steps of all previous segments: phase of s_full / p_full
+  int u = 0;            // segments finished
+  SegIter si(p);
+  Segment sg;
+  while (si.next(sg)) {
+    const int n = sg.kv1 - sg.kv0;
+    float m_used = -INFINITY;   // log2 units
+    float l = 0.0f;             // sum of 2^(s*cs - m_used) in FP32
+    float corr = 0.0f;          // BF16 rounding error of the largest term of each tile
+    for (int j = 0; j < n; ++j) {
+      if (!wait_warp(c, kBarSFull + tile, (gstep + static_cast<uint32_t>(j)) & 1u)) return;
+      tc_fence_after();
+      uint32_t x[128];
+      tmem_ld128(tS, x);
+      float s[128];
 #pragma unroll
-    for (int i = 0; i < 128; ++i) s[i] = __uint_as_float(x[i]);
-    if (!kPosScale) {
+      for (int i = 0; i < 128; ++i) s[i] = __uint_as_float(x[i]);
+      if (!kPosScale) {
 #pragma unroll
-      for (int i = 0; i < 128; ++i) s[i] *= p.scale_log2;
-    }
-    if (j == p.n_kv - 1 && p.kv_tail < kBN) {
-      const int valid = p.kv_tail;
+        for (int i = 0; i < 128; ++i) s[i] *= p.scale_log2;
+      }
+      if (sg.kv0 + j == p.n_kv - 1 && p.kv_tail < kBN) {
+        const int valid = p.kv_tail;
 #pragma unroll
-      for (int i = 0; i < 128; ++i) s[i] = (i < valid) ? s[i] : -INFINITY;
-    }
-    // row max: eight independent three-input max chains over s[0..127]
-    // (chain t covers s[t], s[t + 8], s[t + 16], ..., s[t + 120])
-    float mx[8];
+        for (int i = 0; i < 128; ++i) s[i] = (i < valid) ? s[i] : -INFINITY;
+      }
+      // row max: eight independent three-input max chains over s[0..127]
+      // (chain t covers s[t], s[t + 8], s[t + 16], ..., s[t + 120])
+      float mx[8];
 #pragma unroll
-    for (int t = 0; t < 8; ++t) mx[t] = fmaxf(s[t], s[t + 8]);             // s[0..15]
+      for (int t = 0; t < 8; ++t) mx[t] = fmaxf(s[t], s[t + 8]);             // s[0..15]
 #pragma unroll
-    for (int i = 16; i < 128; i += 16) {                                    // i = 16, 32, ..., 112
+      for (int i = 16; i < 128; i += 16) {                                    // i = 16, 32, ..., 112
 #pragma unroll
-      for (int t = 0; t < 8; ++t) mx[t] = max3(mx[t], s[i + t], s[i + 8 + t]);  // s[i..i+15]
-    }
-    const float m_tile =
-        fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])), fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) * cs;
-    bool rescale = false;
-    float alpha = 1.0f;
-    if (m_tile > m_used + kRescaleLog2) {
-      alpha = ex2(m_used - m_tile);   // 0 on the first tile
-      l *= alpha;
-      corr *= alpha;
-      m_used = m_tile;
-      rescale = j > 0;
-    }
-    // O must be rescaled before this step's first P V MMA accumulates into it.
-    if (__any_sync(0xffffffffu, rescale)) {
-      const float a = rescale ? alpha : 1.0f;
+        for (int t = 0; t < 8; ++t) mx[t] = max3(mx[t], s[i + t], s[i + 8 + t]);  // s[i..i+15]
+      }
+      const float m_tile =
+          fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])), fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) * cs;
+      bool rescale = false;
+      float alpha = 1.0f;
+      if (m_tile > m_used + kRescaleLog2) {
+        alpha = ex2(m_used - m_tile);   // 0 on the first step of a segment
+        l *= alpha;
+        corr *= alpha;
+        m_used = m_tile;
+        rescale = j > 0;
+      }
+      // O must be rescaled before this step's first P V MMA accumulates into it.
+      if (__any_sync(0xffffffffu, rescale)) {
+        const float a = rescale ? alpha : 1.0f;
 #pragma unroll 1
-      for (int ch = 0; ch < 16; ++ch) {   // small chunks: s[] is still live here
-        uint32_t ov[8];
-        tmem_ld8(tO + ch * 8, ov);
+        for (int ch = 0; ch < 16; ++ch) {   // small chunks: s[] is still live here
+          uint32_t ov[8];
+          tmem_ld8(tO + ch * 8, ov);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * a);
-        tmem_st8(tO + ch * 8, ov);
+          for (int i = 0; i < 8; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * a);
+          tmem_st8(tO + ch * 8, ov);
+        }
       }
-    }
-    // The BF16 rounding of P matters most for the tile's largest term, which the stale
-    // running max leaves anywhere in [1, 2^kRescaleLog2]. corr accumulates that term's
-    // rounding error, so that l + corr is the sum of the weights the tensor core
-    // actually applies to V (up to the far smaller errors of the other terms).
-    {
-      const float pm = ex2(m_tile - m_used);
-      corr += __uint_as_float(pack_bf16(pm, 0.0f) << 16) - pm;
-    }
-    // p = 2^(s*cs - m) in two halves of 64 keys; each half is rounded to BF16, stored
-    // over S in TMEM and handed to the MMA warp at once, so the first half of the
-    // P V product runs while the second half is computed.
-    const float neg_m = -m_used;
-    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-    for (int half = 0; half < 2; ++half) {
-      uint32_t pk[32];
-#pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        const int e = half * 64 + 2 * i;
-        float e0, e1;
-        fma2(e0, e1, s[e], s[e + 1], cs, neg_m);
-        e0 = ex2(e0);
-        e1 = ex2(e1);
-        pk[i] = pack_bf16(e0, e1);
-        add2(acc[2 * (i & 3)], acc[2 * (i & 3) + 1], e0, e1);
+      // The BF16 rounding of P matters most for the tile's largest term, which the stale
+      // running max leaves anywhere in [1, 2^kRescaleLog2]. corr accumulates that term's
+      // rounding error, so that l + corr is the sum of the weights the tensor core
+      // actually applies to V (up to the far smaller errors of the other terms).
+      {
+        const float pm = ex2(m_tile - m_used);
+        corr += __uint_as_float(pack_bf16(pm, 0.0f) << 16) - pm;
       }
-      tmem_st32(tS + half * 32, pk);
+      // p = 2^(s*cs - m) in two halves of 64 keys; each half is rounded to BF16, stored
+      // over S in TMEM and handed to the MMA warp at once, so the first half of the
+      // P V product runs while the second half is computed.
+      const float neg_m = -m_used;
+      float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        uint32_t pk[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const int e = half * 64 + 2 * i;
+          float e0, e1;
+          fma2(e0, e1, s[e], s[e + 1], cs, neg_m);
+          e0 = ex2(e0);
+          e1 = ex2(e1);
+          pk[i] = pack_bf16(e0, e1);
+          add2(acc[2 * (i & 3)], acc[2 * (i & 3) + 1], e0, e1);
+        }
+        tmem_st32(tS + half * 32, pk);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(c.bar(kBarPFull + 2 * tile + half));
+      }
+      l += ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
+    }
+
+    if (!wait_warp(c, kBarOFull + tile, u & 1)) return;
+    tc_fence_after();
+    const int bh = sg.group / p.q_groups;
+    const int qrow = (sg.group % p.q_groups) * (kQTiles * kBM) + tile * kBM + r;
+    const bool live = qrow < p.Nq;
+    const size_t row_id = static_cast<size_t>(bh) * static_cast<size_t>(p.Nq) + static_cast<size_t>(qrow);
+    uint4* dst = reinterpret_cast<uint4*>(p.o + row_id * kD);
+    if (!sg.split) {
+      const float inv_l = 1.0f / (l + corr);
+#pragma unroll 1
+      for (int ch = 0; ch < 4; ++ch) {
+        uint32_t ov[32];
+        tmem_ld32(tO + ch * 32, ov);
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          pk[i] = pack_bf16(__uint_as_float(ov[2 * i]) * inv_l, __uint_as_float(ov[2 * i + 1]) * inv_l);
+        if (live) {
+#pragma unroll
+          for (int v = 0; v < 4; ++v)
+            dst[ch * 4 + v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+        }
+      }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(c.bar(kBarPFull + 2 * tile + half));
-    }
-    l += ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
-  }
-
-  if (ok) ok = wait_warp(c, kBarOFull + tile, 0);
-  if (!ok) return;
-  tc_fence_after();
-  const int qrow = q_row0 + tile * kBM + r;
-  const bool live = qrow < p.Nq;
-  const float inv_l = 1.0f / (l + corr);
-  const size_t row_id = static_cast<size_t>(bh) * static_cast<size_t>(p.Nq) + static_cast<size_t>(qrow);
-  uint4* dst = reinterpret_cast<uint4*>(p.o + row_id * kD);
+      if (lane == 0) mbar_arrive(c.bar(kBarOEmpty + tile));
+      if (live) p.lse[row_id] = (m_used + log2f(l)) * 0.69314718055994531f;
+    } else {
+      // This block holds only some key steps of the group: leave the unnormalised
+      // row, its running max and sums in the workspace.
+      float* rec = p.part + ((static_cast<size_t>(blockIdx.x) * 2 + sg.which) * kQTiles + tile) * kBM * kPartStride +
+                   static_cast<size_t>(r) * kPartStride;
 #pragma unroll 1
-  for (int ch = 0; ch < 4; ++ch) {
-    uint32_t ov[32];
-    tmem_ld32(tO + ch * 32, ov);
-    uint32_t pk[16];
+      for (int ch = 0; ch < 4; ++ch) {
+        uint32_t ov[32];
+        tmem_ld32(tO + ch * 32, ov);
+        float4* d4 = reinterpret_cast<float4*>(rec + ch * 32);
 #pragma unroll
-    for (int i = 0; i < 16; ++i)
-      pk[i] = pack_bf16(__uint_as_float(ov[2 * i]) * inv_l, __uint_as_float(ov[2 * i + 1]) * inv_l);
-    if (live) {
-#pragma unroll
-      for (int v = 0; v < 4; ++v)
-        dst[ch * 4 + v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+        for (int v = 0; v < 8; ++v)
+          d4[v] = make_float4(__uint_as_float(ov[4 * v]), __uint_as_float(ov[4 * v + 1]),
+                              __uint_as_float(ov[4 * v + 2]), __uint_as_float(ov[4 * v + 3]));
+      }
+      *reinterpret_cast<float4*>(rec + kD) = make_float4(m_used, l, corr, 0.0f);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(c.bar(kBarOEmpty + tile));   // O_tile may be overwritten now
+      // Count this warp's 32 rows in; the warp that completes the count merges them.
+      __threadfence();
+      __syncwarp();
+      const long long g_rel = sg.group - p.dp_groups;
+      const long long x0 = g_rel * p.n_kv;
+      const int grid = static_cast<int>(gridDim.x);
+      const int c_first = sk_block_of(x0, p.sk_steps, grid);
+      const int c_last = sk_block_of(x0 + p.n_kv - 1, p.sk_steps, grid);
+      unsigned int before = 0;
+      if (lane == 0) {
+        // counter = epoch << 8 | arrivals; a value from another launch counts as zero
+        unsigned int* ctr = p.cnt + (g_rel * kQTiles + tile) * 4 + quarter;
+        unsigned int old = atomicAdd(ctr, 0u);
+        for (;;) {
+          const unsigned int mine = (old >> 8) == p.epoch ? old + 1u : (p.epoch << 8) | 1u;
+          const unsigned int prev = atomicCAS(ctr, old, mine);
+          if (prev == old) break;
+          old = prev;   // another share of this group counted in meanwhile
+        }
+        before = (old >> 8) == p.epoch ? (old & 0xFFu) : 0u;
+      }
+      before = __shfl_sync(0xffffffffu, before, 0);
+      if (static_cast<int>(before) == c_last - c_first) {
+        __threadfence();
+        merge_split_row(p, tile, r, c_first, c_last, x0, live ? dst : nullptr, live ? p.lse + row_id : nullptr);
+      }
     }
+    gstep += static_cast<uint32_t>(n);
+    ++u;
   }
-  if (live) p.lse[row_id] = (m_used + log2f(l)) * 0.69314718055994531f;
 }
 
 // ---------------------------------------------------------------------------------
@@ -587,8 +818,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int bh = blockIdx.x / p.q_groups;
-  const int q_row0 = (blockIdx.x % p.q_groups) * (kQTiles * kBM);
 
   Ctl c;
   c.bars = base + kOffBar;
@@ -597,6 +826,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(c.bar(kBarQFull), 1);
+    mbar_init(c.bar(kBarQEmpty), 1);
     for (int s = 0; s < kSlots; ++s) {
       mbar_init(c.bar(kBarKVFull + s), 1);
       mbar_init(c.bar(kBarKVEmpty + s), 1);
@@ -606,6 +836,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(c.bar(kBarPFull + 2 * t), 4);       // one arrival per softmax warp
       mbar_init(c.bar(kBarPFull + 2 * t + 1), 4);
       mbar_init(c.bar(kBarOFull + t), 1);
+      mbar_init(c.bar(kBarOEmpty + t), 4);          // one arrival per softmax warp
     }
     mbar_init(c.bar(kBarDrain), 1);
     *c.abort = 0u;
@@ -624,13 +855,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + kOffTmemSlot);
 
   if (warp == 0) {
-    if (lane == 0) run_producer(c, base, &tmQ, &tmK, &tmV, p, bh, q_row0);
+    if (lane == 0) run_producer(c, base, &tmQ, &tmK, &tmV, p);
     __syncwarp();
   } else if (warp == 1) {
     if (lane == 0) run_mma(c, base, tmem, p);
     __syncwarp();
   } else if (warp >= 4) {
-    run_softmax<kPosScale>(c, tmem, p, (warp >> 2) - 1, bh, q_row0);
+    run_softmax<kPosScale>(c, tmem, p, (warp >> 2) - 1);
   }
 
   tc_fence_before();
@@ -641,6 +872,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                  : "memory");
   }
 }
+
 
 // ---------------------------------------------------------------------------------
 // Host side
@@ -679,12 +911,91 @@ bool make_map(CUtensorMap* map, const void* ptr, int rows, long long bh) {
 
 constexpr int kMaxDevices = 64;
 std::atomic<int> g_attr_done[2][kMaxDevices];
+std::atomic<int> g_sm_count[kMaxDevices];
+
+int sm_count(int dev) {
+  if (dev >= 0 && dev < kMaxDevices) {
+    const int cached = g_sm_count[dev].load(std::memory_order_relaxed);
+    if (cached > 0) return cached;
+  }
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) return -1;
+  if (dev >= 0 && dev < kMaxDevices) g_sm_count[dev].store(n, std::memory_order_relaxed);
+  return n;
+}
+
+// How the groups are spread over the persistent blocks (see the kernel's header).
+struct Plan {
+  int grid = 1;
+  long long dp_groups = 0;   // processed whole, round-robin
+  long long sk_groups = 0;   // their key steps split evenly over the blocks
+  long long sk_steps = 0;
+  bool has_split = false;    // some group's key steps end up in two or more blocks
+};
+
+Plan make_plan(long long n_groups, int n_kv, int sms) {
+  Plan pl;
+  if (n_groups >= sms) {
+    pl.grid = sms;
+    const long long waves = n_groups / sms, rem = n_groups % sms;
+    // Whole waves of whole groups; the remainder plus one full wave is split, which gives
+    // every block between one and two groups' worth of key steps in the split part.
+    pl.dp_groups = rem == 0 ? n_groups : (waves - 1) * sms;
+  } else {
+    const long long steps = n_groups * n_kv;
+    long long g = steps / kMinSegSteps;
+    pl.grid = static_cast<int>(g < 1 ? 1 : (g > sms ? sms : g));
+    pl.dp_groups = 0;
+  }
+  pl.sk_groups = n_groups - pl.dp_groups;
+  pl.sk_steps = pl.sk_groups * n_kv;
+  for (int c = 1; c < pl.grid && pl.sk_steps > 0; ++c)
+    if (sk_share_start(c, pl.sk_steps, pl.grid) % n_kv != 0) pl.has_split = true;
+  return pl;
+}
+
+// Workspace for split groups, cached per (device, stream) so that calls on different
+// streams never share one; calls on one stream are ordered by the stream.
+struct Workspace {
+  float* part = nullptr;
+  unsigned int* cnt = nullptr;
+  size_t part_bytes = 0, cnt_bytes = 0;
+  unsigned int epoch = 0;
+};
+std::mutex g_ws_mu;
+std::map<std::pair<int, uintptr_t>, Workspace> g_ws;
+
+// Returns ATTN_OK and fills part/cnt/epoch, or ATTN_ERR_CUDA.
+int get_workspace(int dev, cudaStream_t stream, size_t part_bytes, size_t cnt_bytes, float** part,
+                  unsigned int** cnt, unsigned int* epoch) {
+  std::lock_guard<std::mutex> lock(g_ws_mu);
+  Workspace& ws = g_ws[std::make_pair(dev, reinterpret_cast<uintptr_t>(stream))];
+  if (ws.part_bytes < part_bytes) {
+    if (ws.part) cudaFreeAsync(ws.part, stream);
+    ws.part = nullptr;
+    ws.part_bytes = 0;
+    if (cudaMallocAsync(reinterpret_cast<void**>(&ws.part), part_bytes, stream) != cudaSuccess) return ATTN_ERR_CUDA;
+    ws.part_bytes = part_bytes;
+  }
+  if (ws.cnt_bytes < cnt_bytes) {
+    if (ws.cnt) cudaFreeAsync(ws.cnt, stream);
+    ws.cnt = nullptr;
+    ws.cnt_bytes = 0;
+    if (cudaMallocAsync(reinterpret_cast<void**>(&ws.cnt), cnt_bytes, stream) != cudaSuccess) return ATTN_ERR_CUDA;
+    // counters start at epoch 0, which no launch uses
+    if (cudaMemsetAsync(ws.cnt, 0, cnt_bytes, stream) != cudaSuccess) return ATTN_ERR_CUDA;
+    ws.cnt_bytes = cnt_bytes;
+  }
+  ws.epoch = ws.epoch % 0xFFFFFFu + 1u;   // 1 .. 2^24 - 1
+  *part = ws.part;
+  *cnt = ws.cnt;
+  *epoch = ws.epoch;
+  return ATTN_OK;
+}
 
 template <bool kPos>
 int launch(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, const Params& p, int grid,
-           cudaStream_t stream) {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return ATTN_ERR_CUDA;
+           int dev, cudaStream_t stream) {
   auto kern = attn_fwd_kernel<kPos>;
   if (dev < 0 || dev >= kMaxDevices || !g_attr_done[kPos][dev].load(std::memory_order_acquire)) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) != cudaSuccess)
@@ -716,12 +1027,17 @@ extern "C" int attn_fwd(const void* q, const void* k, const void* v, void* o, fl
        reinterpret_cast<uintptr_t>(o)) & 15u)
     return ATTN_ERR_MISALIGNED;
   if (reinterpret_cast<uintptr_t>(lse) & 3u) return ATTN_ERR_MISALIGNED;
-  // index ranges: TMA coordinates and the block index are 32-bit
+  // index ranges: TMA coordinates and group indices are 32-bit
   const long long q_groups = (static_cast<long long>(Nq) + kQTiles * kBM - 1) / (kQTiles * kBM);
   if (bh > INT_MAX || bh * q_groups > INT_MAX) return ATTN_ERR_UNSUPPORTED;
   // element counts must fit a signed 64-bit byte offset
   const long long max_rows = static_cast<long long>(Nq > Nk ? Nq : Nk);
   if (bh > (LLONG_MAX / 256) / max_rows) return ATTN_ERR_INVALID_ARG;
+
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return ATTN_ERR_CUDA;
+  const int sms = sm_count(dev);
+  if (sms <= 0) return ATTN_ERR_CUDA;
 
   CUtensorMap mq, mk, mv;
   if (!make_map(&mq, q, Nq, bh) || !make_map(&mk, k, Nk, bh) || !make_map(&mv, v, Nk, bh))
@@ -735,13 +1051,24 @@ extern "C" int attn_fwd(const void* q, const void* k, const void* v, void* o, fl
   p.q_groups = static_cast<int>(q_groups);
   p.n_kv = (Nk + kBN - 1) / kBN;
   p.kv_tail = Nk - (p.n_kv - 1) * kBN;
+  const Plan pl = make_plan(bh * q_groups, p.n_kv, sms);
+  p.dp_groups = static_cast<int>(pl.dp_groups);
+  p.sk_steps = pl.sk_steps;
+  p.part = nullptr;
+  p.cnt = nullptr;
+  p.epoch = 0;
   p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
   p.wait_limit = g_wait_limit.load(std::memory_order_relaxed);
   p.withhold_tile = g_withhold.load(std::memory_order_relaxed);
 
-  const int grid = static_cast<int>(bh * q_groups);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  return scale > 0.0f ? launch<true>(mq, mk, mv, p, grid, s) : launch<false>(mq, mk, mv, p, grid, s);
+  if (pl.has_split) {
+    const size_t part_bytes = static_cast<size_t>(pl.grid) * kPartBytesPerBlock;
+    const size_t cnt_bytes = static_cast<size_t>(pl.sk_groups) * kQTiles * 4 * sizeof(unsigned int);
+    const int rc = get_workspace(dev, s, part_bytes, cnt_bytes, &p.part, &p.cnt, &p.epoch);
+    if (rc != ATTN_OK) return rc;
+  }
+  return scale > 0.0f ? launch<true>(mq, mk, mv, p, pl.grid, dev, s) : launch<false>(mq, mk, mv, p, pl.grid, dev, s);
 }
 
 extern "C" int attn_fwd_status(void* stream) {

@@ -23,8 +23,13 @@
  *     with d = 128, in device memory reachable from the current CUDA device.
  *   - BF16 is IEEE-style bfloat16 (1 sign, 8 exponent, 7 mantissa bits), passed as
  *     raw 16-bit storage (void*).
- *   - The caller owns every buffer. The library allocates no device memory and
- *     keeps no pointer after a call returns.
+ *   - The caller owns every buffer it passes; the library keeps no pointer to them
+ *     after a call returns. When a call's work does not divide evenly over the SMs,
+ *     the kernel splits the key range of some query tiles between thread blocks and
+ *     merges the pieces; it then needs a workspace (under 300 KB per SM) that the
+ *     library allocates with cudaMallocAsync on the call's stream the first time it
+ *     is needed, grows when a later call needs more, and keeps per (device, stream)
+ *     for the life of the process, so calls on different streams never share one.
  *   - Calls are asynchronous: work is enqueued on `stream` (a cudaStream_t; NULL
  *     means the legacy default stream) and the call returns at once. Only argument
  *     and launch errors are reported by the return value.
@@ -62,11 +67,12 @@ extern "C" {
  *   scale  any finite float, applied to the scores (1/sqrt(d) for standard attention).
  *   stream a cudaStream_t, or NULL.
  *
- * o must not overlap q, k, v or lse (not checked). The call writes o and lse only.
+ * o must not overlap q, k, v or lse (not checked). The call writes o, lse and, when it
+ * splits work between blocks, its own workspace (see above).
  *
  * Returns ATTN_OK once the kernel is enqueued; ATTN_ERR_INVALID_ARG,
  * ATTN_ERR_UNSUPPORTED or ATTN_ERR_MISALIGNED without touching the GPU when an
- * argument is rejected; ATTN_ERR_CUDA when the launch fails.
+ * argument is rejected; ATTN_ERR_CUDA when the launch or the workspace allocation fails.
  */
 int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
              int B, int H, int Nq, int Nk, int d, float scale, void* stream);

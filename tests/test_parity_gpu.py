@@ -26,6 +26,9 @@ SCALE = float(np.float32(1 / math.sqrt(128)))
     (1, 1, 1, 129),
     (1, 3, 1000, 777),
     (2, 2, 128, 2176),    # 17 K/V steps
+    (1, 1, 256, 5120),    # one group of 40 key steps split over 5 blocks
+    (1, 2, 300, 3000),    # 4 groups of 24 steps split three ways, ragged tails
+    (2, 3, 520, 1290),    # 18 groups of 11 steps: shares cut groups at uneven points
 ])
 def test_full_parity_small(gpu_lib, B, H, Nq, Nk):
     check_case(gpu_lib, B, H, Nq, Nk, seed=B * 1000 + Nq + Nk)
@@ -100,7 +103,8 @@ def test_other_scales(gpu_lib, scale):
 
 
 def test_results_are_deterministic(gpu_lib):
-    q, k, v = make_qkv(1, 4, 512, 512, seed=9)
+    # a split group: the merge order must not depend on which share finishes last
+    q, k, v = make_qkv(1, 1, 256, 5120, seed=9)
     o1, l1 = run_gpu(gpu_lib, q, k, v, SCALE)
     o2, l2 = run_gpu(gpu_lib, q, k, v, SCALE)
     assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
