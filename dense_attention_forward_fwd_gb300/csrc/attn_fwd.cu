@@ -1104,3 +1104,96 @@ extern "C" int attn_fwd_set_wait_limit(unsigned long long cycles, int withhold_t
 }
 
 extern "C" unsigned long long attn_fwd_kernel_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+// ---------------------------------------------------------------------------------
+// Entry point that allocates nothing
+// ---------------------------------------------------------------------------------
+// Some callers must not allocate device memory once they are running: applications
+// that budget all of the GPU's memory up front (an extra allocation could fail or push
+// something else out), loops where an allocation may synchronise the device and stall
+// the pipeline, and programs whose own allocator owns every byte of device memory. For
+// them attn_fwd_noalloc runs the same kernel with its split-merge workspace in the
+// fixed array below instead of a cudaMallocAsync allocation. The array belongs to this
+// library's module: every GPU that loads the library holds it until the process exits.
+constexpr size_t kNoAllocScratchBytes = size_t(48) << 20;   // 48 MiB: the records of up to 186 SMs
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+namespace {
+std::mutex g_noalloc_mu;
+void* g_noalloc_addr[kMaxDevices];   // device address of g_noalloc_scratch, looked up once per device
+}  // namespace
+
+extern "C" int attn_fwd_noalloc(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                                int Nq, int Nk, int d, float scale, void* stream) {
+  // the same argument rules as attn_fwd
+  if (B < 0 || H < 0 || Nq < 0 || Nk < 0) return ATTN_ERR_INVALID_ARG;
+  if (d != kD) return ATTN_ERR_UNSUPPORTED;
+  if (!std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
+  const long long bh = static_cast<long long>(B) * H;
+  if (bh == 0 || Nq == 0) return ATTN_OK;
+  if (Nk == 0) return ATTN_ERR_INVALID_ARG;
+  if (!q || !k || !v || !o || !lse) return ATTN_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) | reinterpret_cast<uintptr_t>(v) |
+       reinterpret_cast<uintptr_t>(o)) & 15u)
+    return ATTN_ERR_MISALIGNED;
+  if (reinterpret_cast<uintptr_t>(lse) & 3u) return ATTN_ERR_MISALIGNED;
+  const long long q_groups = (static_cast<long long>(Nq) + kQTiles * kBM - 1) / (kQTiles * kBM);
+  if (bh > INT_MAX || bh * q_groups > INT_MAX) return ATTN_ERR_UNSUPPORTED;
+  const long long max_rows = static_cast<long long>(Nq > Nk ? Nq : Nk);
+  if (bh > (LLONG_MAX / 256) / max_rows) return ATTN_ERR_INVALID_ARG;
+
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return ATTN_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return ATTN_ERR_UNSUPPORTED;
+  const int sms = sm_count(dev);
+  if (sms <= 0) return ATTN_ERR_CUDA;
+
+  // In host code g_noalloc_scratch only stands for the array: its device address has to
+  // be asked for, with this device current. The first call on each device does that.
+  void* scratch = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    if (g_noalloc_addr[dev] == nullptr) {
+      void* ptr = nullptr;
+      if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || ptr == nullptr) return ATTN_ERR_CUDA;
+      g_noalloc_addr[dev] = ptr;
+    }
+    scratch = g_noalloc_addr[dev];
+  }
+
+  CUtensorMap mq, mk, mv;
+  if (!make_map(&mq, q, Nq, bh) || !make_map(&mk, k, Nk, bh) || !make_map(&mv, v, Nk, bh))
+    return ATTN_ERR_CUDA;
+
+  Params p;
+  p.o = static_cast<uint16_t*>(o);
+  p.lse = lse;
+  p.Nq = Nq;
+  p.Nk = Nk;
+  p.q_groups = static_cast<int>(q_groups);
+  p.n_kv = (Nk + kBN - 1) / kBN;
+  p.kv_tail = Nk - (p.n_kv - 1) * kBN;
+  const Plan pl = make_plan(bh * q_groups, p.n_kv, sms);
+  p.dp_groups = static_cast<int>(pl.dp_groups);
+  p.sk_steps = pl.sk_steps;
+  p.part = nullptr;
+  p.cnt = nullptr;
+  p.epoch = 1;
+  p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+  p.wait_limit = g_wait_limit.load(std::memory_order_relaxed);
+  p.withhold_tile = g_withhold.load(std::memory_order_relaxed);
+
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (pl.has_split) {
+    const size_t part_bytes = static_cast<size_t>(pl.grid) * kPartBytesPerBlock;
+    const size_t cnt_off = (part_bytes + 255) & ~static_cast<size_t>(255);
+    const size_t cnt_bytes = static_cast<size_t>(pl.sk_groups) * kQTiles * 4 * sizeof(unsigned int);
+    if (cnt_off + cnt_bytes > kNoAllocScratchBytes) return ATTN_ERR_UNSUPPORTED;   // beyond the fixed maximum
+    p.part = static_cast<float*>(scratch);
+    p.cnt = reinterpret_cast<unsigned int*>(static_cast<unsigned char*>(scratch) + cnt_off);
+    // The array keeps whatever the previous call left; the arrival counters must start
+    // at zero, so they are cleared on the call's stream before the kernel runs.
+    if (cudaMemsetAsync(p.cnt, 0, cnt_bytes, s) != cudaSuccess) return ATTN_ERR_CUDA;
+  }
+  return scale > 0.0f ? launch<true>(mq, mk, mv, p, pl.grid, dev, s) : launch<false>(mq, mk, mv, p, pl.grid, dev, s);
+}

@@ -78,6 +78,33 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
              int B, int H, int Nq, int Nk, int d, float scale, void* stream);
 
 /*
+ * attn_fwd_noalloc -- attn_fwd for callers that cannot allocate device memory.
+ *
+ * There is no counterpart on the pages: this is a service of the library. Some callers
+ * must not allocate once they are running: applications that budget all of the GPU's
+ * memory up front (an extra allocation could fail or evict something else), loops where
+ * an allocation may synchronise the device, and programs whose own allocator owns every
+ * byte of device memory. attn_fwd may allocate a workspace (see the conventions above);
+ * this entry point never calls cudaMalloc, cudaMallocAsync, cudaFree or any allocating
+ * routine. It computes the same result with the same kernel, keeping the workspace for
+ * split work in a fixed 48 MiB array inside the library, which every GPU that loads the
+ * library holds until the process exits.
+ *
+ * Arguments, layouts and return values are those of attn_fwd, plus:
+ *   - ATTN_ERR_UNSUPPORTED when the call would need more than the fixed 48 MiB (only on
+ *     a device with more than 186 SMs) or the device index is 64 or above.
+ *   - The first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call before any
+ *     stream capture on the device.
+ *   - Every call on a device uses the same array, which keeps the previous call's
+ *     contents; each call clears the part that must start at zero on its own stream.
+ *     Calls whose kernels overlap on the GPU (different streams, no ordering between
+ *     them) race on the array and may return wrong results: order them.
+ */
+int attn_fwd_noalloc(const void* q, const void* k, const void* v, void* o, float* lse,
+                     int B, int H, int Nq, int Nk, int d, float scale, void* stream);
+
+/*
  * attn_fwd_status -- synchronises `stream`, then reads and clears the device status
  * word that kernels of this library set when a pipeline wait runs past its time
  * limit (every wait inside the kernel is bounded; on expiry the block stops its work,
