@@ -94,10 +94,11 @@ static_assert(kOffKV % 1024 == 0 && kOffBar % 8 == 0, "swizzle atoms need 1024-b
 static_assert(kSmemBytes <= 232448, "exceeds the 227 KB shared memory of one block");
 
 // Workspace of split groups: per block two partial records (its first and its last
-// split segment), each [tile][row][kPartStride] floats: 128 of unnormalised O, then
-// m (log2 units), l, corr and one pad word.
-constexpr int kPartStride = kD + 4;
-constexpr size_t kPartBytesPerBlock = size_t(2) * kQTiles * kBM * kPartStride * sizeof(float);
+// split segment), each holding per Q tile the unnormalised O column-major (element
+// (column c, row r) at c * kBM + r, so that a warp's 32 rows of one column are one
+// 128-byte line), then m (log2 units), l and corr, kBM floats each.
+constexpr int kPartFloatsPerTile = kD * kBM + 3 * kBM;
+constexpr size_t kPartBytesPerBlock = size_t(2) * kQTiles * kPartFloatsPerTile * sizeof(float);
 constexpr int kMinSegSteps = 8;   // smallest share of a group worth a block of its own
 
 struct Params {
@@ -474,6 +475,51 @@ __device__ __forceinline__ void issue_pv_half(uint32_t d_tmem, uint32_t p_tmem, 
   }
 }
 
+// One K/V step of the MMA issuer: O_i += P_i V_j for both Q tiles and, when another
+// step follows (kMore), S_i = Q_i K_{j+1}^T; otherwise the commits that hand O to the
+// epilogue. Returns false when a wait gave up.
+template <bool kMore>
+__device__ __forceinline__ bool mma_step(const Ctl& c, uint32_t base, const uint32_t (&tS)[2],
+                                         const uint32_t (&tO)[2], const uint32_t (&sQ)[2], int itV,
+                                         uint32_t ph, bool first) {
+  const int slotV = itV % kSlots;
+  const int itK = itV + 1, slotK = itK % kSlots;
+  const uint32_t sV = base + kOffKV + slotV * kTileBytes;
+  const uint32_t sK = base + kOffKV + slotK * kTileBytes;
+  if (!wait_phase(c, kBarKVFull + slotV, (itV / kSlots) & 1, true)) return false;
+  // tile 0: O0 += P0 V_j, then S0 = Q0 K_{j+1}^T
+  if (!wait_phase(c, kBarPFull + 0, ph, true)) return false;
+  tc_fence_after();
+  issue_pv_half(tO[0], tS[0], sV, 0, !first);
+  if (!wait_phase(c, kBarPFull + 1, ph, true)) return false;
+  tc_fence_after();
+  issue_pv_half(tO[0], tS[0], sV, 1, true);
+  if (kMore) {
+    if (!wait_phase(c, kBarKVFull + slotK, (itK / kSlots) & 1, true)) return false;
+    tc_fence_after();
+    issue_qk(tS[0], sQ[0], sK);
+    tc_commit(c.bar(kBarSFull + 0));
+  } else {
+    tc_commit(c.bar(kBarOFull + 0));
+  }
+  // tile 1: O1 += P1 V_j, then S1 = Q1 K_{j+1}^T
+  if (!wait_phase(c, kBarPFull + 2, ph, true)) return false;
+  tc_fence_after();
+  issue_pv_half(tO[1], tS[1], sV, 0, !first);
+  if (!wait_phase(c, kBarPFull + 3, ph, true)) return false;
+  tc_fence_after();
+  issue_pv_half(tO[1], tS[1], sV, 1, true);
+  tc_commit(c.bar(kBarKVEmpty + slotV));
+  if (kMore) {
+    issue_qk(tS[1], sQ[1], sK);
+    tc_commit(c.bar(kBarSFull + 1));
+    tc_commit(c.bar(kBarKVEmpty + slotK));
+  } else {
+    tc_commit(c.bar(kBarOFull + 1));
+  }
+  return true;
+}
+
 __device__ void run_mma(const Ctl& c, uint32_t base, uint32_t tmem, const Params& p) {
   const uint32_t tS[2] = {tmem, tmem + 128};
   const uint32_t tO[2] = {tmem + 256, tmem + 384};
@@ -481,86 +527,38 @@ __device__ void run_mma(const Ctl& c, uint32_t base, uint32_t tmem, const Params
   int it = 0;           // K/V items consumed
   uint32_t gstep = 0;   // K/V steps of all previous segments: phase of s_full / p_full
   int u = 0;            // segments started
-  bool ok = true;
   SegIter si(p);
   Segment sg;
-  while (ok && si.next(sg)) {
+  while (si.next(sg)) {
     const int n = sg.kv1 - sg.kv0;
-    {
-      const int slotK = it % kSlots;
-      if (!wait_phase(c, kBarQFull, u & 1, true) ||
-          !wait_phase(c, kBarKVFull + slotK, (it / kSlots) & 1, true))
-        break;
-      tc_fence_after();
-      const uint32_t sK = base + kOffKV + slotK * kTileBytes;
-      issue_qk(tS[0], sQ[0], sK);
-      tc_commit(c.bar(kBarSFull + 0));
-      issue_qk(tS[1], sQ[1], sK);
-      tc_commit(c.bar(kBarSFull + 1));
-      tc_commit(c.bar(kBarKVEmpty + slotK));
-      if (n == 1) tc_commit(c.bar(kBarQEmpty));   // the segment's last S MMA is issued
-    }
-    for (int j = 0; j < n; ++j) {
-      const int itV = it + 2 * j + 1, slotV = itV % kSlots;
-      const int itK = it + 2 * j + 2, slotK = itK % kSlots;
-      const bool more = j + 1 < n;
-      const uint32_t ph = (gstep + static_cast<uint32_t>(j)) & 1u;
-      const uint32_t sV = base + kOffKV + slotV * kTileBytes;
-      const uint32_t sK = base + kOffKV + slotK * kTileBytes;
-      if (!wait_phase(c, kBarKVFull + slotV, (itV / kSlots) & 1, true)) {
+    const int slotK = it % kSlots;
+    if (!wait_phase(c, kBarQFull, u & 1, true) ||
+        !wait_phase(c, kBarKVFull + slotK, (it / kSlots) & 1, true))
+      break;
+    tc_fence_after();
+    const uint32_t sK = base + kOffKV + slotK * kTileBytes;
+    issue_qk(tS[0], sQ[0], sK);
+    tc_commit(c.bar(kBarSFull + 0));
+    issue_qk(tS[1], sQ[1], sK);
+    tc_commit(c.bar(kBarSFull + 1));
+    tc_commit(c.bar(kBarKVEmpty + slotK));
+    if (n == 1) tc_commit(c.bar(kBarQEmpty));   // the segment's last S MMA is issued
+    // The segment's first P V products overwrite O: the previous segment's epilogue must
+    // have read both accumulators out of TMEM.
+    if (u > 0 && (!wait_phase(c, kBarOEmpty + 0, (u - 1) & 1, true) ||
+                  !wait_phase(c, kBarOEmpty + 1, (u - 1) & 1, true)))
+      break;
+    bool ok = true;
+    int j = 0;
+    for (; j + 1 < n; ++j) {
+      if (!mma_step<true>(c, base, tS, tO, sQ, it + 2 * j + 1, (gstep + j) & 1u, j == 0)) {
         ok = false;
         break;
-      }
-      // tile 0: O0 += P0 V_j (the first product of a segment overwrites O0, so the
-      // previous segment's epilogue must have read it out), then S0 = Q0 K_{j+1}^T
-      if ((j == 0 && u > 0 && !wait_phase(c, kBarOEmpty + 0, (u - 1) & 1, true)) ||
-          !wait_phase(c, kBarPFull + 0, ph, true)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      issue_pv_half(tO[0], tS[0], sV, 0, j > 0);
-      if (!wait_phase(c, kBarPFull + 1, ph, true)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      issue_pv_half(tO[0], tS[0], sV, 1, true);
-      if (more) {
-        if (!wait_phase(c, kBarKVFull + slotK, (itK / kSlots) & 1, true)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        issue_qk(tS[0], sQ[0], sK);
-        tc_commit(c.bar(kBarSFull + 0));
-      } else {
-        tc_commit(c.bar(kBarOFull + 0));
-      }
-      // tile 1: O1 += P1 V_j, then S1 = Q1 K_{j+1}^T
-      if ((j == 0 && u > 0 && !wait_phase(c, kBarOEmpty + 1, (u - 1) & 1, true)) ||
-          !wait_phase(c, kBarPFull + 2, ph, true)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      issue_pv_half(tO[1], tS[1], sV, 0, j > 0);
-      if (!wait_phase(c, kBarPFull + 3, ph, true)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      issue_pv_half(tO[1], tS[1], sV, 1, true);
-      tc_commit(c.bar(kBarKVEmpty + slotV));
-      if (more) {
-        issue_qk(tS[1], sQ[1], sK);
-        tc_commit(c.bar(kBarSFull + 1));
-        tc_commit(c.bar(kBarKVEmpty + slotK));
-        if (j + 2 == n) tc_commit(c.bar(kBarQEmpty));   // the segment's last S MMA is issued
-      } else {
-        tc_commit(c.bar(kBarOFull + 1));
       }
     }
+    if (!ok) break;
+    if (n > 1) tc_commit(c.bar(kBarQEmpty));   // the last S MMA (step n-2) is issued
+    if (!mma_step<false>(c, base, tS, tO, sQ, it + 2 * j + 1, (gstep + j) & 1u, j == 0)) break;
     it += 2 * n;
     gstep += static_cast<uint32_t>(n);
     ++u;
@@ -574,23 +572,28 @@ __device__ void run_mma(const Ctl& c, uint32_t base, uint32_t tmem, const Params
 // calling warp was the last of the group's shares to finish these 32 rows). With
 // m_s, l_s, corr_s, O_s the running max, sums and unnormalised output of share s and
 // M = max m_s, w_s = 2^(m_s - M): O = sum w_s O_s / sum w_s (l_s + corr_s) and
-// LSE = (M + log2 sum w_s l_s) * ln 2.
+// LSE = (M + log2 sum w_s l_s) * ln 2. Shares are visited in block order, so the
+// result does not depend on which share finished last.
 __device__ void merge_split_row(const Params& p, int tile, int r, int c_first, int c_last, long long x0,
                                 uint4* dst, float* lse_out) {
-  const int grid = static_cast<int>(gridDim.x);
+  const long long x0_grid = x0 * static_cast<long long>(gridDim.x);
+  // share cs's record: its first segment's slot when its share starts inside this group
+  // (sk_share_start(cs) >= x0, compared without dividing), else its last segment's
   auto record = [&](int cs) -> const float* {
-    const int which = sk_share_start(cs, p.sk_steps, grid) >= x0 ? 0 : 1;
-    return p.part + ((static_cast<size_t>(cs) * 2 + which) * kQTiles + tile) * kBM * kPartStride +
-           static_cast<size_t>(r) * kPartStride;
+    const int which = static_cast<long long>(cs) * p.sk_steps >= x0_grid ? 0 : 1;
+    return p.part + (static_cast<size_t>(cs) * 2 + which) * kQTiles * kPartFloatsPerTile +
+           static_cast<size_t>(tile) * kPartFloatsPerTile;
   };
+  constexpr int kM = kD * kBM, kL = kM + kBM, kC = kL + kBM;
   float M = -INFINITY;
-  for (int cs = c_first; cs <= c_last; ++cs) M = fmaxf(M, __ldcg(record(cs) + kD));
+  for (int cs = c_first; cs <= c_last; ++cs) M = fmaxf(M, __ldcg(record(cs) + kM + r));
   float L = 0.0f, Lr = 0.0f;
   for (int cs = c_first; cs <= c_last; ++cs) {
-    const float4 st = __ldcg(reinterpret_cast<const float4*>(record(cs) + kD));
-    const float w = ex2(st.x - M);
-    L += st.y * w;
-    Lr += (st.y + st.z) * w;
+    const float* rec = record(cs);
+    const float w = ex2(__ldcg(rec + kM + r) - M);
+    const float l_s = __ldcg(rec + kL + r);
+    L += l_s * w;
+    Lr += (l_s + __ldcg(rec + kC + r)) * w;
   }
   const float inv = 1.0f / Lr;
 #pragma unroll 1
@@ -600,24 +603,20 @@ __device__ void merge_split_row(const Params& p, int tile, int r, int c_first, i
     for (int i = 0; i < 32; ++i) acc[i] = 0.0f;
     for (int cs = c_first; cs <= c_last; ++cs) {
       const float* rec = record(cs);
-      const float w = ex2(__ldcg(rec + kD) - M);
-      const float4* src = reinterpret_cast<const float4*>(rec + ch * 32);
+      const float w = ex2(__ldcg(rec + kM + r) - M);
+      float v[32];
 #pragma unroll
-      for (int v = 0; v < 8; ++v) {
-        const float4 o4 = __ldcg(src + v);
-        acc[4 * v + 0] += o4.x * w;
-        acc[4 * v + 1] += o4.y * w;
-        acc[4 * v + 2] += o4.z * w;
-        acc[4 * v + 3] += o4.w * w;
-      }
+      for (int i = 0; i < 32; ++i) v[i] = __ldcg(rec + (ch * 32 + i) * kBM + r);
+#pragma unroll
+      for (int i = 0; i < 32; ++i) acc[i] = fmaf(v[i], w, acc[i]);
     }
     if (dst != nullptr) {
 #pragma unroll
-      for (int v = 0; v < 4; ++v)
-        dst[ch * 4 + v] = make_uint4(pack_bf16(acc[8 * v + 0] * inv, acc[8 * v + 1] * inv),
-                                     pack_bf16(acc[8 * v + 2] * inv, acc[8 * v + 3] * inv),
-                                     pack_bf16(acc[8 * v + 4] * inv, acc[8 * v + 5] * inv),
-                                     pack_bf16(acc[8 * v + 6] * inv, acc[8 * v + 7] * inv));
+      for (int v4 = 0; v4 < 4; ++v4)
+        dst[ch * 4 + v4] = make_uint4(pack_bf16(acc[8 * v4 + 0] * inv, acc[8 * v4 + 1] * inv),
+                                      pack_bf16(acc[8 * v4 + 2] * inv, acc[8 * v4 + 3] * inv),
+                                      pack_bf16(acc[8 * v4 + 4] * inv, acc[8 * v4 + 5] * inv),
+                                      pack_bf16(acc[8 * v4 + 6] * inv, acc[8 * v4 + 7] * inv));
     }
   }
   if (lse_out != nullptr) *lse_out = (M + log2f(L)) * 0.69314718055994531f;
@@ -756,19 +755,18 @@ __device__ void run_softmax(const Ctl& c, uint32_t tmem, const Params& p, int ti
     } else {
       // This block holds only some key steps of the group: leave the unnormalised
       // row, its running max and sums in the workspace.
-      float* rec = p.part + ((static_cast<size_t>(blockIdx.x) * 2 + sg.which) * kQTiles + tile) * kBM * kPartStride +
-                   static_cast<size_t>(r) * kPartStride;
+      float* rec = p.part + (static_cast<size_t>(blockIdx.x) * 2 + sg.which) * kQTiles * kPartFloatsPerTile +
+                   static_cast<size_t>(tile) * kPartFloatsPerTile;
 #pragma unroll 1
       for (int ch = 0; ch < 4; ++ch) {
         uint32_t ov[32];
         tmem_ld32(tO + ch * 32, ov);
-        float4* d4 = reinterpret_cast<float4*>(rec + ch * 32);
 #pragma unroll
-        for (int v = 0; v < 8; ++v)
-          d4[v] = make_float4(__uint_as_float(ov[4 * v]), __uint_as_float(ov[4 * v + 1]),
-                              __uint_as_float(ov[4 * v + 2]), __uint_as_float(ov[4 * v + 3]));
+        for (int i = 0; i < 32; ++i) rec[(ch * 32 + i) * kBM + r] = __uint_as_float(ov[i]);   // one line per warp
       }
-      *reinterpret_cast<float4*>(rec + kD) = make_float4(m_used, l, corr, 0.0f);
+      rec[kD * kBM + r] = m_used;
+      rec[kD * kBM + kBM + r] = l;
+      rec[kD * kBM + 2 * kBM + r] = corr;
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(c.bar(kBarOEmpty + tile));   // O_tile may be overwritten now
