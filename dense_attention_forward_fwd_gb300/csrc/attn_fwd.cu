@@ -63,7 +63,7 @@ constexpr int kD = 128;                        // head dimension
 constexpr int kBM = 128;                       // query rows per Q tile (= TMEM lanes)
 constexpr int kBN = 128;                       // keys per K/V tile
 constexpr int kQTiles = 2;                     // Q tiles per block
-constexpr int kSlots = 5;                      // K/V ring depth, one 128x128 tile per slot
+constexpr int kSlots = 4;                      // K/V ring depth, one 128x128 tile per slot
 constexpr int kTileBytes = kBM * kD * 2;       // 32 KB of BF16
 constexpr int kBoxBytes = kTileBytes / 2;      // one TMA box: 64 columns (128 B) x 128 rows
 constexpr int kThreads = 384;
@@ -87,7 +87,10 @@ constexpr int kBarDrain = kBarOEmpty + kQTiles;
 constexpr int kNumBars = kBarDrain + 1;
 constexpr int kOffTmemSlot = kOffBar + kNumBars * 8;
 constexpr int kOffAbort = kOffTmemSlot + 4;
-constexpr int kSmemUsed = kOffAbort + 4;
+// Per softmax warp, a staging tile for its 32 rows x 64 columns of BF16 output.
+constexpr int kStageBytes = 32 * 64 * 2;
+constexpr int kOffStage = (kOffAbort + 4 + 127) & ~127;
+constexpr int kSmemUsed = kOffStage + kQTiles * 4 * kStageBytes;   // one stage per softmax warp
 constexpr int kSmemBytes = kSmemUsed + 1024;   // slack to align the dynamic base to 1024
 
 static_assert(kOffKV % 1024 == 0 && kOffBar % 8 == 0, "swizzle atoms need 1024-byte alignment");
@@ -568,6 +571,28 @@ __device__ void run_mma(const Ctl& c, uint32_t base, uint32_t tmem, const Params
   wait_phase(c, kBarDrain, 0, false);
 }
 
+// Stores one 64-column half of this warp's 32 output rows (pk: the calling thread's own
+// row, packed BF16 pairs). The rows go through the warp's staging tile in shared memory
+// (16-byte chunks swizzled by row) so that each global store instruction covers four
+// whole 128-byte lines instead of touching 32 lines with 16 bytes each. Rows from
+// valid_rows on are not stored.
+__device__ __forceinline__ void store_half_rows(uint8_t* stage, const uint32_t (&pk)[32], uint16_t* o_row0,
+                                                int valid_rows, int half) {
+  const int lane = threadIdx.x & 31;
+  uint4* st = reinterpret_cast<uint4*>(stage);
+#pragma unroll
+  for (int k = 0; k < 8; ++k)
+    st[lane * 8 + (k ^ (lane & 7))] = make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
+  __syncwarp();
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int rr = i * 4 + (lane >> 3), cc = lane & 7;   // row within the warp, 16-byte chunk
+    const uint4 v = st[rr * 8 + (cc ^ (rr & 7))];
+    if (rr < valid_rows) reinterpret_cast<uint4*>(o_row0 + static_cast<size_t>(rr) * kD + half * 64)[cc] = v;
+  }
+  __syncwarp();
+}
+
 // Merges the partial records of one split group for this thread's query row (the
 // calling warp was the last of the group's shares to finish these 32 rows). With
 // m_s, l_s, corr_s, O_s the running max, sums and unnormalised output of share s and
@@ -575,7 +600,7 @@ __device__ void run_mma(const Ctl& c, uint32_t base, uint32_t tmem, const Params
 // LSE = (M + log2 sum w_s l_s) * ln 2. Shares are visited in block order, so the
 // result does not depend on which share finished last.
 __device__ void merge_split_row(const Params& p, int tile, int r, int c_first, int c_last, long long x0,
-                                uint4* dst, float* lse_out) {
+                                uint8_t* stage, uint16_t* o_row0, int valid_rows, float* lse_out) {
   const long long x0_grid = x0 * static_cast<long long>(gridDim.x);
   // share cs's record: its first segment's slot when its share starts inside this group
   // (sk_share_start(cs) >= x0, compared without dividing), else its last segment's
@@ -597,33 +622,33 @@ __device__ void merge_split_row(const Params& p, int tile, int r, int c_first, i
   }
   const float inv = 1.0f / Lr;
 #pragma unroll 1
-  for (int ch = 0; ch < 4; ++ch) {
-    float acc[32];
+  for (int h = 0; h < 2; ++h) {
+    uint32_t pk[32];
 #pragma unroll
-    for (int i = 0; i < 32; ++i) acc[i] = 0.0f;
-    for (int cs = c_first; cs <= c_last; ++cs) {
-      const float* rec = record(cs);
-      const float w = ex2(__ldcg(rec + kM + r) - M);
-      float v[32];
+    for (int cc = 0; cc < 2; ++cc) {
+      const int ch = 2 * h + cc;
+      float acc[32];
 #pragma unroll
-      for (int i = 0; i < 32; ++i) v[i] = __ldcg(rec + (ch * 32 + i) * kBM + r);
+      for (int i = 0; i < 32; ++i) acc[i] = 0.0f;
+      for (int cs = c_first; cs <= c_last; ++cs) {
+        const float* rec = record(cs);
+        const float w = ex2(__ldcg(rec + kM + r) - M);
+        float v[32];
 #pragma unroll
-      for (int i = 0; i < 32; ++i) acc[i] = fmaf(v[i], w, acc[i]);
+        for (int i = 0; i < 32; ++i) v[i] = __ldcg(rec + (ch * 32 + i) * kBM + r);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) acc[i] = fmaf(v[i], w, acc[i]);
+      }
+#pragma unroll
+      for (int i = 0; i < 16; ++i) pk[16 * cc + i] = pack_bf16(acc[2 * i] * inv, acc[2 * i + 1] * inv);
     }
-    if (dst != nullptr) {
-#pragma unroll
-      for (int v4 = 0; v4 < 4; ++v4)
-        dst[ch * 4 + v4] = make_uint4(pack_bf16(acc[8 * v4 + 0] * inv, acc[8 * v4 + 1] * inv),
-                                      pack_bf16(acc[8 * v4 + 2] * inv, acc[8 * v4 + 3] * inv),
-                                      pack_bf16(acc[8 * v4 + 4] * inv, acc[8 * v4 + 5] * inv),
-                                      pack_bf16(acc[8 * v4 + 6] * inv, acc[8 * v4 + 7] * inv));
-    }
+    store_half_rows(stage, pk, o_row0, valid_rows, h);
   }
   if (lse_out != nullptr) *lse_out = (M + log2f(L)) * 0.69314718055994531f;
 }
 
 template <bool kPosScale>
-__device__ void run_softmax(const Ctl& c, uint32_t tmem, const Params& p, int tile) {
+__device__ void run_softmax(const Ctl& c, uint32_t tmem, uint8_t* stage, const Params& p, int tile) {
   const int quarter = (threadIdx.x >> 5) & 3;   // TMEM lanes this warp may access
   const int lane = threadIdx.x & 31;
   const int r = quarter * 32 + lane;            // query row within the tile
@@ -728,29 +753,32 @@ __device__ void run_softmax(const Ctl& c, uint32_t tmem, const Params& p, int ti
     if (!wait_warp(c, kBarOFull + tile, u & 1)) return;
     tc_fence_after();
     const int bh = sg.group / p.q_groups;
-    const int qrow = (sg.group % p.q_groups) * (kQTiles * kBM) + tile * kBM + r;
+    const int qrow_w0 = (sg.group % p.q_groups) * (kQTiles * kBM) + tile * kBM + quarter * 32;   // warp's first row
+    const int qrow = qrow_w0 + lane;
     const bool live = qrow < p.Nq;
+    const int valid_rows = p.Nq - qrow_w0;   // rows of this warp inside the sequence (may be <= 0)
     const size_t row_id = static_cast<size_t>(bh) * static_cast<size_t>(p.Nq) + static_cast<size_t>(qrow);
-    uint4* dst = reinterpret_cast<uint4*>(p.o + row_id * kD);
+    uint16_t* o_row0 = p.o + (static_cast<size_t>(bh) * static_cast<size_t>(p.Nq) + static_cast<size_t>(qrow_w0)) * kD;
     if (!sg.split) {
       const float inv_l = 1.0f / (l + corr);
 #pragma unroll 1
-      for (int ch = 0; ch < 4; ++ch) {
-        uint32_t ov[32];
-        tmem_ld32(tO + ch * 32, ov);
-        uint32_t pk[16];
+      for (int h = 0; h < 2; ++h) {
+        uint32_t pk[32];
 #pragma unroll
-        for (int i = 0; i < 16; ++i)
-          pk[i] = pack_bf16(__uint_as_float(ov[2 * i]) * inv_l, __uint_as_float(ov[2 * i + 1]) * inv_l);
-        if (live) {
+        for (int cc = 0; cc < 2; ++cc) {
+          uint32_t ov[32];
+          tmem_ld32(tO + (2 * h + cc) * 32, ov);
 #pragma unroll
-          for (int v = 0; v < 4; ++v)
-            dst[ch * 4 + v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+          for (int i = 0; i < 16; ++i)
+            pk[16 * cc + i] = pack_bf16(__uint_as_float(ov[2 * i]) * inv_l, __uint_as_float(ov[2 * i + 1]) * inv_l);
         }
+        if (h == 1) {   // all of O_tile has been read: it may be overwritten now
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(c.bar(kBarOEmpty + tile));
+        }
+        store_half_rows(stage, pk, o_row0, valid_rows, h);
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(c.bar(kBarOEmpty + tile));
       if (live) p.lse[row_id] = (m_used + log2f(l)) * 0.69314718055994531f;
     } else {
       // This block holds only some key steps of the group: leave the unnormalised
@@ -794,7 +822,7 @@ __device__ void run_softmax(const Ctl& c, uint32_t tmem, const Params& p, int ti
       before = __shfl_sync(0xffffffffu, before, 0);
       if (static_cast<int>(before) == c_last - c_first) {
         __threadfence();
-        merge_split_row(p, tile, r, c_first, c_last, x0, live ? dst : nullptr, live ? p.lse + row_id : nullptr);
+        merge_split_row(p, tile, r, c_first, c_last, x0, stage, o_row0, valid_rows, live ? p.lse + row_id : nullptr);
       }
     }
     gstep += static_cast<uint32_t>(n);
@@ -859,7 +887,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) run_mma(c, base, tmem, p);
     __syncwarp();
   } else if (warp >= 4) {
-    run_softmax<kPosScale>(c, tmem, p, (warp >> 2) - 1);
+    run_softmax<kPosScale>(c, tmem, smem + kOffStage + (warp - 4) * kStageBytes, p, (warp >> 2) - 1);
   }
 
   tc_fence_before();
