@@ -114,8 +114,9 @@ struct Params {
   int dp_groups;          // groups [0, dp_groups) are processed whole, group g by block g % grid
   long long sk_steps;     // key steps of groups [dp_groups, n_groups), split evenly over the blocks
   float* part;            // partial records, kPartBytesPerBlock per block (split groups only)
-  unsigned int* cnt;      // [n_groups - dp_groups][kQTiles][4] epoch-tagged arrival counters
-  unsigned int epoch;     // 1 .. 2^24-1, differs between consecutive launches sharing a workspace
+  unsigned int* cnt;      // [n_groups - dp_groups][kQTiles][4] arrival counters, zero at launch
+  unsigned int* cnt_next; // the other bank: this launch zeroes it for the next one (or null)
+  int cnt_len;            // counters per bank (the whole allocated bank, not only this launch's)
   float scale_log2;       // scale * log2(e)
   unsigned long long wait_limit;
   int withhold_tile;      // test hook: never load the third K/V item of a block (K of its step 1)
@@ -221,6 +222,11 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
+__device__ __forceinline__ unsigned int ld_acquire(const unsigned int* ptr) {
+  unsigned int v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(ptr) : "memory");
+  return v;
+}
 __device__ __forceinline__ void tc_fence_before() {
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
 }
@@ -599,8 +605,12 @@ __device__ __forceinline__ void store_half_rows(uint8_t* stage, const uint32_t (
 // M = max m_s, w_s = 2^(m_s - M): O = sum w_s O_s / sum w_s (l_s + corr_s) and
 // LSE = (M + log2 sum w_s l_s) * ln 2. Shares are visited in block order, so the
 // result does not depend on which share finished last.
+// When own_tO is non-zero the calling block's own share is still in TMEM (O at own_tO,
+// its max and sums in own_m, own_l, own_corr) and its record is not read.
 __device__ void merge_split_row(const Params& p, int tile, int r, int c_first, int c_last, long long x0,
-                                uint8_t* stage, uint16_t* o_row0, int valid_rows, float* lse_out) {
+                                uint8_t* stage, uint16_t* o_row0, int valid_rows, float* lse_out, uint32_t own_tO,
+                                float own_m, float own_l, float own_corr) {
+  const int self = own_tO != 0 ? static_cast<int>(blockIdx.x) : -1;
   const long long x0_grid = x0 * static_cast<long long>(gridDim.x);
   // share cs's record: its first segment's slot when its share starts inside this group
   // (sk_share_start(cs) >= x0, compared without dividing), else its last segment's
@@ -610,10 +620,13 @@ __device__ void merge_split_row(const Params& p, int tile, int r, int c_first, i
            static_cast<size_t>(tile) * kPartFloatsPerTile;
   };
   constexpr int kM = kD * kBM, kL = kM + kBM, kC = kL + kBM;
-  float M = -INFINITY;
-  for (int cs = c_first; cs <= c_last; ++cs) M = fmaxf(M, __ldcg(record(cs) + kM + r));
-  float L = 0.0f, Lr = 0.0f;
+  float M = self >= 0 ? own_m : -INFINITY;
+  for (int cs = c_first; cs <= c_last; ++cs)
+    if (cs != self) M = fmaxf(M, __ldcg(record(cs) + kM + r));
+  const float w_own = self >= 0 ? ex2(own_m - M) : 0.0f;
+  float L = own_l * w_own, Lr = (own_l + own_corr) * w_own;
   for (int cs = c_first; cs <= c_last; ++cs) {
+    if (cs == self) continue;
     const float* rec = record(cs);
     const float w = ex2(__ldcg(rec + kM + r) - M);
     const float l_s = __ldcg(rec + kL + r);
@@ -628,9 +641,17 @@ __device__ void merge_split_row(const Params& p, int tile, int r, int c_first, i
     for (int cc = 0; cc < 2; ++cc) {
       const int ch = 2 * h + cc;
       float acc[32];
+      if (self >= 0) {   // warp-uniform
+        uint32_t ov[32];
+        tmem_ld32(own_tO + ch * 32, ov);
 #pragma unroll
-      for (int i = 0; i < 32; ++i) acc[i] = 0.0f;
+        for (int i = 0; i < 32; ++i) acc[i] = __uint_as_float(ov[i]) * w_own;
+      } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) acc[i] = 0.0f;
+      }
       for (int cs = c_first; cs <= c_last; ++cs) {
+        if (cs == self) continue;
         const float* rec = record(cs);
         const float w = ex2(__ldcg(rec + kM + r) - M);
         float v[32];
@@ -781,48 +802,53 @@ __device__ void run_softmax(const Ctl& c, uint32_t tmem, uint8_t* stage, const P
       }
       if (live) p.lse[row_id] = (m_used + log2f(l)) * 0.69314718055994531f;
     } else {
-      // This block holds only some key steps of the group: leave the unnormalised
-      // row, its running max and sums in the workspace.
-      float* rec = p.part + (static_cast<size_t>(blockIdx.x) * 2 + sg.which) * kQTiles * kPartFloatsPerTile +
-                   static_cast<size_t>(tile) * kPartFloatsPerTile;
-#pragma unroll 1
-      for (int ch = 0; ch < 4; ++ch) {
-        uint32_t ov[32];
-        tmem_ld32(tO + ch * 32, ov);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) rec[(ch * 32 + i) * kBM + r] = __uint_as_float(ov[i]);   // one line per warp
-      }
-      rec[kD * kBM + r] = m_used;
-      rec[kD * kBM + kBM + r] = l;
-      rec[kD * kBM + 2 * kBM + r] = corr;
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(c.bar(kBarOEmpty + tile));   // O_tile may be overwritten now
-      // Count this warp's 32 rows in; the warp that completes the count merges them.
-      __threadfence();
-      __syncwarp();
+      // This block holds only some key steps of the group. Counters count, per 32 rows,
+      // the shares that have left their record; the last share to finish merges.
       const long long g_rel = sg.group - p.dp_groups;
       const long long x0 = g_rel * p.n_kv;
       const int grid = static_cast<int>(gridDim.x);
       const int c_first = sk_block_of(x0, p.sk_steps, grid);
       const int c_last = sk_block_of(x0 + p.n_kv - 1, p.sk_steps, grid);
-      unsigned int before = 0;
-      if (lane == 0) {
-        // counter = epoch << 8 | arrivals; a value from another launch counts as zero
-        unsigned int* ctr = p.cnt + (g_rel * kQTiles + tile) * 4 + quarter;
-        unsigned int old = atomicAdd(ctr, 0u);
-        for (;;) {
-          const unsigned int mine = (old >> 8) == p.epoch ? old + 1u : (p.epoch << 8) | 1u;
-          const unsigned int prev = atomicCAS(ctr, old, mine);
-          if (prev == old) break;
-          old = prev;   // another share of this group counted in meanwhile
-        }
-        before = (old >> 8) == p.epoch ? (old & 0xFFu) : 0u;
-      }
-      before = __shfl_sync(0xffffffffu, before, 0);
-      if (static_cast<int>(before) == c_last - c_first) {
+      unsigned int* ctr = p.cnt + (g_rel * kQTiles + tile) * 4 + quarter;
+      unsigned int arrived = 0;
+      if (lane == 0) arrived = ld_acquire(ctr);
+      __syncwarp();
+      arrived = __shfl_sync(0xffffffffu, arrived, 0);
+      if (static_cast<int>(arrived) == c_last - c_first) {
+        // Every other share has left its record: merge with this share's O straight
+        // from TMEM, without writing a record of its own.
         __threadfence();
-        merge_split_row(p, tile, r, c_first, c_last, x0, stage, o_row0, valid_rows, live ? p.lse + row_id : nullptr);
+        merge_split_row(p, tile, r, c_first, c_last, x0, stage, o_row0, valid_rows, live ? p.lse + row_id : nullptr,
+                        tO, m_used, l, corr);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(c.bar(kBarOEmpty + tile));
+      } else {
+        float* rec = p.part + (static_cast<size_t>(blockIdx.x) * 2 + sg.which) * kQTiles * kPartFloatsPerTile +
+                     static_cast<size_t>(tile) * kPartFloatsPerTile;
+#pragma unroll 1
+        for (int ch = 0; ch < 4; ++ch) {
+          uint32_t ov[32];
+          tmem_ld32(tO + ch * 32, ov);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) rec[(ch * 32 + i) * kBM + r] = __uint_as_float(ov[i]);   // one line per warp
+        }
+        rec[kD * kBM + r] = m_used;
+        rec[kD * kBM + kBM + r] = l;
+        rec[kD * kBM + 2 * kBM + r] = corr;
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(c.bar(kBarOEmpty + tile));   // O_tile may be overwritten now
+        __threadfence();
+        __syncwarp();
+        unsigned int before = 0;
+        if (lane == 0) before = atomicAdd(ctr, 1u);
+        before = __shfl_sync(0xffffffffu, before, 0);
+        if (static_cast<int>(before) == c_last - c_first) {
+          __threadfence();
+          merge_split_row(p, tile, r, c_first, c_last, x0, stage, o_row0, valid_rows,
+                          live ? p.lse + row_id : nullptr, 0u, 0.0f, 0.0f, 0.0f);
+        }
       }
     }
     gstep += static_cast<uint32_t>(n);
@@ -850,6 +876,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   c.abort = reinterpret_cast<volatile uint32_t*>(smem + kOffAbort);
   c.limit = p.wait_limit;
 
+  // Counters of the next launch that shares this workspace: zero this block's slice now,
+  // before any wait, so that it happens even if this launch gives up later.
+  if (p.cnt_next != nullptr) {
+    const int lo = static_cast<int>(static_cast<long long>(blockIdx.x) * p.cnt_len / gridDim.x);
+    const int hi = static_cast<int>((static_cast<long long>(blockIdx.x) + 1) * p.cnt_len / gridDim.x);
+    for (int i = lo + static_cast<int>(threadIdx.x); i < hi; i += kThreads) p.cnt_next[i] = 0u;
+  }
   if (threadIdx.x == 0) {
     mbar_init(c.bar(kBarQFull), 1);
     mbar_init(c.bar(kBarQEmpty), 1);
@@ -984,16 +1017,16 @@ Plan make_plan(long long n_groups, int n_kv, int sms) {
 // streams never share one; calls on one stream are ordered by the stream.
 struct Workspace {
   float* part = nullptr;
-  unsigned int* cnt = nullptr;
-  size_t part_bytes = 0, cnt_bytes = 0;
-  unsigned int epoch = 0;
+  unsigned int* cnt = nullptr;   // two banks of counters
+  size_t part_bytes = 0, cnt_bytes = 0;   // cnt_bytes: one bank
+  int bank = 0;                  // the bank the next launch uses; it is all zero
 };
 std::mutex g_ws_mu;
 std::map<std::pair<int, uintptr_t>, Workspace> g_ws;
 
-// Returns ATTN_OK and fills part/cnt/epoch, or ATTN_ERR_CUDA.
+// Returns ATTN_OK and fills part and the two counter banks (current, next), or ATTN_ERR_CUDA.
 int get_workspace(int dev, cudaStream_t stream, size_t part_bytes, size_t cnt_bytes, float** part,
-                  unsigned int** cnt, unsigned int* epoch) {
+                  unsigned int** cnt, unsigned int** cnt_next, int* bank_len) {
   std::lock_guard<std::mutex> lock(g_ws_mu);
   Workspace& ws = g_ws[std::make_pair(dev, reinterpret_cast<uintptr_t>(stream))];
   if (ws.part_bytes < part_bytes) {
@@ -1007,15 +1040,17 @@ int get_workspace(int dev, cudaStream_t stream, size_t part_bytes, size_t cnt_by
     if (ws.cnt) cudaFreeAsync(ws.cnt, stream);
     ws.cnt = nullptr;
     ws.cnt_bytes = 0;
-    if (cudaMallocAsync(reinterpret_cast<void**>(&ws.cnt), cnt_bytes, stream) != cudaSuccess) return ATTN_ERR_CUDA;
-    // counters start at epoch 0, which no launch uses
-    if (cudaMemsetAsync(ws.cnt, 0, cnt_bytes, stream) != cudaSuccess) return ATTN_ERR_CUDA;
+    if (cudaMallocAsync(reinterpret_cast<void**>(&ws.cnt), 2 * cnt_bytes, stream) != cudaSuccess) return ATTN_ERR_CUDA;
+    if (cudaMemsetAsync(ws.cnt, 0, 2 * cnt_bytes, stream) != cudaSuccess) return ATTN_ERR_CUDA;
     ws.cnt_bytes = cnt_bytes;
+    ws.bank = 0;
   }
-  ws.epoch = ws.epoch % 0xFFFFFFu + 1u;   // 1 .. 2^24 - 1
+  const size_t bank_words = ws.cnt_bytes / sizeof(unsigned int);
   *part = ws.part;
-  *cnt = ws.cnt;
-  *epoch = ws.epoch;
+  *cnt = ws.cnt + ws.bank * bank_words;
+  *cnt_next = ws.cnt + (ws.bank ^ 1) * bank_words;
+  *bank_len = static_cast<int>(bank_words);
+  ws.bank ^= 1;
   return ATTN_OK;
 }
 
@@ -1082,7 +1117,8 @@ extern "C" int attn_fwd(const void* q, const void* k, const void* v, void* o, fl
   p.sk_steps = pl.sk_steps;
   p.part = nullptr;
   p.cnt = nullptr;
-  p.epoch = 0;
+  p.cnt_next = nullptr;
+  p.cnt_len = 0;
   p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
   p.wait_limit = g_wait_limit.load(std::memory_order_relaxed);
   p.withhold_tile = g_withhold.load(std::memory_order_relaxed);
@@ -1091,7 +1127,8 @@ extern "C" int attn_fwd(const void* q, const void* k, const void* v, void* o, fl
   if (pl.has_split) {
     const size_t part_bytes = static_cast<size_t>(pl.grid) * kPartBytesPerBlock;
     const size_t cnt_bytes = static_cast<size_t>(pl.sk_groups) * kQTiles * 4 * sizeof(unsigned int);
-    const int rc = get_workspace(dev, s, part_bytes, cnt_bytes, &p.part, &p.cnt, &p.epoch);
+    // a later launch may use more counters than this one: it zeroes the whole other bank
+    const int rc = get_workspace(dev, s, part_bytes, cnt_bytes, &p.part, &p.cnt, &p.cnt_next, &p.cnt_len);
     if (rc != ATTN_OK) return rc;
   }
   return scale > 0.0f ? launch<true>(mq, mk, mv, p, pl.grid, dev, s) : launch<false>(mq, mk, mv, p, pl.grid, dev, s);
@@ -1204,7 +1241,8 @@ extern "C" int attn_fwd_noalloc(const void* q, const void* k, const void* v, voi
   p.sk_steps = pl.sk_steps;
   p.part = nullptr;
   p.cnt = nullptr;
-  p.epoch = 1;
+  p.cnt_next = nullptr;   // the counters are cleared on the stream before each launch
+  p.cnt_len = 0;
   p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
   p.wait_limit = g_wait_limit.load(std::memory_order_relaxed);
   p.withhold_tile = g_withhold.load(std::memory_order_relaxed);

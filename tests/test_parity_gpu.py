@@ -124,3 +124,11 @@ def test_launch_counter_counts_launches(gpu_lib):
     q, k, v = make_qkv(1, 1, 128, 128, seed=10)
     run_gpu(gpu_lib, q, k, v, SCALE)
     assert gpu_lib.attn_fwd_kernel_count() == before + 1
+
+
+def test_split_workspace_reuse_across_shapes(gpu_lib):
+    # Launches on one stream share a workspace; a launch with few split groups followed
+    # by one with many must not see arrival counts left over from earlier launches.
+    for B, H, Nq, Nk in [(1, 1, 256, 5120), (1, 2, 300, 3000), (1, 1, 256, 5120), (1, 8, 1024, 4096),
+                         (1, 2, 300, 3000)]:
+        check_case(gpu_lib, B, H, Nq, Nk, seed=Nq + Nk)
