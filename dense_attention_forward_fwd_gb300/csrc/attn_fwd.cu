@@ -67,6 +67,14 @@ constexpr int kSlots = 4;                      // K/V ring depth, one 128x128 ti
 constexpr int kTileBytes = kBM * kD * 2;       // 32 KB of BF16
 constexpr int kBoxBytes = kTileBytes / 2;      // one TMA box: 64 columns (128 B) x 128 rows
 constexpr int kThreads = 384;
+// Register split between the warpgroups. setmaxnreg.inc draws only on registers that
+// the block holds: 128 * kRegsCtl + 256 * kRegsSoftmax must equal 384 * kRegsLaunch,
+// the per-thread count the kernel is compiled to (checked on the host before the first
+// launch), or the increase would wait forever.
+constexpr int kRegsLaunch = 168;
+constexpr int kRegsCtl = 120;
+constexpr int kRegsSoftmax = 192;
+static_assert(128 * kRegsCtl + 256 * kRegsSoftmax == kThreads * kRegsLaunch, "register split must balance");
 constexpr int kTmemCols = 512;
 constexpr float kRescaleLog2 = 8.0f;
 constexpr unsigned long long kDefaultWaitLimit = 1ull << 31;
@@ -913,13 +921,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + kOffTmemSlot);
 
-  if (warp == 0) {
-    if (lane == 0) run_producer(c, base, &tmQ, &tmK, &tmV, p);
-    __syncwarp();
-  } else if (warp == 1) {
-    if (lane == 0) run_mma(c, base, tmem, p);
-    __syncwarp();
-  } else if (warp >= 4) {
+  // Whole warpgroups: warps 0-3 give registers back, warps 4-11 take them.
+  if (warp < 4) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsCtl));
+    if (warp == 0) {
+      if (lane == 0) run_producer(c, base, &tmQ, &tmK, &tmV, p);
+      __syncwarp();
+    } else if (warp == 1) {
+      if (lane == 0) run_mma(c, base, tmem, p);
+      __syncwarp();
+    }
+  } else {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsSoftmax));
     run_softmax<kPosScale>(c, tmem, smem + kOffStage + (warp - 4) * kStageBytes, p, (warp >> 2) - 1);
   }
 
@@ -1059,6 +1072,10 @@ int launch(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, 
            int dev, cudaStream_t stream) {
   auto kern = attn_fwd_kernel<kPos>;
   if (dev < 0 || dev >= kMaxDevices || !g_attr_done[kPos][dev].load(std::memory_order_acquire)) {
+    // The in-kernel register split (setmaxnreg) balances only at kRegsLaunch registers
+    // per thread; at any other count the increase would never be granted. Refuse.
+    cudaFuncAttributes fa;
+    if (cudaFuncGetAttributes(&fa, kern) != cudaSuccess || fa.numRegs != kRegsLaunch) return ATTN_ERR_CUDA;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) != cudaSuccess)
       return ATTN_ERR_CUDA;
     if (dev >= 0 && dev < kMaxDevices) g_attr_done[kPos][dev].store(1, std::memory_order_release);
