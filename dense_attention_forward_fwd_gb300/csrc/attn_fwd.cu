@@ -64,6 +64,7 @@ constexpr int kBM = 128;                       // query rows per Q tile (= TMEM 
 constexpr int kBN = 128;                       // keys per K/V tile
 constexpr int kQTiles = 2;                     // Q tiles per block
 constexpr int kSlots = 4;                      // K/V ring depth, one 128x128 tile per slot
+constexpr int kPairs = kSlots / 2;             // the ring hands over units of two slots
 constexpr int kTileBytes = kBM * kD * 2;       // 32 KB of BF16
 constexpr int kBoxBytes = kTileBytes / 2;      // one TMA box: 64 columns (128 B) x 128 rows
 constexpr int kThreads = 384;
@@ -85,9 +86,9 @@ constexpr int kOffKV = kOffQ + kQTiles * kTileBytes;
 constexpr int kOffBar = kOffKV + kSlots * kTileBytes;
 constexpr int kBarQFull = 0;
 constexpr int kBarQEmpty = 1;                      // the Q tiles may be overwritten
-constexpr int kBarKVFull = 2;
-constexpr int kBarKVEmpty = kBarKVFull + kSlots;
-constexpr int kBarSFull = kBarKVEmpty + kSlots;
+constexpr int kBarKVFull = 2;                      // [pair]
+constexpr int kBarKVEmpty = kBarKVFull + kPairs;   // [pair]
+constexpr int kBarSFull = kBarKVEmpty + kPairs;
 constexpr int kBarPFull = kBarSFull + kQTiles;     // [tile][half]: one barrier per 64-key half of P
 constexpr int kBarOFull = kBarPFull + 2 * kQTiles;
 constexpr int kBarOEmpty = kBarOFull + kQTiles;    // the epilogue has read O_i out of TMEM
@@ -127,7 +128,7 @@ struct Params {
   int cnt_len;            // counters per bank (the whole allocated bank, not only this launch's)
   float scale_log2;       // scale * log2(e)
   unsigned long long wait_limit;
-  int withhold_tile;      // test hook: never load the third K/V item of a block (K of its step 1)
+  int withhold_tile;      // test hook: never load the second K/V unit of a block (V of step 0, K of step 1)
 };
 
 // First key step (counted over the split region) of block c's share.
@@ -423,12 +424,12 @@ __device__ void run_producer(const Ctl& c, uint32_t base, const CUtensorMap* tmQ
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tmK)) : "memory");
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tmV)) : "memory");
 
-  int last_item[kSlots];
+  int last_unit[kPairs];
 #pragma unroll
-  for (int s = 0; s < kSlots; ++s) last_item[s] = -1;
+  for (int q = 0; q < kPairs; ++q) last_unit[q] = -1;
 
-  int it = 0;   // K/V items (K_j, V_j of every step of every segment) issued or skipped
-  int u = 0;    // segments whose Q load was issued
+  int unit = 0;   // K/V units of every segment issued or skipped
+  int u = 0;      // segments whose Q load was issued
   bool ok = true;
   SegIter si(p);
   Segment sg;
@@ -443,29 +444,38 @@ __device__ void run_producer(const Ctl& c, uint32_t base, const CUtensorMap* tmQ
         tma_load_3d(base + kOffQ + i * kTileBytes + h * kBoxBytes, tmQ, c.bar(kBarQFull), h * 64,
                     q_row0 + i * kBM, bh);
     ++u;
-    for (int kv = sg.kv0; ok && kv < sg.kv1; ++kv) {
-      for (int kind = 0; kind < 2; ++kind, ++it) {   // K, then V
-        const int slot = it % kSlots;
-        const int use = it / kSlots;
-        if (use > 0 && !wait_phase(c, kBarKVEmpty + slot, (use - 1) & 1, true)) {
-          ok = false;
-          break;
-        }
-        if (p.withhold_tile && it == 2) continue;
-        const uint32_t fb = c.bar(kBarKVFull + slot);
-        mbar_arrive_expect_tx(fb, kTileBytes);
-        const CUtensorMap* m = kind ? tmV : tmK;
-        for (int h = 0; h < 2; ++h)
-          tma_load_3d(base + kOffKV + slot * kTileBytes + h * kBoxBytes, m, fb, h * 64, kv * kBN, bh);
-        last_item[slot] = it;
+    // A segment of n steps streams n + 1 units: {K_0}, {V_0, K_1}, ..., {V_{n-2}, K_{n-1}},
+    // {V_{n-1}}. Unit i is what the MMA thread consumes in one step (V for the P V
+    // products, K for the next S), so it waits once per step. Units alternate between
+    // the two slot pairs; the first tile of a unit takes the pair's first slot.
+    const int n = sg.kv1 - sg.kv0;
+    for (int i = 0; ok && i <= n; ++i, ++unit) {
+      const int pr = unit % kPairs, use = unit / kPairs;
+      if (use > 0 && !wait_phase(c, kBarKVEmpty + pr, (use - 1) & 1, true)) {
+        ok = false;
+        break;
       }
+      if (p.withhold_tile && unit == 1) continue;
+      const bool has_v = i > 0, has_k = i < n;
+      const uint32_t fb = c.bar(kBarKVFull + pr);
+      mbar_arrive_expect_tx(fb, (has_v && has_k ? 2 : 1) * kTileBytes);
+      uint32_t dst = base + kOffKV + 2 * pr * kTileBytes;
+      if (has_v) {
+        for (int h = 0; h < 2; ++h)
+          tma_load_3d(dst + h * kBoxBytes, tmV, fb, h * 64, (sg.kv0 + i - 1) * kBN, bh);
+        dst += kTileBytes;
+      }
+      if (has_k) {
+        for (int h = 0; h < 2; ++h) tma_load_3d(dst + h * kBoxBytes, tmK, fb, h * 64, (sg.kv0 + i) * kBN, bh);
+      }
+      last_unit[pr] = unit;
     }
   }
   // Leave no copy in flight into shared memory that the block is about to release
   // (on the normal path these phases have completed or are about to).
   if (u > 0) wait_phase(c, kBarQFull, (u - 1) & 1, false);
-  for (int s = 0; s < kSlots; ++s)
-    if (last_item[s] >= 0) wait_phase(c, kBarKVFull + s, (last_item[s] / kSlots) & 1, false);
+  for (int q = 0; q < kPairs; ++q)
+    if (last_unit[q] >= 0) wait_phase(c, kBarKVFull + q, (last_unit[q] / kPairs) & 1, false);
 }
 
 __device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint32_t q_smem, uint32_t k_smem) {
@@ -494,16 +504,19 @@ __device__ __forceinline__ void issue_pv_half(uint32_t d_tmem, uint32_t p_tmem, 
 
 // One K/V step of the MMA issuer: O_i += P_i V_j for both Q tiles and, when another
 // step follows (kMore), S_i = Q_i K_{j+1}^T; otherwise the commits that hand O to the
-// epilogue. Returns false when a wait gave up.
+// epilogue. `unit` is the step's K/V unit ({V_j, K_{j+1}}, or {V_j} on the last step).
+// Every operation of this thread that is not an MMA leaves the tensor core idle for
+// about a hundred cycles (its queue is shallow), so a step does one ring wait, the
+// four P waits and two commits; the ring slots are released by a softmax warp.
+// Returns false when a wait gave up.
 template <bool kMore>
 __device__ __forceinline__ bool mma_step(const Ctl& c, uint32_t base, const uint32_t (&tS)[2],
-                                         const uint32_t (&tO)[2], const uint32_t (&sQ)[2], int itV,
+                                         const uint32_t (&tO)[2], const uint32_t (&sQ)[2], int unit,
                                          uint32_t ph, bool first) {
-  const int slotV = itV % kSlots;
-  const int itK = itV + 1, slotK = itK % kSlots;
-  const uint32_t sV = base + kOffKV + slotV * kTileBytes;
-  const uint32_t sK = base + kOffKV + slotK * kTileBytes;
-  if (!wait_phase(c, kBarKVFull + slotV, (itV / kSlots) & 1, true)) return false;
+  const int pr = unit % kPairs;
+  const uint32_t sV = base + kOffKV + 2 * pr * kTileBytes;
+  const uint32_t sK = sV + kTileBytes;
+  if (!wait_phase(c, kBarKVFull + pr, (unit / kPairs) & 1, true)) return false;
   // tile 0: O0 += P0 V_j, then S0 = Q0 K_{j+1}^T
   if (!wait_phase(c, kBarPFull + 0, ph, true)) return false;
   tc_fence_after();
@@ -512,8 +525,6 @@ __device__ __forceinline__ bool mma_step(const Ctl& c, uint32_t base, const uint
   tc_fence_after();
   issue_pv_half(tO[0], tS[0], sV, 1, true);
   if (kMore) {
-    if (!wait_phase(c, kBarKVFull + slotK, (itK / kSlots) & 1, true)) return false;
-    tc_fence_after();
     issue_qk(tS[0], sQ[0], sK);
     tc_commit(c.bar(kBarSFull + 0));
   } else {
@@ -526,11 +537,9 @@ __device__ __forceinline__ bool mma_step(const Ctl& c, uint32_t base, const uint
   if (!wait_phase(c, kBarPFull + 3, ph, true)) return false;
   tc_fence_after();
   issue_pv_half(tO[1], tS[1], sV, 1, true);
-  tc_commit(c.bar(kBarKVEmpty + slotV));
   if (kMore) {
     issue_qk(tS[1], sQ[1], sK);
     tc_commit(c.bar(kBarSFull + 1));
-    tc_commit(c.bar(kBarKVEmpty + slotK));
   } else {
     tc_commit(c.bar(kBarOFull + 1));
   }
@@ -541,24 +550,22 @@ __device__ void run_mma(const Ctl& c, uint32_t base, uint32_t tmem, const Params
   const uint32_t tS[2] = {tmem, tmem + 128};
   const uint32_t tO[2] = {tmem + 256, tmem + 384};
   const uint32_t sQ[2] = {base + kOffQ, base + kOffQ + kTileBytes};
-  int it = 0;           // K/V items consumed
+  int unit = 0;         // K/V units consumed
   uint32_t gstep = 0;   // K/V steps of all previous segments: phase of s_full / p_full
   int u = 0;            // segments started
   SegIter si(p);
   Segment sg;
   while (si.next(sg)) {
     const int n = sg.kv1 - sg.kv0;
-    const int slotK = it % kSlots;
     if (!wait_phase(c, kBarQFull, u & 1, true) ||
-        !wait_phase(c, kBarKVFull + slotK, (it / kSlots) & 1, true))
+        !wait_phase(c, kBarKVFull + unit % kPairs, (unit / kPairs) & 1, true))
       break;
     tc_fence_after();
-    const uint32_t sK = base + kOffKV + slotK * kTileBytes;
+    const uint32_t sK = base + kOffKV + 2 * (unit % kPairs) * kTileBytes;   // unit {K_0}
     issue_qk(tS[0], sQ[0], sK);
     tc_commit(c.bar(kBarSFull + 0));
     issue_qk(tS[1], sQ[1], sK);
     tc_commit(c.bar(kBarSFull + 1));
-    tc_commit(c.bar(kBarKVEmpty + slotK));
     if (n == 1) tc_commit(c.bar(kBarQEmpty));   // the segment's last S MMA is issued
     // The segment's first P V products overwrite O: the previous segment's epilogue must
     // have read both accumulators out of TMEM.
@@ -568,15 +575,15 @@ __device__ void run_mma(const Ctl& c, uint32_t base, uint32_t tmem, const Params
     bool ok = true;
     int j = 0;
     for (; j + 1 < n; ++j) {
-      if (!mma_step<true>(c, base, tS, tO, sQ, it + 2 * j + 1, (gstep + j) & 1u, j == 0)) {
+      if (!mma_step<true>(c, base, tS, tO, sQ, unit + 1 + j, (gstep + j) & 1u, j == 0)) {
         ok = false;
         break;
       }
     }
     if (!ok) break;
     if (n > 1) tc_commit(c.bar(kBarQEmpty));   // the last S MMA (step n-2) is issued
-    if (!mma_step<false>(c, base, tS, tO, sQ, it + 2 * j + 1, (gstep + j) & 1u, j == 0)) break;
-    it += 2 * n;
+    if (!mma_step<false>(c, base, tS, tO, sQ, unit + 1 + j, (gstep + j) & 1u, j == 0)) break;
+    unit += n + 1;
     gstep += static_cast<uint32_t>(n);
     ++u;
   }
@@ -688,6 +695,11 @@ __device__ void run_softmax(const Ctl& c, uint32_t tmem, uint8_t* stage, const P
 
   uint32_t gstep = 0;   // K/V steps of all previous segments: phase of s_full / p_full
   int u = 0;            // segments finished
+  int unit = 0;         // K/V units of all previous segments
+  // One thread of tile 1 releases the K/V ring: once S_1 of step j is complete, every MMA
+  // issued before it (all readers of unit j: S_0 and S_1 of step j, the P V products of
+  // step j - 1) has finished, and once O_1 is complete the segment's last unit is free.
+  const bool releaser = tile == 1 && quarter == 0 && lane == 0;
   SegIter si(p);
   Segment sg;
   while (si.next(sg)) {
@@ -697,6 +709,7 @@ __device__ void run_softmax(const Ctl& c, uint32_t tmem, uint8_t* stage, const P
     float corr = 0.0f;          // BF16 rounding error of the largest term of each tile
     for (int j = 0; j < n; ++j) {
       if (!wait_warp(c, kBarSFull + tile, (gstep + static_cast<uint32_t>(j)) & 1u)) return;
+      if (releaser) mbar_arrive(c.bar(kBarKVEmpty + (unit + j) % kPairs));
       tc_fence_after();
       uint32_t x[128];
       tmem_ld128(tS, x);
@@ -780,6 +793,8 @@ __device__ void run_softmax(const Ctl& c, uint32_t tmem, uint8_t* stage, const P
     }
 
     if (!wait_warp(c, kBarOFull + tile, u & 1)) return;
+    if (releaser) mbar_arrive(c.bar(kBarKVEmpty + (unit + n) % kPairs));
+    unit += n + 1;
     tc_fence_after();
     const int bh = sg.group / p.q_groups;
     const int qrow_w0 = (sg.group % p.q_groups) * (kQTiles * kBM) + tile * kBM + quarter * 32;   // warp's first row
@@ -894,9 +909,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     mbar_init(c.bar(kBarQFull), 1);
     mbar_init(c.bar(kBarQEmpty), 1);
-    for (int s = 0; s < kSlots; ++s) {
-      mbar_init(c.bar(kBarKVFull + s), 1);
-      mbar_init(c.bar(kBarKVEmpty + s), 1);
+    for (int q = 0; q < kPairs; ++q) {
+      mbar_init(c.bar(kBarKVFull + q), 1);
+      mbar_init(c.bar(kBarKVEmpty + q), 1);   // released by one softmax thread of tile 1
     }
     for (int t = 0; t < kQTiles; ++t) {
       mbar_init(c.bar(kBarSFull + t), 1);
