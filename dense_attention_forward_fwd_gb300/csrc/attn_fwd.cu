@@ -649,35 +649,37 @@ __device__ void merge_split_row(const Params& p, int tile, int r, int c_first, i
     Lr += (l_s + __ldcg(rec + kC + r)) * w;
   }
   const float inv = 1.0f / Lr;
+  // Two 64-column halves; per half and share, the share's max and its 64 values are
+  // requested together, so each share costs one round trip to L2 per half.
 #pragma unroll 1
   for (int h = 0; h < 2; ++h) {
+    float acc[64];
+    if (self >= 0) {   // warp-uniform
+#pragma unroll
+      for (int cc = 0; cc < 2; ++cc) {
+        uint32_t ov[32];
+        tmem_ld32(own_tO + (2 * h + cc) * 32, ov);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) acc[32 * cc + i] = __uint_as_float(ov[i]) * w_own;
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < 64; ++i) acc[i] = 0.0f;
+    }
+    for (int cs = c_first; cs <= c_last; ++cs) {
+      if (cs == self) continue;
+      const float* rec = record(cs);
+      const float m_s = __ldcg(rec + kM + r);
+      float v[64];
+#pragma unroll
+      for (int i = 0; i < 64; ++i) v[i] = __ldcg(rec + (h * 64 + i) * kBM + r);
+      const float w = ex2(m_s - M);
+#pragma unroll
+      for (int i = 0; i < 64; ++i) acc[i] = fmaf(v[i], w, acc[i]);
+    }
     uint32_t pk[32];
 #pragma unroll
-    for (int cc = 0; cc < 2; ++cc) {
-      const int ch = 2 * h + cc;
-      float acc[32];
-      if (self >= 0) {   // warp-uniform
-        uint32_t ov[32];
-        tmem_ld32(own_tO + ch * 32, ov);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) acc[i] = __uint_as_float(ov[i]) * w_own;
-      } else {
-#pragma unroll
-        for (int i = 0; i < 32; ++i) acc[i] = 0.0f;
-      }
-      for (int cs = c_first; cs <= c_last; ++cs) {
-        if (cs == self) continue;
-        const float* rec = record(cs);
-        const float w = ex2(__ldcg(rec + kM + r) - M);
-        float v[32];
-#pragma unroll
-        for (int i = 0; i < 32; ++i) v[i] = __ldcg(rec + (ch * 32 + i) * kBM + r);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) acc[i] = fmaf(v[i], w, acc[i]);
-      }
-#pragma unroll
-      for (int i = 0; i < 16; ++i) pk[16 * cc + i] = pack_bf16(acc[2 * i] * inv, acc[2 * i + 1] * inv);
-    }
+    for (int i = 0; i < 32; ++i) pk[i] = pack_bf16(acc[2 * i] * inv, acc[2 * i + 1] * inv);
     store_half_rows(stage, pk, o_row0, valid_rows, h);
   }
   if (lse_out != nullptr) *lse_out = (M + log2f(L)) * 0.69314718055994531f;
@@ -849,12 +851,11 @@ __device__ void run_softmax(const Ctl& c, uint32_t tmem, uint8_t* stage, const P
       } else {
         float* rec = p.part + (static_cast<size_t>(blockIdx.x) * 2 + sg.which) * kQTiles * kPartFloatsPerTile +
                      static_cast<size_t>(tile) * kPartFloatsPerTile;
-#pragma unroll 1
-        for (int ch = 0; ch < 4; ++ch) {
-          uint32_t ov[32];
-          tmem_ld32(tO + ch * 32, ov);
+        {
+          uint32_t ov[128];
+          tmem_ld128(tO, ov);
 #pragma unroll
-          for (int i = 0; i < 32; ++i) rec[(ch * 32 + i) * kBM + r] = __uint_as_float(ov[i]);   // one line per warp
+          for (int i = 0; i < 128; ++i) rec[i * kBM + r] = __uint_as_float(ov[i]);   // one line per warp
         }
         rec[kD * kBM + r] = m_used;
         rec[kD * kBM + kBM + r] = l;
