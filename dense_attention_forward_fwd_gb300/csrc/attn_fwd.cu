@@ -33,7 +33,10 @@
 // end ("normalised once the loop ends, then written", same write-up). The running max
 // only moves when it grows by more than kRescaleLog2 (log2 units): the exponentials
 // are then bounded by 2^kRescaleLog2 and O and l keep sharing one m, so the result is
-// unchanged; skipping the move avoids reading and rewriting O in TMEM.
+// unchanged; skipping the move avoids reading and rewriting O in TMEM. P is BF16 (range
+// to 2^127) and every sum is FP32, so the bound can be generous: at 2^32 the weights
+// keep about 2^90 of headroom below FP32 overflow for any |V| up to 2^20 summed over
+// 2^24 keys, while a row's running max practically never moves after its first tile.
 //
 // Every wait is bounded (clock64 budget). On expiry a block raises a flag in shared
 // memory, the others stop at their next wait, the producer and the MMA thread wait
@@ -77,7 +80,7 @@ constexpr int kRegsCtl = 120;
 constexpr int kRegsSoftmax = 192;
 static_assert(128 * kRegsCtl + 256 * kRegsSoftmax == kThreads * kRegsLaunch, "register split must balance");
 constexpr int kTmemCols = 512;
-constexpr float kRescaleLog2 = 8.0f;
+constexpr float kRescaleLog2 = 32.0f;
 constexpr unsigned long long kDefaultWaitLimit = 1ull << 31;
 
 // shared memory map (byte offsets from a 1024-byte aligned base)
@@ -215,6 +218,19 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
       "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// non-blocking: has the phase with this parity completed?
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
       : "r"(bar), "r"(parity)
@@ -506,8 +522,8 @@ __device__ __forceinline__ void issue_pv_half(uint32_t d_tmem, uint32_t p_tmem, 
 // step follows (kMore), S_i = Q_i K_{j+1}^T; otherwise the commits that hand O to the
 // epilogue. `unit` is the step's K/V unit ({V_j, K_{j+1}}, or {V_j} on the last step).
 // Every operation of this thread that is not an MMA leaves the tensor core idle for
-// about a hundred cycles (its queue is shallow), so a step does one ring wait, the
-// four P waits and two commits; the ring slots are released by a softmax warp.
+// about a hundred cycles (its queue is shallow), so a step does only the four P waits
+// and two commits: softmax threads check and release the ring slots.
 // Returns false when a wait gave up.
 template <bool kMore>
 __device__ __forceinline__ bool mma_step(const Ctl& c, uint32_t base, const uint32_t (&tS)[2],
@@ -516,8 +532,8 @@ __device__ __forceinline__ bool mma_step(const Ctl& c, uint32_t base, const uint
   const int pr = unit % kPairs;
   const uint32_t sV = base + kOffKV + 2 * pr * kTileBytes;
   const uint32_t sK = sV + kTileBytes;
-  if (!wait_phase(c, kBarKVFull + pr, (unit / kPairs) & 1, true)) return false;
-  // tile 0: O0 += P0 V_j, then S0 = Q0 K_{j+1}^T
+  // tile 0: O0 += P0 V_j, then S0 = Q0 K_{j+1}^T. The first half of P0 is handed over only
+  // after a softmax thread has seen the unit loaded, so this wait covers the unit too.
   if (!wait_phase(c, kBarPFull + 0, ph, true)) return false;
   tc_fence_after();
   issue_pv_half(tO[0], tS[0], sV, 0, !first);
@@ -702,6 +718,13 @@ __device__ void run_softmax(const Ctl& c, uint32_t tmem, uint8_t* stage, const P
   // issued before it (all readers of unit j: S_0 and S_1 of step j, the P V products of
   // step j - 1) has finished, and once O_1 is complete the segment's last unit is free.
   const bool releaser = tile == 1 && quarter == 0 && lane == 0;
+  // One thread of tile 0 checks the ring for the MMA thread: before its first P arrival of
+  // step j it has seen unit j + 1 ({V_j, K_j+1}) loaded, so the MMA thread's wait for that
+  // P also covers the unit (the MMA thread's waits are what idle the tensor core). The
+  // check is a non-blocking test issued when the step starts and read before the arrival,
+  // so its latency hides behind the exponentials; a blocking wait follows only if the
+  // unit was not there yet.
+  const bool ringer = tile == 0 && quarter == 0 && lane == 0;
   SegIter si(p);
   Segment sg;
   while (si.next(sg)) {
@@ -712,6 +735,8 @@ __device__ void run_softmax(const Ctl& c, uint32_t tmem, uint8_t* stage, const P
     for (int j = 0; j < n; ++j) {
       if (!wait_warp(c, kBarSFull + tile, (gstep + static_cast<uint32_t>(j)) & 1u)) return;
       if (releaser) mbar_arrive(c.bar(kBarKVEmpty + (unit + j) % kPairs));
+      const int ring_unit = unit + j + 1;
+      const bool ring_seen = ringer && mbar_test_wait(c.bar(kBarKVFull + ring_unit % kPairs), (ring_unit / kPairs) & 1);
       tc_fence_after();
       uint32_t x[128];
       tmem_ld128(tS, x);
@@ -789,8 +814,12 @@ __device__ void run_softmax(const Ctl& c, uint32_t tmem, uint8_t* stage, const P
         tmem_st32(tS + half * 32, pk);
         tc_fence_before();
         __syncwarp();
+        // (on expiry the abort flag is set and the block winds down; arriving is harmless)
+        if (half == 0 && ringer && !ring_seen)
+          wait_phase(c, kBarKVFull + ring_unit % kPairs, (ring_unit / kPairs) & 1, true);
         if (lane == 0) mbar_arrive(c.bar(kBarPFull + 2 * tile + half));
       }
+
       l += ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
     }
 
