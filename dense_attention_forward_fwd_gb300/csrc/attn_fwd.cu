@@ -109,11 +109,13 @@ static_assert(kOffKV % 1024 == 0 && kOffBar % 8 == 0, "swizzle atoms need 1024-b
 static_assert(kSmemBytes <= 232448, "exceeds the 227 KB shared memory of one block");
 
 // Workspace of split groups: per block two partial records (its first and its last
-// split segment), each holding per Q tile the unnormalised O column-major (element
-// (column c, row r) at c * kBM + r, so that a warp's 32 rows of one column are one
-// 128-byte line), then m (log2 units), l and corr, kBM floats each.
+// split segment), each holding per Q tile the unnormalised O in groups of four columns
+// (columns 4g..4g+3 of row r at (g * kBM + r) * 4, so that a warp's 32 rows of one
+// group are 512 contiguous bytes and each thread moves 16-byte vectors), then m (log2
+// units), l and corr, kBM floats each.
 constexpr int kPartFloatsPerTile = kD * kBM + 3 * kBM;
 constexpr size_t kPartBytesPerBlock = size_t(2) * kQTiles * kPartFloatsPerTile * sizeof(float);
+static_assert(kPartFloatsPerTile % 4 == 0, "each tile record must start on a 16-byte boundary");
 constexpr int kMinSegSteps = 8;   // smallest share of a group worth a block of its own
 
 struct Params {
@@ -135,8 +137,18 @@ struct Params {
 };
 
 // First key step (counted over the split region) of block c's share.
+// floor(a / b) for a >= 0, b > 0. On the device a 64-bit division is a long dependent
+// sequence; operands that fit 32 bits (all but enormous problems) take the short one.
+__host__ __device__ __forceinline__ long long div_floor(long long a, long long b) {
+#ifdef __CUDA_ARCH__
+  if (((static_cast<unsigned long long>(a) | static_cast<unsigned long long>(b)) >> 32) == 0)
+    return static_cast<long long>(static_cast<unsigned>(a) / static_cast<unsigned>(b));
+#endif
+  return a / b;
+}
+
 __host__ __device__ __forceinline__ long long sk_share_start(long long c, long long sk_steps, long long grid) {
-  return c * sk_steps / grid;
+  return div_floor(c * sk_steps, grid);
 }
 
 struct Segment {
@@ -171,7 +183,7 @@ struct SegIter {
       return true;
     }
     if (sk_pos < sk_end) {
-      const long long g_rel = sk_pos / n_kv;
+      const long long g_rel = div_floor(sk_pos, n_kv);
       const int kv0 = static_cast<int>(sk_pos - g_rel * n_kv);
       const long long left = sk_end - sk_pos;
       const int kv1 = left < n_kv - kv0 ? kv0 + static_cast<int>(left) : n_kv;
@@ -189,7 +201,7 @@ struct SegIter {
 
 // The block whose share contains split-region key step x (every share is non-empty).
 __device__ __forceinline__ int sk_block_of(long long x, long long sk_steps, int grid) {
-  int c = static_cast<int>(x * grid / sk_steps);
+  int c = static_cast<int>(div_floor(x * grid, sk_steps));
   while (c + 1 < grid && sk_share_start(c + 1, sk_steps, grid) <= x) ++c;
   while (c > 0 && sk_share_start(c, sk_steps, grid) > x) --c;
   return c;
@@ -687,8 +699,15 @@ __device__ void merge_split_row(const Params& p, int tile, int r, int c_first, i
       const float* rec = record(cs);
       const float m_s = __ldcg(rec + kM + r);
       float v[64];
+      const float4* rec4 = reinterpret_cast<const float4*>(rec);
 #pragma unroll
-      for (int i = 0; i < 64; ++i) v[i] = __ldcg(rec + (h * 64 + i) * kBM + r);
+      for (int g = 0; g < 16; ++g) {
+        const float4 t = __ldcg(rec4 + (h * 16 + g) * kBM + r);
+        v[4 * g] = t.x;
+        v[4 * g + 1] = t.y;
+        v[4 * g + 2] = t.z;
+        v[4 * g + 3] = t.w;
+      }
       const float w = ex2(m_s - M);
 #pragma unroll
       for (int i = 0; i < 64; ++i) acc[i] = fmaf(v[i], w, acc[i]);
@@ -883,8 +902,11 @@ __device__ void run_softmax(const Ctl& c, uint32_t tmem, uint8_t* stage, const P
         {
           uint32_t ov[128];
           tmem_ld128(tO, ov);
+          float4* rec4 = reinterpret_cast<float4*>(rec);
 #pragma unroll
-          for (int i = 0; i < 128; ++i) rec[i * kBM + r] = __uint_as_float(ov[i]);   // one line per warp
+          for (int g = 0; g < kD / 4; ++g)   // 512 contiguous bytes per warp
+            rec4[g * kBM + r] = make_float4(__uint_as_float(ov[4 * g]), __uint_as_float(ov[4 * g + 1]),
+                                            __uint_as_float(ov[4 * g + 2]), __uint_as_float(ov[4 * g + 3]));
         }
         rec[kD * kBM + r] = m_used;
         rec[kD * kBM + kBM + r] = l;
