@@ -97,9 +97,16 @@ def test_hot_key_in_last_tile_forces_late_rescale(gpu_lib):
     check_case(gpu_lib, 1, 1, 256, 1024, qkv=(q, k, v), ulp_aware=True)
 
 
-@pytest.mark.parametrize("scale", [0.0, -0.0883883461356163, 0.5, 1e-3])
+@pytest.mark.parametrize("scale", [0.0, -0.0883883461356163, 0.5, 1e-3, 2.0])
 def test_other_scales(gpu_lib, scale):
+    # scale 2: scores with a standard deviation of ~33 in log2 units, so the running max
+    # of most rows moves by more than the rescale threshold after the first tile
     check_case(gpu_lib, 1, 2, 256, 384, seed=8, scale=scale, ulp_aware=True)
+
+
+def test_rescale_on_many_rows_long_sequence(gpu_lib):
+    # scale 2 over 16 key tiles: rescales of O in TMEM at different steps in different rows
+    check_case(gpu_lib, 1, 2, 512, 2048, seed=12, scale=2.0, ulp_aware=True)
 
 
 def test_results_are_deterministic(gpu_lib):
