@@ -9,7 +9,9 @@ Kernel time: CUDA events around each launch on the launching stream, inputs resi
 in HBM, L2 flushed (a 512 MiB write) before every timed launch. value = total
 4*B*H*Nq*Nk*d FLOPs of all ranks / max-over-ranks time. e2e: the same metric through
 the same C-ABI call, with the host->device copy of Q, K, V from pinned memory and the
-device->host copy of O and LSE inside each timed step.
+device->host copy of O and LSE inside each timed step; steps are pipelined over three
+streams (copy in, compute, copy out) with two device buffer sets, so one step's copies
+overlap its neighbours' kernels.
 
 --impl reference times the FP64 CPU oracle (the plain definition) on host cores, on a
 bounded sample of query rows per step.
@@ -278,30 +280,58 @@ def run_ours(args, w):
     if status != attn.ATTN_OK:
         raise RuntimeError(f"kernel status {attn.attn_status_string(status)}")
 
-    # e2e through host buffers: pinned H2D of Q, K, V; attn_fwd; D2H of O and LSE
+    # e2e through host buffers: every step copies its Q, K, V from pinned host memory,
+    # calls attn_fwd and copies O and LSE back, all inside the timed region. Steps are
+    # pipelined over three streams with two device buffer sets, as a serving loop would
+    # run them: the H2D of step i+1 and the D2H of step i-1 overlap the kernel of step i.
     hq, hk, hv = (t.cpu().pin_memory() for t in (q, k, v))
     ho, hl = torch.empty_like(o, device="cpu").pin_memory(), torch.empty_like(lse, device="cpu").pin_memory()
-    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    bufs = [tuple(torch.empty_like(t) for t in (q, k, v, o, lse)) for _ in range(2)]
+    s_in, s_run, s_out = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
+    ev_in = [torch.cuda.Event() for _ in range(2)]
+    ev_done = [torch.cuda.Event() for _ in range(2)]
+    ev_out = [torch.cuda.Event() for _ in range(2)]
+    for e in ev_done + ev_out:
+        e.record(stream)
 
-    def e2e_step():
-        dq.copy_(hq, non_blocking=True)
-        dk.copy_(hk, non_blocking=True)
-        dv.copy_(hv, non_blocking=True)
-        attn.attn_fwd(dq, dk, dv, o, lse, w.B, w.H, w.Nq, w.Nk, w.d, w.scale, stream)
-        ho.copy_(o, non_blocking=True)
-        hl.copy_(lse, non_blocking=True)
+    def e2e_steps(n):
+        for i in range(n):
+            b = i % 2
+            dq, dk, dv, do, dl = bufs[b]
+            s_in.wait_event(ev_done[b])                  # the kernel that read buffer set b is done
+            with torch.cuda.stream(s_in):
+                dq.copy_(hq, non_blocking=True)
+                dk.copy_(hk, non_blocking=True)
+                dv.copy_(hv, non_blocking=True)
+                ev_in[b].record(s_in)
+            s_run.wait_event(ev_in[b])
+            s_run.wait_event(ev_out[b])                  # this output set has been copied out
+            attn.attn_fwd(dq, dk, dv, do, dl, w.B, w.H, w.Nq, w.Nk, w.d, w.scale, s_run)
+            ev_done[b].record(s_run)
+            s_out.wait_event(ev_done[b])
+            with torch.cuda.stream(s_out):
+                ho.copy_(do, non_blocking=True)
+                hl.copy_(dl, non_blocking=True)
+                ev_out[b].record(s_out)
 
-    for _ in range(3):
-        e2e_step()
+    for st in (s_in, s_run, s_out):
+        st.wait_stream(stream)
+    e2e_steps(3)
     torch.cuda.synchronize()
     es, ee = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier()
     es.record(stream)
-    for _ in range(args.e2e_steps):
-        e2e_step()
+    for st in (s_in, s_run, s_out):
+        st.wait_stream(stream)
+    e2e_steps(args.e2e_steps)
+    for st in (s_in, s_run, s_out):
+        stream.wait_stream(st)
     ee.record(stream)
     torch.cuda.synchronize()
     e2e_ms = es.elapsed_time(ee) / args.e2e_steps
+    # the last step's result, read back to the host, must be the device-timed leg's result
+    if not (torch.equal(ho, o.cpu()) and torch.equal(hl, lse.cpu())):
+        raise RuntimeError("end-to-end output differs from the device-resident run")
     h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv))
     d2h = ho.numel() * ho.element_size() + hl.numel() * hl.element_size()
 
