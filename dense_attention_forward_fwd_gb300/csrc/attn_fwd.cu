@@ -8,13 +8,19 @@
 // CUDA C++", v1).
 //
 // Blackwell mapping (one persistent block per SM, 12 warps):
-//   warp 0        TMA producer: the two Q tiles of each work segment, then K_j, V_j
-//                 into a ring of 128B-swizzled shared-memory slots (full/empty mbarriers).
+//   warp 0        TMA producer: the two Q tiles of each work segment, then per step the
+//                 K/V unit {V_j, K_j+1} into one of two pairs of 128B-swizzled
+//                 shared-memory slots (one full and one empty mbarrier per pair).
 //   warp 1        MMA issuer (one thread): tcgen05.mma S_i = Q_i K_j^T into TMEM, and
-//                 O_i += P_i V_j with P_i read from TMEM; owns the TMEM allocation.
+//                 O_i += P_i V_j with P_i read from TMEM; owns the TMEM allocation. Its
+//                 queue is shallow, so anything else it does idles the tensor core: it
+//                 only waits for P and commits S, and softmax threads look after the ring
+//                 (one thread of tile 0 checks each unit before handing over P, one of
+//                 tile 1 releases it once S_1 of its step is complete).
 //   warps 4-7     softmax + epilogue for Q tile 0 (thread = query row = TMEM lane).
 //   warps 8-11    softmax + epilogue for Q tile 1.
 //   warps 2-3     idle.
+// setmaxnreg gives warps 0-3 120 registers per thread and the softmax warps 192.
 // Two Q tiles per block let one tile's softmax run while the tensor core works on
 // the other tile's two GEMMs (the two-query-tile schedule that the FlashAttention-4
 // summary in "Hacker News Digest" describes). TMEM holds S0, S1, O0, O1 (4 x 128
@@ -34,9 +40,9 @@
 // only moves when it grows by more than kRescaleLog2 (log2 units): the exponentials
 // are then bounded by 2^kRescaleLog2 and O and l keep sharing one m, so the result is
 // unchanged; skipping the move avoids reading and rewriting O in TMEM. P is BF16 (range
-// to 2^127) and every sum is FP32, so the bound can be generous: at 2^32 the weights
-// keep about 2^90 of headroom below FP32 overflow for any |V| up to 2^20 summed over
-// 2^24 keys, while a row's running max practically never moves after its first tile.
+// to 2^127) and every sum is FP32, so the bound can be generous: with weights up to 2^32,
+// |V| up to 2^20 and 2^24 keys the accumulators stay below 2^76, far from FP32's 2^128,
+// while a row's running max practically never moves after its first tile.
 //
 // Every wait is bounded (clock64 budget). On expiry a block raises a flag in shared
 // memory, the others stop at their next wait, the producer and the MMA thread wait
