@@ -762,6 +762,7 @@ __device__ void run_softmax(const Ctl& c, uint32_t tmem, uint8_t* stage, const P
       if (releaser) mbar_arrive(c.bar(kBarKVEmpty + (unit + j) % kPairs));
       const int ring_unit = unit + j + 1;
       const bool ring_seen = ringer && mbar_test_wait(c.bar(kBarKVFull + ring_unit % kPairs), (ring_unit / kPairs) & 1);
+      __syncwarp();   // lane 0 alone may have run the two lines above; tcgen05.ld is .sync.aligned
       tc_fence_after();
       uint32_t x[128];
       tmem_ld128(tS, x);
@@ -843,6 +844,7 @@ __device__ void run_softmax(const Ctl& c, uint32_t tmem, uint8_t* stage, const P
         if (half == 0 && ringer && !ring_seen)
           wait_phase(c, kBarKVFull + ring_unit % kPairs, (ring_unit / kPairs) & 1, true);
         if (lane == 0) mbar_arrive(c.bar(kBarPFull + 2 * tile + half));
+        __syncwarp();   // reconverge before the next .sync.aligned TMEM access
       }
 
       l += ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
@@ -850,6 +852,7 @@ __device__ void run_softmax(const Ctl& c, uint32_t tmem, uint8_t* stage, const P
 
     if (!wait_warp(c, kBarOFull + tile, u & 1)) return;
     if (releaser) mbar_arrive(c.bar(kBarKVEmpty + (unit + n) % kPairs));
+    __syncwarp();
     unit += n + 1;
     tc_fence_after();
     const int bh = sg.group / p.q_groups;
