@@ -864,22 +864,20 @@ __device__ void run_softmax(const Ctl& c, uint32_t tmem, uint8_t* stage, const P
     uint16_t* o_row0 = p.o + (static_cast<size_t>(bh) * static_cast<size_t>(p.Nq) + static_cast<size_t>(qrow_w0)) * kD;
     if (!sg.split) {
       const float inv_l = 1.0f / (l + corr);
-#pragma unroll 1
+      // O in one TMEM load; the accumulator is handed back to the MMA thread at once, so
+      // the next segment's first P V products can run while this one's rows are stored.
+      uint32_t ov[128];
+      tmem_ld128(tO, ov);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(c.bar(kBarOEmpty + tile));
+      __syncwarp();
+#pragma unroll
       for (int h = 0; h < 2; ++h) {
         uint32_t pk[32];
 #pragma unroll
-        for (int cc = 0; cc < 2; ++cc) {
-          uint32_t ov[32];
-          tmem_ld32(tO + (2 * h + cc) * 32, ov);
-#pragma unroll
-          for (int i = 0; i < 16; ++i)
-            pk[16 * cc + i] = pack_bf16(__uint_as_float(ov[2 * i]) * inv_l, __uint_as_float(ov[2 * i + 1]) * inv_l);
-        }
-        if (h == 1) {   // all of O_tile has been read: it may be overwritten now
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(c.bar(kBarOEmpty + tile));
-        }
+        for (int i = 0; i < 32; ++i)
+          pk[i] = pack_bf16(__uint_as_float(ov[64 * h + 2 * i]) * inv_l, __uint_as_float(ov[64 * h + 2 * i + 1]) * inv_l);
         store_half_rows(stage, pk, o_row0, valid_rows, h);
       }
       if (live) p.lse[row_id] = (m_used + log2f(l)) * 0.69314718055994531f;
@@ -911,6 +909,10 @@ __device__ void run_softmax(const Ctl& c, uint32_t tmem, uint8_t* stage, const P
         {
           uint32_t ov[128];
           tmem_ld128(tO, ov);
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(c.bar(kBarOEmpty + tile));   // O_tile may be overwritten now
+          __syncwarp();
           float4* rec4 = reinterpret_cast<float4*>(rec);
 #pragma unroll
           for (int g = 0; g < kD / 4; ++g)   // 512 contiguous bytes per warp
@@ -920,9 +922,6 @@ __device__ void run_softmax(const Ctl& c, uint32_t tmem, uint8_t* stage, const P
         rec[kD * kBM + r] = m_used;
         rec[kD * kBM + kBM + r] = l;
         rec[kD * kBM + 2 * kBM + r] = corr;
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(c.bar(kBarOEmpty + tile));   // O_tile may be overwritten now
         __threadfence();
         __syncwarp();
         unsigned int before = 0;
