@@ -480,8 +480,9 @@ __device__ void run_producer(const Ctl& c, uint32_t base, const CUtensorMap* tmQ
     ++u;
     // A segment of n steps streams n + 1 units: {K_0}, {V_0, K_1}, ..., {V_{n-2}, K_{n-1}},
     // {V_{n-1}}. Unit i is what the MMA thread consumes in one step (V for the P V
-    // products, K for the next S), so it waits once per step. Units alternate between
-    // the two slot pairs; the first tile of a unit takes the pair's first slot.
+    // products, K for the next S); one softmax thread checks it has landed, another
+    // releases it. Units alternate between the two slot pairs; the first tile of a unit
+    // takes the pair's first slot.
     const int n = sg.kv1 - sg.kv0;
     for (int i = 0; ok && i <= n; ++i, ++unit) {
       const int pr = unit % kPairs, use = unit / kPairs;
