@@ -18,7 +18,8 @@ import threading
 
 import numpy as np
 
-__all__ = ["build", "Oracle", "default", "attention_rows", "attention", "probs", "max_threads", "LIB_PATH"]
+__all__ = ["build", "Oracle", "default", "attention_rows", "attention_rows_causal", "attention", "probs",
+           "max_threads", "LIB_PATH"]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "attn_ref.c")
@@ -49,6 +50,8 @@ class Oracle:
         i64, dbl, vp = ctypes.c_int64, ctypes.c_double, ctypes.c_void_p
         lib.attn_ref_rows_f64.argtypes = [vp, vp, vp, i64, i64, i64, i64, i64, dbl, vp, i64, vp, vp, ctypes.c_int]
         lib.attn_ref_rows_f64.restype = ctypes.c_int
+        lib.attn_ref_rows_causal_f64.argtypes = lib.attn_ref_rows_f64.argtypes
+        lib.attn_ref_rows_causal_f64.restype = ctypes.c_int
         lib.attn_ref_probs_f64.argtypes = [vp, vp, i64, i64, i64, i64, dbl, vp]
         lib.attn_ref_probs_f64.restype = ctypes.c_int
         lib.attn_ref_max_threads.argtypes = []
@@ -80,6 +83,25 @@ class Oracle:
                                         _ptr(rows), rows.size, _ptr(o), _ptr(lse), int(nthreads))
         if rc != 0:
             raise ValueError(f"attn_ref_rows_f64 failed with status {rc}")
+        return o, lse
+
+    def attention_rows_causal(self, q, k, v, scale: float, rows=None, nthreads: int = 0):
+        """As attention_rows, under the causal mask: query i sees keys 0 .. i + Nk - Nq
+        (bottom-right alignment; needs Nq <= Nk)."""
+        q, k, v = _u16(q, 4), _u16(k, 4), _u16(v, 4)
+        B, H, Nq, d = q.shape
+        Nk, dv = k.shape[2], v.shape[3]
+        if k.shape != (B, H, Nk, d) or v.shape[:3] != (B, H, Nk):
+            raise ValueError(f"shape mismatch q{q.shape} k{k.shape} v{v.shape}")
+        if rows is None:
+            rows = np.arange(B * H * Nq, dtype=np.int64)
+        rows = np.ascontiguousarray(rows, dtype=np.int64)
+        o = np.empty((rows.size, dv), dtype=np.float64)
+        lse = np.empty(rows.size, dtype=np.float64)
+        rc = self.lib.attn_ref_rows_causal_f64(_ptr(q), _ptr(k), _ptr(v), B * H, Nq, Nk, d, dv, float(scale),
+                                               _ptr(rows), rows.size, _ptr(o), _ptr(lse), int(nthreads))
+        if rc != 0:
+            raise ValueError(f"attn_ref_rows_causal_f64 failed with status {rc}")
         return o, lse
 
     def attention(self, q, k, v, scale: float, nthreads: int = 0):
@@ -130,6 +152,10 @@ def max_threads() -> int:
 
 def attention_rows(q, k, v, scale: float, rows=None, nthreads: int = 0):
     return default().attention_rows(q, k, v, scale, rows, nthreads)
+
+
+def attention_rows_causal(q, k, v, scale: float, rows=None, nthreads: int = 0):
+    return default().attention_rows_causal(q, k, v, scale, rows, nthreads)
 
 
 def attention(q, k, v, scale: float, nthreads: int = 0):

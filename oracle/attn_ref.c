@@ -161,6 +161,58 @@ int attn_ref_rows_f64(const uint16_t *q, const uint16_t *k, const uint16_t *v,
 }
 
 /*
+ * attn_ref_rows_causal_f64: O and LSE of selected rows under the causal mask.
+ *
+ * The definition's optional mask B ("FlashAttention'ı Anlamak Bölüm 1", section 0.2)
+ * taken as the causal mask, aligned to the bottom-right corner of the score matrix:
+ * B_ij = 0 when j <= i + (Nk - Nq) and -inf otherwise, so that the last query row sees
+ * every key (the layout of a query block appended after Nk - Nq earlier positions).
+ * exp(-inf) = 0 removes a masked key from both sums, so row i is exactly the plain
+ * definition over its visible keys 0 .. i + Nk - Nq, which is how it is computed here.
+ * Requires Nq <= Nk (every row sees at least one key). Arguments as attn_ref_rows_f64.
+ */
+int attn_ref_rows_causal_f64(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                             int64_t BH, int64_t Nq, int64_t Nk, int64_t d, int64_t dv,
+                             double scale, const int64_t *sel, int64_t nsel,
+                             double *o, double *lse, int nthreads)
+{
+    if (BH < 0 || Nq < 0 || Nk < 1 || d < 1 || dv < 1 || nsel < 0 || Nq > Nk) return REF_EINVAL;
+    if (nsel == 0) return REF_OK;
+    if (!q || !k || !v || !sel || !o || !lse) return REF_EINVAL;
+    for (int64_t r = 0; r < nsel; r++)
+        if (sel[r] < 0 || sel[r] >= BH * Nq) return REF_EINVAL;
+
+    int failed = 0;
+#ifdef _OPENMP
+    int nt = nthreads > 0 ? nthreads : omp_get_max_threads();
+#pragma omp parallel num_threads(nt)
+#else
+    (void)nthreads;
+#endif
+    {
+        double *s = (double *)malloc((size_t)Nk * sizeof(double));
+        if (!s) {
+#ifdef _OPENMP
+#pragma omp atomic write
+#endif
+            failed = 1;
+        } else {
+#ifdef _OPENMP
+#pragma omp for schedule(dynamic, 1)
+#endif
+            for (int64_t r = 0; r < nsel; r++) {
+                int64_t bh = sel[r] / Nq, i = sel[r] % Nq;
+                int64_t visible = i + (Nk - Nq) + 1;   /* keys 0 .. i + Nk - Nq */
+                attend_row(q + (bh * Nq + i) * d, k + bh * Nk * d, v + bh * Nk * dv,
+                           visible, d, dv, scale, s, o + r * dv, lse + r);
+            }
+            free(s);
+        }
+    }
+    return failed ? REF_ENOMEM : REF_OK;
+}
+
+/*
  * attn_ref_probs_f64: the full probability matrix P = softmax_row(scale * Q K^T),
  * p [BH, Nq, Nk], for small shapes (tests of the row normalisation).
  */

@@ -226,6 +226,57 @@ def pin_matches_torch_float64_softmax_on_the_256_workload(orc):
     assert np.max(np.abs(lse - lt.numpy())) < 1e-12
 
 
+# ---- causal mask: the definition's optional mask B, aligned to the bottom-right corner --------
+
+def pin_causal_rows_are_plain_attention_over_the_visible_prefix(orc):
+    # row i sees keys 0 .. i + Nk - Nq: the plain oracle on that prefix of K and V
+    for Nq, Nk, seed in ((5, 9, 30), (7, 7, 31), (1, 4, 32), (6, 11, 33)):
+        q, k, v = make_qkv(2, 1, Nq, Nk, d=8, seed=seed)
+        o, lse = orc.attention_rows_causal(q, k, v, 0.9)
+        o, lse = o.reshape(2, Nq, 8), lse.reshape(2, Nq)
+        for b in range(2):
+            for i in range(Nq):
+                n = i + Nk - Nq + 1
+                op, lp = orc.attention_rows(q[b:b + 1, :, i:i + 1], k[b:b + 1, :, :n], v[b:b + 1, :, :n], 0.9)
+                assert np.max(np.abs(o[b, i] - op[0])) < 1e-14
+                assert abs(lse[b, i] - lp[0]) < 1e-14
+
+
+def pin_causal_square_first_row_is_its_own_key(orc):
+    # Nq = Nk: row 0 sees key 0 alone, with weight exactly 1: O = V[0], LSE = scale * q0.k0
+    q, k, v = make_qkv(1, 2, 6, 6, d=16, seed=34)
+    o, lse = orc.attention_rows_causal(q, k, v, 0.5, rows=np.array([0, 6], dtype=np.int64))
+    for r, h in ((0, 0), (1, 1)):
+        assert np.array_equal(o[r], widen(v)[0, h, 0])
+        assert abs(lse[r] - 0.5 * float(np.dot(widen(q)[0, h, 0], widen(k)[0, h, 0]))) < 1e-12
+
+
+def pin_causal_last_row_sees_every_key(orc):
+    q, k, v = make_qkv(1, 1, 4, 10, d=8, seed=35)
+    rows = np.array([3], dtype=np.int64)
+    oc, lc = orc.attention_rows_causal(q, k, v, 0.8, rows=rows)
+    of, lf = orc.attention_rows(q, k, v, 0.8, rows=rows)
+    assert np.array_equal(oc, of) and np.array_equal(lc, lf)
+
+
+def pin_causal_row_ignores_keys_past_its_diagonal(orc):
+    # Nq = 5, Nk = 8: row i sees keys 0 .. i + 3, so rewriting keys 5..7 leaves rows 0 and 1
+    q, k, v = make_qkv(1, 1, 5, 8, d=8, seed=36)
+    o1, l1 = orc.attention_rows_causal(q, k, v, 0.7)
+    k2, v2 = k.copy(), v.copy()
+    k2[0, 0, 5:] = k[0, 0, :3][::-1]
+    v2[0, 0, 5:] = v[0, 0, 1:4]
+    o2, l2 = orc.attention_rows_causal(q, k2, v2, 0.7)
+    assert np.array_equal(o1[:2], o2[:2]) and np.array_equal(l1[:2], l2[:2])
+    assert not np.array_equal(o1[4], o2[4])
+
+
+def test_causal_rejects_more_queries_than_keys():
+    q, k, v = make_qkv(1, 1, 5, 4, d=8, seed=37)
+    with pytest.raises(ValueError):
+        oracle.default().attention_rows_causal(q, k, v, 1.0)
+
+
 PINS = [v for k_, v in sorted(globals().items()) if k_.startswith("pin_")]
 
 

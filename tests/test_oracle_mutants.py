@@ -1,6 +1,7 @@
 """The oracle's pins must catch plausible slips: each mutant below plants one in a private
-copy of attn_ref.c (compiled into a temporary directory, on the CPU) and at least one pin
-of tests/test_oracle.py must fail against it. The committed oracle is never modified.
+copy of attn_ref.c (compiled into a temporary directory, on the CPU; at every occurrence
+of the mutated text) and at least one pin of tests/test_oracle.py must fail against it.
+The committed oracle is never modified.
 """
 import os
 import shutil
@@ -23,6 +24,8 @@ MUTANTS = {
     "last key dropped from PV": ("for (int64_t j = 0; j < Nk; j++)\n            acc += s[j]",
                                  "for (int64_t j = 0; j < Nk - 1; j++)\n            acc += s[j]"),
     "keys used as values": ("bf16_to_f64(vh[j * dv + c])", "bf16_to_f64(kh[j * d + c])"),
+    "causal mask one key short": ("int64_t visible = i + (Nk - Nq) + 1;", "int64_t visible = i + (Nk - Nq) + (i > 0);"),
+    "causal mask aligned top-left": ("int64_t visible = i + (Nk - Nq) + 1;", "int64_t visible = i + 1;"),
 }
 
 
@@ -30,7 +33,8 @@ MUTANTS = {
 def test_some_pin_catches(name, tmp_path):
     old, new = MUTANTS[name]
     src = open(os.path.join(os.path.dirname(oracle.__file__), "attn_ref.c")).read()
-    assert src.count(old) == 1, f"mutation site for {name!r} not found exactly once"
+    # a slip in code that two row functions share is planted in both
+    assert src.count(old) >= 1, f"mutation site for {name!r} not found"
     mut_src = tmp_path / "attn_ref.c"
     mut_src.write_text(src.replace(old, new))
     lib = oracle.build(force=True, src=str(mut_src), out=str(tmp_path / "libmut.so"))
