@@ -1,5 +1,5 @@
 #!/usr/bin/env python3
-"""Benchmark of the dense BF16 attention forward (d=128, non-causal) on GB300.
+"""Benchmark of the dense BF16 attention forward (d=128; non-causal by default) on GB300.
 
 One step = one attn_fwd call over the whole workload (every (b, h) and every query
 tile). Default workload: B=1, H=8, Nq=4096, Nk=8192 (the shape of the RTX 5090 table
@@ -12,6 +12,9 @@ the same C-ABI call, with the host->device copy of Q, K, V from pinned memory an
 device->host copy of O and LSE inside each timed step; steps are pipelined over three
 streams (copy in, compute, copy out) with two device buffer sets, so one step's copies
 overlap its neighbours' kernels.
+
+--causal times attn_fwd_causal instead (query i sees keys 0 .. i + Nk - Nq); its FLOPs
+count the visible (query, key) pairs only, 4*d each, and vs_baseline is null.
 
 --impl reference times the FP64 CPU oracle (the plain definition) on host cores, on a
 bounded sample of query rows per step.
@@ -54,6 +57,8 @@ def parse():
     ap.add_argument("--e2e-steps", type=int, default=50)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="target CPU time of the oracle sample")
+    ap.add_argument("--causal", action="store_true",
+                    help="causal mask (query i sees keys 0 .. i + Nk - Nq); FLOPs count visible pairs only")
     return ap.parse_args()
 
 
@@ -138,9 +143,18 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(inside), "window": window}
 
 
+def workload_flops(w, causal: bool) -> float:
+    """4*d FLOPs per visible (query, key) pair: all Nq*Nk pairs, or under the causal mask
+    Nq*(Nk - Nq) + Nq*(Nq + 1)/2 of them."""
+    if not causal:
+        return float(w.flops)
+    pairs = w.Nq * (w.Nk - w.Nq) + w.Nq * (w.Nq + 1) / 2
+    return 4.0 * w.B * w.H * w.d * pairs
+
+
 # ------------------------------------------------------------------ reference arm (oracle) ---
 
-def cpu_oracle_sample(w, target_seconds: float, rank_seed: int = 0):
+def cpu_oracle_sample(w, target_seconds: float, rank_seed: int = 0, causal: bool = False):
     """Time the FP64 oracle on a sample of query rows; returns (TFLOPS, rows, seconds, threads)."""
     import numpy as np
 
@@ -150,21 +164,31 @@ def cpu_oracle_sample(w, target_seconds: float, rank_seed: int = 0):
     # K and V of one head are all a row needs; draw the workload's own tensors at full
     # size only when they are small, else draw one head (same distribution).
     H1 = w.H if w.B * w.H * w.Nk * w.d <= (1 << 26) else 1
-    q, k, v = make_qkv(1, H1, min(w.Nq, 4096), w.Nk, d=w.d, seed=w.seed + rank_seed, qk_mult=w.qk_mult)
+    nq = min(w.Nq, 4096)
+    q, k, v = make_qkv(1, H1, nq, w.Nk, d=w.d, seed=w.seed + rank_seed, qk_mult=w.qk_mult)
     threads = oracle.max_threads()
-    flop_row = 4.0 * w.Nk * w.d
+    fn = oracle.attention_rows_causal if causal else oracle.attention_rows
+
+    def flop_rows(rows):   # 4*d FLOPs per visible key of each sampled row
+        if not causal:
+            return 4.0 * w.Nk * w.d * len(rows)
+        # the sample's nq queries are aligned to the end of the key range, like the last nq
+        # rows of the workload: row r sees keys 0 .. r + Nk - nq
+        i = rows % nq + (w.Nq - nq)
+        return float(np.sum(4.0 * w.d * (i + (w.Nk - w.Nq) + 1)))
+
     n_rows_total = q.shape[1] * q.shape[2]
     probe = min(max(threads, 8), n_rows_total)
-    rows = np.arange(probe, dtype=np.int64)
+    rows = np.linspace(0, n_rows_total - 1, probe).astype(np.int64)   # spread: causal rows differ in length
     t = time.perf_counter()
-    oracle.attention_rows(q, k, v, w.scale, rows)
+    fn(q, k, v, w.scale, rows)
     dt = time.perf_counter() - t
     n = int(min(n_rows_total, max(probe, target_seconds / max(dt / probe, 1e-9))))
     rows = np.linspace(0, n_rows_total - 1, n).astype(np.int64)
     t = time.perf_counter()
-    oracle.attention_rows(q, k, v, w.scale, rows)
+    fn(q, k, v, w.scale, rows)
     dt = time.perf_counter() - t
-    return flop_row * n / dt / 1e12, n, dt, threads
+    return flop_rows(rows) / dt / 1e12, n, dt, threads
 
 
 def run_reference(args, w):
@@ -178,32 +202,40 @@ def run_reference(args, w):
 
     steps, warm = args.steps, args.warmup
     H1 = w.H if w.B * w.H * w.Nk * w.d <= (1 << 26) else 1
-    q, k, v = make_qkv(1, H1, min(w.Nq, 4096), w.Nk, d=w.d, seed=w.seed, qk_mult=w.qk_mult)
+    nq = min(w.Nq, 4096)
+    q, k, v = make_qkv(1, H1, nq, w.Nk, d=w.d, seed=w.seed, qk_mult=w.qk_mult)
     threads = oracle.max_threads()
     n_rows_total = q.shape[1] * q.shape[2]
-    flop_row = 4.0 * w.Nk * w.d
+    fn = oracle.attention_rows_causal if args.causal else oracle.attention_rows
+
+    def flop_rows(rows):   # 4*d FLOPs per visible key; causal sample rows sit at the end of the sequence
+        if not args.causal:
+            return 4.0 * w.Nk * w.d * len(rows)
+        return float(np.sum(4.0 * w.d * (rows % nq + (w.Nk - nq) + 1)))
     # size each step so that warmup + steps take about two minutes in all
     t = time.perf_counter()
-    oracle.attention_rows(q, k, v, w.scale, np.arange(threads, dtype=np.int64))
+    fn(q, k, v, w.scale, np.linspace(0, n_rows_total - 1, threads).astype(np.int64))
     per_row = (time.perf_counter() - t) / threads
     rows_per_step = int(max(1, min(n_rows_total, 120.0 / (steps + warm) / per_row)))
     rng = np.random.Generator(np.random.PCG64(1234))
     for _ in range(warm):
-        oracle.attention_rows(q, k, v, w.scale, rng.choice(n_rows_total, rows_per_step, replace=False))
-    total = 0.0
+        fn(q, k, v, w.scale, rng.choice(n_rows_total, rows_per_step, replace=False))
+    total, flops = 0.0, 0.0
     for _ in range(steps):
         rows = rng.choice(n_rows_total, rows_per_step, replace=False)
         t = time.perf_counter()
-        oracle.attention_rows(q, k, v, w.scale, rows)
+        fn(q, k, v, w.scale, rows)
         total += time.perf_counter() - t
+        flops += flop_rows(rows)
     ms = total / steps * 1e3
-    tflops = flop_row * rows_per_step / (ms / 1e3) / 1e12
-    sample = f"{rows_per_step} query rows per step of {w.describe()} (full Nk per row), FP64"
+    tflops = flops / total / 1e12
+    keys = "visible keys of each row, causal" if args.causal else "full Nk per row"
+    sample = f"{rows_per_step} query rows per step of {w.describe()} ({keys}), FP64"
     line = {
         "impl": "reference", "metric": METRIC, "value": tflops, "unit": "TFLOP/s", "n_gpus": world,
         "steps": steps, "warmup": warm, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": w.name, "B": w.B, "H": w.H, "Nq": w.Nq, "Nk": w.Nk, "d": w.d, "causal": False,
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "Nq": w.Nq, "Nk": w.Nk, "d": w.d, "causal": args.causal,
                    "qk_mult": w.qk_mult},
         "cpu_baseline": {"value": tflops, "unit": "TFLOP/s", "cores": threads, "kind": "oracle", "sample": sample},
         "e2e": {"value": tflops, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -246,8 +278,11 @@ def run_ours(args, w):
     flush = torch.empty(L2_FLUSH_BYTES // 4, device=dev, dtype=torch.int32)
     stream = torch.cuda.current_stream(dev)
 
+    fwd = attn.attn_fwd_causal if args.causal else attn.attn_fwd
+    flops = workload_flops(w, args.causal)
+
     def step():
-        attn.attn_fwd(q, k, v, o, lse, w.B, w.H, w.Nq, w.Nk, w.d, w.scale, stream)
+        fwd(q, k, v, o, lse, w.B, w.H, w.Nq, w.Nk, w.d, w.scale, stream)
 
     sampler = ClockSampler(local_rank)   # started early: nvidia-smi needs a moment to come up
     time.sleep(1.0)
@@ -306,7 +341,7 @@ def run_ours(args, w):
                 ev_in[b].record(s_in)
             s_run.wait_event(ev_in[b])
             s_run.wait_event(ev_out[b])                  # this output set has been copied out
-            attn.attn_fwd(dq, dk, dv, do, dl, w.B, w.H, w.Nq, w.Nk, w.d, w.scale, s_run)
+            fwd(dq, dk, dv, do, dl, w.B, w.H, w.Nq, w.Nk, w.d, w.scale, s_run)
             ev_done[b].record(s_run)
             s_out.wait_event(ev_done[b])
             with torch.cuda.stream(s_out):
@@ -340,25 +375,25 @@ def run_ours(args, w):
         tt = torch.tensor([ms, e2e_ms], device=dev, dtype=torch.float64)
         pg.all_reduce(tt, op=pg.ReduceOp.MAX)
         ms, e2e_ms = float(tt[0]), float(tt[1])
-    total_flops = w.flops * world
+    total_flops = flops * world
     value = total_flops / (ms * 1e-3) / 1e12
     e2e_value = total_flops / (e2e_ms * 1e-3) / 1e12
 
     peaks, peak_src = measured_peaks()
     peak = float(peaks["bf16_tflops"])
-    achieved = w.flops / (ms * 1e-3) / 1e12   # one launch on one GPU
+    achieved = flops / (ms * 1e-3) / 1e12   # one launch on one GPU
     traffic = None
     if os.path.exists(TRAFFIC_FILE):
-        rec = json.load(open(TRAFFIC_FILE)).get(w.name)
+        rec = json.load(open(TRAFFIC_FILE)).get(w.name + ("-causal" if args.causal else ""))
         if rec and rec.get("kernel_hash") == kernel_hash():
             traffic = rec.get("bytes_per_launch")
 
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": (value / PAGES_TFLOPS[w.name]) if w.name in PAGES_TFLOPS else None,
+        "vs_baseline": (value / PAGES_TFLOPS[w.name]) if w.name in PAGES_TFLOPS and not args.causal else None,
         "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": w.name, "B": w.B, "H": w.H, "Nq": w.Nq, "Nk": w.Nk, "d": w.d, "causal": False,
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "Nq": w.Nq, "Nk": w.Nk, "d": w.d, "causal": args.causal,
                    "qk_mult": w.qk_mult, "inputs": "iid N(0,1) BF16 (Q,K x qk_mult)",
                    "l2": "flushed (512 MiB write) before every timed launch",
                    "vs_baseline_ref": "RTX 5090 v5 kernel, same shape (other hardware: context only)"},
@@ -371,9 +406,10 @@ def run_ours(args, w):
         "kernel_ms_min": min(durs), "kernel_ms_median": statistics.median(durs),
     }
     if rank == 0 and not args.no_cpu_baseline:
-        tfl, n, dt, thr = cpu_oracle_sample(w, args.cpu_seconds)
+        tfl, n, dt, thr = cpu_oracle_sample(w, args.cpu_seconds, causal=args.causal)
+        keys = "visible keys of each row, causal" if args.causal else "full Nk each"
         line["cpu_baseline"] = {"value": tfl, "unit": "TFLOP/s", "cores": thr, "kind": "oracle",
-                                "sample": f"{n} query rows of {w.describe()} (full Nk each), FP64, {dt:.1f} s"}
+                                "sample": f"{n} query rows of {w.describe()} ({keys}), FP64, {dt:.1f} s"}
     if pg is not None:
         pg.barrier()
         pg.destroy_process_group()

@@ -15,7 +15,7 @@ from ._build import LIB_PATH, build_library
 
 __all__ = [
     "ATTN_OK", "ATTN_ERR_INVALID_ARG", "ATTN_ERR_UNSUPPORTED", "ATTN_ERR_MISALIGNED", "ATTN_ERR_CUDA",
-    "ATTN_ERR_TIMEOUT", "AttnError", "load_library", "attn_fwd", "attn_fwd_noalloc", "attn_fwd_status", "attn_status_string",
+    "ATTN_ERR_TIMEOUT", "AttnError", "load_library", "attn_fwd", "attn_fwd_causal", "attn_fwd_noalloc", "attn_fwd_status", "attn_status_string",
     "attn_fwd_set_wait_limit", "attn_fwd_kernel_count", "attention",
 ]
 
@@ -47,6 +47,7 @@ def load_library(build_if_stale: bool = True) -> ctypes.CDLL:
             lib.attn_fwd.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, f32, vp]
             lib.attn_fwd.restype = i32
             lib.attn_fwd_noalloc.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, f32, vp]
+            lib.attn_fwd_causal.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, f32, vp]
             lib.attn_fwd_noalloc.restype = i32
             lib.attn_fwd_status.argtypes = [vp]
             lib.attn_fwd_status.restype = i32
@@ -114,6 +115,21 @@ def attn_fwd(q, k, v, o, lse, B: int, H: int, Nq: int, Nk: int, d: int, scale: f
                       _stream_handle(stream, q, k, v, o, lse))
     if rc != ATTN_OK:
         raise AttnError(rc)
+
+
+def attn_fwd_causal(q, k, v, o, lse, B: int, H: int, Nq: int, Nk: int, d: int, scale: float, stream=None) -> None:
+    """Like :func:`attn_fwd`, under the causal mask: query i sees keys 0 .. i + Nk - Nq
+    (the mask aligned to the bottom-right corner of the score matrix); needs Nq <= Nk."""
+    lib = load_library()
+    args = (
+        _ptr(q, "q", B * H * Nq * d, "bf16"), _ptr(k, "k", B * H * Nk * d, "bf16"),
+        _ptr(v, "v", B * H * Nk * d, "bf16"), _ptr(o, "o", B * H * Nq * d, "bf16"),
+        _ptr(lse, "lse", B * H * Nq, "f32"),
+    )
+    rc = lib.attn_fwd_causal(*args, int(B), int(H), int(Nq), int(Nk), int(d), float(scale),
+                             _stream_handle(stream, q, k, v, o, lse))
+    if rc != ATTN_OK:
+        raise AttnError(rc, "attn_fwd_causal")
 
 
 def attn_fwd_noalloc(q, k, v, o, lse, B: int, H: int, Nq: int, Nk: int, d: int, scale: float, stream=None) -> None:

@@ -1,4 +1,4 @@
-// attn_fwd.cu -- dense, non-causal BF16 attention forward for GB300 (sm_103a).
+// attn_fwd.cu -- dense BF16 attention forward for GB300 (sm_103a), non-causal and causal.
 //
 // O = softmax(scale * Q K^T) V and the per-row log-sum-exp, head_dim 128, computed
 // FlashAttention-style: Q tiles of 128 query rows are loaded once and 128-key K/V
@@ -140,9 +140,11 @@ struct Params {
   float scale_log2;       // scale * log2(e)
   unsigned long long wait_limit;
   int withhold_tile;      // test hook: never load the second K/V unit of a block (V of step 0, K of step 1)
+  int causal;             // query i sees keys 0 .. i + causal_off only (causal_off = Nk - Nq >= 0)
+  int causal_off;
+  int bh_count;           // B * H
 };
 
-// First key step (counted over the split region) of block c's share.
 // floor(a / b) for a >= 0, b > 0. On the device a 64-bit division is a long dependent
 // sequence; operands that fit 32 bits (all but enormous problems) take the short one.
 __host__ __device__ __forceinline__ long long div_floor(long long a, long long b) {
@@ -153,6 +155,7 @@ __host__ __device__ __forceinline__ long long div_floor(long long a, long long b
   return a / b;
 }
 
+// First key step (counted over the split region) of block c's share.
 __host__ __device__ __forceinline__ long long sk_share_start(long long c, long long sk_steps, long long grid) {
   return div_floor(c * sk_steps, grid);
 }
@@ -166,9 +169,15 @@ struct Segment {
 
 // The segments of one block, in processing order; every role of the block walks the
 // same sequence.
+//
+// Causal launches: a group needs only the keys up to its last row's diagonal, so groups
+// differ in length. They are processed whole (no split), longest first: list position x
+// holds diagonal position q_groups - 1 - x / (B*H) of head x % (B*H), and block b takes
+// position b of even waves and grid - 1 - b of odd ones, which evens out the waves.
 struct SegIter {
   int n_kv, dp_groups, grid, next_dp;
   long long sk_begin, sk_end, sk_pos;
+  int causal, causal_off, q_groups, bh_count, Nq, wave;
   __device__ explicit SegIter(const Params& p) {
     n_kv = p.n_kv;
     dp_groups = p.dp_groups;
@@ -177,8 +186,29 @@ struct SegIter {
     sk_begin = sk_share_start(blockIdx.x, p.sk_steps, grid);
     sk_end = sk_share_start(static_cast<long long>(blockIdx.x) + 1, p.sk_steps, grid);
     sk_pos = sk_begin;
+    causal = p.causal;
+    causal_off = p.causal_off;
+    q_groups = p.q_groups;
+    bh_count = p.bh_count;
+    Nq = p.Nq;
+    wave = 0;
   }
   __device__ bool next(Segment& sg) {
+    if (causal) {
+      const int pos = (wave & 1) ? grid - 1 - static_cast<int>(blockIdx.x) : static_cast<int>(blockIdx.x);
+      const long long x = static_cast<long long>(wave) * grid + pos;
+      if (x >= static_cast<long long>(bh_count) * q_groups) return false;
+      ++wave;
+      const int xi = static_cast<int>(x);
+      const int qg = q_groups - 1 - xi / bh_count;
+      sg.group = (xi % bh_count) * q_groups + qg;
+      const int row_end = min(Nq, (qg + 1) * (kQTiles * kBM));   // one past the group's last row
+      sg.kv0 = 0;
+      sg.kv1 = (row_end + causal_off + kBN - 1) / kBN;
+      sg.which = 0;
+      sg.split = false;
+      return true;
+    }
     if (next_dp < dp_groups) {
       sg.group = next_dp;
       sg.kv0 = 0;
@@ -755,6 +785,8 @@ __device__ void run_softmax(const Ctl& c, uint32_t tmem, uint8_t* stage, const P
   Segment sg;
   while (si.next(sg)) {
     const int n = sg.kv1 - sg.kv0;
+    // this warp's first query row (causal masking)
+    const int seg_row0 = (sg.group % p.q_groups) * (kQTiles * kBM) + tile * kBM + quarter * 32;
     float m_used = -INFINITY;   // log2 units
     float l = 0.0f;             // sum of 2^(s*cs - m_used) in FP32
     float corr = 0.0f;          // BF16 rounding error of the largest term of each tile
@@ -778,6 +810,15 @@ __device__ void run_softmax(const Ctl& c, uint32_t tmem, uint8_t* stage, const P
         const int valid = p.kv_tail;
 #pragma unroll
         for (int i = 0; i < 128; ++i) s[i] = (i < valid) ? s[i] : -INFINITY;
+      }
+      if (p.causal) {
+        // key (kv0 + j) * 128 + i is visible to this row iff it is <= row + causal_off
+        const int lim_warp = seg_row0 + p.causal_off - (sg.kv0 + j) * kBN;   // the warp's first row
+        if (lim_warp < kBN - 1) {   // warp-uniform: some row of this warp has keys masked here
+          const int lim = lim_warp + lane;
+#pragma unroll
+          for (int i = 0; i < 128; ++i) s[i] = (i <= lim) ? s[i] : -INFINITY;
+        }
       }
       // row max: eight independent three-input max chains over s[0..127]
       // (chain t covers s[t], s[t + 8], s[t + 16], ..., s[t + 120])
@@ -1215,6 +1256,9 @@ extern "C" int attn_fwd(const void* q, const void* k, const void* v, void* o, fl
   p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
   p.wait_limit = g_wait_limit.load(std::memory_order_relaxed);
   p.withhold_tile = g_withhold.load(std::memory_order_relaxed);
+  p.causal = 0;
+  p.causal_off = 0;
+  p.bh_count = static_cast<int>(bh);
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (pl.has_split) {
@@ -1225,6 +1269,62 @@ extern "C" int attn_fwd(const void* q, const void* k, const void* v, void* o, fl
     if (rc != ATTN_OK) return rc;
   }
   return scale > 0.0f ? launch<true>(mq, mk, mv, p, pl.grid, dev, s) : launch<false>(mq, mk, mv, p, pl.grid, dev, s);
+}
+
+extern "C" int attn_fwd_causal(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                               int Nq, int Nk, int d, float scale, void* stream) {
+  // the argument rules of attn_fwd, plus Nq <= Nk (every query row sees at least one key)
+  if (B < 0 || H < 0 || Nq < 0 || Nk < 0) return ATTN_ERR_INVALID_ARG;
+  if (d != kD) return ATTN_ERR_UNSUPPORTED;
+  if (!std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
+  const long long bh = static_cast<long long>(B) * H;
+  if (bh == 0 || Nq == 0) return ATTN_OK;
+  if (Nk == 0 || Nq > Nk) return ATTN_ERR_INVALID_ARG;
+  if (Nk > INT_MAX - 1024) return ATTN_ERR_UNSUPPORTED;   // row + causal_off + 2 * kBN stays in int
+  if (!q || !k || !v || !o || !lse) return ATTN_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) | reinterpret_cast<uintptr_t>(v) |
+       reinterpret_cast<uintptr_t>(o)) & 15u)
+    return ATTN_ERR_MISALIGNED;
+  if (reinterpret_cast<uintptr_t>(lse) & 3u) return ATTN_ERR_MISALIGNED;
+  const long long q_groups = (static_cast<long long>(Nq) + kQTiles * kBM - 1) / (kQTiles * kBM);
+  if (bh > INT_MAX || bh * q_groups > INT_MAX) return ATTN_ERR_UNSUPPORTED;
+  const long long max_rows = static_cast<long long>(Nk);
+  if (bh > (LLONG_MAX / 256) / max_rows) return ATTN_ERR_INVALID_ARG;
+
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return ATTN_ERR_CUDA;
+  const int sms = sm_count(dev);
+  if (sms <= 0) return ATTN_ERR_CUDA;
+
+  CUtensorMap mq, mk, mv;
+  if (!make_map(&mq, q, Nq, bh) || !make_map(&mk, k, Nk, bh) || !make_map(&mv, v, Nk, bh))
+    return ATTN_ERR_CUDA;
+
+  // Whole groups only (the causal order of SegIter): no workspace, no merge.
+  const long long n_groups = bh * q_groups;
+  Params p;
+  p.o = static_cast<uint16_t*>(o);
+  p.lse = lse;
+  p.Nq = Nq;
+  p.Nk = Nk;
+  p.q_groups = static_cast<int>(q_groups);
+  p.n_kv = (Nk + kBN - 1) / kBN;
+  p.kv_tail = Nk - (p.n_kv - 1) * kBN;
+  p.dp_groups = 0;
+  p.sk_steps = 0;
+  p.part = nullptr;
+  p.cnt = nullptr;
+  p.cnt_next = nullptr;
+  p.cnt_len = 0;
+  p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+  p.wait_limit = g_wait_limit.load(std::memory_order_relaxed);
+  p.withhold_tile = g_withhold.load(std::memory_order_relaxed);
+  p.causal = 1;
+  p.causal_off = Nk - Nq;
+  p.bh_count = static_cast<int>(bh);
+  const int grid = static_cast<int>(n_groups < sms ? n_groups : sms);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  return scale > 0.0f ? launch<true>(mq, mk, mv, p, grid, dev, s) : launch<false>(mq, mk, mv, p, grid, dev, s);
 }
 
 extern "C" int attn_fwd_status(void* stream) {
@@ -1339,6 +1439,9 @@ extern "C" int attn_fwd_noalloc(const void* q, const void* k, const void* v, voi
   p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
   p.wait_limit = g_wait_limit.load(std::memory_order_relaxed);
   p.withhold_tile = g_withhold.load(std::memory_order_relaxed);
+  p.causal = 0;
+  p.causal_off = 0;
+  p.bh_count = static_cast<int>(bh);
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (pl.has_split) {

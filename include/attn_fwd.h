@@ -78,6 +78,26 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
              int B, int H, int Nq, int Nk, int d, float scale, void* stream);
 
 /*
+ * attn_fwd_causal -- causal attention forward.
+ *
+ * The optional mask B of the definition ("FlashAttention'ı Anlamak Bölüm 1", section 0.2)
+ * taken as the causal mask: B_ij = 0 when j <= i + (Nk - Nq) and -inf otherwise, i.e.
+ * query i sees keys 0 .. i + Nk - Nq. The mask is aligned to the bottom-right corner of
+ * the score matrix, so the last query sees every key (a block of Nq queries that follows
+ * Nk - Nq earlier positions). The pages do not fix the alignment; this is the reading
+ * under which a square problem is the usual lower-triangular mask.
+ *
+ * Arguments, layouts and return values are those of attn_fwd, plus:
+ *   - Nq <= Nk is required (every query row sees at least one key); Nq > Nk returns
+ *     ATTN_ERR_INVALID_ARG without touching the GPU.
+ *   - lse is the log-sum-exp over the visible keys only.
+ *   - The call allocates nothing: each block processes whole (b, h, 256-row) groups,
+ *     longest first, over only the key tiles its rows can see.
+ */
+int attn_fwd_causal(const void* q, const void* k, const void* v, void* o, float* lse,
+                    int B, int H, int Nq, int Nk, int d, float scale, void* stream);
+
+/*
  * attn_fwd_noalloc -- attn_fwd for callers that cannot allocate device memory.
  *
  * There is no counterpart on the pages: this is a service of the library. Some callers

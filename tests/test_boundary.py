@@ -20,8 +20,8 @@ def declared_functions():
 
 def test_header_declares_the_entry_points():
     names = declared_functions()
-    assert {"attn_fwd", "attn_fwd_status", "attn_status_string", "attn_fwd_set_wait_limit",
-            "attn_fwd_kernel_count"} <= set(names)
+    assert {"attn_fwd", "attn_fwd_causal", "attn_fwd_noalloc", "attn_fwd_status", "attn_status_string",
+            "attn_fwd_set_wait_limit", "attn_fwd_kernel_count"} <= set(names)
 
 
 def test_library_exports_every_declared_symbol():
@@ -73,6 +73,27 @@ def call(q=A, k=A, v=A, o=A, lse=A, B=1, H=1, Nq=128, Nk=128, d=128, scale=0.125
 ])
 def test_argument_checks(kw, code):
     assert call(**kw) == code
+
+
+def call_causal(q=A, k=A, v=A, o=A, lse=A, B=1, H=1, Nq=128, Nk=128, d=128, scale=0.125):
+    return attn.load_library().attn_fwd_causal(q, k, v, o, lse, B, H, Nq, Nk, d, scale, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(Nq=129, Nk=128), attn.ATTN_ERR_INVALID_ARG),   # a query row would see no key
+    (dict(Nq=1, Nk=0), attn.ATTN_ERR_INVALID_ARG),
+    (dict(k=None), attn.ATTN_ERR_INVALID_ARG),
+    (dict(scale=math.nan), attn.ATTN_ERR_INVALID_ARG),
+    (dict(d=64), attn.ATTN_ERR_UNSUPPORTED),
+    (dict(o=A + 4), attn.ATTN_ERR_MISALIGNED),
+    (dict(B=1 << 16, H=1 << 16), attn.ATTN_ERR_UNSUPPORTED),
+    (dict(Nq=0, Nk=0, lse=None), attn.ATTN_OK),
+    (dict(B=0), attn.ATTN_OK),
+])
+def test_causal_argument_checks(kw, code):
+    before = attn.attn_fwd_kernel_count()
+    assert call_causal(**kw) == code
+    assert attn.attn_fwd_kernel_count() == before
 
 
 def test_binding_raises_on_rejected_call():

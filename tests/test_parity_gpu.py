@@ -139,3 +139,49 @@ def test_split_workspace_reuse_across_shapes(gpu_lib):
     for B, H, Nq, Nk in [(1, 1, 256, 5120), (1, 2, 300, 3000), (1, 1, 256, 5120), (1, 8, 1024, 4096),
                          (1, 2, 300, 3000)]:
         check_case(gpu_lib, B, H, Nq, Nk, seed=Nq + Nk)
+
+
+# ---- causal mask (query i sees keys 0 .. i + Nk - Nq) ------------------------------------------
+
+@pytest.mark.parametrize("B,H,Nq,Nk", [
+    (1, 1, 256, 256),     # one group: both tiles, the diagonal inside each of the two key tiles
+    (1, 2, 512, 512),     # groups of different lengths, longest first
+    (2, 3, 384, 640),     # Nq < Nk: the diagonal shifted by 256 keys, an odd number of Q tiles
+    (1, 2, 300, 300),     # ragged: partial last Q tile and partial last key tile
+    (1, 1, 1, 1),
+    (1, 1, 1, 200),       # a single query sees every key
+    (1, 1, 129, 129),
+    (1, 3, 1000, 1777),
+    (4, 2, 768, 768),     # more groups than blocks on a small GPU slice: several waves
+])
+def test_causal_full_parity(gpu_lib, B, H, Nq, Nk):
+    check_case(gpu_lib, B, H, Nq, Nk, seed=7000 + Nq + Nk, causal=True)
+
+
+def test_causal_first_row_returns_its_own_value(gpu_lib):
+    # square: row 0 sees key 0 alone with weight exactly 1, so O[0] is V[0] bit for bit
+    q, k, v = make_qkv(1, 2, 384, 384, seed=71)
+    o, lse = run_gpu(gpu_lib, q, k, v, SCALE, causal=True)
+    assert np.array_equal(o[:, :, 0], bf16_bits_to_f32(v)[:, :, 0])
+    expect = SCALE * np.einsum("bhd,bhd->bh", bf16_bits_to_f32(q)[:, :, 0].astype(np.float64),
+                               bf16_bits_to_f32(k)[:, :, 0].astype(np.float64))
+    assert np.max(np.abs(lse[:, :, 0] - expect)) < 1e-4 * np.maximum(1.0, np.abs(expect)).max()
+
+
+def test_causal_peaked_and_other_scales(gpu_lib):
+    check_case(gpu_lib, 1, 2, 512, 1024, seed=72, qk_mult=3.0, ulp_aware=True, causal=True)
+    check_case(gpu_lib, 1, 2, 256, 384, seed=73, scale=-0.0883883461356163, ulp_aware=True, causal=True)
+    check_case(gpu_lib, 1, 2, 512, 2048, seed=74, scale=2.0, ulp_aware=True, causal=True)
+
+
+@pytest.mark.parametrize("name", ["square-4k", "long-16k"])
+def test_causal_workload_sampled_rows(gpu_lib, name):
+    w = by_name(name)
+    rows = sample_rows(w.B, w.H, w.Nq, per_head=16)
+    check_case(gpu_lib, w.B, w.H, w.Nq, w.Nk, seed=w.seed, scale=w.scale, rows=rows, causal=True)
+
+
+def test_causal_rejects_more_queries_than_keys(gpu_lib):
+    with pytest.raises(gpu_lib.AttnError) as e:
+        run_gpu(gpu_lib, *make_qkv(1, 1, 200, 100, seed=75), SCALE, causal=True)
+    assert e.value.status == gpu_lib.ATTN_ERR_INVALID_ARG
