@@ -18,8 +18,8 @@ import threading
 
 import numpy as np
 
-__all__ = ["build", "Oracle", "default", "attention_rows", "attention_rows_causal", "attention", "probs",
-           "max_threads", "LIB_PATH"]
+__all__ = ["build", "Oracle", "default", "attention_rows", "attention_rows_causal", "attention_rows_bias",
+           "attention", "probs", "max_threads", "LIB_PATH"]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "attn_ref.c")
@@ -52,6 +52,9 @@ class Oracle:
         lib.attn_ref_rows_f64.restype = ctypes.c_int
         lib.attn_ref_rows_causal_f64.argtypes = lib.attn_ref_rows_f64.argtypes
         lib.attn_ref_rows_causal_f64.restype = ctypes.c_int
+        lib.attn_ref_rows_bias_f64.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, i64, i64, i64, i64, i64, dbl,
+                                               vp, i64, vp, vp, ctypes.c_int]
+        lib.attn_ref_rows_bias_f64.restype = ctypes.c_int
         lib.attn_ref_probs_f64.argtypes = [vp, vp, i64, i64, i64, i64, dbl, vp]
         lib.attn_ref_probs_f64.restype = ctypes.c_int
         lib.attn_ref_max_threads.argtypes = []
@@ -102,6 +105,34 @@ class Oracle:
                                                _ptr(rows), rows.size, _ptr(o), _ptr(lse), int(nthreads))
         if rc != 0:
             raise ValueError(f"attn_ref_rows_causal_f64 failed with status {rc}")
+        return o, lse
+
+    def attention_rows_bias(self, q, k, v, bias, scale: float, rows=None, nthreads: int = 0):
+        """As attention_rows, with the additive bias B: S = scale * Q K^T + B.
+
+        ``bias`` holds BF16 bits (uint16) of shape (Bb, Hb, Nqb, Nk) with Bb in {1, B},
+        Hb in {1, H}, Nqb in {1, Nq}; a dimension of size 1 is repeated (numpy
+        broadcasting). A C-contiguous view into a larger buffer is used in place.
+        """
+        q, k, v, bias = _u16(q, 4), _u16(k, 4), _u16(v, 4), _u16(bias, 4)
+        B, H, Nq, d = q.shape
+        Nk, dv = k.shape[2], v.shape[3]
+        if k.shape != (B, H, Nk, d) or v.shape[:3] != (B, H, Nk):
+            raise ValueError(f"shape mismatch q{q.shape} k{k.shape} v{v.shape}")
+        Bb, Hb, Nqb, Nkb = bias.shape
+        if Bb not in (1, B) or Hb not in (1, H) or Nqb not in (1, Nq) or Nkb != Nk:
+            raise ValueError(f"bias shape {bias.shape} does not broadcast to {(B, H, Nq, Nk)}")
+        sb, sh, sq = (st // 2 if n > 1 else 0 for st, n in zip(bias.strides[:3], (Bb, Hb, Nqb)))
+        if rows is None:
+            rows = np.arange(B * H * Nq, dtype=np.int64)
+        rows = np.ascontiguousarray(rows, dtype=np.int64)
+        o = np.empty((rows.size, dv), dtype=np.float64)
+        lse = np.empty(rows.size, dtype=np.float64)
+        rc = self.lib.attn_ref_rows_bias_f64(_ptr(q), _ptr(k), _ptr(v), _ptr(bias), H, sb, sh, sq, B * H, Nq, Nk,
+                                             d, dv, float(scale), _ptr(rows), rows.size, _ptr(o), _ptr(lse),
+                                             int(nthreads))
+        if rc != 0:
+            raise ValueError(f"attn_ref_rows_bias_f64 failed with status {rc}")
         return o, lse
 
     def attention(self, q, k, v, scale: float, nthreads: int = 0):
@@ -156,6 +187,10 @@ def attention_rows(q, k, v, scale: float, rows=None, nthreads: int = 0):
 
 def attention_rows_causal(q, k, v, scale: float, rows=None, nthreads: int = 0):
     return default().attention_rows_causal(q, k, v, scale, rows, nthreads)
+
+
+def attention_rows_bias(q, k, v, bias, scale: float, rows=None, nthreads: int = 0):
+    return default().attention_rows_bias(q, k, v, bias, scale, rows, nthreads)
 
 
 def attention(q, k, v, scale: float, nthreads: int = 0):

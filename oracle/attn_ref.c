@@ -11,7 +11,8 @@
  *   S = scale * Q K^T,   P = softmax_row(S),   O = P V
  *
  * ("FlashAttention'ı Anlamak Bölüm 1", section 0.2 Notasyon, with the optional
- * mask/bias B taken as zero; the scale is the caller's, applied to the scores as
+ * mask/bias B taken as zero here, as the causal mask and as a caller-given bias in
+ * the two functions that say so; the scale is the caller's, applied to the scores as
  * in the "Алгоритм Flash Attention 2" pseudocode of "Flash Attention на 5090 в
  * CUDA C++"). The same notes (section 0.1) state that FlashAttention reaches this
  * exact result, only in a different floating-point order, so a tiled GPU kernel
@@ -88,12 +89,20 @@ static double row_exp_sum(double *s, int64_t Nk, double m)
     return l;
 }
 
-/* One query row: writes o[0..dv) and *lse. s is caller scratch of Nk doubles. */
+/*
+ * One query row i: writes o[0..dv) and *lse. s is caller scratch of Nk doubles.
+ * bh_bias, when not NULL, is the head's additive bias B: B_ij = bh_bias[i * sq + j].
+ */
 static void attend_row(const uint16_t *qi, const uint16_t *kh, const uint16_t *vh,
+                       const uint16_t *bh_bias, int64_t i, int64_t sq,
                        int64_t Nk, int64_t d, int64_t dv, double scale,
                        double *s, double *o, double *lse)
 {
     row_scores(qi, kh, Nk, d, scale, s);
+    if (bh_bias) {   /* S = scale * Q K^T + B */
+        for (int64_t j = 0; j < Nk; j++)
+            s[j] += bf16_to_f64(bh_bias[i * sq + j]);
+    }
     double m = row_max(s, Nk);
     double l = row_exp_sum(s, Nk, m);
     /* step 4: weighted sum of value rows */
@@ -152,7 +161,7 @@ int attn_ref_rows_f64(const uint16_t *q, const uint16_t *k, const uint16_t *v,
             for (int64_t r = 0; r < nsel; r++) {
                 int64_t bh = sel[r] / Nq, i = sel[r] % Nq;
                 attend_row(q + (bh * Nq + i) * d, k + bh * Nk * d, v + bh * Nk * dv,
-                           Nk, d, dv, scale, s, o + r * dv, lse + r);
+                           NULL, i, 0, Nk, d, dv, scale, s, o + r * dv, lse + r);
             }
             free(s);
         }
@@ -204,7 +213,65 @@ int attn_ref_rows_causal_f64(const uint16_t *q, const uint16_t *k, const uint16_
                 int64_t bh = sel[r] / Nq, i = sel[r] % Nq;
                 int64_t visible = i + (Nk - Nq) + 1;   /* keys 0 .. i + Nk - Nq */
                 attend_row(q + (bh * Nq + i) * d, k + bh * Nk * d, v + bh * Nk * dv,
-                           visible, d, dv, scale, s, o + r * dv, lse + r);
+                           NULL, i, 0, visible, d, dv, scale, s, o + r * dv, lse + r);
+            }
+            free(s);
+        }
+    }
+    return failed ? REF_ENOMEM : REF_OK;
+}
+
+/*
+ * attn_ref_rows_bias_f64: O and LSE of selected rows with an additive bias.
+ *
+ * The definition's S = Q K^T / sqrt(d) + B, P = softmax_row(S), O = P V
+ * ("FlashAttention'ı Anlamak Bölüm 1", section 0.2 Notasyon), with the caller's scale
+ * in place of 1/sqrt(d) as above and B given per head as BF16 bit patterns:
+ *
+ *   B_ij of head (b, h) = bias[b * sb + h * sh + i * sq + j]     (strides in elements)
+ *
+ * A stride of 0 repeats the same values across batches, heads or query rows (sq = 0:
+ * one bias per key, e.g. a padding mask). An entry of -inf removes that key from the
+ * row (exp(-inf) = 0); a row whose entries are all -inf has no softmax, and its O and
+ * LSE come out NaN. H is the number of heads per batch (BH = B * H). Other arguments as
+ * attn_ref_rows_f64.
+ */
+int attn_ref_rows_bias_f64(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                           const uint16_t *bias, int64_t H, int64_t sb, int64_t sh, int64_t sq,
+                           int64_t BH, int64_t Nq, int64_t Nk, int64_t d, int64_t dv,
+                           double scale, const int64_t *sel, int64_t nsel,
+                           double *o, double *lse, int nthreads)
+{
+    if (BH < 0 || Nq < 0 || Nk < 1 || d < 1 || dv < 1 || nsel < 0) return REF_EINVAL;
+    if (H < 1 || BH % H != 0 || sb < 0 || sh < 0 || sq < 0) return REF_EINVAL;
+    if (nsel == 0) return REF_OK;
+    if (!q || !k || !v || !bias || !sel || !o || !lse) return REF_EINVAL;
+    for (int64_t r = 0; r < nsel; r++)
+        if (sel[r] < 0 || sel[r] >= BH * Nq) return REF_EINVAL;
+
+    int failed = 0;
+#ifdef _OPENMP
+    int nt = nthreads > 0 ? nthreads : omp_get_max_threads();
+#pragma omp parallel num_threads(nt)
+#else
+    (void)nthreads;
+#endif
+    {
+        double *s = (double *)malloc((size_t)Nk * sizeof(double));
+        if (!s) {
+#ifdef _OPENMP
+#pragma omp atomic write
+#endif
+            failed = 1;
+        } else {
+#ifdef _OPENMP
+#pragma omp for schedule(dynamic, 1)
+#endif
+            for (int64_t r = 0; r < nsel; r++) {
+                int64_t bh = sel[r] / Nq, i = sel[r] % Nq;
+                const uint16_t *bh_bias = bias + (bh / H) * sb + (bh % H) * sh;
+                attend_row(q + (bh * Nq + i) * d, k + bh * Nk * d, v + bh * Nk * dv,
+                           bh_bias, i, sq, Nk, d, dv, scale, s, o + r * dv, lse + r);
             }
             free(s);
         }

@@ -277,6 +277,105 @@ def test_causal_rejects_more_queries_than_keys():
         oracle.default().attention_rows_causal(q, k, v, 1.0)
 
 
+# ---- additive bias: S = scale * Q K^T + B ------------------------------------------------------
+
+NEG_INF_BF16 = np.uint16(0xFF80)
+
+
+def pin_bias_constant_per_row_moves_only_lse(orc):
+    # softmax is unchanged by adding c_i to every score of row i; the log-sum-exp grows by c_i
+    q, k, v = make_qkv(2, 2, 6, 6, d=16, seed=40)
+    c = np.array([0.5, -3.0, 2.25, 0.0, 7.5, -0.125], dtype=np.float32)
+    bias = np.broadcast_to(bf16(c)[None, None, :, None], (1, 1, 6, 6)).copy()
+    o0, l0 = orc.attention_rows(q, k, v, 0.6)
+    ob, lb = orc.attention_rows_bias(q, k, v, bias, 0.6)
+    assert np.max(np.abs(ob - o0)) < 1e-14
+    assert np.max(np.abs(lb - (l0 + np.tile(c.astype(np.float64), 4)))) < 1e-13
+
+
+def pin_bias_single_visible_key_per_row(orc):
+    # -inf everywhere but key j(i) = (2i + 1) mod 7: O_i = V_j(i) exactly, LSE_i = scale q_i.k_j(i) + B_i,j(i)
+    Nq = Nk = 7
+    q, k, v = make_qkv(1, 2, Nq, Nk, d=8, seed=41)
+    bias = np.full((1, 2, Nq, Nk), NEG_INF_BF16, dtype=np.uint16)
+    keep = [(2 * i + 1) % Nk for i in range(Nq)]
+    val = np.float32(0.75)
+    for i, j in enumerate(keep):
+        bias[0, :, i, j] = bf16([val])[0]
+    o, lse = orc.attention_rows_bias(q, k, v, bias, 0.4)
+    o, lse = o.reshape(2, Nq, 8), lse.reshape(2, Nq)
+    qw, kw, vw = widen(q), widen(k), widen(v)
+    for h in range(2):
+        for i, j in enumerate(keep):
+            assert np.array_equal(o[h, i], vw[0, h, j])
+            assert abs(lse[h, i] - (0.4 * float(np.dot(qw[0, h, i], kw[0, h, j])) + 0.75)) < 1e-12
+
+
+def pin_bias_causal_pattern_equals_the_causal_oracle(orc):
+    # 0 on and left of the bottom-right diagonal, -inf right of it: the causal oracle's mask
+    for Nq, Nk, seed in ((6, 6, 42), (4, 9, 43)):
+        q, k, v = make_qkv(2, 2, Nq, Nk, d=8, seed=seed)
+        full = np.zeros((1, 1, Nk, Nk), dtype=np.uint16)   # rows past Nq pad the buffer
+        for i in range(Nk):
+            full[0, 0, i, i + Nk - Nq + 1:] = NEG_INF_BF16
+        oc, lc = orc.attention_rows_causal(q, k, v, 0.9)
+        ob, lb = orc.attention_rows_bias(q, k, v, full[:, :, :Nq], 0.9)
+        assert np.max(np.abs(ob - oc)) < 1e-14 and np.max(np.abs(lb - lc)) < 1e-13
+
+
+def pin_bias_matches_high_precision_brute_force(orc):
+    # a bias that differs by row, key, head and batch, against exp(s + b) / sum exp(s + b) in 50 digits
+    mp = pytest.importorskip("mpmath")
+    mp.mp.dps = 50
+    B, H, N, d = 2, 2, 5, 4
+    q, k, v = make_qkv(B, H, N, N, d=d, seed=44)
+    rng = np.random.default_rng(45)
+    bias = f32_to_bf16_bits(rng.normal(0.0, 2.0, size=(B, H, N, N)).astype(np.float32))
+    o, lse = orc.attention_rows_bias(q, k, v, bias, 0.7)
+    o, lse = o.reshape(B, H, N, d), lse.reshape(B, H, N)
+    qw, kw, vw, bw = widen(q), widen(k), widen(v), widen(bias)
+    for b in range(B):
+        for h in range(H):
+            for i in range(N):
+                e = [mp.exp(mp.mpf(0.7) * mp.fsum(mp.mpf(float(x)) * mp.mpf(float(y)) for x, y in zip(qw[b, h, i], kw[b, h, j]))
+                            + mp.mpf(float(bw[b, h, i, j]))) for j in range(N)]
+                den = mp.fsum(e)
+                for c in range(d):
+                    assert abs(o[b, h, i, c] - float(mp.fsum(e[j] * mp.mpf(float(vw[b, h, j, c])) for j in range(N)) / den)) < 1e-13
+                assert abs(lse[b, h, i] - float(mp.log(den))) < 1e-12
+
+
+def pin_bias_broadcast_strides_equal_materialised_bias(orc):
+    # one [Nq, Nk] bias shared by every head and batch, and one bias per key, against the same
+    # values written out in full
+    q, k, v = make_qkv(2, 3, 5, 5, d=8, seed=46)
+    rng = np.random.default_rng(47)
+    shared = f32_to_bf16_bits(rng.normal(size=(1, 1, 5, 5)).astype(np.float32))
+    per_key = f32_to_bf16_bits(rng.normal(size=(1, 1, 1, 5)).astype(np.float32))
+    for small in (shared, per_key):
+        o1, l1 = orc.attention_rows_bias(q, k, v, small, 0.5)
+        # the full copy sits at the start of a buffer three times its size, so that an oracle
+        # with mixed-up strides reads spare memory rather than past the end
+        full = np.zeros((6, 3, 5, 5), dtype=np.uint16)
+        full[:2] = np.broadcast_to(small, (2, 3, 5, 5))
+        o2, l2 = orc.attention_rows_bias(q, k, v, full[:2], 0.5)
+        assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
+    # and a per-head bias really is per head: head 1 with head 0's bias differs
+    per_head = f32_to_bf16_bits(rng.normal(size=(1, 3, 5, 5)).astype(np.float32))
+    o3, _ = orc.attention_rows_bias(q, k, v, per_head, 0.5)
+    o4, _ = orc.attention_rows_bias(q, k, v, per_head[:, [0, 0, 0]].copy(), 0.5)
+    assert np.array_equal(o3.reshape(2, 3, 5, 8)[:, 0], o4.reshape(2, 3, 5, 8)[:, 0])
+    assert not np.array_equal(o3.reshape(2, 3, 5, 8)[:, 1], o4.reshape(2, 3, 5, 8)[:, 1])
+
+
+def test_bias_rejects_a_shape_that_does_not_broadcast():
+    q, k, v = make_qkv(1, 2, 4, 4, d=8, seed=48)
+    with pytest.raises(ValueError):
+        oracle.default().attention_rows_bias(q, k, v, np.zeros((1, 1, 4, 3), np.uint16), 1.0)
+    with pytest.raises(ValueError):
+        oracle.default().attention_rows_bias(q, k, v, np.zeros((1, 2, 2, 4), np.uint16), 1.0)
+
+
 PINS = [v for k_, v in sorted(globals().items()) if k_.startswith("pin_")]
 
 

@@ -26,6 +26,12 @@ MUTANTS = {
     "keys used as values": ("bf16_to_f64(vh[j * dv + c])", "bf16_to_f64(kh[j * d + c])"),
     "causal mask one key short": ("int64_t visible = i + (Nk - Nq) + 1;", "int64_t visible = i + (Nk - Nq) + (i > 0);"),
     "causal mask aligned top-left": ("int64_t visible = i + (Nk - Nq) + 1;", "int64_t visible = i + 1;"),
+    "bias ignored": ("s[j] += bf16_to_f64(bh_bias[i * sq + j]);", "s[j] += 0.0;"),
+    "bias inside the scale": ("s[j] += bf16_to_f64(bh_bias[i * sq + j]);",
+                              "s[j] += scale * bf16_to_f64(bh_bias[i * sq + j]);"),
+    "bias transposed": ("bh_bias[i * sq + j]", "bh_bias[j * sq + i]"),
+    "bias row stride dropped": ("bh_bias[i * sq + j]", "bh_bias[j]"),
+    "bias head and batch strides swapped": ("bias + (bh / H) * sb + (bh % H) * sh", "bias + (bh / H) * sh + (bh % H) * sb"),
 }
 
 
