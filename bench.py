@@ -16,6 +16,10 @@ overlap its neighbours' kernels.
 --causal times attn_fwd_causal instead (query i sees keys 0 .. i + Nk - Nq); its FLOPs
 count the visible (query, key) pairs only, 4*d each, and vs_baseline is null.
 
+--bias shared|full times attn_fwd_bias with a BF16 N(0,1) bias, one [Nq, Nk] matrix for
+every head or one per head; the FLOP count is unchanged (the bias adds one addend per
+score).
+
 --impl reference times the FP64 CPU oracle (the plain definition) on host cores, on a
 bounded sample of query rows per step.
 """
@@ -59,6 +63,8 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="target CPU time of the oracle sample")
     ap.add_argument("--causal", action="store_true",
                     help="causal mask (query i sees keys 0 .. i + Nk - Nq); FLOPs count visible pairs only")
+    ap.add_argument("--bias", choices=["none", "shared", "full"], default="none",
+                    help="additive BF16 bias N(0,1): one [Nq, Nk] matrix for all heads, or one per head")
     return ap.parse_args()
 
 
@@ -154,7 +160,16 @@ def workload_flops(w, causal: bool) -> float:
 
 # ------------------------------------------------------------------ reference arm (oracle) ---
 
-def cpu_oracle_sample(w, target_seconds: float, rank_seed: int = 0, causal: bool = False):
+def oracle_rows_fn(oracle, w, causal: bool, bias_kind: str, H1: int, nq: int):
+    """The oracle entry point for this run's variant, as fn(q, k, v, scale, rows)."""
+    if bias_kind != "none":
+        from dense_attention_forward_fwd_gb300.inputs import make_bias
+        bias = make_bias((1, 1, nq, w.Nk) if bias_kind == "shared" else (1, H1, nq, w.Nk), seed=w.seed + 1)
+        return lambda q, k, v, scale, rows: oracle.attention_rows_bias(q, k, v, bias, scale, rows)
+    return oracle.attention_rows_causal if causal else oracle.attention_rows
+
+
+def cpu_oracle_sample(w, target_seconds: float, rank_seed: int = 0, causal: bool = False, bias_kind: str = "none"):
     """Time the FP64 oracle on a sample of query rows; returns (TFLOPS, rows, seconds, threads)."""
     import numpy as np
 
@@ -167,7 +182,7 @@ def cpu_oracle_sample(w, target_seconds: float, rank_seed: int = 0, causal: bool
     nq = min(w.Nq, 4096)
     q, k, v = make_qkv(1, H1, nq, w.Nk, d=w.d, seed=w.seed + rank_seed, qk_mult=w.qk_mult)
     threads = oracle.max_threads()
-    fn = oracle.attention_rows_causal if causal else oracle.attention_rows
+    fn = oracle_rows_fn(oracle, w, causal, bias_kind, H1, nq)
 
     def flop_rows(rows):   # 4*d FLOPs per visible key of each sampled row
         if not causal:
@@ -206,7 +221,7 @@ def run_reference(args, w):
     q, k, v = make_qkv(1, H1, nq, w.Nk, d=w.d, seed=w.seed, qk_mult=w.qk_mult)
     threads = oracle.max_threads()
     n_rows_total = q.shape[1] * q.shape[2]
-    fn = oracle.attention_rows_causal if args.causal else oracle.attention_rows
+    fn = oracle_rows_fn(oracle, w, args.causal, args.bias, H1, nq)
 
     def flop_rows(rows):   # 4*d FLOPs per visible key; causal sample rows sit at the end of the sequence
         if not args.causal:
@@ -235,7 +250,7 @@ def run_reference(args, w):
         "impl": "reference", "metric": METRIC, "value": tflops, "unit": "TFLOP/s", "n_gpus": world,
         "steps": steps, "warmup": warm, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": w.name, "B": w.B, "H": w.H, "Nq": w.Nq, "Nk": w.Nk, "d": w.d, "causal": args.causal,
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "Nq": w.Nq, "Nk": w.Nk, "d": w.d, "causal": args.causal, "bias": args.bias,
                    "qk_mult": w.qk_mult},
         "cpu_baseline": {"value": tflops, "unit": "TFLOP/s", "cores": threads, "kind": "oracle", "sample": sample},
         "e2e": {"value": tflops, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -278,11 +293,25 @@ def run_ours(args, w):
     flush = torch.empty(L2_FLUSH_BYTES // 4, device=dev, dtype=torch.int32)
     stream = torch.cuda.current_stream(dev)
 
-    fwd = attn.attn_fwd_causal if args.causal else attn.attn_fwd
+    if args.causal and args.bias != "none":
+        raise SystemExit("--causal and --bias are separate entry points; pick one")
+    ins = [q, k, v]
+    if args.bias != "none":
+        bshape = (1, 1, w.Nq, w.Nk) if args.bias == "shared" else (w.B, w.H, w.Nq, w.Nk)
+        ins.append(torch.randn(bshape, device=dev, generator=g).to(torch.bfloat16))
+
+    def fwd(ins_, o_, lse_, st):
+        if args.bias != "none":
+            attn.attn_fwd_bias(ins_[0], ins_[1], ins_[2], ins_[3], o_, lse_, w.B, w.H, w.Nq, w.Nk, w.d, w.scale, st)
+        elif args.causal:
+            attn.attn_fwd_causal(*ins_, o_, lse_, w.B, w.H, w.Nq, w.Nk, w.d, w.scale, st)
+        else:
+            attn.attn_fwd(*ins_, o_, lse_, w.B, w.H, w.Nq, w.Nk, w.d, w.scale, st)
+
     flops = workload_flops(w, args.causal)
 
     def step():
-        fwd(q, k, v, o, lse, w.B, w.H, w.Nq, w.Nk, w.d, w.scale, stream)
+        fwd(ins, o, lse, stream)
 
     sampler = ClockSampler(local_rank)   # started early: nvidia-smi needs a moment to come up
     time.sleep(1.0)
@@ -315,13 +344,13 @@ def run_ours(args, w):
     if status != attn.ATTN_OK:
         raise RuntimeError(f"kernel status {attn.attn_status_string(status)}")
 
-    # e2e through host buffers: every step copies its Q, K, V from pinned host memory,
-    # calls attn_fwd and copies O and LSE back, all inside the timed region. Steps are
-    # pipelined over three streams with two device buffer sets, as a serving loop would
-    # run them: the H2D of step i+1 and the D2H of step i-1 overlap the kernel of step i.
-    hq, hk, hv = (t.cpu().pin_memory() for t in (q, k, v))
+    # e2e through host buffers: every step copies its Q, K, V (and bias) from pinned host
+    # memory, calls the entry point and copies O and LSE back, all inside the timed region.
+    # Steps are pipelined over three streams with two device buffer sets, as a serving loop
+    # would run them: the H2D of step i+1 and the D2H of step i-1 overlap the kernel of step i.
+    h_ins = [t.cpu().pin_memory() for t in ins]
     ho, hl = torch.empty_like(o, device="cpu").pin_memory(), torch.empty_like(lse, device="cpu").pin_memory()
-    bufs = [tuple(torch.empty_like(t) for t in (q, k, v, o, lse)) for _ in range(2)]
+    bufs = [([torch.empty_like(t) for t in ins], torch.empty_like(o), torch.empty_like(lse)) for _ in range(2)]
     s_in, s_run, s_out = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
     ev_in = [torch.cuda.Event() for _ in range(2)]
     ev_done = [torch.cuda.Event() for _ in range(2)]
@@ -332,16 +361,15 @@ def run_ours(args, w):
     def e2e_steps(n):
         for i in range(n):
             b = i % 2
-            dq, dk, dv, do, dl = bufs[b]
+            d_ins, do, dl = bufs[b]
             s_in.wait_event(ev_done[b])                  # the kernel that read buffer set b is done
             with torch.cuda.stream(s_in):
-                dq.copy_(hq, non_blocking=True)
-                dk.copy_(hk, non_blocking=True)
-                dv.copy_(hv, non_blocking=True)
+                for dst, src in zip(d_ins, h_ins):
+                    dst.copy_(src, non_blocking=True)
                 ev_in[b].record(s_in)
             s_run.wait_event(ev_in[b])
             s_run.wait_event(ev_out[b])                  # this output set has been copied out
-            fwd(dq, dk, dv, do, dl, w.B, w.H, w.Nq, w.Nk, w.d, w.scale, s_run)
+            fwd(d_ins, do, dl, s_run)
             ev_done[b].record(s_run)
             s_out.wait_event(ev_done[b])
             with torch.cuda.stream(s_out):
@@ -367,7 +395,7 @@ def run_ours(args, w):
     # the last step's result, read back to the host, must be the device-timed leg's result
     if not (torch.equal(ho, o.cpu()) and torch.equal(hl, lse.cpu())):
         raise RuntimeError("end-to-end output differs from the device-resident run")
-    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv))
+    h2d = sum(t.numel() * t.element_size() for t in h_ins)
     d2h = ho.numel() * ho.element_size() + hl.numel() * hl.element_size()
 
     # max over ranks
@@ -384,16 +412,18 @@ def run_ours(args, w):
     achieved = flops / (ms * 1e-3) / 1e12   # one launch on one GPU
     traffic = None
     if os.path.exists(TRAFFIC_FILE):
-        rec = json.load(open(TRAFFIC_FILE)).get(w.name + ("-causal" if args.causal else ""))
+        key = w.name + ("-causal" if args.causal else "") + ("" if args.bias == "none" else "-bias-" + args.bias)
+        rec = json.load(open(TRAFFIC_FILE)).get(key)
         if rec and rec.get("kernel_hash") == kernel_hash():
             traffic = rec.get("bytes_per_launch")
 
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": (value / PAGES_TFLOPS[w.name]) if w.name in PAGES_TFLOPS and not args.causal else None,
+        "vs_baseline": ((value / PAGES_TFLOPS[w.name])
+                        if w.name in PAGES_TFLOPS and not args.causal and args.bias == "none" else None),
         "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": w.name, "B": w.B, "H": w.H, "Nq": w.Nq, "Nk": w.Nk, "d": w.d, "causal": args.causal,
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "Nq": w.Nq, "Nk": w.Nk, "d": w.d, "causal": args.causal, "bias": args.bias,
                    "qk_mult": w.qk_mult, "inputs": "iid N(0,1) BF16 (Q,K x qk_mult)",
                    "l2": "flushed (512 MiB write) before every timed launch",
                    "vs_baseline_ref": "RTX 5090 v5 kernel, same shape (other hardware: context only)"},
@@ -406,7 +436,7 @@ def run_ours(args, w):
         "kernel_ms_min": min(durs), "kernel_ms_median": statistics.median(durs),
     }
     if rank == 0 and not args.no_cpu_baseline:
-        tfl, n, dt, thr = cpu_oracle_sample(w, args.cpu_seconds, causal=args.causal)
+        tfl, n, dt, thr = cpu_oracle_sample(w, args.cpu_seconds, causal=args.causal, bias_kind=args.bias)
         keys = "visible keys of each row, causal" if args.causal else "full Nk each"
         line["cpu_baseline"] = {"value": tfl, "unit": "TFLOP/s", "cores": thr, "kind": "oracle",
                                 "sample": f"{n} query rows of {w.describe()} ({keys}), FP64, {dt:.1f} s"}

@@ -15,7 +15,7 @@ from ._build import LIB_PATH, build_library
 
 __all__ = [
     "ATTN_OK", "ATTN_ERR_INVALID_ARG", "ATTN_ERR_UNSUPPORTED", "ATTN_ERR_MISALIGNED", "ATTN_ERR_CUDA",
-    "ATTN_ERR_TIMEOUT", "AttnError", "load_library", "attn_fwd", "attn_fwd_causal", "attn_fwd_noalloc", "attn_fwd_status", "attn_status_string",
+    "ATTN_ERR_TIMEOUT", "AttnError", "load_library", "attn_fwd", "attn_fwd_causal", "attn_fwd_bias", "attn_fwd_noalloc", "attn_fwd_status", "attn_status_string",
     "attn_fwd_set_wait_limit", "attn_fwd_kernel_count", "attention",
 ]
 
@@ -48,6 +48,8 @@ def load_library(build_if_stale: bool = True) -> ctypes.CDLL:
             lib.attn_fwd.restype = i32
             lib.attn_fwd_noalloc.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, f32, vp]
             lib.attn_fwd_causal.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, f32, vp]
+            i64 = ctypes.c_longlong
+            lib.attn_fwd_bias.argtypes = [vp, vp, vp, vp, i64, i64, i64, vp, vp, i32, i32, i32, i32, i32, f32, vp]
             lib.attn_fwd_noalloc.restype = i32
             lib.attn_fwd_status.argtypes = [vp]
             lib.attn_fwd_status.restype = i32
@@ -130,6 +132,47 @@ def attn_fwd_causal(q, k, v, o, lse, B: int, H: int, Nq: int, Nk: int, d: int, s
                              _stream_handle(stream, q, k, v, o, lse))
     if rc != ATTN_OK:
         raise AttnError(rc, "attn_fwd_causal")
+
+
+def attn_fwd_bias(q, k, v, bias, o, lse, B: int, H: int, Nq: int, Nk: int, d: int, scale: float, stream=None,
+                  bias_strides=None) -> None:
+    """Like :func:`attn_fwd`, with an additive bias: S = scale * Q K^T + bias.
+
+    ``bias`` is a BF16 CUDA tensor of shape (Bb, Hb, Nqb, Nk), Bb in {1, B}, Hb in {1, H},
+    Nqb in {1, Nq}, with unit stride over keys; a dimension of size 1 (or of stride 0, as
+    from ``expand``) is shared. Its element strides are passed as they are, or given as
+    ``bias_strides`` = (stride_b, stride_h, stride_q) when ``bias`` is an integer pointer.
+    Entries of -inf remove keys; see include/attn_fwd.h for the rules.
+    """
+    lib = load_library()
+    if _is_tensor(bias):
+        import torch
+        if not bias.is_cuda or bias.dtype != torch.bfloat16:
+            raise TypeError("bias must be a BF16 CUDA tensor")
+        if bias.dim() != 4 or bias.shape[3] != Nk or bias.stride(3) != 1:
+            raise ValueError("bias must be (Bb, Hb, Nqb, Nk) with unit stride over keys")
+        Bb, Hb, Nqb, _ = bias.shape
+        if Bb not in (1, B) or Hb not in (1, H) or Nqb not in (1, Nq):
+            raise ValueError(f"bias shape {tuple(bias.shape)} does not broadcast to {(B, H, Nq, Nk)}")
+        if bias_strides is None:
+            bias_strides = tuple(bias.stride(i) if n > 1 else 0 for i, n in enumerate((Bb, Hb, Nqb)))
+        bptr = bias.data_ptr()
+    elif isinstance(bias, int):
+        if bias_strides is None:
+            raise ValueError("bias_strides are needed with an integer bias pointer")
+        bptr = bias
+    else:
+        raise TypeError(f"bias: expected a torch tensor or an integer device pointer, got {type(bias).__name__}")
+    sb, sh, sq = (int(x) for x in bias_strides)
+    args = (
+        _ptr(q, "q", B * H * Nq * d, "bf16"), _ptr(k, "k", B * H * Nk * d, "bf16"),
+        _ptr(v, "v", B * H * Nk * d, "bf16"), bptr, sb, sh, sq, _ptr(o, "o", B * H * Nq * d, "bf16"),
+        _ptr(lse, "lse", B * H * Nq, "f32"),
+    )
+    rc = lib.attn_fwd_bias(*args, int(B), int(H), int(Nq), int(Nk), int(d), float(scale),
+                           _stream_handle(stream, q, k, v, o, lse))
+    if rc != ATTN_OK:
+        raise AttnError(rc, "attn_fwd_bias")
 
 
 def attn_fwd_noalloc(q, k, v, o, lse, B: int, H: int, Nq: int, Nk: int, d: int, scale: float, stream=None) -> None:

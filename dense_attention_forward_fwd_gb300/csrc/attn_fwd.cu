@@ -143,6 +143,12 @@ struct Params {
   int causal;             // query i sees keys 0 .. i + causal_off only (causal_off = Nk - Nq >= 0)
   int causal_off;
   int bh_count;           // B * H
+  // additive bias (kernels instantiated with kBias): B_ij of head (b, h) is
+  // bias[b * bias_sb + h * bias_sh + i * bias_sq + j], BF16, strides in elements
+  const uint16_t* bias;
+  long long bias_sb, bias_sh, bias_sq;
+  int H;                  // heads per batch (splits b*H + h)
+  float scale;            // the caller's scale (the bias path scales before adding B)
 };
 
 // floor(a / b) for a >= 0, b > 0. On the device a 64-bit division is a long dependent
@@ -354,6 +360,17 @@ __device__ __forceinline__ void tmem_ld128(uint32_t taddr, uint32_t (&x)[128]) {
       : "r"(taddr)
       : "memory");
 }
+// 64 TMEM columns of this warp's 32 lanes; the load is only issued here and completes
+// at tmem_wait_ld64, which takes the same registers so that no use is scheduled before it
+__device__ __forceinline__ void tmem_ld64_issue(uint32_t taddr, uint32_t (&x)[64]) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x64.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32, %33, %34, %35, %36, %37, %38, %39, %40, %41, %42, %43, %44, %45, %46, %47, %48, %49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, %60, %61, %62, %63}, [%64];"
+               : "=r"(x[0]), "=r"(x[1]), "=r"(x[2]), "=r"(x[3]), "=r"(x[4]), "=r"(x[5]), "=r"(x[6]), "=r"(x[7]), "=r"(x[8]), "=r"(x[9]), "=r"(x[10]), "=r"(x[11]), "=r"(x[12]), "=r"(x[13]), "=r"(x[14]), "=r"(x[15]), "=r"(x[16]), "=r"(x[17]), "=r"(x[18]), "=r"(x[19]), "=r"(x[20]), "=r"(x[21]), "=r"(x[22]), "=r"(x[23]), "=r"(x[24]), "=r"(x[25]), "=r"(x[26]), "=r"(x[27]), "=r"(x[28]), "=r"(x[29]), "=r"(x[30]), "=r"(x[31]), "=r"(x[32]), "=r"(x[33]), "=r"(x[34]), "=r"(x[35]), "=r"(x[36]), "=r"(x[37]), "=r"(x[38]), "=r"(x[39]), "=r"(x[40]), "=r"(x[41]), "=r"(x[42]), "=r"(x[43]), "=r"(x[44]), "=r"(x[45]), "=r"(x[46]), "=r"(x[47]), "=r"(x[48]), "=r"(x[49]), "=r"(x[50]), "=r"(x[51]), "=r"(x[52]), "=r"(x[53]), "=r"(x[54]), "=r"(x[55]), "=r"(x[56]), "=r"(x[57]), "=r"(x[58]), "=r"(x[59]), "=r"(x[60]), "=r"(x[61]), "=r"(x[62]), "=r"(x[63])
+               : "r"(taddr)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_wait_ld64(uint32_t (&x)[64]) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" : "+r"(x[0]), "+r"(x[1]), "+r"(x[2]), "+r"(x[3]), "+r"(x[4]), "+r"(x[5]), "+r"(x[6]), "+r"(x[7]), "+r"(x[8]), "+r"(x[9]), "+r"(x[10]), "+r"(x[11]), "+r"(x[12]), "+r"(x[13]), "+r"(x[14]), "+r"(x[15]), "+r"(x[16]), "+r"(x[17]), "+r"(x[18]), "+r"(x[19]), "+r"(x[20]), "+r"(x[21]), "+r"(x[22]), "+r"(x[23]), "+r"(x[24]), "+r"(x[25]), "+r"(x[26]), "+r"(x[27]), "+r"(x[28]), "+r"(x[29]), "+r"(x[30]), "+r"(x[31]), "+r"(x[32]), "+r"(x[33]), "+r"(x[34]), "+r"(x[35]), "+r"(x[36]), "+r"(x[37]), "+r"(x[38]), "+r"(x[39]), "+r"(x[40]), "+r"(x[41]), "+r"(x[42]), "+r"(x[43]), "+r"(x[44]), "+r"(x[45]), "+r"(x[46]), "+r"(x[47]), "+r"(x[48]), "+r"(x[49]), "+r"(x[50]), "+r"(x[51]), "+r"(x[52]), "+r"(x[53]), "+r"(x[54]), "+r"(x[55]), "+r"(x[56]), "+r"(x[57]), "+r"(x[58]), "+r"(x[59]), "+r"(x[60]), "+r"(x[61]), "+r"(x[62]), "+r"(x[63]) : : "memory");
+}
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&x)[32]) {
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];\n\t"
@@ -411,6 +428,112 @@ __device__ __forceinline__ void fma2(float& y0, float& y1, float x0, float x1, f
       "mov.b64 {%0, %1}, y;\n\t}"
       : "=f"(y0), "=f"(y1)
       : "f"(x0), "f"(x1), "f"(a), "f"(b));
+}
+// (y0, y1) = (x0, x1) * a + (b0, b1) as one packed FP32x2 FMA
+__device__ __forceinline__ void fma2v(float& y0, float& y1, float x0, float x1, float a, float b0, float b1) {
+  asm("{\n\t.reg .b64 x, a, b, y;\n\t"
+      "mov.b64 x, {%2, %3};\n\t"
+      "mov.b64 a, {%4, %4};\n\t"
+      "mov.b64 b, {%5, %6};\n\t"
+      "fma.rn.f32x2 y, x, a, b;\n\t"
+      "mov.b64 {%0, %1}, y;\n\t}"
+      : "=f"(y0), "=f"(y1)
+      : "f"(x0), "f"(x1), "f"(a), "f"(b0), "f"(b1));
+}
+// 16 bytes of read-only data, not kept in L1 (little of it is left beside shared memory)
+__device__ __forceinline__ uint4 ld_nc_v4(const void* ptr) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(ptr));
+  return v;
+}
+// The bias of a warp's 32 query rows for keys k0 .. k0 + 127, read with coalesced
+// 16-byte loads: load i of half h covers rows 4i .. 4i + 3 of the warp, eight lanes per
+// row, each lane 8 keys (lane >> 3 picks the row, lane & 7 the 8 keys), so one load
+// instruction touches four 128-byte lines. g[32h + 4i .. 32h + 4i + 3] receives the
+// lane's piece. BiasRows holds what stays fixed over a segment: `piece` points at the
+// lane's first piece (row row0 + (lane >> 3), keys from 8 (lane & 7)), `s4` is four rows.
+struct BiasRows {
+  const uint16_t* piece;
+  long long sq, s4;
+  int row0;
+  bool rows_full;   // all 32 rows of the warp lie inside the sequence (warp-uniform)
+};
+// Rows at or past Nq and keys at or past Nk read nothing and get 0 (those scores are
+// masked or never stored); a piece that straddles Nk is read key by key.
+__device__ __forceinline__ void load_bias_pieces(uint32_t (&g)[64], const BiasRows& br, int Nq, int k0, int Nk) {
+  if (br.rows_full && k0 + kBN <= Nk) {   // warp-uniform: every piece is in range
+    const uint16_t* src = br.piece + k0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const uint4 t0 = ld_nc_v4(src + i * br.s4);
+      const uint4 t1 = ld_nc_v4(src + i * br.s4 + 64);
+      g[4 * i] = t0.x;
+      g[4 * i + 1] = t0.y;
+      g[4 * i + 2] = t0.z;
+      g[4 * i + 3] = t0.w;
+      g[32 + 4 * i] = t1.x;
+      g[32 + 4 * i + 1] = t1.y;
+      g[32 + 4 * i + 2] = t1.z;
+      g[32 + 4 * i + 3] = t1.w;
+    }
+    return;
+  }
+  const int lane = threadIdx.x & 31;
+  const int sub = lane >> 3, cc = lane & 7;
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int row = br.row0 + 4 * i + sub;
+      const int key = k0 + 64 * h + 8 * cc;
+      uint4 t = make_uint4(0u, 0u, 0u, 0u);
+      if (row < Nq) {
+        const uint16_t* src = br.piece + i * br.s4 + k0 + 64 * h;
+        if (key + 8 <= Nk) {
+          t = ld_nc_v4(src);
+        } else if (key < Nk) {
+          uint32_t w[4];
+#pragma unroll
+          for (int m = 0; m < 4; ++m) {
+            const uint32_t lo = key + 2 * m < Nk ? src[2 * m] : 0u;
+            const uint32_t hi = key + 2 * m + 1 < Nk ? src[2 * m + 1] : 0u;
+            w[m] = lo | (hi << 16);
+          }
+          t = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+      }
+      g[32 * h + 4 * i] = t.x;
+      g[32 * h + 4 * i + 1] = t.y;
+      g[32 * h + 4 * i + 2] = t.z;
+      g[32 * h + 4 * i + 3] = t.w;
+    }
+  }
+}
+// Half h of the pieces above, transposed through the warp's 4 KB staging tile: b[w]
+// receives this lane's row, keys 64h + 2w (low half) and 64h + 2w + 1. The 16-byte
+// chunks are swizzled by row, so both the writes and the reads are free of bank conflicts.
+__device__ __forceinline__ void bias_half_to_row(uint8_t* stage, const uint32_t (&g)[64], int h, uint32_t (&b)[32]) {
+  const int lane = threadIdx.x & 31;
+  const int sub = lane >> 3, cc = lane & 7;
+  uint4* st = reinterpret_cast<uint4*>(stage);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int rr = 4 * i + sub;
+    st[rr * 8 + (cc ^ (rr & 7))] =
+        make_uint4(g[32 * h + 4 * i], g[32 * h + 4 * i + 1], g[32 * h + 4 * i + 2], g[32 * h + 4 * i + 3]);
+  }
+  __syncwarp();
+#pragma unroll
+  for (int c = 0; c < 8; ++c) {
+    const uint4 v = st[lane * 8 + (c ^ (lane & 7))];
+    b[4 * c] = v.x;
+    b[4 * c + 1] = v.y;
+    b[4 * c + 2] = v.z;
+    b[4 * c + 3] = v.w;
+  }
+  __syncwarp();   // the tile is written again by the next half
 }
 // (a0, a1) += (x0, x1) as one packed FP32x2 add
 __device__ __forceinline__ void add2(float& a0, float& a1, float x0, float x1) {
@@ -700,18 +823,22 @@ __device__ void merge_split_row(const Params& p, int tile, int r, int c_first, i
            static_cast<size_t>(tile) * kPartFloatsPerTile;
   };
   constexpr int kM = kD * kBM, kL = kM + kBM, kC = kL + kBM;
-  float M = self >= 0 ? own_m : -INFINITY;
-  for (int cs = c_first; cs <= c_last; ++cs)
-    if (cs != self) M = fmaxf(M, __ldcg(record(cs) + kM + r));
-  const float w_own = self >= 0 ? ex2(own_m - M) : 0.0f;
-  float L = own_l * w_own, Lr = (own_l + own_corr) * w_own;
+  // Every sum runs over the shares in share order, the merging block's own share in its
+  // place, so the result does not depend on which block happened to finish last.
+  float M = -INFINITY;
+  for (int cs = c_first; cs <= c_last; ++cs) M = fmaxf(M, cs == self ? own_m : __ldcg(record(cs) + kM + r));
+  float L = 0.0f, Lr = 0.0f;
   for (int cs = c_first; cs <= c_last; ++cs) {
-    if (cs == self) continue;
-    const float* rec = record(cs);
-    const float w = ex2(__ldcg(rec + kM + r) - M);
-    const float l_s = __ldcg(rec + kL + r);
+    float m_s = own_m, l_s = own_l, c_s = own_corr;
+    if (cs != self) {
+      const float* rec = record(cs);
+      m_s = __ldcg(rec + kM + r);
+      l_s = __ldcg(rec + kL + r);
+      c_s = __ldcg(rec + kC + r);
+    }
+    const float w = ex2(m_s - M);
     L += l_s * w;
-    Lr += (l_s + __ldcg(rec + kC + r)) * w;
+    Lr += (l_s + c_s) * w;
   }
   const float inv = 1.0f / Lr;
   // Two 64-column halves; per half and share, the share's max and its 64 values are
@@ -719,31 +846,31 @@ __device__ void merge_split_row(const Params& p, int tile, int r, int c_first, i
 #pragma unroll 1
   for (int h = 0; h < 2; ++h) {
     float acc[64];
-    if (self >= 0) {   // warp-uniform
 #pragma unroll
-      for (int cc = 0; cc < 2; ++cc) {
-        uint32_t ov[32];
-        tmem_ld32(own_tO + (2 * h + cc) * 32, ov);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) acc[32 * cc + i] = __uint_as_float(ov[i]) * w_own;
-      }
-    } else {
-#pragma unroll
-      for (int i = 0; i < 64; ++i) acc[i] = 0.0f;
-    }
+    for (int i = 0; i < 64; ++i) acc[i] = 0.0f;
     for (int cs = c_first; cs <= c_last; ++cs) {
-      if (cs == self) continue;
-      const float* rec = record(cs);
-      const float m_s = __ldcg(rec + kM + r);
       float v[64];
-      const float4* rec4 = reinterpret_cast<const float4*>(rec);
+      float m_s = own_m;
+      if (cs == self) {   // warp-uniform: the TMEM loads below are .sync.aligned
 #pragma unroll
-      for (int g = 0; g < 16; ++g) {
-        const float4 t = __ldcg(rec4 + (h * 16 + g) * kBM + r);
-        v[4 * g] = t.x;
-        v[4 * g + 1] = t.y;
-        v[4 * g + 2] = t.z;
-        v[4 * g + 3] = t.w;
+        for (int cc = 0; cc < 2; ++cc) {
+          uint32_t ov[32];
+          tmem_ld32(own_tO + (2 * h + cc) * 32, ov);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[32 * cc + i] = __uint_as_float(ov[i]);
+        }
+      } else {
+        const float* rec = record(cs);
+        m_s = __ldcg(rec + kM + r);
+        const float4* rec4 = reinterpret_cast<const float4*>(rec);
+#pragma unroll
+        for (int g = 0; g < 16; ++g) {
+          const float4 t = __ldcg(rec4 + (h * 16 + g) * kBM + r);
+          v[4 * g] = t.x;
+          v[4 * g + 1] = t.y;
+          v[4 * g + 2] = t.z;
+          v[4 * g + 3] = t.w;
+        }
       }
       const float w = ex2(m_s - M);
 #pragma unroll
@@ -757,7 +884,7 @@ __device__ void merge_split_row(const Params& p, int tile, int r, int c_first, i
   if (lse_out != nullptr) *lse_out = (M + log2f(L)) * 0.69314718055994531f;
 }
 
-template <bool kPosScale>
+template <bool kPosScale, bool kBias>
 __device__ void run_softmax(const Ctl& c, uint32_t tmem, uint8_t* stage, const Params& p, int tile) {
   const int quarter = (threadIdx.x >> 5) & 3;   // TMEM lanes this warp may access
   const int lane = threadIdx.x & 31;
@@ -765,7 +892,8 @@ __device__ void run_softmax(const Ctl& c, uint32_t tmem, uint8_t* stage, const P
   const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
   const uint32_t tS = tmem + lane_off + tile * 128;
   const uint32_t tO = tmem + lane_off + 256 + tile * 128;
-  const float cs = kPosScale ? p.scale_log2 : 1.0f;   // factor still to apply to s
+  // factor still to apply to s: with a bias, s already holds scale * q.k + B in natural units
+  const float cs = kBias ? 1.4426950408889634f : (kPosScale ? p.scale_log2 : 1.0f);
 
   uint32_t gstep = 0;   // K/V steps of all previous segments: phase of s_full / p_full
   int u = 0;            // segments finished
@@ -790,21 +918,53 @@ __device__ void run_softmax(const Ctl& c, uint32_t tmem, uint8_t* stage, const P
     float m_used = -INFINITY;   // log2 units
     float l = 0.0f;             // sum of 2^(s*cs - m_used) in FP32
     float corr = 0.0f;          // BF16 rounding error of the largest term of each tile
+    // bias of this warp's rows: each step's tile is loaded before the wait for its scores,
+    // so the loads overlap that wait
+    BiasRows br;
+    uint32_t bg[kBias ? 64 : 1];
+    if constexpr (kBias) {
+      const int bh = sg.group / p.q_groups;
+      br.row0 = seg_row0;
+      br.rows_full = seg_row0 + 32 <= p.Nq;
+      br.sq = p.bias_sq;
+      br.s4 = 4 * p.bias_sq;
+      br.piece = p.bias + static_cast<long long>(bh / p.H) * p.bias_sb + static_cast<long long>(bh % p.H) * p.bias_sh +
+                 static_cast<long long>(seg_row0 + (lane >> 3)) * p.bias_sq + 8 * (lane & 7);
+    }
     for (int j = 0; j < n; ++j) {
+      if constexpr (kBias) load_bias_pieces(bg, br, p.Nq, (sg.kv0 + j) * kBN, p.Nk);
       if (!wait_warp(c, kBarSFull + tile, (gstep + static_cast<uint32_t>(j)) & 1u)) return;
       if (releaser) mbar_arrive(c.bar(kBarKVEmpty + (unit + j) % kPairs));
       const int ring_unit = unit + j + 1;
       const bool ring_seen = ringer && mbar_test_wait(c.bar(kBarKVFull + ring_unit % kPairs), (ring_unit / kPairs) & 1);
       __syncwarp();   // lane 0 alone may have run the two lines above; tcgen05.ld is .sync.aligned
       tc_fence_after();
-      uint32_t x[128];
-      tmem_ld128(tS, x);
       float s[128];
+      if constexpr (kBias) {
+        // s = scale * q.k + B, one 64-key half at a time
 #pragma unroll
-      for (int i = 0; i < 128; ++i) s[i] = __uint_as_float(x[i]);
-      if (!kPosScale) {
+        for (int h = 0; h < 2; ++h) {
+          uint32_t x[64];
+          tmem_ld64_issue(tS + h * 64, x);   // completes while the bias half is transposed
+          uint32_t b[32];
+          bias_half_to_row(stage, bg, h, b);
+          tmem_wait_ld64(x);
 #pragma unroll
-        for (int i = 0; i < 128; ++i) s[i] *= p.scale_log2;
+          for (int i = 0; i < 32; ++i) {
+            const uint32_t b2 = b[i];
+            fma2v(s[h * 64 + 2 * i], s[h * 64 + 2 * i + 1], __uint_as_float(x[2 * i]), __uint_as_float(x[2 * i + 1]),
+                  p.scale, __uint_as_float(b2 << 16), __uint_as_float(b2 & 0xffff0000u));
+          }
+        }
+      } else {
+        uint32_t x[128];
+        tmem_ld128(tS, x);
+#pragma unroll
+        for (int i = 0; i < 128; ++i) s[i] = __uint_as_float(x[i]);
+        if (!kPosScale) {
+#pragma unroll
+          for (int i = 0; i < 128; ++i) s[i] *= p.scale_log2;
+        }
       }
       if (sg.kv0 + j == p.n_kv - 1 && p.kv_tail < kBN) {
         const int valid = p.kv_tail;
@@ -858,13 +1018,14 @@ __device__ void run_softmax(const Ctl& c, uint32_t tmem, uint8_t* stage, const P
       // rounding error, so that l + corr is the sum of the weights the tensor core
       // actually applies to V (up to the far smaller errors of the other terms).
       {
-        const float pm = ex2(m_tile - m_used);
+        // (with a bias a row may have seen only -inf so far: its largest term is then 0)
+        const float pm = (kBias && m_tile == -INFINITY) ? 0.0f : ex2(m_tile - m_used);
         corr += __uint_as_float(pack_bf16(pm, 0.0f) << 16) - pm;
       }
       // p = 2^(s*cs - m) in two halves of 64 keys; each half is rounded to BF16, stored
       // over S in TMEM and handed to the MMA warp at once, so the first half of the
       // P V product runs while the second half is computed.
-      const float neg_m = -m_used;
+      const float neg_m = (kBias && m_used == -INFINITY) ? 0.0f : -m_used;   // every p is 0 then
       float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
@@ -984,7 +1145,7 @@ __device__ void run_softmax(const Ctl& c, uint32_t tmem, uint8_t* stage, const P
 // ---------------------------------------------------------------------------------
 // Kernel
 // ---------------------------------------------------------------------------------
-template <bool kPosScale>
+template <bool kPosScale, bool kBias>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const Params p) {
@@ -1050,7 +1211,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsSoftmax));
-    run_softmax<kPosScale>(c, tmem, smem + kOffStage + (warp - 4) * kStageBytes, p, (warp >> 2) - 1);
+    run_softmax<kPosScale, kBias>(c, tmem, smem + kOffStage + (warp - 4) * kStageBytes, p, (warp >> 2) - 1);
   }
 
   tc_fence_before();
@@ -1099,7 +1260,7 @@ bool make_map(CUtensorMap* map, const void* ptr, int rows, long long bh) {
 }
 
 constexpr int kMaxDevices = 64;
-std::atomic<int> g_attr_done[2][kMaxDevices];
+std::atomic<int> g_attr_done[4][kMaxDevices];   // per instantiation (kPos + 2 * kBias)
 std::atomic<int> g_sm_count[kMaxDevices];
 
 int sm_count(int dev) {
@@ -1184,18 +1345,19 @@ int get_workspace(int dev, cudaStream_t stream, size_t part_bytes, size_t cnt_by
   return ATTN_OK;
 }
 
-template <bool kPos>
+template <bool kPos, bool kBias = false>
 int launch(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, const Params& p, int grid,
            int dev, cudaStream_t stream) {
-  auto kern = attn_fwd_kernel<kPos>;
-  if (dev < 0 || dev >= kMaxDevices || !g_attr_done[kPos][dev].load(std::memory_order_acquire)) {
+  auto kern = attn_fwd_kernel<kPos, kBias>;
+  constexpr int kInst = (kPos ? 1 : 0) + (kBias ? 2 : 0);
+  if (dev < 0 || dev >= kMaxDevices || !g_attr_done[kInst][dev].load(std::memory_order_acquire)) {
     // The in-kernel register split (setmaxnreg) balances only at kRegsLaunch registers
     // per thread; at any other count the increase would never be granted. Refuse.
     cudaFuncAttributes fa;
     if (cudaFuncGetAttributes(&fa, kern) != cudaSuccess || fa.numRegs != kRegsLaunch) return ATTN_ERR_CUDA;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) != cudaSuccess)
       return ATTN_ERR_CUDA;
-    if (dev >= 0 && dev < kMaxDevices) g_attr_done[kPos][dev].store(1, std::memory_order_release);
+    if (dev >= 0 && dev < kMaxDevices) g_attr_done[kInst][dev].store(1, std::memory_order_release);
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(grid));
@@ -1207,10 +1369,14 @@ int launch(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, 
   return ATTN_OK;
 }
 
-}  // namespace
+struct BiasArg {
+  const void* ptr;
+  long long sb, sh, sq;
+};
 
-extern "C" int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Nq,
-                        int Nk, int d, float scale, void* stream) {
+// attn_fwd and attn_fwd_bias (bias != nullptr): the argument rules, the plan, the launch.
+int forward(const void* q, const void* k, const void* v, const BiasArg* bias, void* o, float* lse, int B, int H,
+            int Nq, int Nk, int d, float scale, void* stream) {
   if (B < 0 || H < 0 || Nq < 0 || Nk < 0) return ATTN_ERR_INVALID_ARG;
   if (d != kD) return ATTN_ERR_UNSUPPORTED;
   if (!std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
@@ -1228,6 +1394,18 @@ extern "C" int attn_fwd(const void* q, const void* k, const void* v, void* o, fl
   // element counts must fit a signed 64-bit byte offset
   const long long max_rows = static_cast<long long>(Nq > Nk ? Nq : Nk);
   if (bh > (LLONG_MAX / 256) / max_rows) return ATTN_ERR_INVALID_ARG;
+  if (bias != nullptr) {
+    if (!bias->ptr || bias->sb < 0 || bias->sh < 0 || bias->sq < 0) return ATTN_ERR_INVALID_ARG;
+    // the last element's offset, (B-1) sb + (H-1) sh + (Nq-1) sq + Nk - 1, in bytes must fit int64
+    constexpr long long kCap = LLONG_MAX / 8;
+    const long long ext[3] = {B - 1LL, H - 1LL, Nq - 1LL};
+    const long long str[3] = {bias->sb, bias->sh, bias->sq};
+    for (int i = 0; i < 3; ++i)
+      if (str[i] > 0 && ext[i] > kCap / str[i]) return ATTN_ERR_INVALID_ARG;
+    // 16-byte vector loads of each row's 8-key chunks
+    if ((reinterpret_cast<uintptr_t>(bias->ptr) & 15u) || ((bias->sb | bias->sh | bias->sq) & 7))
+      return ATTN_ERR_MISALIGNED;
+  }
 
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return ATTN_ERR_CUDA;
@@ -1259,6 +1437,12 @@ extern "C" int attn_fwd(const void* q, const void* k, const void* v, void* o, fl
   p.causal = 0;
   p.causal_off = 0;
   p.bh_count = static_cast<int>(bh);
+  p.bias = bias ? static_cast<const uint16_t*>(bias->ptr) : nullptr;
+  p.bias_sb = bias ? bias->sb : 0;
+  p.bias_sh = bias ? bias->sh : 0;
+  p.bias_sq = bias ? bias->sq : 0;
+  p.H = H;
+  p.scale = scale;
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (pl.has_split) {
@@ -1268,7 +1452,23 @@ extern "C" int attn_fwd(const void* q, const void* k, const void* v, void* o, fl
     const int rc = get_workspace(dev, s, part_bytes, cnt_bytes, &p.part, &p.cnt, &p.cnt_next, &p.cnt_len);
     if (rc != ATTN_OK) return rc;
   }
+  // with a bias the scale is applied before the row max, so one instantiation serves any sign
+  if (bias != nullptr) return launch<true, true>(mq, mk, mv, p, pl.grid, dev, s);
   return scale > 0.0f ? launch<true>(mq, mk, mv, p, pl.grid, dev, s) : launch<false>(mq, mk, mv, p, pl.grid, dev, s);
+}
+
+}  // namespace
+
+extern "C" int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Nq,
+                        int Nk, int d, float scale, void* stream) {
+  return forward(q, k, v, nullptr, o, lse, B, H, Nq, Nk, d, scale, stream);
+}
+
+extern "C" int attn_fwd_bias(const void* q, const void* k, const void* v, const void* bias, long long bias_stride_b,
+                             long long bias_stride_h, long long bias_stride_q, void* o, float* lse, int B, int H,
+                             int Nq, int Nk, int d, float scale, void* stream) {
+  const BiasArg ba = {bias, bias_stride_b, bias_stride_h, bias_stride_q};
+  return forward(q, k, v, &ba, o, lse, B, H, Nq, Nk, d, scale, stream);
 }
 
 extern "C" int attn_fwd_causal(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
@@ -1322,6 +1522,10 @@ extern "C" int attn_fwd_causal(const void* q, const void* k, const void* v, void
   p.causal = 1;
   p.causal_off = Nk - Nq;
   p.bh_count = static_cast<int>(bh);
+  p.bias = nullptr;
+  p.bias_sb = p.bias_sh = p.bias_sq = 0;
+  p.H = H;
+  p.scale = scale;
   const int grid = static_cast<int>(n_groups < sms ? n_groups : sms);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   return scale > 0.0f ? launch<true>(mq, mk, mv, p, grid, dev, s) : launch<false>(mq, mk, mv, p, grid, dev, s);
@@ -1442,6 +1646,10 @@ extern "C" int attn_fwd_noalloc(const void* q, const void* k, const void* v, voi
   p.causal = 0;
   p.causal_off = 0;
   p.bh_count = static_cast<int>(bh);
+  p.bias = nullptr;
+  p.bias_sb = p.bias_sh = p.bias_sq = 0;
+  p.H = H;
+  p.scale = scale;
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (pl.has_split) {

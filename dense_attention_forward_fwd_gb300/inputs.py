@@ -28,8 +28,12 @@ __all__ = [
     "f32_to_bf16_bits",
     "bf16_bits_to_f32",
     "make_qkv",
+    "make_bias",
+    "BF16_NEG_INF",
     "sample_rows",
 ]
+
+BF16_NEG_INF = np.uint16(0xFF80)   # -inf as BF16 bits (a bias entry that removes a key)
 
 
 def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
@@ -62,6 +66,17 @@ def make_qkv(B: int, H: int, Nq: int, Nk: int, d: int = 128, seed: int = 0,
         q = q * m
         k = k * m
     return f32_to_bf16_bits(q), f32_to_bf16_bits(k), f32_to_bf16_bits(v)
+
+
+def make_bias(shape, seed: int, std: float = 1.0) -> np.ndarray:
+    """Seeded additive bias of the given shape (e.g. (B, H, Nq, Nk), or 1 in any of the first
+    three dimensions for a shared bias): float32 normals with standard deviation ``std`` from
+    one PCG64 stream, rounded to BF16 bits. Masks (-inf entries) are set by the caller."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    x = rng.standard_normal(tuple(shape), dtype=np.float32)
+    if std != 1.0:
+        x = x * np.float32(std)
+    return f32_to_bf16_bits(x)
 
 
 def sample_rows(B: int, H: int, Nq: int, per_head: int = 64, seed_base: int = 1_000_003,

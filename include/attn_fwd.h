@@ -98,6 +98,35 @@ int attn_fwd_causal(const void* q, const void* k, const void* v, void* o, float*
                     int B, int H, int Nq, int Nk, int d, float scale, void* stream);
 
 /*
+ * attn_fwd_bias -- attention forward with an additive bias.
+ *
+ * S = scale * Q K^T + B, P = softmax_row(S), O = P V: the definition's optional bias B
+ * ("FlashAttention'ı Anlamak Bölüm 1", section 0.2 Notasyon), one Nq x Nk matrix per head,
+ * with the caller's scale in place of 1/sqrt(d) as in attn_fwd.
+ *
+ *   bias   device, BF16, read only. B_ij of head (b, h) is
+ *          bias[b * bias_stride_b + h * bias_stride_h + i * bias_stride_q + j]
+ *          (strides in elements, keys contiguous). A stride of 0 shares the values:
+ *          (0, 0, Nk) is one Nq x Nk matrix for every head, (0, 0, 0) one bias per key
+ *          (e.g. a key padding mask). The caller owns it; it must not alias o or lse.
+ *
+ * Arguments, layouts and return values are otherwise those of attn_fwd, plus:
+ *   - ATTN_ERR_INVALID_ARG: bias is NULL, a stride is negative, or the offset of the
+ *     last element overflows a 64-bit byte offset.
+ *   - ATTN_ERR_MISALIGNED: bias is not 16-byte aligned or a stride is not a multiple
+ *     of 8 elements (each row is read in 16-byte pieces).
+ *   - Entries must be finite or -inf; -inf removes the key from that row. A row whose
+ *     entries are all -inf has no softmax: its O and LSE are unspecified (NaN or inf).
+ *     NaN or +inf entries give unspecified results for their row.
+ *   - lse is the log-sum-exp of the biased scores, in natural-log units.
+ *   - The work split and workspace are those of attn_fwd (the bias adds no state). The
+ *     bias is read once per (query row, key), from L2 when it is shared across heads.
+ */
+int attn_fwd_bias(const void* q, const void* k, const void* v, const void* bias,
+                  long long bias_stride_b, long long bias_stride_h, long long bias_stride_q,
+                  void* o, float* lse, int B, int H, int Nq, int Nk, int d, float scale, void* stream);
+
+/*
  * attn_fwd_noalloc -- attn_fwd for callers that cannot allocate device memory.
  *
  * There is no counterpart on the pages: this is a service of the library. Some callers

@@ -65,27 +65,37 @@ def bf16_to_np(t) -> np.ndarray:
     return t.view(torch.int16).cpu().numpy().view(np.uint16).astype(np.uint32).__lshift__(16).view(np.float32)
 
 
-def run_gpu(attn, q, k, v, scale: float, causal: bool = False):
-    """Run the CUDA path on uint16 BF16 host arrays; return (o float32 [B,H,Nq,d], lse float32)."""
+def run_gpu(attn, q, k, v, scale: float, causal: bool = False, bias=None):
+    """Run the CUDA path on uint16 BF16 host arrays; return (o float32 [B,H,Nq,d], lse float32).
+
+    ``bias`` (uint16 BF16 bits, shape (Bb, Hb, Nqb, Nk) broadcastable to [B,H,Nq,Nk]) selects
+    attn_fwd_bias; its size-1 dimensions are shared through stride 0."""
     import torch
     B, H, Nq, d = q.shape
     Nk = k.shape[2]
     qd, kd, vd = to_device(q), to_device(k), to_device(v)
     o = torch.full((B, H, Nq, d), float("nan"), dtype=torch.bfloat16, device="cuda")
     lse = torch.full((B, H, Nq), float("nan"), dtype=torch.float32, device="cuda")
-    (attn.attn_fwd_causal if causal else attn.attn_fwd)(qd, kd, vd, o, lse, B, H, Nq, Nk, d, scale)
+    if bias is not None:
+        attn.attn_fwd_bias(qd, kd, vd, to_device(bias), o, lse, B, H, Nq, Nk, d, scale)
+    else:
+        (attn.attn_fwd_causal if causal else attn.attn_fwd)(qd, kd, vd, o, lse, B, H, Nq, Nk, d, scale)
     assert attn.attn_fwd_status() == attn.ATTN_OK
     return bf16_to_np(o), lse.cpu().numpy()
 
 
 def check_case(attn, B, H, Nq, Nk, seed=0, qk_mult=1.0, scale=None, rows=None, ulp_aware=False, qkv=None,
-               causal=False):
-    """Full or row-sampled parity of one seeded case (causal: under the causal mask); returns the Report."""
+               causal=False, bias=None):
+    """Full or row-sampled parity of one seeded case (causal: under the causal mask; bias: with
+    that additive bias); returns the Report."""
     d = 128
     scale = float(np.float32(1 / np.sqrt(d))) if scale is None else scale
     q, k, v = qkv if qkv is not None else make_qkv(B, H, Nq, Nk, d=d, seed=seed, qk_mult=qk_mult)
-    o_gpu, lse_gpu = run_gpu(attn, q, k, v, scale, causal)
-    o_ref, lse_ref = (oracle.attention_rows_causal if causal else oracle.attention_rows)(q, k, v, scale, rows)
+    o_gpu, lse_gpu = run_gpu(attn, q, k, v, scale, causal, bias)
+    if bias is not None:
+        o_ref, lse_ref = oracle.attention_rows_bias(q, k, v, bias, scale, rows)
+    else:
+        o_ref, lse_ref = (oracle.attention_rows_causal if causal else oracle.attention_rows)(q, k, v, scale, rows)
     o_flat, l_flat = o_gpu.reshape(-1, d), lse_gpu.reshape(-1)
     if rows is not None:
         o_flat, l_flat = o_flat[rows], l_flat[rows]

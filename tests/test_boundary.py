@@ -20,7 +20,7 @@ def declared_functions():
 
 def test_header_declares_the_entry_points():
     names = declared_functions()
-    assert {"attn_fwd", "attn_fwd_causal", "attn_fwd_noalloc", "attn_fwd_status", "attn_status_string",
+    assert {"attn_fwd", "attn_fwd_causal", "attn_fwd_bias", "attn_fwd_noalloc", "attn_fwd_status", "attn_status_string",
             "attn_fwd_set_wait_limit", "attn_fwd_kernel_count"} <= set(names)
 
 
@@ -94,6 +94,39 @@ def test_causal_argument_checks(kw, code):
     before = attn.attn_fwd_kernel_count()
     assert call_causal(**kw) == code
     assert attn.attn_fwd_kernel_count() == before
+
+
+def call_bias(q=A, k=A, v=A, bias=A, sb=0, sh=0, sq=128, o=A, lse=A, B=1, H=1, Nq=128, Nk=128, d=128, scale=0.125):
+    return attn.load_library().attn_fwd_bias(q, k, v, bias, sb, sh, sq, o, lse, B, H, Nq, Nk, d, scale, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(bias=None), attn.ATTN_ERR_INVALID_ARG),
+    (dict(sq=-128), attn.ATTN_ERR_INVALID_ARG),
+    (dict(sb=-8, B=2), attn.ATTN_ERR_INVALID_ARG),
+    (dict(sh=1 << 62, H=4), attn.ATTN_ERR_INVALID_ARG),     # the last element's offset overflows
+    (dict(bias=A + 8), attn.ATTN_ERR_MISALIGNED),
+    (dict(sq=130, Nk=130), attn.ATTN_ERR_MISALIGNED),       # rows not on 16-byte boundaries
+    (dict(sh=12, H=2), attn.ATTN_ERR_MISALIGNED),
+    (dict(q=None), attn.ATTN_ERR_INVALID_ARG),
+    (dict(d=64), attn.ATTN_ERR_UNSUPPORTED),
+    (dict(Nk=0), attn.ATTN_ERR_INVALID_ARG),
+    (dict(B=0), attn.ATTN_OK),
+    (dict(Nq=0, bias=None), attn.ATTN_OK),
+])
+def test_bias_argument_checks(kw, code):
+    before = attn.attn_fwd_kernel_count()
+    assert call_bias(**kw) == code
+    assert attn.attn_fwd_kernel_count() == before
+
+
+def test_bias_binding_checks_shapes():
+    torch = pytest.importorskip("torch")
+    with pytest.raises(TypeError):   # a CPU tensor is refused before any pointer is passed
+        attn.attn_fwd_bias(A, A, A, torch.zeros(1, 1, 128, 128, dtype=torch.bfloat16), A, A,
+                           1, 1, 128, 128, 128, 0.1)
+    with pytest.raises(ValueError):  # an integer pointer needs its strides
+        attn.attn_fwd_bias(A, A, A, A, A, A, 1, 1, 128, 128, 128, 0.1)
 
 
 def test_binding_raises_on_rejected_call():

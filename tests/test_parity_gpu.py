@@ -6,7 +6,8 @@ import pytest
 
 import oracle
 from dense_attention_forward_fwd_gb300.configs import WORKLOADS, by_name
-from dense_attention_forward_fwd_gb300.inputs import bf16_bits_to_f32, f32_to_bf16_bits, make_qkv, sample_rows
+from dense_attention_forward_fwd_gb300.inputs import (BF16_NEG_INF, bf16_bits_to_f32, f32_to_bf16_bits, make_bias,
+                                                      make_qkv, sample_rows)
 from parity import check_case, compare, run_gpu
 
 pytestmark = pytest.mark.gpu
@@ -185,3 +186,123 @@ def test_causal_rejects_more_queries_than_keys(gpu_lib):
     with pytest.raises(gpu_lib.AttnError) as e:
         run_gpu(gpu_lib, *make_qkv(1, 1, 200, 100, seed=75), SCALE, causal=True)
     assert e.value.status == gpu_lib.ATTN_ERR_INVALID_ARG
+
+
+# ---- additive bias: S = scale * Q K^T + B --------------------------------------------------------
+
+def _bias_shape(kind, B, H, Nq, Nk):
+    return {"full": (B, H, Nq, Nk), "shared": (1, 1, Nq, Nk), "per_head": (1, H, Nq, Nk),
+            "per_key": (1, 1, 1, Nk)}[kind]
+
+
+@pytest.mark.parametrize("B,H,Nq,Nk,kind", [
+    (1, 2, 256, 256, "full"),
+    (2, 3, 300, 1000, "full"),       # ragged query and key tails
+    (1, 2, 384, 640, "shared"),
+    (1, 3, 1000, 1777, "per_key"),
+    (1, 1, 1, 200, "full"),
+    (1, 1, 129, 129, "per_key"),
+    (1, 2, 256, 5120, "shared"),     # few groups with long rows: key steps split across blocks
+    (4, 2, 768, 768, "per_head"),
+])
+def test_bias_full_parity(gpu_lib, B, H, Nq, Nk, kind):
+    bias = make_bias(_bias_shape(kind, B, H, Nq, Nk), seed=9000 + Nq + Nk, std=2.0)
+    check_case(gpu_lib, B, H, Nq, Nk, seed=8000 + Nq + Nk, bias=bias)
+
+
+def test_bias_padding_mask_hides_whole_key_tiles(gpu_lib):
+    # keys 0..299 and 900..999 removed for every row: each row starts with two key tiles that
+    # are entirely -inf, so its running maximum is still -inf when the first visible key arrives
+    Nk = 1000
+    bias = make_bias((1, 1, 1, Nk), seed=80)
+    bias[..., :300] = BF16_NEG_INF
+    bias[..., 900:] = BF16_NEG_INF
+    check_case(gpu_lib, 1, 2, 384, Nk, seed=81, bias=bias)
+
+
+def test_bias_causal_pattern_agrees_with_the_causal_entry_point(gpu_lib):
+    Nq, Nk = 384, 640
+    bias = np.zeros((1, 1, Nq, Nk), dtype=np.uint16)
+    for i in range(Nq):
+        bias[0, 0, i, i + Nk - Nq + 1:] = BF16_NEG_INF
+    q, k, v = make_qkv(1, 2, Nq, Nk, seed=82)
+    check_case(gpu_lib, 1, 2, Nq, Nk, qkv=(q, k, v), bias=bias)
+    check_case(gpu_lib, 1, 2, Nq, Nk, qkv=(q, k, v), causal=True)
+    ob, lb = run_gpu(gpu_lib, q, k, v, SCALE, bias=bias)
+    oc, lc = run_gpu(gpu_lib, q, k, v, SCALE, causal=True)
+    assert np.max(np.abs(ob - oc)) <= 2e-2 and np.max(np.abs(lb - lc)) <= 1e-4 * max(1.0, np.max(np.abs(lc)))
+
+
+def test_bias_peaked_and_negative_scale(gpu_lib):
+    # a bias of standard deviation 8 on top of peaked scores: frequent late maxima and O rescales
+    check_case(gpu_lib, 1, 2, 512, 2048, seed=83, qk_mult=3.0, ulp_aware=True,
+               bias=make_bias((1, 2, 512, 2048), seed=84, std=8.0))
+    check_case(gpu_lib, 1, 2, 256, 384, seed=85, scale=-0.0883883461356163,
+               bias=make_bias((1, 1, 256, 384), seed=86, std=2.0))
+
+
+def test_bias_of_zeros_matches_the_plain_entry_point(gpu_lib):
+    q, k, v = make_qkv(1, 2, 256, 512, seed=87)
+    ob, lb = run_gpu(gpu_lib, q, k, v, SCALE, bias=np.zeros((1, 1, 1, 512), dtype=np.uint16))
+    o0, l0 = run_gpu(gpu_lib, q, k, v, SCALE)
+    assert np.max(np.abs(ob - o0)) <= 1e-2 and np.max(np.abs(lb - l0)) <= 1e-5 * np.max(np.abs(l0))
+
+
+@pytest.mark.parametrize("name", ["rect-4k-8k"])
+def test_bias_workload_sampled_rows(gpu_lib, name):
+    # the default benchmark shape with one [Nq, Nk] bias shared by every head
+    w = by_name(name)
+    rows = sample_rows(w.B, w.H, w.Nq, per_head=16)
+    bias = make_bias((1, 1, w.Nq, w.Nk), seed=88, std=1.0)
+    check_case(gpu_lib, w.B, w.H, w.Nq, w.Nk, seed=w.seed, scale=w.scale, rows=rows, bias=bias)
+
+
+def test_bias_rejects_misaligned_strides(gpu_lib):
+    with pytest.raises(gpu_lib.AttnError) as e:
+        run_gpu(gpu_lib, *make_qkv(1, 1, 128, 100, seed=89), SCALE, bias=np.zeros((1, 1, 128, 100), np.uint16))
+    assert e.value.status == gpu_lib.ATTN_ERR_MISALIGNED
+
+
+def test_bias_rows_padded_to_16_bytes_for_a_ragged_key_count(gpu_lib):
+    # Nk = 129 keys: each bias row is stored with a stride of 136 elements (16-byte rows)
+    import torch
+    from parity import bf16_to_np, to_device
+    Nq, Nk, ld = 200, 129, 136
+    q, k, v = make_qkv(1, 2, Nq, Nk, seed=90)
+    bias = make_bias((1, 1, Nq, Nk), seed=91, std=2.0)
+    padded = np.zeros((1, 1, Nq, ld), dtype=np.uint16)
+    padded[..., :Nk] = bias
+    bd = to_device(padded)[..., :Nk]
+    assert bd.stride(2) == ld
+    o = torch.empty(1, 2, Nq, 128, dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty(1, 2, Nq, dtype=torch.float32, device="cuda")
+    gpu_lib.attn_fwd_bias(to_device(q), to_device(k), to_device(v), bd, o, lse, 1, 2, Nq, Nk, 128, SCALE)
+    o_ref, l_ref = oracle.attention_rows_bias(q, k, v, bias, SCALE)
+    compare(bf16_to_np(o).reshape(-1, 128), lse.cpu().numpy().reshape(-1), o_ref, l_ref)
+
+
+@pytest.mark.parametrize("bias_kind", [None, "shared"])
+def test_split_groups_give_bit_identical_results_on_every_run(gpu_lib, bias_kind):
+    # the benchmark shape: every group's key steps are split across blocks, and the block
+    # that merges a group is whichever finishes last; the merge order must not depend on it
+    import torch
+    from parity import to_device
+    w = by_name("rect-4k-8k")
+    q, k, v = (to_device(x) for x in make_qkv(w.B, w.H, w.Nq, w.Nk, seed=92))
+    bias = to_device(make_bias((1, 1, w.Nq, w.Nk), seed=93)) if bias_kind else None
+    outs = []
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    for i in range(6):
+        o = torch.empty(w.B, w.H, w.Nq, 128, dtype=torch.bfloat16, device="cuda")
+        lse = torch.empty(w.B, w.H, w.Nq, dtype=torch.float32, device="cuda")
+        st = streams[i % 2]
+        st.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(st):
+            if bias is None:
+                gpu_lib.attn_fwd(q, k, v, o, lse, w.B, w.H, w.Nq, w.Nk, 128, w.scale, st)
+            else:
+                gpu_lib.attn_fwd_bias(q, k, v, bias, o, lse, w.B, w.H, w.Nq, w.Nk, 128, w.scale, st)
+        torch.cuda.synchronize()
+        outs.append((o.cpu(), lse.cpu()))
+    for o, lse in outs[1:]:
+        assert torch.equal(o, outs[0][0]) and torch.equal(lse, outs[0][1])
