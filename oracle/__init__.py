@@ -19,7 +19,7 @@ import threading
 import numpy as np
 
 __all__ = ["build", "Oracle", "default", "attention_rows", "attention_rows_causal", "attention_rows_bias",
-           "attention", "probs", "max_threads", "LIB_PATH"]
+           "attention", "attention_dense", "attention_bwd", "probs", "max_threads", "LIB_PATH"]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "attn_ref.c")
@@ -55,6 +55,10 @@ class Oracle:
         lib.attn_ref_rows_bias_f64.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, i64, i64, i64, i64, i64, dbl,
                                                vp, i64, vp, vp, ctypes.c_int]
         lib.attn_ref_rows_bias_f64.restype = ctypes.c_int
+        lib.attn_ref_dense_f64.argtypes = [vp, vp, vp, i64, i64, i64, i64, i64, dbl, vp, vp]
+        lib.attn_ref_dense_f64.restype = ctypes.c_int
+        lib.attn_ref_bwd_f64.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, i64, dbl, vp, vp, vp, ctypes.c_int]
+        lib.attn_ref_bwd_f64.restype = ctypes.c_int
         lib.attn_ref_probs_f64.argtypes = [vp, vp, i64, i64, i64, i64, dbl, vp]
         lib.attn_ref_probs_f64.restype = ctypes.c_int
         lib.attn_ref_max_threads.argtypes = []
@@ -142,6 +146,39 @@ class Oracle:
         o, lse = self.attention_rows(q, k, v, scale, None, nthreads)
         return o.reshape(B, H, Nq, dv), lse.reshape(B, H, Nq)
 
+    def attention_dense(self, q, k, v, scale: float):
+        """Forward on float64 (or BF16-bit uint16, widened exactly) inputs: (o [B,H,Nq,dv], lse [B,H,Nq])."""
+        q, k, v = _f64(q), _f64(k), _f64(v)
+        B, H, Nq, d = q.shape
+        Nk, dv = k.shape[2], v.shape[3]
+        if k.shape != (B, H, Nk, d) or v.shape[:3] != (B, H, Nk):
+            raise ValueError(f"shape mismatch q{q.shape} k{k.shape} v{v.shape}")
+        o = np.empty((B, H, Nq, dv), dtype=np.float64)
+        lse = np.empty((B, H, Nq), dtype=np.float64)
+        rc = self.lib.attn_ref_dense_f64(_ptr(q), _ptr(k), _ptr(v), B * H, Nq, Nk, d, dv, float(scale), _ptr(o),
+                                         _ptr(lse))
+        if rc != 0:
+            raise ValueError(f"attn_ref_dense_f64 failed with status {rc}")
+        return o, lse
+
+    def attention_bwd(self, q, k, v, dout, scale: float, nthreads: int = 0):
+        """Gradients (dq, dk, dv) in float64 of the forward for upstream gradient dout [B,H,Nq,dv].
+
+        Inputs are float64 arrays, or BF16 bits (uint16) widened exactly."""
+        q, k, v, dout = _f64(q), _f64(k), _f64(v), _f64(dout)
+        B, H, Nq, d = q.shape
+        Nk, dv = k.shape[2], v.shape[3]
+        if k.shape != (B, H, Nk, d) or v.shape[:3] != (B, H, Nk) or dout.shape != (B, H, Nq, dv):
+            raise ValueError(f"shape mismatch q{q.shape} k{k.shape} v{v.shape} dout{dout.shape}")
+        dq = np.empty((B, H, Nq, d), dtype=np.float64)
+        dk = np.empty((B, H, Nk, d), dtype=np.float64)
+        dvv = np.empty((B, H, Nk, dv), dtype=np.float64)
+        rc = self.lib.attn_ref_bwd_f64(_ptr(q), _ptr(k), _ptr(v), _ptr(dout), B * H, Nq, Nk, d, dv, float(scale),
+                                       _ptr(dq), _ptr(dk), _ptr(dvv), int(nthreads))
+        if rc != 0:
+            raise ValueError(f"attn_ref_bwd_f64 failed with status {rc}")
+        return dq, dk, dvv
+
     def probs(self, q, k, scale: float):
         """Full P = softmax_row(scale * Q K^T) as float64 [B,H,Nq,Nk] (small shapes only)."""
         q, k = _u16(q, 4), _u16(k, 4)
@@ -173,6 +210,16 @@ def _u16(a: np.ndarray, ndim: int) -> np.ndarray:
     return a
 
 
+def _f64(a: np.ndarray) -> np.ndarray:
+    """float64 C-contiguous copy of a float array, or of BF16 bits (uint16) widened exactly."""
+    a = np.asarray(a)
+    if a.dtype == np.uint16:
+        a = (a.astype(np.uint32) << np.uint32(16)).view(np.float32)
+    if a.ndim != 4:
+        raise ValueError(f"expected 4 dims, got shape {a.shape}")
+    return np.ascontiguousarray(a, dtype=np.float64)
+
+
 def _ptr(a: np.ndarray):
     return a.ctypes.data_as(ctypes.c_void_p)
 
@@ -199,3 +246,11 @@ def attention(q, k, v, scale: float, nthreads: int = 0):
 
 def probs(q, k, scale: float):
     return default().probs(q, k, scale)
+
+
+def attention_dense(q, k, v, scale: float):
+    return default().attention_dense(q, k, v, scale)
+
+
+def attention_bwd(q, k, v, dout, scale: float, nthreads: int = 0):
+    return default().attention_bwd(q, k, v, dout, scale, nthreads)

@@ -311,3 +311,136 @@ int attn_ref_max_threads(void)
     return 1;
 #endif
 }
+
+/*
+ * ---- Backward pass ---------------------------------------------------------------
+ *
+ * The notes name the backward pass and recomputation as parts of the method
+ * ("FlashAttention'ı Anlamak Bölüm 1", section 0 Giriş: tiling, online softmax and
+ * recomputation; forward and backward passes) without giving its formulas. What it
+ * computes is fixed by the mathematics: the gradient of the forward above for a loss L
+ * whose gradient with respect to O is dO. Row by row, in double precision:
+ *
+ *   p_j   = exp(s_j - m) / l                     (the forward's probabilities, recomputed)
+ *   dv_j += p_j * dO_i                           (O_i = sum_j p_j v_j)
+ *   dp_j  = dO_i . v_j
+ *   D_i   = sum_j p_j dp_j                       (= dO_i . O_i)
+ *   ds_j  = p_j (dp_j - D_i)                     (softmax Jacobian: dp/ds = diag(p) - p p^T)
+ *   dq_i  = scale * sum_j ds_j k_j               (s_j = scale * q_i . k_j)
+ *   dk_j += scale * ds_j q_i
+ *
+ * These take double inputs so that central differences of attn_ref_dense_f64 can check
+ * them; BF16 inputs are widened exactly by the caller.
+ */
+
+/* The forward on double inputs: o [BH, Nq, dv], lse [BH, Nq] (same steps as above). */
+int attn_ref_dense_f64(const double *q, const double *k, const double *v,
+                       int64_t BH, int64_t Nq, int64_t Nk, int64_t d, int64_t dv,
+                       double scale, double *o, double *lse)
+{
+    if (BH < 0 || Nq < 0 || Nk < 1 || d < 1 || dv < 1) return REF_EINVAL;
+    if (BH * Nq == 0) return REF_OK;
+    if (!q || !k || !v || !o || !lse) return REF_EINVAL;
+    double *s = (double *)malloc((size_t)Nk * sizeof(double));
+    if (!s) return REF_ENOMEM;
+    for (int64_t bh = 0; bh < BH; bh++) {
+        const double *kh = k + bh * Nk * d, *vh = v + bh * Nk * dv;
+        for (int64_t i = 0; i < Nq; i++) {
+            const double *qi = q + (bh * Nq + i) * d;
+            for (int64_t j = 0; j < Nk; j++) {
+                double acc = 0.0;
+                for (int64_t c = 0; c < d; c++) acc += qi[c] * kh[j * d + c];
+                s[j] = scale * acc;
+            }
+            double m = row_max(s, Nk);
+            double l = row_exp_sum(s, Nk, m);
+            double *oi = o + (bh * Nq + i) * dv;
+            for (int64_t c = 0; c < dv; c++) {
+                double acc = 0.0;
+                for (int64_t j = 0; j < Nk; j++) acc += s[j] * vh[j * dv + c];
+                oi[c] = acc / l;
+            }
+            lse[bh * Nq + i] = m + log(l);
+        }
+    }
+    free(s);
+    return REF_OK;
+}
+
+/*
+ * attn_ref_bwd_f64: dq [BH, Nq, d], dk [BH, Nk, d], dv [BH, Nk, dv] for upstream
+ * gradient dout [BH, Nq, dv]. OpenMP over heads (each head's dk and dv are summed over
+ * its query rows in order).
+ */
+int attn_ref_bwd_f64(const double *q, const double *k, const double *v, const double *dout,
+                     int64_t BH, int64_t Nq, int64_t Nk, int64_t d, int64_t dv,
+                     double scale, double *dq, double *dk, double *dvv, int nthreads)
+{
+    if (BH < 0 || Nq < 0 || Nk < 1 || d < 1 || dv < 1) return REF_EINVAL;
+    if (BH == 0) return REF_OK;
+    if (!q || !k || !v || !dout || !dq || !dk || !dvv) return REF_EINVAL;
+    int failed = 0;
+#ifdef _OPENMP
+    int nt = nthreads > 0 ? nthreads : omp_get_max_threads();
+#pragma omp parallel num_threads(nt)
+#else
+    (void)nthreads;
+#endif
+    {
+        double *p = (double *)malloc((size_t)Nk * sizeof(double));
+        double *dp = (double *)malloc((size_t)Nk * sizeof(double));
+        if (!p || !dp) {
+#ifdef _OPENMP
+#pragma omp atomic write
+#endif
+            failed = 1;
+        } else {
+#ifdef _OPENMP
+#pragma omp for schedule(dynamic, 1)
+#endif
+            for (int64_t bh = 0; bh < BH; bh++) {
+                const double *kh = k + bh * Nk * d, *vh = v + bh * Nk * dv;
+                double *dkh = dk + bh * Nk * d, *dvh = dvv + bh * Nk * dv;
+                memset(dkh, 0, (size_t)(Nk * d) * sizeof(double));
+                memset(dvh, 0, (size_t)(Nk * dv) * sizeof(double));
+                for (int64_t i = 0; i < Nq; i++) {
+                    const double *qi = q + (bh * Nq + i) * d;
+                    const double *doi = dout + (bh * Nq + i) * dv;
+                    double *dqi = dq + (bh * Nq + i) * d;
+                    /* the forward's probabilities of row i */
+                    for (int64_t j = 0; j < Nk; j++) {
+                        double acc = 0.0;
+                        for (int64_t c = 0; c < d; c++) acc += qi[c] * kh[j * d + c];
+                        p[j] = scale * acc;
+                    }
+                    double m = row_max(p, Nk);
+                    double l = row_exp_sum(p, Nk, m);
+                    for (int64_t j = 0; j < Nk; j++) p[j] /= l;
+                    /* dv, dp and D */
+                    double D = 0.0;
+                    for (int64_t j = 0; j < Nk; j++) {
+                        double acc = 0.0;
+                        for (int64_t c = 0; c < dv; c++) {
+                            dvh[j * dv + c] += p[j] * doi[c];
+                            acc += doi[c] * vh[j * dv + c];
+                        }
+                        dp[j] = acc;
+                        D += p[j] * acc;
+                    }
+                    /* ds, dq, dk */
+                    for (int64_t c = 0; c < d; c++) dqi[c] = 0.0;
+                    for (int64_t j = 0; j < Nk; j++) {
+                        double ds = p[j] * (dp[j] - D);
+                        for (int64_t c = 0; c < d; c++) {
+                            dqi[c] += scale * ds * kh[j * d + c];
+                            dkh[j * d + c] += scale * ds * qi[c];
+                        }
+                    }
+                }
+            }
+        }
+        free(p);
+        free(dp);
+    }
+    return failed ? REF_ENOMEM : REF_OK;
+}

@@ -376,6 +376,75 @@ def test_bias_rejects_a_shape_that_does_not_broadcast():
         oracle.default().attention_rows_bias(q, k, v, np.zeros((1, 2, 2, 4), np.uint16), 1.0)
 
 
+# ---- backward: the gradient of the forward for an upstream gradient dO ------------------------
+
+def pin_dense_forward_equals_the_bf16_oracle_on_bf16_inputs(orc):
+    # the double-input forward (used for finite differences) is the pinned forward on the BF16 lattice
+    q, k, v = make_qkv(2, 2, 5, 7, d=8, seed=50)
+    o1, l1 = orc.attention(q, k, v, 0.6)
+    o2, l2 = orc.attention_dense(q, k, v, 0.6)
+    assert np.max(np.abs(o1 - o2)) < 1e-15 and np.max(np.abs(l1 - l2)) < 1e-14
+
+
+def pin_bwd_matches_central_differences(orc):
+    # L = sum(dO * O): dL/dx by central differences of the forward for every element of q, k, v
+    rng = np.random.default_rng(51)
+    # dv > d: a mutant oracle that indexes value rows with the key stride stays inside v
+    B, H, Nq, Nk, d, dv = 1, 2, 3, 4, 3, 5
+    q, k = rng.normal(size=(B, H, Nq, d)), rng.normal(size=(B, H, Nk, d))
+    v, dout = rng.normal(size=(B, H, Nk, dv)), rng.normal(size=(B, H, Nq, dv))
+    scale = 0.8
+    grads = dict(zip("qkv", orc.attention_bwd(q, k, v, dout, scale)))
+    h = 1e-6
+    for name in "qkv":
+        base = {"q": q, "k": k, "v": v}
+        x, g = base[name], grads[name]
+        fd = np.zeros_like(x)
+        for idx in np.ndindex(x.shape):
+            lo, hi = dict(base), dict(base)
+            hi[name] = x.copy()
+            hi[name][idx] += h
+            lo[name] = x.copy()
+            lo[name][idx] -= h
+            l_hi = np.sum(orc.attention_dense(hi["q"], hi["k"], hi["v"], scale)[0] * dout)
+            l_lo = np.sum(orc.attention_dense(lo["q"], lo["k"], lo["v"], scale)[0] * dout)
+            fd[idx] = (l_hi - l_lo) / (2 * h)
+        assert np.max(np.abs(fd - g)) < 1e-7 * max(1.0, np.max(np.abs(g))), name
+
+
+def pin_bwd_key_gradients_sum_to_zero(orc):
+    # a common shift of every key changes no probability, so sum_j dK_j = 0 in every head
+    q, k, v = make_qkv(2, 3, 9, 11, d=8, seed=52, qk_mult=2.0)
+    dout = np.random.default_rng(53).normal(size=(2, 3, 9, 8))
+    _, dk, _ = orc.attention_bwd(q, k, v, dout, 0.5)
+    assert np.max(np.abs(dk.sum(axis=2))) < 1e-12 * max(1.0, np.max(np.abs(dk)))
+    assert np.max(np.abs(dk)) > 1e-3
+
+
+def pin_bwd_dv_is_probabilities_transposed_times_dout(orc):
+    q, k, v = make_qkv(1, 2, 6, 5, d=8, seed=54)
+    dout = np.random.default_rng(55).normal(size=(1, 2, 6, 8))
+    _, _, dv = orc.attention_bwd(q, k, v, dout, 0.9)
+    p = orc.probs(q, k, 0.9)
+    assert np.max(np.abs(dv - np.einsum("bhij,bhic->bhjc", p, dout))) < 1e-13
+
+
+def pin_bwd_zero_upstream_gradient_gives_zero(orc):
+    q, k, v = make_qkv(1, 1, 4, 6, d=8, seed=56)
+    for g in orc.attention_bwd(q, k, v, np.zeros((1, 1, 4, 8)), 0.7):
+        assert np.all(g == 0.0)
+
+
+def pin_bwd_equal_value_rows_give_no_query_or_key_gradient(orc):
+    # every value row equal: O is that row whatever the probabilities, so dQ = dK = 0
+    q, k, _ = make_qkv(1, 2, 5, 7, d=8, seed=57)
+    v = np.broadcast_to(np.random.default_rng(58).normal(size=(1, 2, 1, 8)), (1, 2, 7, 8)).copy()
+    dout = np.random.default_rng(59).normal(size=(1, 2, 5, 8))
+    dq, dk, dv = orc.attention_bwd(q, k, v, dout, 0.6)
+    assert np.max(np.abs(dq)) < 1e-13 and np.max(np.abs(dk)) < 1e-13
+    assert np.max(np.abs(dv)) > 1e-2
+
+
 PINS = [v for k_, v in sorted(globals().items()) if k_.startswith("pin_")]
 
 

@@ -32,6 +32,12 @@ MUTANTS = {
     "bias transposed": ("bh_bias[i * sq + j]", "bh_bias[j * sq + i]"),
     "bias row stride dropped": ("bh_bias[i * sq + j]", "bh_bias[j]"),
     "bias head and batch strides swapped": ("bias + (bh / H) * sb + (bh % H) * sh", "bias + (bh / H) * sh + (bh % H) * sb"),
+    "bwd row term D dropped": ("double ds = p[j] * (dp[j] - D);", "double ds = p[j] * dp[j];"),
+    "bwd dq without the scale": ("dqi[c] += scale * ds * kh[j * d + c];", "dqi[c] += ds * kh[j * d + c];"),
+    "bwd dk from keys": ("dkh[j * d + c] += scale * ds * qi[c];", "dkh[j * d + c] += scale * ds * kh[j * d + c];"),
+    "bwd dv from dp": ("dvh[j * dv + c] += p[j] * doi[c];", "dvh[j * dv + c] += dp[j] * doi[c];"),
+    "bwd probabilities not normalised": ("for (int64_t j = 0; j < Nk; j++) p[j] /= l;", ""),
+    "dense forward without 1/l": ("oi[c] = acc / l;", "oi[c] = acc;"),
 }
 
 
