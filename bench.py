@@ -20,6 +20,10 @@ count the visible (query, key) pairs only, 4*d each, and vs_baseline is null.
 every head or one per head; the FLOP count is unchanged (the bias adds one addend per
 score).
 
+--backward times attn_bwd (dQ, dK, dV for an N(0,1) upstream gradient, given the forward's
+O and LSE) and counts 2.5x the forward's FLOPs (the five products of the method's
+backward); with --impl reference it times the FP64 backward oracle.
+
 --impl reference times the FP64 CPU oracle (the plain definition) on host cores, on a
 bounded sample of query rows per step.
 """
@@ -65,6 +69,8 @@ def parse():
                     help="causal mask (query i sees keys 0 .. i + Nk - Nq); FLOPs count visible pairs only")
     ap.add_argument("--bias", choices=["none", "shared", "full"], default="none",
                     help="additive BF16 bias N(0,1): one [Nq, Nk] matrix for all heads, or one per head")
+    ap.add_argument("--backward", action="store_true",
+                    help="time attn_bwd (dQ, dK, dV for an N(0,1) upstream gradient); FLOPs = 2.5x the forward's")
     return ap.parse_args()
 
 
@@ -72,9 +78,11 @@ def dist_env():
     return int(os.environ.get("RANK", 0)), int(os.environ.get("LOCAL_RANK", 0)), int(os.environ.get("WORLD_SIZE", 1))
 
 
-def kernel_hash() -> str:
+def kernel_hash(backward: bool = False) -> str:
     h = hashlib.sha256()
-    for f in (KERNEL_SRC, os.path.join(ROOT, "include", "attn_fwd.h")):
+    files = ((KERNEL_SRC.replace("attn_fwd.cu", "attn_bwd.cu"), os.path.join(ROOT, "include", "attn_bwd.h"))
+             if backward else (KERNEL_SRC, os.path.join(ROOT, "include", "attn_fwd.h")))
+    for f in files:
         h.update(open(f, "rb").read())
     return h.hexdigest()[:16]
 
@@ -169,6 +177,29 @@ def oracle_rows_fn(oracle, w, causal: bool, bias_kind: str, H1: int, nq: int):
     return oracle.attention_rows_causal if causal else oracle.attention_rows
 
 
+def cpu_oracle_backward_sample(w, target_seconds: float):
+    """Time the FP64 backward oracle on one head with nq of the workload's query rows (all Nk
+    keys, as dK and dV need every row); returns (TFLOPS at 2.5x forward FLOPs, rows, seconds,
+    threads)."""
+    import numpy as np
+
+    import oracle
+    from dense_attention_forward_fwd_gb300.inputs import make_qkv
+
+    def run(nq):
+        q, k, v = make_qkv(1, 1, nq, w.Nk, d=w.d, seed=w.seed, qk_mult=w.qk_mult)
+        do = np.random.Generator(np.random.PCG64(w.seed + 7)).standard_normal((1, 1, nq, w.d))
+        t = time.perf_counter()
+        oracle.attention_bwd(q, k, v, do, w.scale)
+        return time.perf_counter() - t
+
+    nq = min(w.Nq, 32)
+    dt = run(nq)
+    nq = int(min(w.Nq, max(nq, nq * target_seconds / max(dt, 1e-6))))
+    dt = run(nq)
+    return 2.5 * 4.0 * nq * w.Nk * w.d / dt / 1e12, nq, dt, oracle.max_threads()
+
+
 def cpu_oracle_sample(w, target_seconds: float, rank_seed: int = 0, causal: bool = False, bias_kind: str = "none"):
     """Time the FP64 oracle on a sample of query rows; returns (TFLOPS, rows, seconds, threads)."""
     import numpy as np
@@ -216,6 +247,28 @@ def run_reference(args, w):
     from dense_attention_forward_fwd_gb300.inputs import make_qkv
 
     steps, warm = args.steps, args.warmup
+    if args.backward:   # each step: the backward oracle on one head, sized to share ~2 minutes
+        total, flops_sum = 0.0, 0.0
+        for i in range(warm + steps):
+            tfl, n, dt, threads = cpu_oracle_backward_sample(w, 120.0 / (steps + warm))
+            if i >= warm:
+                total += dt
+                flops_sum += tfl * 1e12 * dt
+        ms = total / steps * 1e3
+        tflops = flops_sum / total / 1e12
+        sample = f"backward of one head with {n} query rows x {w.Nk} keys of {w.describe()} per step, FP64"
+        print(json.dumps({
+            "impl": "reference", "metric": METRIC, "value": tflops, "unit": "TFLOP/s", "n_gpus": world,
+            "steps": steps, "warmup": warm, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name, "B": w.B, "H": w.H, "Nq": w.Nq, "Nk": w.Nk, "d": w.d, "causal": False,
+                       "bias": "none", "pass": "backward", "qk_mult": w.qk_mult},
+            "cpu_baseline": {"value": tflops, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": tflops, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "gpu_launches": 0,
+        }), flush=True)
+        return 0
     H1 = w.H if w.B * w.H * w.Nk * w.d <= (1 << 26) else 1
     nq = min(w.Nq, 4096)
     q, k, v = make_qkv(1, H1, nq, w.Nk, d=w.d, seed=w.seed, qk_mult=w.qk_mult)
@@ -251,7 +304,7 @@ def run_reference(args, w):
         "steps": steps, "warmup": warm, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": w.name, "B": w.B, "H": w.H, "Nq": w.Nq, "Nk": w.Nk, "d": w.d, "causal": args.causal, "bias": args.bias,
-                   "qk_mult": w.qk_mult},
+                   "pass": "forward", "qk_mult": w.qk_mult},
         "cpu_baseline": {"value": tflops, "unit": "TFLOP/s", "cores": threads, "kind": "oracle", "sample": sample},
         "e2e": {"value": tflops, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
         "gpu_launches": 0,
@@ -293,38 +346,52 @@ def run_ours(args, w):
     flush = torch.empty(L2_FLUSH_BYTES // 4, device=dev, dtype=torch.int32)
     stream = torch.cuda.current_stream(dev)
 
-    if args.causal and args.bias != "none":
-        raise SystemExit("--causal and --bias are separate entry points; pick one")
+    if sum([args.causal, args.bias != "none", args.backward]) > 1:
+        raise SystemExit("--causal, --bias and --backward are separate entry points; pick one")
     ins = [q, k, v]
+    outs = [o, lse]
     if args.bias != "none":
         bshape = (1, 1, w.Nq, w.Nk) if args.bias == "shared" else (w.B, w.H, w.Nq, w.Nk)
         ins.append(torch.randn(bshape, device=dev, generator=g).to(torch.bfloat16))
+    if args.backward:   # the forward's O and LSE and an upstream gradient are the inputs
+        dout = torch.randn(w.B, w.H, w.Nq, w.d, device=dev, generator=g).to(torch.bfloat16)
+        attn.attn_fwd(q, k, v, o, lse, w.B, w.H, w.Nq, w.Nk, w.d, w.scale, stream)
+        ins = [q, k, v, o, dout, lse]
+        outs = [torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)]
 
-    def fwd(ins_, o_, lse_, st):
-        if args.bias != "none":
-            attn.attn_fwd_bias(ins_[0], ins_[1], ins_[2], ins_[3], o_, lse_, w.B, w.H, w.Nq, w.Nk, w.d, w.scale, st)
+    def call(ins_, outs_, st):
+        if args.backward:
+            attn.attn_bwd(*ins_, *outs_, w.B, w.H, w.Nq, w.Nk, w.d, w.scale, st)
+        elif args.bias != "none":
+            attn.attn_fwd_bias(ins_[0], ins_[1], ins_[2], ins_[3], *outs_, w.B, w.H, w.Nq, w.Nk, w.d, w.scale, st)
         elif args.causal:
-            attn.attn_fwd_causal(*ins_, o_, lse_, w.B, w.H, w.Nq, w.Nk, w.d, w.scale, st)
+            attn.attn_fwd_causal(*ins_, *outs_, w.B, w.H, w.Nq, w.Nk, w.d, w.scale, st)
         else:
-            attn.attn_fwd(*ins_, o_, lse_, w.B, w.H, w.Nq, w.Nk, w.d, w.scale, st)
+            attn.attn_fwd(*ins_, *outs_, w.B, w.H, w.Nq, w.Nk, w.d, w.scale, st)
 
-    flops = workload_flops(w, args.causal)
+    def kernel_count():
+        return attn.attn_fwd_kernel_count() + attn.attn_bwd_kernel_count()
+
+    def status_ok(st):
+        return attn.attn_fwd_status(st) == attn.ATTN_OK and attn.attn_bwd_status(st) == attn.ATTN_OK
+
+    flops = 2.5 * workload_flops(w, False) if args.backward else workload_flops(w, args.causal)
 
     def step():
-        fwd(ins, o, lse, stream)
+        call(ins, outs, stream)
 
     sampler = ClockSampler(local_rank)   # started early: nvidia-smi needs a moment to come up
     time.sleep(1.0)
     for _ in range(max(args.warmup, 3)):
         flush.zero_()
         step()
-    if attn.attn_fwd_status(stream) != attn.ATTN_OK:
+    if not status_ok(stream):
         raise RuntimeError("kernel reported a timeout during warm-up")
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     barrier()
     torch.cuda.synchronize()
-    launches0 = attn.attn_fwd_kernel_count()
+    launches0 = kernel_count()
     t0 = time.time()
     for i in range(args.steps):
         flush.zero_()
@@ -334,23 +401,23 @@ def run_ours(args, w):
     torch.cuda.synchronize()
     t1 = time.time()
     barrier()
-    launches = attn.attn_fwd_kernel_count() - launches0
+    launches = kernel_count() - launches0
     time.sleep(0.2)
     sampler.stop()
     clocks = sampler.summary(t0, t1)
     durs = [s.elapsed_time(e) for s, e in zip(starts, ends)]
     ms = sum(durs) / len(durs)
-    status = attn.attn_fwd_status(stream)
-    if status != attn.ATTN_OK:
-        raise RuntimeError(f"kernel status {attn.attn_status_string(status)}")
+    if not status_ok(stream):
+        raise RuntimeError("kernel reported a timeout")
 
-    # e2e through host buffers: every step copies its Q, K, V (and bias) from pinned host
-    # memory, calls the entry point and copies O and LSE back, all inside the timed region.
+    # e2e through host buffers: every step copies its inputs (Q, K, V, and the bias, or for
+    # the backward also O, dO and LSE) from pinned host memory, calls the entry point and
+    # copies its outputs (O and LSE, or dQ, dK, dV) back, all inside the timed region.
     # Steps are pipelined over three streams with two device buffer sets, as a serving loop
     # would run them: the H2D of step i+1 and the D2H of step i-1 overlap the kernel of step i.
     h_ins = [t.cpu().pin_memory() for t in ins]
-    ho, hl = torch.empty_like(o, device="cpu").pin_memory(), torch.empty_like(lse, device="cpu").pin_memory()
-    bufs = [([torch.empty_like(t) for t in ins], torch.empty_like(o), torch.empty_like(lse)) for _ in range(2)]
+    h_outs = [torch.empty_like(t, device="cpu").pin_memory() for t in outs]
+    bufs = [([torch.empty_like(t) for t in ins], [torch.empty_like(t) for t in outs]) for _ in range(2)]
     s_in, s_run, s_out = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
     ev_in = [torch.cuda.Event() for _ in range(2)]
     ev_done = [torch.cuda.Event() for _ in range(2)]
@@ -361,7 +428,7 @@ def run_ours(args, w):
     def e2e_steps(n):
         for i in range(n):
             b = i % 2
-            d_ins, do, dl = bufs[b]
+            d_ins, d_outs = bufs[b]
             s_in.wait_event(ev_done[b])                  # the kernel that read buffer set b is done
             with torch.cuda.stream(s_in):
                 for dst, src in zip(d_ins, h_ins):
@@ -369,12 +436,12 @@ def run_ours(args, w):
                 ev_in[b].record(s_in)
             s_run.wait_event(ev_in[b])
             s_run.wait_event(ev_out[b])                  # this output set has been copied out
-            fwd(d_ins, do, dl, s_run)
+            call(d_ins, d_outs, s_run)
             ev_done[b].record(s_run)
             s_out.wait_event(ev_done[b])
             with torch.cuda.stream(s_out):
-                ho.copy_(do, non_blocking=True)
-                hl.copy_(dl, non_blocking=True)
+                for dst, src in zip(h_outs, d_outs):
+                    dst.copy_(src, non_blocking=True)
                 ev_out[b].record(s_out)
 
     for st in (s_in, s_run, s_out):
@@ -393,10 +460,10 @@ def run_ours(args, w):
     torch.cuda.synchronize()
     e2e_ms = es.elapsed_time(ee) / args.e2e_steps
     # the last step's result, read back to the host, must be the device-timed leg's result
-    if not (torch.equal(ho, o.cpu()) and torch.equal(hl, lse.cpu())):
+    if not all(torch.equal(h, t.cpu()) for h, t in zip(h_outs, outs)):
         raise RuntimeError("end-to-end output differs from the device-resident run")
     h2d = sum(t.numel() * t.element_size() for t in h_ins)
-    d2h = ho.numel() * ho.element_size() + hl.numel() * hl.element_size()
+    d2h = sum(t.numel() * t.element_size() for t in h_outs)
 
     # max over ranks
     if pg is not None:
@@ -412,19 +479,21 @@ def run_ours(args, w):
     achieved = flops / (ms * 1e-3) / 1e12   # one launch on one GPU
     traffic = None
     if os.path.exists(TRAFFIC_FILE):
-        key = w.name + ("-causal" if args.causal else "") + ("" if args.bias == "none" else "-bias-" + args.bias)
+        key = (w.name + ("-causal" if args.causal else "") + ("" if args.bias == "none" else "-bias-" + args.bias)
+               + ("-backward" if args.backward else ""))
         rec = json.load(open(TRAFFIC_FILE)).get(key)
-        if rec and rec.get("kernel_hash") == kernel_hash():
+        if rec and rec.get("kernel_hash") == kernel_hash(args.backward):
             traffic = rec.get("bytes_per_launch")
 
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": ((value / PAGES_TFLOPS[w.name])
-                        if w.name in PAGES_TFLOPS and not args.causal and args.bias == "none" else None),
+                        if w.name in PAGES_TFLOPS and not args.causal and args.bias == "none" and not args.backward
+                        else None),
         "dtype": "bf16", "data": "synthetic",
         "config": {"workload": w.name, "B": w.B, "H": w.H, "Nq": w.Nq, "Nk": w.Nk, "d": w.d, "causal": args.causal, "bias": args.bias,
-                   "qk_mult": w.qk_mult, "inputs": "iid N(0,1) BF16 (Q,K x qk_mult)",
+                   "pass": "backward" if args.backward else "forward", "qk_mult": w.qk_mult, "inputs": "iid N(0,1) BF16 (Q,K x qk_mult)",
                    "l2": "flushed (512 MiB write) before every timed launch",
                    "vs_baseline_ref": "RTX 5090 v5 kernel, same shape (other hardware: context only)"},
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
@@ -436,10 +505,14 @@ def run_ours(args, w):
         "kernel_ms_min": min(durs), "kernel_ms_median": statistics.median(durs),
     }
     if rank == 0 and not args.no_cpu_baseline:
-        tfl, n, dt, thr = cpu_oracle_sample(w, args.cpu_seconds, causal=args.causal, bias_kind=args.bias)
-        keys = "visible keys of each row, causal" if args.causal else "full Nk each"
-        line["cpu_baseline"] = {"value": tfl, "unit": "TFLOP/s", "cores": thr, "kind": "oracle",
-                                "sample": f"{n} query rows of {w.describe()} ({keys}), FP64, {dt:.1f} s"}
+        if args.backward:
+            tfl, n, dt, thr = cpu_oracle_backward_sample(w, args.cpu_seconds)
+            sample = f"backward of one head with {n} query rows x {w.Nk} keys of {w.describe()}, FP64, {dt:.1f} s"
+        else:
+            tfl, n, dt, thr = cpu_oracle_sample(w, args.cpu_seconds, causal=args.causal, bias_kind=args.bias)
+            keys = "visible keys of each row, causal" if args.causal else "full Nk each"
+            sample = f"{n} query rows of {w.describe()} ({keys}), FP64, {dt:.1f} s"
+        line["cpu_baseline"] = {"value": tfl, "unit": "TFLOP/s", "cores": thr, "kind": "oracle", "sample": sample}
     if pg is not None:
         pg.barrier()
         pg.destroy_process_group()

@@ -16,7 +16,8 @@ from ._build import LIB_PATH, build_library
 __all__ = [
     "ATTN_OK", "ATTN_ERR_INVALID_ARG", "ATTN_ERR_UNSUPPORTED", "ATTN_ERR_MISALIGNED", "ATTN_ERR_CUDA",
     "ATTN_ERR_TIMEOUT", "AttnError", "load_library", "attn_fwd", "attn_fwd_causal", "attn_fwd_bias", "attn_fwd_noalloc", "attn_fwd_status", "attn_status_string",
-    "attn_fwd_set_wait_limit", "attn_fwd_kernel_count", "attention",
+    "attn_fwd_set_wait_limit", "attn_fwd_kernel_count", "attention", "attn_bwd", "attn_bwd_status",
+    "attn_bwd_kernel_count",
 ]
 
 ATTN_OK = 0
@@ -59,6 +60,12 @@ def load_library(build_if_stale: bool = True) -> ctypes.CDLL:
             lib.attn_fwd_set_wait_limit.restype = i32
             lib.attn_fwd_kernel_count.argtypes = []
             lib.attn_fwd_kernel_count.restype = ctypes.c_ulonglong
+            lib.attn_bwd.argtypes = [vp] * 9 + [i32] * 5 + [f32, vp]
+            lib.attn_bwd.restype = i32
+            lib.attn_bwd_status.argtypes = [vp]
+            lib.attn_bwd_status.restype = i32
+            lib.attn_bwd_kernel_count.argtypes = []
+            lib.attn_bwd_kernel_count.restype = ctypes.c_ulonglong
             _lib = lib
     return _lib
 
@@ -192,6 +199,35 @@ def attn_fwd_noalloc(q, k, v, o, lse, B: int, H: int, Nq: int, Nk: int, d: int, 
                               _stream_handle(stream, q, k, v, o, lse))
     if rc != ATTN_OK:
         raise AttnError(rc, "attn_fwd_noalloc")
+
+
+def attn_bwd(q, k, v, o, dout, lse, dq, dk, dv, B: int, H: int, Nq: int, Nk: int, d: int, scale: float,
+             stream=None) -> None:
+    """Enqueue the gradients dQ, dK, dV of the forward for upstream gradient ``dout`` (see
+    include/attn_bwd.h). q, o, dout, dq: BF16 [B,H,Nq,d]; k, v, dk, dv: BF16 [B,H,Nk,d];
+    lse: the forward's FP32 [B,H,Nq]. CUDA tensors or integer device pointers."""
+    lib = load_library()
+    args = (
+        _ptr(q, "q", B * H * Nq * d, "bf16"), _ptr(k, "k", B * H * Nk * d, "bf16"),
+        _ptr(v, "v", B * H * Nk * d, "bf16"), _ptr(o, "o", B * H * Nq * d, "bf16"),
+        _ptr(dout, "dout", B * H * Nq * d, "bf16"), _ptr(lse, "lse", B * H * Nq, "f32"),
+        _ptr(dq, "dq", B * H * Nq * d, "bf16"), _ptr(dk, "dk", B * H * Nk * d, "bf16"),
+        _ptr(dv, "dv", B * H * Nk * d, "bf16"),
+    )
+    rc = lib.attn_bwd(*args, int(B), int(H), int(Nq), int(Nk), int(d), float(scale),
+                      _stream_handle(stream, q, k, v, o, dout, lse, dq, dk, dv))
+    if rc != ATTN_OK:
+        raise AttnError(rc, "attn_bwd")
+
+
+def attn_bwd_status(stream=None) -> int:
+    """Synchronise ``stream`` and return (and clear) the backward kernels' timeout status."""
+    return load_library().attn_bwd_status(_stream_handle(stream))
+
+
+def attn_bwd_kernel_count() -> int:
+    """Backward kernel launches made by the library in this process."""
+    return int(load_library().attn_bwd_kernel_count())
 
 
 def attn_fwd_status(stream=None) -> int:

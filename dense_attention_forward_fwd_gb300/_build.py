@@ -1,4 +1,4 @@
-"""Build libattn_fwd.so in-tree with nvcc for sm_103a (GB300)."""
+"""Build libattn_fwd.so (forward and backward kernels) in-tree with nvcc for sm_103a (GB300)."""
 from __future__ import annotations
 
 import fcntl
@@ -8,8 +8,8 @@ import subprocess
 
 PKG = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(PKG)
-SOURCES = [os.path.join(PKG, "csrc", "attn_fwd.cu")]
-HEADERS = [os.path.join(ROOT, "include", "attn_fwd.h")]
+SOURCES = [os.path.join(PKG, "csrc", "attn_fwd.cu"), os.path.join(PKG, "csrc", "attn_bwd.cu")]
+HEADERS = [os.path.join(ROOT, "include", "attn_fwd.h"), os.path.join(ROOT, "include", "attn_bwd.h")]
 LIB_PATH = os.path.join(PKG, "libattn_fwd.so")
 
 NVCC_FLAGS = [

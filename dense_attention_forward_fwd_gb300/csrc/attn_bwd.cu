@@ -1,0 +1,735 @@
+// attn_bwd.cu -- dense BF16 attention backward for GB300 (sm_103a).
+//
+// Gradients of O = softmax(scale * Q K^T) V for an upstream gradient dO, head_dim 128,
+// with P recomputed from the forward's log-sum-exp ("FlashAttention'ı Anlamak Bölüm 1",
+// section 0 Giriş: recomputation instead of storing S or P):
+//
+//   D_i = dO_i . O_i,  P = 2^(s * scale * log2 e - LSE_i * log2 e),  dP = dO V^T,
+//   dS = P * (dP - D),  dV = P^T dO,  dK = scale * dS^T Q,  dQ = scale * dS K.
+//
+// Three kernels, all on the caller's stream:
+//
+//   bwd_rows_kernel  one warp per query row: D_i and LSE_i * log2 e, written as a float2
+//                    per row into a workspace padded to whole 128-row tiles (pad rows get
+//                    LSE = +inf, D = 0, so their P is exactly 0).
+//   bwd_dkdv_kernel  one block per (b, h, 128-key tile). K and V are loaded once; then per
+//                    128-query tile j (double-buffered Q_j, dO_j and the rows' float2 by
+//                    TMA): S^T = K Q_j^T and dP^T = V dO_j^T on tcgen05 into TMEM; four
+//                    compute warps (thread = key) form P^T and dS^T, write them back over
+//                    S^T and dP^T as BF16 pairs; then dV += P^T dO_j and dK += dS^T Q_j
+//                    take P^T and dS^T straight from TMEM (the A operand) with dO_j and Q_j
+//                    as MN-major B operands.
+//   bwd_dq_kernel    one block per (b, h, 128-query tile). Q and dO are loaded once; per
+//                    key tile j (double-buffered K_j, V_j): S = Q K_j^T, dP = dO V_j^T; the
+//                    compute warps (thread = query) form dS and write it over S; then
+//                    dQ += dS K_j.
+//
+// TMEM: dK/dV block: S^T | dP^T | dV | dK (4 x 128 columns); dQ block: S | dP | dQ.
+// Warp roles: warp 0 lane 0 issues TMA, warp 1 lane 0 issues MMAs (and owns TMEM),
+// warps 4-7 compute (warp 4 + q reads TMEM lanes 32q .. 32q + 31). The steps of a block
+// run one after another (S/dP MMAs, then the compute warps, then the accumulating MMAs);
+// ragged tails are zero-filled by TMA and masked. Every mbarrier wait is bounded: on
+// expiry the block raises an abort flag, sets the status word and winds down.
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <atomic>
+#include <climits>
+#include <cmath>
+#include <cstdint>
+#include <map>
+#include <mutex>
+#include <utility>
+
+#include "attn_bwd.h"
+
+namespace {
+
+constexpr int kD = 128;
+constexpr int kT = 128;                         // rows of a tile (queries or keys)
+constexpr int kTileBytes = kT * kD * 2;         // 32 KB of BF16
+constexpr int kBoxBytes = kTileBytes / 2;       // one TMA box: 64 columns (128 B) x 128 rows
+constexpr int kThreads = 256;
+constexpr int kTmemCols = 512;
+constexpr int kStageWarpBytes = 32 * 64 * 2;    // epilogue staging per compute warp
+constexpr unsigned long long kDefaultWaitLimit = 1ull << 31;
+constexpr float kLog2e = 1.4426950408889634f;
+
+// dK/dV block shared memory: K | V | 2 x (Q_j | dO_j | rows) | barriers | flags
+constexpr int kRowsBytes = kT * 8;              // float2 (LSE log2, D) per query row
+constexpr int kKVOffK = 0;
+constexpr int kKVOffV = kTileBytes;
+constexpr int kKVOffStage = 2 * kTileBytes;
+constexpr int kKVStageBytes = 2 * kTileBytes + kRowsBytes;   // 1024-aligned (66,560)
+constexpr int kKVOffBar = kKVOffStage + 2 * kKVStageBytes;
+// dQ block shared memory: Q | dO | 2 x (K_j | V_j) | barriers | flags
+constexpr int kQOffQ = 0;
+constexpr int kQOffDO = kTileBytes;
+constexpr int kQOffStage = 2 * kTileBytes;
+constexpr int kQStageBytes = 2 * kTileBytes;
+constexpr int kQOffBar = kQOffStage + 2 * kQStageBytes;
+
+// barriers (both kernels)
+constexpr int kBarFixed = 0;        // the block's fixed tiles (K, V or Q, dO) have landed
+constexpr int kBarFull = 1;         // [2] stage landed
+constexpr int kBarEmpty = 3;        // [2] stage consumed by the MMAs
+constexpr int kBarSdP = 5;          // S and dP complete in TMEM
+constexpr int kBarPdS = 6;          // compute warps wrote P / dS (one arrival per warp)
+constexpr int kBarAcc = 7;          // accumulators complete
+constexpr int kNumBars = 8;
+constexpr int kFlagsBytes = kNumBars * 8 + 16;   // barriers, TMEM slot, abort flag
+
+constexpr int kKVSmem = kKVOffBar + kFlagsBytes + 1024;
+constexpr int kQSmem = kQOffBar + kFlagsBytes + 1024;
+static_assert(kKVStageBytes % 1024 == 0, "stage tiles need 1024-byte alignment");
+static_assert(kKVSmem <= 232448 && kQSmem <= 232448, "exceeds the 227 KB shared memory of one block");
+static_assert(4 * kStageWarpBytes <= kTileBytes, "epilogue staging reuses one tile");
+
+__device__ unsigned int g_bwd_status;   // bit 0: a wait timed out
+
+// ---------------------------------------------------------------------------------
+// PTX wrappers (the same instruction forms as the forward kernel)
+// ---------------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int x, int y,
+                                            int z) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "r"(z)
+      : "memory");
+}
+// contiguous global -> shared copy (16-byte aligned addresses, size a multiple of 16)
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+               "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+               : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+               : "memory");
+}
+__device__ __forceinline__ void mma_ss(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, bool acc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
+      "l"(a), "l"(b), "r"(idesc), "r"(static_cast<uint32_t>(acc))
+      : "memory");
+}
+__device__ __forceinline__ void mma_ts(uint32_t d, uint32_t a, uint64_t b, uint32_t idesc, bool acc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d),
+      "r"(a), "l"(b), "r"(idesc), "r"(static_cast<uint32_t>(acc))
+      : "memory");
+}
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&x)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+      "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(x[0]), "=r"(x[1]), "=r"(x[2]), "=r"(x[3]), "=r"(x[4]), "=r"(x[5]), "=r"(x[6]), "=r"(x[7]),
+        "=r"(x[8]), "=r"(x[9]), "=r"(x[10]), "=r"(x[11]), "=r"(x[12]), "=r"(x[13]), "=r"(x[14]), "=r"(x[15]),
+        "=r"(x[16]), "=r"(x[17]), "=r"(x[18]), "=r"(x[19]), "=r"(x[20]), "=r"(x[21]), "=r"(x[22]), "=r"(x[23]),
+        "=r"(x[24]), "=r"(x[25]), "=r"(x[26]), "=r"(x[27]), "=r"(x[28]), "=r"(x[29]), "=r"(x[30]), "=r"(x[31])
+      : "r"(taddr)
+      : "memory");
+}
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&x)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, "
+      "%14, %15, %16};\n\t"
+      "tcgen05.wait::st.sync.aligned;" ::"r"(taddr),
+      "r"(x[0]), "r"(x[1]), "r"(x[2]), "r"(x[3]), "r"(x[4]), "r"(x[5]), "r"(x[6]), "r"(x[7]), "r"(x[8]),
+      "r"(x[9]), "r"(x[10]), "r"(x[11]), "r"(x[12]), "r"(x[13]), "r"(x[14]), "r"(x[15])
+      : "memory");
+}
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+// two floats -> packed BF16x2 (round to nearest even), lo in the low half
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// 128B-swizzled operand descriptor: start address, leading / stride byte offsets,
+// descriptor version 1 (bits 46-48), swizzle mode 2 = 128B (bits 61-63).
+__device__ __forceinline__ uint64_t sdesc_sw128(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+  return static_cast<uint64_t>((addr >> 4) & 0x3FFFu) | (static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16) |
+         (static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
+}
+// BF16 x BF16 -> FP32, M = N = 128, A K-major, B K-major or MN-major.
+__host__ __device__ constexpr uint32_t idesc_bf16(bool b_mn_major) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((b_mn_major ? 1u : 0u) << 16) | (static_cast<uint32_t>(kT >> 3) << 17) |
+         (static_cast<uint32_t>(kT >> 4) << 24);
+}
+// D = A B^T over d = 128 with both tiles row-major [128][d] in smem (two 64-column
+// boxes each, 128B swizzle): S^T = K Q^T, dP^T = V dO^T, S = Q K^T, dP = dO V^T.
+__device__ __forceinline__ void mma_rows_by_rows(uint32_t d_tmem, uint32_t a_smem, uint32_t b_smem) {
+  constexpr uint32_t idesc = idesc_bf16(false);
+#pragma unroll
+  for (int kk = 0; kk < kD / 16; ++kk) {
+    const uint32_t off = static_cast<uint32_t>((kk >> 2) * kBoxBytes + (kk & 3) * 32);
+    mma_ss(d_tmem, sdesc_sw128(a_smem + off, 16, 1024), sdesc_sw128(b_smem + off, 16, 1024), idesc, kk > 0);
+  }
+}
+// D (+)= A B with A (128 x 128) in TMEM as packed BF16 pairs (8 columns per 16 of K) and
+// B a row-major [128][d] tile in smem (K along rows: MN-major): dV += P^T dO, dK += dS^T Q,
+// dQ += dS K.
+__device__ __forceinline__ void mma_tmem_by_rows(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_smem, bool acc) {
+  constexpr uint32_t idesc = idesc_bf16(true);
+#pragma unroll
+  for (int kk = 0; kk < kT / 16; ++kk)
+    mma_ts(d_tmem, a_tmem + kk * 8, sdesc_sw128(b_smem + kk * 16 * 128, kBoxBytes, 1024), idesc, acc || kk > 0);
+}
+
+// ---------------------------------------------------------------------------------
+// Bounded waits
+// ---------------------------------------------------------------------------------
+struct Ctl {
+  uint32_t bars;
+  volatile uint32_t* abort;
+  unsigned long long limit;
+  __device__ __forceinline__ uint32_t bar(int i) const { return bars + 8u * static_cast<uint32_t>(i); }
+};
+__device__ __forceinline__ bool wait_phase(const Ctl& c, int idx, uint32_t parity, bool watch_abort) {
+  const uint32_t b = c.bar(idx);
+  if (mbar_try_wait(b, parity)) return true;
+  const long long t0 = clock64();
+  for (;;) {
+    if (mbar_try_wait(b, parity)) return true;
+    if (watch_abort && *c.abort) return false;
+    if (static_cast<unsigned long long>(clock64() - t0) > c.limit) {
+      *c.abort = 1u;
+      atomicOr(&g_bwd_status, 1u);
+      return false;
+    }
+  }
+}
+// warp-uniform result (the callers' next step is a .sync.aligned TMEM access)
+__device__ __forceinline__ bool wait_warp(const Ctl& c, int idx, uint32_t parity) {
+  const bool ok = wait_phase(c, idx, parity, true);
+  return __all_sync(0xffffffffu, ok);
+}
+
+struct BwdParams {
+  uint16_t* dq;
+  uint16_t* dk;
+  uint16_t* dv;
+  const float2* rows;   // [BH, q_pad]: (LSE * log2 e, D)
+  int Nq, Nk, q_tiles, k_tiles, q_pad;
+  float scale, scale_log2;
+  unsigned long long wait_limit;
+};
+
+// Stores one 64-column half of this warp's 32 rows (pk: the thread's own row, packed
+// BF16 pairs) through the warp's staging tile so that each global store instruction
+// covers four whole 128-byte lines. Rows from valid_rows on are not stored.
+__device__ __forceinline__ void store_half_rows(uint8_t* stage, const uint32_t (&pk)[32], uint16_t* row0,
+                                                int valid_rows, int half) {
+  const int lane = threadIdx.x & 31;
+  uint4* st = reinterpret_cast<uint4*>(stage);
+#pragma unroll
+  for (int k = 0; k < 8; ++k)
+    st[lane * 8 + (k ^ (lane & 7))] = make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
+  __syncwarp();
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int rr = i * 4 + (lane >> 3), cc = lane & 7;
+    const uint4 v = st[rr * 8 + (cc ^ (rr & 7))];
+    if (rr < valid_rows) reinterpret_cast<uint4*>(row0 + static_cast<size_t>(rr) * kD + half * 64)[cc] = v;
+  }
+  __syncwarp();
+}
+
+// Writes this thread's accumulator row (128 FP32 TMEM columns at t_acc) times `mul` as
+// BF16 to row0[lane] .. (the warp's 32 rows).
+__device__ __forceinline__ void store_acc_rows(uint32_t t_acc, float mul, uint8_t* stage, uint16_t* row0,
+                                               int valid_rows) {
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    uint32_t pk[32];
+#pragma unroll
+    for (int c2 = 0; c2 < 2; ++c2) {
+      uint32_t x[32];
+      tmem_ld32(t_acc + h * 64 + c2 * 32, x);
+#pragma unroll
+      for (int i = 0; i < 16; ++i)
+        pk[c2 * 16 + i] = pack_bf16(__uint_as_float(x[2 * i]) * mul, __uint_as_float(x[2 * i + 1]) * mul);
+    }
+    store_half_rows(stage, pk, row0, valid_rows, h);
+  }
+}
+
+// Block setup shared by both kernels: barrier init, TMEM allocation. Returns the TMEM base.
+__device__ __forceinline__ uint32_t block_setup(const Ctl& c, uint8_t* flags, uint32_t flags_u32, int warp) {
+  if (threadIdx.x == 0) {
+    mbar_init(c.bar(kBarFixed), 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(c.bar(kBarFull + s), 1);
+      mbar_init(c.bar(kBarEmpty + s), 1);
+    }
+    mbar_init(c.bar(kBarSdP), 1);
+    mbar_init(c.bar(kBarPdS), 4);   // one arrival per compute warp
+    mbar_init(c.bar(kBarAcc), 1);
+    *c.abort = 0u;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(flags_u32 + kNumBars * 8),
+                 "r"(kTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  return *reinterpret_cast<volatile uint32_t*>(flags + kNumBars * 8);
+}
+
+__device__ __forceinline__ void block_teardown(uint32_t tmem, int warp) {
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
+  }
+}
+
+// ---------------------------------------------------------------------------------
+// Row pass: (LSE_i log2 e, D_i = dO_i . O_i) per query row, pad rows (+inf, 0)
+// ---------------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) bwd_rows_kernel(const uint16_t* __restrict__ o, const uint16_t* __restrict__ dout,
+                                                       const float* __restrict__ lse, float2* __restrict__ rows,
+                                                       long long bh_count, int Nq, int q_pad) {
+  const long long row = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (row >= bh_count * q_pad) return;
+  const long long bh = row / q_pad;
+  const int i = static_cast<int>(row - bh * q_pad);
+  if (i >= Nq) {
+    if (lane == 0) rows[row] = make_float2(INFINITY, 0.0f);
+    return;
+  }
+  const size_t base = (static_cast<size_t>(bh) * Nq + i) * kD + lane * 4;
+  const uint2 a = *reinterpret_cast<const uint2*>(o + base);
+  const uint2 b = *reinterpret_cast<const uint2*>(dout + base);
+  float acc = __uint_as_float(a.x << 16) * __uint_as_float(b.x << 16) +
+              __uint_as_float(a.x & 0xffff0000u) * __uint_as_float(b.x & 0xffff0000u) +
+              __uint_as_float(a.y << 16) * __uint_as_float(b.y << 16) +
+              __uint_as_float(a.y & 0xffff0000u) * __uint_as_float(b.y & 0xffff0000u);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+  if (lane == 0) rows[row] = make_float2(lse[static_cast<size_t>(bh) * Nq + i] * kLog2e, acc);
+}
+
+// ---------------------------------------------------------------------------------
+// dK / dV: one block per (b, h, key tile)
+// ---------------------------------------------------------------------------------
+__global__ void __launch_bounds__(kThreads, 1)
+    bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                    const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
+                    const BwdParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* smem = smem_raw + (base - raw);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int kt = blockIdx.x % p.k_tiles;
+  const int bh = blockIdx.x / p.k_tiles;
+  Ctl c;
+  c.bars = base + kKVOffBar;
+  c.abort = reinterpret_cast<volatile uint32_t*>(smem + kKVOffBar + kNumBars * 8 + 4);
+  c.limit = p.wait_limit;
+  const uint32_t tmem = block_setup(c, smem + kKVOffBar, base + kKVOffBar, warp);
+  const uint32_t tS = tmem, tdP = tmem + 128, tdV = tmem + 256, tdK = tmem + 384;
+  const int nq = p.q_tiles;
+  auto stage = [&](int s) { return base + kKVOffStage + s * kKVStageBytes; };   // Q | dO | rows
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // K and V of this tile, then per query tile Q_j, dO_j and the rows' (LSE, D)
+      mbar_arrive_expect_tx(c.bar(kBarFixed), 2 * kTileBytes);
+      for (int h = 0; h < 2; ++h) {
+        tma_load_3d(base + kKVOffK + h * kBoxBytes, &tmK, c.bar(kBarFixed), h * 64, kt * kT, bh);
+        tma_load_3d(base + kKVOffV + h * kBoxBytes, &tmV, c.bar(kBarFixed), h * 64, kt * kT, bh);
+      }
+      int issued = 0;
+      for (int j = 0; j < nq; ++j, ++issued) {
+        const int s = j & 1;
+        if (j >= 2 && !wait_phase(c, kBarEmpty + s, ((j >> 1) - 1) & 1, true)) break;
+        const uint32_t fb = c.bar(kBarFull + s);
+        mbar_arrive_expect_tx(fb, 2 * kTileBytes + kRowsBytes);
+        for (int h = 0; h < 2; ++h) {
+          tma_load_3d(stage(s) + h * kBoxBytes, &tmQ, fb, h * 64, j * kT, bh);
+          tma_load_3d(stage(s) + kTileBytes + h * kBoxBytes, &tmDO, fb, h * 64, j * kT, bh);
+        }
+        bulk_load(stage(s) + 2 * kTileBytes, p.rows + static_cast<size_t>(bh) * p.q_pad + static_cast<size_t>(j) * kT,
+                  kRowsBytes, fb);
+      }
+      // no copy into shared memory may be in flight when the block exits
+      wait_phase(c, kBarFixed, 0, false);
+      for (int j = issued - 2 < 0 ? 0 : issued - 2; j < issued; ++j)
+        wait_phase(c, kBarFull + (j & 1), (j >> 1) & 1, false);
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    if (lane == 0) {
+      bool ok = wait_phase(c, kBarFixed, 0, true);
+      for (int j = 0; ok && j < nq; ++j) {
+        const int s = j & 1;
+        if (!wait_phase(c, kBarFull + s, (j >> 1) & 1, true)) break;
+        tc_fence_after();
+        mma_rows_by_rows(tS, base + kKVOffK, stage(s));                   // S^T = K Q_j^T
+        mma_rows_by_rows(tdP, base + kKVOffV, stage(s) + kTileBytes);     // dP^T = V dO_j^T
+        tc_commit(c.bar(kBarSdP));
+        if (!wait_phase(c, kBarPdS, j & 1, true)) break;
+        tc_fence_after();
+        mma_tmem_by_rows(tdV, tS, stage(s) + kTileBytes, j > 0);        // dV += P^T dO_j
+        mma_tmem_by_rows(tdK, tdP, stage(s), j > 0);                    // dK += dS^T Q_j
+        tc_commit(c.bar(kBarEmpty + s));
+      }
+      tc_commit(c.bar(kBarAcc));   // also: every MMA this thread issued is done before TMEM is freed
+      wait_phase(c, kBarAcc, 0, false);
+    }
+    __syncwarp();
+  } else if (warp >= 4) {
+    const int quarter = warp & 3;
+    const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+    bool ok = true;
+    for (int j = 0; j < nq; ++j) {
+      const int s = j & 1;
+      // the rows' (LSE, D) arrive with the stage; S^T and dP^T once the MMAs are done
+      if (!wait_warp(c, kBarFull + s, (j >> 1) & 1) || !wait_warp(c, kBarSdP, j & 1)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const float2* rw = reinterpret_cast<const float2*>(smem + kKVOffStage + s * kKVStageBytes + 2 * kTileBytes);
+#pragma unroll 1
+      for (int ch = 0; ch < 4; ++ch) {   // 32 query columns at a time
+        uint32_t xs[32], xd[32];
+        tmem_ld32(tS + lane_off + ch * 32, xs);
+        tmem_ld32(tdP + lane_off + ch * 32, xd);
+        uint32_t pw[16], dw[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const float2 r0 = rw[ch * 32 + 2 * i], r1 = rw[ch * 32 + 2 * i + 1];
+          const float p0 = ex2(fmaf(__uint_as_float(xs[2 * i]), p.scale_log2, -r0.x));
+          const float p1 = ex2(fmaf(__uint_as_float(xs[2 * i + 1]), p.scale_log2, -r1.x));
+          const float d0 = p0 * (__uint_as_float(xd[2 * i]) - r0.y);
+          const float d1 = p1 * (__uint_as_float(xd[2 * i + 1]) - r1.y);
+          pw[i] = pack_bf16(p0, p1);
+          dw[i] = pack_bf16(d0, d1);
+        }
+        // columns 16 ch .. 16 ch + 15 were read in this or an earlier chunk
+        tmem_st16(tS + lane_off + ch * 16, pw);
+        tmem_st16(tdP + lane_off + ch * 16, dw);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(c.bar(kBarPdS));
+      __syncwarp();
+    }
+    if (ok && wait_warp(c, kBarAcc, 0)) {
+      tc_fence_after();
+      const int row0 = kt * kT + quarter * 32;   // the warp's first key
+      const int valid = p.Nk - row0;
+      uint8_t* st = smem + kKVOffK + quarter * kStageWarpBytes;   // K is no longer read
+      const size_t off = (static_cast<size_t>(bh) * p.Nk + row0) * kD;
+      store_acc_rows(tdV + lane_off, 1.0f, st, p.dv + off, valid);
+      store_acc_rows(tdK + lane_off, p.scale, st, p.dk + off, valid);
+    }
+  }
+  block_teardown(tmem, warp);
+}
+
+// ---------------------------------------------------------------------------------
+// dQ: one block per (b, h, query tile)
+// ---------------------------------------------------------------------------------
+__global__ void __launch_bounds__(kThreads, 1)
+    bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                  const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
+                  const BwdParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* smem = smem_raw + (base - raw);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int qt = blockIdx.x % p.q_tiles;
+  const int bh = blockIdx.x / p.q_tiles;
+  Ctl c;
+  c.bars = base + kQOffBar;
+  c.abort = reinterpret_cast<volatile uint32_t*>(smem + kQOffBar + kNumBars * 8 + 4);
+  c.limit = p.wait_limit;
+  const uint32_t tmem = block_setup(c, smem + kQOffBar, base + kQOffBar, warp);
+  const uint32_t tS = tmem, tdP = tmem + 128, tdQ = tmem + 256;
+  const int nk = p.k_tiles;
+  auto stage = [&](int s) { return base + kQOffStage + s * kQStageBytes; };   // K | V
+
+  if (warp == 0) {
+    if (lane == 0) {
+      mbar_arrive_expect_tx(c.bar(kBarFixed), 2 * kTileBytes);
+      for (int h = 0; h < 2; ++h) {
+        tma_load_3d(base + kQOffQ + h * kBoxBytes, &tmQ, c.bar(kBarFixed), h * 64, qt * kT, bh);
+        tma_load_3d(base + kQOffDO + h * kBoxBytes, &tmDO, c.bar(kBarFixed), h * 64, qt * kT, bh);
+      }
+      int issued = 0;
+      for (int j = 0; j < nk; ++j, ++issued) {
+        const int s = j & 1;
+        if (j >= 2 && !wait_phase(c, kBarEmpty + s, ((j >> 1) - 1) & 1, true)) break;
+        const uint32_t fb = c.bar(kBarFull + s);
+        mbar_arrive_expect_tx(fb, 2 * kTileBytes);
+        for (int h = 0; h < 2; ++h) {
+          tma_load_3d(stage(s) + h * kBoxBytes, &tmK, fb, h * 64, j * kT, bh);
+          tma_load_3d(stage(s) + kTileBytes + h * kBoxBytes, &tmV, fb, h * 64, j * kT, bh);
+        }
+      }
+      wait_phase(c, kBarFixed, 0, false);
+      for (int j = issued - 2 < 0 ? 0 : issued - 2; j < issued; ++j)
+        wait_phase(c, kBarFull + (j & 1), (j >> 1) & 1, false);
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    if (lane == 0) {
+      bool ok = wait_phase(c, kBarFixed, 0, true);
+      for (int j = 0; ok && j < nk; ++j) {
+        const int s = j & 1;
+        if (!wait_phase(c, kBarFull + s, (j >> 1) & 1, true)) break;
+        tc_fence_after();
+        mma_rows_by_rows(tS, base + kQOffQ, stage(s));                    // S = Q K_j^T
+        mma_rows_by_rows(tdP, base + kQOffDO, stage(s) + kTileBytes);     // dP = dO V_j^T
+        tc_commit(c.bar(kBarSdP));
+        if (!wait_phase(c, kBarPdS, j & 1, true)) break;
+        tc_fence_after();
+        mma_tmem_by_rows(tdQ, tS, stage(s), j > 0);                       // dQ += dS K_j
+        tc_commit(c.bar(kBarEmpty + s));
+      }
+      tc_commit(c.bar(kBarAcc));
+      wait_phase(c, kBarAcc, 0, false);
+    }
+    __syncwarp();
+  } else if (warp >= 4) {
+    const int quarter = warp & 3;
+    const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+    const int qrow = qt * kT + quarter * 32 + lane;
+    float2 rw = make_float2(0.0f, 0.0f);   // rows past Nq: any finite values (never stored)
+    if (qrow < p.Nq) rw = p.rows[static_cast<size_t>(bh) * p.q_pad + qrow];
+    bool ok = true;
+    for (int j = 0; j < nk; ++j) {
+      if (!wait_warp(c, kBarSdP, j & 1)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const int valid = p.Nk - j * kT;   // keys of this tile inside the sequence
+#pragma unroll 1
+      for (int ch = 0; ch < 4; ++ch) {
+        uint32_t xs[32], xd[32];
+        tmem_ld32(tS + lane_off + ch * 32, xs);
+        tmem_ld32(tdP + lane_off + ch * 32, xd);
+        uint32_t dw[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const int key = ch * 32 + 2 * i;
+          const float p0 = key < valid ? ex2(fmaf(__uint_as_float(xs[2 * i]), p.scale_log2, -rw.x)) : 0.0f;
+          const float p1 = key + 1 < valid ? ex2(fmaf(__uint_as_float(xs[2 * i + 1]), p.scale_log2, -rw.x)) : 0.0f;
+          dw[i] = pack_bf16(p0 * (__uint_as_float(xd[2 * i]) - rw.y), p1 * (__uint_as_float(xd[2 * i + 1]) - rw.y));
+        }
+        tmem_st16(tS + lane_off + ch * 16, dw);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(c.bar(kBarPdS));
+      __syncwarp();
+    }
+    if (ok && wait_warp(c, kBarAcc, 0)) {
+      tc_fence_after();
+      const int row0 = qt * kT + quarter * 32;
+      uint8_t* st = smem + kQOffQ + quarter * kStageWarpBytes;   // Q is no longer read
+      store_acc_rows(tdQ + lane_off, p.scale, st, p.dq + (static_cast<size_t>(bh) * p.Nq + row0) * kD,
+                     p.Nq - row0);
+    }
+  }
+  block_teardown(tmem, warp);
+}
+
+// ---------------------------------------------------------------------------------
+// Host side
+// ---------------------------------------------------------------------------------
+std::atomic<unsigned long long> g_bwd_launches{0};
+std::atomic<unsigned long long> g_bwd_wait_limit{kDefaultWaitLimit};
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+PFN_cuTensorMapEncodeTiled_v12000 encoder() {
+  std::call_once(g_encode_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  return g_encode;
+}
+
+// [BH, rows, 128] BF16 viewed as a 3-D tensor (d innermost); box = 64 columns x 128 rows x 1.
+bool make_map(CUtensorMap* map, const void* ptr, int rows, long long bh) {
+  auto enc = encoder();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(kD), static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(bh)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(kD) * 2, static_cast<cuuint64_t>(rows) * kD * 2};
+  cuuint32_t box[3] = {64, static_cast<cuuint32_t>(kT), 1};
+  cuuint32_t elem[3] = {1, 1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, elem,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Workspace of the row pass, per (device, stream); calls on one stream are ordered.
+std::mutex g_ws_mu;
+std::map<std::pair<int, uintptr_t>, std::pair<void*, size_t>> g_ws;
+
+int get_rows_workspace(int dev, cudaStream_t stream, size_t bytes, float2** out) {
+  std::lock_guard<std::mutex> lock(g_ws_mu);
+  auto& ws = g_ws[std::make_pair(dev, reinterpret_cast<uintptr_t>(stream))];
+  if (ws.second < bytes) {
+    if (ws.first) cudaFreeAsync(ws.first, stream);
+    ws.first = nullptr;
+    ws.second = 0;
+    if (cudaMallocAsync(&ws.first, bytes, stream) != cudaSuccess) return ATTN_ERR_CUDA;
+    ws.second = bytes;
+  }
+  *out = static_cast<float2*>(ws.first);
+  return ATTN_OK;
+}
+
+std::atomic<int> g_attr_done{0};
+
+}  // namespace
+
+extern "C" int attn_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                        const float* lse, void* dq, void* dk, void* dv, int B, int H, int Nq, int Nk, int d,
+                        float scale, void* stream) {
+  if (B < 0 || H < 0 || Nq < 0 || Nk < 0) return ATTN_ERR_INVALID_ARG;
+  if (d != kD) return ATTN_ERR_UNSUPPORTED;
+  if (!std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
+  const long long bh = static_cast<long long>(B) * H;
+  if (bh == 0 || Nq == 0) return ATTN_OK;
+  if (Nk == 0) return ATTN_ERR_INVALID_ARG;
+  if (!q || !k || !v || !o || !dout || !lse || !dq || !dk || !dv) return ATTN_ERR_INVALID_ARG;
+  const uintptr_t a16 = reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) |
+                        reinterpret_cast<uintptr_t>(v) | reinterpret_cast<uintptr_t>(o) |
+                        reinterpret_cast<uintptr_t>(dout) | reinterpret_cast<uintptr_t>(dq) |
+                        reinterpret_cast<uintptr_t>(dk) | reinterpret_cast<uintptr_t>(dv);
+  if ((a16 & 15u) || (reinterpret_cast<uintptr_t>(lse) & 3u)) return ATTN_ERR_MISALIGNED;
+  const long long q_tiles = (static_cast<long long>(Nq) + kT - 1) / kT;
+  const long long k_tiles = (static_cast<long long>(Nk) + kT - 1) / kT;
+  if (bh * q_tiles > INT_MAX || bh * k_tiles > INT_MAX || q_tiles * kT > INT_MAX) return ATTN_ERR_UNSUPPORTED;
+  if ((bh * q_tiles * kT + 7) / 8 > INT_MAX) return ATTN_ERR_UNSUPPORTED;   // the row pass's grid
+  const long long max_rows = static_cast<long long>(Nq > Nk ? Nq : Nk);
+  if (bh > (LLONG_MAX / 256) / max_rows) return ATTN_ERR_INVALID_ARG;
+
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return ATTN_ERR_CUDA;
+  CUtensorMap mq, mk, mv, mdo;
+  if (!make_map(&mq, q, Nq, bh) || !make_map(&mk, k, Nk, bh) || !make_map(&mv, v, Nk, bh) ||
+      !make_map(&mdo, dout, Nq, bh))
+    return ATTN_ERR_CUDA;
+
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  BwdParams p;
+  p.dq = static_cast<uint16_t*>(dq);
+  p.dk = static_cast<uint16_t*>(dk);
+  p.dv = static_cast<uint16_t*>(dv);
+  p.Nq = Nq;
+  p.Nk = Nk;
+  p.q_tiles = static_cast<int>(q_tiles);
+  p.k_tiles = static_cast<int>(k_tiles);
+  p.q_pad = static_cast<int>(q_tiles * kT);
+  p.scale = scale;
+  p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+  p.wait_limit = g_bwd_wait_limit.load(std::memory_order_relaxed);
+  float2* rows = nullptr;
+  {
+    const int rc = get_rows_workspace(dev, s, static_cast<size_t>(bh) * p.q_pad * sizeof(float2), &rows);
+    if (rc != ATTN_OK) return rc;
+  }
+  p.rows = rows;
+
+  if (!g_attr_done.load(std::memory_order_acquire)) {
+    if (cudaFuncSetAttribute(bwd_dkdv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kKVSmem) != cudaSuccess ||
+        cudaFuncSetAttribute(bwd_dq_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kQSmem) != cudaSuccess)
+      return ATTN_ERR_CUDA;
+    g_attr_done.store(1, std::memory_order_release);
+  }
+  const long long n_rows = bh * p.q_pad;
+  bwd_rows_kernel<<<static_cast<unsigned>((n_rows + 7) / 8), 256, 0, s>>>(
+      static_cast<const uint16_t*>(o), static_cast<const uint16_t*>(dout), lse, rows, bh, Nq, p.q_pad);
+  if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
+  g_bwd_launches.fetch_add(1, std::memory_order_relaxed);
+
+  cudaLaunchConfig_t cfg = {};
+  cfg.blockDim = dim3(kThreads);
+  cfg.stream = s;
+  cfg.gridDim = dim3(static_cast<unsigned>(bh * k_tiles));
+  cfg.dynamicSmemBytes = kKVSmem;
+  if (cudaLaunchKernelEx(&cfg, bwd_dkdv_kernel, mq, mk, mv, mdo, p) != cudaSuccess) return ATTN_ERR_CUDA;
+  g_bwd_launches.fetch_add(1, std::memory_order_relaxed);
+  cfg.gridDim = dim3(static_cast<unsigned>(bh * q_tiles));
+  cfg.dynamicSmemBytes = kQSmem;
+  if (cudaLaunchKernelEx(&cfg, bwd_dq_kernel, mq, mk, mv, mdo, p) != cudaSuccess) return ATTN_ERR_CUDA;
+  g_bwd_launches.fetch_add(1, std::memory_order_relaxed);
+  return ATTN_OK;
+}
+
+extern "C" int attn_bwd_status(void* stream) {
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  unsigned int h = 0;
+  if (cudaMemcpyFromSymbolAsync(&h, g_bwd_status, sizeof h, 0, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return ATTN_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return ATTN_ERR_CUDA;
+  if (h == 0) return ATTN_OK;
+  const unsigned int zero = 0;
+  if (cudaMemcpyToSymbolAsync(g_bwd_status, &zero, sizeof zero, 0, cudaMemcpyHostToDevice, s) != cudaSuccess ||
+      cudaStreamSynchronize(s) != cudaSuccess)
+    return ATTN_ERR_CUDA;
+  return ATTN_ERR_TIMEOUT;
+}
+
+extern "C" unsigned long long attn_bwd_kernel_count(void) { return g_bwd_launches.load(std::memory_order_relaxed); }

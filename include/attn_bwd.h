@@ -1,0 +1,67 @@
+/*
+ * attn_bwd.h -- C ABI of the dense BF16 attention backward pass for GB300 (sm_103a).
+ *
+ * The notes on the method name the backward pass and recomputation as part of it
+ * ("FlashAttention'ı Anlamak Bölüm 1", section 0 Giriş) without giving formulas; what it
+ * computes is the gradient of the forward of attn_fwd.h (S = scale * Q K^T,
+ * P = softmax_row(S), O = P V) for an upstream gradient dO:
+ *
+ *   D_i = sum_c dO[i,c] O[i,c]                     (= sum_j P_ij dP_ij)
+ *   P   = exp(scale * Q K^T - LSE)                  recomputed from the forward's LSE
+ *   dV  = P^T dO,   dP = dO V^T,   dS = P * (dP - D)
+ *   dQ  = scale * dS K,   dK = scale * dS^T Q
+ *
+ * S and P are recomputed tile by tile on the tensor cores and never reach HBM.
+ *
+ * Return values: the ATTN_* codes of attn_fwd.h.
+ */
+#ifndef ATTN_BWD_H
+#define ATTN_BWD_H
+
+#include "attn_fwd.h"
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/*
+ * attn_bwd -- gradients of the non-causal forward (no bias).
+ *
+ *   q, k, v   device, BF16, [B, H, Nq | Nk | Nk, d] contiguous, read only (the forward's inputs)
+ *   o         device, BF16, [B, H, Nq, d], the forward's output
+ *   dout      device, BF16, [B, H, Nq, d], the upstream gradient dO
+ *   lse       device, FP32, [B, H, Nq], the forward's log-sum-exp (natural log)
+ *   dq        device, BF16, [B, H, Nq, d], written
+ *   dk, dv    device, BF16, [B, H, Nk, d], written
+ *   scale     the forward's scale (finite)
+ *   stream    cudaStream_t (0 = legacy default stream)
+ *
+ * Sizes and alignment follow attn_fwd: d must be 128 (else ATTN_ERR_UNSUPPORTED), every
+ * BF16 pointer 16-byte aligned and lse 4-byte aligned (else ATTN_ERR_MISALIGNED), null
+ * pointers or negative sizes give ATTN_ERR_INVALID_ARG; B*H*Nq = 0 with Nk >= 0 is a no-op
+ * (dk and dv are then left unwritten); Nk = 0 with rows is invalid. Outputs must not alias
+ * inputs. All checks happen before the GPU is touched.
+ *
+ * Work: three kernels on `stream` -- a row pass that forms D and the LSE in log2 units
+ * (into a workspace of B*H*ceil(Nq/128)*128*8 bytes that the library allocates with
+ * cudaMallocAsync on the stream the first time it is needed and keeps per (device,
+ * stream)), a pass over key tiles that forms dK and dV, and a pass over query tiles that
+ * forms dQ. Calls on one stream are ordered by the stream; calls on different streams
+ * use different workspaces. Every wait inside the kernels is bounded; a wait that gives
+ * up ends its block and sets a status word read by attn_bwd_status.
+ */
+int attn_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
+             void* dq, void* dk, void* dv, int B, int H, int Nq, int Nk, int d, float scale, void* stream);
+
+/* Synchronises `stream`, then reads and clears the backward kernels' timeout status:
+ * ATTN_OK, ATTN_ERR_TIMEOUT or ATTN_ERR_CUDA. */
+int attn_bwd_status(void* stream);
+
+/* Kernel launches made by attn_bwd in this process (three per call that does work). */
+unsigned long long attn_bwd_kernel_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ATTN_BWD_H */

@@ -11,16 +11,23 @@ import dense_attention_forward_fwd_gb300 as attn
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 HEADER = os.path.join(ROOT, "include", "attn_fwd.h")
+HEADERS = [os.path.join(ROOT, "include", f) for f in sorted(os.listdir(os.path.join(ROOT, "include")))
+           if f.endswith(".h")]
 
 
 def declared_functions():
-    text = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
-    return sorted(set(re.findall(r"^\s*(?:const\s+)?[A-Za-z_][\w\s\*]*?\b(attn_\w+)\s*\(", text, flags=re.M)))
+    names = set()
+    for h in HEADERS:
+        text = re.sub(r"/\*.*?\*/", "", open(h).read(), flags=re.S)
+        names |= set(re.findall(r"^\s*(?:const\s+|unsigned\s+long\s+long\s+)?[A-Za-z_][\w\s\*]*?\b(attn_\w+)\s*\(",
+                                text, flags=re.M))
+    return sorted(names)
 
 
 def test_header_declares_the_entry_points():
     names = declared_functions()
-    assert {"attn_fwd", "attn_fwd_causal", "attn_fwd_bias", "attn_fwd_noalloc", "attn_fwd_status", "attn_status_string",
+    assert {"attn_fwd", "attn_fwd_causal", "attn_fwd_bias", "attn_fwd_noalloc", "attn_bwd", "attn_bwd_status",
+            "attn_bwd_kernel_count", "attn_fwd_status", "attn_status_string",
             "attn_fwd_set_wait_limit", "attn_fwd_kernel_count"} <= set(names)
 
 
@@ -127,6 +134,29 @@ def test_bias_binding_checks_shapes():
                            1, 1, 128, 128, 128, 0.1)
     with pytest.raises(ValueError):  # an integer pointer needs its strides
         attn.attn_fwd_bias(A, A, A, A, A, A, 1, 1, 128, 128, 128, 0.1)
+
+
+def call_bwd(q=A, k=A, v=A, o=A, do=A, lse=A, dq=A, dk=A, dv=A, B=1, H=1, Nq=128, Nk=128, d=128, scale=0.125):
+    return attn.load_library().attn_bwd(q, k, v, o, do, lse, dq, dk, dv, B, H, Nq, Nk, d, scale, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(do=None), attn.ATTN_ERR_INVALID_ARG),
+    (dict(dk=None), attn.ATTN_ERR_INVALID_ARG),
+    (dict(B=-1), attn.ATTN_ERR_INVALID_ARG),
+    (dict(Nk=0), attn.ATTN_ERR_INVALID_ARG),
+    (dict(scale=math.inf), attn.ATTN_ERR_INVALID_ARG),
+    (dict(d=64), attn.ATTN_ERR_UNSUPPORTED),
+    (dict(dq=A + 8), attn.ATTN_ERR_MISALIGNED),
+    (dict(lse=A + 2), attn.ATTN_ERR_MISALIGNED),
+    (dict(B=1 << 16, H=1 << 16), attn.ATTN_ERR_UNSUPPORTED),
+    (dict(B=0), attn.ATTN_OK),
+    (dict(Nq=0, Nk=0), attn.ATTN_OK),
+])
+def test_bwd_argument_checks(kw, code):
+    before = attn.attn_bwd_kernel_count()
+    assert call_bwd(**kw) == code
+    assert attn.attn_bwd_kernel_count() == before
 
 
 def test_binding_raises_on_rejected_call():
