@@ -26,9 +26,12 @@
 //
 // TMEM: dK/dV block: S^T | dP^T | dV | dK (4 x 128 columns); dQ block: S | dP | dQ.
 // Warp roles: warp 0 lane 0 issues TMA, warp 1 lane 0 issues MMAs (and owns TMEM),
-// warps 4-7 compute (warp 4 + q reads TMEM lanes 32q .. 32q + 31). The steps of a block
-// run one after another (S/dP MMAs, then the compute warps, then the accumulating MMAs);
-// ragged tails are zero-filled by TMA and masked. Every mbarrier wait is bounded: on
+// warps 4-11 compute in two groups: group g (warps 4 + 4g ..) takes score columns
+// 64g .. 64g + 63, warp 4 + 4g + q the TMEM lanes 32q .. 32q + 31. Each group writes its
+// packed BF16 half over the first 32 of its own 64 columns, so the groups never touch
+// each other's columns, and hands it to the MMA thread at once, which runs that half of
+// the accumulating products while the other group finishes. Ragged tails are
+// zero-filled by TMA and masked. Every mbarrier wait is bounded: on
 // expiry the block raises an abort flag, sets the status word and winds down.
 
 #include <cuda.h>
@@ -51,7 +54,7 @@ constexpr int kD = 128;
 constexpr int kT = 128;                         // rows of a tile (queries or keys)
 constexpr int kTileBytes = kT * kD * 2;         // 32 KB of BF16
 constexpr int kBoxBytes = kTileBytes / 2;       // one TMA box: 64 columns (128 B) x 128 rows
-constexpr int kThreads = 256;
+constexpr int kThreads = 384;                   // warps 0-3 control, 4-11 compute
 constexpr int kTmemCols = 512;
 constexpr int kStageWarpBytes = 32 * 64 * 2;    // epilogue staging per compute warp
 constexpr unsigned long long kDefaultWaitLimit = 1ull << 31;
@@ -76,16 +79,16 @@ constexpr int kBarFixed = 0;        // the block's fixed tiles (K, V or Q, dO) h
 constexpr int kBarFull = 1;         // [2] stage landed
 constexpr int kBarEmpty = 3;        // [2] stage consumed by the MMAs
 constexpr int kBarSdP = 5;          // S and dP complete in TMEM
-constexpr int kBarPdS = 6;          // compute warps wrote P / dS (one arrival per warp)
-constexpr int kBarAcc = 7;          // accumulators complete
-constexpr int kNumBars = 8;
+constexpr int kBarPdS = 6;          // [2] a column half of P / dS is in TMEM (one arrival per warp)
+constexpr int kBarAcc = 8;          // accumulators complete
+constexpr int kNumBars = 9;
 constexpr int kFlagsBytes = kNumBars * 8 + 16;   // barriers, TMEM slot, abort flag
 
 constexpr int kKVSmem = kKVOffBar + kFlagsBytes + 1024;
 constexpr int kQSmem = kQOffBar + kFlagsBytes + 1024;
 static_assert(kKVStageBytes % 1024 == 0, "stage tiles need 1024-byte alignment");
 static_assert(kKVSmem <= 232448 && kQSmem <= 232448, "exceeds the 227 KB shared memory of one block");
-static_assert(4 * kStageWarpBytes <= kTileBytes, "epilogue staging reuses one tile");
+static_assert(8 * kStageWarpBytes <= kTileBytes, "epilogue staging reuses one tile");
 
 __device__ unsigned int g_bwd_status;   // bit 0: a wait timed out
 
@@ -205,14 +208,17 @@ __device__ __forceinline__ void mma_rows_by_rows(uint32_t d_tmem, uint32_t a_sme
     mma_ss(d_tmem, sdesc_sw128(a_smem + off, 16, 1024), sdesc_sw128(b_smem + off, 16, 1024), idesc, kk > 0);
   }
 }
-// D (+)= A B with A (128 x 128) in TMEM as packed BF16 pairs (8 columns per 16 of K) and
-// B a row-major [128][d] tile in smem (K along rows: MN-major): dV += P^T dO, dK += dS^T Q,
+// D (+)= A B over K = 64h .. 64h + 63 (one half of K = 128) with A in TMEM as packed BF16
+// pairs (8 columns per 16 of K, the half's 32 columns starting at a_half) and B a
+// row-major [128][d] tile in smem (K along rows: MN-major): dV += P^T dO, dK += dS^T Q,
 // dQ += dS K.
-__device__ __forceinline__ void mma_tmem_by_rows(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_smem, bool acc) {
+__device__ __forceinline__ void mma_tmem_by_rows_half(uint32_t d_tmem, uint32_t a_half, uint32_t b_smem, int h,
+                                                      bool acc) {
   constexpr uint32_t idesc = idesc_bf16(true);
 #pragma unroll
-  for (int kk = 0; kk < kT / 16; ++kk)
-    mma_ts(d_tmem, a_tmem + kk * 8, sdesc_sw128(b_smem + kk * 16 * 128, kBoxBytes, 1024), idesc, acc || kk > 0);
+  for (int kk = 0; kk < 4; ++kk)
+    mma_ts(d_tmem, a_half + kk * 8, sdesc_sw128(b_smem + (4 * h + kk) * 16 * 128, kBoxBytes, 1024), idesc,
+           acc || kk > 0);
 }
 
 // ---------------------------------------------------------------------------------
@@ -274,23 +280,20 @@ __device__ __forceinline__ void store_half_rows(uint8_t* stage, const uint32_t (
   __syncwarp();
 }
 
-// Writes this thread's accumulator row (128 FP32 TMEM columns at t_acc) times `mul` as
-// BF16 to row0[lane] .. (the warp's 32 rows).
-__device__ __forceinline__ void store_acc_rows(uint32_t t_acc, float mul, uint8_t* stage, uint16_t* row0,
+// Writes columns 64h .. 64h + 63 of this thread's accumulator row (FP32 TMEM columns at
+// t_acc) times `mul` as BF16 to the warp's 32 rows starting at row0.
+__device__ __forceinline__ void store_acc_half(uint32_t t_acc, int h, float mul, uint8_t* stage, uint16_t* row0,
                                                int valid_rows) {
+  uint32_t pk[32];
 #pragma unroll
-  for (int h = 0; h < 2; ++h) {
-    uint32_t pk[32];
+  for (int c2 = 0; c2 < 2; ++c2) {
+    uint32_t x[32];
+    tmem_ld32(t_acc + h * 64 + c2 * 32, x);
 #pragma unroll
-    for (int c2 = 0; c2 < 2; ++c2) {
-      uint32_t x[32];
-      tmem_ld32(t_acc + h * 64 + c2 * 32, x);
-#pragma unroll
-      for (int i = 0; i < 16; ++i)
-        pk[c2 * 16 + i] = pack_bf16(__uint_as_float(x[2 * i]) * mul, __uint_as_float(x[2 * i + 1]) * mul);
-    }
-    store_half_rows(stage, pk, row0, valid_rows, h);
+    for (int i = 0; i < 16; ++i)
+      pk[c2 * 16 + i] = pack_bf16(__uint_as_float(x[2 * i]) * mul, __uint_as_float(x[2 * i + 1]) * mul);
   }
+  store_half_rows(stage, pk, row0, valid_rows, h);
 }
 
 // Block setup shared by both kernels: barrier init, TMEM allocation. Returns the TMEM base.
@@ -302,7 +305,8 @@ __device__ __forceinline__ uint32_t block_setup(const Ctl& c, uint8_t* flags, ui
       mbar_init(c.bar(kBarEmpty + s), 1);
     }
     mbar_init(c.bar(kBarSdP), 1);
-    mbar_init(c.bar(kBarPdS), 4);   // one arrival per compute warp
+    mbar_init(c.bar(kBarPdS), 4);       // one arrival per warp of compute group 0
+    mbar_init(c.bar(kBarPdS + 1), 4);   // ... of compute group 1
     mbar_init(c.bar(kBarAcc), 1);
     *c.abort = 0u;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -416,10 +420,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         mma_rows_by_rows(tS, base + kKVOffK, stage(s));                   // S^T = K Q_j^T
         mma_rows_by_rows(tdP, base + kKVOffV, stage(s) + kTileBytes);     // dP^T = V dO_j^T
         tc_commit(c.bar(kBarSdP));
-        if (!wait_phase(c, kBarPdS, j & 1, true)) break;
-        tc_fence_after();
-        mma_tmem_by_rows(tdV, tS, stage(s) + kTileBytes, j > 0);        // dV += P^T dO_j
-        mma_tmem_by_rows(tdK, tdP, stage(s), j > 0);                    // dK += dS^T Q_j
+        for (int h = 0; ok && h < 2; ++h) {   // queries 64h .. 64h + 63, as each group hands them over
+          if (!wait_phase(c, kBarPdS + h, j & 1, true)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          mma_tmem_by_rows_half(tdV, tS + 64 * h, stage(s) + kTileBytes, h, j > 0 || h > 0);   // dV += P^T dO_j
+          mma_tmem_by_rows_half(tdK, tdP + 64 * h, stage(s), h, j > 0 || h > 0);               // dK += dS^T Q_j
+        }
+        if (!ok) break;
         tc_commit(c.bar(kBarEmpty + s));
       }
       tc_commit(c.bar(kBarAcc));   // also: every MMA this thread issued is done before TMEM is freed
@@ -428,6 +438,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else if (warp >= 4) {
     const int quarter = warp & 3;
+    const int grp = (warp - 4) >> 2;   // query columns 64 grp .. 64 grp + 63
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
     bool ok = true;
     for (int j = 0; j < nq; ++j) {
@@ -440,14 +451,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const float2* rw = reinterpret_cast<const float2*>(smem + kKVOffStage + s * kKVStageBytes + 2 * kTileBytes);
 #pragma unroll 1
-      for (int ch = 0; ch < 4; ++ch) {   // 32 query columns at a time
+      for (int ch = 0; ch < 2; ++ch) {   // 32 query columns at a time
+        const int col0 = 64 * grp + 32 * ch;
         uint32_t xs[32], xd[32];
-        tmem_ld32(tS + lane_off + ch * 32, xs);
-        tmem_ld32(tdP + lane_off + ch * 32, xd);
+        tmem_ld32(tS + lane_off + col0, xs);
+        tmem_ld32(tdP + lane_off + col0, xd);
         uint32_t pw[16], dw[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-          const float2 r0 = rw[ch * 32 + 2 * i], r1 = rw[ch * 32 + 2 * i + 1];
+          const float2 r0 = rw[col0 + 2 * i], r1 = rw[col0 + 2 * i + 1];
           const float p0 = ex2(fmaf(__uint_as_float(xs[2 * i]), p.scale_log2, -r0.x));
           const float p1 = ex2(fmaf(__uint_as_float(xs[2 * i + 1]), p.scale_log2, -r1.x));
           const float d0 = p0 * (__uint_as_float(xd[2 * i]) - r0.y);
@@ -455,23 +467,23 @@ __global__ void __launch_bounds__(kThreads, 1)
           pw[i] = pack_bf16(p0, p1);
           dw[i] = pack_bf16(d0, d1);
         }
-        // columns 16 ch .. 16 ch + 15 were read in this or an earlier chunk
-        tmem_st16(tS + lane_off + ch * 16, pw);
-        tmem_st16(tdP + lane_off + ch * 16, dw);
+        // group columns 64 grp + 16 ch .. + 15 were read in this or the previous chunk
+        tmem_st16(tS + lane_off + 64 * grp + 16 * ch, pw);
+        tmem_st16(tdP + lane_off + 64 * grp + 16 * ch, dw);
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(c.bar(kBarPdS));
+      if (lane == 0) mbar_arrive(c.bar(kBarPdS + grp));
       __syncwarp();
     }
     if (ok && wait_warp(c, kBarAcc, 0)) {
       tc_fence_after();
       const int row0 = kt * kT + quarter * 32;   // the warp's first key
       const int valid = p.Nk - row0;
-      uint8_t* st = smem + kKVOffK + quarter * kStageWarpBytes;   // K is no longer read
+      uint8_t* st = smem + kKVOffK + (warp - 4) * kStageWarpBytes;   // K is no longer read
       const size_t off = (static_cast<size_t>(bh) * p.Nk + row0) * kD;
-      store_acc_rows(tdV + lane_off, 1.0f, st, p.dv + off, valid);
-      store_acc_rows(tdK + lane_off, p.scale, st, p.dk + off, valid);
+      store_acc_half(tdV + lane_off, grp, 1.0f, st, p.dv + off, valid);      // d columns 64 grp ..
+      store_acc_half(tdK + lane_off, grp, p.scale, st, p.dk + off, valid);
     }
   }
   block_teardown(tmem, warp);
@@ -533,9 +545,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         mma_rows_by_rows(tS, base + kQOffQ, stage(s));                    // S = Q K_j^T
         mma_rows_by_rows(tdP, base + kQOffDO, stage(s) + kTileBytes);     // dP = dO V_j^T
         tc_commit(c.bar(kBarSdP));
-        if (!wait_phase(c, kBarPdS, j & 1, true)) break;
-        tc_fence_after();
-        mma_tmem_by_rows(tdQ, tS, stage(s), j > 0);                       // dQ += dS K_j
+        for (int h = 0; ok && h < 2; ++h) {   // keys 64h .. 64h + 63
+          if (!wait_phase(c, kBarPdS + h, j & 1, true)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          mma_tmem_by_rows_half(tdQ, tS + 64 * h, stage(s), h, j > 0 || h > 0);   // dQ += dS K_j
+        }
+        if (!ok) break;
         tc_commit(c.bar(kBarEmpty + s));
       }
       tc_commit(c.bar(kBarAcc));
@@ -544,6 +562,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else if (warp >= 4) {
     const int quarter = warp & 3;
+    const int grp = (warp - 4) >> 2;   // key columns 64 grp .. 64 grp + 63
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
     const int qrow = qt * kT + quarter * 32 + lane;
     float2 rw = make_float2(0.0f, 0.0f);   // rows past Nq: any finite values (never stored)
@@ -557,30 +576,31 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const int valid = p.Nk - j * kT;   // keys of this tile inside the sequence
 #pragma unroll 1
-      for (int ch = 0; ch < 4; ++ch) {
+      for (int ch = 0; ch < 2; ++ch) {
+        const int col0 = 64 * grp + 32 * ch;
         uint32_t xs[32], xd[32];
-        tmem_ld32(tS + lane_off + ch * 32, xs);
-        tmem_ld32(tdP + lane_off + ch * 32, xd);
+        tmem_ld32(tS + lane_off + col0, xs);
+        tmem_ld32(tdP + lane_off + col0, xd);
         uint32_t dw[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-          const int key = ch * 32 + 2 * i;
+          const int key = col0 + 2 * i;
           const float p0 = key < valid ? ex2(fmaf(__uint_as_float(xs[2 * i]), p.scale_log2, -rw.x)) : 0.0f;
           const float p1 = key + 1 < valid ? ex2(fmaf(__uint_as_float(xs[2 * i + 1]), p.scale_log2, -rw.x)) : 0.0f;
           dw[i] = pack_bf16(p0 * (__uint_as_float(xd[2 * i]) - rw.y), p1 * (__uint_as_float(xd[2 * i + 1]) - rw.y));
         }
-        tmem_st16(tS + lane_off + ch * 16, dw);
+        tmem_st16(tS + lane_off + 64 * grp + 16 * ch, dw);
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(c.bar(kBarPdS));
+      if (lane == 0) mbar_arrive(c.bar(kBarPdS + grp));
       __syncwarp();
     }
     if (ok && wait_warp(c, kBarAcc, 0)) {
       tc_fence_after();
       const int row0 = qt * kT + quarter * 32;
-      uint8_t* st = smem + kQOffQ + quarter * kStageWarpBytes;   // Q is no longer read
-      store_acc_rows(tdQ + lane_off, p.scale, st, p.dq + (static_cast<size_t>(bh) * p.Nq + row0) * kD,
+      uint8_t* st = smem + kQOffQ + (warp - 4) * kStageWarpBytes;   // Q is no longer read
+      store_acc_half(tdQ + lane_off, grp, p.scale, st, p.dq + (static_cast<size_t>(bh) * p.Nq + row0) * kD,
                      p.Nq - row0);
     }
   }
