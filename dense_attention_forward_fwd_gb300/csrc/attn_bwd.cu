@@ -22,9 +22,10 @@
 //   bwd_dq_kernel    one block per (b, h, 128-query tile). Q and dO are loaded once; per
 //                    key tile j (double-buffered K_j, V_j): S = Q K_j^T, dP = dO V_j^T; the
 //                    compute warps (thread = query) form dS and write it over S; then
-//                    dQ += dS K_j.
+//                    dQ += dS K_j. S is double-buffered in TMEM, so the next tile's S and
+//                    dP run on the tensor cores while the compute warps work on this one.
 //
-// TMEM: dK/dV block: S^T | dP^T | dV | dK (4 x 128 columns); dQ block: S | dP | dQ.
+// TMEM: dK/dV block: S^T | dP^T | dV | dK (4 x 128 columns); dQ block: S0 | dP | dQ | S1.
 // Warp roles: warp 0 lane 0 issues TMA, warp 1 lane 0 issues MMAs (and owns TMEM),
 // warps 4-11 compute in two groups: group g (warps 4 + 4g ..) takes score columns
 // 64g .. 64g + 63, warp 4 + 4g + q the TMEM lanes 32q .. 32q + 31. Each group writes its
@@ -79,9 +80,11 @@ constexpr int kBarFixed = 0;        // the block's fixed tiles (K, V or Q, dO) h
 constexpr int kBarFull = 1;         // [2] stage landed
 constexpr int kBarEmpty = 3;        // [2] stage consumed by the MMAs
 constexpr int kBarSdP = 5;          // S and dP complete in TMEM
-constexpr int kBarPdS = 6;          // [2] a column half of P / dS is in TMEM (one arrival per warp)
-constexpr int kBarAcc = 8;          // accumulators complete
-constexpr int kNumBars = 9;
+constexpr int kBarPdS = 6;          // [step parity][2]: a column half of P / dS is in TMEM (one
+                                    // arrival per warp); the dK/dV block uses set 0 only
+constexpr int kBarAcc = 10;         // accumulators complete
+constexpr int kBarDPFree = 11;      // dQ block: every compute warp holds dP of the step in registers
+constexpr int kNumBars = 12;
 constexpr int kFlagsBytes = kNumBars * 8 + 16;   // barriers, TMEM slot, abort flag
 
 constexpr int kKVSmem = kKVOffBar + kFlagsBytes + 1024;
@@ -305,9 +308,9 @@ __device__ __forceinline__ uint32_t block_setup(const Ctl& c, uint8_t* flags, ui
       mbar_init(c.bar(kBarEmpty + s), 1);
     }
     mbar_init(c.bar(kBarSdP), 1);
-    mbar_init(c.bar(kBarPdS), 4);       // one arrival per warp of compute group 0
-    mbar_init(c.bar(kBarPdS + 1), 4);   // ... of compute group 1
+    for (int b = 0; b < 4; ++b) mbar_init(c.bar(kBarPdS + b), 4);   // one arrival per warp of a group
     mbar_init(c.bar(kBarAcc), 1);
+    mbar_init(c.bar(kBarDPFree), 8);    // one arrival per compute warp
     *c.abort = 0u;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -508,7 +511,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   c.abort = reinterpret_cast<volatile uint32_t*>(smem + kQOffBar + kNumBars * 8 + 4);
   c.limit = p.wait_limit;
   const uint32_t tmem = block_setup(c, smem + kQOffBar, base + kQOffBar, warp);
-  const uint32_t tS = tmem, tdP = tmem + 128, tdQ = tmem + 256;
+  // S is double-buffered (the fourth 128 columns), so S and dP of the next key tile are
+  // computed while the compute warps work on this one; dP has one buffer, which the
+  // compute warps release as soon as they hold their columns of it in registers.
+  const uint32_t tS0 = tmem, tdP = tmem + 128, tdQ = tmem + 256, tS1 = tmem + 384;
   const int nk = p.k_tiles;
   auto stage = [&](int s) { return base + kQOffStage + s * kQStageBytes; };   // K | V
 
@@ -537,21 +543,38 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else if (warp == 1) {
     if (lane == 0) {
-      bool ok = wait_phase(c, kBarFixed, 0, true);
+      bool ok = wait_phase(c, kBarFixed, 0, true) && wait_phase(c, kBarFull, 0, true);
+      if (ok) {
+        tc_fence_after();
+        mma_rows_by_rows(tS0, base + kQOffQ, stage(0));                   // S(0) = Q K_0^T
+        mma_rows_by_rows(tdP, base + kQOffDO, stage(0) + kTileBytes);     // dP(0) = dO V_0^T
+        tc_commit(c.bar(kBarSdP));
+      }
       for (int j = 0; ok && j < nk; ++j) {
         const int s = j & 1;
-        if (!wait_phase(c, kBarFull + s, (j >> 1) & 1, true)) break;
-        tc_fence_after();
-        mma_rows_by_rows(tS, base + kQOffQ, stage(s));                    // S = Q K_j^T
-        mma_rows_by_rows(tdP, base + kQOffDO, stage(s) + kTileBytes);     // dP = dO V_j^T
-        tc_commit(c.bar(kBarSdP));
+        const uint32_t tSj = s ? tS1 : tS0;
+        if (j + 1 < nk) {
+          // S(j+1) into the other buffer (its dS(j-1) was read by the dQ MMAs issued before);
+          // dP(j+1) once every compute warp has taken dP(j) into registers
+          const int s1 = s ^ 1;
+          if (!wait_phase(c, kBarFull + s1, ((j + 1) >> 1) & 1, true)) break;
+          tc_fence_after();
+          mma_rows_by_rows(s1 ? tS1 : tS0, base + kQOffQ, stage(s1));
+          if (!wait_phase(c, kBarDPFree, j & 1, true)) break;
+          tc_fence_after();
+          mma_rows_by_rows(tdP, base + kQOffDO, stage(s1) + kTileBytes);
+          tc_commit(c.bar(kBarSdP));
+        }
+        // The compute warps may finish step j + 1 before this thread gets here, so steps
+        // alternate between two sets of hand-off barriers: a set completes at most once
+        // more before it is waited on, which keeps its phase parity unambiguous.
         for (int h = 0; ok && h < 2; ++h) {   // keys 64h .. 64h + 63
-          if (!wait_phase(c, kBarPdS + h, j & 1, true)) {
+          if (!wait_phase(c, kBarPdS + 2 * s + h, (j >> 1) & 1, true)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          mma_tmem_by_rows_half(tdQ, tS + 64 * h, stage(s), h, j > 0 || h > 0);   // dQ += dS K_j
+          mma_tmem_by_rows_half(tdQ, tSj + 64 * h, stage(s), h, j > 0 || h > 0);   // dQ += dS K_j
         }
         if (!ok) break;
         tc_commit(c.bar(kBarEmpty + s));
@@ -574,26 +597,34 @@ __global__ void __launch_bounds__(kThreads, 1)
         break;
       }
       tc_fence_after();
+      const uint32_t tSj = (j & 1) ? tS1 : tS0;
       const int valid = p.Nk - j * kT;   // keys of this tile inside the sequence
-#pragma unroll 1
+      uint32_t xd[2][32];
+      tmem_ld32(tdP + lane_off + 64 * grp, xd[0]);
+      tmem_ld32(tdP + lane_off + 64 * grp + 32, xd[1]);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(c.bar(kBarDPFree));   // dP may be overwritten now
+      __syncwarp();
+#pragma unroll
       for (int ch = 0; ch < 2; ++ch) {
         const int col0 = 64 * grp + 32 * ch;
-        uint32_t xs[32], xd[32];
-        tmem_ld32(tS + lane_off + col0, xs);
-        tmem_ld32(tdP + lane_off + col0, xd);
+        uint32_t xs[32];
+        tmem_ld32(tSj + lane_off + col0, xs);
         uint32_t dw[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
           const int key = col0 + 2 * i;
           const float p0 = key < valid ? ex2(fmaf(__uint_as_float(xs[2 * i]), p.scale_log2, -rw.x)) : 0.0f;
           const float p1 = key + 1 < valid ? ex2(fmaf(__uint_as_float(xs[2 * i + 1]), p.scale_log2, -rw.x)) : 0.0f;
-          dw[i] = pack_bf16(p0 * (__uint_as_float(xd[2 * i]) - rw.y), p1 * (__uint_as_float(xd[2 * i + 1]) - rw.y));
+          dw[i] = pack_bf16(p0 * (__uint_as_float(xd[ch][2 * i]) - rw.y),
+                            p1 * (__uint_as_float(xd[ch][2 * i + 1]) - rw.y));
         }
-        tmem_st16(tS + lane_off + 64 * grp + 16 * ch, dw);
+        tmem_st16(tSj + lane_off + 64 * grp + 16 * ch, dw);
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(c.bar(kBarPdS + grp));
+      if (lane == 0) mbar_arrive(c.bar(kBarPdS + 2 * (j & 1) + grp));
       __syncwarp();
     }
     if (ok && wait_warp(c, kBarAcc, 0)) {
