@@ -78,6 +78,20 @@ def dist_env():
     return int(os.environ.get("RANK", 0)), int(os.environ.get("LOCAL_RANK", 0)), int(os.environ.get("WORLD_SIZE", 1))
 
 
+def max_over_ranks(values, pg, device):
+    """Each value's maximum over all ranks (a job takes as long as its slowest rank)."""
+    import torch
+    t = torch.tensor([float(x) for x in values], dtype=torch.float64, device=device)
+    pg.all_reduce(t, op=pg.ReduceOp.MAX)
+    return [float(x) for x in t.cpu()]
+
+
+def job_tflops(flops_per_rank: float, world: int, ms: float) -> float:
+    """Whole-job throughput: every rank runs its own copy of the workload (weak scaling, no
+    collective on the data path), so the job does world x the work in the slowest rank's time."""
+    return flops_per_rank * world / (ms * 1e-3) / 1e12
+
+
 def kernel_hash(backward: bool = False) -> str:
     h = hashlib.sha256()
     files = ((KERNEL_SRC.replace("attn_fwd.cu", "attn_bwd.cu"), os.path.join(ROOT, "include", "attn_bwd.h"))
@@ -467,12 +481,9 @@ def run_ours(args, w):
 
     # max over ranks
     if pg is not None:
-        tt = torch.tensor([ms, e2e_ms], device=dev, dtype=torch.float64)
-        pg.all_reduce(tt, op=pg.ReduceOp.MAX)
-        ms, e2e_ms = float(tt[0]), float(tt[1])
-    total_flops = flops * world
-    value = total_flops / (ms * 1e-3) / 1e12
-    e2e_value = total_flops / (e2e_ms * 1e-3) / 1e12
+        ms, e2e_ms = max_over_ranks([ms, e2e_ms], pg, dev)
+    value = job_tflops(flops, world, ms)
+    e2e_value = job_tflops(flops, world, e2e_ms)
 
     peaks, peak_src = measured_peaks()
     peak = float(peaks["bf16_tflops"])
