@@ -59,6 +59,10 @@ class Oracle:
         lib.attn_ref_dense_f64.restype = ctypes.c_int
         lib.attn_ref_bwd_f64.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, i64, dbl, vp, vp, vp, ctypes.c_int]
         lib.attn_ref_bwd_f64.restype = ctypes.c_int
+        lib.attn_ref_dense_causal_f64.argtypes = lib.attn_ref_dense_f64.argtypes
+        lib.attn_ref_dense_causal_f64.restype = ctypes.c_int
+        lib.attn_ref_bwd_causal_f64.argtypes = lib.attn_ref_bwd_f64.argtypes
+        lib.attn_ref_bwd_causal_f64.restype = ctypes.c_int
         lib.attn_ref_probs_f64.argtypes = [vp, vp, i64, i64, i64, i64, dbl, vp]
         lib.attn_ref_probs_f64.restype = ctypes.c_int
         lib.attn_ref_max_threads.argtypes = []
@@ -146,8 +150,9 @@ class Oracle:
         o, lse = self.attention_rows(q, k, v, scale, None, nthreads)
         return o.reshape(B, H, Nq, dv), lse.reshape(B, H, Nq)
 
-    def attention_dense(self, q, k, v, scale: float):
-        """Forward on float64 (or BF16-bit uint16, widened exactly) inputs: (o [B,H,Nq,dv], lse [B,H,Nq])."""
+    def attention_dense(self, q, k, v, scale: float, causal: bool = False):
+        """Forward on float64 (or BF16-bit uint16, widened exactly) inputs: (o [B,H,Nq,dv], lse [B,H,Nq]).
+        causal: the causal mask of attention_rows_causal (needs Nq <= Nk)."""
         q, k, v = _f64(q), _f64(k), _f64(v)
         B, H, Nq, d = q.shape
         Nk, dv = k.shape[2], v.shape[3]
@@ -155,16 +160,17 @@ class Oracle:
             raise ValueError(f"shape mismatch q{q.shape} k{k.shape} v{v.shape}")
         o = np.empty((B, H, Nq, dv), dtype=np.float64)
         lse = np.empty((B, H, Nq), dtype=np.float64)
-        rc = self.lib.attn_ref_dense_f64(_ptr(q), _ptr(k), _ptr(v), B * H, Nq, Nk, d, dv, float(scale), _ptr(o),
-                                         _ptr(lse))
+        fn = self.lib.attn_ref_dense_causal_f64 if causal else self.lib.attn_ref_dense_f64
+        rc = fn(_ptr(q), _ptr(k), _ptr(v), B * H, Nq, Nk, d, dv, float(scale), _ptr(o), _ptr(lse))
         if rc != 0:
             raise ValueError(f"attn_ref_dense_f64 failed with status {rc}")
         return o, lse
 
-    def attention_bwd(self, q, k, v, dout, scale: float, nthreads: int = 0):
+    def attention_bwd(self, q, k, v, dout, scale: float, nthreads: int = 0, causal: bool = False):
         """Gradients (dq, dk, dv) in float64 of the forward for upstream gradient dout [B,H,Nq,dv].
 
-        Inputs are float64 arrays, or BF16 bits (uint16) widened exactly."""
+        Inputs are float64 arrays, or BF16 bits (uint16) widened exactly. causal: of the
+        causal forward (needs Nq <= Nk)."""
         q, k, v, dout = _f64(q), _f64(k), _f64(v), _f64(dout)
         B, H, Nq, d = q.shape
         Nk, dv = k.shape[2], v.shape[3]
@@ -173,8 +179,9 @@ class Oracle:
         dq = np.empty((B, H, Nq, d), dtype=np.float64)
         dk = np.empty((B, H, Nk, d), dtype=np.float64)
         dvv = np.empty((B, H, Nk, dv), dtype=np.float64)
-        rc = self.lib.attn_ref_bwd_f64(_ptr(q), _ptr(k), _ptr(v), _ptr(dout), B * H, Nq, Nk, d, dv, float(scale),
-                                       _ptr(dq), _ptr(dk), _ptr(dvv), int(nthreads))
+        fn = self.lib.attn_ref_bwd_causal_f64 if causal else self.lib.attn_ref_bwd_f64
+        rc = fn(_ptr(q), _ptr(k), _ptr(v), _ptr(dout), B * H, Nq, Nk, d, dv, float(scale), _ptr(dq), _ptr(dk),
+                _ptr(dvv), int(nthreads))
         if rc != 0:
             raise ValueError(f"attn_ref_bwd_f64 failed with status {rc}")
         return dq, dk, dvv
@@ -248,9 +255,9 @@ def probs(q, k, scale: float):
     return default().probs(q, k, scale)
 
 
-def attention_dense(q, k, v, scale: float):
-    return default().attention_dense(q, k, v, scale)
+def attention_dense(q, k, v, scale: float, causal: bool = False):
+    return default().attention_dense(q, k, v, scale, causal)
 
 
-def attention_bwd(q, k, v, dout, scale: float, nthreads: int = 0):
-    return default().attention_bwd(q, k, v, dout, scale, nthreads)
+def attention_bwd(q, k, v, dout, scale: float, nthreads: int = 0, causal: bool = False):
+    return default().attention_bwd(q, k, v, dout, scale, nthreads, causal)

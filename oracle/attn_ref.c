@@ -333,12 +333,17 @@ int attn_ref_max_threads(void)
  * them; BF16 inputs are widened exactly by the caller.
  */
 
-/* The forward on double inputs: o [BH, Nq, dv], lse [BH, Nq] (same steps as above). */
-int attn_ref_dense_f64(const double *q, const double *k, const double *v,
-                       int64_t BH, int64_t Nq, int64_t Nk, int64_t d, int64_t dv,
-                       double scale, double *o, double *lse)
+/*
+ * The forward on double inputs: o [BH, Nq, dv], lse [BH, Nq] (same steps as above).
+ * causal != 0: row i uses keys 0 .. i + (Nk - Nq) only (the causal mask of
+ * attn_ref_rows_causal_f64; needs Nq <= Nk).
+ */
+static int dense_impl(const double *q, const double *k, const double *v,
+                      int64_t BH, int64_t Nq, int64_t Nk, int64_t d, int64_t dv,
+                      double scale, double *o, double *lse, int causal)
 {
     if (BH < 0 || Nq < 0 || Nk < 1 || d < 1 || dv < 1) return REF_EINVAL;
+    if (causal && Nq > Nk) return REF_EINVAL;
     if (BH * Nq == 0) return REF_OK;
     if (!q || !k || !v || !o || !lse) return REF_EINVAL;
     double *s = (double *)malloc((size_t)Nk * sizeof(double));
@@ -347,17 +352,18 @@ int attn_ref_dense_f64(const double *q, const double *k, const double *v,
         const double *kh = k + bh * Nk * d, *vh = v + bh * Nk * dv;
         for (int64_t i = 0; i < Nq; i++) {
             const double *qi = q + (bh * Nq + i) * d;
-            for (int64_t j = 0; j < Nk; j++) {
+            const int64_t nv = causal ? i + (Nk - Nq) + 1 : Nk;   /* keys of row i */
+            for (int64_t j = 0; j < nv; j++) {
                 double acc = 0.0;
                 for (int64_t c = 0; c < d; c++) acc += qi[c] * kh[j * d + c];
                 s[j] = scale * acc;
             }
-            double m = row_max(s, Nk);
-            double l = row_exp_sum(s, Nk, m);
+            double m = row_max(s, nv);
+            double l = row_exp_sum(s, nv, m);
             double *oi = o + (bh * Nq + i) * dv;
             for (int64_t c = 0; c < dv; c++) {
                 double acc = 0.0;
-                for (int64_t j = 0; j < Nk; j++) acc += s[j] * vh[j * dv + c];
+                for (int64_t j = 0; j < nv; j++) acc += s[j] * vh[j * dv + c];
                 oi[c] = acc / l;
             }
             lse[bh * Nq + i] = m + log(l);
@@ -367,16 +373,32 @@ int attn_ref_dense_f64(const double *q, const double *k, const double *v,
     return REF_OK;
 }
 
+int attn_ref_dense_f64(const double *q, const double *k, const double *v,
+                       int64_t BH, int64_t Nq, int64_t Nk, int64_t d, int64_t dv,
+                       double scale, double *o, double *lse)
+{
+    return dense_impl(q, k, v, BH, Nq, Nk, d, dv, scale, o, lse, 0);
+}
+
+int attn_ref_dense_causal_f64(const double *q, const double *k, const double *v,
+                              int64_t BH, int64_t Nq, int64_t Nk, int64_t d, int64_t dv,
+                              double scale, double *o, double *lse)
+{
+    return dense_impl(q, k, v, BH, Nq, Nk, d, dv, scale, o, lse, 1);
+}
+
 /*
  * attn_ref_bwd_f64: dq [BH, Nq, d], dk [BH, Nk, d], dv [BH, Nk, dv] for upstream
  * gradient dout [BH, Nq, dv]. OpenMP over heads (each head's dk and dv are summed over
- * its query rows in order).
+ * its query rows in order). causal != 0 (attn_ref_bwd_causal_f64): the gradient of the
+ * causal forward, every sum of row i running over its keys 0 .. i + (Nk - Nq) only.
  */
-int attn_ref_bwd_f64(const double *q, const double *k, const double *v, const double *dout,
-                     int64_t BH, int64_t Nq, int64_t Nk, int64_t d, int64_t dv,
-                     double scale, double *dq, double *dk, double *dvv, int nthreads)
+static int bwd_impl(const double *q, const double *k, const double *v, const double *dout,
+                    int64_t BH, int64_t Nq, int64_t Nk, int64_t d, int64_t dv,
+                    double scale, double *dq, double *dk, double *dvv, int nthreads, int causal)
 {
     if (BH < 0 || Nq < 0 || Nk < 1 || d < 1 || dv < 1) return REF_EINVAL;
+    if (causal && Nq > Nk) return REF_EINVAL;
     if (BH == 0) return REF_OK;
     if (!q || !k || !v || !dout || !dq || !dk || !dvv) return REF_EINVAL;
     int failed = 0;
@@ -407,18 +429,19 @@ int attn_ref_bwd_f64(const double *q, const double *k, const double *v, const do
                     const double *qi = q + (bh * Nq + i) * d;
                     const double *doi = dout + (bh * Nq + i) * dv;
                     double *dqi = dq + (bh * Nq + i) * d;
+                    const int64_t nvis = causal ? i + (Nk - Nq) + 1 : Nk;   /* keys of row i */
                     /* the forward's probabilities of row i */
-                    for (int64_t j = 0; j < Nk; j++) {
+                    for (int64_t j = 0; j < nvis; j++) {
                         double acc = 0.0;
                         for (int64_t c = 0; c < d; c++) acc += qi[c] * kh[j * d + c];
                         p[j] = scale * acc;
                     }
-                    double m = row_max(p, Nk);
-                    double l = row_exp_sum(p, Nk, m);
-                    for (int64_t j = 0; j < Nk; j++) p[j] /= l;
+                    double m = row_max(p, nvis);
+                    double l = row_exp_sum(p, nvis, m);
+                    for (int64_t j = 0; j < nvis; j++) p[j] /= l;
                     /* dv, dp and D */
                     double D = 0.0;
-                    for (int64_t j = 0; j < Nk; j++) {
+                    for (int64_t j = 0; j < nvis; j++) {
                         double acc = 0.0;
                         for (int64_t c = 0; c < dv; c++) {
                             dvh[j * dv + c] += p[j] * doi[c];
@@ -429,7 +452,7 @@ int attn_ref_bwd_f64(const double *q, const double *k, const double *v, const do
                     }
                     /* ds, dq, dk */
                     for (int64_t c = 0; c < d; c++) dqi[c] = 0.0;
-                    for (int64_t j = 0; j < Nk; j++) {
+                    for (int64_t j = 0; j < nvis; j++) {
                         double ds = p[j] * (dp[j] - D);
                         for (int64_t c = 0; c < d; c++) {
                             dqi[c] += scale * ds * kh[j * d + c];
@@ -443,4 +466,18 @@ int attn_ref_bwd_f64(const double *q, const double *k, const double *v, const do
         free(dp);
     }
     return failed ? REF_ENOMEM : REF_OK;
+}
+
+int attn_ref_bwd_f64(const double *q, const double *k, const double *v, const double *dout,
+                     int64_t BH, int64_t Nq, int64_t Nk, int64_t d, int64_t dv,
+                     double scale, double *dq, double *dk, double *dvv, int nthreads)
+{
+    return bwd_impl(q, k, v, dout, BH, Nq, Nk, d, dv, scale, dq, dk, dvv, nthreads, 0);
+}
+
+int attn_ref_bwd_causal_f64(const double *q, const double *k, const double *v, const double *dout,
+                            int64_t BH, int64_t Nq, int64_t Nk, int64_t d, int64_t dv,
+                            double scale, double *dq, double *dk, double *dvv, int nthreads)
+{
+    return bwd_impl(q, k, v, dout, BH, Nq, Nk, d, dv, scale, dq, dk, dvv, nthreads, 1);
 }

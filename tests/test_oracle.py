@@ -445,6 +445,57 @@ def pin_bwd_equal_value_rows_give_no_query_or_key_gradient(orc):
     assert np.max(np.abs(dv)) > 1e-2
 
 
+def pin_causal_dense_forward_equals_the_bf16_causal_oracle(orc):
+    q, k, v = make_qkv(2, 2, 5, 8, d=8, seed=60)
+    o1, l1 = orc.attention_rows_causal(q, k, v, 0.6)
+    o2, l2 = orc.attention_dense(q, k, v, 0.6, causal=True)
+    assert np.max(np.abs(o1 - o2.reshape(-1, 8))) < 1e-15 and np.max(np.abs(l1 - l2.reshape(-1))) < 1e-14
+
+
+def pin_causal_bwd_matches_central_differences(orc):
+    # the gradient of the causal forward, Nq < Nk (bottom-right alignment matters), dv > d
+    rng = np.random.default_rng(61)
+    B, H, Nq, Nk, d, dv = 1, 2, 3, 5, 3, 4
+    q, k = rng.normal(size=(B, H, Nq, d)), rng.normal(size=(B, H, Nk, d))
+    v, dout = rng.normal(size=(B, H, Nk, dv)), rng.normal(size=(B, H, Nq, dv))
+    scale = 0.9
+    grads = dict(zip("qkv", orc.attention_bwd(q, k, v, dout, scale, causal=True)))
+    h = 1e-6
+    for name in "qkv":
+        base = {"q": q, "k": k, "v": v}
+        x, g = base[name], grads[name]
+        fd = np.zeros_like(x)
+        for idx in np.ndindex(x.shape):
+            hi, lo = dict(base), dict(base)
+            hi[name] = x.copy()
+            hi[name][idx] += h
+            lo[name] = x.copy()
+            lo[name][idx] -= h
+            l_hi = np.sum(orc.attention_dense(hi["q"], hi["k"], hi["v"], scale, causal=True)[0] * dout)
+            l_lo = np.sum(orc.attention_dense(lo["q"], lo["k"], lo["v"], scale, causal=True)[0] * dout)
+            fd[idx] = (l_hi - l_lo) / (2 * h)
+        assert np.max(np.abs(fd - g)) < 1e-7 * max(1.0, np.max(np.abs(g))), name
+
+
+def pin_causal_bwd_single_query_equals_the_full_gradient(orc):
+    # one query row at the end of the sequence sees every key
+    q, k, v = make_qkv(1, 2, 1, 6, d=8, seed=62)
+    dout = np.random.default_rng(63).normal(size=(1, 2, 1, 8))
+    for gc, gf in zip(orc.attention_bwd(q, k, v, dout, 0.7, causal=True), orc.attention_bwd(q, k, v, dout, 0.7)):
+        assert np.array_equal(gc, gf)
+
+
+def pin_causal_bwd_keys_see_only_later_rows(orc):
+    # Nq = Nk = 6 with dO zero on rows 3..5: keys 3..5 are seen only by those rows, so their
+    # dK and dV are exactly zero, while keys 0..2 have gradients
+    q, k, v = make_qkv(1, 1, 6, 6, d=8, seed=64)
+    dout = np.random.default_rng(65).normal(size=(1, 1, 6, 8))
+    dout[:, :, 3:] = 0.0
+    _, dk, dv = orc.attention_bwd(q, k, v, dout, 0.8, causal=True)
+    assert np.all(dk[0, 0, 3:] == 0.0) and np.all(dv[0, 0, 3:] == 0.0)
+    assert np.min(np.abs(dv[0, 0, :3]).max(axis=-1)) > 1e-3
+
+
 PINS = [v for k_, v in sorted(globals().items()) if k_.startswith("pin_")]
 
 

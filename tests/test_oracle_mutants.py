@@ -36,8 +36,11 @@ MUTANTS = {
     "bwd dq without the scale": ("dqi[c] += scale * ds * kh[j * d + c];", "dqi[c] += ds * kh[j * d + c];"),
     "bwd dk from keys": ("dkh[j * d + c] += scale * ds * qi[c];", "dkh[j * d + c] += scale * ds * kh[j * d + c];"),
     "bwd dv from dp": ("dvh[j * dv + c] += p[j] * doi[c];", "dvh[j * dv + c] += dp[j] * doi[c];"),
-    "bwd probabilities not normalised": ("for (int64_t j = 0; j < Nk; j++) p[j] /= l;", ""),
+    "bwd probabilities not normalised": ("for (int64_t j = 0; j < nvis; j++) p[j] /= l;", ""),
     "dense forward without 1/l": ("oi[c] = acc / l;", "oi[c] = acc;"),
+    "causal bwd mask half offset": ("nvis = causal ? i + (Nk - Nq) + 1", "nvis = causal ? i + (Nk - Nq) / 2 + 1"),
+    "causal dense forward one key short": ("const int64_t nv = causal ? i + (Nk - Nq) + 1 : Nk;",
+                                           "const int64_t nv = causal ? i + (Nk - Nq) + (i > 0) : Nk;"),
 }
 
 
