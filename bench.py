@@ -191,7 +191,7 @@ def oracle_rows_fn(oracle, w, causal: bool, bias_kind: str, H1: int, nq: int):
     return oracle.attention_rows_causal if causal else oracle.attention_rows
 
 
-def cpu_oracle_backward_sample(w, target_seconds: float):
+def cpu_oracle_backward_sample(w, target_seconds: float, causal: bool = False):
     """Time the FP64 backward oracle on one head with nq of the workload's query rows (all Nk
     keys, as dK and dV need every row); returns (TFLOPS at 2.5x forward FLOPs, rows, seconds,
     threads)."""
@@ -204,14 +204,15 @@ def cpu_oracle_backward_sample(w, target_seconds: float):
         q, k, v = make_qkv(1, 1, nq, w.Nk, d=w.d, seed=w.seed, qk_mult=w.qk_mult)
         do = np.random.Generator(np.random.PCG64(w.seed + 7)).standard_normal((1, 1, nq, w.d))
         t = time.perf_counter()
-        oracle.attention_bwd(q, k, v, do, w.scale)
+        oracle.attention_bwd(q, k, v, do, w.scale, causal=causal)
         return time.perf_counter() - t
 
     nq = min(w.Nq, 32)
     dt = run(nq)
     nq = int(min(w.Nq, max(nq, nq * target_seconds / max(dt, 1e-6))))
     dt = run(nq)
-    return 2.5 * 4.0 * nq * w.Nk * w.d / dt / 1e12, nq, dt, oracle.max_threads()
+    pairs = nq * (w.Nk - nq) + nq * (nq + 1) / 2 if causal else nq * w.Nk   # the sample's last nq rows
+    return 2.5 * 4.0 * pairs * w.d / dt / 1e12, nq, dt, oracle.max_threads()
 
 
 def cpu_oracle_sample(w, target_seconds: float, rank_seed: int = 0, causal: bool = False, bias_kind: str = "none"):
@@ -264,7 +265,7 @@ def run_reference(args, w):
     if args.backward:   # each step: the backward oracle on one head, sized to share ~2 minutes
         total, flops_sum = 0.0, 0.0
         for i in range(warm + steps):
-            tfl, n, dt, threads = cpu_oracle_backward_sample(w, 120.0 / (steps + warm))
+            tfl, n, dt, threads = cpu_oracle_backward_sample(w, 120.0 / (steps + warm), args.causal)
             if i >= warm:
                 total += dt
                 flops_sum += tfl * 1e12 * dt
@@ -275,8 +276,8 @@ def run_reference(args, w):
             "impl": "reference", "metric": METRIC, "value": tflops, "unit": "TFLOP/s", "n_gpus": world,
             "steps": steps, "warmup": warm, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": w.name, "B": w.B, "H": w.H, "Nq": w.Nq, "Nk": w.Nk, "d": w.d, "causal": False,
-                       "bias": "none", "pass": "backward", "qk_mult": w.qk_mult},
+            "config": {"workload": w.name, "B": w.B, "H": w.H, "Nq": w.Nq, "Nk": w.Nk, "d": w.d,
+                       "causal": args.causal, "bias": "none", "pass": "backward", "qk_mult": w.qk_mult},
             "cpu_baseline": {"value": tflops, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": tflops, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -360,8 +361,8 @@ def run_ours(args, w):
     flush = torch.empty(L2_FLUSH_BYTES // 4, device=dev, dtype=torch.int32)
     stream = torch.cuda.current_stream(dev)
 
-    if sum([args.causal, args.bias != "none", args.backward]) > 1:
-        raise SystemExit("--causal, --bias and --backward are separate entry points; pick one")
+    if args.bias != "none" and (args.causal or args.backward):
+        raise SystemExit("--bias has no causal or backward entry point; use it alone")
     ins = [q, k, v]
     outs = [o, lse]
     if args.bias != "none":
@@ -369,13 +370,14 @@ def run_ours(args, w):
         ins.append(torch.randn(bshape, device=dev, generator=g).to(torch.bfloat16))
     if args.backward:   # the forward's O and LSE and an upstream gradient are the inputs
         dout = torch.randn(w.B, w.H, w.Nq, w.d, device=dev, generator=g).to(torch.bfloat16)
-        attn.attn_fwd(q, k, v, o, lse, w.B, w.H, w.Nq, w.Nk, w.d, w.scale, stream)
+        (attn.attn_fwd_causal if args.causal else attn.attn_fwd)(q, k, v, o, lse, w.B, w.H, w.Nq, w.Nk, w.d,
+                                                                 w.scale, stream)
         ins = [q, k, v, o, dout, lse]
         outs = [torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)]
 
     def call(ins_, outs_, st):
         if args.backward:
-            attn.attn_bwd(*ins_, *outs_, w.B, w.H, w.Nq, w.Nk, w.d, w.scale, st)
+            attn.attn_bwd(*ins_, *outs_, w.B, w.H, w.Nq, w.Nk, w.d, w.scale, st, causal=args.causal)
         elif args.bias != "none":
             attn.attn_fwd_bias(ins_[0], ins_[1], ins_[2], ins_[3], *outs_, w.B, w.H, w.Nq, w.Nk, w.d, w.scale, st)
         elif args.causal:
@@ -389,7 +391,7 @@ def run_ours(args, w):
     def status_ok(st):
         return attn.attn_fwd_status(st) == attn.ATTN_OK and attn.attn_bwd_status(st) == attn.ATTN_OK
 
-    flops = 2.5 * workload_flops(w, False) if args.backward else workload_flops(w, args.causal)
+    flops = (2.5 if args.backward else 1.0) * workload_flops(w, args.causal)
 
     def step():
         call(ins, outs, stream)
@@ -517,7 +519,7 @@ def run_ours(args, w):
     }
     if rank == 0 and not args.no_cpu_baseline:
         if args.backward:
-            tfl, n, dt, thr = cpu_oracle_backward_sample(w, args.cpu_seconds)
+            tfl, n, dt, thr = cpu_oracle_backward_sample(w, args.cpu_seconds, args.causal)
             sample = f"backward of one head with {n} query rows x {w.Nk} keys of {w.describe()}, FP64, {dt:.1f} s"
         else:
             tfl, n, dt, thr = cpu_oracle_sample(w, args.cpu_seconds, causal=args.causal, bias_kind=args.bias)

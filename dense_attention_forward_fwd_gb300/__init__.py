@@ -16,7 +16,7 @@ from ._build import LIB_PATH, build_library
 __all__ = [
     "ATTN_OK", "ATTN_ERR_INVALID_ARG", "ATTN_ERR_UNSUPPORTED", "ATTN_ERR_MISALIGNED", "ATTN_ERR_CUDA",
     "ATTN_ERR_TIMEOUT", "AttnError", "load_library", "attn_fwd", "attn_fwd_causal", "attn_fwd_bias", "attn_fwd_noalloc", "attn_fwd_status", "attn_status_string",
-    "attn_fwd_set_wait_limit", "attn_fwd_kernel_count", "attention", "attn_bwd", "attn_bwd_status",
+    "attn_fwd_set_wait_limit", "attn_fwd_kernel_count", "attention", "attn_bwd", "attn_bwd_causal", "attn_bwd_status",
     "attn_bwd_kernel_count",
 ]
 
@@ -62,6 +62,8 @@ def load_library(build_if_stale: bool = True) -> ctypes.CDLL:
             lib.attn_fwd_kernel_count.restype = ctypes.c_ulonglong
             lib.attn_bwd.argtypes = [vp] * 9 + [i32] * 5 + [f32, vp]
             lib.attn_bwd.restype = i32
+            lib.attn_bwd_causal.argtypes = lib.attn_bwd.argtypes
+            lib.attn_bwd_causal.restype = i32
             lib.attn_bwd_status.argtypes = [vp]
             lib.attn_bwd_status.restype = i32
             lib.attn_bwd_kernel_count.argtypes = []
@@ -202,10 +204,11 @@ def attn_fwd_noalloc(q, k, v, o, lse, B: int, H: int, Nq: int, Nk: int, d: int, 
 
 
 def attn_bwd(q, k, v, o, dout, lse, dq, dk, dv, B: int, H: int, Nq: int, Nk: int, d: int, scale: float,
-             stream=None) -> None:
+             stream=None, causal: bool = False) -> None:
     """Enqueue the gradients dQ, dK, dV of the forward for upstream gradient ``dout`` (see
     include/attn_bwd.h). q, o, dout, dq: BF16 [B,H,Nq,d]; k, v, dk, dv: BF16 [B,H,Nk,d];
-    lse: the forward's FP32 [B,H,Nq]. CUDA tensors or integer device pointers."""
+    lse: the forward's FP32 [B,H,Nq]. CUDA tensors or integer device pointers. causal: of
+    the causal forward (attn_bwd_causal)."""
     lib = load_library()
     args = (
         _ptr(q, "q", B * H * Nq * d, "bf16"), _ptr(k, "k", B * H * Nk * d, "bf16"),
@@ -214,10 +217,17 @@ def attn_bwd(q, k, v, o, dout, lse, dq, dk, dv, B: int, H: int, Nq: int, Nk: int
         _ptr(dq, "dq", B * H * Nq * d, "bf16"), _ptr(dk, "dk", B * H * Nk * d, "bf16"),
         _ptr(dv, "dv", B * H * Nk * d, "bf16"),
     )
-    rc = lib.attn_bwd(*args, int(B), int(H), int(Nq), int(Nk), int(d), float(scale),
-                      _stream_handle(stream, q, k, v, o, dout, lse, dq, dk, dv))
+    fn = lib.attn_bwd_causal if causal else lib.attn_bwd
+    rc = fn(*args, int(B), int(H), int(Nq), int(Nk), int(d), float(scale),
+            _stream_handle(stream, q, k, v, o, dout, lse, dq, dk, dv))
     if rc != ATTN_OK:
-        raise AttnError(rc, "attn_bwd")
+        raise AttnError(rc, "attn_bwd_causal" if causal else "attn_bwd")
+
+
+def attn_bwd_causal(q, k, v, o, dout, lse, dq, dk, dv, B: int, H: int, Nq: int, Nk: int, d: int, scale: float,
+                    stream=None) -> None:
+    """:func:`attn_bwd` of the causal forward (query i sees keys 0 .. i + Nk - Nq; Nq <= Nk)."""
+    attn_bwd(q, k, v, o, dout, lse, dq, dk, dv, B, H, Nq, Nk, d, scale, stream, causal=True)
 
 
 def attn_bwd_status(stream=None) -> int:

@@ -7,6 +7,11 @@
 //   D_i = dO_i . O_i,  P = 2^(s * scale * log2 e - LSE_i * log2 e),  dP = dO V^T,
 //   dS = P * (dP - D),  dV = P^T dO,  dK = scale * dS^T Q,  dQ = scale * dS K.
 //
+// attn_bwd_causal: the gradient of the causal forward (query i sees keys 0 .. i + Nk - Nq):
+// a dK/dV block starts at the first query tile whose rows see its first key, a dQ block
+// stops at the key tile of its last row's diagonal, and the tiles that cross the
+// diagonal mask P (hence dS) to zero past it.
+//
 // Three kernels, all on the caller's stream:
 //
 //   bwd_rows_kernel  one warp per query row: D_i and LSE_i * log2 e, written as a float2
@@ -259,6 +264,8 @@ struct BwdParams {
   uint16_t* dv;
   const float2* rows;   // [BH, q_pad]: (LSE * log2 e, D)
   int Nq, Nk, q_tiles, k_tiles, q_pad;
+  int causal;   // query i sees keys 0 .. i + off only (off = Nk - Nq >= 0)
+  int off;
   float scale, scale_log2;
   unsigned long long wait_limit;
 };
@@ -383,7 +390,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   c.limit = p.wait_limit;
   const uint32_t tmem = block_setup(c, smem + kKVOffBar, base + kKVOffBar, warp);
   const uint32_t tS = tmem, tdP = tmem + 128, tdV = tmem + 256, tdK = tmem + 384;
-  const int nq = p.q_tiles;
+  // query tiles q0 .. q_tiles - 1; causal: from the first tile whose rows see this tile's
+  // first key (query i sees key r when i >= r - off). Step t of the loops is tile q0 + t.
+  int q0 = 0;
+  if (p.causal) {
+    const int first_row = kt * kT - p.off;
+    q0 = first_row > 0 ? first_row / kT : 0;
+  }
+  const int nq = p.q_tiles - q0;
   auto stage = [&](int s) { return base + kKVOffStage + s * kKVStageBytes; };   // Q | dO | rows
 
   if (warp == 0) {
@@ -401,11 +415,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t fb = c.bar(kBarFull + s);
         mbar_arrive_expect_tx(fb, 2 * kTileBytes + kRowsBytes);
         for (int h = 0; h < 2; ++h) {
-          tma_load_3d(stage(s) + h * kBoxBytes, &tmQ, fb, h * 64, j * kT, bh);
-          tma_load_3d(stage(s) + kTileBytes + h * kBoxBytes, &tmDO, fb, h * 64, j * kT, bh);
+          tma_load_3d(stage(s) + h * kBoxBytes, &tmQ, fb, h * 64, (q0 + j) * kT, bh);
+          tma_load_3d(stage(s) + kTileBytes + h * kBoxBytes, &tmDO, fb, h * 64, (q0 + j) * kT, bh);
         }
-        bulk_load(stage(s) + 2 * kTileBytes, p.rows + static_cast<size_t>(bh) * p.q_pad + static_cast<size_t>(j) * kT,
-                  kRowsBytes, fb);
+        bulk_load(stage(s) + 2 * kTileBytes,
+                  p.rows + static_cast<size_t>(bh) * p.q_pad + static_cast<size_t>(q0 + j) * kT, kRowsBytes, fb);
       }
       // no copy into shared memory may be in flight when the block exits
       wait_phase(c, kBarFixed, 0, false);
@@ -453,6 +467,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_after();
       const float2* rw = reinterpret_cast<const float2*>(smem + kKVOffStage + s * kKVStageBytes + 2 * kTileBytes);
+      // causal: this thread's key r is seen by query columns c >= r - off - (q0 + j) * 128
+      const int key = kt * kT + quarter * 32 + lane;
+      const int c_lo = p.causal ? key - p.off - (q0 + j) * kT : -1;
+      const bool mask_warp = p.causal && (kt * kT + quarter * 32 + 31 - p.off - (q0 + j) * kT) > 64 * grp;
 #pragma unroll 1
       for (int ch = 0; ch < 2; ++ch) {   // 32 query columns at a time
         const int col0 = 64 * grp + 32 * ch;
@@ -463,8 +481,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
           const float2 r0 = rw[col0 + 2 * i], r1 = rw[col0 + 2 * i + 1];
-          const float p0 = ex2(fmaf(__uint_as_float(xs[2 * i]), p.scale_log2, -r0.x));
-          const float p1 = ex2(fmaf(__uint_as_float(xs[2 * i + 1]), p.scale_log2, -r1.x));
+          float p0 = ex2(fmaf(__uint_as_float(xs[2 * i]), p.scale_log2, -r0.x));
+          float p1 = ex2(fmaf(__uint_as_float(xs[2 * i + 1]), p.scale_log2, -r1.x));
+          if (mask_warp) {
+            p0 = col0 + 2 * i >= c_lo ? p0 : 0.0f;
+            p1 = col0 + 2 * i + 1 >= c_lo ? p1 : 0.0f;
+          }
           const float d0 = p0 * (__uint_as_float(xd[2 * i]) - r0.y);
           const float d1 = p1 * (__uint_as_float(xd[2 * i + 1]) - r1.y);
           pw[i] = pack_bf16(p0, p1);
@@ -504,7 +526,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* smem = smem_raw + (base - raw);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int qt = blockIdx.x % p.q_tiles;
+  // causal: the longest blocks (last query tiles) are launched first
+  const int qt = p.causal ? p.q_tiles - 1 - static_cast<int>(blockIdx.x % p.q_tiles)
+                          : static_cast<int>(blockIdx.x % p.q_tiles);
   const int bh = blockIdx.x / p.q_tiles;
   Ctl c;
   c.bars = base + kQOffBar;
@@ -515,7 +539,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   // computed while the compute warps work on this one; dP has one buffer, which the
   // compute warps release as soon as they hold their columns of it in registers.
   const uint32_t tS0 = tmem, tdP = tmem + 128, tdQ = tmem + 256, tS1 = tmem + 384;
-  const int nk = p.k_tiles;
+  // key tiles 0 .. nk - 1; causal: up to the diagonal of this tile's last row
+  const int nk = p.causal ? (min(p.Nq, (qt + 1) * kT) + p.off + kT - 1) / kT : p.k_tiles;
   auto stage = [&](int s) { return base + kQOffStage + s * kQStageBytes; };   // K | V
 
   if (warp == 0) {
@@ -598,7 +623,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_after();
       const uint32_t tSj = (j & 1) ? tS1 : tS0;
-      const int valid = p.Nk - j * kT;   // keys of this tile inside the sequence
+      // keys of this tile inside the sequence: columns < valid; causal: also <= c_hi
+      const int valid = p.Nk - j * kT;
+      const int c_hi = p.causal ? qrow + p.off - j * kT : kT;
+      const bool mask_warp = p.causal && (qt * kT + quarter * 32 + p.off - j * kT) < 64 * grp + 63;
       uint32_t xd[2][32];
       tmem_ld32(tdP + lane_off + 64 * grp, xd[0]);
       tmem_ld32(tdP + lane_off + 64 * grp + 32, xd[1]);
@@ -615,8 +643,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
           const int key = col0 + 2 * i;
-          const float p0 = key < valid ? ex2(fmaf(__uint_as_float(xs[2 * i]), p.scale_log2, -rw.x)) : 0.0f;
-          const float p1 = key + 1 < valid ? ex2(fmaf(__uint_as_float(xs[2 * i + 1]), p.scale_log2, -rw.x)) : 0.0f;
+          float p0 = key < valid ? ex2(fmaf(__uint_as_float(xs[2 * i]), p.scale_log2, -rw.x)) : 0.0f;
+          float p1 = key + 1 < valid ? ex2(fmaf(__uint_as_float(xs[2 * i + 1]), p.scale_log2, -rw.x)) : 0.0f;
+          if (mask_warp) {
+            p0 = key <= c_hi ? p0 : 0.0f;
+            p1 = key + 1 <= c_hi ? p1 : 0.0f;
+          }
           dw[i] = pack_bf16(p0 * (__uint_as_float(xd[ch][2 * i]) - rw.y),
                             p1 * (__uint_as_float(xd[ch][2 * i + 1]) - rw.y));
         }
@@ -692,17 +724,16 @@ int get_rows_workspace(int dev, cudaStream_t stream, size_t bytes, float2** out)
 
 std::atomic<int> g_attr_done{0};
 
-}  // namespace
-
-extern "C" int attn_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,
-                        const float* lse, void* dq, void* dk, void* dv, int B, int H, int Nq, int Nk, int d,
-                        float scale, void* stream) {
+int backward(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
+             void* dq, void* dk, void* dv, int B, int H, int Nq, int Nk, int d, float scale, void* stream,
+             bool causal) {
   if (B < 0 || H < 0 || Nq < 0 || Nk < 0) return ATTN_ERR_INVALID_ARG;
   if (d != kD) return ATTN_ERR_UNSUPPORTED;
   if (!std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
   const long long bh = static_cast<long long>(B) * H;
   if (bh == 0 || Nq == 0) return ATTN_OK;
-  if (Nk == 0) return ATTN_ERR_INVALID_ARG;
+  if (Nk == 0 || (causal && Nq > Nk)) return ATTN_ERR_INVALID_ARG;
+  if (causal && Nk > INT_MAX - 1024) return ATTN_ERR_UNSUPPORTED;   // row + off + 2 * kT stays in int
   if (!q || !k || !v || !o || !dout || !lse || !dq || !dk || !dv) return ATTN_ERR_INVALID_ARG;
   const uintptr_t a16 = reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) |
                         reinterpret_cast<uintptr_t>(v) | reinterpret_cast<uintptr_t>(o) |
@@ -736,6 +767,8 @@ extern "C" int attn_bwd(const void* q, const void* k, const void* v, const void*
   p.scale = scale;
   p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
   p.wait_limit = g_bwd_wait_limit.load(std::memory_order_relaxed);
+  p.causal = causal ? 1 : 0;
+  p.off = causal ? Nk - Nq : 0;
   float2* rows = nullptr;
   {
     const int rc = get_rows_workspace(dev, s, static_cast<size_t>(bh) * p.q_pad * sizeof(float2), &rows);
@@ -767,6 +800,20 @@ extern "C" int attn_bwd(const void* q, const void* k, const void* v, const void*
   if (cudaLaunchKernelEx(&cfg, bwd_dq_kernel, mq, mk, mv, mdo, p) != cudaSuccess) return ATTN_ERR_CUDA;
   g_bwd_launches.fetch_add(1, std::memory_order_relaxed);
   return ATTN_OK;
+}
+
+}  // namespace
+
+extern "C" int attn_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                        const float* lse, void* dq, void* dk, void* dv, int B, int H, int Nq, int Nk, int d,
+                        float scale, void* stream) {
+  return backward(q, k, v, o, dout, lse, dq, dk, dv, B, H, Nq, Nk, d, scale, stream, false);
+}
+
+extern "C" int attn_bwd_causal(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                               const float* lse, void* dq, void* dk, void* dv, int B, int H, int Nq, int Nk, int d,
+                               float scale, void* stream) {
+  return backward(q, k, v, o, dout, lse, dq, dk, dv, B, H, Nq, Nk, d, scale, stream, true);
 }
 
 extern "C" int attn_bwd_status(void* stream) {

@@ -53,6 +53,17 @@ extern "C" {
 int attn_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
              void* dq, void* dk, void* dv, int B, int H, int Nq, int Nk, int d, float scale, void* stream);
 
+/*
+ * attn_bwd_causal -- gradients of the causal forward (attn_fwd_causal: query i sees keys
+ * 0 .. i + Nk - Nq, the mask aligned to the bottom-right corner). Arguments, layouts,
+ * rules and work are those of attn_bwd, with o and lse from attn_fwd_causal, plus
+ * Nq <= Nk (else ATTN_ERR_INVALID_ARG). Blocks visit only the tiles their rows or keys
+ * can see.
+ */
+int attn_bwd_causal(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                    const float* lse, void* dq, void* dk, void* dv, int B, int H, int Nq, int Nk, int d,
+                    float scale, void* stream);
+
 /* Synchronises `stream`, then reads and clears the backward kernels' timeout status:
  * ATTN_OK, ATTN_ERR_TIMEOUT or ATTN_ERR_CUDA. */
 int attn_bwd_status(void* stream);

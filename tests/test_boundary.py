@@ -26,7 +26,8 @@ def declared_functions():
 
 def test_header_declares_the_entry_points():
     names = declared_functions()
-    assert {"attn_fwd", "attn_fwd_causal", "attn_fwd_bias", "attn_fwd_noalloc", "attn_bwd", "attn_bwd_status",
+    assert {"attn_fwd", "attn_fwd_causal", "attn_fwd_bias", "attn_fwd_noalloc", "attn_bwd", "attn_bwd_causal",
+            "attn_bwd_status",
             "attn_bwd_kernel_count", "attn_fwd_status", "attn_status_string",
             "attn_fwd_set_wait_limit", "attn_fwd_kernel_count"} <= set(names)
 
@@ -156,6 +157,20 @@ def call_bwd(q=A, k=A, v=A, o=A, do=A, lse=A, dq=A, dk=A, dv=A, B=1, H=1, Nq=128
 def test_bwd_argument_checks(kw, code):
     before = attn.attn_bwd_kernel_count()
     assert call_bwd(**kw) == code
+    assert attn.attn_bwd_kernel_count() == before
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(Nq=129, Nk=128), attn.ATTN_ERR_INVALID_ARG),   # a query row would see no key
+    (dict(do=None), attn.ATTN_ERR_INVALID_ARG),
+    (dict(d=64), attn.ATTN_ERR_UNSUPPORTED),
+    (dict(B=0), attn.ATTN_OK),
+])
+def test_bwd_causal_argument_checks(kw, code):
+    args = dict(q=A, k=A, v=A, o=A, do=A, lse=A, dq=A, dk=A, dv=A, B=1, H=1, Nq=128, Nk=128, d=128, scale=0.125)
+    args.update(kw)
+    before = attn.attn_bwd_kernel_count()
+    assert attn.load_library().attn_bwd_causal(*args.values(), None) == code
     assert attn.attn_bwd_kernel_count() == before
 
 

@@ -33,7 +33,7 @@ def make_dout(B, H, Nq, seed):
     return f32_to_bf16_bits(rng.standard_normal((B, H, Nq, 128), dtype=np.float32))
 
 
-def run_fwd_bwd(attn, q, k, v, do, scale, stream=None):
+def run_fwd_bwd(attn, q, k, v, do, scale, stream=None, causal=False):
     import torch
     B, H, Nq, d = q.shape
     Nk = k.shape[2]
@@ -42,23 +42,23 @@ def run_fwd_bwd(attn, q, k, v, do, scale, stream=None):
     lse = torch.empty((B, H, Nq), dtype=torch.float32, device="cuda")
     if stream is not None:
         stream.wait_stream(torch.cuda.current_stream())
-    attn.attn_fwd(qd, kd, vd, o, lse, B, H, Nq, Nk, d, scale, stream)
+    (attn.attn_fwd_causal if causal else attn.attn_fwd)(qd, kd, vd, o, lse, B, H, Nq, Nk, d, scale, stream)
     dq = torch.full((B, H, Nq, d), float("nan"), dtype=torch.bfloat16, device="cuda")
     dk = torch.full((B, H, Nk, d), float("nan"), dtype=torch.bfloat16, device="cuda")
     dv = torch.full((B, H, Nk, d), float("nan"), dtype=torch.bfloat16, device="cuda")
     if stream is not None:   # the inputs and outputs were made on the current stream
         stream.wait_stream(torch.cuda.current_stream())
-    attn.attn_bwd(qd, kd, vd, o, dod, lse, dq, dk, dv, B, H, Nq, Nk, d, scale, stream)
+    attn.attn_bwd(qd, kd, vd, o, dod, lse, dq, dk, dv, B, H, Nq, Nk, d, scale, stream, causal=causal)
     assert attn.attn_fwd_status(stream) == attn.ATTN_OK
     assert attn.attn_bwd_status(stream) == attn.ATTN_OK
     return bf16_to_np(dq), bf16_to_np(dk), bf16_to_np(dv)
 
 
-def check_bwd(attn, B, H, Nq, Nk, seed, qk_mult=1.0, scale=SCALE):
+def check_bwd(attn, B, H, Nq, Nk, seed, qk_mult=1.0, scale=SCALE, causal=False):
     q, k, v = make_qkv(B, H, Nq, Nk, seed=seed, qk_mult=qk_mult)
     do = make_dout(B, H, Nq, seed + 1)
-    got = run_fwd_bwd(attn, q, k, v, do, scale)
-    ref = oracle.attention_bwd(q, k, v, do, scale)
+    got = run_fwd_bwd(attn, q, k, v, do, scale, causal=causal)
+    ref = oracle.attention_bwd(q, k, v, do, scale, causal=causal)
     report = {}
     for name, g, r in zip(("dq", "dk", "dv"), got, ref):
         assert np.all(np.isfinite(g)), f"{name}: non-finite output"
@@ -126,3 +126,32 @@ def test_bwd_rejects_bad_arguments(gpu_lib):
     with pytest.raises(gpu_lib.AttnError) as e:
         gpu_lib.attn_bwd(a, a, a, a, a, b, a, a, a, 1, 1, 128, 128, 64, SCALE)
     assert e.value.status == gpu_lib.ATTN_ERR_UNSUPPORTED
+
+
+# ---- causal backward (the gradient of attn_fwd_causal) --------------------------------------------
+
+@pytest.mark.parametrize("B,H,Nq,Nk", [
+    (1, 1, 256, 256),      # two tiles each way: one diagonal tile per block
+    (1, 2, 384, 640),      # Nq < Nk: the diagonal shifted by 256 keys
+    (2, 3, 300, 300),      # ragged tails on the diagonal
+    (1, 1, 1, 200),        # a single query row sees every key
+    (1, 2, 129, 257),      # the shift not a multiple of the tile
+    (1, 2, 1024, 1024),    # blocks of very different lengths
+])
+def test_causal_bwd_parity(gpu_lib, B, H, Nq, Nk):
+    check_bwd(gpu_lib, B, H, Nq, Nk, seed=12000 + Nq + Nk, causal=True)
+
+
+def test_causal_bwd_peaked_and_other_scale(gpu_lib):
+    check_bwd(gpu_lib, 1, 2, 512, 768, seed=12100, qk_mult=3.0, causal=True)
+    check_bwd(gpu_lib, 1, 1, 256, 384, seed=12101, scale=-0.0883883461356163, causal=True)
+
+
+def test_causal_bwd_rejects_more_queries_than_keys(gpu_lib):
+    import torch
+    t = torch.zeros(1, 1, 256, 128, dtype=torch.bfloat16, device="cuda")
+    lse = torch.zeros(1, 1, 256, dtype=torch.float32, device="cuda")
+    a, b = t.data_ptr(), lse.data_ptr()
+    with pytest.raises(gpu_lib.AttnError) as e:
+        gpu_lib.attn_bwd_causal(a, a, a, a, a, b, a, a, a, 1, 1, 256, 128, 128, SCALE)
+    assert e.value.status == gpu_lib.ATTN_ERR_INVALID_ARG
