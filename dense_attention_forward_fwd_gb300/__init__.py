@@ -17,7 +17,7 @@ __all__ = [
     "ATTN_OK", "ATTN_ERR_INVALID_ARG", "ATTN_ERR_UNSUPPORTED", "ATTN_ERR_MISALIGNED", "ATTN_ERR_CUDA",
     "ATTN_ERR_TIMEOUT", "AttnError", "load_library", "attn_fwd", "attn_fwd_causal", "attn_fwd_bias", "attn_fwd_noalloc", "attn_fwd_status", "attn_status_string",
     "attn_fwd_set_wait_limit", "attn_fwd_kernel_count", "attention", "attn_bwd", "attn_bwd_causal", "attn_bwd_status",
-    "attn_bwd_kernel_count",
+    "attn_bwd_kernel_count", "attn_bwd_set_wait_limit",
 ]
 
 ATTN_OK = 0
@@ -68,6 +68,8 @@ def load_library(build_if_stale: bool = True) -> ctypes.CDLL:
             lib.attn_bwd_status.restype = i32
             lib.attn_bwd_kernel_count.argtypes = []
             lib.attn_bwd_kernel_count.restype = ctypes.c_ulonglong
+            lib.attn_bwd_set_wait_limit.argtypes = [ctypes.c_ulonglong, i32]
+            lib.attn_bwd_set_wait_limit.restype = i32
             _lib = lib
     return _lib
 
@@ -233,6 +235,12 @@ def attn_bwd_causal(q, k, v, o, dout, lse, dq, dk, dv, B: int, H: int, Nq: int, 
 def attn_bwd_status(stream=None) -> int:
     """Synchronise ``stream`` and return (and clear) the backward kernels' timeout status."""
     return load_library().attn_bwd_status(_stream_handle(stream))
+
+
+def attn_bwd_set_wait_limit(cycles: int = 0, withhold_tile: bool = False) -> None:
+    """Test hook: per-wait time limit of backward launches in SM cycles (0 = default) and the
+    withheld-tile switch."""
+    load_library().attn_bwd_set_wait_limit(int(cycles), 1 if withhold_tile else 0)
 
 
 def attn_bwd_kernel_count() -> int:

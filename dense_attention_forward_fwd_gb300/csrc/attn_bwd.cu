@@ -266,6 +266,7 @@ struct BwdParams {
   int Nq, Nk, q_tiles, k_tiles, q_pad;
   int causal;   // query i sees keys 0 .. i + off only (off = Nk - Nq >= 0)
   int off;
+  int withhold;   // test hook: the dK/dV producer stops before its second query tile
   float scale, scale_log2;
   unsigned long long wait_limit;
 };
@@ -412,6 +413,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int j = 0; j < nq; ++j, ++issued) {
         const int s = j & 1;
         if (j >= 2 && !wait_phase(c, kBarEmpty + s, ((j >> 1) - 1) & 1, true)) break;
+        if (p.withhold && j == 1) break;   // test hook: the consumers' waits for this tile run out
         const uint32_t fb = c.bar(kBarFull + s);
         mbar_arrive_expect_tx(fb, 2 * kTileBytes + kRowsBytes);
         for (int h = 0; h < 2; ++h) {
@@ -675,6 +677,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 // ---------------------------------------------------------------------------------
 std::atomic<unsigned long long> g_bwd_launches{0};
 std::atomic<unsigned long long> g_bwd_wait_limit{kDefaultWaitLimit};
+std::atomic<int> g_bwd_withhold{0};
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 std::once_flag g_encode_once;
@@ -769,6 +772,7 @@ int backward(const void* q, const void* k, const void* v, const void* o, const v
   p.wait_limit = g_bwd_wait_limit.load(std::memory_order_relaxed);
   p.causal = causal ? 1 : 0;
   p.off = causal ? Nk - Nq : 0;
+  p.withhold = g_bwd_withhold.load(std::memory_order_relaxed);
   float2* rows = nullptr;
   {
     const int rc = get_rows_workspace(dev, s, static_cast<size_t>(bh) * p.q_pad * sizeof(float2), &rows);
@@ -831,3 +835,9 @@ extern "C" int attn_bwd_status(void* stream) {
 }
 
 extern "C" unsigned long long attn_bwd_kernel_count(void) { return g_bwd_launches.load(std::memory_order_relaxed); }
+
+extern "C" int attn_bwd_set_wait_limit(unsigned long long cycles, int withhold_tile) {
+  g_bwd_wait_limit.store(cycles ? cycles : kDefaultWaitLimit, std::memory_order_relaxed);
+  g_bwd_withhold.store(withhold_tile ? 1 : 0, std::memory_order_relaxed);
+  return ATTN_OK;
+}

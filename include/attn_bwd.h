@@ -68,6 +68,15 @@ int attn_bwd_causal(const void* q, const void* k, const void* v, const void* o, 
  * ATTN_OK, ATTN_ERR_TIMEOUT or ATTN_ERR_CUDA. */
 int attn_bwd_status(void* stream);
 
+/*
+ * Test hook for the failure path (mirrors attn_fwd_set_wait_limit): `cycles` sets the
+ * per-wait time limit of later backward launches in SM clock cycles (0 restores the
+ * default of 2^31); `withhold_tile` != 0 makes the dK/dV kernel's loader stop before the
+ * second query tile of every block, so the waits for it run out and the call reports
+ * ATTN_ERR_TIMEOUT through attn_bwd_status. Not for production use.
+ */
+int attn_bwd_set_wait_limit(unsigned long long cycles, int withhold_tile);
+
 /* Kernel launches made by attn_bwd in this process (three per call that does work). */
 unsigned long long attn_bwd_kernel_count(void);
 

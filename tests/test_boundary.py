@@ -27,7 +27,7 @@ def declared_functions():
 def test_header_declares_the_entry_points():
     names = declared_functions()
     assert {"attn_fwd", "attn_fwd_causal", "attn_fwd_bias", "attn_fwd_noalloc", "attn_bwd", "attn_bwd_causal",
-            "attn_bwd_status",
+            "attn_bwd_status", "attn_bwd_set_wait_limit",
             "attn_bwd_kernel_count", "attn_fwd_status", "attn_status_string",
             "attn_fwd_set_wait_limit", "attn_fwd_kernel_count"} <= set(names)
 

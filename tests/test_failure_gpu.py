@@ -35,3 +35,30 @@ def test_withheld_tile_times_out_cleanly(gpu_lib):
     assert attn.attn_fwd_status() == attn.ATTN_OK   # reading the status clears it
     # the context is still usable and the next launch is exact again
     check_case(attn, 1, 2, 512, 1024, seed=21)
+
+
+def test_backward_withheld_tile_times_out_cleanly(gpu_lib):
+    # the dK/dV kernel's loader stops before the second query tile: every waiting role of
+    # every block gives up after the short limit, the call reports ATTN_ERR_TIMEOUT, and
+    # the next backward is exact again
+    import torch
+    attn = gpu_lib
+    from test_bwd_gpu import check_bwd, make_dout
+    q, k, v = make_qkv(1, 2, 512, 384, seed=22)
+    do = make_dout(1, 2, 512, 23)
+    qd, kd, vd, dod = (to_device(x) for x in (q, k, v, do))
+    o = torch.empty((1, 2, 512, 128), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((1, 2, 512), dtype=torch.float32, device="cuda")
+    attn.attn_fwd(qd, kd, vd, o, lse, 1, 2, 512, 384, 128, 0.0883883461356163)
+    assert attn.attn_fwd_status() == attn.ATTN_OK
+    grads = [torch.zeros((1, 2, n, 128), dtype=torch.bfloat16, device="cuda") for n in (512, 384, 384)]
+    assert attn.attn_bwd_status() == attn.ATTN_OK
+    attn.attn_bwd_set_wait_limit(SHORT_LIMIT, withhold_tile=True)
+    try:
+        attn.attn_bwd(qd, kd, vd, o, dod, lse, *grads, 1, 2, 512, 384, 128, 0.0883883461356163)
+        status = attn.attn_bwd_status()
+    finally:
+        attn.attn_bwd_set_wait_limit(0, withhold_tile=False)
+    assert status == attn.ATTN_ERR_TIMEOUT
+    assert attn.attn_bwd_status() == attn.ATTN_OK
+    check_bwd(attn, 1, 2, 512, 384, seed=24)
