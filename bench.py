@@ -78,6 +78,15 @@ def dist_env():
     return int(os.environ.get("RANK", 0)), int(os.environ.get("LOCAL_RANK", 0)), int(os.environ.get("WORLD_SIZE", 1))
 
 
+def run_config(w, args) -> dict:
+    """The workload description both arms print (the reference arm times the same one)."""
+    return {"workload": w.name, "B": w.B, "H": w.H, "Nq": w.Nq, "Nk": w.Nk, "d": w.d, "causal": args.causal,
+            "bias": args.bias, "pass": "backward" if args.backward else "forward", "qk_mult": w.qk_mult,
+            "inputs": "iid N(0,1) BF16 (Q,K x qk_mult)",
+            "l2": "flushed (512 MiB write) before every timed launch",
+            "vs_baseline_ref": "RTX 5090 v5 kernel, same shape (other hardware: context only)"}
+
+
 def max_over_ranks(values, pg, device):
     """Each value's maximum over all ranks (a job takes as long as its slowest rank)."""
     import torch
@@ -276,8 +285,7 @@ def run_reference(args, w):
             "impl": "reference", "metric": METRIC, "value": tflops, "unit": "TFLOP/s", "n_gpus": world,
             "steps": steps, "warmup": warm, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": w.name, "B": w.B, "H": w.H, "Nq": w.Nq, "Nk": w.Nk, "d": w.d,
-                       "causal": args.causal, "bias": "none", "pass": "backward", "qk_mult": w.qk_mult},
+            "config": run_config(w, args),
             "cpu_baseline": {"value": tflops, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": tflops, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -318,8 +326,7 @@ def run_reference(args, w):
         "impl": "reference", "metric": METRIC, "value": tflops, "unit": "TFLOP/s", "n_gpus": world,
         "steps": steps, "warmup": warm, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": w.name, "B": w.B, "H": w.H, "Nq": w.Nq, "Nk": w.Nk, "d": w.d, "causal": args.causal, "bias": args.bias,
-                   "pass": "forward", "qk_mult": w.qk_mult},
+        "config": run_config(w, args),
         "cpu_baseline": {"value": tflops, "unit": "TFLOP/s", "cores": threads, "kind": "oracle", "sample": sample},
         "e2e": {"value": tflops, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
         "gpu_launches": 0,
@@ -505,10 +512,7 @@ def run_ours(args, w):
                         if w.name in PAGES_TFLOPS and not args.causal and args.bias == "none" and not args.backward
                         else None),
         "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": w.name, "B": w.B, "H": w.H, "Nq": w.Nq, "Nk": w.Nk, "d": w.d, "causal": args.causal, "bias": args.bias,
-                   "pass": "backward" if args.backward else "forward", "qk_mult": w.qk_mult, "inputs": "iid N(0,1) BF16 (Q,K x qk_mult)",
-                   "l2": "flushed (512 MiB write) before every timed launch",
-                   "vs_baseline_ref": "RTX 5090 v5 kernel, same shape (other hardware: context only)"},
+        "config": run_config(w, args),
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak, "traffic": traffic,
                      "peak_source": f"{peak_src} bf16_tflops (burst: each launch is timed alone)"},
