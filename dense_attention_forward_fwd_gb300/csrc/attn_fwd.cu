@@ -1,4 +1,5 @@
-// attn_fwd.cu -- dense BF16 attention forward for GB300 (sm_103a), non-causal and causal.
+// attn_fwd.cu -- dense BF16 attention forward for GB300 (sm_103a): non-causal, causal
+// (attn_fwd_causal) and with an additive bias (attn_fwd_bias, a third instantiation).
 //
 // O = softmax(scale * Q K^T) V and the per-row log-sum-exp, head_dim 128, computed
 // FlashAttention-style: Q tiles of 128 query rows are loaded once and 128-key K/V
@@ -32,7 +33,13 @@
 // or two waves' worth of groups, an even split of their key steps over all blocks, so
 // no SM idles at the end. A group split between blocks is finished by whichever block
 // completes its share last: every share leaves its unnormalised O, running max and
-// sums in a workspace, and the last one merges them. No block waits for another.
+// sums in a workspace, and the last one merges them in share order (so results do not
+// depend on which block finished last). No block waits for another. Causal launches
+// take whole groups only, each over the key steps up to its last row's diagonal,
+// longest first in snake order across blocks; the softmax masks keys past each row's
+// diagonal on the steps that cross it. Bias launches add the bias to the scaled scores
+// before the row max; each softmax warp reads its rows' bias with coalesced loads and
+// transposes it through its staging tile.
 //
 // The softmax keeps, per row, m (running max of scale*s in log2 units) and l (running
 // sum of 2^(scale*s*log2e - m)). O is accumulated unnormalised and divided once at the
