@@ -374,6 +374,7 @@ __global__ void __launch_bounds__(256) bwd_rows_kernel(const uint16_t* __restric
 // ---------------------------------------------------------------------------------
 // dK / dV: one block per (b, h, key tile)
 // ---------------------------------------------------------------------------------
+template <bool kCausal>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
@@ -394,7 +395,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // query tiles q0 .. q_tiles - 1; causal: from the first tile whose rows see this tile's
   // first key (query i sees key r when i >= r - off). Step t of the loops is tile q0 + t.
   int q0 = 0;
-  if (p.causal) {
+  if (kCausal) {
     const int first_row = kt * kT - p.off;
     q0 = first_row > 0 ? first_row / kT : 0;
   }
@@ -471,8 +472,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float2* rw = reinterpret_cast<const float2*>(smem + kKVOffStage + s * kKVStageBytes + 2 * kTileBytes);
       // causal: this thread's key r is seen by query columns c >= r - off - (q0 + j) * 128
       const int key = kt * kT + quarter * 32 + lane;
-      const int c_lo = p.causal ? key - p.off - (q0 + j) * kT : -1;
-      const bool mask_warp = p.causal && (kt * kT + quarter * 32 + 31 - p.off - (q0 + j) * kT) > 64 * grp;
+      const int c_lo = kCausal ? key - p.off - (q0 + j) * kT : -1;
+      const bool mask_warp = kCausal && (kt * kT + quarter * 32 + 31 - p.off - (q0 + j) * kT) > 64 * grp;
 #pragma unroll 1
       for (int ch = 0; ch < 2; ++ch) {   // 32 query columns at a time
         const int col0 = 64 * grp + 32 * ch;
@@ -519,6 +520,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 // ---------------------------------------------------------------------------------
 // dQ: one block per (b, h, query tile)
 // ---------------------------------------------------------------------------------
+template <bool kCausal>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
@@ -529,7 +531,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* smem = smem_raw + (base - raw);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // causal: the longest blocks (last query tiles) are launched first
-  const int qt = p.causal ? p.q_tiles - 1 - static_cast<int>(blockIdx.x % p.q_tiles)
+  const int qt = kCausal ? p.q_tiles - 1 - static_cast<int>(blockIdx.x % p.q_tiles)
                           : static_cast<int>(blockIdx.x % p.q_tiles);
   const int bh = blockIdx.x / p.q_tiles;
   Ctl c;
@@ -542,7 +544,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // compute warps release as soon as they hold their columns of it in registers.
   const uint32_t tS0 = tmem, tdP = tmem + 128, tdQ = tmem + 256, tS1 = tmem + 384;
   // key tiles 0 .. nk - 1; causal: up to the diagonal of this tile's last row
-  const int nk = p.causal ? (min(p.Nq, (qt + 1) * kT) + p.off + kT - 1) / kT : p.k_tiles;
+  const int nk = kCausal ? (min(p.Nq, (qt + 1) * kT) + p.off + kT - 1) / kT : p.k_tiles;
   auto stage = [&](int s) { return base + kQOffStage + s * kQStageBytes; };   // K | V
 
   if (warp == 0) {
@@ -627,8 +629,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t tSj = (j & 1) ? tS1 : tS0;
       // keys of this tile inside the sequence: columns < valid; causal: also <= c_hi
       const int valid = p.Nk - j * kT;
-      const int c_hi = p.causal ? qrow + p.off - j * kT : kT;
-      const bool mask_warp = p.causal && (qt * kT + quarter * 32 + p.off - j * kT) < 64 * grp + 63;
+      const int c_hi = kCausal ? qrow + p.off - j * kT : kT;
+      const bool mask_warp = kCausal && (qt * kT + quarter * 32 + p.off - j * kT) < 64 * grp + 63;
       uint32_t xd[2][32];
       tmem_ld32(tdP + lane_off + 64 * grp, xd[0]);
       tmem_ld32(tdP + lane_off + 64 * grp + 32, xd[1]);
@@ -725,7 +727,32 @@ int get_rows_workspace(int dev, cudaStream_t stream, size_t bytes, float2** out)
   return ATTN_OK;
 }
 
-std::atomic<int> g_attr_done{0};
+std::atomic<int> g_attr_done[2] = {{0}, {0}};   // per instantiation (plain, causal)
+
+template <bool kCausal>
+int launch_bwd(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, const CUtensorMap& mdo,
+               const BwdParams& p, long long bh, long long k_tiles, long long q_tiles, cudaStream_t s) {
+  if (!g_attr_done[kCausal].load(std::memory_order_acquire)) {
+    if (cudaFuncSetAttribute(bwd_dkdv_kernel<kCausal>, cudaFuncAttributeMaxDynamicSharedMemorySize, kKVSmem) !=
+            cudaSuccess ||
+        cudaFuncSetAttribute(bwd_dq_kernel<kCausal>, cudaFuncAttributeMaxDynamicSharedMemorySize, kQSmem) !=
+            cudaSuccess)
+      return ATTN_ERR_CUDA;
+    g_attr_done[kCausal].store(1, std::memory_order_release);
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.blockDim = dim3(kThreads);
+  cfg.stream = s;
+  cfg.gridDim = dim3(static_cast<unsigned>(bh * k_tiles));
+  cfg.dynamicSmemBytes = kKVSmem;
+  if (cudaLaunchKernelEx(&cfg, bwd_dkdv_kernel<kCausal>, mq, mk, mv, mdo, p) != cudaSuccess) return ATTN_ERR_CUDA;
+  g_bwd_launches.fetch_add(1, std::memory_order_relaxed);
+  cfg.gridDim = dim3(static_cast<unsigned>(bh * q_tiles));
+  cfg.dynamicSmemBytes = kQSmem;
+  if (cudaLaunchKernelEx(&cfg, bwd_dq_kernel<kCausal>, mq, mk, mv, mdo, p) != cudaSuccess) return ATTN_ERR_CUDA;
+  g_bwd_launches.fetch_add(1, std::memory_order_relaxed);
+  return ATTN_OK;
+}
 
 int backward(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
              void* dq, void* dk, void* dv, int B, int H, int Nq, int Nk, int d, float scale, void* stream,
@@ -780,30 +807,14 @@ int backward(const void* q, const void* k, const void* v, const void* o, const v
   }
   p.rows = rows;
 
-  if (!g_attr_done.load(std::memory_order_acquire)) {
-    if (cudaFuncSetAttribute(bwd_dkdv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kKVSmem) != cudaSuccess ||
-        cudaFuncSetAttribute(bwd_dq_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kQSmem) != cudaSuccess)
-      return ATTN_ERR_CUDA;
-    g_attr_done.store(1, std::memory_order_release);
-  }
   const long long n_rows = bh * p.q_pad;
   bwd_rows_kernel<<<static_cast<unsigned>((n_rows + 7) / 8), 256, 0, s>>>(
       static_cast<const uint16_t*>(o), static_cast<const uint16_t*>(dout), lse, rows, bh, Nq, p.q_pad);
   if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
   g_bwd_launches.fetch_add(1, std::memory_order_relaxed);
 
-  cudaLaunchConfig_t cfg = {};
-  cfg.blockDim = dim3(kThreads);
-  cfg.stream = s;
-  cfg.gridDim = dim3(static_cast<unsigned>(bh * k_tiles));
-  cfg.dynamicSmemBytes = kKVSmem;
-  if (cudaLaunchKernelEx(&cfg, bwd_dkdv_kernel, mq, mk, mv, mdo, p) != cudaSuccess) return ATTN_ERR_CUDA;
-  g_bwd_launches.fetch_add(1, std::memory_order_relaxed);
-  cfg.gridDim = dim3(static_cast<unsigned>(bh * q_tiles));
-  cfg.dynamicSmemBytes = kQSmem;
-  if (cudaLaunchKernelEx(&cfg, bwd_dq_kernel, mq, mk, mv, mdo, p) != cudaSuccess) return ATTN_ERR_CUDA;
-  g_bwd_launches.fetch_add(1, std::memory_order_relaxed);
-  return ATTN_OK;
+  return causal ? launch_bwd<true>(mq, mk, mv, mdo, p, bh, k_tiles, q_tiles, s)
+                : launch_bwd<false>(mq, mk, mv, mdo, p, bh, k_tiles, q_tiles, s);
 }
 
 }  // namespace
