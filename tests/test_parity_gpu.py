@@ -306,3 +306,25 @@ def test_split_groups_give_bit_identical_results_on_every_run(gpu_lib, bias_kind
         outs.append((o.cpu(), lse.cpu()))
     for o, lse in outs[1:]:
         assert torch.equal(o, outs[0][0]) and torch.equal(lse, outs[0][1])
+
+
+# ---- shapes at the edges of the schedule ---------------------------------------------------------
+
+def test_many_tiny_heads(gpu_lib):
+    # 2560 groups of one key step each: many waves of short segments, a 16-key ragged tile
+    check_case(gpu_lib, 64, 40, 16, 16, seed=13000)
+
+
+def test_one_query_over_twenty_thousand_keys(gpu_lib):
+    # one group, 157 key steps: every block takes a share of the same group and one merges
+    check_case(gpu_lib, 1, 1, 1, 20000, seed=13001)
+
+
+def test_causal_single_row_over_a_long_sequence(gpu_lib):
+    check_case(gpu_lib, 1, 2, 1, 9000, seed=13002, causal=True)
+
+
+def test_bias_over_a_single_key(gpu_lib):
+    # Nk = 1: every row's softmax is exactly 1 whatever the bias; O = V_0
+    bias = make_bias((1, 1, 1, 1), seed=13003, std=3.0)
+    check_case(gpu_lib, 1, 2, 300, 1, seed=13004, bias=bias)
