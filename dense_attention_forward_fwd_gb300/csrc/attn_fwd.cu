@@ -367,17 +367,6 @@ __device__ __forceinline__ void tmem_ld128(uint32_t taddr, uint32_t (&x)[128]) {
       : "r"(taddr)
       : "memory");
 }
-// 64 TMEM columns of this warp's 32 lanes; the load is only issued here and completes
-// at tmem_wait_ld64, which takes the same registers so that no use is scheduled before it
-__device__ __forceinline__ void tmem_ld64_issue(uint32_t taddr, uint32_t (&x)[64]) {
-  asm volatile("tcgen05.ld.sync.aligned.32x32b.x64.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32, %33, %34, %35, %36, %37, %38, %39, %40, %41, %42, %43, %44, %45, %46, %47, %48, %49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, %60, %61, %62, %63}, [%64];"
-               : "=r"(x[0]), "=r"(x[1]), "=r"(x[2]), "=r"(x[3]), "=r"(x[4]), "=r"(x[5]), "=r"(x[6]), "=r"(x[7]), "=r"(x[8]), "=r"(x[9]), "=r"(x[10]), "=r"(x[11]), "=r"(x[12]), "=r"(x[13]), "=r"(x[14]), "=r"(x[15]), "=r"(x[16]), "=r"(x[17]), "=r"(x[18]), "=r"(x[19]), "=r"(x[20]), "=r"(x[21]), "=r"(x[22]), "=r"(x[23]), "=r"(x[24]), "=r"(x[25]), "=r"(x[26]), "=r"(x[27]), "=r"(x[28]), "=r"(x[29]), "=r"(x[30]), "=r"(x[31]), "=r"(x[32]), "=r"(x[33]), "=r"(x[34]), "=r"(x[35]), "=r"(x[36]), "=r"(x[37]), "=r"(x[38]), "=r"(x[39]), "=r"(x[40]), "=r"(x[41]), "=r"(x[42]), "=r"(x[43]), "=r"(x[44]), "=r"(x[45]), "=r"(x[46]), "=r"(x[47]), "=r"(x[48]), "=r"(x[49]), "=r"(x[50]), "=r"(x[51]), "=r"(x[52]), "=r"(x[53]), "=r"(x[54]), "=r"(x[55]), "=r"(x[56]), "=r"(x[57]), "=r"(x[58]), "=r"(x[59]), "=r"(x[60]), "=r"(x[61]), "=r"(x[62]), "=r"(x[63])
-               : "r"(taddr)
-               : "memory");
-}
-__device__ __forceinline__ void tmem_wait_ld64(uint32_t (&x)[64]) {
-  asm volatile("tcgen05.wait::ld.sync.aligned;" : "+r"(x[0]), "+r"(x[1]), "+r"(x[2]), "+r"(x[3]), "+r"(x[4]), "+r"(x[5]), "+r"(x[6]), "+r"(x[7]), "+r"(x[8]), "+r"(x[9]), "+r"(x[10]), "+r"(x[11]), "+r"(x[12]), "+r"(x[13]), "+r"(x[14]), "+r"(x[15]), "+r"(x[16]), "+r"(x[17]), "+r"(x[18]), "+r"(x[19]), "+r"(x[20]), "+r"(x[21]), "+r"(x[22]), "+r"(x[23]), "+r"(x[24]), "+r"(x[25]), "+r"(x[26]), "+r"(x[27]), "+r"(x[28]), "+r"(x[29]), "+r"(x[30]), "+r"(x[31]), "+r"(x[32]), "+r"(x[33]), "+r"(x[34]), "+r"(x[35]), "+r"(x[36]), "+r"(x[37]), "+r"(x[38]), "+r"(x[39]), "+r"(x[40]), "+r"(x[41]), "+r"(x[42]), "+r"(x[43]), "+r"(x[44]), "+r"(x[45]), "+r"(x[46]), "+r"(x[47]), "+r"(x[48]), "+r"(x[49]), "+r"(x[50]), "+r"(x[51]), "+r"(x[52]), "+r"(x[53]), "+r"(x[54]), "+r"(x[55]), "+r"(x[56]), "+r"(x[57]), "+r"(x[58]), "+r"(x[59]), "+r"(x[60]), "+r"(x[61]), "+r"(x[62]), "+r"(x[63]) : : "memory");
-}
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&x)[32]) {
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];\n\t"
@@ -951,16 +940,19 @@ __device__ void run_softmax(const Ctl& c, uint32_t tmem, uint8_t* stage, const P
         // s = scale * q.k + B, one 64-key half at a time
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
-          uint32_t x[64];
-          tmem_ld64_issue(tS + h * 64, x);   // completes while the bias half is transposed
           uint32_t b[32];
           bias_half_to_row(stage, bg, h, b);
-          tmem_wait_ld64(x);
 #pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            const uint32_t b2 = b[i];
-            fma2v(s[h * 64 + 2 * i], s[h * 64 + 2 * i + 1], __uint_as_float(x[2 * i]), __uint_as_float(x[2 * i + 1]),
-                  p.scale, __uint_as_float(b2 << 16), __uint_as_float(b2 & 0xffff0000u));
+          for (int q2 = 0; q2 < 2; ++q2) {
+            uint32_t x[32];
+            tmem_ld32(tS + h * 64 + q2 * 32, x);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const uint32_t b2 = b[q2 * 16 + i];
+              fma2v(s[h * 64 + q2 * 32 + 2 * i], s[h * 64 + q2 * 32 + 2 * i + 1], __uint_as_float(x[2 * i]),
+                    __uint_as_float(x[2 * i + 1]), p.scale, __uint_as_float(b2 << 16),
+                    __uint_as_float(b2 & 0xffff0000u));
+            }
           }
         }
       } else {
