@@ -1,7 +1,7 @@
 """Seeded synthetic inputs for dense attention (shared by the CUDA path's tests and the oracle's).
 
-This module draws random numbers and rounds them to BF16; it holds none of the
-attention arithmetic. Both the GPU parity tests and the CPU oracle take their
+This module draws random numbers and rounds them to BF16 (or, for Q and K given as
+FP8, quantizes them to E4M3 codes); it holds none of the attention arithmetic. Both the GPU parity tests and the CPU oracle take their
 Q, K, V from here, so the two sides always see bit-identical inputs.
 
 Recipe (the pages' workloads are iid-normal BF16 tensors of shape
@@ -29,6 +29,7 @@ __all__ = [
     "bf16_bits_to_f32",
     "make_qkv",
     "make_bias",
+    "make_qk_e4m3",
     "BF16_NEG_INF",
     "sample_rows",
 ]
@@ -66,6 +67,33 @@ def make_qkv(B: int, H: int, Nq: int, Nk: int, d: int = 128, seed: int = 0,
         q = q * m
         k = k * m
     return f32_to_bf16_bits(q), f32_to_bf16_bits(k), f32_to_bf16_bits(v)
+
+
+def make_qk_e4m3(B: int, H: int, Nq: int, Nk: int, d: int = 128, seed: int = 0, qk_mult: float = 1.0):
+    """Q and K as FP8 E4M3 codes with per-tensor descale factors, V as BF16 bits.
+
+    Draws the float32 normals of :func:`make_qkv` with the same seed (so V is bit-identical
+    to its V), then quantizes Q and K per tensor the usual way for FP8 inputs: descale =
+    amax / 448 (448 being the largest finite E4M3 value), rounded to float32, and codes =
+    E4M3(x / descale) by torch's round-to-nearest-even conversion. Returns
+    (q8 uint8 [B,H,Nq,d], k8 uint8 [B,H,Nk,d], v uint16 [B,H,Nk,d], q_descale, k_descale).
+    """
+    import torch
+    rng = np.random.Generator(np.random.PCG64(seed))
+    q = rng.standard_normal((B, H, Nq, d), dtype=np.float32)
+    k = rng.standard_normal((B, H, Nk, d), dtype=np.float32)
+    v = rng.standard_normal((B, H, Nk, d), dtype=np.float32)
+    if qk_mult != 1.0:
+        m = np.float32(qk_mult)
+        q = q * m
+        k = k * m
+    out = []
+    for x in (q, k):
+        amax = float(np.abs(x).max()) if x.size else 1.0
+        ds = np.float32(amax / 448.0) if amax > 0 else np.float32(1.0)
+        codes = torch.from_numpy(np.ascontiguousarray(x / ds)).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+        out += [codes, float(ds)]
+    return out[0], out[2], f32_to_bf16_bits(v), out[1], out[3]
 
 
 def make_bias(shape, seed: int, std: float = 1.0) -> np.ndarray:

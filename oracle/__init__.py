@@ -19,7 +19,8 @@ import threading
 import numpy as np
 
 __all__ = ["build", "Oracle", "default", "attention_rows", "attention_rows_causal", "attention_rows_bias",
-           "attention", "attention_dense", "attention_bwd", "probs", "max_threads", "LIB_PATH"]
+           "attention", "attention_dense", "attention_bwd", "probs", "max_threads", "LIB_PATH",
+           "attention_rows_e4m3qk", "e4m3_to_f64"]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "attn_ref.c")
@@ -55,6 +56,11 @@ class Oracle:
         lib.attn_ref_rows_bias_f64.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, i64, i64, i64, i64, i64, dbl,
                                                vp, i64, vp, vp, ctypes.c_int]
         lib.attn_ref_rows_bias_f64.restype = ctypes.c_int
+        lib.attn_ref_rows_e4m3qk_f64.argtypes = [vp, vp, vp, i64, i64, i64, i64, i64, dbl, dbl, dbl, vp, i64, vp,
+                                                 vp, ctypes.c_int]
+        lib.attn_ref_rows_e4m3qk_f64.restype = ctypes.c_int
+        lib.attn_ref_e4m3_to_f64.argtypes = [vp, i64, vp]
+        lib.attn_ref_e4m3_to_f64.restype = None
         lib.attn_ref_dense_f64.argtypes = [vp, vp, vp, i64, i64, i64, i64, i64, dbl, vp, vp]
         lib.attn_ref_dense_f64.restype = ctypes.c_int
         lib.attn_ref_bwd_f64.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, i64, dbl, vp, vp, vp, ctypes.c_int]
@@ -141,6 +147,38 @@ class Oracle:
                                              int(nthreads))
         if rc != 0:
             raise ValueError(f"attn_ref_rows_bias_f64 failed with status {rc}")
+        return o, lse
+
+    def e4m3_to_f64(self, codes):
+        """Values of FP8 E4M3 codes (uint8 array of any shape) as float64 (NaN for the NaN codes)."""
+        c = np.ascontiguousarray(codes, dtype=np.uint8)
+        out = np.empty(c.shape, dtype=np.float64)
+        self.lib.attn_ref_e4m3_to_f64(_ptr(c), c.size, _ptr(out))
+        return out
+
+    def attention_rows_e4m3qk(self, q8, k8, v, scale: float, q_descale: float = 1.0, k_descale: float = 1.0,
+                              rows=None, nthreads: int = 0):
+        """As attention_rows with Q and K given as FP8 E4M3 codes (uint8 [B,H,N,d]) and their
+        per-tensor descale factors: the scores are scale * (q_descale Q8)(k_descale K8)^T."""
+        q8 = np.ascontiguousarray(q8)
+        k8 = np.ascontiguousarray(k8)
+        if q8.dtype != np.uint8 or k8.dtype != np.uint8:
+            raise TypeError("q8 and k8 must be uint8 E4M3 codes")
+        v = _u16(v, 4)
+        B, H, Nq, d = q8.shape
+        Nk, dv = k8.shape[2], v.shape[3]
+        if k8.shape != (B, H, Nk, d) or v.shape[:3] != (B, H, Nk):
+            raise ValueError(f"shape mismatch q8{q8.shape} k8{k8.shape} v{v.shape}")
+        if rows is None:
+            rows = np.arange(B * H * Nq, dtype=np.int64)
+        rows = np.ascontiguousarray(rows, dtype=np.int64)
+        o = np.empty((rows.size, dv), dtype=np.float64)
+        lse = np.empty(rows.size, dtype=np.float64)
+        rc = self.lib.attn_ref_rows_e4m3qk_f64(_ptr(q8), _ptr(k8), _ptr(v), B * H, Nq, Nk, d, dv, float(scale),
+                                               float(q_descale), float(k_descale), _ptr(rows), rows.size,
+                                               _ptr(o), _ptr(lse), int(nthreads))
+        if rc != 0:
+            raise ValueError(f"attn_ref_rows_e4m3qk_f64 failed with status {rc}")
         return o, lse
 
     def attention(self, q, k, v, scale: float, nthreads: int = 0):
@@ -245,6 +283,15 @@ def attention_rows_causal(q, k, v, scale: float, rows=None, nthreads: int = 0):
 
 def attention_rows_bias(q, k, v, bias, scale: float, rows=None, nthreads: int = 0):
     return default().attention_rows_bias(q, k, v, bias, scale, rows, nthreads)
+
+
+def e4m3_to_f64(codes):
+    return default().e4m3_to_f64(codes)
+
+
+def attention_rows_e4m3qk(q8, k8, v, scale: float, q_descale: float = 1.0, k_descale: float = 1.0, rows=None,
+                          nthreads: int = 0):
+    return default().attention_rows_e4m3qk(q8, k8, v, scale, q_descale, k_descale, rows, nthreads)
 
 
 def attention(q, k, v, scale: float, nthreads: int = 0):

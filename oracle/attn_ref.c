@@ -481,3 +481,103 @@ int attn_ref_bwd_causal_f64(const double *q, const double *k, const double *v, c
 {
     return bwd_impl(q, k, v, dout, BH, Nq, Nk, d, dv, scale, dq, dk, dvv, nthreads, 1);
 }
+
+/*
+ * FP8 E4M3 scores.
+ *
+ * "Flash Attention на 5090 в CUDA C++" (section "Что дальше") names low-precision (FP8)
+ * MMA as the next step. Read plainly: Q and K arrive as 8-bit E4M3 codes with one
+ * descale factor per tensor, the real inputs being q_descale * Q8 and k_descale * K8,
+ * and the definition above is applied to them unchanged:
+ *   s_j = scale * sum_c (q_descale * q8[i,c]) * (k_descale * k8[j,c]),
+ * then steps 2-5 with V in BF16.
+ *
+ * E4M3 as the OCP 8-bit floating point format defines it: bit 7 the sign, bits 6-3 the
+ * exponent e with bias 7, bits 2-0 the mantissa m; no infinities.
+ *   e = 0:              (-1)^s * (m / 8) * 2^(1 - 7)   (subnormals; m = 0 is a signed zero)
+ *   e = 15 and m = 7:   NaN
+ *   otherwise:          (-1)^s * (1 + m / 8) * 2^(e - 7)
+ */
+static double e4m3_to_f64(uint8_t code)
+{
+    int sign = code >> 7, e = (code >> 3) & 15, m = code & 7;
+    double mag;
+    if (e == 15 && m == 7) return NAN;
+    if (e == 0)
+        mag = ldexp((double)m / 8.0, 1 - 7);
+    else
+        mag = ldexp(1.0 + (double)m / 8.0, e - 7);
+    return sign ? -mag : mag;
+}
+
+/* attn_ref_e4m3_to_f64: decode n codes (for the pins). */
+void attn_ref_e4m3_to_f64(const uint8_t *codes, int64_t n, double *out)
+{
+    for (int64_t i = 0; i < n; i++) out[i] = e4m3_to_f64(codes[i]);
+}
+
+/*
+ * attn_ref_rows_e4m3qk_f64: O and LSE of selected rows with Q and K given as E4M3 codes.
+ *
+ *   q8 [BH, Nq, d], k8 [BH, Nk, d]   E4M3 codes, C order
+ *   v  [BH, Nk, dv]                  BF16 bit patterns
+ *   q_descale, k_descale             the per-tensor factors of the real inputs
+ * Other arguments and the return value as attn_ref_rows_f64.
+ */
+int attn_ref_rows_e4m3qk_f64(const uint8_t *q8, const uint8_t *k8, const uint16_t *v,
+                             int64_t BH, int64_t Nq, int64_t Nk, int64_t d, int64_t dv,
+                             double scale, double q_descale, double k_descale,
+                             const int64_t *sel, int64_t nsel, double *o, double *lse, int nthreads)
+{
+    if (BH < 0 || Nq < 0 || Nk < 1 || d < 1 || dv < 1 || nsel < 0) return REF_EINVAL;
+    if (nsel == 0) return REF_OK;
+    if (!q8 || !k8 || !v || !sel || !o || !lse) return REF_EINVAL;
+    for (int64_t r = 0; r < nsel; r++)
+        if (sel[r] < 0 || sel[r] >= BH * Nq) return REF_EINVAL;
+
+    int failed = 0;
+#ifdef _OPENMP
+    int nt = nthreads > 0 ? nthreads : omp_get_max_threads();
+#pragma omp parallel num_threads(nt)
+#else
+    (void)nthreads;
+#endif
+    {
+        double *s = (double *)malloc((size_t)Nk * sizeof(double));
+        if (!s) {
+#ifdef _OPENMP
+#pragma omp atomic write
+#endif
+            failed = 1;
+        } else {
+#ifdef _OPENMP
+#pragma omp for schedule(dynamic, 1)
+#endif
+            for (int64_t r = 0; r < nsel; r++) {
+                int64_t bh = sel[r] / Nq, i = sel[r] % Nq;
+                const uint8_t *qi = q8 + (bh * Nq + i) * d, *kh = k8 + bh * Nk * d;
+                /* step 1 on the real inputs q_descale * Q8 and k_descale * K8 */
+                for (int64_t j = 0; j < Nk; j++) {
+                    double acc = 0.0;
+                    for (int64_t c = 0; c < d; c++)
+                        acc += (q_descale * e4m3_to_f64(qi[c])) * (k_descale * e4m3_to_f64(kh[j * d + c]));
+                    s[j] = scale * acc;
+                }
+                /* steps 2-5 with the head's BF16 value rows */
+                const uint16_t *vrows = v + bh * Nk * dv;
+                double *orow = o + r * dv;
+                double mx = row_max(s, Nk);
+                double den = row_exp_sum(s, Nk, mx);
+                for (int64_t c = 0; c < dv; c++) {
+                    double num = 0.0;
+                    for (int64_t j = 0; j < Nk; j++)
+                        num += s[j] * bf16_to_f64(vrows[j * dv + c]);
+                    orow[c] = num / den;
+                }
+                lse[r] = mx + log(den);
+            }
+            free(s);
+        }
+    }
+    return failed ? REF_ENOMEM : REF_OK;
+}

@@ -496,6 +496,57 @@ def pin_causal_bwd_keys_see_only_later_rows(orc):
     assert np.min(np.abs(dv[0, 0, :3]).max(axis=-1)) > 1e-3
 
 
+# ---- FP8 E4M3 scores ------------------------------------------------------------------------
+# Q and K as E4M3 codes (the OCP 8-bit floating point format) with per-tensor descale factors.
+
+def pin_e4m3_decoder_closed_forms_and_torch(orc):
+    codes = np.arange(256, dtype=np.uint8)
+    got = orc.e4m3_to_f64(codes)
+    # values fixed by the format: bias 7, three mantissa bits, subnormals below 2^-6
+    fixed = {0x38: 1.0, 0x40: 2.0, 0x30: 0.5, 0x3C: 1.5, 0x7E: 448.0, 0x77: 240.0, 0x08: 2.0 ** -6,
+             0x0F: 1.875 * 2.0 ** -6, 0x01: 2.0 ** -9, 0x07: 7 * 2.0 ** -9, 0x04: 2.0 ** -7, 0xB8: -1.0,
+             0xFE: -448.0, 0x00: 0.0}
+    for c, val in fixed.items():
+        assert got[c] == val, f"code {c:#04x}: {got[c]} != {val}"
+    assert math.copysign(1.0, got[0x80]) == -1.0 and got[0x80] == 0.0
+    assert np.isnan(got[0x7F]) and np.isnan(got[0xFF]) and np.count_nonzero(np.isnan(got)) == 2
+    assert np.all(np.diff(got[:127]) > 0), "positive codes must increase with their value"
+    assert np.array_equal(got[128:255], -got[:127])
+    torch = pytest.importorskip("torch")
+    ref = torch.from_numpy(codes).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    fin = ~np.isnan(ref)
+    assert np.array_equal(np.isnan(got), ~fin) and np.array_equal(got[fin], ref[fin])
+
+
+def pin_e4m3_scores_equal_the_bf16_oracle_on_the_same_values(orc):
+    # every E4M3 value is a BF16 value, so codes widened to BF16 bits give the pinned BF16
+    # oracle the same real inputs once the descale factors move into its scale
+    from dense_attention_forward_fwd_gb300.inputs import make_qk_e4m3
+    q8, k8, v, dq, dk = make_qk_e4m3(1, 2, 9, 37, d=16, seed=70, qk_mult=2.0)
+    qb, kb = bf16(orc.e4m3_to_f64(q8)), bf16(orc.e4m3_to_f64(k8))
+    o8, l8 = orc.attention_rows_e4m3qk(q8, k8, v, 0.3, dq, dk)
+    ob, lb = orc.attention_rows(qb, kb, v, 0.3 * dq * dk)
+    assert np.max(np.abs(o8 - ob)) < 1e-12 and np.max(np.abs(l8 - lb)) < 1e-12 * np.max(np.abs(lb))
+    # the descale factors act only through their product
+    o2, l2 = orc.attention_rows_e4m3qk(q8, k8, v, 0.3, dq * 4.0, dk / 4.0)
+    assert np.max(np.abs(o2 - o8)) < 1e-12 and np.max(np.abs(l2 - l8)) < 1e-12 * np.max(np.abs(l8))
+
+
+def pin_e4m3_two_keys_logistic_closed_form(orc):
+    # one query row over two keys: P_0 = 1 / (1 + exp(s_1 - s_0)), with s_j written out by hand
+    q8 = np.zeros((1, 1, 1, 4), np.uint8)
+    k8 = np.zeros((1, 1, 2, 4), np.uint8)
+    q8[..., 0], q8[..., 1] = 0x38, 0x40                 # q = (1, 2, 0, 0)
+    k8[0, 0, 0, 0], k8[0, 0, 1, 1] = 0x3C, 0xB0          # k_0 = (1.5, 0, ..), k_1 = (0, -0.5, ..)
+    v = bf16(np.array([[[[1.0, 0.0], [0.0, 1.0]]]]))
+    scale, dq, dk = 0.75, 0.5, 3.0
+    s0, s1 = scale * dq * dk * 1.5, scale * dq * dk * (2 * -0.5)
+    p0 = 1.0 / (1.0 + math.exp(s1 - s0))
+    o, lse = orc.attention_rows_e4m3qk(q8, k8, v, scale, dq, dk)
+    assert abs(o[0, 0] - p0) < 1e-15 and abs(o[0, 1] - (1 - p0)) < 1e-15
+    assert abs(lse[0] - math.log(math.exp(s0) + math.exp(s1))) < 1e-14
+
+
 PINS = [v for k_, v in sorted(globals().items()) if k_.startswith("pin_")]
 
 

@@ -39,6 +39,14 @@ MUTANTS = {
     "bwd probabilities not normalised": ("for (int64_t j = 0; j < nvis; j++) p[j] /= l;", ""),
     "dense forward without 1/l": ("oi[c] = acc / l;", "oi[c] = acc;"),
     "causal bwd mask half offset": ("nvis = causal ? i + (Nk - Nq) + 1", "nvis = causal ? i + (Nk - Nq) / 2 + 1"),
+    "e4m3 exponent bias 8": ("mag = ldexp(1.0 + (double)m / 8.0, e - 7);", "mag = ldexp(1.0 + (double)m / 8.0, e - 8);"),
+    "e4m3 subnormals one binade low": ("ldexp((double)m / 8.0, 1 - 7)", "ldexp((double)m / 8.0, -7)"),
+    "e4m3 sign dropped": ("return sign ? -mag : mag;", "return mag;"),
+    "e4m3 mantissa without the implicit one": ("ldexp(1.0 + (double)m / 8.0, e - 7)", "ldexp((double)m / 8.0, e - 7)"),
+    "e4m3 key descale dropped": ("(k_descale * e4m3_to_f64(kh[j * d + c]))", "(e4m3_to_f64(kh[j * d + c]))"),
+    "e4m3 query descale squared": ("(q_descale * e4m3_to_f64(qi[c]))", "(q_descale * q_descale * e4m3_to_f64(qi[c]))"),
+    "e4m3 values from the keys": ("num += s[j] * bf16_to_f64(vrows[j * dv + c]);",
+                                  "num += s[j] * (double)kh[j * d + c];"),
     "causal dense forward one key short": ("const int64_t nv = causal ? i + (Nk - Nq) + 1 : Nk;",
                                            "const int64_t nv = causal ? i + (Nk - Nq) + (i > 0) : Nk;"),
 }
