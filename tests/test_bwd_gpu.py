@@ -155,3 +155,31 @@ def test_causal_bwd_rejects_more_queries_than_keys(gpu_lib):
     with pytest.raises(gpu_lib.AttnError) as e:
         gpu_lib.attn_bwd_causal(a, a, a, a, a, b, a, a, a, 1, 1, 256, 128, 128, SCALE)
     assert e.value.status == gpu_lib.ATTN_ERR_INVALID_ARG
+
+
+# ---- the measured workloads at full size: one launch over every head, sampled heads checked ---------
+
+@pytest.mark.parametrize("name,causal,heads", [
+    ("rect-4k-8k", False, ((0, 7),)),              # one head: about 20 s of FP64 oracle on 8 cores
+    ("square-4k", False, ((0, 0), (3, 15))),
+    ("square-4k", True, ((0, 0), (3, 15))),
+])
+def test_bwd_workload_sampled_heads(gpu_lib, name, causal, heads):
+    """attn_bwd (or attn_bwd_causal) over all B*H heads of a measured workload, as the backward
+    bench launches it; the sampled heads (the last one always) are compared with the exact FP64
+    gradient on every row of dQ and every key of dK and dV."""
+    from dense_attention_forward_fwd_gb300.configs import by_name
+    w = by_name(name)
+    q, k, v = make_qkv(w.B, w.H, w.Nq, w.Nk, seed=w.seed, qk_mult=w.qk_mult)
+    do = make_dout(w.B, w.H, w.Nq, w.seed + 1)
+    got = run_fwd_bwd(gpu_lib, q, k, v, do, w.scale, causal=causal)
+    assert (w.B - 1, w.H - 1) in heads
+    for b, h in heads:
+        sl = (slice(b, b + 1), slice(h, h + 1))
+        ref = oracle.attention_bwd(q[sl], k[sl], v[sl], do[sl], w.scale, causal=causal)
+        for gname, g, r in zip(("dq", "dk", "dv"), got, ref):
+            g = g[sl]
+            assert np.all(np.isfinite(g)), f"{gname} head ({b},{h}): non-finite output"
+            err = np.abs(g.astype(np.float64) - r)
+            assert err.max() <= MAX_REL * np.abs(r).max(), f"{gname} head ({b},{h}): max err {err.max():.3e}"
+            assert err.mean() <= MEAN_REL * np.abs(r).mean(), f"{gname} head ({b},{h}): mean err {err.mean():.3e}"

@@ -248,12 +248,13 @@ def test_bias_of_zeros_matches_the_plain_entry_point(gpu_lib):
     assert np.max(np.abs(ob - o0)) <= 1e-2 and np.max(np.abs(lb - l0)) <= 1e-5 * np.max(np.abs(l0))
 
 
-@pytest.mark.parametrize("name", ["rect-4k-8k"])
-def test_bias_workload_sampled_rows(gpu_lib, name):
-    # the default benchmark shape with one [Nq, Nk] bias shared by every head
+@pytest.mark.parametrize("name,kind", [("rect-4k-8k", "shared"), ("rect-4k-8k", "full")])
+def test_bias_workload_sampled_rows(gpu_lib, name, kind):
+    # the default benchmark shape with one [Nq, Nk] bias shared by every head, or one bias per
+    # (batch, head) (537 MB of BF16 for this shape), as `bench.py --bias` times them
     w = by_name(name)
     rows = sample_rows(w.B, w.H, w.Nq, per_head=16)
-    bias = make_bias((1, 1, w.Nq, w.Nk), seed=88, std=1.0)
+    bias = make_bias(_bias_shape(kind, w.B, w.H, w.Nq, w.Nk), seed=88, std=1.0)
     check_case(gpu_lib, w.B, w.H, w.Nq, w.Nk, seed=w.seed, scale=w.scale, rows=rows, bias=bias)
 
 
