@@ -24,6 +24,11 @@ score).
 O and LSE) and counts 2.5x the forward's FLOPs (the five products of the method's
 backward); with --impl reference it times the FP64 backward oracle.
 
+--fp8-qk times attn_fwd_fp8qk: Q and K quantized per tensor to FP8 E4M3 codes (descale =
+amax / 448), V in BF16; the FLOP count is unchanged and the roofline peak is that of a
+contraction done half at the FP8 rate (twice the measured BF16 rate, the nominal ratio) and
+half at the BF16 rate.
+
 --impl reference times the FP64 CPU oracle (the plain definition) on host cores, on a
 bounded sample of query rows per step.
 """
@@ -71,7 +76,14 @@ def parse():
                     help="additive BF16 bias N(0,1): one [Nq, Nk] matrix for all heads, or one per head")
     ap.add_argument("--backward", action="store_true",
                     help="time attn_bwd (dQ, dK, dV for an N(0,1) upstream gradient); FLOPs = 2.5x the forward's")
-    return ap.parse_args()
+    ap.add_argument("--fp8-qk", action="store_true",
+                    help="time attn_fwd_fp8qk (Q and K as FP8 E4M3 codes with per-tensor descale factors)")
+    args = ap.parse_args()
+    if args.fp8_qk and (args.causal or args.backward or args.bias != "none"):
+        ap.error("--fp8-qk has no causal, bias or backward entry point; use it alone")
+    if args.bias != "none" and (args.causal or args.backward):
+        ap.error("--bias has no causal or backward entry point; use it alone")
+    return args
 
 
 def dist_env():
@@ -82,7 +94,9 @@ def run_config(w, args) -> dict:
     """The workload description both arms print (the reference arm times the same one)."""
     return {"workload": w.name, "B": w.B, "H": w.H, "Nq": w.Nq, "Nk": w.Nk, "d": w.d, "causal": args.causal,
             "bias": args.bias, "pass": "backward" if args.backward else "forward", "qk_mult": w.qk_mult,
-            "inputs": "iid N(0,1) BF16 (Q,K x qk_mult)",
+            "qk": "e4m3" if args.fp8_qk else "bf16",
+            "inputs": ("iid N(0,1) (Q,K x qk_mult); Q, K quantized per tensor to E4M3 (descale = amax/448), V BF16"
+                       if args.fp8_qk else "iid N(0,1) BF16 (Q,K x qk_mult)"),
             "l2": "flushed (512 MiB write) before every timed launch",
             "vs_baseline_ref": "RTX 5090 v5 kernel, same shape (other hardware: context only)"}
 
@@ -191,8 +205,12 @@ def workload_flops(w, causal: bool) -> float:
 
 # ------------------------------------------------------------------ reference arm (oracle) ---
 
-def oracle_rows_fn(oracle, w, causal: bool, bias_kind: str, H1: int, nq: int):
+def oracle_rows_fn(oracle, w, causal: bool, bias_kind: str, H1: int, nq: int, fp8_qk: bool = False):
     """The oracle entry point for this run's variant, as fn(q, k, v, scale, rows)."""
+    if fp8_qk:   # Q and K of the same draw (seed, shape) as E4M3 codes; V is make_qkv's V
+        from dense_attention_forward_fwd_gb300.inputs import make_qk_e4m3
+        q8, k8, _, dq, dk = make_qk_e4m3(1, H1, nq, w.Nk, d=w.d, seed=w.seed, qk_mult=w.qk_mult)
+        return lambda q, k, v, scale, rows: oracle.attention_rows_e4m3qk(q8, k8, v, scale, dq, dk, rows)
     if bias_kind != "none":
         from dense_attention_forward_fwd_gb300.inputs import make_bias
         bias = make_bias((1, 1, nq, w.Nk) if bias_kind == "shared" else (1, H1, nq, w.Nk), seed=w.seed + 1)
@@ -224,7 +242,8 @@ def cpu_oracle_backward_sample(w, target_seconds: float, causal: bool = False):
     return 2.5 * 4.0 * pairs * w.d / dt / 1e12, nq, dt, oracle.max_threads()
 
 
-def cpu_oracle_sample(w, target_seconds: float, rank_seed: int = 0, causal: bool = False, bias_kind: str = "none"):
+def cpu_oracle_sample(w, target_seconds: float, rank_seed: int = 0, causal: bool = False, bias_kind: str = "none",
+                      fp8_qk: bool = False):
     """Time the FP64 oracle on a sample of query rows; returns (TFLOPS, rows, seconds, threads)."""
     import numpy as np
 
@@ -237,7 +256,7 @@ def cpu_oracle_sample(w, target_seconds: float, rank_seed: int = 0, causal: bool
     nq = min(w.Nq, 4096)
     q, k, v = make_qkv(1, H1, nq, w.Nk, d=w.d, seed=w.seed + rank_seed, qk_mult=w.qk_mult)
     threads = oracle.max_threads()
-    fn = oracle_rows_fn(oracle, w, causal, bias_kind, H1, nq)
+    fn = oracle_rows_fn(oracle, w, causal, bias_kind, H1, nq, fp8_qk)
 
     def flop_rows(rows):   # 4*d FLOPs per visible key of each sampled row
         if not causal:
@@ -297,7 +316,7 @@ def run_reference(args, w):
     q, k, v = make_qkv(1, H1, nq, w.Nk, d=w.d, seed=w.seed, qk_mult=w.qk_mult)
     threads = oracle.max_threads()
     n_rows_total = q.shape[1] * q.shape[2]
-    fn = oracle_rows_fn(oracle, w, args.causal, args.bias, H1, nq)
+    fn = oracle_rows_fn(oracle, w, args.causal, args.bias, H1, nq, args.fp8_qk)
 
     def flop_rows(rows):   # 4*d FLOPs per visible key; causal sample rows sit at the end of the sequence
         if not args.causal:
@@ -368,9 +387,15 @@ def run_ours(args, w):
     flush = torch.empty(L2_FLUSH_BYTES // 4, device=dev, dtype=torch.int32)
     stream = torch.cuda.current_stream(dev)
 
-    if args.bias != "none" and (args.causal or args.backward):
-        raise SystemExit("--bias has no causal or backward entry point; use it alone")
     ins = [q, k, v]
+    descale = (1.0, 1.0)
+    if args.fp8_qk:   # per-tensor quantization of Q and K to E4M3 codes
+        qk8, descale = [], []
+        for x in (q, k):
+            ds = float(torch.tensor(x.float().abs().max().item() / 448.0, dtype=torch.float32))
+            qk8.append((x.float() / ds).to(torch.float8_e4m3fn))
+            descale.append(ds)
+        ins = [qk8[0], qk8[1], v]
     outs = [o, lse]
     if args.bias != "none":
         bshape = (1, 1, w.Nq, w.Nk) if args.bias == "shared" else (w.B, w.H, w.Nq, w.Nk)
@@ -389,6 +414,8 @@ def run_ours(args, w):
             attn.attn_fwd_bias(ins_[0], ins_[1], ins_[2], ins_[3], *outs_, w.B, w.H, w.Nq, w.Nk, w.d, w.scale, st)
         elif args.causal:
             attn.attn_fwd_causal(*ins_, *outs_, w.B, w.H, w.Nq, w.Nk, w.d, w.scale, st)
+        elif args.fp8_qk:
+            attn.attn_fwd_fp8qk(*ins_, *outs_, w.B, w.H, w.Nq, w.Nk, w.d, w.scale, descale[0], descale[1], st)
         else:
             attn.attn_fwd(*ins_, *outs_, w.B, w.H, w.Nq, w.Nk, w.d, w.scale, st)
 
@@ -496,11 +523,16 @@ def run_ours(args, w):
 
     peaks, peak_src = measured_peaks()
     peak = float(peaks["bf16_tflops"])
+    peak_note = f"{peak_src} bf16_tflops (burst: each launch is timed alone)"
+    if args.fp8_qk:   # Q K^T (half the FLOPs) at the FP8 rate, 2x BF16 nominally; P V at the BF16 rate
+        peak = 2.0 / (1.0 / (2.0 * peak) + 1.0 / peak)
+        peak_note = (f"half the FLOPs at 2 x {peak_src} bf16_tflops (FP8 E4M3, nominal ratio 4.5/2.25), "
+                     "half at bf16_tflops (burst)")
     achieved = flops / (ms * 1e-3) / 1e12   # one launch on one GPU
     traffic = None
     if os.path.exists(TRAFFIC_FILE):
         key = (w.name + ("-causal" if args.causal else "") + ("" if args.bias == "none" else "-bias-" + args.bias)
-               + ("-backward" if args.backward else ""))
+               + ("-backward" if args.backward else "") + ("-fp8qk" if args.fp8_qk else ""))
         rec = json.load(open(TRAFFIC_FILE)).get(key)
         if rec and rec.get("kernel_hash") == kernel_hash(args.backward):
             traffic = rec.get("bytes_per_launch")
@@ -510,12 +542,11 @@ def run_ours(args, w):
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": ((value / PAGES_TFLOPS[w.name])
                         if w.name in PAGES_TFLOPS and not args.causal and args.bias == "none" and not args.backward
-                        else None),
-        "dtype": "bf16", "data": "synthetic",
+                        and not args.fp8_qk else None),
+        "dtype": "e4m3+bf16" if args.fp8_qk else "bf16", "data": "synthetic",
         "config": run_config(w, args),
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                     "frac": achieved / peak, "traffic": traffic,
-                     "peak_source": f"{peak_src} bf16_tflops (burst: each launch is timed alone)"},
+                     "frac": achieved / peak, "traffic": traffic, "peak_source": peak_note},
         "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": launches,
         "clocks": clocks,
@@ -526,7 +557,8 @@ def run_ours(args, w):
             tfl, n, dt, thr = cpu_oracle_backward_sample(w, args.cpu_seconds, args.causal)
             sample = f"backward of one head with {n} query rows x {w.Nk} keys of {w.describe()}, FP64, {dt:.1f} s"
         else:
-            tfl, n, dt, thr = cpu_oracle_sample(w, args.cpu_seconds, causal=args.causal, bias_kind=args.bias)
+            tfl, n, dt, thr = cpu_oracle_sample(w, args.cpu_seconds, causal=args.causal, bias_kind=args.bias,
+                                                fp8_qk=args.fp8_qk)
             keys = "visible keys of each row, causal" if args.causal else "full Nk each"
             sample = f"{n} query rows of {w.describe()} ({keys}), FP64, {dt:.1f} s"
         line["cpu_baseline"] = {"value": tfl, "unit": "TFLOP/s", "cores": thr, "kind": "oracle", "sample": sample}

@@ -15,7 +15,7 @@ from ._build import LIB_PATH, build_library
 
 __all__ = [
     "ATTN_OK", "ATTN_ERR_INVALID_ARG", "ATTN_ERR_UNSUPPORTED", "ATTN_ERR_MISALIGNED", "ATTN_ERR_CUDA",
-    "ATTN_ERR_TIMEOUT", "AttnError", "load_library", "attn_fwd", "attn_fwd_causal", "attn_fwd_bias", "attn_fwd_noalloc", "attn_fwd_status", "attn_status_string",
+    "ATTN_ERR_TIMEOUT", "AttnError", "load_library", "attn_fwd", "attn_fwd_causal", "attn_fwd_bias", "attn_fwd_fp8qk", "attn_fwd_noalloc", "attn_fwd_status", "attn_status_string",
     "attn_fwd_set_wait_limit", "attn_fwd_kernel_count", "attention", "attn_bwd", "attn_bwd_causal", "attn_bwd_status",
     "attn_bwd_kernel_count", "attn_bwd_set_wait_limit",
 ]
@@ -49,6 +49,8 @@ def load_library(build_if_stale: bool = True) -> ctypes.CDLL:
             lib.attn_fwd.restype = i32
             lib.attn_fwd_noalloc.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, f32, vp]
             lib.attn_fwd_causal.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, f32, vp]
+            lib.attn_fwd_fp8qk.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, f32, f32, f32, vp]
+            lib.attn_fwd_fp8qk.restype = i32
             i64 = ctypes.c_longlong
             lib.attn_fwd_bias.argtypes = [vp, vp, vp, vp, i64, i64, i64, vp, vp, i32, i32, i32, i32, i32, f32, vp]
             lib.attn_fwd_noalloc.restype = i32
@@ -86,11 +88,12 @@ def _ptr(x, name: str, numel: int | None, dtype_name: str):
         return x
     if _is_tensor(x):
         import torch
-        want = {"bf16": torch.bfloat16, "f32": torch.float32}[dtype_name]
+        want = {"bf16": (torch.bfloat16,), "f32": (torch.float32,),
+                "e4m3": (torch.float8_e4m3fn, torch.uint8)}[dtype_name]   # E4M3 codes, or their bytes
         if not x.is_cuda:
             raise ValueError(f"{name} must be a CUDA tensor")
-        if x.dtype != want:
-            raise TypeError(f"{name} must be {want}, got {x.dtype}")
+        if x.dtype not in want:
+            raise TypeError(f"{name} must be {' or '.join(map(str, want))}, got {x.dtype}")
         if not x.is_contiguous():
             raise ValueError(f"{name} must be contiguous")
         if numel is not None and x.numel() != numel:
@@ -143,6 +146,23 @@ def attn_fwd_causal(q, k, v, o, lse, B: int, H: int, Nq: int, Nk: int, d: int, s
                              _stream_handle(stream, q, k, v, o, lse))
     if rc != ATTN_OK:
         raise AttnError(rc, "attn_fwd_causal")
+
+
+def attn_fwd_fp8qk(q8, k8, v, o, lse, B: int, H: int, Nq: int, Nk: int, d: int, scale: float,
+                   q_descale: float = 1.0, k_descale: float = 1.0, stream=None) -> None:
+    """Like :func:`attn_fwd`, with Q and K given as FP8 E4M3 codes (torch.float8_e4m3fn or
+    uint8 CUDA tensors [B,H,N,d]) and one positive descale factor each:
+    S = scale * q_descale * k_descale * (Q8 K8^T); V, O and LSE as in attn_fwd."""
+    lib = load_library()
+    args = (
+        _ptr(q8, "q8", B * H * Nq * d, "e4m3"), _ptr(k8, "k8", B * H * Nk * d, "e4m3"),
+        _ptr(v, "v", B * H * Nk * d, "bf16"), _ptr(o, "o", B * H * Nq * d, "bf16"),
+        _ptr(lse, "lse", B * H * Nq, "f32"),
+    )
+    rc = lib.attn_fwd_fp8qk(*args, int(B), int(H), int(Nq), int(Nk), int(d), float(scale), float(q_descale),
+                            float(k_descale), _stream_handle(stream, q8, k8, v, o, lse))
+    if rc != ATTN_OK:
+        raise AttnError(rc, "attn_fwd_fp8qk")
 
 
 def attn_fwd_bias(q, k, v, bias, o, lse, B: int, H: int, Nq: int, Nk: int, d: int, scale: float, stream=None,

@@ -1,5 +1,7 @@
 // attn_fwd.cu -- dense BF16 attention forward for GB300 (sm_103a): non-causal, causal
-// (attn_fwd_causal) and with an additive bias (attn_fwd_bias, a third instantiation).
+// (attn_fwd_causal), with an additive bias (attn_fwd_bias, its own instantiation) and with
+// Q and K as FP8 E4M3 codes (attn_fwd_fp8qk: the producer loads one 128-byte box per Q or
+// K tile and S = Q K^T is issued as kind::f8f6f4 MMAs; everything from S on is shared).
 //
 // O = softmax(scale * Q K^T) V and the per-row log-sum-exp, head_dim 128, computed
 // FlashAttention-style: Q tiles of 128 query rows are loaded once and 128-key K/V
@@ -61,6 +63,7 @@
 #include <cudaTypedefs.h>
 
 #include <atomic>
+#include <cfloat>
 #include <climits>
 #include <cmath>
 #include <cstdint>
@@ -83,6 +86,7 @@ constexpr int kSlots = 4;                      // K/V ring depth, one 128x128 ti
 constexpr int kPairs = kSlots / 2;             // the ring hands over units of two slots
 constexpr int kTileBytes = kBM * kD * 2;       // 32 KB of BF16
 constexpr int kBoxBytes = kTileBytes / 2;      // one TMA box: 64 columns (128 B) x 128 rows
+constexpr int kTile8Bytes = kBM * kD;          // 16 KB of FP8 codes: one box of 128 columns (128 B)
 constexpr int kThreads = 384;
 // Register split between the warpgroups. setmaxnreg.inc draws only on registers that
 // the block holds: 128 * kRegsCtl + 256 * kRegsSoftmax must equal 384 * kRegsLaunch,
@@ -333,6 +337,15 @@ __device__ __forceinline__ void mma_ss(uint32_t d, uint64_t a, uint64_t b, uint3
       "l"(a), "l"(b), "r"(idesc), "r"(static_cast<uint32_t>(acc))
       : "memory");
 }
+// D(tmem) (+)= A(smem desc) * B(smem desc), 8-bit floating-point operands
+__device__ __forceinline__ void mma_ss_f8(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, bool acc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
+      "l"(a), "l"(b), "r"(idesc), "r"(static_cast<uint32_t>(acc))
+      : "memory");
+}
 // D(tmem) (+)= A(tmem) * B(smem desc)
 __device__ __forceinline__ void mma_ts(uint32_t d, uint32_t a, uint64_t b, uint32_t idesc, bool acc) {
   asm volatile(
@@ -565,6 +578,11 @@ __host__ __device__ constexpr uint32_t idesc_bf16(bool b_mn_major) {
   return (1u << 4) | (1u << 7) | (1u << 10) | ((b_mn_major ? 1u : 0u) << 16) |
          (static_cast<uint32_t>(kBN >> 3) << 17) | (static_cast<uint32_t>(kBM >> 4) << 24);
 }
+// kind::f8f6f4: E4M3 x E4M3 -> FP32 (format code 0 for A and B), M = 128, N = 128, both
+// K-major (S = Q K^T from FP8 codes).
+__host__ __device__ constexpr uint32_t idesc_e4m3() {
+  return (1u << 4) | (static_cast<uint32_t>(kBN >> 3) << 17) | (static_cast<uint32_t>(kBM >> 4) << 24);
+}
 
 // ---------------------------------------------------------------------------------
 // Bounded waits
@@ -601,6 +619,8 @@ __device__ __forceinline__ bool wait_warp(const Ctl& c, int idx, uint32_t parity
 // ---------------------------------------------------------------------------------
 // Roles
 // ---------------------------------------------------------------------------------
+// kQK8: Q and K are FP8 codes, one 128-byte box per tile in the first half of its slot.
+template <bool kQK8>
 __device__ void run_producer(const Ctl& c, uint32_t base, const CUtensorMap* tmQ,
                              const CUtensorMap* tmK, const CUtensorMap* tmV, const Params& p) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tmQ)) : "memory");
@@ -621,9 +641,9 @@ __device__ void run_producer(const Ctl& c, uint32_t base, const CUtensorMap* tmQ
     const int q_row0 = (sg.group % p.q_groups) * (kQTiles * kBM);
     // the previous segment's S MMAs must be done with the Q tiles
     if (u > 0 && !wait_phase(c, kBarQEmpty, (u - 1) & 1, true)) break;
-    mbar_arrive_expect_tx(c.bar(kBarQFull), kQTiles * kTileBytes);
+    mbar_arrive_expect_tx(c.bar(kBarQFull), kQTiles * (kQK8 ? kTile8Bytes : kTileBytes));
     for (int i = 0; i < kQTiles; ++i)
-      for (int h = 0; h < 2; ++h)
+      for (int h = 0; h < (kQK8 ? 1 : 2); ++h)
         tma_load_3d(base + kOffQ + i * kTileBytes + h * kBoxBytes, tmQ, c.bar(kBarQFull), h * 64,
                     q_row0 + i * kBM, bh);
     ++u;
@@ -642,7 +662,7 @@ __device__ void run_producer(const Ctl& c, uint32_t base, const CUtensorMap* tmQ
       if (p.withhold_tile && unit == 1) continue;
       const bool has_v = i > 0, has_k = i < n;
       const uint32_t fb = c.bar(kBarKVFull + pr);
-      mbar_arrive_expect_tx(fb, (has_v && has_k ? 2 : 1) * kTileBytes);
+      mbar_arrive_expect_tx(fb, (has_v ? kTileBytes : 0) + (has_k ? (kQK8 ? kTile8Bytes : kTileBytes) : 0));
       uint32_t dst = base + kOffKV + 2 * pr * kTileBytes;
       if (has_v) {
         for (int h = 0; h < 2; ++h)
@@ -650,7 +670,8 @@ __device__ void run_producer(const Ctl& c, uint32_t base, const CUtensorMap* tmQ
         dst += kTileBytes;
       }
       if (has_k) {
-        for (int h = 0; h < 2; ++h) tma_load_3d(dst + h * kBoxBytes, tmK, fb, h * 64, (sg.kv0 + i) * kBN, bh);
+        for (int h = 0; h < (kQK8 ? 1 : 2); ++h)
+          tma_load_3d(dst + h * kBoxBytes, tmK, fb, h * 64, (sg.kv0 + i) * kBN, bh);
       }
       last_unit[pr] = unit;
     }
@@ -662,7 +683,20 @@ __device__ void run_producer(const Ctl& c, uint32_t base, const CUtensorMap* tmQ
     if (last_unit[q] >= 0) wait_phase(c, kBarKVFull + q, (last_unit[q] / kPairs) & 1, false);
 }
 
+template <bool kQK8>
 __device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint32_t q_smem, uint32_t k_smem) {
+  if constexpr (kQK8) {
+    // FP8 codes: the whole head dimension is one 128-byte row of the box; 32 columns
+    // (32 bytes) per MMA.
+    constexpr uint32_t idesc = idesc_e4m3();
+#pragma unroll
+    for (int kk = 0; kk < kD / 32; ++kk) {
+      const uint32_t off = static_cast<uint32_t>(kk * 32);
+      mma_ss_f8(d_tmem, sdesc_sw128(q_smem + off, 16, 1024), sdesc_sw128(k_smem + off, 16, 1024), idesc,
+                kk > 0);
+    }
+    return;
+  }
   constexpr uint32_t idesc = idesc_bf16(false);
 #pragma unroll
   for (int kk = 0; kk < kD / 16; ++kk) {
@@ -693,7 +727,7 @@ __device__ __forceinline__ void issue_pv_half(uint32_t d_tmem, uint32_t p_tmem, 
 // about a hundred cycles (its queue is shallow), so a step does only the four P waits
 // and two commits: softmax threads check and release the ring slots.
 // Returns false when a wait gave up.
-template <bool kMore>
+template <bool kMore, bool kQK8>
 __device__ __forceinline__ bool mma_step(const Ctl& c, uint32_t base, const uint32_t (&tS)[2],
                                          const uint32_t (&tO)[2], const uint32_t (&sQ)[2], int unit,
                                          uint32_t ph, bool first) {
@@ -709,7 +743,7 @@ __device__ __forceinline__ bool mma_step(const Ctl& c, uint32_t base, const uint
   tc_fence_after();
   issue_pv_half(tO[0], tS[0], sV, 1, true);
   if (kMore) {
-    issue_qk(tS[0], sQ[0], sK);
+    issue_qk<kQK8>(tS[0], sQ[0], sK);
     tc_commit(c.bar(kBarSFull + 0));
   } else {
     tc_commit(c.bar(kBarOFull + 0));
@@ -722,7 +756,7 @@ __device__ __forceinline__ bool mma_step(const Ctl& c, uint32_t base, const uint
   tc_fence_after();
   issue_pv_half(tO[1], tS[1], sV, 1, true);
   if (kMore) {
-    issue_qk(tS[1], sQ[1], sK);
+    issue_qk<kQK8>(tS[1], sQ[1], sK);
     tc_commit(c.bar(kBarSFull + 1));
   } else {
     tc_commit(c.bar(kBarOFull + 1));
@@ -730,6 +764,7 @@ __device__ __forceinline__ bool mma_step(const Ctl& c, uint32_t base, const uint
   return true;
 }
 
+template <bool kQK8>
 __device__ void run_mma(const Ctl& c, uint32_t base, uint32_t tmem, const Params& p) {
   const uint32_t tS[2] = {tmem, tmem + 128};
   const uint32_t tO[2] = {tmem + 256, tmem + 384};
@@ -746,9 +781,9 @@ __device__ void run_mma(const Ctl& c, uint32_t base, uint32_t tmem, const Params
       break;
     tc_fence_after();
     const uint32_t sK = base + kOffKV + 2 * (unit % kPairs) * kTileBytes;   // unit {K_0}
-    issue_qk(tS[0], sQ[0], sK);
+    issue_qk<kQK8>(tS[0], sQ[0], sK);
     tc_commit(c.bar(kBarSFull + 0));
-    issue_qk(tS[1], sQ[1], sK);
+    issue_qk<kQK8>(tS[1], sQ[1], sK);
     tc_commit(c.bar(kBarSFull + 1));
     if (n == 1) tc_commit(c.bar(kBarQEmpty));   // the segment's last S MMA is issued
     // The segment's first P V products overwrite O: the previous segment's epilogue must
@@ -759,14 +794,14 @@ __device__ void run_mma(const Ctl& c, uint32_t base, uint32_t tmem, const Params
     bool ok = true;
     int j = 0;
     for (; j + 1 < n; ++j) {
-      if (!mma_step<true>(c, base, tS, tO, sQ, unit + 1 + j, (gstep + j) & 1u, j == 0)) {
+      if (!mma_step<true, kQK8>(c, base, tS, tO, sQ, unit + 1 + j, (gstep + j) & 1u, j == 0)) {
         ok = false;
         break;
       }
     }
     if (!ok) break;
     if (n > 1) tc_commit(c.bar(kBarQEmpty));   // the last S MMA (step n-2) is issued
-    if (!mma_step<false>(c, base, tS, tO, sQ, unit + 1 + j, (gstep + j) & 1u, j == 0)) break;
+    if (!mma_step<false, kQK8>(c, base, tS, tO, sQ, unit + 1 + j, (gstep + j) & 1u, j == 0)) break;
     unit += n + 1;
     gstep += static_cast<uint32_t>(n);
     ++u;
@@ -1144,7 +1179,7 @@ __device__ void run_softmax(const Ctl& c, uint32_t tmem, uint8_t* stage, const P
 // ---------------------------------------------------------------------------------
 // Kernel
 // ---------------------------------------------------------------------------------
-template <bool kPosScale, bool kBias>
+template <bool kPosScale, bool kBias, bool kQK8 = false>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const Params p) {
@@ -1202,10 +1237,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp < 4) {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsCtl));
     if (warp == 0) {
-      if (lane == 0) run_producer(c, base, &tmQ, &tmK, &tmV, p);
+      if (lane == 0) run_producer<kQK8>(c, base, &tmQ, &tmK, &tmV, p);
       __syncwarp();
     } else if (warp == 1) {
-      if (lane == 0) run_mma(c, base, tmem, p);
+      if (lane == 0) run_mma<kQK8>(c, base, tmem, p);
       __syncwarp();
     }
   } else {
@@ -1245,21 +1280,25 @@ PFN_cuTensorMapEncodeTiled_v12000 encoder() {
   return g_encode;
 }
 
-// [BH, rows, 128] BF16 viewed as a 3-D tensor (d innermost); box = 64 columns x 128 rows x 1.
-bool make_map(CUtensorMap* map, const void* ptr, int rows, long long bh) {
+// [BH, rows, 128] viewed as a 3-D tensor (d innermost). BF16: box = 64 columns x 128 rows x 1;
+// 8-bit codes (codes8): box = 128 columns x 128 rows x 1. Either way one box row is 128 bytes,
+// the span of the 128-byte swizzle.
+bool make_map(CUtensorMap* map, const void* ptr, int rows, long long bh, bool codes8 = false) {
   auto enc = encoder();
   if (!enc) return false;
+  const cuuint64_t esize = codes8 ? 1 : 2;
   cuuint64_t dims[3] = {static_cast<cuuint64_t>(kD), static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(bh)};
-  cuuint64_t strides[2] = {static_cast<cuuint64_t>(kD) * 2, static_cast<cuuint64_t>(rows) * kD * 2};
-  cuuint32_t box[3] = {64, static_cast<cuuint32_t>(kBM), 1};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(kD) * esize, static_cast<cuuint64_t>(rows) * kD * esize};
+  cuuint32_t box[3] = {codes8 ? 128u : 64u, static_cast<cuuint32_t>(kBM), 1};
   cuuint32_t elem[3] = {1, 1, 1};
-  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, elem,
+  return enc(map, codes8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+             const_cast<void*>(ptr), dims, strides, box, elem,
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 constexpr int kMaxDevices = 64;
-std::atomic<int> g_attr_done[4][kMaxDevices];   // per instantiation (kPos + 2 * kBias)
+std::atomic<int> g_attr_done[8][kMaxDevices];   // per instantiation (kPos + 2 * kBias + 4 * kQK8)
 std::atomic<int> g_sm_count[kMaxDevices];
 
 int sm_count(int dev) {
@@ -1344,11 +1383,11 @@ int get_workspace(int dev, cudaStream_t stream, size_t part_bytes, size_t cnt_by
   return ATTN_OK;
 }
 
-template <bool kPos, bool kBias = false>
+template <bool kPos, bool kBias = false, bool kQK8 = false>
 int launch(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, const Params& p, int grid,
            int dev, cudaStream_t stream) {
-  auto kern = attn_fwd_kernel<kPos, kBias>;
-  constexpr int kInst = (kPos ? 1 : 0) + (kBias ? 2 : 0);
+  auto kern = attn_fwd_kernel<kPos, kBias, kQK8>;
+  constexpr int kInst = (kPos ? 1 : 0) + (kBias ? 2 : 0) + (kQK8 ? 4 : 0);
   if (dev < 0 || dev >= kMaxDevices || !g_attr_done[kInst][dev].load(std::memory_order_acquire)) {
     // The in-kernel register split (setmaxnreg) balances only at kRegsLaunch registers
     // per thread; at any other count the increase would never be granted. Refuse.
@@ -1373,9 +1412,10 @@ struct BiasArg {
   long long sb, sh, sq;
 };
 
-// attn_fwd and attn_fwd_bias (bias != nullptr): the argument rules, the plan, the launch.
+// attn_fwd, attn_fwd_bias (bias != nullptr) and attn_fwd_fp8qk (qk8: q and k hold FP8 E4M3
+// codes): the argument rules, the plan, the launch.
 int forward(const void* q, const void* k, const void* v, const BiasArg* bias, void* o, float* lse, int B, int H,
-            int Nq, int Nk, int d, float scale, void* stream) {
+            int Nq, int Nk, int d, float scale, void* stream, bool qk8 = false) {
   if (B < 0 || H < 0 || Nq < 0 || Nk < 0) return ATTN_ERR_INVALID_ARG;
   if (d != kD) return ATTN_ERR_UNSUPPORTED;
   if (!std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
@@ -1412,7 +1452,7 @@ int forward(const void* q, const void* k, const void* v, const BiasArg* bias, vo
   if (sms <= 0) return ATTN_ERR_CUDA;
 
   CUtensorMap mq, mk, mv;
-  if (!make_map(&mq, q, Nq, bh) || !make_map(&mk, k, Nk, bh) || !make_map(&mv, v, Nk, bh))
+  if (!make_map(&mq, q, Nq, bh, qk8) || !make_map(&mk, k, Nk, bh, qk8) || !make_map(&mv, v, Nk, bh))
     return ATTN_ERR_CUDA;
 
   Params p;
@@ -1453,6 +1493,9 @@ int forward(const void* q, const void* k, const void* v, const BiasArg* bias, vo
   }
   // with a bias the scale is applied before the row max, so one instantiation serves any sign
   if (bias != nullptr) return launch<true, true>(mq, mk, mv, p, pl.grid, dev, s);
+  if (qk8)
+    return scale > 0.0f ? launch<true, false, true>(mq, mk, mv, p, pl.grid, dev, s)
+                        : launch<false, false, true>(mq, mk, mv, p, pl.grid, dev, s);
   return scale > 0.0f ? launch<true>(mq, mk, mv, p, pl.grid, dev, s) : launch<false>(mq, mk, mv, p, pl.grid, dev, s);
 }
 
@@ -1468,6 +1511,19 @@ extern "C" int attn_fwd_bias(const void* q, const void* k, const void* v, const 
                              int Nq, int Nk, int d, float scale, void* stream) {
   const BiasArg ba = {bias, bias_stride_b, bias_stride_h, bias_stride_q};
   return forward(q, k, v, &ba, o, lse, B, H, Nq, Nk, d, scale, stream);
+}
+
+extern "C" int attn_fwd_fp8qk(const void* q8, const void* k8, const void* v, void* o, float* lse, int B, int H,
+                              int Nq, int Nk, int d, float scale, float q_descale, float k_descale,
+                              void* stream) {
+  // S = scale * q_descale * k_descale * (Q8 K8^T): the three factors are folded into one FP32
+  // scale on the host; the codes' products are exact in the FP32 accumulators.
+  if (!std::isfinite(scale) || !std::isfinite(q_descale) || !std::isfinite(k_descale) || !(q_descale > 0.0f) ||
+      !(k_descale > 0.0f))
+    return ATTN_ERR_INVALID_ARG;
+  const double eff = static_cast<double>(scale) * q_descale * k_descale;
+  if (!(std::fabs(eff) <= static_cast<double>(FLT_MAX))) return ATTN_ERR_INVALID_ARG;
+  return forward(q8, k8, v, nullptr, o, lse, B, H, Nq, Nk, d, static_cast<float>(eff), stream, true);
 }
 
 extern "C" int attn_fwd_causal(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,

@@ -127,6 +127,35 @@ int attn_fwd_bias(const void* q, const void* k, const void* v, const void* bias,
                   void* o, float* lse, int B, int H, int Nq, int Nk, int d, float scale, void* stream);
 
 /*
+ * attn_fwd_fp8qk -- attention forward with the scores computed from 8-bit floating point.
+ *
+ * The low-precision MMA that "Flash Attention на 5090 в CUDA C++" (section "Что дальше")
+ * lists as the next step, applied to S: Q and K arrive as FP8 E4M3 codes (the OCP 8-bit
+ * floating point format: 1 sign, 4 exponent bits with bias 7, 3 mantissa bits, no
+ * infinities, S.1111.111 = NaN, largest finite value 448) with one positive descale factor
+ * per tensor, so the real inputs are q_descale * Q8 and k_descale * K8, and
+ *
+ *     S = scale * q_descale * k_descale * (Q8 K8^T),   P = softmax_row(S),   O = P V
+ *
+ * with V, P and O in BF16 as in attn_fwd. The products of two E4M3 values are exact in
+ * the FP32 accumulators of the tensor cores (kind::f8f6f4); scale * q_descale * k_descale
+ * is rounded once to FP32 on the host.
+ *
+ *   q8     device, [B, H, Nq, d] bytes (E4M3 codes), read only
+ *   k8     device, [B, H, Nk, d] bytes (E4M3 codes), read only
+ *   v      device, BF16, [B, H, Nk, d], read only
+ *   q_descale, k_descale   finite and > 0 (else ATTN_ERR_INVALID_ARG); a combined scale
+ *          whose magnitude exceeds FLT_MAX is ATTN_ERR_INVALID_ARG too
+ *
+ * Arguments, layouts, alignment rules (q8 and k8 16-byte aligned), the work split,
+ * workspace and return values are otherwise those of attn_fwd. NaN codes give
+ * unspecified results for the rows they reach.
+ */
+int attn_fwd_fp8qk(const void* q8, const void* k8, const void* v, void* o, float* lse,
+                   int B, int H, int Nq, int Nk, int d, float scale, float q_descale, float k_descale,
+                   void* stream);
+
+/*
  * attn_fwd_noalloc -- attn_fwd for callers that cannot allocate device memory.
  *
  * There is no counterpart on the pages: this is a service of the library. Some callers

@@ -26,7 +26,7 @@ def declared_functions():
 
 def test_header_declares_the_entry_points():
     names = declared_functions()
-    assert {"attn_fwd", "attn_fwd_causal", "attn_fwd_bias", "attn_fwd_noalloc", "attn_bwd", "attn_bwd_causal",
+    assert {"attn_fwd", "attn_fwd_causal", "attn_fwd_bias", "attn_fwd_fp8qk", "attn_fwd_noalloc", "attn_bwd", "attn_bwd_causal",
             "attn_bwd_status", "attn_bwd_set_wait_limit",
             "attn_bwd_kernel_count", "attn_fwd_status", "attn_status_string",
             "attn_fwd_set_wait_limit", "attn_fwd_kernel_count"} <= set(names)
@@ -126,6 +126,38 @@ def test_bias_argument_checks(kw, code):
     before = attn.attn_fwd_kernel_count()
     assert call_bias(**kw) == code
     assert attn.attn_fwd_kernel_count() == before
+
+
+def call_fp8(q8=A, k8=A, v=A, o=A, lse=A, B=1, H=1, Nq=128, Nk=128, d=128, scale=0.125, dq=0.01, dk=0.02):
+    return attn.load_library().attn_fwd_fp8qk(q8, k8, v, o, lse, B, H, Nq, Nk, d, scale, dq, dk, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(dq=0.0), attn.ATTN_ERR_INVALID_ARG),
+    (dict(dk=-0.5), attn.ATTN_ERR_INVALID_ARG),
+    (dict(dq=math.nan), attn.ATTN_ERR_INVALID_ARG),
+    (dict(dk=math.inf), attn.ATTN_ERR_INVALID_ARG),
+    (dict(scale=3e38, dq=10.0, dk=10.0), attn.ATTN_ERR_INVALID_ARG),   # the combined scale overflows FP32
+    (dict(scale=math.nan), attn.ATTN_ERR_INVALID_ARG),
+    (dict(q8=None), attn.ATTN_ERR_INVALID_ARG),
+    (dict(k8=A + 8), attn.ATTN_ERR_MISALIGNED),
+    (dict(d=64), attn.ATTN_ERR_UNSUPPORTED),
+    (dict(Nk=0), attn.ATTN_ERR_INVALID_ARG),
+    (dict(B=0, q8=None), attn.ATTN_OK),
+    (dict(Nq=0, lse=None), attn.ATTN_OK),
+])
+def test_fp8qk_argument_checks(kw, code):
+    before = attn.attn_fwd_kernel_count()
+    assert call_fp8(**kw) == code
+    assert attn.attn_fwd_kernel_count() == before
+
+
+def test_fp8qk_binding_checks_types():
+    torch = pytest.importorskip("torch")
+    with pytest.raises(ValueError):   # a CPU tensor is refused before any pointer is passed
+        attn.attn_fwd_fp8qk(torch.zeros(1, 1, 128, 128, dtype=torch.uint8), A, A, A, A, 1, 1, 128, 128, 128, 0.1)
+    with pytest.raises(attn.AttnError):
+        attn.attn_fwd_fp8qk(A, A, A, A, A, 1, 1, 128, 128, 128, 0.1, q_descale=0.0)
 
 
 def test_bias_binding_checks_shapes():

@@ -1,0 +1,92 @@
+"""GPU parity of attn_fwd_fp8qk (Q and K as FP8 E4M3 codes with per-tensor descale factors)
+against the FP64 oracle on the same codes.
+
+The tensor cores form each product of two E4M3 values exactly and sum them in FP32, as they
+do for BF16 inputs, so the tolerance is the forward's own: max|dO| <= 1e-2, mean|dO| <= 1e-3,
+LSE relative error <= 1e-4 (tests/parity.py).
+"""
+import math
+
+import numpy as np
+import pytest
+
+import oracle
+from dense_attention_forward_fwd_gb300.configs import by_name
+from dense_attention_forward_fwd_gb300.inputs import make_qk_e4m3, sample_rows
+from parity import bf16_to_np, compare, run_gpu, to_device
+
+pytestmark = pytest.mark.gpu
+
+SCALE = float(np.float32(1 / math.sqrt(128)))
+
+
+def run_fp8(attn, q8, k8, v, scale, dq, dk):
+    import torch
+    B, H, Nq, d = q8.shape
+    Nk = k8.shape[2]
+    o = torch.full((B, H, Nq, d), float("nan"), dtype=torch.bfloat16, device="cuda")
+    lse = torch.full((B, H, Nq), float("nan"), dtype=torch.float32, device="cuda")
+    q8d = torch.from_numpy(np.ascontiguousarray(q8)).cuda().view(torch.float8_e4m3fn)
+    k8d = torch.from_numpy(np.ascontiguousarray(k8)).cuda()          # raw bytes are accepted too
+    attn.attn_fwd_fp8qk(q8d, k8d, to_device(v), o, lse, B, H, Nq, Nk, d, scale, dq, dk)
+    assert attn.attn_fwd_status() == attn.ATTN_OK
+    return bf16_to_np(o), lse.cpu().numpy()
+
+
+def check_fp8(attn, B, H, Nq, Nk, seed, qk_mult=1.0, scale=SCALE, rows=None):
+    q8, k8, v, dq, dk = make_qk_e4m3(B, H, Nq, Nk, seed=seed, qk_mult=qk_mult)
+    o, lse = run_fp8(attn, q8, k8, v, scale, dq, dk)
+    o_ref, lse_ref = oracle.attention_rows_e4m3qk(q8, k8, v, scale, dq, dk, rows)
+    o, lse = o.reshape(-1, 128), lse.reshape(-1)
+    if rows is not None:
+        o, lse = o[rows], lse[rows]
+    return compare(o, lse, o_ref, lse_ref, ulp_aware=qk_mult != 1.0)
+
+
+@pytest.mark.parametrize("B,H,Nq,Nk", [
+    (1, 1, 128, 128),
+    (1, 2, 256, 384),
+    (2, 3, 300, 1000),     # ragged query and key tails
+    (1, 1, 1, 200),        # a single query row
+    (1, 2, 129, 129),
+    (1, 2, 256, 5120),     # few groups with long rows: key steps split across blocks
+    (4, 2, 768, 768),
+])
+def test_fp8qk_full_parity(gpu_lib, B, H, Nq, Nk):
+    check_fp8(gpu_lib, B, H, Nq, Nk, seed=13000 + Nq + Nk)
+
+
+def test_fp8qk_peaked_scores(gpu_lib):
+    check_fp8(gpu_lib, 1, 2, 512, 2048, seed=13100, qk_mult=3.0)
+
+
+@pytest.mark.parametrize("scale", [0.0, -0.0883883461356163, 0.5])
+def test_fp8qk_other_scales(gpu_lib, scale):
+    check_fp8(gpu_lib, 1, 2, 256, 640, seed=13200, scale=scale)
+
+
+@pytest.mark.parametrize("name", ["rect-4k-8k", "square-4k"])
+def test_fp8qk_workload_sampled_rows(gpu_lib, name):
+    # the measured shapes at full size, in the launch configuration the benchmark times
+    w = by_name(name)
+    rows = sample_rows(w.B, w.H, w.Nq, per_head=16)
+    check_fp8(gpu_lib, w.B, w.H, w.Nq, w.Nk, seed=w.seed, scale=w.scale, rows=rows)
+
+
+def test_fp8qk_agrees_with_the_bf16_entry_point_on_the_same_values(gpu_lib):
+    # descale factors of 1: the codes' values are BF16 values, so attn_fwd sees the same inputs
+    q8, k8, v, dq, dk = make_qk_e4m3(1, 2, 384, 640, seed=13300)
+    torch = pytest.importorskip("torch")
+    widen = lambda c: torch.from_numpy(c).view(torch.float8_e4m3fn).to(torch.bfloat16).view(torch.int16).numpy() \
+        .view(np.uint16)
+    scale = float(np.float32(SCALE * dq * dk))   # the scores of the unquantized N(0,1) inputs
+    o8, l8 = run_fp8(gpu_lib, q8, k8, v, scale, 1.0, 1.0)
+    ob, lb = run_gpu(gpu_lib, widen(q8), widen(k8), v, scale)
+    assert np.max(np.abs(o8 - ob)) <= 1e-2 and np.max(np.abs(l8 - lb)) <= 1e-4 * max(1.0, np.max(np.abs(lb)))
+
+
+def test_fp8qk_is_deterministic(gpu_lib):
+    q8, k8, v, dq, dk = make_qk_e4m3(1, 2, 256, 5120, seed=13400)
+    a = run_fp8(gpu_lib, q8, k8, v, SCALE, dq, dk)
+    b = run_fp8(gpu_lib, q8, k8, v, SCALE, dq, dk)
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
