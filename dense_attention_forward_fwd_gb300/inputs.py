@@ -30,6 +30,7 @@ __all__ = [
     "make_qkv",
     "make_bias",
     "make_qk_e4m3",
+    "make_qkv_e4m3",
     "BF16_NEG_INF",
     "sample_rows",
 ]
@@ -94,6 +95,25 @@ def make_qk_e4m3(B: int, H: int, Nq: int, Nk: int, d: int = 128, seed: int = 0, 
         codes = torch.from_numpy(np.ascontiguousarray(x / ds)).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
         out += [codes, float(ds)]
     return out[0], out[2], f32_to_bf16_bits(v), out[1], out[3]
+
+
+def make_qkv_e4m3(B: int, H: int, Nq: int, Nk: int, d: int = 128, seed: int = 0, qk_mult: float = 1.0):
+    """Q, K and V as FP8 E4M3 codes with per-tensor descale factors.
+
+    Q and K as :func:`make_qk_e4m3`; V's float32 normals (the same draw) quantized the same
+    way (descale = amax / 448). Returns (q8, k8, v8 uint8 [B,H,N,d], q_descale, k_descale,
+    v_descale); v8 is key-major like V, [B,H,Nk,d].
+    """
+    import torch
+    q8, k8, _, dq, dk = make_qk_e4m3(B, H, Nq, Nk, d=d, seed=seed, qk_mult=qk_mult)
+    rng = np.random.Generator(np.random.PCG64(seed))
+    rng.standard_normal((B, H, Nq, d), dtype=np.float32)
+    rng.standard_normal((B, H, Nk, d), dtype=np.float32)
+    v = rng.standard_normal((B, H, Nk, d), dtype=np.float32)
+    amax = float(np.abs(v).max()) if v.size else 1.0
+    dv = np.float32(amax / 448.0) if amax > 0 else np.float32(1.0)
+    v8 = torch.from_numpy(np.ascontiguousarray(v / dv)).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    return q8, k8, v8, dq, dk, float(dv)
 
 
 def make_bias(shape, seed: int, std: float = 1.0) -> np.ndarray:

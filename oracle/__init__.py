@@ -20,7 +20,7 @@ import numpy as np
 
 __all__ = ["build", "Oracle", "default", "attention_rows", "attention_rows_causal", "attention_rows_bias",
            "attention", "attention_dense", "attention_bwd", "probs", "max_threads", "LIB_PATH",
-           "attention_rows_e4m3qk", "e4m3_to_f64"]
+           "attention_rows_e4m3qk", "attention_rows_e4m3", "e4m3_to_f64"]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "attn_ref.c")
@@ -59,6 +59,9 @@ class Oracle:
         lib.attn_ref_rows_e4m3qk_f64.argtypes = [vp, vp, vp, i64, i64, i64, i64, i64, dbl, dbl, dbl, vp, i64, vp,
                                                  vp, ctypes.c_int]
         lib.attn_ref_rows_e4m3qk_f64.restype = ctypes.c_int
+        lib.attn_ref_rows_e4m3_f64.argtypes = [vp, vp, vp, i64, i64, i64, i64, i64, dbl, dbl, dbl, dbl, vp, i64,
+                                               vp, vp, ctypes.c_int]
+        lib.attn_ref_rows_e4m3_f64.restype = ctypes.c_int
         lib.attn_ref_e4m3_to_f64.argtypes = [vp, i64, vp]
         lib.attn_ref_e4m3_to_f64.restype = None
         lib.attn_ref_dense_f64.argtypes = [vp, vp, vp, i64, i64, i64, i64, i64, dbl, vp, vp]
@@ -181,6 +184,29 @@ class Oracle:
             raise ValueError(f"attn_ref_rows_e4m3qk_f64 failed with status {rc}")
         return o, lse
 
+    def attention_rows_e4m3(self, q8, k8, v8, scale: float, q_descale: float = 1.0, k_descale: float = 1.0,
+                            v_descale: float = 1.0, rows=None, nthreads: int = 0):
+        """As attention_rows_e4m3qk with V given as E4M3 codes too (uint8 [B,H,Nk,dv], real
+        values v_descale * V8); P is not rounded: this is the definition on the real inputs."""
+        q8, k8, v8 = (np.ascontiguousarray(a) for a in (q8, k8, v8))
+        if q8.dtype != np.uint8 or k8.dtype != np.uint8 or v8.dtype != np.uint8:
+            raise TypeError("q8, k8 and v8 must be uint8 E4M3 codes")
+        B, H, Nq, d = q8.shape
+        Nk, dv = k8.shape[2], v8.shape[3]
+        if k8.shape != (B, H, Nk, d) or v8.shape[:3] != (B, H, Nk):
+            raise ValueError(f"shape mismatch q8{q8.shape} k8{k8.shape} v8{v8.shape}")
+        if rows is None:
+            rows = np.arange(B * H * Nq, dtype=np.int64)
+        rows = np.ascontiguousarray(rows, dtype=np.int64)
+        o = np.empty((rows.size, dv), dtype=np.float64)
+        lse = np.empty(rows.size, dtype=np.float64)
+        rc = self.lib.attn_ref_rows_e4m3_f64(_ptr(q8), _ptr(k8), _ptr(v8), B * H, Nq, Nk, d, dv, float(scale),
+                                             float(q_descale), float(k_descale), float(v_descale), _ptr(rows),
+                                             rows.size, _ptr(o), _ptr(lse), int(nthreads))
+        if rc != 0:
+            raise ValueError(f"attn_ref_rows_e4m3_f64 failed with status {rc}")
+        return o, lse
+
     def attention(self, q, k, v, scale: float, nthreads: int = 0):
         """Full O [B,H,Nq,dv] and LSE [B,H,Nq] in float64."""
         B, H, Nq, _ = q.shape
@@ -292,6 +318,11 @@ def e4m3_to_f64(codes):
 def attention_rows_e4m3qk(q8, k8, v, scale: float, q_descale: float = 1.0, k_descale: float = 1.0, rows=None,
                           nthreads: int = 0):
     return default().attention_rows_e4m3qk(q8, k8, v, scale, q_descale, k_descale, rows, nthreads)
+
+
+def attention_rows_e4m3(q8, k8, v8, scale: float, q_descale: float = 1.0, k_descale: float = 1.0,
+                        v_descale: float = 1.0, rows=None, nthreads: int = 0):
+    return default().attention_rows_e4m3(q8, k8, v8, scale, q_descale, k_descale, v_descale, rows, nthreads)
 
 
 def attention(q, k, v, scale: float, nthreads: int = 0):

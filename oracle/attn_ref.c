@@ -581,3 +581,64 @@ int attn_ref_rows_e4m3qk_f64(const uint8_t *q8, const uint8_t *k8, const uint16_
     }
     return failed ? REF_ENOMEM : REF_OK;
 }
+
+/*
+ * attn_ref_rows_e4m3_f64: as attn_ref_rows_e4m3qk_f64 with V given as E4M3 codes too,
+ * v8 [BH, Nk, dv] in C order with its descale factor: the real values are v_descale * V8,
+ * and O is the definition's weighted sum of them (P is not rounded here).
+ */
+int attn_ref_rows_e4m3_f64(const uint8_t *q8, const uint8_t *k8, const uint8_t *v8,
+                           int64_t BH, int64_t Nq, int64_t Nk, int64_t d, int64_t dv,
+                           double scale, double q_descale, double k_descale, double v_descale,
+                           const int64_t *sel, int64_t nsel, double *o, double *lse, int nthreads)
+{
+    if (BH < 0 || Nq < 0 || Nk < 1 || d < 1 || dv < 1 || nsel < 0) return REF_EINVAL;
+    if (nsel == 0) return REF_OK;
+    if (!q8 || !k8 || !v8 || !sel || !o || !lse) return REF_EINVAL;
+    for (int64_t r = 0; r < nsel; r++)
+        if (sel[r] < 0 || sel[r] >= BH * Nq) return REF_EINVAL;
+
+    int failed = 0;
+#ifdef _OPENMP
+    int nt = nthreads > 0 ? nthreads : omp_get_max_threads();
+#pragma omp parallel num_threads(nt)
+#else
+    (void)nthreads;
+#endif
+    {
+        double *w = (double *)malloc((size_t)Nk * sizeof(double));
+        if (!w) {
+#ifdef _OPENMP
+#pragma omp atomic write
+#endif
+            failed = 1;
+        } else {
+#ifdef _OPENMP
+#pragma omp for schedule(dynamic, 1)
+#endif
+            for (int64_t r = 0; r < nsel; r++) {
+                int64_t bh = sel[r] / Nq, i = sel[r] % Nq;
+                const uint8_t *qrow = q8 + (bh * Nq + i) * d, *khead = k8 + bh * Nk * d, *vhead = v8 + bh * Nk * dv;
+                /* step 1 on the real inputs */
+                for (int64_t j = 0; j < Nk; j++) {
+                    double dot = 0.0;
+                    for (int64_t c = 0; c < d; c++)
+                        dot += (q_descale * e4m3_to_f64(qrow[c])) * (k_descale * e4m3_to_f64(khead[j * d + c]));
+                    w[j] = scale * dot;
+                }
+                /* steps 2-5 with the real values v_descale * V8 */
+                double top = row_max(w, Nk);
+                double sum = row_exp_sum(w, Nk, top);
+                for (int64_t c = 0; c < dv; c++) {
+                    double num = 0.0;
+                    for (int64_t j = 0; j < Nk; j++)
+                        num += w[j] * (v_descale * e4m3_to_f64(vhead[j * dv + c]));
+                    o[r * dv + c] = num / sum;
+                }
+                lse[r] = top + log(sum);
+            }
+            free(w);
+        }
+    }
+    return failed ? REF_ENOMEM : REF_OK;
+}

@@ -547,6 +547,27 @@ def pin_e4m3_two_keys_logistic_closed_form(orc):
     assert abs(lse[0] - math.log(math.exp(s0) + math.exp(s1))) < 1e-14
 
 
+def pin_e4m3_values_equal_the_scores_only_oracle_times_the_value_descale(orc):
+    # O is linear in V: with V as codes, O = v_descale * (the E4M3-score oracle on the codes'
+    # values, which are BF16 values); the LSE does not involve V. dv != d catches a value
+    # row read with the key stride.
+    from dense_attention_forward_fwd_gb300.inputs import make_qkv_e4m3
+    q8, k8, v8, dq, dk, dv = make_qkv_e4m3(1, 2, 7, 29, d=16, seed=71, qk_mult=2.0)
+    v8 = np.ascontiguousarray(v8[..., :8])
+    o8, l8 = orc.attention_rows_e4m3(q8, k8, v8, 0.4, dq, dk, dv)
+    ob, lb = orc.attention_rows_e4m3qk(q8, k8, bf16(orc.e4m3_to_f64(v8)), 0.4, dq, dk)
+    assert np.max(np.abs(o8 - dv * ob)) < 1e-12 * max(1.0, np.max(np.abs(o8))) and np.array_equal(l8, lb)
+
+
+def pin_e4m3_constant_values_are_returned(orc):
+    # every value row equal to one code: O = v_descale * its value in every row and column
+    from dense_attention_forward_fwd_gb300.inputs import make_qkv_e4m3
+    q8, k8, v8, dq, dk, _ = make_qkv_e4m3(1, 1, 5, 40, d=16, seed=72)
+    v8[:] = 0xC5   # -(1 + 5/8) * 2^(8 - 7) = -3.25
+    o8, _ = orc.attention_rows_e4m3(q8, k8, v8, 0.25, dq, dk, 0.5)
+    assert np.max(np.abs(o8 + 1.625)) < 1e-13
+
+
 PINS = [v for k_, v in sorted(globals().items()) if k_.startswith("pin_")]
 
 

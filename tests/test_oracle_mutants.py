@@ -47,6 +47,8 @@ MUTANTS = {
     "e4m3 query descale squared": ("(q_descale * e4m3_to_f64(qi[c]))", "(q_descale * q_descale * e4m3_to_f64(qi[c]))"),
     "e4m3 values from the keys": ("num += s[j] * bf16_to_f64(vrows[j * dv + c]);",
                                   "num += s[j] * (double)kh[j * d + c];"),
+    "e4m3 value descale dropped": ("(v_descale * e4m3_to_f64(vhead[j * dv + c]))", "(e4m3_to_f64(vhead[j * dv + c]))"),
+    "e4m3 value rows with the key stride": ("vhead[j * dv + c]", "vhead[j * d + c]"),
     "causal dense forward one key short": ("const int64_t nv = causal ? i + (Nk - Nq) + 1 : Nk;",
                                            "const int64_t nv = causal ? i + (Nk - Nq) + (i > 0) : Nk;"),
 }
