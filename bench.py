@@ -29,6 +29,9 @@ amax / 448), V in BF16; the FLOP count is unchanged and the roofline peak is tha
 contraction done half at the FP8 rate (twice the measured BF16 rate, the nominal ratio) and
 half at the BF16 rate.
 
+--fp8 times attn_fwd_fp8: Q, K and V quantized per tensor to E4M3 (V passed transposed), P
+rounded to E4M3 for the P V product; the roofline peak is the FP8 rate for all FLOPs.
+
 --impl reference times the FP64 CPU oracle (the plain definition) on host cores, on a
 bounded sample of query rows per step.
 """
@@ -78,9 +81,13 @@ def parse():
                     help="time attn_bwd (dQ, dK, dV for an N(0,1) upstream gradient); FLOPs = 2.5x the forward's")
     ap.add_argument("--fp8-qk", action="store_true",
                     help="time attn_fwd_fp8qk (Q and K as FP8 E4M3 codes with per-tensor descale factors)")
+    ap.add_argument("--fp8", action="store_true",
+                    help="time attn_fwd_fp8 (Q, K and V as FP8 E4M3 codes, P rounded to E4M3 for P V)")
     args = ap.parse_args()
-    if args.fp8_qk and (args.causal or args.backward or args.bias != "none"):
-        ap.error("--fp8-qk has no causal, bias or backward entry point; use it alone")
+    if (args.fp8_qk or args.fp8) and (args.causal or args.backward or args.bias != "none"):
+        ap.error("--fp8-qk and --fp8 have no causal, bias or backward entry point; use them alone")
+    if args.fp8_qk and args.fp8:
+        ap.error("--fp8-qk and --fp8 are two entry points; pick one")
     if args.bias != "none" and (args.causal or args.backward):
         ap.error("--bias has no causal or backward entry point; use it alone")
     return args
@@ -94,8 +101,10 @@ def run_config(w, args) -> dict:
     """The workload description both arms print (the reference arm times the same one)."""
     return {"workload": w.name, "B": w.B, "H": w.H, "Nq": w.Nq, "Nk": w.Nk, "d": w.d, "causal": args.causal,
             "bias": args.bias, "pass": "backward" if args.backward else "forward", "qk_mult": w.qk_mult,
-            "qk": "e4m3" if args.fp8_qk else "bf16",
-            "inputs": ("iid N(0,1) (Q,K x qk_mult); Q, K quantized per tensor to E4M3 (descale = amax/448), V BF16"
+            "qk": "e4m3" if (args.fp8_qk or args.fp8) else "bf16", "pv": "e4m3" if args.fp8 else "bf16",
+            "inputs": ("iid N(0,1) (Q,K x qk_mult); Q, K, V quantized per tensor to E4M3 (descale = amax/448)"
+                       if args.fp8 else
+                       "iid N(0,1) (Q,K x qk_mult); Q, K quantized per tensor to E4M3 (descale = amax/448), V BF16"
                        if args.fp8_qk else "iid N(0,1) BF16 (Q,K x qk_mult)"),
             "l2": "flushed (512 MiB write) before every timed launch",
             "vs_baseline_ref": "RTX 5090 v5 kernel, same shape (other hardware: context only)"}
@@ -205,8 +214,13 @@ def workload_flops(w, causal: bool) -> float:
 
 # ------------------------------------------------------------------ reference arm (oracle) ---
 
-def oracle_rows_fn(oracle, w, causal: bool, bias_kind: str, H1: int, nq: int, fp8_qk: bool = False):
+def oracle_rows_fn(oracle, w, causal: bool, bias_kind: str, H1: int, nq: int, fp8_qk: bool = False,
+                   fp8: bool = False):
     """The oracle entry point for this run's variant, as fn(q, k, v, scale, rows)."""
+    if fp8:   # Q, K and V of the same draw as E4M3 codes
+        from dense_attention_forward_fwd_gb300.inputs import make_qkv_e4m3
+        q8, k8, v8, dq, dk, dv = make_qkv_e4m3(1, H1, nq, w.Nk, d=w.d, seed=w.seed, qk_mult=w.qk_mult)
+        return lambda q, k, v, scale, rows: oracle.attention_rows_e4m3(q8, k8, v8, scale, dq, dk, dv, rows)
     if fp8_qk:   # Q and K of the same draw (seed, shape) as E4M3 codes; V is make_qkv's V
         from dense_attention_forward_fwd_gb300.inputs import make_qk_e4m3
         q8, k8, _, dq, dk = make_qk_e4m3(1, H1, nq, w.Nk, d=w.d, seed=w.seed, qk_mult=w.qk_mult)
@@ -243,7 +257,7 @@ def cpu_oracle_backward_sample(w, target_seconds: float, causal: bool = False):
 
 
 def cpu_oracle_sample(w, target_seconds: float, rank_seed: int = 0, causal: bool = False, bias_kind: str = "none",
-                      fp8_qk: bool = False):
+                      fp8_qk: bool = False, fp8: bool = False):
     """Time the FP64 oracle on a sample of query rows; returns (TFLOPS, rows, seconds, threads)."""
     import numpy as np
 
@@ -256,7 +270,7 @@ def cpu_oracle_sample(w, target_seconds: float, rank_seed: int = 0, causal: bool
     nq = min(w.Nq, 4096)
     q, k, v = make_qkv(1, H1, nq, w.Nk, d=w.d, seed=w.seed + rank_seed, qk_mult=w.qk_mult)
     threads = oracle.max_threads()
-    fn = oracle_rows_fn(oracle, w, causal, bias_kind, H1, nq, fp8_qk)
+    fn = oracle_rows_fn(oracle, w, causal, bias_kind, H1, nq, fp8_qk, fp8)
 
     def flop_rows(rows):   # 4*d FLOPs per visible key of each sampled row
         if not causal:
@@ -316,7 +330,7 @@ def run_reference(args, w):
     q, k, v = make_qkv(1, H1, nq, w.Nk, d=w.d, seed=w.seed, qk_mult=w.qk_mult)
     threads = oracle.max_threads()
     n_rows_total = q.shape[1] * q.shape[2]
-    fn = oracle_rows_fn(oracle, w, args.causal, args.bias, H1, nq, args.fp8_qk)
+    fn = oracle_rows_fn(oracle, w, args.causal, args.bias, H1, nq, args.fp8_qk, args.fp8)
 
     def flop_rows(rows):   # 4*d FLOPs per visible key; causal sample rows sit at the end of the sequence
         if not args.causal:
@@ -388,14 +402,16 @@ def run_ours(args, w):
     stream = torch.cuda.current_stream(dev)
 
     ins = [q, k, v]
-    descale = (1.0, 1.0)
-    if args.fp8_qk:   # per-tensor quantization of Q and K to E4M3 codes
-        qk8, descale = [], []
-        for x in (q, k):
+    descale = (1.0, 1.0, 1.0)
+    if args.fp8_qk or args.fp8:   # per-tensor quantization to E4M3 codes
+        x8, descale = [], []
+        for x in ((q, k, v) if args.fp8 else (q, k)):
             ds = float(torch.tensor(x.float().abs().max().item() / 448.0, dtype=torch.float32))
-            qk8.append((x.float() / ds).to(torch.float8_e4m3fn))
+            x8.append((x.float() / ds).to(torch.float8_e4m3fn))
             descale.append(ds)
-        ins = [qk8[0], qk8[1], v]
+        if args.fp8:   # V^T, keys innermost (Nk of every workload is a multiple of 16)
+            x8[2] = x8[2].transpose(2, 3).contiguous()
+        ins = [x8[0], x8[1], x8[2] if args.fp8 else v]
     outs = [o, lse]
     if args.bias != "none":
         bshape = (1, 1, w.Nq, w.Nk) if args.bias == "shared" else (w.B, w.H, w.Nq, w.Nk)
@@ -416,6 +432,9 @@ def run_ours(args, w):
             attn.attn_fwd_causal(*ins_, *outs_, w.B, w.H, w.Nq, w.Nk, w.d, w.scale, st)
         elif args.fp8_qk:
             attn.attn_fwd_fp8qk(*ins_, *outs_, w.B, w.H, w.Nq, w.Nk, w.d, w.scale, descale[0], descale[1], st)
+        elif args.fp8:
+            attn.attn_fwd_fp8(*ins_, *outs_, w.B, w.H, w.Nq, w.Nk, w.d, w.scale, descale[0], descale[1], descale[2],
+                              st)
         else:
             attn.attn_fwd(*ins_, *outs_, w.B, w.H, w.Nq, w.Nk, w.d, w.scale, st)
 
@@ -528,11 +547,15 @@ def run_ours(args, w):
         peak = 2.0 / (1.0 / (2.0 * peak) + 1.0 / peak)
         peak_note = (f"half the FLOPs at 2 x {peak_src} bf16_tflops (FP8 E4M3, nominal ratio 4.5/2.25), "
                      "half at bf16_tflops (burst)")
+    if args.fp8:   # both products at the FP8 rate
+        peak = 2.0 * peak
+        peak_note = f"2 x {peak_src} bf16_tflops (FP8 E4M3, nominal ratio 4.5/2.25; burst)"
     achieved = flops / (ms * 1e-3) / 1e12   # one launch on one GPU
     traffic = None
     if os.path.exists(TRAFFIC_FILE):
         key = (w.name + ("-causal" if args.causal else "") + ("" if args.bias == "none" else "-bias-" + args.bias)
-               + ("-backward" if args.backward else "") + ("-fp8qk" if args.fp8_qk else ""))
+               + ("-backward" if args.backward else "") + ("-fp8qk" if args.fp8_qk else "")
+               + ("-fp8" if args.fp8 else ""))
         rec = json.load(open(TRAFFIC_FILE)).get(key)
         if rec and rec.get("kernel_hash") == kernel_hash(args.backward):
             traffic = rec.get("bytes_per_launch")
@@ -542,8 +565,8 @@ def run_ours(args, w):
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": ((value / PAGES_TFLOPS[w.name])
                         if w.name in PAGES_TFLOPS and not args.causal and args.bias == "none" and not args.backward
-                        and not args.fp8_qk else None),
-        "dtype": "e4m3+bf16" if args.fp8_qk else "bf16", "data": "synthetic",
+                        and not args.fp8_qk and not args.fp8 else None),
+        "dtype": "e4m3" if args.fp8 else "e4m3+bf16" if args.fp8_qk else "bf16", "data": "synthetic",
         "config": run_config(w, args),
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak, "traffic": traffic, "peak_source": peak_note},
@@ -558,7 +581,7 @@ def run_ours(args, w):
             sample = f"backward of one head with {n} query rows x {w.Nk} keys of {w.describe()}, FP64, {dt:.1f} s"
         else:
             tfl, n, dt, thr = cpu_oracle_sample(w, args.cpu_seconds, causal=args.causal, bias_kind=args.bias,
-                                                fp8_qk=args.fp8_qk)
+                                                fp8_qk=args.fp8_qk, fp8=args.fp8)
             keys = "visible keys of each row, causal" if args.causal else "full Nk each"
             sample = f"{n} query rows of {w.describe()} ({keys}), FP64, {dt:.1f} s"
         line["cpu_baseline"] = {"value": tfl, "unit": "TFLOP/s", "cores": thr, "kind": "oracle", "sample": sample}

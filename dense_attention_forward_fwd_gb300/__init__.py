@@ -15,7 +15,7 @@ from ._build import LIB_PATH, build_library
 
 __all__ = [
     "ATTN_OK", "ATTN_ERR_INVALID_ARG", "ATTN_ERR_UNSUPPORTED", "ATTN_ERR_MISALIGNED", "ATTN_ERR_CUDA",
-    "ATTN_ERR_TIMEOUT", "AttnError", "load_library", "attn_fwd", "attn_fwd_causal", "attn_fwd_bias", "attn_fwd_fp8qk", "attn_fwd_noalloc", "attn_fwd_status", "attn_status_string",
+    "ATTN_ERR_TIMEOUT", "AttnError", "load_library", "attn_fwd", "attn_fwd_causal", "attn_fwd_bias", "attn_fwd_fp8qk", "attn_fwd_fp8", "attn_fwd_noalloc", "attn_fwd_status", "attn_status_string",
     "attn_fwd_set_wait_limit", "attn_fwd_kernel_count", "attention", "attn_bwd", "attn_bwd_causal", "attn_bwd_status",
     "attn_bwd_kernel_count", "attn_bwd_set_wait_limit",
 ]
@@ -51,6 +51,9 @@ def load_library(build_if_stale: bool = True) -> ctypes.CDLL:
             lib.attn_fwd_causal.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, f32, vp]
             lib.attn_fwd_fp8qk.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, f32, f32, f32, vp]
             lib.attn_fwd_fp8qk.restype = i32
+            lib.attn_fwd_fp8.argtypes = [vp, vp, vp, ctypes.c_longlong, vp, vp, i32, i32, i32, i32, i32, f32, f32, f32,
+                                         f32, vp]
+            lib.attn_fwd_fp8.restype = i32
             i64 = ctypes.c_longlong
             lib.attn_fwd_bias.argtypes = [vp, vp, vp, vp, i64, i64, i64, vp, vp, i32, i32, i32, i32, i32, f32, vp]
             lib.attn_fwd_noalloc.restype = i32
@@ -163,6 +166,32 @@ def attn_fwd_fp8qk(q8, k8, v, o, lse, B: int, H: int, Nq: int, Nk: int, d: int, 
                             float(k_descale), _stream_handle(stream, q8, k8, v, o, lse))
     if rc != ATTN_OK:
         raise AttnError(rc, "attn_fwd_fp8qk")
+
+
+def attn_fwd_fp8(q8, k8, vt8, o, lse, B: int, H: int, Nq: int, Nk: int, d: int, scale: float,
+                 q_descale: float = 1.0, k_descale: float = 1.0, v_descale: float = 1.0, stream=None,
+                 ldv: int | None = None) -> None:
+    """Like :func:`attn_fwd_fp8qk`, with V as E4M3 codes too, passed transposed: ``vt8`` is
+    [B,H,d,ldv] (keys innermost, ldv >= Nk a multiple of 16; a tensor's last dimension is
+    taken as ldv). P is rounded to E4M3 for the P V product (see include/attn_fwd.h for the
+    accuracy this costs)."""
+    lib = load_library()
+    if _is_tensor(vt8):
+        if vt8.dim() != 4 or tuple(vt8.shape[:3]) != (B, H, d):
+            raise ValueError(f"vt8 must be [B, H, d, ldv] = [{B}, {H}, {d}, ldv], got {tuple(vt8.shape)}")
+        ldv = int(vt8.shape[3])
+    elif ldv is None:
+        raise ValueError("ldv is required when vt8 is an integer pointer")
+    args = (
+        _ptr(q8, "q8", B * H * Nq * d, "e4m3"), _ptr(k8, "k8", B * H * Nk * d, "e4m3"),
+        _ptr(vt8, "vt8", B * H * d * ldv, "e4m3"),
+    )
+    outs = (_ptr(o, "o", B * H * Nq * d, "bf16"), _ptr(lse, "lse", B * H * Nq, "f32"))
+    rc = lib.attn_fwd_fp8(*args, int(ldv), *outs, int(B), int(H), int(Nq), int(Nk), int(d), float(scale),
+                          float(q_descale), float(k_descale), float(v_descale),
+                          _stream_handle(stream, q8, k8, vt8, o, lse))
+    if rc != ATTN_OK:
+        raise AttnError(rc, "attn_fwd_fp8")
 
 
 def attn_fwd_bias(q, k, v, bias, o, lse, B: int, H: int, Nq: int, Nk: int, d: int, scale: float, stream=None,

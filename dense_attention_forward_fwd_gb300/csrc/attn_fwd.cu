@@ -1,7 +1,9 @@
 // attn_fwd.cu -- dense BF16 attention forward for GB300 (sm_103a): non-causal, causal
 // (attn_fwd_causal), with an additive bias (attn_fwd_bias, its own instantiation) and with
-// Q and K as FP8 E4M3 codes (attn_fwd_fp8qk: the producer loads one 128-byte box per Q or
-// K tile and S = Q K^T is issued as kind::f8f6f4 MMAs; everything from S on is shared).
+// 8-bit inputs: Q and K as FP8 E4M3 codes (attn_fwd_fp8qk: the producer loads one 128-byte
+// box per Q or K tile and S = Q K^T is issued as kind::f8f6f4 MMAs), or Q, K and V
+// (attn_fwd_fp8: V^T tiles as one box each, P rounded to E4M3 in TMEM, four keys per
+// column, and O += P V issued as kind::f8f6f4 MMAs with P read from TMEM).
 //
 // O = softmax(scale * Q K^T) V and the per-row log-sum-exp, head_dim 128, computed
 // FlashAttention-style: Q tiles of 128 query rows are loaded once and 128-key K/V
@@ -46,7 +48,8 @@
 // The softmax keeps, per row, m (running max of scale*s in log2 units) and l (running
 // sum of 2^(scale*s*log2e - m)). O is accumulated unnormalised and divided once at the
 // end ("normalised once the loop ends, then written", same write-up). The running max
-// only moves when it grows by more than kRescaleLog2 (log2 units): the exponentials
+// only moves when it grows by more than kRescaleLog2 (log2 units; 8 when P is rounded to
+// E4M3, whose largest value is 448): the exponentials
 // are then bounded by 2^kRescaleLog2 and O and l keep sharing one m, so the result is
 // unchanged; skipping the move avoids reading and rewriting O in TMEM. P is BF16 (range
 // to 2^127) and every sum is FP32, so the bound can be generous: with weights up to 2^32,
@@ -160,6 +163,7 @@ struct Params {
   long long bias_sb, bias_sh, bias_sq;
   int H;                  // heads per batch (splits b*H + h)
   float scale;            // the caller's scale (the bias path scales before adding B)
+  float v_scale = 1.0f;   // V's descale factor (V as FP8 codes), applied with 1 / l
 };
 
 // floor(a / b) for a >= 0, b > 0. On the device a 64-bit division is a long dependent
@@ -346,6 +350,15 @@ __device__ __forceinline__ void mma_ss_f8(uint32_t d, uint64_t a, uint64_t b, ui
       "l"(a), "l"(b), "r"(idesc), "r"(static_cast<uint32_t>(acc))
       : "memory");
 }
+// D(tmem) (+)= A(tmem) * B(smem desc), 8-bit floating-point operands
+__device__ __forceinline__ void mma_ts_f8(uint32_t d, uint32_t a, uint64_t b, uint32_t idesc, bool acc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d),
+      "r"(a), "l"(b), "r"(idesc), "r"(static_cast<uint32_t>(acc))
+      : "memory");
+}
 // D(tmem) (+)= A(tmem) * B(smem desc)
 __device__ __forceinline__ void mma_ts(uint32_t d, uint32_t a, uint64_t b, uint32_t idesc, bool acc) {
   asm volatile(
@@ -404,6 +417,14 @@ __device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&x)[8])
       "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};\n\t"
       "tcgen05.wait::st.sync.aligned;" ::"r"(taddr),
       "r"(x[0]), "r"(x[1]), "r"(x[2]), "r"(x[3]), "r"(x[4]), "r"(x[5]), "r"(x[6]), "r"(x[7])
+      : "memory");
+}
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&x)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};\n\t"
+      "tcgen05.wait::st.sync.aligned;" ::"r"(taddr),
+      "r"(x[0]), "r"(x[1]), "r"(x[2]), "r"(x[3]), "r"(x[4]), "r"(x[5]), "r"(x[6]), "r"(x[7]),
+        "r"(x[8]), "r"(x[9]), "r"(x[10]), "r"(x[11]), "r"(x[12]), "r"(x[13]), "r"(x[14]), "r"(x[15])
       : "memory");
 }
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&x)[32]) {
@@ -560,6 +581,24 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
   return r;
 }
+// Four values rounded to E4M3 (nearest even, saturating), the first in the lowest byte.
+// As with the BF16 pair, cvt puts its first source in the upper half of the result.
+__device__ __forceinline__ uint32_t pack_e4m3x4(float a0, float a1, float a2, float a3) {
+  uint16_t lo, hi;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(lo) : "f"(a1), "f"(a0));
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(hi) : "f"(a3), "f"(a2));
+  return static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
+}
+// x rounded to E4M3 and widened back (exactly, through FP16) to FP32.
+__device__ __forceinline__ float round_e4m3(float x) {
+  uint16_t c;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(c) : "f"(0.0f), "f"(x));
+  uint32_t h2;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(c));
+  float r;
+  asm("cvt.f32.f16 %0, %1;" : "=f"(r) : "h"(static_cast<uint16_t>(h2 & 0xffffu)));
+  return r;
+}
 
 // ---------------------------------------------------------------------------------
 // Descriptors (tcgen05 shared-memory matrix descriptor and kind::f16 instruction
@@ -619,8 +658,9 @@ __device__ __forceinline__ bool wait_warp(const Ctl& c, int idx, uint32_t parity
 // ---------------------------------------------------------------------------------
 // Roles
 // ---------------------------------------------------------------------------------
-// kQK8: Q and K are FP8 codes, one 128-byte box per tile in the first half of its slot.
-template <bool kQK8>
+// kF8 >= 1: Q and K are FP8 codes, one 128-byte box per tile in the first half of its
+// slot; kF8 == 2: V too, transposed (keys innermost), one box in the first half of its slot.
+template <int kF8>
 __device__ void run_producer(const Ctl& c, uint32_t base, const CUtensorMap* tmQ,
                              const CUtensorMap* tmK, const CUtensorMap* tmV, const Params& p) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tmQ)) : "memory");
@@ -641,6 +681,7 @@ __device__ void run_producer(const Ctl& c, uint32_t base, const CUtensorMap* tmQ
     const int q_row0 = (sg.group % p.q_groups) * (kQTiles * kBM);
     // the previous segment's S MMAs must be done with the Q tiles
     if (u > 0 && !wait_phase(c, kBarQEmpty, (u - 1) & 1, true)) break;
+    constexpr bool kQK8 = kF8 >= 1, kV8 = kF8 == 2;
     mbar_arrive_expect_tx(c.bar(kBarQFull), kQTiles * (kQK8 ? kTile8Bytes : kTileBytes));
     for (int i = 0; i < kQTiles; ++i)
       for (int h = 0; h < (kQK8 ? 1 : 2); ++h)
@@ -662,11 +703,16 @@ __device__ void run_producer(const Ctl& c, uint32_t base, const CUtensorMap* tmQ
       if (p.withhold_tile && unit == 1) continue;
       const bool has_v = i > 0, has_k = i < n;
       const uint32_t fb = c.bar(kBarKVFull + pr);
-      mbar_arrive_expect_tx(fb, (has_v ? kTileBytes : 0) + (has_k ? (kQK8 ? kTile8Bytes : kTileBytes) : 0));
+      mbar_arrive_expect_tx(fb, (has_v ? (kV8 ? kTile8Bytes : kTileBytes) : 0) +
+                                    (has_k ? (kQK8 ? kTile8Bytes : kTileBytes) : 0));
       uint32_t dst = base + kOffKV + 2 * pr * kTileBytes;
       if (has_v) {
-        for (int h = 0; h < 2; ++h)
-          tma_load_3d(dst + h * kBoxBytes, tmV, fb, h * 64, (sg.kv0 + i - 1) * kBN, bh);
+        if constexpr (kV8) {   // V^T: keys are the innermost coordinate
+          tma_load_3d(dst, tmV, fb, (sg.kv0 + i - 1) * kBN, 0, bh);
+        } else {
+          for (int h = 0; h < 2; ++h)
+            tma_load_3d(dst + h * kBoxBytes, tmV, fb, h * 64, (sg.kv0 + i - 1) * kBN, bh);
+        }
         dst += kTileBytes;
       }
       if (has_k) {
@@ -709,7 +755,18 @@ __device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint32_t q_smem, uint3
 }
 
 // keys [64*half, 64*half + 64) of O += P V
+template <bool kPV8>
 __device__ __forceinline__ void issue_pv_half(uint32_t d_tmem, uint32_t p_tmem, uint32_t v_smem, int half, bool acc) {
+  if constexpr (kPV8) {
+    // P as E4M3 in TMEM (four keys per column: 32 keys = 8 columns per MMA) times V^T as
+    // E4M3 codes in shared memory (d rows of 128 keys, K-major like K for S): 32 keys
+    // (32 bytes of each V^T row) per MMA.
+    constexpr uint32_t idesc = idesc_e4m3();
+#pragma unroll
+    for (int kk = 2 * half; kk < 2 * half + 2; ++kk)
+      mma_ts_f8(d_tmem, p_tmem + kk * 8, sdesc_sw128(v_smem + kk * 32, 16, 1024), idesc, acc || kk > 0);
+    return;
+  }
   constexpr uint32_t idesc = idesc_bf16(true);
 #pragma unroll
   for (int kk = 4 * half; kk < 4 * half + 4; ++kk) {
@@ -727,7 +784,7 @@ __device__ __forceinline__ void issue_pv_half(uint32_t d_tmem, uint32_t p_tmem, 
 // about a hundred cycles (its queue is shallow), so a step does only the four P waits
 // and two commits: softmax threads check and release the ring slots.
 // Returns false when a wait gave up.
-template <bool kMore, bool kQK8>
+template <bool kMore, int kF8>
 __device__ __forceinline__ bool mma_step(const Ctl& c, uint32_t base, const uint32_t (&tS)[2],
                                          const uint32_t (&tO)[2], const uint32_t (&sQ)[2], int unit,
                                          uint32_t ph, bool first) {
@@ -738,10 +795,11 @@ __device__ __forceinline__ bool mma_step(const Ctl& c, uint32_t base, const uint
   // after a softmax thread has seen the unit loaded, so this wait covers the unit too.
   if (!wait_phase(c, kBarPFull + 0, ph, true)) return false;
   tc_fence_after();
-  issue_pv_half(tO[0], tS[0], sV, 0, !first);
+  constexpr bool kQK8 = kF8 >= 1, kPV8 = kF8 == 2;
+  issue_pv_half<kPV8>(tO[0], tS[0], sV, 0, !first);
   if (!wait_phase(c, kBarPFull + 1, ph, true)) return false;
   tc_fence_after();
-  issue_pv_half(tO[0], tS[0], sV, 1, true);
+  issue_pv_half<kPV8>(tO[0], tS[0], sV, 1, true);
   if (kMore) {
     issue_qk<kQK8>(tS[0], sQ[0], sK);
     tc_commit(c.bar(kBarSFull + 0));
@@ -751,10 +809,10 @@ __device__ __forceinline__ bool mma_step(const Ctl& c, uint32_t base, const uint
   // tile 1: O1 += P1 V_j, then S1 = Q1 K_{j+1}^T
   if (!wait_phase(c, kBarPFull + 2, ph, true)) return false;
   tc_fence_after();
-  issue_pv_half(tO[1], tS[1], sV, 0, !first);
+  issue_pv_half<kPV8>(tO[1], tS[1], sV, 0, !first);
   if (!wait_phase(c, kBarPFull + 3, ph, true)) return false;
   tc_fence_after();
-  issue_pv_half(tO[1], tS[1], sV, 1, true);
+  issue_pv_half<kPV8>(tO[1], tS[1], sV, 1, true);
   if (kMore) {
     issue_qk<kQK8>(tS[1], sQ[1], sK);
     tc_commit(c.bar(kBarSFull + 1));
@@ -764,7 +822,7 @@ __device__ __forceinline__ bool mma_step(const Ctl& c, uint32_t base, const uint
   return true;
 }
 
-template <bool kQK8>
+template <int kF8>
 __device__ void run_mma(const Ctl& c, uint32_t base, uint32_t tmem, const Params& p) {
   const uint32_t tS[2] = {tmem, tmem + 128};
   const uint32_t tO[2] = {tmem + 256, tmem + 384};
@@ -781,9 +839,9 @@ __device__ void run_mma(const Ctl& c, uint32_t base, uint32_t tmem, const Params
       break;
     tc_fence_after();
     const uint32_t sK = base + kOffKV + 2 * (unit % kPairs) * kTileBytes;   // unit {K_0}
-    issue_qk<kQK8>(tS[0], sQ[0], sK);
+    issue_qk<(kF8 >= 1)>(tS[0], sQ[0], sK);
     tc_commit(c.bar(kBarSFull + 0));
-    issue_qk<kQK8>(tS[1], sQ[1], sK);
+    issue_qk<(kF8 >= 1)>(tS[1], sQ[1], sK);
     tc_commit(c.bar(kBarSFull + 1));
     if (n == 1) tc_commit(c.bar(kBarQEmpty));   // the segment's last S MMA is issued
     // The segment's first P V products overwrite O: the previous segment's epilogue must
@@ -794,14 +852,14 @@ __device__ void run_mma(const Ctl& c, uint32_t base, uint32_t tmem, const Params
     bool ok = true;
     int j = 0;
     for (; j + 1 < n; ++j) {
-      if (!mma_step<true, kQK8>(c, base, tS, tO, sQ, unit + 1 + j, (gstep + j) & 1u, j == 0)) {
+      if (!mma_step<true, kF8>(c, base, tS, tO, sQ, unit + 1 + j, (gstep + j) & 1u, j == 0)) {
         ok = false;
         break;
       }
     }
     if (!ok) break;
     if (n > 1) tc_commit(c.bar(kBarQEmpty));   // the last S MMA (step n-2) is issued
-    if (!mma_step<false, kQK8>(c, base, tS, tO, sQ, unit + 1 + j, (gstep + j) & 1u, j == 0)) break;
+    if (!mma_step<false, kF8>(c, base, tS, tO, sQ, unit + 1 + j, (gstep + j) & 1u, j == 0)) break;
     unit += n + 1;
     gstep += static_cast<uint32_t>(n);
     ++u;
@@ -840,10 +898,11 @@ __device__ __forceinline__ void store_half_rows(uint8_t* stage, const uint32_t (
 // LSE = (M + log2 sum w_s l_s) * ln 2. Shares are visited in block order, so the
 // result does not depend on which share finished last.
 // When own_tO is non-zero the calling block's own share is still in TMEM (O at own_tO,
-// its max and sums in own_m, own_l, own_corr) and its record is not read.
+// its max and sums in own_m, own_l, own_corr) and its record is not read. O is also
+// multiplied by o_scale (V's descale factor when V is given as FP8 codes, else 1).
 __device__ void merge_split_row(const Params& p, int tile, int r, int c_first, int c_last, long long x0,
                                 uint8_t* stage, uint16_t* o_row0, int valid_rows, float* lse_out, uint32_t own_tO,
-                                float own_m, float own_l, float own_corr) {
+                                float own_m, float own_l, float own_corr, float o_scale) {
   const int self = own_tO != 0 ? static_cast<int>(blockIdx.x) : -1;
   const long long x0_grid = x0 * static_cast<long long>(gridDim.x);
   // share cs's record: its first segment's slot when its share starts inside this group
@@ -871,7 +930,7 @@ __device__ void merge_split_row(const Params& p, int tile, int r, int c_first, i
     L += l_s * w;
     Lr += (l_s + c_s) * w;
   }
-  const float inv = 1.0f / Lr;
+  const float inv = o_scale / Lr;   // o_scale: V's descale factor, else 1
   // Two 64-column halves; per half and share, the share's max and its 64 values are
   // requested together, so each share costs one round trip to L2 per half.
 #pragma unroll 1
@@ -915,8 +974,12 @@ __device__ void merge_split_row(const Params& p, int tile, int r, int c_first, i
   if (lse_out != nullptr) *lse_out = (M + log2f(L)) * 0.69314718055994531f;
 }
 
-template <bool kPosScale, bool kBias>
+// kP8: P is rounded to E4M3 (four keys per TMEM column) for an FP8 P V product; the
+// running max then moves once it grows by 8 (log2 units), so that every p <= 2^8 stays
+// below E4M3's largest value 448, and O is scaled by V's descale factor with 1 / l.
+template <bool kPosScale, bool kBias, bool kP8 = false>
 __device__ void run_softmax(const Ctl& c, uint32_t tmem, uint8_t* stage, const Params& p, int tile) {
+  constexpr float kTau = kP8 ? 8.0f : kRescaleLog2;
   const int quarter = (threadIdx.x >> 5) & 3;   // TMEM lanes this warp may access
   const int lane = threadIdx.x & 31;
   const int r = quarter * 32 + lane;            // query row within the tile
@@ -1028,7 +1091,7 @@ __device__ void run_softmax(const Ctl& c, uint32_t tmem, uint8_t* stage, const P
           fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])), fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) * cs;
       bool rescale = false;
       float alpha = 1.0f;
-      if (m_tile > m_used + kRescaleLog2) {
+      if (m_tile > m_used + kTau) {
         alpha = ex2(m_used - m_tile);   // 0 on the first step of a segment
         l *= alpha;
         corr *= alpha;
@@ -1054,7 +1117,10 @@ __device__ void run_softmax(const Ctl& c, uint32_t tmem, uint8_t* stage, const P
       {
         // (with a bias a row may have seen only -inf so far: its largest term is then 0)
         const float pm = (kBias && m_tile == -INFINITY) ? 0.0f : ex2(m_tile - m_used);
-        corr += __uint_as_float(pack_bf16(pm, 0.0f) << 16) - pm;
+        if constexpr (kP8)
+          corr += round_e4m3(pm) - pm;
+        else
+          corr += __uint_as_float(pack_bf16(pm, 0.0f) << 16) - pm;
       }
       // p = 2^(s*cs - m) in two halves of 64 keys; each half is rounded to BF16, stored
       // over S in TMEM and handed to the MMA warp at once, so the first half of the
@@ -1063,18 +1129,37 @@ __device__ void run_softmax(const Ctl& c, uint32_t tmem, uint8_t* stage, const P
       float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
-        uint32_t pk[32];
+        if constexpr (kP8) {   // 64 keys = 16 columns of four E4M3 values
+          uint32_t pk[16];
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const int e = half * 64 + 2 * i;
-          float e0, e1;
-          fma2(e0, e1, s[e], s[e + 1], cs, neg_m);
-          e0 = ex2(e0);
-          e1 = ex2(e1);
-          pk[i] = pack_bf16(e0, e1);
-          add2(acc[2 * (i & 3)], acc[2 * (i & 3) + 1], e0, e1);
+          for (int i = 0; i < 16; ++i) {
+            const int e = half * 64 + 4 * i;
+            float e0, e1, e2, e3;
+            fma2(e0, e1, s[e], s[e + 1], cs, neg_m);
+            fma2(e2, e3, s[e + 2], s[e + 3], cs, neg_m);
+            e0 = ex2(e0);
+            e1 = ex2(e1);
+            e2 = ex2(e2);
+            e3 = ex2(e3);
+            pk[i] = pack_e4m3x4(e0, e1, e2, e3);
+            add2(acc[2 * (i & 3)], acc[2 * (i & 3) + 1], e0, e1);
+            add2(acc[2 * ((i + 2) & 3)], acc[2 * ((i + 2) & 3) + 1], e2, e3);
+          }
+          tmem_st16(tS + half * 16, pk);
+        } else {
+          uint32_t pk[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const int e = half * 64 + 2 * i;
+            float e0, e1;
+            fma2(e0, e1, s[e], s[e + 1], cs, neg_m);
+            e0 = ex2(e0);
+            e1 = ex2(e1);
+            pk[i] = pack_bf16(e0, e1);
+            add2(acc[2 * (i & 3)], acc[2 * (i & 3) + 1], e0, e1);
+          }
+          tmem_st32(tS + half * 32, pk);
         }
-        tmem_st32(tS + half * 32, pk);
         tc_fence_before();
         __syncwarp();
         // (on expiry the abort flag is set and the block winds down; arriving is harmless)
@@ -1100,7 +1185,7 @@ __device__ void run_softmax(const Ctl& c, uint32_t tmem, uint8_t* stage, const P
     const size_t row_id = static_cast<size_t>(bh) * static_cast<size_t>(p.Nq) + static_cast<size_t>(qrow);
     uint16_t* o_row0 = p.o + (static_cast<size_t>(bh) * static_cast<size_t>(p.Nq) + static_cast<size_t>(qrow_w0)) * kD;
     if (!sg.split) {
-      const float inv_l = 1.0f / (l + corr);
+      const float inv_l = kP8 ? p.v_scale / (l + corr) : 1.0f / (l + corr);
       // O in one TMEM load; the accumulator is handed back to the MMA thread at once, so
       // the next segment's first P V products can run while this one's rows are stored.
       uint32_t ov[128];
@@ -1136,7 +1221,7 @@ __device__ void run_softmax(const Ctl& c, uint32_t tmem, uint8_t* stage, const P
         // from TMEM, without writing a record of its own.
         __threadfence();
         merge_split_row(p, tile, r, c_first, c_last, x0, stage, o_row0, valid_rows, live ? p.lse + row_id : nullptr,
-                        tO, m_used, l, corr);
+                        tO, m_used, l, corr, kP8 ? p.v_scale : 1.0f);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(c.bar(kBarOEmpty + tile));
@@ -1167,7 +1252,7 @@ __device__ void run_softmax(const Ctl& c, uint32_t tmem, uint8_t* stage, const P
         if (static_cast<int>(before) == c_last - c_first) {
           __threadfence();
           merge_split_row(p, tile, r, c_first, c_last, x0, stage, o_row0, valid_rows,
-                          live ? p.lse + row_id : nullptr, 0u, 0.0f, 0.0f, 0.0f);
+                          live ? p.lse + row_id : nullptr, 0u, 0.0f, 0.0f, 0.0f, kP8 ? p.v_scale : 1.0f);
         }
       }
     }
@@ -1179,7 +1264,7 @@ __device__ void run_softmax(const Ctl& c, uint32_t tmem, uint8_t* stage, const P
 // ---------------------------------------------------------------------------------
 // Kernel
 // ---------------------------------------------------------------------------------
-template <bool kPosScale, bool kBias, bool kQK8 = false>
+template <bool kPosScale, bool kBias, int kF8 = 0>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const Params p) {
@@ -1237,15 +1322,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp < 4) {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsCtl));
     if (warp == 0) {
-      if (lane == 0) run_producer<kQK8>(c, base, &tmQ, &tmK, &tmV, p);
+      if (lane == 0) run_producer<kF8>(c, base, &tmQ, &tmK, &tmV, p);
       __syncwarp();
     } else if (warp == 1) {
-      if (lane == 0) run_mma<kQK8>(c, base, tmem, p);
+      if (lane == 0) run_mma<kF8>(c, base, tmem, p);
       __syncwarp();
     }
   } else {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsSoftmax));
-    run_softmax<kPosScale, kBias>(c, tmem, smem + kOffStage + (warp - 4) * kStageBytes, p, (warp >> 2) - 1);
+    run_softmax<kPosScale, kBias, kF8 == 2>(c, tmem, smem + kOffStage + (warp - 4) * kStageBytes, p, (warp >> 2) - 1);
   }
 
   tc_fence_before();
@@ -1297,8 +1382,22 @@ bool make_map(CUtensorMap* map, const void* ptr, int rows, long long bh, bool co
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// V^T as 8-bit codes, [BH, 128, ldv] with keys innermost (Nk of each row of ldv used); box =
+// 128 keys x 128 rows of d x 1, one 128-byte swizzle span per row.
+bool make_map_vt(CUtensorMap* map, const void* ptr, int Nk, long long ldv, long long bh) {
+  auto enc = encoder();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(Nk), static_cast<cuuint64_t>(kD), static_cast<cuuint64_t>(bh)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(ldv), static_cast<cuuint64_t>(ldv) * kD};
+  cuuint32_t box[3] = {static_cast<cuuint32_t>(kBN), static_cast<cuuint32_t>(kD), 1};
+  cuuint32_t elem[3] = {1, 1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(ptr), dims, strides, box, elem,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 constexpr int kMaxDevices = 64;
-std::atomic<int> g_attr_done[8][kMaxDevices];   // per instantiation (kPos + 2 * kBias + 4 * kQK8)
+std::atomic<int> g_attr_done[12][kMaxDevices];   // per instantiation (kPos + 2 * kBias + 4 * kF8)
 std::atomic<int> g_sm_count[kMaxDevices];
 
 int sm_count(int dev) {
@@ -1383,11 +1482,11 @@ int get_workspace(int dev, cudaStream_t stream, size_t part_bytes, size_t cnt_by
   return ATTN_OK;
 }
 
-template <bool kPos, bool kBias = false, bool kQK8 = false>
+template <bool kPos, bool kBias = false, int kF8 = 0>
 int launch(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, const Params& p, int grid,
            int dev, cudaStream_t stream) {
-  auto kern = attn_fwd_kernel<kPos, kBias, kQK8>;
-  constexpr int kInst = (kPos ? 1 : 0) + (kBias ? 2 : 0) + (kQK8 ? 4 : 0);
+  auto kern = attn_fwd_kernel<kPos, kBias, kF8>;
+  constexpr int kInst = (kPos ? 1 : 0) + (kBias ? 2 : 0) + 4 * kF8;
   if (dev < 0 || dev >= kMaxDevices || !g_attr_done[kInst][dev].load(std::memory_order_acquire)) {
     // The in-kernel register split (setmaxnreg) balances only at kRegsLaunch registers
     // per thread; at any other count the increase would never be granted. Refuse.
@@ -1412,10 +1511,12 @@ struct BiasArg {
   long long sb, sh, sq;
 };
 
-// attn_fwd, attn_fwd_bias (bias != nullptr) and attn_fwd_fp8qk (qk8: q and k hold FP8 E4M3
-// codes): the argument rules, the plan, the launch.
+// attn_fwd, attn_fwd_bias (bias != nullptr), attn_fwd_fp8qk (f8 = 1: q and k hold FP8 E4M3
+// codes) and attn_fwd_fp8 (f8 = 2: v too, as V^T with row stride ldv, descaled by v_scale):
+// the argument rules, the plan, the launch.
 int forward(const void* q, const void* k, const void* v, const BiasArg* bias, void* o, float* lse, int B, int H,
-            int Nq, int Nk, int d, float scale, void* stream, bool qk8 = false) {
+            int Nq, int Nk, int d, float scale, void* stream, int f8 = 0, long long ldv = 0, float v_scale = 1.0f) {
+  const bool qk8 = f8 >= 1;
   if (B < 0 || H < 0 || Nq < 0 || Nk < 0) return ATTN_ERR_INVALID_ARG;
   if (d != kD) return ATTN_ERR_UNSUPPORTED;
   if (!std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
@@ -1433,6 +1534,13 @@ int forward(const void* q, const void* k, const void* v, const BiasArg* bias, vo
   // element counts must fit a signed 64-bit byte offset
   const long long max_rows = static_cast<long long>(Nq > Nk ? Nq : Nk);
   if (bh > (LLONG_MAX / 256) / max_rows) return ATTN_ERR_INVALID_ARG;
+  if (f8 == 2) {
+    // V^T rows of ldv bytes: at least Nk, 16-byte multiples (TMA strides), and the last
+    // byte's offset, bh * 128 * ldv, must fit a signed 64-bit offset
+    if (ldv < Nk) return ATTN_ERR_INVALID_ARG;
+    if (ldv % 16 != 0) return ATTN_ERR_MISALIGNED;
+    if (bh > (LLONG_MAX / kD) / ldv) return ATTN_ERR_INVALID_ARG;
+  }
   if (bias != nullptr) {
     if (!bias->ptr || bias->sb < 0 || bias->sh < 0 || bias->sq < 0) return ATTN_ERR_INVALID_ARG;
     // the last element's offset, (B-1) sb + (H-1) sh + (Nq-1) sq + Nk - 1, in bytes must fit int64
@@ -1452,7 +1560,8 @@ int forward(const void* q, const void* k, const void* v, const BiasArg* bias, vo
   if (sms <= 0) return ATTN_ERR_CUDA;
 
   CUtensorMap mq, mk, mv;
-  if (!make_map(&mq, q, Nq, bh, qk8) || !make_map(&mk, k, Nk, bh, qk8) || !make_map(&mv, v, Nk, bh))
+  if (!make_map(&mq, q, Nq, bh, qk8) || !make_map(&mk, k, Nk, bh, qk8) ||
+      !(f8 == 2 ? make_map_vt(&mv, v, Nk, ldv, bh) : make_map(&mv, v, Nk, bh)))
     return ATTN_ERR_CUDA;
 
   Params p;
@@ -1482,6 +1591,7 @@ int forward(const void* q, const void* k, const void* v, const BiasArg* bias, vo
   p.bias_sq = bias ? bias->sq : 0;
   p.H = H;
   p.scale = scale;
+  p.v_scale = v_scale;
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (pl.has_split) {
@@ -1493,9 +1603,12 @@ int forward(const void* q, const void* k, const void* v, const BiasArg* bias, vo
   }
   // with a bias the scale is applied before the row max, so one instantiation serves any sign
   if (bias != nullptr) return launch<true, true>(mq, mk, mv, p, pl.grid, dev, s);
+  if (f8 == 2)
+    return scale > 0.0f ? launch<true, false, 2>(mq, mk, mv, p, pl.grid, dev, s)
+                        : launch<false, false, 2>(mq, mk, mv, p, pl.grid, dev, s);
   if (qk8)
-    return scale > 0.0f ? launch<true, false, true>(mq, mk, mv, p, pl.grid, dev, s)
-                        : launch<false, false, true>(mq, mk, mv, p, pl.grid, dev, s);
+    return scale > 0.0f ? launch<true, false, 1>(mq, mk, mv, p, pl.grid, dev, s)
+                        : launch<false, false, 1>(mq, mk, mv, p, pl.grid, dev, s);
   return scale > 0.0f ? launch<true>(mq, mk, mv, p, pl.grid, dev, s) : launch<false>(mq, mk, mv, p, pl.grid, dev, s);
 }
 
@@ -1523,7 +1636,20 @@ extern "C" int attn_fwd_fp8qk(const void* q8, const void* k8, const void* v, voi
     return ATTN_ERR_INVALID_ARG;
   const double eff = static_cast<double>(scale) * q_descale * k_descale;
   if (!(std::fabs(eff) <= static_cast<double>(FLT_MAX))) return ATTN_ERR_INVALID_ARG;
-  return forward(q8, k8, v, nullptr, o, lse, B, H, Nq, Nk, d, static_cast<float>(eff), stream, true);
+  return forward(q8, k8, v, nullptr, o, lse, B, H, Nq, Nk, d, static_cast<float>(eff), stream, 1);
+}
+
+extern "C" int attn_fwd_fp8(const void* q8, const void* k8, const void* vt8, long long ldv, void* o, float* lse,
+                            int B, int H, int Nq, int Nk, int d, float scale, float q_descale, float k_descale,
+                            float v_descale, void* stream) {
+  // S = scale * q_descale * k_descale * (Q8 K8^T) as in attn_fwd_fp8qk; O = v_descale * P8 V8
+  // with P rounded to E4M3 and the sum l of the unrounded weights.
+  if (!std::isfinite(scale) || !std::isfinite(q_descale) || !std::isfinite(k_descale) ||
+      !std::isfinite(v_descale) || !(q_descale > 0.0f) || !(k_descale > 0.0f) || !(v_descale > 0.0f))
+    return ATTN_ERR_INVALID_ARG;
+  const double eff = static_cast<double>(scale) * q_descale * k_descale;
+  if (!(std::fabs(eff) <= static_cast<double>(FLT_MAX))) return ATTN_ERR_INVALID_ARG;
+  return forward(q8, k8, vt8, nullptr, o, lse, B, H, Nq, Nk, d, static_cast<float>(eff), stream, 2, ldv, v_descale);
 }
 
 extern "C" int attn_fwd_causal(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,

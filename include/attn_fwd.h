@@ -156,6 +156,34 @@ int attn_fwd_fp8qk(const void* q8, const void* k8, const void* v, void* o, float
                    void* stream);
 
 /*
+ * attn_fwd_fp8 -- attention forward with both products in 8-bit floating point.
+ *
+ * As attn_fwd_fp8qk, and V arrives as E4M3 codes too, with its own positive descale factor:
+ *
+ *     O = v_descale * (P8 V8) / l,   P8 = the weights p_j rounded to E4M3,
+ *
+ * where l sums the unrounded weights (plus the rounding error of each tile's largest one),
+ * so the LSE is exactly that of attn_fwd_fp8qk. Rounding P to E4M3 (3 mantissa bits;
+ * weights below 2^-6 of the running maximum lose precision, below 2^-10 they vanish) is
+ * the price of the FP8 P V product: O is close to the definition only to within a few
+ * 1e-2 on N(0,1) inputs and about 1e-1 on sharply peaked rows, versus 1e-2 for the BF16
+ * path.
+ *
+ *   vt8    device, V^T as E4M3 codes: [B, H, d, ldv] bytes, keys innermost; key j of row c
+ *          of head (b, h) at vt8[((b * H + h) * d + c) * ldv + j]. Bytes from Nk to ldv of
+ *          each row are not read.
+ *   ldv    row stride of vt8 in bytes: ldv >= Nk (else ATTN_ERR_INVALID_ARG), a multiple
+ *          of 16 (else ATTN_ERR_MISALIGNED); the tensor cores read V with keys contiguous
+ *   v_descale   finite and > 0 (else ATTN_ERR_INVALID_ARG)
+ *
+ * Everything else (q8, k8, their descale factors, o, lse, sizes, alignment, work split,
+ * workspace, return values) is as attn_fwd_fp8qk.
+ */
+int attn_fwd_fp8(const void* q8, const void* k8, const void* vt8, long long ldv, void* o, float* lse,
+                 int B, int H, int Nq, int Nk, int d, float scale, float q_descale, float k_descale,
+                 float v_descale, void* stream);
+
+/*
  * attn_fwd_noalloc -- attn_fwd for callers that cannot allocate device memory.
  *
  * There is no counterpart on the pages: this is a service of the library. Some callers

@@ -26,7 +26,7 @@ def declared_functions():
 
 def test_header_declares_the_entry_points():
     names = declared_functions()
-    assert {"attn_fwd", "attn_fwd_causal", "attn_fwd_bias", "attn_fwd_fp8qk", "attn_fwd_noalloc", "attn_bwd", "attn_bwd_causal",
+    assert {"attn_fwd", "attn_fwd_causal", "attn_fwd_bias", "attn_fwd_fp8qk", "attn_fwd_fp8", "attn_fwd_noalloc", "attn_bwd", "attn_bwd_causal",
             "attn_bwd_status", "attn_bwd_set_wait_limit",
             "attn_bwd_kernel_count", "attn_fwd_status", "attn_status_string",
             "attn_fwd_set_wait_limit", "attn_fwd_kernel_count"} <= set(names)
@@ -158,6 +158,30 @@ def test_fp8qk_binding_checks_types():
         attn.attn_fwd_fp8qk(torch.zeros(1, 1, 128, 128, dtype=torch.uint8), A, A, A, A, 1, 1, 128, 128, 128, 0.1)
     with pytest.raises(attn.AttnError):
         attn.attn_fwd_fp8qk(A, A, A, A, A, 1, 1, 128, 128, 128, 0.1, q_descale=0.0)
+
+
+def call_fp8pv(q8=A, k8=A, vt8=A, ldv=128, o=A, lse=A, B=1, H=1, Nq=128, Nk=128, d=128, scale=0.125, dq=0.01,
+               dk=0.02, dv=0.03):
+    return attn.load_library().attn_fwd_fp8(q8, k8, vt8, ldv, o, lse, B, H, Nq, Nk, d, scale, dq, dk, dv, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(dv=0.0), attn.ATTN_ERR_INVALID_ARG),
+    (dict(dv=math.inf), attn.ATTN_ERR_INVALID_ARG),
+    (dict(dq=-1.0), attn.ATTN_ERR_INVALID_ARG),
+    (dict(ldv=120), attn.ATTN_ERR_INVALID_ARG),              # shorter than Nk
+    (dict(ldv=136, Nk=130), attn.ATTN_ERR_MISALIGNED),       # rows not on 16-byte boundaries
+    (dict(ldv=1 << 60, B=1 << 10), attn.ATTN_ERR_INVALID_ARG),   # offsets overflow
+    (dict(vt8=None), attn.ATTN_ERR_INVALID_ARG),
+    (dict(vt8=A + 8), attn.ATTN_ERR_MISALIGNED),
+    (dict(d=64), attn.ATTN_ERR_UNSUPPORTED),
+    (dict(Nk=0), attn.ATTN_ERR_INVALID_ARG),
+    (dict(B=0), attn.ATTN_OK),
+])
+def test_fp8_argument_checks(kw, code):
+    before = attn.attn_fwd_kernel_count()
+    assert call_fp8pv(**kw) == code
+    assert attn.attn_fwd_kernel_count() == before
 
 
 def test_bias_binding_checks_shapes():

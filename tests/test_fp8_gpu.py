@@ -1,9 +1,10 @@
 """GPU parity of attn_fwd_fp8qk (Q and K as FP8 E4M3 codes with per-tensor descale factors)
-against the FP64 oracle on the same codes.
+and attn_fwd_fp8 (V too) against the FP64 oracle on the same codes.
 
-The tensor cores form each product of two E4M3 values exactly and sum them in FP32, as they
-do for BF16 inputs, so the tolerance is the forward's own: max|dO| <= 1e-2, mean|dO| <= 1e-3,
-LSE relative error <= 1e-4 (tests/parity.py).
+attn_fwd_fp8qk: the tensor cores form each product of two E4M3 values exactly and sum them
+in FP32, as they do for BF16 inputs, so the tolerance is the forward's own: max|dO| <= 1e-2,
+mean|dO| <= 1e-3, LSE relative error <= 1e-4 (tests/parity.py). attn_fwd_fp8 also rounds P
+to E4M3; its tolerance is derived below.
 """
 import math
 
@@ -89,4 +90,108 @@ def test_fp8qk_is_deterministic(gpu_lib):
     q8, k8, v, dq, dk = make_qk_e4m3(1, 2, 256, 5120, seed=13400)
     a = run_fp8(gpu_lib, q8, k8, v, SCALE, dq, dk)
     b = run_fp8(gpu_lib, q8, k8, v, SCALE, dq, dk)
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+
+
+# ---- attn_fwd_fp8: V as E4M3 codes too, P rounded to E4M3 for the P V product ----------------
+#
+# Tolerance. P rounded to E4M3 keeps 3 mantissa bits: each weight moves by up to 2^-4 of
+# itself, weights below 2^-6 of the running maximum keep fewer bits and those below 2^-10
+# vanish. A CPU emulation of the kernel's rounding points (FP32 scores and weights, the
+# running maximum moved in steps of more than 8 in log2 units, P rounded to E4M3, l the
+# FP32 sum of the unrounded weights plus the rounding error of each tile's largest, BF16
+# output) against the FP64 definition on exactly the inputs below gives at most 1.85e-2
+# (max) and 2.5e-3 (mean) on N(0,1) inputs, and 9.2e-2 / 4.3e-3 on the peaked (x3) ones.
+# The bounds are about twice that. A P byte in the wrong key position, V's descale dropped
+# or V read from the wrong rows moves O by 1e-1 or more on average. The LSE does not depend
+# on P's rounding and keeps the forward's 1e-4.
+
+def fp8pv_tolerance(qk_mult):
+    return (4e-2, 5e-3) if qk_mult == 1.0 else (2e-1, 1e-2)
+
+
+def run_fp8pv(attn, q8, k8, v8, scale, dq, dk, dv, ldv=None, pad_code=0x7F):
+    """v8 is key-major [B,H,Nk,d]; the kernel gets V^T [B,H,d,ldv] with the bytes past Nk of
+    each row set to pad_code (NaN by default: a read of them would show in O)."""
+    import torch
+    B, H, Nq, d = q8.shape
+    Nk = k8.shape[2]
+    ldv = ldv or (Nk + 15) // 16 * 16
+    vt = np.full((B, H, d, ldv), pad_code, dtype=np.uint8)
+    vt[..., :Nk] = np.swapaxes(v8, 2, 3)
+    o = torch.full((B, H, Nq, d), float("nan"), dtype=torch.bfloat16, device="cuda")
+    lse = torch.full((B, H, Nq), float("nan"), dtype=torch.float32, device="cuda")
+    attn.attn_fwd_fp8(torch.from_numpy(np.ascontiguousarray(q8)).cuda(), torch.from_numpy(np.ascontiguousarray(k8)).cuda(),
+                      torch.from_numpy(vt).cuda().view(torch.float8_e4m3fn), o, lse, B, H, Nq, Nk, d, scale, dq, dk, dv)
+    assert attn.attn_fwd_status() == attn.ATTN_OK
+    return bf16_to_np(o), lse.cpu().numpy()
+
+
+def check_fp8pv(attn, B, H, Nq, Nk, seed, qk_mult=1.0, scale=SCALE, rows=None, ldv=None):
+    from dense_attention_forward_fwd_gb300.inputs import make_qkv_e4m3
+    q8, k8, v8, dq, dk, dv = make_qkv_e4m3(B, H, Nq, Nk, seed=seed, qk_mult=qk_mult)
+    o, lse = run_fp8pv(attn, q8, k8, v8, scale, dq, dk, dv, ldv)
+    o_ref, lse_ref = oracle.attention_rows_e4m3(q8, k8, v8, scale, dq, dk, dv, rows)
+    o, lse = o.reshape(-1, 128), lse.reshape(-1)
+    if rows is not None:
+        o, lse = o[rows], lse[rows]
+    assert np.all(np.isfinite(o)) and np.all(np.isfinite(lse)), "non-finite output"
+    err = np.abs(o.astype(np.float64) - o_ref)
+    lse_err = np.abs(lse.astype(np.float64) - lse_ref) / np.maximum(1.0, np.abs(lse_ref))
+    t_max, t_mean = fp8pv_tolerance(qk_mult)
+    assert err.max() <= t_max and err.mean() <= t_mean and lse_err.max() <= 1e-4, \
+        f"max {err.max():.3e} mean {err.mean():.3e} lse {lse_err.max():.3e}"
+    return err.max(), err.mean()
+
+
+@pytest.mark.parametrize("B,H,Nq,Nk", [
+    (1, 1, 128, 128),
+    (1, 2, 256, 384),
+    (2, 3, 300, 1000),     # ragged tails; V^T rows padded to 1008 bytes
+    (1, 1, 1, 200),
+    (1, 2, 129, 129),
+    (1, 2, 256, 5120),     # key steps split across blocks
+    (4, 2, 768, 768),
+])
+def test_fp8_full_parity(gpu_lib, B, H, Nq, Nk):
+    check_fp8pv(gpu_lib, B, H, Nq, Nk, seed=14000 + Nq + Nk)
+
+
+def test_fp8_peaked_scores(gpu_lib):
+    check_fp8pv(gpu_lib, 1, 2, 512, 2048, seed=14100, qk_mult=3.0)
+
+
+@pytest.mark.parametrize("scale", [0.0, -0.0883883461356163])
+def test_fp8_other_scales(gpu_lib, scale):
+    check_fp8pv(gpu_lib, 1, 2, 256, 640, seed=14200, scale=scale)
+
+
+def test_fp8_wide_value_rows(gpu_lib):
+    # ldv well past Nk: the rows' tails (NaN codes) are never read
+    check_fp8pv(gpu_lib, 1, 2, 256, 300, seed=14300, ldv=512)
+
+
+@pytest.mark.parametrize("name", ["rect-4k-8k", "square-4k"])
+def test_fp8_workload_sampled_rows(gpu_lib, name):
+    w = by_name(name)
+    rows = sample_rows(w.B, w.H, w.Nq, per_head=16)
+    check_fp8pv(gpu_lib, w.B, w.H, w.Nq, w.Nk, seed=w.seed, scale=w.scale, rows=rows)
+
+
+def test_fp8_lse_matches_the_fp8_score_entry_point(gpu_lib):
+    # same scores, same row sums: only the rounding order of l differs between the two
+    from dense_attention_forward_fwd_gb300.inputs import make_qkv_e4m3
+    q8, k8, v8, dq, dk, dv = make_qkv_e4m3(1, 2, 384, 1000, seed=14400)
+    _, l8 = run_fp8pv(gpu_lib, q8, k8, v8, SCALE, dq, dk, dv)
+    vb = (oracle.e4m3_to_f64(v8) * dv).astype(np.float32)
+    from dense_attention_forward_fwd_gb300.inputs import f32_to_bf16_bits
+    _, lq = run_fp8(gpu_lib, q8, k8, f32_to_bf16_bits(vb), SCALE, dq, dk)
+    assert np.max(np.abs(l8 - lq) / np.maximum(1.0, np.abs(lq))) <= 1e-5
+
+
+def test_fp8_is_deterministic(gpu_lib):
+    from dense_attention_forward_fwd_gb300.inputs import make_qkv_e4m3
+    q8, k8, v8, dq, dk, dv = make_qkv_e4m3(1, 2, 256, 5120, seed=14500)
+    a = run_fp8pv(gpu_lib, q8, k8, v8, SCALE, dq, dk, dv)
+    b = run_fp8pv(gpu_lib, q8, k8, v8, SCALE, dq, dk, dv)
     assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
