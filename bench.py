@@ -141,6 +141,29 @@ def measured_peaks():
     return {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}, "fallback"
 
 
+def roofline_peak(args, peaks: dict, peak_src: str):
+    """(peak TFLOP/s, description) of the timed kernel's tensor work. Every FLOP of the BF16
+    kernels runs at the measured BF16 burst rate (each launch is timed alone). FP8 MMAs run
+    at twice that, the nominal 4.5 / 2.25 PFLOP/s ratio: with FP8 scores only, half the FLOPs
+    (Q K^T) do, which gives the harmonic mean 2 / (1/(2P) + 1/P) = 4P/3; with FP8 scores and
+    values, all of them (2P)."""
+    peak = float(peaks["bf16_tflops"])
+    if args.fp8_qk:
+        return (2.0 / (1.0 / (2.0 * peak) + 1.0 / peak),
+                f"half the FLOPs at 2 x {peak_src} bf16_tflops (FP8 E4M3, nominal ratio 4.5/2.25), "
+                "half at bf16_tflops (burst)")
+    if args.fp8:
+        return 2.0 * peak, f"2 x {peak_src} bf16_tflops (FP8 E4M3, nominal ratio 4.5/2.25; burst)"
+    return peak, f"{peak_src} bf16_tflops (burst: each launch is timed alone)"
+
+
+def traffic_key(w, args) -> str:
+    """The profiles/traffic.json key of this run's kernel and workload."""
+    return (w.name + ("-causal" if args.causal else "") + ("" if args.bias == "none" else "-bias-" + args.bias)
+            + ("-backward" if args.backward else "") + ("-fp8qk" if args.fp8_qk else "")
+            + ("-fp8" if args.fp8 else ""))
+
+
 def host_cores() -> int:
     try:
         return len(os.sched_getaffinity(0))
@@ -540,22 +563,11 @@ def run_ours(args, w):
     value = job_tflops(flops, world, ms)
     e2e_value = job_tflops(flops, world, e2e_ms)
 
-    peaks, peak_src = measured_peaks()
-    peak = float(peaks["bf16_tflops"])
-    peak_note = f"{peak_src} bf16_tflops (burst: each launch is timed alone)"
-    if args.fp8_qk:   # Q K^T (half the FLOPs) at the FP8 rate, 2x BF16 nominally; P V at the BF16 rate
-        peak = 2.0 / (1.0 / (2.0 * peak) + 1.0 / peak)
-        peak_note = (f"half the FLOPs at 2 x {peak_src} bf16_tflops (FP8 E4M3, nominal ratio 4.5/2.25), "
-                     "half at bf16_tflops (burst)")
-    if args.fp8:   # both products at the FP8 rate
-        peak = 2.0 * peak
-        peak_note = f"2 x {peak_src} bf16_tflops (FP8 E4M3, nominal ratio 4.5/2.25; burst)"
+    peak, peak_note = roofline_peak(args, *measured_peaks())
     achieved = flops / (ms * 1e-3) / 1e12   # one launch on one GPU
     traffic = None
     if os.path.exists(TRAFFIC_FILE):
-        key = (w.name + ("-causal" if args.causal else "") + ("" if args.bias == "none" else "-bias-" + args.bias)
-               + ("-backward" if args.backward else "") + ("-fp8qk" if args.fp8_qk else "")
-               + ("-fp8" if args.fp8 else ""))
+        key = traffic_key(w, args)
         rec = json.load(open(TRAFFIC_FILE)).get(key)
         if rec and rec.get("kernel_hash") == kernel_hash(args.backward):
             traffic = rec.get("bytes_per_launch")
