@@ -31,6 +31,7 @@ __all__ = [
     "make_bias",
     "make_qk_e4m3",
     "make_qkv_e4m3",
+    "make_qkv_mxfp8",
     "BF16_NEG_INF",
     "sample_rows",
 ]
@@ -114,6 +115,49 @@ def make_qkv_e4m3(B: int, H: int, Nq: int, Nk: int, d: int = 128, seed: int = 0,
     dv = np.float32(amax / 448.0) if amax > 0 else np.float32(1.0)
     v8 = torch.from_numpy(np.ascontiguousarray(v / dv)).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
     return q8, k8, v8, dq, dk, float(dv)
+
+
+def _mx_blocks(x: np.ndarray, axis: int):
+    """Quantize float32 x to E4M3 codes with one E8M0 scale per 32 elements along ``axis``
+    (the last block may be shorter): shared exponent floor(log2(amax)) - 8 (8 being E4M3's
+    largest exponent), elements x / 2^exponent saturated to +-448 and rounded by torch's
+    nearest-even conversion. Returns (codes uint8 like x, scales uint8 with that axis
+    shrunk to ceil(n / 32))."""
+    import torch
+    x = np.moveaxis(np.asarray(x, dtype=np.float32), axis, -1)
+    n = x.shape[-1]
+    nb = (n + 31) // 32
+    pad = np.zeros(x.shape[:-1] + (nb * 32,), dtype=np.float32)
+    pad[..., :n] = x
+    blocks = pad.reshape(x.shape[:-1] + (nb, 32))
+    amax = np.abs(blocks).max(axis=-1)
+    exp = np.where(amax > 0, np.floor(np.log2(np.where(amax > 0, amax, 1.0))) - 8, 0).astype(np.int64)
+    exp = np.clip(exp, -127, 127)
+    scaled = np.clip(blocks / np.ldexp(np.float32(1), exp)[..., None].astype(np.float32), -448.0, 448.0)
+    codes = torch.from_numpy(np.ascontiguousarray(scaled, dtype=np.float32)).to(torch.float8_e4m3fn)
+    codes = codes.view(torch.uint8).numpy().reshape(pad.shape)[..., :n]
+    return np.ascontiguousarray(np.moveaxis(codes, -1, axis)), \
+        np.ascontiguousarray(np.moveaxis((exp + 127).astype(np.uint8), -1, axis))
+
+
+def make_qkv_mxfp8(B: int, H: int, Nq: int, Nk: int, d: int = 128, seed: int = 0, qk_mult: float = 1.0):
+    """Q, K and V in MXFP8: the float32 normals of :func:`make_qkv` (same seed) as E4M3 codes
+    with E8M0 scales per 32 elements along d for Q and K and per 32 keys for V (the
+    dimensions the two products contract over). Returns (q8, sq, k8, sk, v8, sv) with
+    shapes [B,H,Nq,d], [B,H,Nq,d/32], [B,H,Nk,d], [B,H,Nk,d/32], [B,H,Nk,d],
+    [B,H,ceil(Nk/32),d]."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    q = rng.standard_normal((B, H, Nq, d), dtype=np.float32)
+    k = rng.standard_normal((B, H, Nk, d), dtype=np.float32)
+    v = rng.standard_normal((B, H, Nk, d), dtype=np.float32)
+    if qk_mult != 1.0:
+        m = np.float32(qk_mult)
+        q = q * m
+        k = k * m
+    q8, sq = _mx_blocks(q, 3)
+    k8, sk = _mx_blocks(k, 3)
+    v8, sv = _mx_blocks(v, 2)
+    return q8, sq, k8, sk, v8, sv
 
 
 def make_bias(shape, seed: int, std: float = 1.0) -> np.ndarray:

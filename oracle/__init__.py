@@ -20,7 +20,7 @@ import numpy as np
 
 __all__ = ["build", "Oracle", "default", "attention_rows", "attention_rows_causal", "attention_rows_bias",
            "attention", "attention_dense", "attention_bwd", "probs", "max_threads", "LIB_PATH",
-           "attention_rows_e4m3qk", "attention_rows_e4m3", "e4m3_to_f64"]
+           "attention_rows_e4m3qk", "attention_rows_e4m3", "attention_rows_mxfp8", "e4m3_to_f64", "e8m0_to_f64"]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "attn_ref.c")
@@ -62,6 +62,11 @@ class Oracle:
         lib.attn_ref_rows_e4m3_f64.argtypes = [vp, vp, vp, i64, i64, i64, i64, i64, dbl, dbl, dbl, dbl, vp, i64,
                                                vp, vp, ctypes.c_int]
         lib.attn_ref_rows_e4m3_f64.restype = ctypes.c_int
+        lib.attn_ref_rows_mxfp8_f64.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, dbl, vp, i64, vp,
+                                                vp, ctypes.c_int]
+        lib.attn_ref_rows_mxfp8_f64.restype = ctypes.c_int
+        lib.attn_ref_e8m0_to_f64.argtypes = [vp, i64, vp]
+        lib.attn_ref_e8m0_to_f64.restype = None
         lib.attn_ref_e4m3_to_f64.argtypes = [vp, i64, vp]
         lib.attn_ref_e4m3_to_f64.restype = None
         lib.attn_ref_dense_f64.argtypes = [vp, vp, vp, i64, i64, i64, i64, i64, dbl, vp, vp]
@@ -207,6 +212,40 @@ class Oracle:
             raise ValueError(f"attn_ref_rows_e4m3_f64 failed with status {rc}")
         return o, lse
 
+    def e8m0_to_f64(self, codes):
+        """Values 2^(e - 127) of E8M0 scale codes (uint8 array of any shape); NaN for 255."""
+        c = np.ascontiguousarray(codes, dtype=np.uint8)
+        out = np.empty(c.shape, dtype=np.float64)
+        self.lib.attn_ref_e8m0_to_f64(_ptr(c), c.size, _ptr(out))
+        return out
+
+    def attention_rows_mxfp8(self, q8, sq, k8, sk, v8, sv, scale: float, rows=None, nthreads: int = 0):
+        """O and LSE (float64) of selected rows from MXFP8 inputs: E4M3 codes q8 [B,H,Nq,d],
+        k8 [B,H,Nk,d], v8 [B,H,Nk,dv] with E8M0 block scales sq [B,H,Nq,d/32] and
+        sk [B,H,Nk,d/32] (32 elements along d) and sv [B,H,ceil(Nk/32),dv] (32 keys per column)."""
+        arrs = [np.ascontiguousarray(a) for a in (q8, sq, k8, sk, v8, sv)]
+        if any(a.dtype != np.uint8 for a in arrs):
+            raise TypeError("MXFP8 codes and scales must be uint8")
+        q8, sq, k8, sk, v8, sv = arrs
+        B, H, Nq, d = q8.shape
+        Nk, dv = k8.shape[2], v8.shape[3]
+        if (k8.shape != (B, H, Nk, d) or v8.shape[:3] != (B, H, Nk) or d % 32 != 0
+                or sq.shape != (B, H, Nq, d // 32) or sk.shape != (B, H, Nk, d // 32)
+                or sv.shape != (B, H, (Nk + 31) // 32, dv)):
+            raise ValueError(f"shape mismatch q8{q8.shape} sq{sq.shape} k8{k8.shape} sk{sk.shape} v8{v8.shape} "
+                             f"sv{sv.shape}")
+        if rows is None:
+            rows = np.arange(B * H * Nq, dtype=np.int64)
+        rows = np.ascontiguousarray(rows, dtype=np.int64)
+        o = np.empty((rows.size, dv), dtype=np.float64)
+        lse = np.empty(rows.size, dtype=np.float64)
+        rc = self.lib.attn_ref_rows_mxfp8_f64(_ptr(q8), _ptr(sq), _ptr(k8), _ptr(sk), _ptr(v8), _ptr(sv), B * H, Nq,
+                                              Nk, d, dv, float(scale), _ptr(rows), rows.size, _ptr(o), _ptr(lse),
+                                              int(nthreads))
+        if rc != 0:
+            raise ValueError(f"attn_ref_rows_mxfp8_f64 failed with status {rc}")
+        return o, lse
+
     def attention(self, q, k, v, scale: float, nthreads: int = 0):
         """Full O [B,H,Nq,dv] and LSE [B,H,Nq] in float64."""
         B, H, Nq, _ = q.shape
@@ -323,6 +362,14 @@ def attention_rows_e4m3qk(q8, k8, v, scale: float, q_descale: float = 1.0, k_des
 def attention_rows_e4m3(q8, k8, v8, scale: float, q_descale: float = 1.0, k_descale: float = 1.0,
                         v_descale: float = 1.0, rows=None, nthreads: int = 0):
     return default().attention_rows_e4m3(q8, k8, v8, scale, q_descale, k_descale, v_descale, rows, nthreads)
+
+
+def e8m0_to_f64(codes):
+    return default().e8m0_to_f64(codes)
+
+
+def attention_rows_mxfp8(q8, sq, k8, sk, v8, sv, scale: float, rows=None, nthreads: int = 0):
+    return default().attention_rows_mxfp8(q8, sq, k8, sk, v8, sv, scale, rows, nthreads)
 
 
 def attention(q, k, v, scale: float, nthreads: int = 0):

@@ -642,3 +642,94 @@ int attn_ref_rows_e4m3_f64(const uint8_t *q8, const uint8_t *k8, const uint8_t *
     }
     return failed ? REF_ENOMEM : REF_OK;
 }
+
+/*
+ * MXFP8 inputs (the "MXFP8" of "Flash Attention на 5090 в CUDA C++", section "Что дальше").
+ *
+ * Read as the OCP microscaling format: E4M3 elements in blocks of 32 along the dimension a
+ * product contracts over, each block with one E8M0 scale, an unsigned 8-bit exponent e
+ * standing for 2^(e - 127) (e = 255 is NaN). The real inputs are
+ *   q[i,c] = 2^(sq[i, c/32] - 127) * E4M3(q8[i,c])        blocks along d
+ *   k[j,c] = 2^(sk[j, c/32] - 127) * E4M3(k8[j,c])        blocks along d
+ *   v[j,c] = 2^(sv[j/32, c] - 127) * E4M3(v8[j,c])        blocks along the keys
+ * and the definition is applied to them unchanged.
+ */
+static double e8m0_to_f64(uint8_t e)
+{
+    if (e == 255) return NAN;
+    return ldexp(1.0, (int)e - 127);
+}
+
+/* attn_ref_e8m0_to_f64: decode n scale codes (for the pins). */
+void attn_ref_e8m0_to_f64(const uint8_t *codes, int64_t n, double *out)
+{
+    for (int64_t i = 0; i < n; i++) out[i] = e8m0_to_f64(codes[i]);
+}
+
+/*
+ * attn_ref_rows_mxfp8_f64: O and LSE of selected rows from MXFP8 Q, K and V.
+ *
+ *   q8 [BH, Nq, d], k8 [BH, Nk, d], v8 [BH, Nk, dv]   E4M3 codes, C order
+ *   sq [BH, Nq, d/32], sk [BH, Nk, d/32]              E8M0 scales of 32 elements along d
+ *   sv [BH, ceil(Nk/32), dv]                          E8M0 scales of 32 keys per column
+ * d must be a multiple of 32. Other arguments and the return value as attn_ref_rows_f64.
+ */
+int attn_ref_rows_mxfp8_f64(const uint8_t *q8, const uint8_t *sq, const uint8_t *k8, const uint8_t *sk,
+                            const uint8_t *v8, const uint8_t *sv,
+                            int64_t BH, int64_t Nq, int64_t Nk, int64_t d, int64_t dv, double scale,
+                            const int64_t *sel, int64_t nsel, double *o, double *lse, int nthreads)
+{
+    if (BH < 0 || Nq < 0 || Nk < 1 || d < 32 || d % 32 != 0 || dv < 1 || nsel < 0) return REF_EINVAL;
+    if (nsel == 0) return REF_OK;
+    if (!q8 || !sq || !k8 || !sk || !v8 || !sv || !sel || !o || !lse) return REF_EINVAL;
+    for (int64_t r = 0; r < nsel; r++)
+        if (sel[r] < 0 || sel[r] >= BH * Nq) return REF_EINVAL;
+    const int64_t db = d / 32, kb = (Nk + 31) / 32;
+
+    int failed = 0;
+#ifdef _OPENMP
+    int nt = nthreads > 0 ? nthreads : omp_get_max_threads();
+#pragma omp parallel num_threads(nt)
+#else
+    (void)nthreads;
+#endif
+    {
+        double *sc = (double *)malloc((size_t)Nk * sizeof(double));
+        if (!sc) {
+#ifdef _OPENMP
+#pragma omp atomic write
+#endif
+            failed = 1;
+        } else {
+#ifdef _OPENMP
+#pragma omp for schedule(dynamic, 1)
+#endif
+            for (int64_t r = 0; r < nsel; r++) {
+                int64_t bh = sel[r] / Nq, i = sel[r] % Nq;
+                const uint8_t *qi = q8 + (bh * Nq + i) * d, *qs = sq + (bh * Nq + i) * db;
+                const uint8_t *kh = k8 + bh * Nk * d, *ks = sk + bh * Nk * db;
+                const uint8_t *vh = v8 + bh * Nk * dv, *vs = sv + bh * kb * dv;
+                /* step 1 on the real inputs */
+                for (int64_t j = 0; j < Nk; j++) {
+                    double dot = 0.0;
+                    for (int64_t c = 0; c < d; c++)
+                        dot += (e8m0_to_f64(qs[c / 32]) * e4m3_to_f64(qi[c])) *
+                               (e8m0_to_f64(ks[j * db + c / 32]) * e4m3_to_f64(kh[j * d + c]));
+                    sc[j] = scale * dot;
+                }
+                /* steps 2-5 with the real values */
+                double top = row_max(sc, Nk);
+                double den = row_exp_sum(sc, Nk, top);
+                for (int64_t c = 0; c < dv; c++) {
+                    double num = 0.0;
+                    for (int64_t j = 0; j < Nk; j++)
+                        num += sc[j] * (e8m0_to_f64(vs[(j / 32) * dv + c]) * e4m3_to_f64(vh[j * dv + c]));
+                    o[r * dv + c] = num / den;
+                }
+                lse[r] = top + log(den);
+            }
+            free(sc);
+        }
+    }
+    return failed ? REF_ENOMEM : REF_OK;
+}

@@ -43,3 +43,25 @@ def test_sample_rows():
     per_head = np.bincount(r // 16384, minlength=16)
     assert np.all(per_head >= 64)
     assert np.array_equal(r, sample_rows(1, 16, 16384, per_head=64))
+
+
+def test_mxfp8_inputs_use_each_block_s_range_and_round_closely():
+    # per block of 32 along the contraction axis: the shared exponent puts the block's largest
+    # magnitude in [256, 512) before saturation to 448, and every element is the E4M3 rounding
+    # of its normal clamped to +-448 block units (relative error <= 2^-4, or an absolute 2^-10
+    # of the block scale below 2^-6)
+    import numpy as np
+    import oracle
+    from dense_attention_forward_fwd_gb300.inputs import make_qkv_mxfp8
+    q8, sq, k8, sk, v8, sv = make_qkv_mxfp8(1, 2, 40, 70, d=64, seed=9)
+    rng = np.random.Generator(np.random.PCG64(9))
+    q = rng.standard_normal((1, 2, 40, 64), dtype=np.float32)
+    vals = oracle.e4m3_to_f64(q8)
+    blocks = np.abs(vals).reshape(1, 2, 40, 2, 32).max(axis=-1)
+    assert np.all((blocks >= 256) & (blocks <= 448))
+    real = vals * np.repeat(oracle.e8m0_to_f64(sq), 32, axis=3)
+    unit = np.repeat(oracle.e8m0_to_f64(sq), 32, axis=3)
+    clamped = np.clip(q, -448.0 * unit, 448.0 * unit)
+    assert np.all(np.abs(real - clamped) <= np.maximum(np.abs(clamped) * 2.0 ** -4, unit * 2.0 ** -10) * (1 + 1e-6))
+    assert np.count_nonzero(clamped != q) < q.size // 50   # saturation is rare
+    assert sv.shape == (1, 2, 3, 64) and sk.shape == (1, 2, 70, 2)

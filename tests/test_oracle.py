@@ -568,6 +568,46 @@ def pin_e4m3_constant_values_are_returned(orc):
     assert np.max(np.abs(o8 + 1.625)) < 1e-13
 
 
+# ---- MXFP8: E4M3 elements with E8M0 scales per 32 elements along each contraction ----------
+
+def pin_e8m0_decoder_closed_forms(orc):
+    got = orc.e8m0_to_f64(np.array([127, 128, 126, 0, 254, 255, 137], dtype=np.uint8))
+    assert list(got[:5]) == [1.0, 2.0, 0.5, 2.0 ** -127, 2.0 ** 127] and np.isnan(got[5]) and got[6] == 1024.0
+
+
+def _mx_real(orc, codes, scales, axis):
+    """Real values of MX codes, with the scales repeated over their 32-element blocks."""
+    rep = np.repeat(orc.e8m0_to_f64(scales), 32, axis=axis)
+    idx = [slice(None)] * codes.ndim
+    idx[axis] = slice(0, codes.shape[axis])
+    return orc.e4m3_to_f64(codes) * rep[tuple(idx)]
+
+
+def pin_mxfp8_equals_the_bf16_oracle_on_the_scaled_values(orc):
+    # E4M3 values times powers of two are BF16 values here, so the block-scaled inputs widen
+    # exactly; random block scales, a partial last key block (Nk = 70) and dv != d catch a
+    # scale applied to the wrong block, row or axis
+    from dense_attention_forward_fwd_gb300.inputs import make_qkv_mxfp8
+    q8, sq, k8, sk, v8, sv = make_qkv_mxfp8(1, 2, 9, 70, d=64, seed=73, qk_mult=2.0)
+    v8, sv = np.ascontiguousarray(v8[..., :8]), np.ascontiguousarray(sv[..., :8])
+    rng = np.random.default_rng(74)
+    sq, sk, sv = (np.ascontiguousarray(x + rng.integers(-3, 4, size=x.shape)).astype(np.uint8) for x in (sq, sk, sv))
+    qb, kb, vb = (bf16(_mx_real(orc, c, sc, ax)) for c, sc, ax in ((q8, sq, 3), (k8, sk, 3), (v8, sv, 2)))
+    om, lm = orc.attention_rows_mxfp8(q8, sq, k8, sk, v8, sv, 0.3)
+    ob, lb = orc.attention_rows(qb, kb, vb, 0.3)
+    assert np.max(np.abs(om - ob)) < 1e-12 * max(1.0, np.max(np.abs(ob)))
+    assert np.max(np.abs(lm - lb)) < 1e-12 * np.max(np.abs(lb))
+
+
+def pin_mxfp8_with_uniform_scales_is_per_tensor_fp8(orc):
+    from dense_attention_forward_fwd_gb300.inputs import make_qkv_mxfp8
+    q8, sq, k8, sk, v8, sv = make_qkv_mxfp8(1, 1, 6, 45, d=32, seed=75)
+    sq[:], sk[:], sv[:] = 126, 129, 125        # 2^-1, 2^2, 2^-2 everywhere
+    om, lm = orc.attention_rows_mxfp8(q8, sq, k8, sk, v8, sv, 0.2)
+    oe, le = orc.attention_rows_e4m3(q8, k8, v8, 0.2, 0.5, 4.0, 0.25)
+    assert np.max(np.abs(om - oe)) < 1e-13 and np.max(np.abs(lm - le)) < 1e-13
+
+
 PINS = [v for k_, v in sorted(globals().items()) if k_.startswith("pin_")]
 
 

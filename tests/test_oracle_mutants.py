@@ -49,6 +49,13 @@ MUTANTS = {
                                   "num += s[j] * (double)kh[j * d + c];"),
     "e4m3 value descale dropped": ("(v_descale * e4m3_to_f64(vhead[j * dv + c]))", "(e4m3_to_f64(vhead[j * dv + c]))"),
     "e4m3 value rows with the key stride": ("vhead[j * dv + c]", "vhead[j * d + c]"),
+    "mx scale bias 128": ("return ldexp(1.0, (int)e - 127);", "return ldexp(1.0, (int)e - 128);"),
+    "mx key scales taken from the query": ("(e8m0_to_f64(ks[j * db + c / 32]) * e4m3_to_f64(kh[j * d + c]))",
+                                           "(e8m0_to_f64(qs[c / 32]) * e4m3_to_f64(kh[j * d + c]))"),
+    "mx value scales ignored": ("(e8m0_to_f64(vs[(j / 32) * dv + c]) * e4m3_to_f64(vh[j * dv + c]))",
+                                "(1.0 * e4m3_to_f64(vh[j * dv + c]))"),
+    "mx query scales of the first block only": ("(e8m0_to_f64(qs[c / 32]) * e4m3_to_f64(qi[c]))",
+                                                "(e8m0_to_f64(qs[0]) * e4m3_to_f64(qi[c]))"),
     "causal dense forward one key short": ("const int64_t nv = causal ? i + (Nk - Nq) + 1 : Nk;",
                                            "const int64_t nv = causal ? i + (Nk - Nq) + (i > 0) : Nk;"),
 }
