@@ -6,7 +6,6 @@ The missing tile is withheld by the library's test hook (attn_fwd_set_wait_limit
 producer simply skips one load, so the consumer's wait runs out after the short limit
 set here. Nothing traps, faults or hangs.
 """
-import numpy as np
 import pytest
 
 from dense_attention_forward_fwd_gb300.inputs import make_qkv
