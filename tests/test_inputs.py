@@ -65,3 +65,25 @@ def test_mxfp8_inputs_use_each_block_s_range_and_round_closely():
     assert np.all(np.abs(real - clamped) <= np.maximum(np.abs(clamped) * 2.0 ** -4, unit * 2.0 ** -10) * (1 + 1e-6))
     assert np.count_nonzero(clamped != q) < q.size // 50   # saturation is rare
     assert sv.shape == (1, 2, 3, 64) and sk.shape == (1, 2, 70, 2)
+
+
+def test_e4m3_inputs_are_per_tensor_quantizations_of_the_bf16_draw():
+    # descale = amax / 448 (so the largest code is 448), every code the E4M3 rounding of its
+    # normal over the descale, and V of make_qkv_e4m3 the same draw as make_qkv's V
+    import numpy as np
+    import oracle
+    from dense_attention_forward_fwd_gb300.inputs import make_qk_e4m3, make_qkv, make_qkv_e4m3
+    q8, k8, v8, dq, dk, dv = make_qkv_e4m3(1, 2, 50, 70, d=32, seed=12, qk_mult=3.0)
+    q8b, k8b, vb, dqb, dkb = make_qk_e4m3(1, 2, 50, 70, d=32, seed=12, qk_mult=3.0)
+    assert np.array_equal(q8, q8b) and np.array_equal(k8, k8b) and (dq, dk) == (dqb, dkb)
+    assert np.array_equal(vb, make_qkv(1, 2, 50, 70, d=32, seed=12)[2])
+    rng = np.random.Generator(np.random.PCG64(12))
+    q = rng.standard_normal((1, 2, 50, 32), dtype=np.float32) * np.float32(3.0)
+    k = rng.standard_normal((1, 2, 70, 32), dtype=np.float32) * np.float32(3.0)
+    v = rng.standard_normal((1, 2, 70, 32), dtype=np.float32)
+    for codes, ds, x in ((q8, dq, q), (k8, dk, k), (v8, dv, v)):
+        vals = oracle.e4m3_to_f64(codes)
+        assert np.max(np.abs(vals)) == 448.0
+        assert ds == float(np.float32(np.abs(x).max() / 448.0))
+        t = x.astype(np.float64) / ds
+        assert np.all(np.abs(vals - t) <= np.maximum(np.abs(t) * 2.0 ** -4, 2.0 ** -10) * (1 + 1e-6))
