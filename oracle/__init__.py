@@ -3,7 +3,9 @@
 Only the test suite, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
 ``bench.py`` may import this package. The library under test never does, and
 this package imports nothing from it: the two share no code. Inputs are BF16
-bit patterns (uint16 numpy arrays), as produced by the seeded generators.
+bit patterns (uint16 numpy arrays), or for the 8-bit functions E4M3 codes and E8M0
+block scales (uint8 arrays), as produced by the seeded generators; the oracle decodes
+the 8-bit formats itself.
 
 The arithmetic lives in ``attn_ref.c`` (plain C, double precision, OpenMP over
 query rows); this module compiles it with gcc on first use and marshals numpy
