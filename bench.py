@@ -585,6 +585,8 @@ def run_ours(args, w):
         "gpu_launches": launches,
         "clocks": clocks,
         "kernel_ms_min": min(durs), "kernel_ms_median": statistics.median(durs),
+        "gpu": {"name": torch.cuda.get_device_properties(dev).name,
+                "sms": torch.cuda.get_device_properties(dev).multi_processor_count},
     }
     if rank == 0 and not args.no_cpu_baseline:
         if args.backward:
