@@ -196,7 +196,8 @@ def _mp_attention(qw, kw, vw, scale):
 
 
 BRUTE_CASES = [(1, 1, 1, 1.0, 1.0), (2, 3, 4, 1.0, 0.5), (3, 5, 4, 3.0, SCALE), (5, 2, 128, 1.0, SCALE),
-               (2, 5, 128, 3.0, SCALE), (3, 4, 6, 1.0, 0.8, 5)]
+               (2, 5, 128, 3.0, SCALE), (3, 4, 6, 1.0, 0.8, 5),
+               (3, 4, 256, 1.0, 1 / 16, 192)]   # a head dim past 128 (and a different value dim)
 
 
 def pin_matches_high_precision_brute_force(orc, cases=BRUTE_CASES):
