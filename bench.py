@@ -2,8 +2,10 @@
 """Benchmark of the dense BF16 attention forward (d=128; non-causal by default) on GB300.
 
 One step = one attn_fwd call over the whole workload (every (b, h) and every query
-tile). Default workload: B=1, H=8, Nq=4096, Nk=8192 (the shape of the RTX 5090 table
-in "Flash Attention на 5090 в CUDA C++"); --workload picks another of the five.
+tile). Default workload: long-16k, B=1, H=16, Nq=Nk=16384 (the largest of the 4K/8K/16K
+sequence lengths that "Sıfırdan yazılan CUDA attention kerneli..." measures at, and the
+largest of the five that fits one GPU); --workload picks another of the five (rect-4k-8k
+is the shape of the RTX 5090 table in "Flash Attention на 5090 в CUDA C++").
 
 Kernel time: CUDA events around each launch on the launching stream, inputs resident
 in HBM, L2 flushed (a 512 MiB write) before every timed launch. value = total
@@ -53,7 +55,7 @@ sys.path.insert(0, ROOT)
 from dense_attention_forward_fwd_gb300.configs import WORKLOADS, by_name  # noqa: E402
 
 METRIC = "attention fwd TFLOPS (4·B·H·N²·d) and % of GB300 dense-BF16 tensor peak"
-DEFAULT_WORKLOAD = "rect-4k-8k"
+DEFAULT_WORKLOAD = "long-16k"
 # The pages' own figure for this shape: the from-scratch v5 kernel on an RTX 5090
 # ("Flash Attention на 5090 в CUDA C++", benchmark table). Another GPU: context only.
 PAGES_TFLOPS = {"rect-4k-8k": 197.74}

@@ -15,7 +15,7 @@ from ._build import LIB_PATH, build_library
 
 __all__ = [
     "ATTN_OK", "ATTN_ERR_INVALID_ARG", "ATTN_ERR_UNSUPPORTED", "ATTN_ERR_MISALIGNED", "ATTN_ERR_CUDA",
-    "ATTN_ERR_TIMEOUT", "AttnError", "load_library", "attn_fwd", "attn_fwd_causal", "attn_fwd_bias", "attn_fwd_fp8qk", "attn_fwd_fp8", "attn_fwd_noalloc", "attn_fwd_status", "attn_status_string",
+    "ATTN_ERR_TIMEOUT", "AttnError", "load_library", "attn_fwd", "attn_fwd_causal", "attn_fwd_bias", "attn_fwd_fp8qk", "attn_fwd_fp8", "attn_fwd_o32", "attn_fwd_noalloc", "attn_fwd_status", "attn_status_string",
     "attn_fwd_set_wait_limit", "attn_fwd_kernel_count", "attention", "attn_bwd", "attn_bwd_causal", "attn_bwd_status",
     "attn_bwd_kernel_count", "attn_bwd_set_wait_limit",
 ]
@@ -48,6 +48,8 @@ def load_library(build_if_stale: bool = True) -> ctypes.CDLL:
             lib.attn_fwd.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, f32, vp]
             lib.attn_fwd.restype = i32
             lib.attn_fwd_noalloc.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, f32, vp]
+            lib.attn_fwd_o32.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, f32, vp]
+            lib.attn_fwd_o32.restype = i32
             lib.attn_fwd_causal.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, f32, vp]
             lib.attn_fwd_fp8qk.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, f32, f32, f32, vp]
             lib.attn_fwd_fp8qk.restype = i32
@@ -233,6 +235,21 @@ def attn_fwd_bias(q, k, v, bias, o, lse, B: int, H: int, Nq: int, Nk: int, d: in
                            _stream_handle(stream, q, k, v, o, lse))
     if rc != ATTN_OK:
         raise AttnError(rc, "attn_fwd_bias")
+
+
+def attn_fwd_o32(q, k, v, o32, lse, B: int, H: int, Nq: int, Nk: int, d: int, scale: float, stream=None) -> None:
+    """Like :func:`attn_fwd`, with O written as FP32 [B,H,Nq,d] (``o32``) before its rounding to
+    BF16: the same kernel code, for checking the computation's own error."""
+    lib = load_library()
+    args = (
+        _ptr(q, "q", B * H * Nq * d, "bf16"), _ptr(k, "k", B * H * Nk * d, "bf16"),
+        _ptr(v, "v", B * H * Nk * d, "bf16"), _ptr(o32, "o32", B * H * Nq * d, "f32"),
+        _ptr(lse, "lse", B * H * Nq, "f32"),
+    )
+    rc = lib.attn_fwd_o32(*args, int(B), int(H), int(Nq), int(Nk), int(d), float(scale),
+                          _stream_handle(stream, q, k, v, o32, lse))
+    if rc != ATTN_OK:
+        raise AttnError(rc, "attn_fwd_o32")
 
 
 def attn_fwd_noalloc(q, k, v, o, lse, B: int, H: int, Nq: int, Nk: int, d: int, scale: float, stream=None) -> None:

@@ -164,6 +164,7 @@ struct Params {
   int H;                  // heads per batch (splits b*H + h)
   float scale;            // the caller's scale (the bias path scales before adding B)
   float v_scale = 1.0f;   // V's descale factor (V as FP8 codes), applied with 1 / l
+  float* o32 = nullptr;   // FP32 [BH, Nq, 128]: O before rounding (kernels instantiated with kO32)
 };
 
 // floor(a / b) for a >= 0, b > 0. On the device a 64-bit division is a long dependent
@@ -900,9 +901,11 @@ __device__ __forceinline__ void store_half_rows(uint8_t* stage, const uint32_t (
 // When own_tO is non-zero the calling block's own share is still in TMEM (O at own_tO,
 // its max and sums in own_m, own_l, own_corr) and its record is not read. O is also
 // multiplied by o_scale (V's descale factor when V is given as FP8 codes, else 1).
+// kO32: the row goes to o32_row in FP32 (null for rows past the sequence) instead of BF16.
+template <bool kO32 = false>
 __device__ void merge_split_row(const Params& p, int tile, int r, int c_first, int c_last, long long x0,
                                 uint8_t* stage, uint16_t* o_row0, int valid_rows, float* lse_out, uint32_t own_tO,
-                                float own_m, float own_l, float own_corr, float o_scale) {
+                                float own_m, float own_l, float own_corr, float o_scale, float* o32_row) {
   const int self = own_tO != 0 ? static_cast<int>(blockIdx.x) : -1;
   const long long x0_grid = x0 * static_cast<long long>(gridDim.x);
   // share cs's record: its first segment's slot when its share starts inside this group
@@ -966,10 +969,19 @@ __device__ void merge_split_row(const Params& p, int tile, int r, int c_first, i
 #pragma unroll
       for (int i = 0; i < 64; ++i) acc[i] = fmaf(v[i], w, acc[i]);
     }
-    uint32_t pk[32];
+    if constexpr (kO32) {
+      if (o32_row != nullptr) {
+        float4* dst = reinterpret_cast<float4*>(o32_row + h * 64);
 #pragma unroll
-    for (int i = 0; i < 32; ++i) pk[i] = pack_bf16(acc[2 * i] * inv, acc[2 * i + 1] * inv);
-    store_half_rows(stage, pk, o_row0, valid_rows, h);
+        for (int g = 0; g < 16; ++g)
+          dst[g] = make_float4(acc[4 * g] * inv, acc[4 * g + 1] * inv, acc[4 * g + 2] * inv, acc[4 * g + 3] * inv);
+      }
+    } else {
+      uint32_t pk[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) pk[i] = pack_bf16(acc[2 * i] * inv, acc[2 * i + 1] * inv);
+      store_half_rows(stage, pk, o_row0, valid_rows, h);
+    }
   }
   if (lse_out != nullptr) *lse_out = (M + log2f(L)) * 0.69314718055994531f;
 }
@@ -977,7 +989,8 @@ __device__ void merge_split_row(const Params& p, int tile, int r, int c_first, i
 // kP8: P is rounded to E4M3 (four keys per TMEM column) for an FP8 P V product; the
 // running max then moves once it grows by 8 (log2 units), so that every p <= 2^8 stays
 // below E4M3's largest value 448, and O is scaled by V's descale factor with 1 / l.
-template <bool kPosScale, bool kBias, bool kP8 = false>
+// kO32: O is written in FP32 to p.o32 (the value the BF16 output is rounded from).
+template <bool kPosScale, bool kBias, bool kP8 = false, bool kO32 = false>
 __device__ void run_softmax(const Ctl& c, uint32_t tmem, uint8_t* stage, const Params& p, int tile) {
   constexpr float kTau = kP8 ? 8.0f : kRescaleLog2;
   const int quarter = (threadIdx.x >> 5) & 3;   // TMEM lanes this warp may access
@@ -1194,13 +1207,23 @@ __device__ void run_softmax(const Ctl& c, uint32_t tmem, uint8_t* stage, const P
       __syncwarp();
       if (lane == 0) mbar_arrive(c.bar(kBarOEmpty + tile));
       __syncwarp();
+      if constexpr (kO32) {
+        if (live) {
+          float4* dst = reinterpret_cast<float4*>(p.o32 + row_id * kD);
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        uint32_t pk[32];
+          for (int g = 0; g < kD / 4; ++g)
+            dst[g] = make_float4(__uint_as_float(ov[4 * g]) * inv_l, __uint_as_float(ov[4 * g + 1]) * inv_l,
+                                 __uint_as_float(ov[4 * g + 2]) * inv_l, __uint_as_float(ov[4 * g + 3]) * inv_l);
+        }
+      } else {
 #pragma unroll
-        for (int i = 0; i < 32; ++i)
-          pk[i] = pack_bf16(__uint_as_float(ov[64 * h + 2 * i]) * inv_l, __uint_as_float(ov[64 * h + 2 * i + 1]) * inv_l);
-        store_half_rows(stage, pk, o_row0, valid_rows, h);
+        for (int h = 0; h < 2; ++h) {
+          uint32_t pk[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            pk[i] = pack_bf16(__uint_as_float(ov[64 * h + 2 * i]) * inv_l, __uint_as_float(ov[64 * h + 2 * i + 1]) * inv_l);
+          store_half_rows(stage, pk, o_row0, valid_rows, h);
+        }
       }
       if (live) p.lse[row_id] = (m_used + log2f(l)) * 0.69314718055994531f;
     } else {
@@ -1220,8 +1243,9 @@ __device__ void run_softmax(const Ctl& c, uint32_t tmem, uint8_t* stage, const P
         // Every other share has left its record: merge with this share's O straight
         // from TMEM, without writing a record of its own.
         __threadfence();
-        merge_split_row(p, tile, r, c_first, c_last, x0, stage, o_row0, valid_rows, live ? p.lse + row_id : nullptr,
-                        tO, m_used, l, corr, kP8 ? p.v_scale : 1.0f);
+        merge_split_row<kO32>(p, tile, r, c_first, c_last, x0, stage, o_row0, valid_rows,
+                              live ? p.lse + row_id : nullptr, tO, m_used, l, corr, kP8 ? p.v_scale : 1.0f,
+                              kO32 && live ? p.o32 + row_id * kD : nullptr);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(c.bar(kBarOEmpty + tile));
@@ -1251,8 +1275,9 @@ __device__ void run_softmax(const Ctl& c, uint32_t tmem, uint8_t* stage, const P
         before = __shfl_sync(0xffffffffu, before, 0);
         if (static_cast<int>(before) == c_last - c_first) {
           __threadfence();
-          merge_split_row(p, tile, r, c_first, c_last, x0, stage, o_row0, valid_rows,
-                          live ? p.lse + row_id : nullptr, 0u, 0.0f, 0.0f, 0.0f, kP8 ? p.v_scale : 1.0f);
+          merge_split_row<kO32>(p, tile, r, c_first, c_last, x0, stage, o_row0, valid_rows,
+                                live ? p.lse + row_id : nullptr, 0u, 0.0f, 0.0f, 0.0f, kP8 ? p.v_scale : 1.0f,
+                                kO32 && live ? p.o32 + row_id * kD : nullptr);
         }
       }
     }
@@ -1264,7 +1289,7 @@ __device__ void run_softmax(const Ctl& c, uint32_t tmem, uint8_t* stage, const P
 // ---------------------------------------------------------------------------------
 // Kernel
 // ---------------------------------------------------------------------------------
-template <bool kPosScale, bool kBias, int kF8 = 0>
+template <bool kPosScale, bool kBias, int kF8 = 0, bool kO32 = false>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const Params p) {
@@ -1330,7 +1355,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsSoftmax));
-    run_softmax<kPosScale, kBias, kF8 == 2>(c, tmem, smem + kOffStage + (warp - 4) * kStageBytes, p, (warp >> 2) - 1);
+    run_softmax<kPosScale, kBias, kF8 == 2, kO32>(c, tmem, smem + kOffStage + (warp - 4) * kStageBytes, p, (warp >> 2) - 1);
   }
 
   tc_fence_before();
@@ -1397,7 +1422,7 @@ bool make_map_vt(CUtensorMap* map, const void* ptr, int Nk, long long ldv, long 
 }
 
 constexpr int kMaxDevices = 64;
-std::atomic<int> g_attr_done[12][kMaxDevices];   // per instantiation (kPos + 2 * kBias + 4 * kF8)
+std::atomic<int> g_attr_done[14][kMaxDevices];   // per instantiation (kPos + 2 * kBias + 4 * kF8, 12 + kPos for kO32)
 std::atomic<int> g_sm_count[kMaxDevices];
 
 int sm_count(int dev) {
@@ -1482,11 +1507,11 @@ int get_workspace(int dev, cudaStream_t stream, size_t part_bytes, size_t cnt_by
   return ATTN_OK;
 }
 
-template <bool kPos, bool kBias = false, int kF8 = 0>
+template <bool kPos, bool kBias = false, int kF8 = 0, bool kO32 = false>
 int launch(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, const Params& p, int grid,
            int dev, cudaStream_t stream) {
-  auto kern = attn_fwd_kernel<kPos, kBias, kF8>;
-  constexpr int kInst = (kPos ? 1 : 0) + (kBias ? 2 : 0) + 4 * kF8;
+  auto kern = attn_fwd_kernel<kPos, kBias, kF8, kO32>;
+  constexpr int kInst = kO32 ? 12 + (kPos ? 1 : 0) : (kPos ? 1 : 0) + (kBias ? 2 : 0) + 4 * kF8;
   if (dev < 0 || dev >= kMaxDevices || !g_attr_done[kInst][dev].load(std::memory_order_acquire)) {
     // The in-kernel register split (setmaxnreg) balances only at kRegsLaunch registers
     // per thread; at any other count the increase would never be granted. Refuse.
@@ -1512,10 +1537,12 @@ struct BiasArg {
 };
 
 // attn_fwd, attn_fwd_bias (bias != nullptr), attn_fwd_fp8qk (f8 = 1: q and k hold FP8 E4M3
-// codes) and attn_fwd_fp8 (f8 = 2: v too, as V^T with row stride ldv, descaled by v_scale):
-// the argument rules, the plan, the launch.
+// codes), attn_fwd_fp8 (f8 = 2: v too, as V^T with row stride ldv, descaled by v_scale) and
+// attn_fwd_o32 (o32 != nullptr: O in FP32 there, o unused): the argument rules, the plan,
+// the launch.
 int forward(const void* q, const void* k, const void* v, const BiasArg* bias, void* o, float* lse, int B, int H,
-            int Nq, int Nk, int d, float scale, void* stream, int f8 = 0, long long ldv = 0, float v_scale = 1.0f) {
+            int Nq, int Nk, int d, float scale, void* stream, int f8 = 0, long long ldv = 0, float v_scale = 1.0f,
+            float* o32 = nullptr) {
   const bool qk8 = f8 >= 1;
   if (B < 0 || H < 0 || Nq < 0 || Nk < 0) return ATTN_ERR_INVALID_ARG;
   if (d != kD) return ATTN_ERR_UNSUPPORTED;
@@ -1523,6 +1550,7 @@ int forward(const void* q, const void* k, const void* v, const BiasArg* bias, vo
   const long long bh = static_cast<long long>(B) * H;
   if (bh == 0 || Nq == 0) return ATTN_OK;   // nothing to compute
   if (Nk == 0) return ATTN_ERR_INVALID_ARG;  // softmax over an empty key set
+  if (o32 != nullptr) o = o32;               // the output, whichever type it has
   if (!q || !k || !v || !o || !lse) return ATTN_ERR_INVALID_ARG;
   if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) | reinterpret_cast<uintptr_t>(v) |
        reinterpret_cast<uintptr_t>(o)) & 15u)
@@ -1592,6 +1620,7 @@ int forward(const void* q, const void* k, const void* v, const BiasArg* bias, vo
   p.H = H;
   p.scale = scale;
   p.v_scale = v_scale;
+  p.o32 = o32;
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (pl.has_split) {
@@ -1601,6 +1630,9 @@ int forward(const void* q, const void* k, const void* v, const BiasArg* bias, vo
     const int rc = get_workspace(dev, s, part_bytes, cnt_bytes, &p.part, &p.cnt, &p.cnt_next, &p.cnt_len);
     if (rc != ATTN_OK) return rc;
   }
+  if (o32 != nullptr)
+    return scale > 0.0f ? launch<true, false, 0, true>(mq, mk, mv, p, pl.grid, dev, s)
+                        : launch<false, false, 0, true>(mq, mk, mv, p, pl.grid, dev, s);
   // with a bias the scale is applied before the row max, so one instantiation serves any sign
   if (bias != nullptr) return launch<true, true>(mq, mk, mv, p, pl.grid, dev, s);
   if (f8 == 2)
@@ -1617,6 +1649,11 @@ int forward(const void* q, const void* k, const void* v, const BiasArg* bias, vo
 extern "C" int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Nq,
                         int Nk, int d, float scale, void* stream) {
   return forward(q, k, v, nullptr, o, lse, B, H, Nq, Nk, d, scale, stream);
+}
+
+extern "C" int attn_fwd_o32(const void* q, const void* k, const void* v, float* o32, float* lse, int B, int H,
+                            int Nq, int Nk, int d, float scale, void* stream) {
+  return forward(q, k, v, nullptr, nullptr, lse, B, H, Nq, Nk, d, scale, stream, 0, 0, 1.0f, o32);
 }
 
 extern "C" int attn_fwd_bias(const void* q, const void* k, const void* v, const void* bias, long long bias_stride_b,
@@ -1760,8 +1797,37 @@ constexpr size_t kNoAllocScratchBytes = size_t(48) << 20;   // 48 MiB: the recor
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
 namespace {
+// The array's device address differs between CUDA contexts (the library's module is loaded
+// into each context on its own, again after cudaDeviceReset), so it is cached per context,
+// keyed by the context's process-unique id.
 std::mutex g_noalloc_mu;
-void* g_noalloc_addr[kMaxDevices];   // device address of g_noalloc_scratch, looked up once per device
+std::map<unsigned long long, void*> g_noalloc_addr;
+using PFN_ctxGetCurrent = CUresult (*)(CUcontext*);
+using PFN_ctxGetId = CUresult (*)(CUcontext, unsigned long long*);
+PFN_ctxGetCurrent g_ctx_current = nullptr;
+PFN_ctxGetId g_ctx_id = nullptr;
+std::once_flag g_ctx_once;
+
+// The id of the calling thread's current context, or 0 when there is none yet.
+unsigned long long current_context_id() {
+  std::call_once(g_ctx_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &fn, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_ctx_current = reinterpret_cast<PFN_ctxGetCurrent>(fn);
+    fn = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &fn, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_ctx_id = reinterpret_cast<PFN_ctxGetId>(fn);
+  });
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (g_ctx_current == nullptr || g_ctx_id == nullptr || g_ctx_current(&ctx) != CUDA_SUCCESS || ctx == nullptr ||
+      g_ctx_id(ctx, &id) != CUDA_SUCCESS)
+    return 0;
+  return id;
+}
 }  // namespace
 
 extern "C" int attn_fwd_noalloc(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
@@ -1785,21 +1851,26 @@ extern "C" int attn_fwd_noalloc(const void* q, const void* k, const void* v, voi
 
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return ATTN_ERR_CUDA;
-  if (dev < 0 || dev >= kMaxDevices) return ATTN_ERR_UNSUPPORTED;
   const int sms = sm_count(dev);
   if (sms <= 0) return ATTN_ERR_CUDA;
 
   // In host code g_noalloc_scratch only stands for the array: its device address has to
-  // be asked for, with this device current. The first call on each device does that.
+  // be asked for, with this device current. The first call in each context does that (a
+  // lookup, no allocation); later calls in the same context reuse the address.
   void* scratch = nullptr;
   {
     std::lock_guard<std::mutex> lock(g_noalloc_mu);
-    if (g_noalloc_addr[dev] == nullptr) {
+    unsigned long long ctx = current_context_id();
+    auto it = ctx != 0 ? g_noalloc_addr.find(ctx) : g_noalloc_addr.end();
+    if (it != g_noalloc_addr.end()) {
+      scratch = it->second;
+    } else {
       void* ptr = nullptr;
       if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || ptr == nullptr) return ATTN_ERR_CUDA;
-      g_noalloc_addr[dev] = ptr;
+      scratch = ptr;
+      ctx = current_context_id();   // the lookup makes the device's primary context current if none was
+      if (ctx != 0) g_noalloc_addr[ctx] = ptr;
     }
-    scratch = g_noalloc_addr[dev];
   }
 
   CUtensorMap mq, mk, mv;

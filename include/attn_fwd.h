@@ -184,6 +184,25 @@ int attn_fwd_fp8(const void* q8, const void* k8, const void* vt8, long long ldv,
                  float v_descale, void* stream);
 
 /*
+ * attn_fwd_o32 -- attn_fwd with O written in FP32, before its rounding to BF16.
+ *
+ * A diagnostic of the computation itself. The notes state that the tiled computation
+ * reaches exact attention, not an approximation ("FlashAttention'ı Anlamak Bölüm 1",
+ * section 0.1): its only errors are rounding. With a BF16 output, half a BF16 ulp of O
+ * (up to 1/64 for |O| in [4, 8)) can exceed an error bound of 1e-2 by itself, so a test
+ * of the kernel's own arithmetic against such a bound needs O before that last rounding.
+ * This call runs the same kernel code as attn_fwd (same tiles, same online softmax,
+ * same work split and merge) and differs only in the store of O.
+ *
+ *   o32  device, FP32 [B, H, Nq, d], written; 16-byte aligned (else ATTN_ERR_MISALIGNED).
+ *        attn_fwd's o is this array rounded to nearest-even BF16.
+ *
+ * Everything else (q, k, v, lse, sizes, scale, workspace, return values) is as attn_fwd.
+ */
+int attn_fwd_o32(const void* q, const void* k, const void* v, float* o32, float* lse,
+                 int B, int H, int Nq, int Nk, int d, float scale, void* stream);
+
+/*
  * attn_fwd_noalloc -- attn_fwd for callers that cannot allocate device memory.
  *
  * There is no counterpart on the pages: this is a service of the library. Some callers
@@ -198,10 +217,11 @@ int attn_fwd_fp8(const void* q8, const void* k8, const void* vt8, long long ldv,
  *
  * Arguments, layouts and return values are those of attn_fwd, plus:
  *   - ATTN_ERR_UNSUPPORTED when the call would need more than the fixed 48 MiB (only on
- *     a device with more than 186 SMs) or the device index is 64 or above.
- *   - The first call on each device looks up the array's device address
- *     (cudaGetSymbolAddress) with that device current; make that first call before any
- *     stream capture on the device.
+ *     a device with more than 186 SMs).
+ *   - The first call in each CUDA context (on each device, and again after
+ *     cudaDeviceReset or in another context made current by the caller) looks up the
+ *     array's device address (cudaGetSymbolAddress, which allocates nothing) with that
+ *     context current; make that first call before any stream capture on the device.
  *   - Every call on a device uses the same array, which keeps the previous call's
  *     contents; each call clears the part that must start at zero on its own stream.
  *     Calls whose kernels overlap on the GPU (different streams, no ordering between

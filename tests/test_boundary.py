@@ -26,7 +26,7 @@ def declared_functions():
 
 def test_header_declares_the_entry_points():
     names = declared_functions()
-    assert {"attn_fwd", "attn_fwd_causal", "attn_fwd_bias", "attn_fwd_fp8qk", "attn_fwd_fp8", "attn_fwd_noalloc", "attn_bwd", "attn_bwd_causal",
+    assert {"attn_fwd", "attn_fwd_causal", "attn_fwd_bias", "attn_fwd_fp8qk", "attn_fwd_fp8", "attn_fwd_o32", "attn_fwd_noalloc", "attn_bwd", "attn_bwd_causal",
             "attn_bwd_status", "attn_bwd_set_wait_limit",
             "attn_bwd_kernel_count", "attn_fwd_status", "attn_status_string",
             "attn_fwd_set_wait_limit", "attn_fwd_kernel_count"} <= set(names)
@@ -58,6 +58,21 @@ A = 1 << 20  # fake, 16-byte aligned addresses: every call below is rejected bef
 
 def call(q=A, k=A, v=A, o=A, lse=A, B=1, H=1, Nq=128, Nk=128, d=128, scale=0.125):
     return attn.load_library().attn_fwd(q, k, v, o, lse, B, H, Nq, Nk, d, scale, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(o=None), attn.ATTN_ERR_INVALID_ARG),
+    (dict(o=A + 8), attn.ATTN_ERR_MISALIGNED),    # FP32 rows are stored in 16-byte vectors
+    (dict(d=64), attn.ATTN_ERR_UNSUPPORTED),
+    (dict(Nk=0), attn.ATTN_ERR_INVALID_ARG),
+    (dict(B=0, q=None, o=None), attn.ATTN_OK),
+])
+def test_o32_rejects_like_attn_fwd(kw, code):
+    a = dict(q=A, k=A, v=A, o=A, lse=A, B=1, H=1, Nq=128, Nk=128, d=128, scale=0.125)
+    a.update(kw)
+    lib = attn.load_library()
+    assert lib.attn_fwd_o32(a["q"], a["k"], a["v"], a["o"], a["lse"], a["B"], a["H"], a["Nq"], a["Nk"], a["d"],
+                            a["scale"], None) == code
 
 
 @pytest.mark.parametrize("kw,code", [

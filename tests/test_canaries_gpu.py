@@ -41,6 +41,10 @@ def test_forward_entry_points(gpu_lib, B, H, Nq, Nk):
         "attn_fwd_noalloc": lambda o, l: gpu_lib.attn_fwd_noalloc(q, k, v, o, l, B, H, Nq, Nk, 128, SCALE),
         "attn_fwd_causal": lambda o, l: gpu_lib.attn_fwd_causal(q, k, v, o, l, B, H, Nq, Nk, 128, SCALE),
     }
+    # the FP32-output diagnostic: its O is FP32, guarded the same way
+    (fo32, o32), (fl32, l32) = guarded((B, H, Nq, 128), "f32", "cuda"), guarded((B, H, Nq), "f32", "cuda")
+    gpu_lib.attn_fwd_o32(q, k, v, o32, l32, B, H, Nq, Nk, 128, SCALE)
+    check(gpu_lib, ((fo32, o32), "f32"), ((fl32, l32), "f32"))
     bias = to_device(make_bias((B, H, Nq, Nk), seed=17100, std=1.0)) if Nk % 8 == 0 else None
     if bias is not None:   # rows of Nk BF16 values on 16-byte boundaries
         calls["attn_fwd_bias"] = lambda o, l: gpu_lib.attn_fwd_bias(q, k, v, bias, o, l, B, H, Nq, Nk, 128, SCALE)

@@ -47,10 +47,11 @@ def test_full_parity_peaked_small(gpu_lib, seed):
     check_case(gpu_lib, 1, 2, 512, 2048, seed=seed, qk_mult=3.0, ulp_aware=True)
 
 
-# ---- the five workloads at full size, on seeded samples of query rows --------------------------
+# ---- the five workloads at full size: every element of O and every LSE on the first four,
+# ---- 64 seeded query rows per head on the 16K one ----------------------------------------------
 
 @pytest.mark.parametrize("name", [w.name for w in WORKLOADS])
-def test_workload_sampled_rows(gpu_lib, name):
+def test_workload_full_size(gpu_lib, name):
     w = by_name(name)
     rows = None
     if w.oracle_rows_per_head is not None:

@@ -1,26 +1,95 @@
 """attn_fwd_noalloc, the entry point for callers that cannot allocate device memory
-(applications with a fixed memory budget, allocation-free hot loops, programs whose
-own allocator owns the device), must give the same results as attn_fwd.
+(applications that budget all GPU memory up front, allocation-free hot loops, programs
+whose own allocator owns the device), must give attn_fwd's results and allocate nothing.
 
-It runs the same kernel with its split-merge workspace in a fixed array inside the
-library. Two calls in a row check that what the first call leaves in the shared array
-does not leak into the second. The file is named to be collected last, and passes both
-alone in a fresh process and after the rest of the suite.
+It runs the same kernel with the same work split and a merge whose order does not depend
+on timing, so its O and LSE must equal attn_fwd's bit for bit. The workspace for split
+work is a fixed array inside the library that keeps the previous call's contents: two
+calls in a row, and a second call on another shape, check that nothing of an earlier call
+leaks into a later one. The allocation check reads the device's default memory pool (the
+pool cudaMallocAsync draws from) through the driver API around a call on a fresh stream,
+where attn_fwd would have to allocate its workspace, and checks that attn_fwd on another
+fresh stream does move the pool, so the probe can see an allocation.
+
+The file is named to be collected last; it passes alone in a fresh process and after the
+rest of the suite.
 """
+import ctypes
+
 import numpy as np
 import pytest
 
 from dense_attention_forward_fwd_gb300.inputs import make_qkv
-from parity import LSE_REL, MAX_ABS, MEAN_ABS, bf16_to_np, to_device
+from parity import bf16_to_np, to_device
 
 pytestmark = pytest.mark.gpu
 
+SCALE = float(np.float32(1 / np.sqrt(128)))
 
-def _same_within_tolerance(o_a, l_a, o_b, l_b):
-    err = np.abs(o_a.astype(np.float64) - o_b.astype(np.float64))
-    lse_err = np.abs(l_a.astype(np.float64) - l_b.astype(np.float64)) / np.maximum(1.0, np.abs(l_b))
-    assert err.max() <= MAX_ABS and err.mean() <= MEAN_ABS and lse_err.max() <= LSE_REL, \
-        (err.max(), err.mean(), lse_err.max())
+
+class Driver:
+    """The few CUDA driver calls the allocation check needs, on the current context."""
+    RESERVED_MEM_CURRENT, USED_MEM_CURRENT = 5, 7   # CUmemPool_attribute values
+
+    def __init__(self):
+        self.cu = ctypes.CDLL("libcuda.so.1")
+        dev = ctypes.c_int()
+        assert self.cu.cuCtxGetDevice(ctypes.byref(dev)) == 0
+        self.pool = ctypes.c_void_p()
+        assert self.cu.cuDeviceGetDefaultMemPool(ctypes.byref(self.pool), dev) == 0
+
+    def pool_bytes(self):
+        out = []
+        for attr in (self.RESERVED_MEM_CURRENT, self.USED_MEM_CURRENT):
+            v = ctypes.c_uint64()
+            assert self.cu.cuMemPoolGetAttribute(self.pool, attr, ctypes.byref(v)) == 0
+            out.append(v.value)
+        return tuple(out)
+
+    def new_stream(self) -> int:
+        """A stream no earlier call has used (torch's streams come from a reused pool)."""
+        s = ctypes.c_void_p()
+        assert self.cu.cuStreamCreate(ctypes.byref(s), 1) == 0   # CU_STREAM_NON_BLOCKING
+        return s.value
+
+
+def _prepare(shape):
+    """Seeded inputs and NaN-filled outputs on the device, ready before any timed or probed call."""
+    import torch
+    B, H, Nq, Nk = shape
+    q, k, v = make_qkv(B, H, Nq, Nk, seed=Nq + Nk)
+    o = torch.full((B, H, Nq, 128), float("nan"), dtype=torch.bfloat16, device="cuda")
+    lse = torch.full((B, H, Nq), float("nan"), dtype=torch.float32, device="cuda")
+    bufs = (to_device(q), to_device(k), to_device(v), o, lse)
+    torch.cuda.synchronize()   # a call on another stream must see the copies and fills done
+    return bufs
+
+
+def _call(attn, fn_name, shape, bufs, stream=None):
+    """One call of attn_fwd or attn_fwd_noalloc through the C ABI, waited for."""
+    import torch
+    B, H, Nq, Nk = shape
+    st = torch.cuda.current_stream().cuda_stream if stream is None else stream
+    rc = getattr(attn.load_library(), fn_name)(*(t.data_ptr() for t in bufs), B, H, Nq, Nk, 128, SCALE, st)
+    assert rc == attn.ATTN_OK, attn.attn_status_string(rc)
+    assert attn.attn_fwd_status(st) == attn.ATTN_OK   # synchronises the stream
+
+
+def _result(bufs):
+    return bf16_to_np(bufs[3]), bufs[4].cpu().numpy()
+
+
+def _run(attn, fn_name, shape, stream=None):
+    bufs = _prepare(shape)
+    _call(attn, fn_name, shape, bufs, stream)
+    return _result(bufs)
+
+
+def _assert_same(got, want, what):
+    (o, lse), (o_ref, lse_ref) = got, want
+    assert np.all(np.isfinite(o)) and np.all(np.isfinite(lse)), f"{what}: an output element left unwritten"
+    assert np.array_equal(o, o_ref), f"{what}: O differs from attn_fwd's"
+    assert np.array_equal(lse, lse_ref), f"{what}: LSE differs from attn_fwd's"
 
 
 @pytest.mark.parametrize("B,H,Nq,Nk", [
@@ -28,31 +97,41 @@ def _same_within_tolerance(o_a, l_a, o_b, l_b):
     (1, 8, 4096, 8192),   # 128 groups on all SMs, split two or three ways
     (2, 3, 520, 1290),    # ragged tails, uneven split points
 ])
-def test_noalloc_matches_attn_fwd_on_two_calls(gpu_lib, B, H, Nq, Nk):
-    import torch
-    attn = gpu_lib
-    lib = attn.load_library()
-    q, k, v = make_qkv(B, H, Nq, Nk, seed=Nq + Nk)
-    qd, kd, vd = to_device(q), to_device(k), to_device(v)
-    scale = float(np.float32(1 / np.sqrt(128)))
-
-    o_ref = torch.empty((B, H, Nq, 128), dtype=torch.bfloat16, device="cuda")
-    l_ref = torch.empty((B, H, Nq), dtype=torch.float32, device="cuda")
-    attn.attn_fwd(qd, kd, vd, o_ref, l_ref, B, H, Nq, Nk, 128, scale)
-    assert attn.attn_fwd_status() == attn.ATTN_OK
-    o_ref_np, l_ref_np = bf16_to_np(o_ref), l_ref.cpu().numpy()
-
+def test_noalloc_equals_attn_fwd_on_two_calls(gpu_lib, B, H, Nq, Nk):
+    want = _run(gpu_lib, "attn_fwd", (B, H, Nq, Nk))
     for call in range(2):
-        o = torch.full((B, H, Nq, 128), float("nan"), dtype=torch.bfloat16, device="cuda")
-        lse = torch.full((B, H, Nq), float("nan"), dtype=torch.float32, device="cuda")
-        stream = torch.cuda.current_stream().cuda_stream
-        rc = lib.attn_fwd_noalloc(qd.data_ptr(), kd.data_ptr(), vd.data_ptr(), o.data_ptr(), lse.data_ptr(),
-                                  B, H, Nq, Nk, 128, scale, stream)
-        assert rc == attn.ATTN_OK, attn.attn_status_string(rc)
-        assert attn.attn_fwd_status() == attn.ATTN_OK
-        o_np, l_np = bf16_to_np(o), lse.cpu().numpy()
-        assert np.all(np.isfinite(o_np)) and np.all(np.isfinite(l_np)), f"call {call}: unwritten output"
-        _same_within_tolerance(o_np, l_np, o_ref_np, l_ref_np)
+        _assert_same(_run(gpu_lib, "attn_fwd_noalloc", (B, H, Nq, Nk)), want, f"call {call}")
+
+
+def test_noalloc_second_call_on_another_shape(gpu_lib):
+    # the first call leaves partial records and counters of a many-group split in the array;
+    # the second splits fewer, longer groups at other points and must not see them
+    first, second = (1, 8, 4096, 8192), (2, 3, 520, 1290)
+    want = {s: _run(gpu_lib, "attn_fwd", s) for s in (first, second)}
+    for s in (first, second, first):
+        _assert_same(_run(gpu_lib, "attn_fwd_noalloc", s), want[s], f"shape {s}")
+
+
+def test_noalloc_allocates_nothing(gpu_lib):
+    import torch
+    if torch.cuda.get_allocator_backend() != "native":
+        pytest.skip("torch's own allocations come from the probed pool under this allocator backend")
+    drv = Driver()
+    shape = (1, 8, 4096, 8192)   # split work: attn_fwd needs its workspace here
+    want = _run(gpu_lib, "attn_fwd", shape)   # also loads the library's kernels on this device
+    s1, s2 = drv.new_stream(), drv.new_stream()
+    bufs1, bufs2 = _prepare(shape), _prepare(shape)
+
+    before = drv.pool_bytes()
+    _call(gpu_lib, "attn_fwd_noalloc", shape, bufs1, stream=s1)
+    after = drv.pool_bytes()
+    assert after == before, f"attn_fwd_noalloc changed the memory pool: {before} -> {after}"
+    _assert_same(_result(bufs1), want, "noalloc on a fresh stream")
+
+    # the probe sees an allocation: attn_fwd allocates its workspace on a stream it has not used
+    _call(gpu_lib, "attn_fwd", shape, bufs2, stream=s2)
+    assert drv.pool_bytes()[1] > after[1], "attn_fwd on a fresh stream did not allocate: the probe sees nothing"
+    _assert_same(_result(bufs2), want, "attn_fwd on a fresh stream")
 
 
 def test_noalloc_rejects_bad_arguments_like_attn_fwd(gpu_lib):
