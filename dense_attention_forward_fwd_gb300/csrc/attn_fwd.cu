@@ -1100,8 +1100,9 @@ __device__ void run_softmax(const Ctl& c, uint32_t tmem, uint8_t* stage, const P
 #pragma unroll
         for (int t = 0; t < 8; ++t) mx[t] = max3(mx[t], s[i + t], s[i + 8 + t]);  // s[i..i+15]
       }
-      const float m_tile =
-          fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])), fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) * cs;
+      const float m_raw =
+          fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])), fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+      const float m_tile = m_raw * cs;
       bool rescale = false;
       float alpha = 1.0f;
       if (m_tile > m_used + kTau) {
@@ -1123,13 +1124,18 @@ __device__ void run_softmax(const Ctl& c, uint32_t tmem, uint8_t* stage, const P
           tmem_st8(tO + ch * 8, ov);
         }
       }
+      const float neg_m = (kBias && m_used == -INFINITY) ? 0.0f : -m_used;   // every p is 0 then
       // The BF16 rounding of P matters most for the tile's largest term, which the stale
       // running max leaves anywhere in [1, 2^kRescaleLog2]. corr accumulates that term's
       // rounding error, so that l + corr is the sum of the weights the tensor core
-      // actually applies to V (up to the far smaller errors of the other terms).
+      // actually applies to V (up to the far smaller errors of the other terms). The term
+      // is recomputed with exactly the arithmetic that produces it below (one FMA of the
+      // raw maximum score, then ex2): a value computed another way can differ in its last
+      // bit and round to the other BF16 neighbour, which would put a whole BF16 ulp of the
+      // row's dominant weight into the sum.
       {
         // (with a bias a row may have seen only -inf so far: its largest term is then 0)
-        const float pm = (kBias && m_tile == -INFINITY) ? 0.0f : ex2(m_tile - m_used);
+        const float pm = (kBias && m_tile == -INFINITY) ? 0.0f : ex2(fmaf(m_raw, cs, neg_m));
         if constexpr (kP8)
           corr += round_e4m3(pm) - pm;
         else
@@ -1138,7 +1144,6 @@ __device__ void run_softmax(const Ctl& c, uint32_t tmem, uint8_t* stage, const P
       // p = 2^(s*cs - m) in two halves of 64 keys; each half is rounded to BF16, stored
       // over S in TMEM and handed to the MMA warp at once, so the first half of the
       // P V product runs while the second half is computed.
-      const float neg_m = (kBias && m_used == -INFINITY) ? 0.0f : -m_used;   // every p is 0 then
       float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
