@@ -34,6 +34,10 @@ half at the BF16 rate.
 --fp8 times attn_fwd_fp8: Q, K and V quantized per tensor to E4M3 (V passed transposed), P
 rounded to E4M3 for the P V product; the roofline peak is the FP8 rate for all FLOPs.
 
+--mxfp8 times attn_fwd_mxfp8: Q, K and V quantized to MXFP8 (E4M3 codes, one E8M0 scale per 32
+elements along d for Q and K, per 32 keys for V), both products block-scaled on the tensor
+cores; the roofline peak is the FP8 rate for all FLOPs.
+
 --impl reference times the FP64 CPU oracle (the plain definition) on host cores, on a
 bounded sample of query rows per step.
 """
@@ -84,11 +88,13 @@ def parse():
                     help="time attn_fwd_fp8qk (Q and K as FP8 E4M3 codes with per-tensor descale factors)")
     ap.add_argument("--fp8", action="store_true",
                     help="time attn_fwd_fp8 (Q, K and V as FP8 E4M3 codes, P rounded to E4M3 for P V)")
+    ap.add_argument("--mxfp8", action="store_true",
+                    help="time attn_fwd_mxfp8 (Q, K and V in MXFP8, both products block-scaled)")
     args = ap.parse_args()
-    if (args.fp8_qk or args.fp8) and (args.causal or args.backward or args.bias != "none"):
-        ap.error("--fp8-qk and --fp8 have no causal, bias or backward entry point; use them alone")
-    if args.fp8_qk and args.fp8:
-        ap.error("--fp8-qk and --fp8 are two entry points; pick one")
+    if (args.fp8_qk or args.fp8 or args.mxfp8) and (args.causal or args.backward or args.bias != "none"):
+        ap.error("--fp8-qk, --fp8 and --mxfp8 have no causal, bias or backward entry point; use them alone")
+    if args.fp8_qk + args.fp8 + args.mxfp8 > 1:
+        ap.error("--fp8-qk, --fp8 and --mxfp8 are different entry points; pick one")
     if args.bias != "none" and (args.causal or args.backward):
         ap.error("--bias has no causal or backward entry point; use it alone")
     return args
@@ -102,8 +108,11 @@ def run_config(w, args) -> dict:
     """The workload description both arms print (the reference arm times the same one)."""
     return {"workload": w.name, "B": w.B, "H": w.H, "Nq": w.Nq, "Nk": w.Nk, "d": w.d, "causal": args.causal,
             "bias": args.bias, "pass": "backward" if args.backward else "forward", "qk_mult": w.qk_mult,
-            "qk": "e4m3" if (args.fp8_qk or args.fp8) else "bf16", "pv": "e4m3" if args.fp8 else "bf16",
-            "inputs": ("iid N(0,1) (Q,K x qk_mult); Q, K, V quantized per tensor to E4M3 (descale = amax/448)"
+            "qk": "mxfp8" if args.mxfp8 else "e4m3" if (args.fp8_qk or args.fp8) else "bf16",
+            "pv": "mxfp8" if args.mxfp8 else "e4m3" if args.fp8 else "bf16",
+            "inputs": ("iid N(0,1) (Q,K x qk_mult); Q, K, V in MXFP8 (E4M3, E8M0 scale per 32 along d for Q, K "
+                       "and per 32 keys for V)" if args.mxfp8 else
+                       "iid N(0,1) (Q,K x qk_mult); Q, K, V quantized per tensor to E4M3 (descale = amax/448)"
                        if args.fp8 else
                        "iid N(0,1) (Q,K x qk_mult); Q, K quantized per tensor to E4M3 (descale = amax/448), V BF16"
                        if args.fp8_qk else "iid N(0,1) BF16 (Q,K x qk_mult)"),
@@ -153,7 +162,7 @@ def roofline_peak(args, peaks: dict, peak_src: str):
         return (2.0 / (1.0 / (2.0 * peak) + 1.0 / peak),
                 f"half the FLOPs at 2 x {peak_src} bf16_tflops (FP8 E4M3, nominal ratio 4.5/2.25), "
                 "half at bf16_tflops (burst)")
-    if args.fp8:
+    if args.fp8 or args.mxfp8:
         return 2.0 * peak, f"2 x {peak_src} bf16_tflops (FP8 E4M3, nominal ratio 4.5/2.25; burst)"
     return peak, f"{peak_src} bf16_tflops (burst: each launch is timed alone)"
 
@@ -162,7 +171,7 @@ def traffic_key(w, args) -> str:
     """The profiles/traffic.json key of this run's kernel and workload."""
     return (w.name + ("-causal" if args.causal else "") + ("" if args.bias == "none" else "-bias-" + args.bias)
             + ("-backward" if args.backward else "") + ("-fp8qk" if args.fp8_qk else "")
-            + ("-fp8" if args.fp8 else ""))
+            + ("-fp8" if args.fp8 else "") + ("-mxfp8" if args.mxfp8 else ""))
 
 
 def host_cores() -> int:
@@ -239,8 +248,12 @@ def workload_flops(w, causal: bool) -> float:
 # ------------------------------------------------------------------ reference arm (oracle) ---
 
 def oracle_rows_fn(oracle, w, causal: bool, bias_kind: str, H1: int, nq: int, fp8_qk: bool = False,
-                   fp8: bool = False):
+                   fp8: bool = False, mxfp8: bool = False):
     """The oracle entry point for this run's variant, as fn(q, k, v, scale, rows)."""
+    if mxfp8:   # Q, K and V of the same draw in MXFP8
+        from dense_attention_forward_fwd_gb300.inputs import make_qkv_mxfp8
+        q8, sq, k8, sk, v8, sv = make_qkv_mxfp8(1, H1, nq, w.Nk, d=w.d, seed=w.seed, qk_mult=w.qk_mult)
+        return lambda q, k, v, scale, rows: oracle.attention_rows_mxfp8(q8, sq, k8, sk, v8, sv, scale, rows)
     if fp8:   # Q, K and V of the same draw as E4M3 codes
         from dense_attention_forward_fwd_gb300.inputs import make_qkv_e4m3
         q8, k8, v8, dq, dk, dv = make_qkv_e4m3(1, H1, nq, w.Nk, d=w.d, seed=w.seed, qk_mult=w.qk_mult)
@@ -281,7 +294,7 @@ def cpu_oracle_backward_sample(w, target_seconds: float, causal: bool = False):
 
 
 def cpu_oracle_sample(w, target_seconds: float, rank_seed: int = 0, causal: bool = False, bias_kind: str = "none",
-                      fp8_qk: bool = False, fp8: bool = False):
+                      fp8_qk: bool = False, fp8: bool = False, mxfp8: bool = False):
     """Time the FP64 oracle on a sample of query rows; returns (TFLOPS, rows, seconds, threads)."""
     import numpy as np
 
@@ -294,7 +307,7 @@ def cpu_oracle_sample(w, target_seconds: float, rank_seed: int = 0, causal: bool
     nq = min(w.Nq, 4096)
     q, k, v = make_qkv(1, H1, nq, w.Nk, d=w.d, seed=w.seed + rank_seed, qk_mult=w.qk_mult)
     threads = oracle.max_threads()
-    fn = oracle_rows_fn(oracle, w, causal, bias_kind, H1, nq, fp8_qk, fp8)
+    fn = oracle_rows_fn(oracle, w, causal, bias_kind, H1, nq, fp8_qk, fp8, mxfp8)
 
     def flop_rows(rows):   # 4*d FLOPs per visible key of each sampled row
         if not causal:
@@ -354,7 +367,7 @@ def run_reference(args, w):
     q, k, v = make_qkv(1, H1, nq, w.Nk, d=w.d, seed=w.seed, qk_mult=w.qk_mult)
     threads = oracle.max_threads()
     n_rows_total = q.shape[1] * q.shape[2]
-    fn = oracle_rows_fn(oracle, w, args.causal, args.bias, H1, nq, args.fp8_qk, args.fp8)
+    fn = oracle_rows_fn(oracle, w, args.causal, args.bias, H1, nq, args.fp8_qk, args.fp8, args.mxfp8)
 
     def flop_rows(rows):   # 4*d FLOPs per visible key; causal sample rows sit at the end of the sequence
         if not args.causal:
@@ -436,6 +449,18 @@ def run_ours(args, w):
         if args.fp8:   # V^T, keys innermost (Nk of every workload is a multiple of 16)
             x8[2] = x8[2].transpose(2, 3).contiguous()
         ins = [x8[0], x8[1], x8[2] if args.fp8 else v]
+    if args.mxfp8:   # E4M3 codes with an E8M0 scale per 32 elements: along d for Q and K, keys for V
+        def mx(x, dim):
+            xb = x.float().movedim(dim, -1)
+            blocks = xb.reshape(*xb.shape[:-1], -1, 32)
+            amax = blocks.abs().amax(dim=-1).clamp_min(torch.finfo(torch.float32).tiny)
+            e = (torch.floor(torch.log2(amax)) - 8).clamp(-127, 127)
+            codes = (blocks / torch.exp2(e)[..., None]).clamp(-448, 448).to(torch.float8_e4m3fn)
+            return codes.reshape(xb.shape), (e + 127).to(torch.uint8)
+        q8, sq = mx(q, 3)
+        k8, sk = mx(k, 3)
+        vt8, svt = mx(v.transpose(2, 3), 3)   # V^T [B,H,d,Nk]: blocks of 32 keys (Nk a multiple of 128)
+        ins = [q8.contiguous(), sq.contiguous(), k8.contiguous(), sk.contiguous(), vt8.contiguous(), svt.contiguous()]
     outs = [o, lse]
     if args.bias != "none":
         bshape = (1, 1, w.Nq, w.Nk) if args.bias == "shared" else (w.B, w.H, w.Nq, w.Nk)
@@ -456,6 +481,8 @@ def run_ours(args, w):
             attn.attn_fwd_causal(*ins_, *outs_, w.B, w.H, w.Nq, w.Nk, w.d, w.scale, st)
         elif args.fp8_qk:
             attn.attn_fwd_fp8qk(*ins_, *outs_, w.B, w.H, w.Nq, w.Nk, w.d, w.scale, descale[0], descale[1], st)
+        elif args.mxfp8:
+            attn.attn_fwd_mxfp8(*ins_, *outs_, w.B, w.H, w.Nq, w.Nk, w.d, w.scale, st)
         elif args.fp8:
             attn.attn_fwd_fp8(*ins_, *outs_, w.B, w.H, w.Nq, w.Nk, w.d, w.scale, descale[0], descale[1], descale[2],
                               st)
@@ -578,8 +605,9 @@ def run_ours(args, w):
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": ((value / PAGES_TFLOPS[w.name])
                         if w.name in PAGES_TFLOPS and not args.causal and args.bias == "none" and not args.backward
-                        and not args.fp8_qk and not args.fp8 else None),
-        "dtype": "e4m3" if args.fp8 else "e4m3+bf16" if args.fp8_qk else "bf16", "data": "synthetic",
+                        and not args.fp8_qk and not args.fp8 and not args.mxfp8 else None),
+        "dtype": "mxfp8" if args.mxfp8 else "e4m3" if args.fp8 else "e4m3+bf16" if args.fp8_qk else "bf16",
+        "data": "synthetic",
         "config": run_config(w, args),
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak, "traffic": traffic, "peak_source": peak_note},
@@ -596,7 +624,7 @@ def run_ours(args, w):
             sample = f"backward of one head with {n} query rows x {w.Nk} keys of {w.describe()}, FP64, {dt:.1f} s"
         else:
             tfl, n, dt, thr = cpu_oracle_sample(w, args.cpu_seconds, causal=args.causal, bias_kind=args.bias,
-                                                fp8_qk=args.fp8_qk, fp8=args.fp8)
+                                                fp8_qk=args.fp8_qk, fp8=args.fp8, mxfp8=args.mxfp8)
             keys = "visible keys of each row, causal" if args.causal else "full Nk each"
             sample = f"{n} query rows of {w.describe()} ({keys}), FP64, {dt:.1f} s"
         line["cpu_baseline"] = {"value": tfl, "unit": "TFLOP/s", "cores": thr, "kind": "oracle", "sample": sample}

@@ -15,7 +15,7 @@ from ._build import LIB_PATH, build_library
 
 __all__ = [
     "ATTN_OK", "ATTN_ERR_INVALID_ARG", "ATTN_ERR_UNSUPPORTED", "ATTN_ERR_MISALIGNED", "ATTN_ERR_CUDA",
-    "ATTN_ERR_TIMEOUT", "AttnError", "load_library", "attn_fwd", "attn_fwd_causal", "attn_fwd_bias", "attn_fwd_fp8qk", "attn_fwd_fp8", "attn_fwd_o32", "attn_fwd_noalloc", "attn_fwd_status", "attn_status_string",
+    "ATTN_ERR_TIMEOUT", "AttnError", "load_library", "attn_fwd", "attn_fwd_causal", "attn_fwd_bias", "attn_fwd_fp8qk", "attn_fwd_fp8", "attn_fwd_mxfp8", "attn_fwd_o32", "attn_fwd_noalloc", "attn_fwd_status", "attn_status_string",
     "attn_fwd_set_wait_limit", "attn_fwd_kernel_count", "attention", "attn_bwd", "attn_bwd_causal", "attn_bwd_status",
     "attn_bwd_kernel_count", "attn_bwd_set_wait_limit",
 ]
@@ -56,6 +56,9 @@ def load_library(build_if_stale: bool = True) -> ctypes.CDLL:
             lib.attn_fwd_fp8.argtypes = [vp, vp, vp, ctypes.c_longlong, vp, vp, i32, i32, i32, i32, i32, f32, f32, f32,
                                          f32, vp]
             lib.attn_fwd_fp8.restype = i32
+            lib.attn_fwd_mxfp8.argtypes = [vp, vp, vp, vp, vp, ctypes.c_longlong, vp, ctypes.c_longlong, vp, vp, i32, i32,
+                                           i32, i32, i32, f32, vp]
+            lib.attn_fwd_mxfp8.restype = i32
             i64 = ctypes.c_longlong
             lib.attn_fwd_bias.argtypes = [vp, vp, vp, vp, i64, i64, i64, vp, vp, i32, i32, i32, i32, i32, f32, vp]
             lib.attn_fwd_noalloc.restype = i32
@@ -194,6 +197,35 @@ def attn_fwd_fp8(q8, k8, vt8, o, lse, B: int, H: int, Nq: int, Nk: int, d: int, 
                           _stream_handle(stream, q8, k8, vt8, o, lse))
     if rc != ATTN_OK:
         raise AttnError(rc, "attn_fwd_fp8")
+
+
+def attn_fwd_mxfp8(q8, sq, k8, sk, vt8, svt, o, lse, B: int, H: int, Nq: int, Nk: int, d: int, scale: float,
+                   stream=None, ldv: int | None = None, ldsv: int | None = None) -> None:
+    """Attention from MXFP8 inputs (see include/attn_fwd.h): E4M3 codes q8 [B,H,Nq,d] and
+    k8 [B,H,Nk,d] with E8M0 scales sq [B,H,Nq,d/32] and sk [B,H,Nk,d/32] (32 elements along
+    d), V transposed as codes vt8 [B,H,d,ldv] (keys innermost) with scales svt [B,H,d,ldsv]
+    (byte t of a row: keys 32t .. 32t+31). A tensor's last dimension is taken as ldv / ldsv.
+    O (BF16) and LSE (FP32) as in attn_fwd."""
+    lib = load_library()
+    for name, t, want in (("vt8", vt8, (B, H, d)), ("svt", svt, (B, H, d))):
+        if _is_tensor(t) and (t.dim() != 4 or tuple(t.shape[:3]) != want):
+            raise ValueError(f"{name} must be [B, H, d, row bytes] = [{B}, {H}, {d}, ...], got {tuple(t.shape)}")
+    if _is_tensor(vt8):
+        ldv = int(vt8.shape[3])
+    if _is_tensor(svt):
+        ldsv = int(svt.shape[3])
+    if ldv is None or ldsv is None:
+        raise ValueError("ldv and ldsv are required with integer pointers")
+    args = (
+        _ptr(q8, "q8", B * H * Nq * d, "e4m3"), _ptr(sq, "sq", B * H * Nq * (d // 32), "e4m3"),
+        _ptr(k8, "k8", B * H * Nk * d, "e4m3"), _ptr(sk, "sk", B * H * Nk * (d // 32), "e4m3"),
+        _ptr(vt8, "vt8", B * H * d * ldv, "e4m3"), int(ldv), _ptr(svt, "svt", B * H * d * ldsv, "e4m3"), int(ldsv),
+        _ptr(o, "o", B * H * Nq * d, "bf16"), _ptr(lse, "lse", B * H * Nq, "f32"),
+    )
+    rc = lib.attn_fwd_mxfp8(*args, int(B), int(H), int(Nq), int(Nk), int(d), float(scale),
+                            _stream_handle(stream, q8, k8, vt8, o, lse))
+    if rc != ATTN_OK:
+        raise AttnError(rc, "attn_fwd_mxfp8")
 
 
 def attn_fwd_bias(q, k, v, bias, o, lse, B: int, H: int, Nq: int, Nk: int, d: int, scale: float, stream=None,

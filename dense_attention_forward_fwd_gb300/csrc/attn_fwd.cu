@@ -116,7 +116,8 @@ constexpr int kBarPFull = kBarSFull + kQTiles;     // [tile][half]: one barrier 
 constexpr int kBarOFull = kBarPFull + 2 * kQTiles;
 constexpr int kBarOEmpty = kBarOFull + kQTiles;    // the epilogue has read O_i out of TMEM
 constexpr int kBarDrain = kBarOEmpty + kQTiles;
-constexpr int kNumBars = kBarDrain + 1;
+constexpr int kBarSfReady = kBarDrain + 1;         // [tile]: the scale factors of S_tile's next product are in TMEM (MXFP8)
+constexpr int kNumBars = kBarSfReady + kQTiles;
 constexpr int kOffTmemSlot = kOffBar + kNumBars * 8;
 constexpr int kOffAbort = kOffTmemSlot + 4;
 // Per softmax warp, a staging tile for its 32 rows x 64 columns of BF16 output.
@@ -165,6 +166,11 @@ struct Params {
   float scale;            // the caller's scale (the bias path scales before adding B)
   float v_scale = 1.0f;   // V's descale factor (V as FP8 codes), applied with 1 / l
   float* o32 = nullptr;   // FP32 [BH, Nq, 128]: O before rounding (kernels instantiated with kO32)
+  // MXFP8 inputs (kF8 == 3): E8M0 block scales, byte b of a word for elements 32b .. 32b+31
+  const uint32_t* sfq = nullptr;   // [BH, Nq]: a query row's four scales along d
+  const uint32_t* sfk = nullptr;   // [BH, Nk]: a key row's four scales along d
+  const uint8_t* sfv = nullptr;    // [BH, 128, ldsv]: row c of V^T, byte t = keys 32t .. 32t+31
+  long long ldsv = 0;
 };
 
 // floor(a / b) for a >= 0, b > 0. On the device a 64-bit division is a long dependent
@@ -367,6 +373,28 @@ __device__ __forceinline__ void mma_ts(uint32_t d, uint32_t a, uint64_t b, uint3
       "setp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d),
       "r"(a), "l"(b), "r"(idesc), "r"(static_cast<uint32_t>(acc))
+      : "memory");
+}
+
+// D(tmem) (+)= A(smem desc) * B(smem desc), E4M3 operands scaled per 32 elements of K by E8M0
+// factors read from TMEM (sfa for the rows of A, sfb for the rows of B)
+__device__ __forceinline__ void mma_ss_mx(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t sfa, uint32_t sfb,
+                                          bool acc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(d),
+      "l"(a), "l"(b), "r"(idesc), "r"(sfa), "r"(sfb), "r"(static_cast<uint32_t>(acc))
+      : "memory");
+}
+// D(tmem) (+)= A(tmem) * B(smem desc), scaled as mma_ss_mx
+__device__ __forceinline__ void mma_ts_mx(uint32_t d, uint32_t a, uint64_t b, uint32_t idesc, uint32_t sfa, uint32_t sfb,
+                                          bool acc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], [%1], %2, %3, [%4], [%5], p;\n\t}" ::"r"(d),
+      "r"(a), "l"(b), "r"(idesc), "r"(sfa), "r"(sfb), "r"(static_cast<uint32_t>(acc))
       : "memory");
 }
 
@@ -624,6 +652,14 @@ __host__ __device__ constexpr uint32_t idesc_e4m3() {
   return (1u << 4) | (static_cast<uint32_t>(kBN >> 3) << 17) | (static_cast<uint32_t>(kBM >> 4) << 24);
 }
 
+// kind::mxf8f6f4 with block scaling: E4M3 x E4M3 -> FP32, M = 128, N = 128, both K-major, E8M0
+// scale factors (bit 23), the scale byte of A's and B's rows chosen by sf (bits 29-30 and
+// 4-5): byte sf of each 32-bit scale column holds the factor of K block sf.
+__host__ __device__ constexpr uint32_t idesc_mx(uint32_t sf) {
+  return (sf << 4) | (static_cast<uint32_t>(kBN >> 3) << 17) | (1u << 23) | (static_cast<uint32_t>(kBM >> 4) << 24) |
+         (sf << 29);
+}
+
 // ---------------------------------------------------------------------------------
 // Bounded waits
 // ---------------------------------------------------------------------------------
@@ -682,7 +718,7 @@ __device__ void run_producer(const Ctl& c, uint32_t base, const CUtensorMap* tmQ
     const int q_row0 = (sg.group % p.q_groups) * (kQTiles * kBM);
     // the previous segment's S MMAs must be done with the Q tiles
     if (u > 0 && !wait_phase(c, kBarQEmpty, (u - 1) & 1, true)) break;
-    constexpr bool kQK8 = kF8 >= 1, kV8 = kF8 == 2;
+    constexpr bool kQK8 = kF8 >= 1, kV8 = kF8 >= 2;
     mbar_arrive_expect_tx(c.bar(kBarQFull), kQTiles * (kQK8 ? kTile8Bytes : kTileBytes));
     for (int i = 0; i < kQTiles; ++i)
       for (int h = 0; h < (kQK8 ? 1 : 2); ++h)
@@ -755,6 +791,25 @@ __device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint32_t q_smem, uint3
   }
 }
 
+// S = Q K^T from MXFP8 codes: four K32 blocks of the head dimension, block kk scaled by byte kk
+// of the scale columns at sfa (rows of Q) and sfb (rows of K).
+__device__ __forceinline__ void issue_qk_mx(uint32_t d_tmem, uint32_t q_smem, uint32_t k_smem, uint32_t sfa, uint32_t sfb) {
+#pragma unroll
+  for (int kk = 0; kk < kD / 32; ++kk) {
+    const uint32_t off = static_cast<uint32_t>(kk * 32);
+    mma_ss_mx(d_tmem, sdesc_sw128(q_smem + off, 16, 1024), sdesc_sw128(k_smem + off, 16, 1024),
+              idesc_mx(static_cast<uint32_t>(kk)), sfa, sfb, kk > 0);
+  }
+}
+// keys [64*half, 64*half + 64) of O += P V with P and V^T as MXFP8 (key blocks 2*half, 2*half + 1)
+__device__ __forceinline__ void issue_pv_half_mx(uint32_t d_tmem, uint32_t p_tmem, uint32_t v_smem, int half, bool acc,
+                                                 uint32_t sfa, uint32_t sfb) {
+#pragma unroll
+  for (int kk = 2 * half; kk < 2 * half + 2; ++kk)
+    mma_ts_mx(d_tmem, p_tmem + kk * 8, sdesc_sw128(v_smem + kk * 32, 16, 1024), idesc_mx(static_cast<uint32_t>(kk)),
+              sfa, sfb, acc || kk > 0);
+}
+
 // keys [64*half, 64*half + 64) of O += P V
 template <bool kPV8>
 __device__ __forceinline__ void issue_pv_half(uint32_t d_tmem, uint32_t p_tmem, uint32_t v_smem, int half, bool acc) {
@@ -785,6 +840,11 @@ __device__ __forceinline__ void issue_pv_half(uint32_t d_tmem, uint32_t p_tmem, 
 // about a hundred cycles (its queue is shallow), so a step does only the four P waits
 // and two commits: softmax threads check and release the ring slots.
 // Returns false when a wait gave up.
+// MXFP8 (kF8 == 3): the scale factors of S_i's next product sit in the other tile's S
+// columns 96..103 (written by the other tile's softmax once it holds its own scores), those
+// of P_i V in S_i's columns 32..39 (written with P_i); see run_softmax.
+__device__ __forceinline__ uint32_t mx_sf_qk(const uint32_t (&tS)[2], int i) { return tS[1 - i] + 96; }
+
 template <bool kMore, int kF8>
 __device__ __forceinline__ bool mma_step(const Ctl& c, uint32_t base, const uint32_t (&tS)[2],
                                          const uint32_t (&tO)[2], const uint32_t (&sQ)[2], int unit,
@@ -792,33 +852,35 @@ __device__ __forceinline__ bool mma_step(const Ctl& c, uint32_t base, const uint
   const int pr = unit % kPairs;
   const uint32_t sV = base + kOffKV + 2 * pr * kTileBytes;
   const uint32_t sK = sV + kTileBytes;
-  // tile 0: O0 += P0 V_j, then S0 = Q0 K_{j+1}^T. The first half of P0 is handed over only
-  // after a softmax thread has seen the unit loaded, so this wait covers the unit too.
-  if (!wait_phase(c, kBarPFull + 0, ph, true)) return false;
-  tc_fence_after();
-  constexpr bool kQK8 = kF8 >= 1, kPV8 = kF8 == 2;
-  issue_pv_half<kPV8>(tO[0], tS[0], sV, 0, !first);
-  if (!wait_phase(c, kBarPFull + 1, ph, true)) return false;
-  tc_fence_after();
-  issue_pv_half<kPV8>(tO[0], tS[0], sV, 1, true);
-  if (kMore) {
-    issue_qk<kQK8>(tS[0], sQ[0], sK);
-    tc_commit(c.bar(kBarSFull + 0));
-  } else {
-    tc_commit(c.bar(kBarOFull + 0));
-  }
-  // tile 1: O1 += P1 V_j, then S1 = Q1 K_{j+1}^T
-  if (!wait_phase(c, kBarPFull + 2, ph, true)) return false;
-  tc_fence_after();
-  issue_pv_half<kPV8>(tO[1], tS[1], sV, 0, !first);
-  if (!wait_phase(c, kBarPFull + 3, ph, true)) return false;
-  tc_fence_after();
-  issue_pv_half<kPV8>(tO[1], tS[1], sV, 1, true);
-  if (kMore) {
-    issue_qk<kQK8>(tS[1], sQ[1], sK);
-    tc_commit(c.bar(kBarSFull + 1));
-  } else {
-    tc_commit(c.bar(kBarOFull + 1));
+  constexpr bool kQK8 = kF8 >= 1, kPV8 = kF8 >= 2, kMX = kF8 == 3;
+#pragma unroll
+  for (int i = 0; i < kQTiles; ++i) {
+    // tile i: O_i += P_i V_j, then S_i = Q_i K_{j+1}^T. The first half of P_0 is handed over
+    // only after a softmax thread has seen the unit loaded, so that wait covers the unit too.
+    if (!wait_phase(c, kBarPFull + 2 * i, ph, true)) return false;
+    tc_fence_after();
+    if constexpr (kMX)
+      issue_pv_half_mx(tO[i], tS[i], sV, 0, !first, tS[i] + 32, tS[i] + 36);
+    else
+      issue_pv_half<kPV8>(tO[i], tS[i], sV, 0, !first);
+    if (!wait_phase(c, kBarPFull + 2 * i + 1, ph, true)) return false;
+    tc_fence_after();
+    if constexpr (kMX)
+      issue_pv_half_mx(tO[i], tS[i], sV, 1, true, tS[i] + 32, tS[i] + 36);
+    else
+      issue_pv_half<kPV8>(tO[i], tS[i], sV, 1, true);
+    if (kMore) {
+      if constexpr (kMX) {
+        if (!wait_phase(c, kBarSfReady + i, ph ^ 1u, true)) return false;
+        tc_fence_after();
+        issue_qk_mx(tS[i], sQ[i], sK, mx_sf_qk(tS, i), mx_sf_qk(tS, i) + 4);
+      } else {
+        issue_qk<kQK8>(tS[i], sQ[i], sK);
+      }
+      tc_commit(c.bar(kBarSFull + i));
+    } else {
+      tc_commit(c.bar(kBarOFull + i));
+    }
   }
   return true;
 }
@@ -840,10 +902,19 @@ __device__ void run_mma(const Ctl& c, uint32_t base, uint32_t tmem, const Params
       break;
     tc_fence_after();
     const uint32_t sK = base + kOffKV + 2 * (unit % kPairs) * kTileBytes;   // unit {K_0}
-    issue_qk<(kF8 >= 1)>(tS[0], sQ[0], sK);
-    tc_commit(c.bar(kBarSFull + 0));
-    issue_qk<(kF8 >= 1)>(tS[1], sQ[1], sK);
-    tc_commit(c.bar(kBarSFull + 1));
+    bool sf_ok = true;
+    for (int i = 0; i < kQTiles && sf_ok; ++i) {
+      if constexpr (kF8 == 3) {
+        sf_ok = wait_phase(c, kBarSfReady + i, gstep & 1u, true);
+        if (!sf_ok) break;
+        tc_fence_after();
+        issue_qk_mx(tS[i], sQ[i], sK, mx_sf_qk(tS, i), mx_sf_qk(tS, i) + 4);
+      } else {
+        issue_qk<(kF8 >= 1)>(tS[i], sQ[i], sK);
+      }
+      tc_commit(c.bar(kBarSFull + i));
+    }
+    if (!sf_ok) break;
     if (n == 1) tc_commit(c.bar(kBarQEmpty));   // the segment's last S MMA is issued
     // The segment's first P V products overwrite O: the previous segment's epilogue must
     // have read both accumulators out of TMEM.
@@ -990,7 +1061,13 @@ __device__ void merge_split_row(const Params& p, int tile, int r, int c_first, i
 // running max then moves once it grows by 8 (log2 units), so that every p <= 2^8 stays
 // below E4M3's largest value 448, and O is scaled by V's descale factor with 1 / l.
 // kO32: O is written in FP32 to p.o32 (the value the BF16 output is rounded from).
-template <bool kPosScale, bool kBias, bool kP8 = false, bool kO32 = false>
+// kMX (with kP8): Q, K and V are MXFP8; each tile's softmax warps also write scale factors
+// into TMEM, in the layout the block-scaled MMA reads (each 32-lane quarter holds the same
+// 4 columns: lane l, column c = the 4 scale bytes of operand row l + 32c, byte t for K block
+// t): those of its own P V product (P's, all 2^0, and V^T's) at S columns 32..39 with P, and
+// those of the other tile's next Q K^T (the other tile's Q rows and the key tile's K rows) at
+// S columns 96..103, right after it has read its own scores out of those columns.
+template <bool kPosScale, bool kBias, bool kP8 = false, bool kO32 = false, bool kMX = false>
 __device__ void run_softmax(const Ctl& c, uint32_t tmem, uint8_t* stage, const Params& p, int tile) {
   constexpr float kTau = kP8 ? 8.0f : kRescaleLog2;
   const int quarter = (threadIdx.x >> 5) & 3;   // TMEM lanes this warp may access
@@ -1038,8 +1115,61 @@ __device__ void run_softmax(const Ctl& c, uint32_t tmem, uint8_t* stage, const P
       br.piece = p.bias + static_cast<long long>(bh / p.H) * p.bias_sb + static_cast<long long>(bh % p.H) * p.bias_sh +
                  static_cast<long long>(seg_row0 + (lane >> 3)) * p.bias_sq + 8 * (lane & 7);
     }
+    // MXFP8: the other tile's query scales for the whole segment; per step, the scales of
+    // the key tile whose Q K^T the other tile computes next and of this step's V^T tile
+    uint32_t sf_qo[kMX ? 4 : 1], sf_k[kMX ? 4 : 1], sf_v[kMX ? 4 : 1];
+    const int bh_mx = sg.group / p.q_groups;
+    auto mx_load_k = [&](int kt) {   // key tile kt: rows kt*128 + lane + 32c
+      if constexpr (kMX) {
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc) {
+          const int key = kt * kBN + lane + 32 * cc;
+          sf_k[cc] = key < p.Nk ? __ldg(p.sfk + static_cast<size_t>(bh_mx) * p.Nk + key) : 0x7F7F7F7Fu;
+        }
+      }
+    };
+    auto mx_load_v = [&](int kt) {   // V^T rows lane + 32c, key blocks 4kt .. 4kt+3 (past the keys: 2^0)
+      if constexpr (kMX) {
+        const int nkb = (p.Nk + 31) / 32;
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc) {
+          uint32_t w = __ldg(reinterpret_cast<const uint32_t*>(
+              p.sfv + (static_cast<size_t>(bh_mx) * kD + lane + 32 * cc) * static_cast<size_t>(p.ldsv) + 4 * kt));
+#pragma unroll
+          for (int t = 0; t < 4; ++t)
+            if (4 * kt + t >= nkb) w = (w & ~(0xFFu << (8 * t))) | (0x7Fu << (8 * t));
+          sf_v[cc] = w;
+        }
+      }
+    };
+    auto mx_store_qk = [&]() {   // the other tile's next Q K^T: its Q rows, then the key rows
+      if constexpr (kMX) {
+        const uint32_t w[8] = {sf_qo[0], sf_qo[1], sf_qo[2], sf_qo[3], sf_k[0], sf_k[1], sf_k[2], sf_k[3]};
+        tmem_st8(tS + 96, w);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(c.bar(kBarSfReady + (1 - tile)));
+        __syncwarp();
+      }
+    };
+    if constexpr (kMX) {
+      const int orow0 = (sg.group % p.q_groups) * (kQTiles * kBM) + (1 - tile) * kBM;
+#pragma unroll
+      for (int cc = 0; cc < 4; ++cc) {
+        const int row = orow0 + lane + 32 * cc;
+        sf_qo[cc] = row < p.Nq ? __ldg(p.sfq + static_cast<size_t>(bh_mx) * p.Nq + row) : 0x7F7F7F7Fu;
+      }
+      if (tile == 1) {   // the segment's first S_0: S_1's columns are free once the last segment ended
+        mx_load_k(sg.kv0);
+        mx_store_qk();
+      }
+    }
     for (int j = 0; j < n; ++j) {
       if constexpr (kBias) load_bias_pieces(bg, br, p.Nq, (sg.kv0 + j) * kBN, p.Nk);
+      if constexpr (kMX) {   // loads in flight while the step's scores are awaited
+        mx_load_v(sg.kv0 + j);
+        if (tile == 0 || j + 1 < n) mx_load_k(sg.kv0 + j + tile);
+      }
       if (!wait_warp(c, kBarSFull + tile, (gstep + static_cast<uint32_t>(j)) & 1u)) return;
       if (releaser) mbar_arrive(c.bar(kBarKVEmpty + (unit + j) % kPairs));
       const int ring_unit = unit + j + 1;
@@ -1075,6 +1205,13 @@ __device__ void run_softmax(const Ctl& c, uint32_t tmem, uint8_t* stage, const P
 #pragma unroll
           for (int i = 0; i < 128; ++i) s[i] *= p.scale_log2;
         }
+      }
+      if constexpr (kMX) {
+        // the scores are in registers: this step's P V scales go next to P (P's own are 2^0),
+        // and the other tile's next Q K^T scales into columns 96..103
+        const uint32_t wv[8] = {0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu, sf_v[0], sf_v[1], sf_v[2], sf_v[3]};
+        tmem_st8(tS + 32, wv);
+        if (tile == 0 || j + 1 < n) mx_store_qk();
       }
       if (sg.kv0 + j == p.n_kv - 1 && p.kv_tail < kBN) {
         const int valid = p.kv_tail;
@@ -1333,6 +1470,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(c.bar(kBarOEmpty + t), 4);          // one arrival per softmax warp
     }
     mbar_init(c.bar(kBarDrain), 1);
+    for (int t = 0; t < kQTiles; ++t) mbar_init(c.bar(kBarSfReady + t), 4);   // one arrival per softmax warp
     *c.abort = 0u;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -1360,7 +1498,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsSoftmax));
-    run_softmax<kPosScale, kBias, kF8 == 2, kO32>(c, tmem, smem + kOffStage + (warp - 4) * kStageBytes, p, (warp >> 2) - 1);
+    run_softmax<kPosScale, kBias, kF8 >= 2, kO32, kF8 == 3>(c, tmem, smem + kOffStage + (warp - 4) * kStageBytes, p, (warp >> 2) - 1);
   }
 
   tc_fence_before();
@@ -1427,7 +1565,7 @@ bool make_map_vt(CUtensorMap* map, const void* ptr, int Nk, long long ldv, long 
 }
 
 constexpr int kMaxDevices = 64;
-std::atomic<int> g_attr_done[14][kMaxDevices];   // per instantiation (kPos + 2 * kBias + 4 * kF8, 12 + kPos for kO32)
+std::atomic<int> g_attr_done[18][kMaxDevices];   // per instantiation (kPos + 2 * kBias + 4 * kF8, 16 + kPos for kO32)
 std::atomic<int> g_sm_count[kMaxDevices];
 
 int sm_count(int dev) {
@@ -1516,7 +1654,7 @@ template <bool kPos, bool kBias = false, int kF8 = 0, bool kO32 = false>
 int launch(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, const Params& p, int grid,
            int dev, cudaStream_t stream) {
   auto kern = attn_fwd_kernel<kPos, kBias, kF8, kO32>;
-  constexpr int kInst = kO32 ? 12 + (kPos ? 1 : 0) : (kPos ? 1 : 0) + (kBias ? 2 : 0) + 4 * kF8;
+  constexpr int kInst = kO32 ? 16 + (kPos ? 1 : 0) : (kPos ? 1 : 0) + (kBias ? 2 : 0) + 4 * kF8;
   if (dev < 0 || dev >= kMaxDevices || !g_attr_done[kInst][dev].load(std::memory_order_acquire)) {
     // The in-kernel register split (setmaxnreg) balances only at kRegsLaunch registers
     // per thread; at any other count the increase would never be granted. Refuse.
@@ -1541,13 +1679,21 @@ struct BiasArg {
   long long sb, sh, sq;
 };
 
+// MXFP8 block scales (attn_fwd_mxfp8)
+struct MxArg {
+  const void* sq;   // [BH, Nq, 4] bytes
+  const void* sk;   // [BH, Nk, 4] bytes
+  const void* svt;  // [BH, 128, ldsv] bytes
+  long long ldsv;
+};
+
 // attn_fwd, attn_fwd_bias (bias != nullptr), attn_fwd_fp8qk (f8 = 1: q and k hold FP8 E4M3
 // codes), attn_fwd_fp8 (f8 = 2: v too, as V^T with row stride ldv, descaled by v_scale) and
 // attn_fwd_o32 (o32 != nullptr: O in FP32 there, o unused): the argument rules, the plan,
 // the launch.
 int forward(const void* q, const void* k, const void* v, const BiasArg* bias, void* o, float* lse, int B, int H,
             int Nq, int Nk, int d, float scale, void* stream, int f8 = 0, long long ldv = 0, float v_scale = 1.0f,
-            float* o32 = nullptr) {
+            float* o32 = nullptr, const MxArg* mx = nullptr) {
   const bool qk8 = f8 >= 1;
   if (B < 0 || H < 0 || Nq < 0 || Nk < 0) return ATTN_ERR_INVALID_ARG;
   if (d != kD) return ATTN_ERR_UNSUPPORTED;
@@ -1567,12 +1713,24 @@ int forward(const void* q, const void* k, const void* v, const BiasArg* bias, vo
   // element counts must fit a signed 64-bit byte offset
   const long long max_rows = static_cast<long long>(Nq > Nk ? Nq : Nk);
   if (bh > (LLONG_MAX / 256) / max_rows) return ATTN_ERR_INVALID_ARG;
-  if (f8 == 2) {
+  if (f8 >= 2) {
     // V^T rows of ldv bytes: at least Nk, 16-byte multiples (TMA strides), and the last
     // byte's offset, bh * 128 * ldv, must fit a signed 64-bit offset
     if (ldv < Nk) return ATTN_ERR_INVALID_ARG;
     if (ldv % 16 != 0) return ATTN_ERR_MISALIGNED;
     if (bh > (LLONG_MAX / kD) / ldv) return ATTN_ERR_INVALID_ARG;
+  }
+  if (f8 == 3) {
+    // scale rows: 4 bytes per Q or K row (read as words); V^T scale rows of ldsv bytes, a
+    // word per key tile of 128, so at least 4 * ceil(Nk / 128) bytes (those past the last
+    // key block are read and replaced by 2^0)
+    if (mx == nullptr || !mx->sq || !mx->sk || !mx->svt) return ATTN_ERR_INVALID_ARG;
+    const long long n_kv = (static_cast<long long>(Nk) + kBN - 1) / kBN;
+    if (mx->ldsv < 4 * n_kv) return ATTN_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(mx->sq) | reinterpret_cast<uintptr_t>(mx->sk) |
+         reinterpret_cast<uintptr_t>(mx->svt)) & 3u || mx->ldsv % 16 != 0)
+      return ATTN_ERR_MISALIGNED;
+    if (bh > (LLONG_MAX / kD) / mx->ldsv) return ATTN_ERR_INVALID_ARG;
   }
   if (bias != nullptr) {
     if (!bias->ptr || bias->sb < 0 || bias->sh < 0 || bias->sq < 0) return ATTN_ERR_INVALID_ARG;
@@ -1594,7 +1752,7 @@ int forward(const void* q, const void* k, const void* v, const BiasArg* bias, vo
 
   CUtensorMap mq, mk, mv;
   if (!make_map(&mq, q, Nq, bh, qk8) || !make_map(&mk, k, Nk, bh, qk8) ||
-      !(f8 == 2 ? make_map_vt(&mv, v, Nk, ldv, bh) : make_map(&mv, v, Nk, bh)))
+      !(f8 >= 2 ? make_map_vt(&mv, v, Nk, ldv, bh) : make_map(&mv, v, Nk, bh)))
     return ATTN_ERR_CUDA;
 
   Params p;
@@ -1626,6 +1784,12 @@ int forward(const void* q, const void* k, const void* v, const BiasArg* bias, vo
   p.scale = scale;
   p.v_scale = v_scale;
   p.o32 = o32;
+  if (mx != nullptr) {
+    p.sfq = static_cast<const uint32_t*>(mx->sq);
+    p.sfk = static_cast<const uint32_t*>(mx->sk);
+    p.sfv = static_cast<const uint8_t*>(mx->svt);
+    p.ldsv = mx->ldsv;
+  }
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (pl.has_split) {
@@ -1640,6 +1804,9 @@ int forward(const void* q, const void* k, const void* v, const BiasArg* bias, vo
                         : launch<false, false, 0, true>(mq, mk, mv, p, pl.grid, dev, s);
   // with a bias the scale is applied before the row max, so one instantiation serves any sign
   if (bias != nullptr) return launch<true, true>(mq, mk, mv, p, pl.grid, dev, s);
+  if (f8 == 3)
+    return scale > 0.0f ? launch<true, false, 3>(mq, mk, mv, p, pl.grid, dev, s)
+                        : launch<false, false, 3>(mq, mk, mv, p, pl.grid, dev, s);
   if (f8 == 2)
     return scale > 0.0f ? launch<true, false, 2>(mq, mk, mv, p, pl.grid, dev, s)
                         : launch<false, false, 2>(mq, mk, mv, p, pl.grid, dev, s);
@@ -1692,6 +1859,16 @@ extern "C" int attn_fwd_fp8(const void* q8, const void* k8, const void* vt8, lon
   const double eff = static_cast<double>(scale) * q_descale * k_descale;
   if (!(std::fabs(eff) <= static_cast<double>(FLT_MAX))) return ATTN_ERR_INVALID_ARG;
   return forward(q8, k8, vt8, nullptr, o, lse, B, H, Nq, Nk, d, static_cast<float>(eff), stream, 2, ldv, v_descale);
+}
+
+extern "C" int attn_fwd_mxfp8(const void* q8, const void* sq, const void* k8, const void* sk, const void* vt8,
+                              long long ldv, const void* svt, long long ldsv, void* o, float* lse, int B, int H, int Nq,
+                              int Nk, int d, float scale, void* stream) {
+  // S = scale * (Q K^T) from block-scaled E4M3 codes, O = P V with P rounded to E4M3 (scale
+  // 2^0 per block) and V^T block-scaled per 32 keys; the tensor cores apply every scale.
+  if (!std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
+  const MxArg mx = {sq, sk, svt, ldsv};
+  return forward(q8, k8, vt8, nullptr, o, lse, B, H, Nq, Nk, d, scale, stream, 3, ldv, 1.0f, nullptr, &mx);
 }
 
 extern "C" int attn_fwd_causal(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,

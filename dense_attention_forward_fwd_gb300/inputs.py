@@ -160,6 +160,23 @@ def make_qkv_mxfp8(B: int, H: int, Nq: int, Nk: int, d: int = 128, seed: int = 0
     return q8, sq, k8, sk, v8, sv
 
 
+def mx_value_layout(v8: np.ndarray, sv: np.ndarray, pad_code: int = 0x7F, pad_scale: int = 0xFF):
+    """V in MXFP8 as :func:`make_qkv_mxfp8` returns it (codes [B,H,Nk,d], scales
+    [B,H,ceil(Nk/32),d]) laid out for attn_fwd_mxfp8: V^T codes [B,H,d,ldv] and V^T scales
+    [B,H,d,ldsv], keys innermost, rows padded to 16 bytes (ldsv to at least four bytes per
+    128-key tile). Padding holds pad_code / pad_scale (NaN by default: a read of it would show
+    in the output). Returns (vt8, svt)."""
+    B, H, Nk, d = v8.shape
+    ldv = (Nk + 15) // 16 * 16
+    nkb = sv.shape[2]
+    ldsv = max((nkb + 15) // 16 * 16, (4 * ((Nk + 127) // 128) + 15) // 16 * 16)
+    vt8 = np.full((B, H, d, ldv), pad_code, dtype=np.uint8)
+    vt8[..., :Nk] = np.swapaxes(v8, 2, 3)
+    svt = np.full((B, H, d, ldsv), pad_scale, dtype=np.uint8)
+    svt[..., :nkb] = np.swapaxes(sv, 2, 3)
+    return vt8, svt
+
+
 def make_bias(shape, seed: int, std: float = 1.0) -> np.ndarray:
     """Seeded additive bias of the given shape (e.g. (B, H, Nq, Nk), or 1 in any of the first
     three dimensions for a shared bias): float32 normals with standard deviation ``std`` from

@@ -184,6 +184,40 @@ int attn_fwd_fp8(const void* q8, const void* k8, const void* vt8, long long ldv,
                  float v_descale, void* stream);
 
 /*
+ * attn_fwd_mxfp8 -- attention forward from MXFP8 inputs, both products block-scaled.
+ *
+ * The "MXFP8 MMA" that "Flash Attention на 5090 в CUDA C++" (section "Что дальше") names as
+ * the next step: each input is given as OCP microscaling FP8, E4M3 codes (the format of
+ * attn_fwd_fp8qk) with one E8M0 scale 2^(e - 127) per block of 32 elements along the
+ * dimension its product contracts over: along d for Q and K, along the keys for V. So
+ *
+ *     S = scale * Q K^T,   Q[i][c] = 2^(sq[i][c/32] - 127) * E4M3(q8[i][c]),   likewise K,
+ *     O = P V,   V[j][c] = 2^(svt[c][j/32] - 127) * E4M3(vt8[c][j]),
+ *
+ * and the tensor cores apply every scale (kind::mxf8f6f4 with scale factors in tensor
+ * memory). P is rounded to E4M3 with a block scale of 2^0 for the P V product, so O carries
+ * the E4M3 rounding of P described under attn_fwd_fp8; the row sums, and so the LSE, use the
+ * unrounded weights.
+ *
+ *   q8, k8  device, [B, H, Nq|Nk, d] bytes (E4M3 codes), 16-byte aligned
+ *   sq, sk  device, [B, H, Nq|Nk, d/32] bytes (E8M0 scales), 4-byte aligned
+ *   vt8     device, V^T as E4M3 codes, [B, H, d, ldv] bytes, keys innermost; ldv >= Nk, a
+ *           multiple of 16; bytes from Nk on are not used
+ *   svt     device, V^T's scales, [B, H, d, ldsv] bytes: byte t of row c scales keys
+ *           32t .. 32t+31 of column c; ldsv a multiple of 16 and at least 4 * ceil(Nk/128)
+ *           (whole 128-key tiles are read; bytes past ceil(Nk/32) are read and replaced by
+ *           2^0); 4-byte aligned
+ *
+ * d must be 128. A scale byte of 255 (NaN in E8M0) gives unspecified results for the rows it
+ * reaches. Returns ATTN_ERR_INVALID_ARG for a null pointer, ldv < Nk or ldsv too short,
+ * ATTN_ERR_MISALIGNED for the alignment rules above; everything else (o, lse, the work split,
+ * workspace, return values) as attn_fwd.
+ */
+int attn_fwd_mxfp8(const void* q8, const void* sq, const void* k8, const void* sk, const void* vt8, long long ldv,
+                   const void* svt, long long ldsv, void* o, float* lse, int B, int H, int Nq, int Nk, int d,
+                   float scale, void* stream);
+
+/*
  * attn_fwd_o32 -- attn_fwd with O written in FP32, before its rounding to BF16.
  *
  * A diagnostic of the computation itself. The notes state that the tiled computation

@@ -55,23 +55,26 @@ def test_roofline_peaks():
     sys.path.insert(0, ROOT)
     import bench
     peaks = {"bf16_tflops": 1800.0}
-    base = dict(fp8_qk=False, fp8=False)
+    base = dict(fp8_qk=False, fp8=False, mxfp8=False)
     assert bench.roofline_peak(SimpleNamespace(**base), peaks, "measured")[0] == 1800.0
     assert bench.roofline_peak(SimpleNamespace(**dict(base, fp8_qk=True)), peaks, "measured")[0] == \
         pytest.approx(2400.0)   # 4P/3: Q K^T at 2P, P V at P
     assert bench.roofline_peak(SimpleNamespace(**dict(base, fp8=True)), peaks, "measured")[0] == 3600.0
+    assert bench.roofline_peak(SimpleNamespace(**dict(base, mxfp8=True)), peaks, "measured")[0] == 3600.0
 
 
 def test_traffic_keys_match_the_recorded_ones():
     sys.path.insert(0, ROOT)
     import bench
     from dense_attention_forward_fwd_gb300.configs import by_name
-    base = dict(causal=False, bias="none", backward=False, fp8_qk=False, fp8=False)
-    cases = {"rect-4k-8k": ("rect-4k-8k", {}), "rect-4k-8k-fp8qk": ("rect-4k-8k", {"fp8_qk": True}),
+    base = dict(causal=False, bias="none", backward=False, fp8_qk=False, fp8=False, mxfp8=False)
+    cases = {"rect-4k-8k": ("rect-4k-8k", {}), "long-16k": ("long-16k", {}), "peaked-8k": ("peaked-8k", {}),
+             "square-4k": ("square-4k", {}), "long-16k-mxfp8": ("long-16k", {"mxfp8": True}),
+             "rect-4k-8k-mxfp8": ("rect-4k-8k", {"mxfp8": True}), "rect-4k-8k-fp8qk": ("rect-4k-8k", {"fp8_qk": True}),
              "rect-4k-8k-fp8": ("rect-4k-8k", {"fp8": True}), "square-4k-causal": ("square-4k", {"causal": True}),
              "rect-4k-8k-bias-shared": ("rect-4k-8k", {"bias": "shared"}),
              "square-4k-backward": ("square-4k", {"backward": True})}
     recorded = json.load(open(os.path.join(ROOT, "profiles", "traffic.json")))
-    assert set(recorded) == set(cases)
+    assert set(recorded) <= set(cases)
     for key, (name, over) in cases.items():
         assert bench.traffic_key(by_name(name), SimpleNamespace(**dict(base, **over))) == key
