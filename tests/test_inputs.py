@@ -87,3 +87,16 @@ def test_e4m3_inputs_are_per_tensor_quantizations_of_the_bf16_draw():
         assert ds == float(np.float32(np.abs(x).max() / 448.0))
         t = x.astype(np.float64) / ds
         assert np.all(np.abs(vals - t) <= np.maximum(np.abs(t) * 2.0 ** -4, 2.0 ** -10) * (1 + 1e-6))
+
+
+def test_mx_value_layout_transposes_and_pads():
+    from dense_attention_forward_fwd_gb300.inputs import make_qkv_mxfp8, mx_value_layout
+    for Nk in (33, 130, 640):
+        _, _, _, _, v8, sv = make_qkv_mxfp8(1, 2, 4, Nk, seed=Nk)
+        vt8, svt = mx_value_layout(v8, sv)
+        ldv, ldsv = vt8.shape[3], svt.shape[3]
+        assert ldv % 16 == 0 and ldv >= Nk
+        assert ldsv % 16 == 0 and ldsv >= 4 * ((Nk + 127) // 128) and ldsv >= sv.shape[2]
+        assert np.array_equal(vt8[..., :Nk], np.swapaxes(v8, 2, 3))
+        assert np.array_equal(svt[..., :sv.shape[2]], np.swapaxes(sv, 2, 3))
+        assert np.all(vt8[..., Nk:] == 0x7F) and np.all(svt[..., sv.shape[2]:] == 0xFF)   # NaN padding
