@@ -19,11 +19,14 @@
 //                    LSE = +inf, D = 0, so their P is exactly 0).
 //   bwd_dkdv_kernel  one block per (b, h, 128-key tile). K and V are loaded once; then per
 //                    128-query tile j (double-buffered Q_j, dO_j and the rows' float2 by
-//                    TMA): S^T = K Q_j^T and dP^T = V dO_j^T on tcgen05 into TMEM; four
-//                    compute warps (thread = key) form P^T and dS^T, write them back over
-//                    S^T and dP^T as BF16 pairs; then dV += P^T dO_j and dK += dS^T Q_j
-//                    take P^T and dS^T straight from TMEM (the A operand) with dO_j and Q_j
-//                    as MN-major B operands.
+//                    TMA): S^T = K Q_j^T and dP^T = V dO_j^T on tcgen05 into TMEM; the
+//                    compute warps (thread = key) form P^T and write it back over S^T as
+//                    BF16 pairs, then dS^T over dP^T; dV += P^T dO_j and dK += dS^T Q_j take
+//                    them straight from TMEM (the A operand) with dO_j and Q_j as MN-major B
+//                    operands. The MMA thread issues the next tile's S^T as soon as P^T has
+//                    been handed over (its columns are then free) and the next dP^T after
+//                    dK, so the tensor cores compute tile j+1's scores while the compute
+//                    warps work on tile j's dS^T.
 //   bwd_dq_kernel    one block per (b, h, 128-query tile). Q and dO are loaded once; per
 //                    key tile j (double-buffered K_j, V_j): S = Q K_j^T, dP = dO V_j^T; the
 //                    compute warps (thread = query) form dS and write it over S; then
@@ -84,12 +87,13 @@ constexpr int kQOffBar = kQOffStage + 2 * kQStageBytes;
 constexpr int kBarFixed = 0;        // the block's fixed tiles (K, V or Q, dO) have landed
 constexpr int kBarFull = 1;         // [2] stage landed
 constexpr int kBarEmpty = 3;        // [2] stage consumed by the MMAs
-constexpr int kBarSdP = 5;          // S and dP complete in TMEM
+constexpr int kBarSdP = 5;          // S and dP complete in TMEM (dK/dV block: S^T alone)
 constexpr int kBarPdS = 6;          // [step parity][2]: a column half of P / dS is in TMEM (one
-                                    // arrival per warp); the dK/dV block uses set 0 only
+                                    // arrival per warp); the dK/dV block: [0][g] P^T, [1][g] dS^T
 constexpr int kBarAcc = 10;         // accumulators complete
 constexpr int kBarDPFree = 11;      // dQ block: every compute warp holds dP of the step in registers
-constexpr int kNumBars = 12;
+constexpr int kBarDPReady = 12;     // dK/dV block: dP^T complete in TMEM
+constexpr int kNumBars = 13;
 constexpr int kFlagsBytes = kNumBars * 8 + 16;   // barriers, TMEM slot, abort flag
 
 constexpr int kKVSmem = kKVOffBar + kFlagsBytes + 1024;
@@ -319,6 +323,7 @@ __device__ __forceinline__ uint32_t block_setup(const Ctl& c, uint8_t* flags, ui
     for (int b = 0; b < 4; ++b) mbar_init(c.bar(kBarPdS + b), 4);   // one arrival per warp of a group
     mbar_init(c.bar(kBarAcc), 1);
     mbar_init(c.bar(kBarDPFree), 8);    // one arrival per compute warp
+    mbar_init(c.bar(kBarDPReady), 1);
     *c.abort = 0u;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -432,24 +437,48 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else if (warp == 1) {
     if (lane == 0) {
+      // Per query tile j: dV += P^T dO_j as each group hands its half of P^T over, then
+      // S^T of tile j+1 into the columns P^T leaves (the compute warps hold S^T_j in
+      // registers by then), then dK += dS^T Q_j as the halves of dS^T arrive, then dP^T of
+      // tile j+1 into the columns dS^T leaves. The next tile's scores thus run on the tensor
+      // cores while the compute warps work on this tile's dS^T, and its dP^T while they
+      // compute its P^T.
       bool ok = wait_phase(c, kBarFixed, 0, true);
-      for (int j = 0; ok && j < nq; ++j) {
-        const int s = j & 1;
-        if (!wait_phase(c, kBarFull + s, (j >> 1) & 1, true)) break;
+      if (ok && nq > 0) ok = wait_phase(c, kBarFull + 0, 0, true);
+      if (ok && nq > 0) {
         tc_fence_after();
-        mma_rows_by_rows(tS, base + kKVOffK, stage(s));                   // S^T = K Q_j^T
-        mma_rows_by_rows(tdP, base + kKVOffV, stage(s) + kTileBytes);     // dP^T = V dO_j^T
+        mma_rows_by_rows(tS, base + kKVOffK, stage(0));                   // S^T = K Q_0^T
         tc_commit(c.bar(kBarSdP));
+        mma_rows_by_rows(tdP, base + kKVOffV, stage(0) + kTileBytes);     // dP^T = V dO_0^T
+        tc_commit(c.bar(kBarDPReady));
+      }
+      for (int j = 0; ok && j < nq; ++j) {
+        const int s = j & 1, s1 = (j + 1) & 1;
+        const bool more = j + 1 < nq;
         for (int h = 0; ok && h < 2; ++h) {   // queries 64h .. 64h + 63, as each group hands them over
-          if (!wait_phase(c, kBarPdS + h, j & 1, true)) {
-            ok = false;
-            break;
-          }
+          ok = wait_phase(c, kBarPdS + h, j & 1, true);
+          if (!ok) break;
           tc_fence_after();
           mma_tmem_by_rows_half(tdV, tS + 64 * h, stage(s) + kTileBytes, h, j > 0 || h > 0);   // dV += P^T dO_j
+        }
+        if (!ok) break;
+        if (more) {
+          if (!wait_phase(c, kBarFull + s1, ((j + 1) >> 1) & 1, true)) break;
+          tc_fence_after();
+          mma_rows_by_rows(tS, base + kKVOffK, stage(s1));                // S^T = K Q_{j+1}^T
+          tc_commit(c.bar(kBarSdP));
+        }
+        for (int h = 0; ok && h < 2; ++h) {
+          ok = wait_phase(c, kBarPdS + 2 + h, j & 1, true);
+          if (!ok) break;
+          tc_fence_after();
           mma_tmem_by_rows_half(tdK, tdP + 64 * h, stage(s), h, j > 0 || h > 0);               // dK += dS^T Q_j
         }
         if (!ok) break;
+        if (more) {
+          mma_rows_by_rows(tdP, base + kKVOffV, stage(s1) + kTileBytes);  // dP^T = V dO_{j+1}^T
+          tc_commit(c.bar(kBarDPReady));
+        }
         tc_commit(c.bar(kBarEmpty + s));
       }
       tc_commit(c.bar(kBarAcc));   // also: every MMA this thread issued is done before TMEM is freed
@@ -463,7 +492,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     for (int j = 0; j < nq; ++j) {
       const int s = j & 1;
-      // the rows' (LSE, D) arrive with the stage; S^T and dP^T once the MMAs are done
+      // the rows' (LSE, D) arrive with the stage; S^T and dP^T once their MMAs are done
       if (!wait_warp(c, kBarFull + s, (j >> 1) & 1) || !wait_warp(c, kBarSdP, j & 1)) {
         ok = false;
         break;
@@ -474,13 +503,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int key = kt * kT + quarter * 32 + lane;
       const int c_lo = kCausal ? key - p.off - (q0 + j) * kT : -1;
       const bool mask_warp = kCausal && (kt * kT + quarter * 32 + 31 - p.off - (q0 + j) * kT) > 64 * grp;
-#pragma unroll 1
+      // P^T of the group's 64 query columns, kept in registers for dS^T; handed over first
+      float pv[64];
+#pragma unroll
       for (int ch = 0; ch < 2; ++ch) {   // 32 query columns at a time
         const int col0 = 64 * grp + 32 * ch;
-        uint32_t xs[32], xd[32];
+        uint32_t xs[32];
         tmem_ld32(tS + lane_off + col0, xs);
-        tmem_ld32(tdP + lane_off + col0, xd);
-        uint32_t pw[16], dw[16];
+        uint32_t pw[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
           const float2 r0 = rw[col0 + 2 * i], r1 = rw[col0 + 2 * i + 1];
@@ -490,18 +520,39 @@ __global__ void __launch_bounds__(kThreads, 1)
             p0 = col0 + 2 * i >= c_lo ? p0 : 0.0f;
             p1 = col0 + 2 * i + 1 >= c_lo ? p1 : 0.0f;
           }
-          const float d0 = p0 * (__uint_as_float(xd[2 * i]) - r0.y);
-          const float d1 = p1 * (__uint_as_float(xd[2 * i + 1]) - r1.y);
+          pv[32 * ch + 2 * i] = p0;
+          pv[32 * ch + 2 * i + 1] = p1;
           pw[i] = pack_bf16(p0, p1);
-          dw[i] = pack_bf16(d0, d1);
         }
         // group columns 64 grp + 16 ch .. + 15 were read in this or the previous chunk
         tmem_st16(tS + lane_off + 64 * grp + 16 * ch, pw);
-        tmem_st16(tdP + lane_off + 64 * grp + 16 * ch, dw);
       }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(c.bar(kBarPdS + grp));
+      __syncwarp();
+      if (!wait_warp(c, kBarDPReady, j & 1)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+#pragma unroll
+      for (int ch = 0; ch < 2; ++ch) {
+        const int col0 = 64 * grp + 32 * ch;
+        uint32_t xd[32];
+        tmem_ld32(tdP + lane_off + col0, xd);
+        uint32_t dw[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const float d0 = pv[32 * ch + 2 * i] * (__uint_as_float(xd[2 * i]) - rw[col0 + 2 * i].y);
+          const float d1 = pv[32 * ch + 2 * i + 1] * (__uint_as_float(xd[2 * i + 1]) - rw[col0 + 2 * i + 1].y);
+          dw[i] = pack_bf16(d0, d1);
+        }
+        tmem_st16(tdP + lane_off + 64 * grp + 16 * ch, dw);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(c.bar(kBarPdS + 2 + grp));
       __syncwarp();
     }
     if (ok && wait_warp(c, kBarAcc, 0)) {
