@@ -76,12 +76,15 @@ constexpr int kKVOffV = kTileBytes;
 constexpr int kKVOffStage = 2 * kTileBytes;
 constexpr int kKVStageBytes = 2 * kTileBytes + kRowsBytes;   // 1024-aligned (66,560)
 constexpr int kKVOffBar = kKVOffStage + 2 * kKVStageBytes;
-// dQ block shared memory: Q | dO | 2 x (K_j | V_j) | barriers | flags
+// dQ block shared memory: Q | dO | 3 x K_j | 2 x V_j | barriers | flags. K_j is read until
+// dQ += dS K_j, V_j only by dP = dO V_j^T, so V's slots turn over sooner: three K slots and
+// two V slots request every tile more than a step before its product needs it.
 constexpr int kQOffQ = 0;
 constexpr int kQOffDO = kTileBytes;
-constexpr int kQOffStage = 2 * kTileBytes;
-constexpr int kQStageBytes = 2 * kTileBytes;
-constexpr int kQOffBar = kQOffStage + 2 * kQStageBytes;
+constexpr int kQKSlots = 3, kQVSlots = 2;
+constexpr int kQOffK = 2 * kTileBytes;
+constexpr int kQOffV = kQOffK + kQKSlots * kTileBytes;
+constexpr int kQOffBar = kQOffV + kQVSlots * kTileBytes;
 
 // barriers (both kernels)
 constexpr int kBarFixed = 0;        // the block's fixed tiles (K, V or Q, dO) have landed
@@ -93,7 +96,11 @@ constexpr int kBarPdS = 6;          // [step parity][2]: a column half of P / dS
 constexpr int kBarAcc = 10;         // accumulators complete
 constexpr int kBarDPFree = 11;      // dQ block: every compute warp holds dP of the step in registers
 constexpr int kBarDPReady = 12;     // dK/dV block: dP^T complete in TMEM
-constexpr int kNumBars = 13;
+constexpr int kBarKFull = 13;       // dQ block: [3] K slot landed
+constexpr int kBarKEmpty = 16;      // dQ block: [3] K slot read by its last product (dQ)
+constexpr int kBarVFull = 19;       // dQ block: [2] V slot landed
+constexpr int kBarVEmpty = 21;      // dQ block: [2] V slot read by its product (dP)
+constexpr int kNumBars = 23;
 constexpr int kFlagsBytes = kNumBars * 8 + 16;   // barriers, TMEM slot, abort flag
 
 constexpr int kKVSmem = kKVOffBar + kFlagsBytes + 1024;
@@ -324,6 +331,7 @@ __device__ __forceinline__ uint32_t block_setup(const Ctl& c, uint8_t* flags, ui
     mbar_init(c.bar(kBarAcc), 1);
     mbar_init(c.bar(kBarDPFree), 8);    // one arrival per compute warp
     mbar_init(c.bar(kBarDPReady), 1);
+    for (int b = kBarKFull; b < kNumBars; ++b) mbar_init(c.bar(b), 1);
     *c.abort = 0u;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -596,7 +604,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tS0 = tmem, tdP = tmem + 128, tdQ = tmem + 256, tS1 = tmem + 384;
   // key tiles 0 .. nk - 1; causal: up to the diagonal of this tile's last row
   const int nk = kCausal ? (min(p.Nq, (qt + 1) * kT) + p.off + kT - 1) / kT : p.k_tiles;
-  auto stage = [&](int s) { return base + kQOffStage + s * kQStageBytes; };   // K | V
+  auto kslot = [&](int j) { return base + kQOffK + (j % kQKSlots) * kTileBytes; };
+  auto vslot = [&](int j) { return base + kQOffV + (j % kQVSlots) * kTileBytes; };
 
   if (warp == 0) {
     if (lane == 0) {
@@ -605,30 +614,37 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_load_3d(base + kQOffQ + h * kBoxBytes, &tmQ, c.bar(kBarFixed), h * 64, qt * kT, bh);
         tma_load_3d(base + kQOffDO + h * kBoxBytes, &tmDO, c.bar(kBarFixed), h * 64, qt * kT, bh);
       }
-      int issued = 0;
+      int issued = 0;   // key tiles whose K and V were both requested
       for (int j = 0; j < nk; ++j, ++issued) {
-        const int s = j & 1;
-        if (j >= 2 && !wait_phase(c, kBarEmpty + s, ((j >> 1) - 1) & 1, true)) break;
-        const uint32_t fb = c.bar(kBarFull + s);
-        mbar_arrive_expect_tx(fb, 2 * kTileBytes);
-        for (int h = 0; h < 2; ++h) {
-          tma_load_3d(stage(s) + h * kBoxBytes, &tmK, fb, h * 64, j * kT, bh);
-          tma_load_3d(stage(s) + kTileBytes + h * kBoxBytes, &tmV, fb, h * 64, j * kT, bh);
+        const int ks = j % kQKSlots, vs = j % kQVSlots;
+        if (j >= kQKSlots && !wait_phase(c, kBarKEmpty + ks, (j / kQKSlots - 1) & 1, true)) break;
+        mbar_arrive_expect_tx(c.bar(kBarKFull + ks), kTileBytes);
+        for (int h = 0; h < 2; ++h) tma_load_3d(kslot(j) + h * kBoxBytes, &tmK, c.bar(kBarKFull + ks), h * 64, j * kT, bh);
+        if (j >= kQVSlots && !wait_phase(c, kBarVEmpty + vs, (j / kQVSlots - 1) & 1, true)) {
+          wait_phase(c, kBarKFull + ks, (j / kQKSlots) & 1, false);   // that K copy is in flight
+          break;
         }
+        mbar_arrive_expect_tx(c.bar(kBarVFull + vs), kTileBytes);
+        for (int h = 0; h < 2; ++h) tma_load_3d(vslot(j) + h * kBoxBytes, &tmV, c.bar(kBarVFull + vs), h * 64, j * kT, bh);
       }
+      // no copy into shared memory may be in flight when the block exits
       wait_phase(c, kBarFixed, 0, false);
-      for (int j = issued - 2 < 0 ? 0 : issued - 2; j < issued; ++j)
-        wait_phase(c, kBarFull + (j & 1), (j >> 1) & 1, false);
+      for (int j = issued - kQKSlots < 0 ? 0 : issued - kQKSlots; j < issued; ++j)
+        wait_phase(c, kBarKFull + j % kQKSlots, (j / kQKSlots) & 1, false);
+      for (int j = issued - kQVSlots < 0 ? 0 : issued - kQVSlots; j < issued; ++j)
+        wait_phase(c, kBarVFull + j % kQVSlots, (j / kQVSlots) & 1, false);
     }
     __syncwarp();
   } else if (warp == 1) {
     if (lane == 0) {
-      bool ok = wait_phase(c, kBarFixed, 0, true) && wait_phase(c, kBarFull, 0, true);
+      bool ok = wait_phase(c, kBarFixed, 0, true) && wait_phase(c, kBarKFull, 0, true) &&
+                wait_phase(c, kBarVFull, 0, true);
       if (ok) {
         tc_fence_after();
-        mma_rows_by_rows(tS0, base + kQOffQ, stage(0));                   // S(0) = Q K_0^T
-        mma_rows_by_rows(tdP, base + kQOffDO, stage(0) + kTileBytes);     // dP(0) = dO V_0^T
+        mma_rows_by_rows(tS0, base + kQOffQ, kslot(0));                   // S(0) = Q K_0^T
+        mma_rows_by_rows(tdP, base + kQOffDO, vslot(0));                  // dP(0) = dO V_0^T
         tc_commit(c.bar(kBarSdP));
+        tc_commit(c.bar(kBarVEmpty + 0));
       }
       for (int j = 0; ok && j < nk; ++j) {
         const int s = j & 1;
@@ -636,14 +652,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (j + 1 < nk) {
           // S(j+1) into the other buffer (its dS(j-1) was read by the dQ MMAs issued before);
           // dP(j+1) once every compute warp has taken dP(j) into registers
-          const int s1 = s ^ 1;
-          if (!wait_phase(c, kBarFull + s1, ((j + 1) >> 1) & 1, true)) break;
+          const int j1 = j + 1, s1 = s ^ 1;
+          if (!wait_phase(c, kBarKFull + j1 % kQKSlots, (j1 / kQKSlots) & 1, true)) break;
           tc_fence_after();
-          mma_rows_by_rows(s1 ? tS1 : tS0, base + kQOffQ, stage(s1));
-          if (!wait_phase(c, kBarDPFree, j & 1, true)) break;
+          mma_rows_by_rows(s1 ? tS1 : tS0, base + kQOffQ, kslot(j1));
+          if (!wait_phase(c, kBarDPFree, j & 1, true) ||
+              !wait_phase(c, kBarVFull + j1 % kQVSlots, (j1 / kQVSlots) & 1, true))
+            break;
           tc_fence_after();
-          mma_rows_by_rows(tdP, base + kQOffDO, stage(s1) + kTileBytes);
+          mma_rows_by_rows(tdP, base + kQOffDO, vslot(j1));
           tc_commit(c.bar(kBarSdP));
+          tc_commit(c.bar(kBarVEmpty + j1 % kQVSlots));   // V_{j+1} is free once dP(j+1) is done
         }
         // The compute warps may finish step j + 1 before this thread gets here, so steps
         // alternate between two sets of hand-off barriers: a set completes at most once
@@ -654,10 +673,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           tc_fence_after();
-          mma_tmem_by_rows_half(tdQ, tSj + 64 * h, stage(s), h, j > 0 || h > 0);   // dQ += dS K_j
+          mma_tmem_by_rows_half(tdQ, tSj + 64 * h, kslot(j), h, j > 0 || h > 0);   // dQ += dS K_j
         }
         if (!ok) break;
-        tc_commit(c.bar(kBarEmpty + s));
+        tc_commit(c.bar(kBarKEmpty + j % kQKSlots));
       }
       tc_commit(c.bar(kBarAcc));
       wait_phase(c, kBarAcc, 0, false);
