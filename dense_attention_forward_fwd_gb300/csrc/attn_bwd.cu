@@ -69,47 +69,49 @@ constexpr int kStageWarpBytes = 32 * 64 * 2;    // epilogue staging per compute 
 constexpr unsigned long long kDefaultWaitLimit = 1ull << 31;
 constexpr float kLog2e = 1.4426950408889634f;
 
-// dK/dV block shared memory: K | V | 2 x (Q_j | dO_j | rows) | barriers | flags
-constexpr int kRowsBytes = kT * 8;              // float2 (LSE log2, D) per query row
-constexpr int kKVOffK = 0;
-constexpr int kKVOffV = kTileBytes;
-constexpr int kKVOffStage = 2 * kTileBytes;
-constexpr int kKVStageBytes = 2 * kTileBytes + kRowsBytes;   // 1024-aligned (66,560)
-constexpr int kKVOffBar = kKVOffStage + 2 * kKVStageBytes;
-// dQ block shared memory: Q | dO | 3 x K_j | 2 x V_j | barriers | flags. K_j is read until
-// dQ += dS K_j, V_j only by dP = dO V_j^T, so V's slots turn over sooner: three K slots and
-// two V slots request every tile more than a step before its product needs it.
-constexpr int kQOffQ = 0;
-constexpr int kQOffDO = kTileBytes;
-constexpr int kQKSlots = 3, kQVSlots = 2;
-constexpr int kQOffK = 2 * kTileBytes;
-constexpr int kQOffV = kQOffK + kQKSlots * kTileBytes;
-constexpr int kQOffBar = kQOffV + kQVSlots * kTileBytes;
+// Both main kernels hold two fixed tiles and stream two tiles per step through two rings.
+// The step's first operand (Q_j in the dK/dV block, K_j in the dQ block) is read by a score
+// product and again by the step's last product (dK += dS^T Q_j, dQ += dS K_j); the second
+// (dO_j, V_j) only by products early in the step. The first ring has three slots, the
+// second two: both request every tile more than a step before its first product needs it.
+// In the dK/dV block the query rows' (LSE, D) travel with dO_j, and its slot comes free with
+// the commit that ends step j (dV and dK of the step done, so dS^T_j and the rows were read).
+// Seven 32 KB tiles and the rows fill the dK/dV block's shared memory, with no room to
+// realign its base: that kernel declares it 1024-aligned (the 128-byte swizzle's atom) and
+// checks the alignment before touching it. The dQ block has no rows: its barriers follow
+// the tiles, and it realigns its base itself.
+constexpr int kSlotsA = 3, kSlotsB = 2;
+constexpr int kRowsBytes = kT * 8;                             // float2 (LSE log2, D) per query row
+constexpr int kOffFixed0 = 0;                                  // K (dK/dV block) or Q (dQ block)
+constexpr int kOffFixed1 = kTileBytes;                         // V or dO
+constexpr int kOffRingA = 2 * kTileBytes;                      // Q_j or K_j
+constexpr int kOffRingB = kOffRingA + kSlotsA * kTileBytes;    // dO_j or V_j
+constexpr int kOffRows = kOffRingB + kSlotsB * kTileBytes;     // dK/dV block: rows of dO_j's tile
+constexpr int kOffBar = kOffRows + kSlotsB * kRowsBytes;      // dK/dV block
+constexpr int kOffBarQ = kOffRows;                             // dQ block
 
 // barriers (both kernels)
 constexpr int kBarFixed = 0;        // the block's fixed tiles (K, V or Q, dO) have landed
-constexpr int kBarFull = 1;         // [2] stage landed
-constexpr int kBarEmpty = 3;        // [2] stage consumed by the MMAs
-constexpr int kBarSdP = 5;          // S and dP complete in TMEM (dK/dV block: S^T alone)
-constexpr int kBarPdS = 6;          // [step parity][2]: a column half of P / dS is in TMEM (one
+constexpr int kBarFullA = 1;        // [3] ring A slot landed
+constexpr int kBarEmptyA = 4;       // [3] ring A slot read by its last product
+constexpr int kBarFullB = 7;        // [2] ring B slot landed
+constexpr int kBarEmptyB = 9;       // [2] dQ block: ring B slot read by its product
+constexpr int kBarSdP = 11;         // S and dP complete in TMEM (dK/dV block: S^T alone)
+constexpr int kBarPdS = 12;         // [step parity][2]: a column half of P / dS is in TMEM (one
                                     // arrival per warp); the dK/dV block: [0][g] P^T, [1][g] dS^T
-constexpr int kBarAcc = 10;         // accumulators complete
-constexpr int kBarDPFree = 11;      // dQ block: every compute warp holds dP of the step in registers
-constexpr int kBarDPReady = 12;     // dK/dV block: dP^T complete in TMEM
-constexpr int kBarKFull = 13;       // dQ block: [3] K slot landed
-constexpr int kBarKEmpty = 16;      // dQ block: [3] K slot read by its last product (dQ)
-constexpr int kBarVFull = 19;       // dQ block: [2] V slot landed
-constexpr int kBarVEmpty = 21;      // dQ block: [2] V slot read by its product (dP)
-constexpr int kNumBars = 23;
+constexpr int kBarAcc = 16;         // accumulators complete
+constexpr int kBarDPFree = 17;      // dQ block: every compute warp holds dP of the step in registers
+constexpr int kBarDPReady = 18;     // dK/dV block: dP^T complete in TMEM
+constexpr int kNumBars = 19;
 constexpr int kFlagsBytes = kNumBars * 8 + 16;   // barriers, TMEM slot, abort flag
 
-constexpr int kKVSmem = kKVOffBar + kFlagsBytes + 1024;
-constexpr int kQSmem = kQOffBar + kFlagsBytes + 1024;
-static_assert(kKVStageBytes % 1024 == 0, "stage tiles need 1024-byte alignment");
-static_assert(kKVSmem <= 232448 && kQSmem <= 232448, "exceeds the 227 KB shared memory of one block");
+constexpr int kSmemKV = kOffBar + kFlagsBytes;
+constexpr int kSmemQ = kOffBarQ + kFlagsBytes + 1024;   // + realignment of the base
+static_assert(kTileBytes % 1024 == 0, "tiles need 1024-byte alignment");
+static_assert(kSmemKV <= 232448 && kSmemQ <= 232448, "exceeds the 227 KB shared memory of one block");
 static_assert(8 * kStageWarpBytes <= kTileBytes, "epilogue staging reuses one tile");
 
-__device__ unsigned int g_bwd_status;   // bit 0: a wait timed out
+__device__ unsigned int g_bwd_status;   // bit 0: a wait timed out; bit 1: shared memory misaligned
 
 // ---------------------------------------------------------------------------------
 // PTX wrappers (the same instruction forms as the forward kernel)
@@ -321,17 +323,11 @@ __device__ __forceinline__ void store_acc_half(uint32_t t_acc, int h, float mul,
 // Block setup shared by both kernels: barrier init, TMEM allocation. Returns the TMEM base.
 __device__ __forceinline__ uint32_t block_setup(const Ctl& c, uint8_t* flags, uint32_t flags_u32, int warp) {
   if (threadIdx.x == 0) {
-    mbar_init(c.bar(kBarFixed), 1);
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(c.bar(kBarFull + s), 1);
-      mbar_init(c.bar(kBarEmpty + s), 1);
-    }
-    mbar_init(c.bar(kBarSdP), 1);
+    for (int b = kBarFixed; b <= kBarSdP; ++b) mbar_init(c.bar(b), 1);   // fixed tiles, rings, S
     for (int b = 0; b < 4; ++b) mbar_init(c.bar(kBarPdS + b), 4);   // one arrival per warp of a group
     mbar_init(c.bar(kBarAcc), 1);
     mbar_init(c.bar(kBarDPFree), 8);    // one arrival per compute warp
     mbar_init(c.bar(kBarDPReady), 1);
-    for (int b = kBarKFull; b < kNumBars; ++b) mbar_init(c.bar(b), 1);
     *c.abort = 0u;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -392,19 +388,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
                     const BwdParams p) {
-  extern __shared__ uint8_t smem_raw[];
-  const uint32_t raw = smem_u32(smem_raw);
-  const uint32_t base = (raw + 1023u) & ~1023u;
-  uint8_t* smem = smem_raw + (base - raw);
+  extern __shared__ __align__(1024) uint8_t smem[];
+  const uint32_t base = smem_u32(smem);
+  if (base & 1023u) {   // every thread leaves before any barrier, copy or TMEM allocation
+    if (threadIdx.x == 0) atomicOr(&g_bwd_status, 2u);
+    return;
+  }
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int kt = blockIdx.x % p.k_tiles;
   const int bh = blockIdx.x / p.k_tiles;
   Ctl c;
-  c.bars = base + kKVOffBar;
-  c.abort = reinterpret_cast<volatile uint32_t*>(smem + kKVOffBar + kNumBars * 8 + 4);
+  c.bars = base + kOffBar;
+  c.abort = reinterpret_cast<volatile uint32_t*>(smem + kOffBar + kNumBars * 8 + 4);
   c.limit = p.wait_limit;
-  const uint32_t tmem = block_setup(c, smem + kKVOffBar, base + kKVOffBar, warp);
+  const uint32_t tmem = block_setup(c, smem + kOffBar, base + kOffBar, warp);
   const uint32_t tS = tmem, tdP = tmem + 128, tdV = tmem + 256, tdK = tmem + 384;
+  const uint32_t sK = base + kOffFixed0, sV = base + kOffFixed1;
   // query tiles q0 .. q_tiles - 1; causal: from the first tile whose rows see this tile's
   // first key (query i sees key r when i >= r - off). Step t of the loops is tile q0 + t.
   int q0 = 0;
@@ -413,34 +412,41 @@ __global__ void __launch_bounds__(kThreads, 1)
     q0 = first_row > 0 ? first_row / kT : 0;
   }
   const int nq = p.q_tiles - q0;
-  auto stage = [&](int s) { return base + kKVOffStage + s * kKVStageBytes; };   // Q | dO | rows
+  auto sQ = [&](int j) { return base + kOffRingA + (j % kSlotsA) * kTileBytes; };
+  auto sDO = [&](int j) { return base + kOffRingB + (j % kSlotsB) * kTileBytes; };
 
   if (warp == 0) {
     if (lane == 0) {
-      // K and V of this tile, then per query tile Q_j, dO_j and the rows' (LSE, D)
+      // K and V of this tile, then per query tile Q_j, and dO_j with the rows' (LSE, D)
       mbar_arrive_expect_tx(c.bar(kBarFixed), 2 * kTileBytes);
       for (int h = 0; h < 2; ++h) {
-        tma_load_3d(base + kKVOffK + h * kBoxBytes, &tmK, c.bar(kBarFixed), h * 64, kt * kT, bh);
-        tma_load_3d(base + kKVOffV + h * kBoxBytes, &tmV, c.bar(kBarFixed), h * 64, kt * kT, bh);
+        tma_load_3d(sK + h * kBoxBytes, &tmK, c.bar(kBarFixed), h * 64, kt * kT, bh);
+        tma_load_3d(sV + h * kBoxBytes, &tmV, c.bar(kBarFixed), h * 64, kt * kT, bh);
       }
-      int issued = 0;
+      int issued = 0;   // query tiles whose Q and dO were both requested
       for (int j = 0; j < nq; ++j, ++issued) {
-        const int s = j & 1;
-        if (j >= 2 && !wait_phase(c, kBarEmpty + s, ((j >> 1) - 1) & 1, true)) break;
+        const int a = j % kSlotsA, b = j % kSlotsB;
+        if (j >= kSlotsA && !wait_phase(c, kBarEmptyA + a, (j / kSlotsA - 1) & 1, true)) break;
         if (p.withhold && j == 1) break;   // test hook: the consumers' waits for this tile run out
-        const uint32_t fb = c.bar(kBarFull + s);
-        mbar_arrive_expect_tx(fb, 2 * kTileBytes + kRowsBytes);
-        for (int h = 0; h < 2; ++h) {
-          tma_load_3d(stage(s) + h * kBoxBytes, &tmQ, fb, h * 64, (q0 + j) * kT, bh);
-          tma_load_3d(stage(s) + kTileBytes + h * kBoxBytes, &tmDO, fb, h * 64, (q0 + j) * kT, bh);
+        mbar_arrive_expect_tx(c.bar(kBarFullA + a), kTileBytes);
+        for (int h = 0; h < 2; ++h) tma_load_3d(sQ(j) + h * kBoxBytes, &tmQ, c.bar(kBarFullA + a), h * 64, (q0 + j) * kT, bh);
+        // dO_j's slot held dO_{j-2}: free once step j-2 has ended (its ring A commit)
+        if (j >= kSlotsB && !wait_phase(c, kBarEmptyA + (j - kSlotsB) % kSlotsA, ((j - kSlotsB) / kSlotsA) & 1, true)) {
+          wait_phase(c, kBarFullA + a, (j / kSlotsA) & 1, false);   // that Q copy is in flight
+          break;
         }
-        bulk_load(stage(s) + 2 * kTileBytes,
-                  p.rows + static_cast<size_t>(bh) * p.q_pad + static_cast<size_t>(q0 + j) * kT, kRowsBytes, fb);
+        mbar_arrive_expect_tx(c.bar(kBarFullB + b), kTileBytes + kRowsBytes);
+        for (int h = 0; h < 2; ++h) tma_load_3d(sDO(j) + h * kBoxBytes, &tmDO, c.bar(kBarFullB + b), h * 64, (q0 + j) * kT, bh);
+        bulk_load(base + kOffRows + b * kRowsBytes,
+                  p.rows + static_cast<size_t>(bh) * p.q_pad + static_cast<size_t>(q0 + j) * kT, kRowsBytes,
+                  c.bar(kBarFullB + b));
       }
       // no copy into shared memory may be in flight when the block exits
       wait_phase(c, kBarFixed, 0, false);
-      for (int j = issued - 2 < 0 ? 0 : issued - 2; j < issued; ++j)
-        wait_phase(c, kBarFull + (j & 1), (j >> 1) & 1, false);
+      for (int j = issued - kSlotsA < 0 ? 0 : issued - kSlotsA; j < issued; ++j)
+        wait_phase(c, kBarFullA + j % kSlotsA, (j / kSlotsA) & 1, false);
+      for (int j = issued - kSlotsB < 0 ? 0 : issued - kSlotsB; j < issued; ++j)
+        wait_phase(c, kBarFullB + j % kSlotsB, (j / kSlotsB) & 1, false);
     }
     __syncwarp();
   } else if (warp == 1) {
@@ -452,42 +458,44 @@ __global__ void __launch_bounds__(kThreads, 1)
       // cores while the compute warps work on this tile's dS^T, and its dP^T while they
       // compute its P^T.
       bool ok = wait_phase(c, kBarFixed, 0, true);
-      if (ok && nq > 0) ok = wait_phase(c, kBarFull + 0, 0, true);
+      if (ok && nq > 0) ok = wait_phase(c, kBarFullA, 0, true) && wait_phase(c, kBarFullB, 0, true);
       if (ok && nq > 0) {
         tc_fence_after();
-        mma_rows_by_rows(tS, base + kKVOffK, stage(0));                   // S^T = K Q_0^T
+        mma_rows_by_rows(tS, sK, sQ(0));                                  // S^T = K Q_0^T
         tc_commit(c.bar(kBarSdP));
-        mma_rows_by_rows(tdP, base + kKVOffV, stage(0) + kTileBytes);     // dP^T = V dO_0^T
+        mma_rows_by_rows(tdP, sV, sDO(0));                                // dP^T = V dO_0^T
         tc_commit(c.bar(kBarDPReady));
       }
       for (int j = 0; ok && j < nq; ++j) {
-        const int s = j & 1, s1 = (j + 1) & 1;
-        const bool more = j + 1 < nq;
+        const int j1 = j + 1;
+        const bool more = j1 < nq;
         for (int h = 0; ok && h < 2; ++h) {   // queries 64h .. 64h + 63, as each group hands them over
           ok = wait_phase(c, kBarPdS + h, j & 1, true);
           if (!ok) break;
           tc_fence_after();
-          mma_tmem_by_rows_half(tdV, tS + 64 * h, stage(s) + kTileBytes, h, j > 0 || h > 0);   // dV += P^T dO_j
+          mma_tmem_by_rows_half(tdV, tS + 64 * h, sDO(j), h, j > 0 || h > 0);   // dV += P^T dO_j
         }
         if (!ok) break;
         if (more) {
-          if (!wait_phase(c, kBarFull + s1, ((j + 1) >> 1) & 1, true)) break;
+          if (!wait_phase(c, kBarFullA + j1 % kSlotsA, (j1 / kSlotsA) & 1, true)) break;
           tc_fence_after();
-          mma_rows_by_rows(tS, base + kKVOffK, stage(s1));                // S^T = K Q_{j+1}^T
+          mma_rows_by_rows(tS, sK, sQ(j1));                               // S^T = K Q_{j+1}^T
           tc_commit(c.bar(kBarSdP));
         }
         for (int h = 0; ok && h < 2; ++h) {
           ok = wait_phase(c, kBarPdS + 2 + h, j & 1, true);
           if (!ok) break;
           tc_fence_after();
-          mma_tmem_by_rows_half(tdK, tdP + 64 * h, stage(s), h, j > 0 || h > 0);               // dK += dS^T Q_j
+          mma_tmem_by_rows_half(tdK, tdP + 64 * h, sQ(j), h, j > 0 || h > 0);    // dK += dS^T Q_j
         }
         if (!ok) break;
         if (more) {
-          mma_rows_by_rows(tdP, base + kKVOffV, stage(s1) + kTileBytes);  // dP^T = V dO_{j+1}^T
+          if (!wait_phase(c, kBarFullB + j1 % kSlotsB, (j1 / kSlotsB) & 1, true)) break;
+          tc_fence_after();
+          mma_rows_by_rows(tdP, sV, sDO(j1));                             // dP^T = V dO_{j+1}^T
           tc_commit(c.bar(kBarDPReady));
         }
-        tc_commit(c.bar(kBarEmpty + s));
+        tc_commit(c.bar(kBarEmptyA + j % kSlotsA));   // frees Q_j, and dO_j with its rows
       }
       tc_commit(c.bar(kBarAcc));   // also: every MMA this thread issued is done before TMEM is freed
       wait_phase(c, kBarAcc, 0, false);
@@ -499,14 +507,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
     bool ok = true;
     for (int j = 0; j < nq; ++j) {
-      const int s = j & 1;
-      // the rows' (LSE, D) arrive with the stage; S^T and dP^T once their MMAs are done
-      if (!wait_warp(c, kBarFull + s, (j >> 1) & 1) || !wait_warp(c, kBarSdP, j & 1)) {
+      // the rows' (LSE, D) arrive with dO_j; S^T once its MMA is done
+      const int b = j % kSlotsB;
+      if (!wait_warp(c, kBarFullB + b, (j / kSlotsB) & 1) || !wait_warp(c, kBarSdP, j & 1)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      const float2* rw = reinterpret_cast<const float2*>(smem + kKVOffStage + s * kKVStageBytes + 2 * kTileBytes);
+      const float2* rw = reinterpret_cast<const float2*>(smem + kOffRows + b * kRowsBytes);
       // causal: this thread's key r is seen by query columns c >= r - off - (q0 + j) * 128
       const int key = kt * kT + quarter * 32 + lane;
       const int c_lo = kCausal ? key - p.off - (q0 + j) * kT : -1;
@@ -567,7 +575,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const int row0 = kt * kT + quarter * 32;   // the warp's first key
       const int valid = p.Nk - row0;
-      uint8_t* st = smem + kKVOffK + (warp - 4) * kStageWarpBytes;   // K is no longer read
+      uint8_t* st = smem + kOffFixed0 + (warp - 4) * kStageWarpBytes;   // K is no longer read
       const size_t off = (static_cast<size_t>(bh) * p.Nk + row0) * kD;
       store_acc_half(tdV + lane_off, grp, 1.0f, st, p.dv + off, valid);      // d columns 64 grp ..
       store_acc_half(tdK + lane_off, grp, p.scale, st, p.dk + off, valid);
@@ -594,57 +602,58 @@ __global__ void __launch_bounds__(kThreads, 1)
                           : static_cast<int>(blockIdx.x % p.q_tiles);
   const int bh = blockIdx.x / p.q_tiles;
   Ctl c;
-  c.bars = base + kQOffBar;
-  c.abort = reinterpret_cast<volatile uint32_t*>(smem + kQOffBar + kNumBars * 8 + 4);
+  c.bars = base + kOffBarQ;
+  c.abort = reinterpret_cast<volatile uint32_t*>(smem + kOffBarQ + kNumBars * 8 + 4);
   c.limit = p.wait_limit;
-  const uint32_t tmem = block_setup(c, smem + kQOffBar, base + kQOffBar, warp);
+  const uint32_t tmem = block_setup(c, smem + kOffBarQ, base + kOffBarQ, warp);
+  const uint32_t sQ = base + kOffFixed0, sDO = base + kOffFixed1;
   // S is double-buffered (the fourth 128 columns), so S and dP of the next key tile are
   // computed while the compute warps work on this one; dP has one buffer, which the
   // compute warps release as soon as they hold their columns of it in registers.
   const uint32_t tS0 = tmem, tdP = tmem + 128, tdQ = tmem + 256, tS1 = tmem + 384;
   // key tiles 0 .. nk - 1; causal: up to the diagonal of this tile's last row
   const int nk = kCausal ? (min(p.Nq, (qt + 1) * kT) + p.off + kT - 1) / kT : p.k_tiles;
-  auto kslot = [&](int j) { return base + kQOffK + (j % kQKSlots) * kTileBytes; };
-  auto vslot = [&](int j) { return base + kQOffV + (j % kQVSlots) * kTileBytes; };
+  auto kslot = [&](int j) { return base + kOffRingA + (j % kSlotsA) * kTileBytes; };
+  auto vslot = [&](int j) { return base + kOffRingB + (j % kSlotsB) * kTileBytes; };
 
   if (warp == 0) {
     if (lane == 0) {
       mbar_arrive_expect_tx(c.bar(kBarFixed), 2 * kTileBytes);
       for (int h = 0; h < 2; ++h) {
-        tma_load_3d(base + kQOffQ + h * kBoxBytes, &tmQ, c.bar(kBarFixed), h * 64, qt * kT, bh);
-        tma_load_3d(base + kQOffDO + h * kBoxBytes, &tmDO, c.bar(kBarFixed), h * 64, qt * kT, bh);
+        tma_load_3d(sQ + h * kBoxBytes, &tmQ, c.bar(kBarFixed), h * 64, qt * kT, bh);
+        tma_load_3d(sDO + h * kBoxBytes, &tmDO, c.bar(kBarFixed), h * 64, qt * kT, bh);
       }
       int issued = 0;   // key tiles whose K and V were both requested
       for (int j = 0; j < nk; ++j, ++issued) {
-        const int ks = j % kQKSlots, vs = j % kQVSlots;
-        if (j >= kQKSlots && !wait_phase(c, kBarKEmpty + ks, (j / kQKSlots - 1) & 1, true)) break;
-        mbar_arrive_expect_tx(c.bar(kBarKFull + ks), kTileBytes);
-        for (int h = 0; h < 2; ++h) tma_load_3d(kslot(j) + h * kBoxBytes, &tmK, c.bar(kBarKFull + ks), h * 64, j * kT, bh);
-        if (j >= kQVSlots && !wait_phase(c, kBarVEmpty + vs, (j / kQVSlots - 1) & 1, true)) {
-          wait_phase(c, kBarKFull + ks, (j / kQKSlots) & 1, false);   // that K copy is in flight
+        const int ks = j % kSlotsA, vs = j % kSlotsB;
+        if (j >= kSlotsA && !wait_phase(c, kBarEmptyA + ks, (j / kSlotsA - 1) & 1, true)) break;
+        mbar_arrive_expect_tx(c.bar(kBarFullA + ks), kTileBytes);
+        for (int h = 0; h < 2; ++h) tma_load_3d(kslot(j) + h * kBoxBytes, &tmK, c.bar(kBarFullA + ks), h * 64, j * kT, bh);
+        if (j >= kSlotsB && !wait_phase(c, kBarEmptyB + vs, (j / kSlotsB - 1) & 1, true)) {
+          wait_phase(c, kBarFullA + ks, (j / kSlotsA) & 1, false);   // that K copy is in flight
           break;
         }
-        mbar_arrive_expect_tx(c.bar(kBarVFull + vs), kTileBytes);
-        for (int h = 0; h < 2; ++h) tma_load_3d(vslot(j) + h * kBoxBytes, &tmV, c.bar(kBarVFull + vs), h * 64, j * kT, bh);
+        mbar_arrive_expect_tx(c.bar(kBarFullB + vs), kTileBytes);
+        for (int h = 0; h < 2; ++h) tma_load_3d(vslot(j) + h * kBoxBytes, &tmV, c.bar(kBarFullB + vs), h * 64, j * kT, bh);
       }
       // no copy into shared memory may be in flight when the block exits
       wait_phase(c, kBarFixed, 0, false);
-      for (int j = issued - kQKSlots < 0 ? 0 : issued - kQKSlots; j < issued; ++j)
-        wait_phase(c, kBarKFull + j % kQKSlots, (j / kQKSlots) & 1, false);
-      for (int j = issued - kQVSlots < 0 ? 0 : issued - kQVSlots; j < issued; ++j)
-        wait_phase(c, kBarVFull + j % kQVSlots, (j / kQVSlots) & 1, false);
+      for (int j = issued - kSlotsA < 0 ? 0 : issued - kSlotsA; j < issued; ++j)
+        wait_phase(c, kBarFullA + j % kSlotsA, (j / kSlotsA) & 1, false);
+      for (int j = issued - kSlotsB < 0 ? 0 : issued - kSlotsB; j < issued; ++j)
+        wait_phase(c, kBarFullB + j % kSlotsB, (j / kSlotsB) & 1, false);
     }
     __syncwarp();
   } else if (warp == 1) {
     if (lane == 0) {
-      bool ok = wait_phase(c, kBarFixed, 0, true) && wait_phase(c, kBarKFull, 0, true) &&
-                wait_phase(c, kBarVFull, 0, true);
+      bool ok = wait_phase(c, kBarFixed, 0, true) && wait_phase(c, kBarFullA, 0, true) &&
+                wait_phase(c, kBarFullB, 0, true);
       if (ok) {
         tc_fence_after();
-        mma_rows_by_rows(tS0, base + kQOffQ, kslot(0));                   // S(0) = Q K_0^T
-        mma_rows_by_rows(tdP, base + kQOffDO, vslot(0));                  // dP(0) = dO V_0^T
+        mma_rows_by_rows(tS0, sQ, kslot(0));                   // S(0) = Q K_0^T
+        mma_rows_by_rows(tdP, sDO, vslot(0));                  // dP(0) = dO V_0^T
         tc_commit(c.bar(kBarSdP));
-        tc_commit(c.bar(kBarVEmpty + 0));
+        tc_commit(c.bar(kBarEmptyB + 0));
       }
       for (int j = 0; ok && j < nk; ++j) {
         const int s = j & 1;
@@ -653,16 +662,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           // S(j+1) into the other buffer (its dS(j-1) was read by the dQ MMAs issued before);
           // dP(j+1) once every compute warp has taken dP(j) into registers
           const int j1 = j + 1, s1 = s ^ 1;
-          if (!wait_phase(c, kBarKFull + j1 % kQKSlots, (j1 / kQKSlots) & 1, true)) break;
+          if (!wait_phase(c, kBarFullA + j1 % kSlotsA, (j1 / kSlotsA) & 1, true)) break;
           tc_fence_after();
-          mma_rows_by_rows(s1 ? tS1 : tS0, base + kQOffQ, kslot(j1));
+          mma_rows_by_rows(s1 ? tS1 : tS0, sQ, kslot(j1));
           if (!wait_phase(c, kBarDPFree, j & 1, true) ||
-              !wait_phase(c, kBarVFull + j1 % kQVSlots, (j1 / kQVSlots) & 1, true))
+              !wait_phase(c, kBarFullB + j1 % kSlotsB, (j1 / kSlotsB) & 1, true))
             break;
           tc_fence_after();
-          mma_rows_by_rows(tdP, base + kQOffDO, vslot(j1));
+          mma_rows_by_rows(tdP, sDO, vslot(j1));
           tc_commit(c.bar(kBarSdP));
-          tc_commit(c.bar(kBarVEmpty + j1 % kQVSlots));   // V_{j+1} is free once dP(j+1) is done
+          tc_commit(c.bar(kBarEmptyB + j1 % kSlotsB));   // V_{j+1} is free once dP(j+1) is done
         }
         // The compute warps may finish step j + 1 before this thread gets here, so steps
         // alternate between two sets of hand-off barriers: a set completes at most once
@@ -676,7 +685,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           mma_tmem_by_rows_half(tdQ, tSj + 64 * h, kslot(j), h, j > 0 || h > 0);   // dQ += dS K_j
         }
         if (!ok) break;
-        tc_commit(c.bar(kBarKEmpty + j % kQKSlots));
+        tc_commit(c.bar(kBarEmptyA + j % kSlotsA));
       }
       tc_commit(c.bar(kBarAcc));
       wait_phase(c, kBarAcc, 0, false);
@@ -736,7 +745,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (ok && wait_warp(c, kBarAcc, 0)) {
       tc_fence_after();
       const int row0 = qt * kT + quarter * 32;
-      uint8_t* st = smem + kQOffQ + (warp - 4) * kStageWarpBytes;   // Q is no longer read
+      uint8_t* st = smem + kOffFixed0 + (warp - 4) * kStageWarpBytes;   // Q is no longer read
       store_acc_half(tdQ + lane_off, grp, p.scale, st, p.dq + (static_cast<size_t>(bh) * p.Nq + row0) * kD,
                      p.Nq - row0);
     }
@@ -803,9 +812,9 @@ template <bool kCausal>
 int launch_bwd(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, const CUtensorMap& mdo,
                const BwdParams& p, long long bh, long long k_tiles, long long q_tiles, cudaStream_t s) {
   if (!g_attr_done[kCausal].load(std::memory_order_acquire)) {
-    if (cudaFuncSetAttribute(bwd_dkdv_kernel<kCausal>, cudaFuncAttributeMaxDynamicSharedMemorySize, kKVSmem) !=
+    if (cudaFuncSetAttribute(bwd_dkdv_kernel<kCausal>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemKV) !=
             cudaSuccess ||
-        cudaFuncSetAttribute(bwd_dq_kernel<kCausal>, cudaFuncAttributeMaxDynamicSharedMemorySize, kQSmem) !=
+        cudaFuncSetAttribute(bwd_dq_kernel<kCausal>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemQ) !=
             cudaSuccess)
       return ATTN_ERR_CUDA;
     g_attr_done[kCausal].store(1, std::memory_order_release);
@@ -814,11 +823,11 @@ int launch_bwd(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& 
   cfg.blockDim = dim3(kThreads);
   cfg.stream = s;
   cfg.gridDim = dim3(static_cast<unsigned>(bh * k_tiles));
-  cfg.dynamicSmemBytes = kKVSmem;
+  cfg.dynamicSmemBytes = kSmemKV;
   if (cudaLaunchKernelEx(&cfg, bwd_dkdv_kernel<kCausal>, mq, mk, mv, mdo, p) != cudaSuccess) return ATTN_ERR_CUDA;
   g_bwd_launches.fetch_add(1, std::memory_order_relaxed);
   cfg.gridDim = dim3(static_cast<unsigned>(bh * q_tiles));
-  cfg.dynamicSmemBytes = kQSmem;
+  cfg.dynamicSmemBytes = kSmemQ;
   if (cudaLaunchKernelEx(&cfg, bwd_dq_kernel<kCausal>, mq, mk, mv, mdo, p) != cudaSuccess) return ATTN_ERR_CUDA;
   g_bwd_launches.fetch_add(1, std::memory_order_relaxed);
   return ATTN_OK;
@@ -912,7 +921,7 @@ extern "C" int attn_bwd_status(void* stream) {
   if (cudaMemcpyToSymbolAsync(g_bwd_status, &zero, sizeof zero, 0, cudaMemcpyHostToDevice, s) != cudaSuccess ||
       cudaStreamSynchronize(s) != cudaSuccess)
     return ATTN_ERR_CUDA;
-  return ATTN_ERR_TIMEOUT;
+  return (h & 2u) ? ATTN_ERR_CUDA : ATTN_ERR_TIMEOUT;
 }
 
 extern "C" unsigned long long attn_bwd_kernel_count(void) { return g_bwd_launches.load(std::memory_order_relaxed); }
