@@ -14,12 +14,12 @@
 //
 // Three kernels, all on the caller's stream:
 //
-//   bwd_rows_kernel  one warp per query row: D_i and LSE_i * log2 e, written as a float2
-//                    per row into a workspace padded to whole 128-row tiles (pad rows get
-//                    LSE = +inf, D = 0, so their P is exactly 0).
+//   bwd_rows_kernel  one warp per query row: -D_i and -LSE_i * log2 e, written planar per
+//                    128-row tile into a workspace padded to whole tiles (pad rows get
+//                    -LSE = -inf, -D = -0, so their P is exactly 0).
 //   bwd_dkdv_kernel  one block per (b, h, 128-key tile). K and V are loaded once; then per
-//                    128-query tile j (double-buffered Q_j, dO_j and the rows' float2 by
-//                    TMA): S^T = K Q_j^T and dP^T = V dO_j^T on tcgen05 into TMEM; the
+//                    128-query tile j (Q_j, dO_j and the tile's row values by TMA, in
+//                    rings): S^T = K Q_j^T and dP^T = V dO_j^T on tcgen05 into TMEM; the
 //                    compute warps (thread = key) form P^T and write it back over S^T as
 //                    BF16 pairs, then dS^T over dP^T; dV += P^T dO_j and dK += dS^T Q_j take
 //                    them straight from TMEM (the A operand) with dO_j and Q_j as MN-major B
@@ -81,7 +81,7 @@ constexpr float kLog2e = 1.4426950408889634f;
 // checks the alignment before touching it. The dQ block has no rows: its barriers follow
 // the tiles, and it realigns its base itself.
 constexpr int kSlotsA = 3, kSlotsB = 2;
-constexpr int kRowsBytes = kT * 8;                             // float2 (LSE log2, D) per query row
+constexpr int kRowsBytes = kT * 8;                             // a query tile's 128 (-LSE log2 e) and 128 (-D)
 constexpr int kOffFixed0 = 0;                                  // K (dK/dV block) or Q (dQ block)
 constexpr int kOffFixed1 = kTileBytes;                         // V or dO
 constexpr int kOffRingA = 2 * kTileBytes;                      // Q_j or K_j
@@ -196,11 +196,56 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&x)[16
       "r"(x[9]), "r"(x[10]), "r"(x[11]), "r"(x[12]), "r"(x[13]), "r"(x[14]), "r"(x[15])
       : "memory");
 }
+__device__ __forceinline__ void tmem_ld64(uint32_t taddr, uint32_t (&x)[64]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x64.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32, %33, %34, %35, %36, %37, %38, %39, %40, %41, %42, %43, %44, %45, %46, %47, %48, %49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, %60, %61, %62, %63}, [%64];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(x[0]), "=r"(x[1]), "=r"(x[2]), "=r"(x[3]), "=r"(x[4]), "=r"(x[5]), "=r"(x[6]), "=r"(x[7]), "=r"(x[8]), "=r"(x[9]), "=r"(x[10]), "=r"(x[11]), "=r"(x[12]), "=r"(x[13]), "=r"(x[14]), "=r"(x[15]), "=r"(x[16]), "=r"(x[17]), "=r"(x[18]), "=r"(x[19]), "=r"(x[20]), "=r"(x[21]), "=r"(x[22]), "=r"(x[23]), "=r"(x[24]), "=r"(x[25]), "=r"(x[26]), "=r"(x[27]), "=r"(x[28]), "=r"(x[29]), "=r"(x[30]), "=r"(x[31]), "=r"(x[32]), "=r"(x[33]), "=r"(x[34]), "=r"(x[35]), "=r"(x[36]), "=r"(x[37]), "=r"(x[38]), "=r"(x[39]), "=r"(x[40]), "=r"(x[41]), "=r"(x[42]), "=r"(x[43]), "=r"(x[44]), "=r"(x[45]), "=r"(x[46]), "=r"(x[47]), "=r"(x[48]), "=r"(x[49]), "=r"(x[50]), "=r"(x[51]), "=r"(x[52]), "=r"(x[53]), "=r"(x[54]), "=r"(x[55]), "=r"(x[56]), "=r"(x[57]), "=r"(x[58]), "=r"(x[59]), "=r"(x[60]), "=r"(x[61]), "=r"(x[62]), "=r"(x[63])
+      : "r"(taddr)
+      : "memory");
+}
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&x)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};\n\t"
+      "tcgen05.wait::st.sync.aligned;" ::"r"(taddr),
+      "r"(x[0]), "r"(x[1]), "r"(x[2]), "r"(x[3]), "r"(x[4]), "r"(x[5]), "r"(x[6]), "r"(x[7]), "r"(x[8]), "r"(x[9]), "r"(x[10]), "r"(x[11]), "r"(x[12]), "r"(x[13]), "r"(x[14]), "r"(x[15]), "r"(x[16]), "r"(x[17]), "r"(x[18]), "r"(x[19]), "r"(x[20]), "r"(x[21]), "r"(x[22]), "r"(x[23]), "r"(x[24]), "r"(x[25]), "r"(x[26]), "r"(x[27]), "r"(x[28]), "r"(x[29]), "r"(x[30]), "r"(x[31])
+      : "memory");
+}
 __device__ __forceinline__ float ex2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
+// Packed FP32x2 arithmetic: each lane of the pair is rounded exactly as the scalar
+// operation would round it (fma / add / mul, round to nearest, no flush of denormals).
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {   // a * b + c
+  float2 d;
+  asm("{\n\t.reg .b64 a, b, c, d;\n\t"
+      "mov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\tmov.b64 c, {%6, %7};\n\t"
+      "fma.rn.f32x2 d, a, b, c;\n\tmov.b64 {%0, %1}, d;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+  return d;
+}
+__device__ __forceinline__ float2 fadd2(float2 a, float2 b) {
+  float2 d;
+  asm("{\n\t.reg .b64 a, b, d;\n\t"
+      "mov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\t"
+      "add.rn.f32x2 d, a, b;\n\tmov.b64 {%0, %1}, d;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return d;
+}
+__device__ __forceinline__ float2 fmul2(float2 a, float2 b) {
+  float2 d;
+  asm("{\n\t.reg .b64 a, b, d;\n\t"
+      "mov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\t"
+      "mul.rn.f32x2 d, a, b;\n\tmov.b64 {%0, %1}, d;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return d;
+}
+__device__ __forceinline__ float2 f2(uint32_t lo, uint32_t hi) { return make_float2(__uint_as_float(lo), __uint_as_float(hi)); }
 // two floats -> packed BF16x2 (round to nearest even), lo in the low half
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   uint32_t r;
@@ -275,7 +320,8 @@ struct BwdParams {
   uint16_t* dq;
   uint16_t* dk;
   uint16_t* dv;
-  const float2* rows;   // [BH, q_pad]: (LSE * log2 e, D)
+  // [BH, q_pad / 128, 2, 128]: per 128-row query tile, -LSE * log2 e of its rows, then -D
+  const float* rows;
   int Nq, Nk, q_tiles, k_tiles, q_pad;
   int causal;   // query i sees keys 0 .. i + off only (off = Nk - Nq >= 0)
   int off;
@@ -354,18 +400,26 @@ __device__ __forceinline__ void block_teardown(uint32_t tmem, int warp) {
 }
 
 // ---------------------------------------------------------------------------------
-// Row pass: (LSE_i log2 e, D_i = dO_i . O_i) per query row, pad rows (+inf, 0)
+// Row pass: -LSE_i log2 e and -D_i (D_i = dO_i . O_i) per query row, stored planar per
+// 128-row tile (the tile's 128 values of -LSE log2 e, then its 128 of -D), so the dK/dV
+// block reads four consecutive query columns with one shared-memory load. Both are kept
+// negated so that the kernels add them: s * c + (-LSE) and dP + (-D) round exactly as
+// s * c - LSE and dP - D. Pad rows: (-inf, -0), so their P is exactly 0.
 // ---------------------------------------------------------------------------------
 __global__ void __launch_bounds__(256) bwd_rows_kernel(const uint16_t* __restrict__ o, const uint16_t* __restrict__ dout,
-                                                       const float* __restrict__ lse, float2* __restrict__ rows,
+                                                       const float* __restrict__ lse, float* __restrict__ rows,
                                                        long long bh_count, int Nq, int q_pad) {
   const long long row = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (row >= bh_count * q_pad) return;
   const long long bh = row / q_pad;
   const int i = static_cast<int>(row - bh * q_pad);
+  float* nl = rows + 2 * row - (i & (kT - 1));   // the tile's first float is 2 * (row - i % 128)
   if (i >= Nq) {
-    if (lane == 0) rows[row] = make_float2(INFINITY, 0.0f);
+    if (lane == 0) {
+      nl[0] = -INFINITY;
+      nl[kT] = -0.0f;
+    }
     return;
   }
   const size_t base = (static_cast<size_t>(bh) * Nq + i) * kD + lane * 4;
@@ -377,7 +431,10 @@ __global__ void __launch_bounds__(256) bwd_rows_kernel(const uint16_t* __restric
               __uint_as_float(a.y & 0xffff0000u) * __uint_as_float(b.y & 0xffff0000u);
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-  if (lane == 0) rows[row] = make_float2(lse[static_cast<size_t>(bh) * Nq + i] * kLog2e, acc);
+  if (lane == 0) {
+    nl[0] = -(lse[static_cast<size_t>(bh) * Nq + i] * kLog2e);
+    nl[kT] = -acc;
+  }
 }
 
 // ---------------------------------------------------------------------------------
@@ -438,7 +495,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive_expect_tx(c.bar(kBarFullB + b), kTileBytes + kRowsBytes);
         for (int h = 0; h < 2; ++h) tma_load_3d(sDO(j) + h * kBoxBytes, &tmDO, c.bar(kBarFullB + b), h * 64, (q0 + j) * kT, bh);
         bulk_load(base + kOffRows + b * kRowsBytes,
-                  p.rows + static_cast<size_t>(bh) * p.q_pad + static_cast<size_t>(q0 + j) * kT, kRowsBytes,
+                  p.rows + 2 * (static_cast<size_t>(bh) * p.q_pad + static_cast<size_t>(q0 + j) * kT), kRowsBytes,
                   c.bar(kBarFullB + b));
       }
       // no copy into shared memory may be in flight when the block exits
@@ -514,34 +571,37 @@ __global__ void __launch_bounds__(kThreads, 1)
         break;
       }
       tc_fence_after();
-      const float2* rw = reinterpret_cast<const float2*>(smem + kOffRows + b * kRowsBytes);
+      // the tile's -LSE log2 e and -D, 128 query columns each (every lane reads the same words)
+      const float* nl = reinterpret_cast<const float*>(smem + kOffRows + b * kRowsBytes) + 64 * grp;
+      const float* nd = nl + kT;
       // causal: this thread's key r is seen by query columns c >= r - off - (q0 + j) * 128
       const int key = kt * kT + quarter * 32 + lane;
-      const int c_lo = kCausal ? key - p.off - (q0 + j) * kT : -1;
+      const int c_lo = kCausal ? key - p.off - (q0 + j) * kT - 64 * grp : -1;   // in group columns
       const bool mask_warp = kCausal && (kt * kT + quarter * 32 + 31 - p.off - (q0 + j) * kT) > 64 * grp;
-      // P^T of the group's 64 query columns, kept in registers for dS^T; handed over first
+      // P^T of the group's 64 query columns, kept in registers for dS^T; written over the
+      // first 32 of the group's S^T columns as BF16 pairs and handed over first
+      const float2 c2 = make_float2(p.scale_log2, p.scale_log2);
       float pv[64];
+      {
+        uint32_t xs[64];
+        tmem_ld64(tS + lane_off + 64 * grp, xs);
+        uint32_t pw[32];
 #pragma unroll
-      for (int ch = 0; ch < 2; ++ch) {   // 32 query columns at a time
-        const int col0 = 64 * grp + 32 * ch;
-        uint32_t xs[32];
-        tmem_ld32(tS + lane_off + col0, xs);
-        uint32_t pw[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const float2 r0 = rw[col0 + 2 * i], r1 = rw[col0 + 2 * i + 1];
-          float p0 = ex2(fmaf(__uint_as_float(xs[2 * i]), p.scale_log2, -r0.x));
-          float p1 = ex2(fmaf(__uint_as_float(xs[2 * i + 1]), p.scale_log2, -r1.x));
+        for (int i = 0; i < 16; ++i) {   // query columns 4i .. 4i + 3 of the group
+          const float4 l4 = *reinterpret_cast<const float4*>(nl + 4 * i);
+          const float2 a0 = ffma2(f2(xs[4 * i], xs[4 * i + 1]), c2, make_float2(l4.x, l4.y));
+          const float2 a1 = ffma2(f2(xs[4 * i + 2], xs[4 * i + 3]), c2, make_float2(l4.z, l4.w));
+          float q[4] = {ex2(a0.x), ex2(a0.y), ex2(a1.x), ex2(a1.y)};
           if (mask_warp) {
-            p0 = col0 + 2 * i >= c_lo ? p0 : 0.0f;
-            p1 = col0 + 2 * i + 1 >= c_lo ? p1 : 0.0f;
+#pragma unroll
+            for (int t = 0; t < 4; ++t) q[t] = 4 * i + t >= c_lo ? q[t] : 0.0f;
           }
-          pv[32 * ch + 2 * i] = p0;
-          pv[32 * ch + 2 * i + 1] = p1;
-          pw[i] = pack_bf16(p0, p1);
+#pragma unroll
+          for (int t = 0; t < 4; ++t) pv[4 * i + t] = q[t];
+          pw[2 * i] = pack_bf16(q[0], q[1]);
+          pw[2 * i + 1] = pack_bf16(q[2], q[3]);
         }
-        // group columns 64 grp + 16 ch .. + 15 were read in this or the previous chunk
-        tmem_st16(tS + lane_off + 64 * grp + 16 * ch, pw);
+        tmem_st32(tS + lane_off + 64 * grp, pw);
       }
       tc_fence_before();
       __syncwarp();
@@ -552,19 +612,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         break;
       }
       tc_fence_after();
-#pragma unroll
-      for (int ch = 0; ch < 2; ++ch) {
-        const int col0 = 64 * grp + 32 * ch;
-        uint32_t xd[32];
-        tmem_ld32(tdP + lane_off + col0, xd);
-        uint32_t dw[16];
+      {
+        // dS^T = P^T (dP^T - D), written over the first 32 of the group's dP^T columns
+        uint32_t xd[64];
+        tmem_ld64(tdP + lane_off + 64 * grp, xd);
+        uint32_t dw[32];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-          const float d0 = pv[32 * ch + 2 * i] * (__uint_as_float(xd[2 * i]) - rw[col0 + 2 * i].y);
-          const float d1 = pv[32 * ch + 2 * i + 1] * (__uint_as_float(xd[2 * i + 1]) - rw[col0 + 2 * i + 1].y);
-          dw[i] = pack_bf16(d0, d1);
+          const float4 d4 = *reinterpret_cast<const float4*>(nd + 4 * i);
+          const float2 t0 = fmul2(make_float2(pv[4 * i], pv[4 * i + 1]), fadd2(f2(xd[4 * i], xd[4 * i + 1]), make_float2(d4.x, d4.y)));
+          const float2 t1 = fmul2(make_float2(pv[4 * i + 2], pv[4 * i + 3]), fadd2(f2(xd[4 * i + 2], xd[4 * i + 3]), make_float2(d4.z, d4.w)));
+          dw[2 * i] = pack_bf16(t0.x, t0.y);
+          dw[2 * i + 1] = pack_bf16(t1.x, t1.y);
         }
-        tmem_st16(tdP + lane_off + 64 * grp + 16 * ch, dw);
+        tmem_st32(tdP + lane_off + 64 * grp, dw);
       }
       tc_fence_before();
       __syncwarp();
@@ -696,8 +757,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int grp = (warp - 4) >> 2;   // key columns 64 grp .. 64 grp + 63
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
     const int qrow = qt * kT + quarter * 32 + lane;
-    float2 rw = make_float2(0.0f, 0.0f);   // rows past Nq: any finite values (never stored)
-    if (qrow < p.Nq) rw = p.rows[static_cast<size_t>(bh) * p.q_pad + qrow];
+    // this row's -LSE log2 e and -D; rows past Nq: any finite values (never stored)
+    float nl = 0.0f, nd = 0.0f;
+    if (qrow < p.Nq) {
+      const float* rt = p.rows + 2 * (static_cast<size_t>(bh) * p.q_pad + static_cast<size_t>(qt) * kT);
+      nl = rt[quarter * 32 + lane];
+      nd = rt[kT + quarter * 32 + lane];
+    }
+    const float2 c2 = make_float2(p.scale_log2, p.scale_log2), nl2 = make_float2(nl, nl), nd2 = make_float2(nd, nd);
     bool ok = true;
     for (int j = 0; j < nk; ++j) {
       if (!wait_warp(c, kBarSdP, j & 1)) {
@@ -707,35 +774,37 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const uint32_t tSj = (j & 1) ? tS1 : tS0;
       // keys of this tile inside the sequence: columns < valid; causal: also <= c_hi
-      const int valid = p.Nk - j * kT;
-      const int c_hi = kCausal ? qrow + p.off - j * kT : kT;
+      const int valid = p.Nk - j * kT - 64 * grp;   // in group columns
+      const int c_hi = kCausal ? qrow + p.off - j * kT - 64 * grp : kT;
       const bool mask_warp = kCausal && (qt * kT + quarter * 32 + p.off - j * kT) < 64 * grp + 63;
-      uint32_t xd[2][32];
-      tmem_ld32(tdP + lane_off + 64 * grp, xd[0]);
-      tmem_ld32(tdP + lane_off + 64 * grp + 32, xd[1]);
+      const bool full = valid >= 64 && !mask_warp;   // warp-uniform: no column of the group is masked
+      uint32_t xd[64];
+      tmem_ld64(tdP + lane_off + 64 * grp, xd);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(c.bar(kBarDPFree));   // dP may be overwritten now
       __syncwarp();
+      {
+        // dS = P (dP - D) over the group's 64 key columns, written over the first 32 of them
+        uint32_t xs[64];
+        tmem_ld64(tSj + lane_off + 64 * grp, xs);
+        uint32_t dw[32];
 #pragma unroll
-      for (int ch = 0; ch < 2; ++ch) {
-        const int col0 = 64 * grp + 32 * ch;
-        uint32_t xs[32];
-        tmem_ld32(tSj + lane_off + col0, xs);
-        uint32_t dw[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const int key = col0 + 2 * i;
-          float p0 = key < valid ? ex2(fmaf(__uint_as_float(xs[2 * i]), p.scale_log2, -rw.x)) : 0.0f;
-          float p1 = key + 1 < valid ? ex2(fmaf(__uint_as_float(xs[2 * i + 1]), p.scale_log2, -rw.x)) : 0.0f;
-          if (mask_warp) {
-            p0 = key <= c_hi ? p0 : 0.0f;
-            p1 = key + 1 <= c_hi ? p1 : 0.0f;
+        for (int i = 0; i < 32; ++i) {
+          const float2 a = ffma2(f2(xs[2 * i], xs[2 * i + 1]), c2, nl2);
+          float p0 = ex2(a.x), p1 = ex2(a.y);
+          if (!full) {
+            p0 = 2 * i < valid ? p0 : 0.0f;
+            p1 = 2 * i + 1 < valid ? p1 : 0.0f;
+            if (mask_warp) {
+              p0 = 2 * i <= c_hi ? p0 : 0.0f;
+              p1 = 2 * i + 1 <= c_hi ? p1 : 0.0f;
+            }
           }
-          dw[i] = pack_bf16(p0 * (__uint_as_float(xd[ch][2 * i]) - rw.y),
-                            p1 * (__uint_as_float(xd[ch][2 * i + 1]) - rw.y));
+          const float2 d = fmul2(make_float2(p0, p1), fadd2(f2(xd[2 * i], xd[2 * i + 1]), nd2));
+          dw[i] = pack_bf16(d.x, d.y);
         }
-        tmem_st16(tSj + lane_off + 64 * grp + 16 * ch, dw);
+        tmem_st32(tSj + lane_off + 64 * grp, dw);
       }
       tc_fence_before();
       __syncwarp();
@@ -792,7 +861,7 @@ bool make_map(CUtensorMap* map, const void* ptr, int rows, long long bh) {
 std::mutex g_ws_mu;
 std::map<std::pair<int, uintptr_t>, std::pair<void*, size_t>> g_ws;
 
-int get_rows_workspace(int dev, cudaStream_t stream, size_t bytes, float2** out) {
+int get_rows_workspace(int dev, cudaStream_t stream, size_t bytes, float** out) {
   std::lock_guard<std::mutex> lock(g_ws_mu);
   auto& ws = g_ws[std::make_pair(dev, reinterpret_cast<uintptr_t>(stream))];
   if (ws.second < bytes) {
@@ -802,7 +871,7 @@ int get_rows_workspace(int dev, cudaStream_t stream, size_t bytes, float2** out)
     if (cudaMallocAsync(&ws.first, bytes, stream) != cudaSuccess) return ATTN_ERR_CUDA;
     ws.second = bytes;
   }
-  *out = static_cast<float2*>(ws.first);
+  *out = static_cast<float*>(ws.first);
   return ATTN_OK;
 }
 
@@ -879,9 +948,9 @@ int backward(const void* q, const void* k, const void* v, const void* o, const v
   p.causal = causal ? 1 : 0;
   p.off = causal ? Nk - Nq : 0;
   p.withhold = g_bwd_withhold.load(std::memory_order_relaxed);
-  float2* rows = nullptr;
+  float* rows = nullptr;
   {
-    const int rc = get_rows_workspace(dev, s, static_cast<size_t>(bh) * p.q_pad * sizeof(float2), &rows);
+    const int rc = get_rows_workspace(dev, s, static_cast<size_t>(bh) * p.q_pad * 2 * sizeof(float), &rows);
     if (rc != ATTN_OK) return rc;
   }
   p.rows = rows;
