@@ -74,8 +74,10 @@ constexpr float kLog2e = 1.4426950408889634f;
 // product and again by the step's last product (dK += dS^T Q_j, dQ += dS K_j); the second
 // (dO_j, V_j) only by products early in the step. The first ring has three slots, the
 // second two: both request every tile more than a step before its first product needs it.
-// In the dK/dV block the query rows' (LSE, D) travel with dO_j, and its slot comes free with
-// the commit that ends step j (dV and dK of the step done, so dS^T_j and the rows were read).
+// In the dK/dV block the query rows' (-LSE, -D) travel with dO_j. The compute warps free the
+// slots there: each of them, on seeing S^T_{j+1} complete (hence dV_j, the last reader of
+// dO_j), has also finished its own work on tile j's rows, and frees dO_j's slot with one
+// arrival of eight; one of them, on seeing dP^T_{j+1} complete (hence dK_j), frees Q_j's.
 // Seven 32 KB tiles and the rows fill the dK/dV block's shared memory, with no room to
 // realign its base: that kernel declares it 1024-aligned (the 128-byte swizzle's atom) and
 // checks the alignment before touching it. The dQ block has no rows: its barriers follow
@@ -95,10 +97,12 @@ constexpr int kBarFixed = 0;        // the block's fixed tiles (K, V or Q, dO) h
 constexpr int kBarFullA = 1;        // [3] ring A slot landed
 constexpr int kBarEmptyA = 4;       // [3] ring A slot read by its last product
 constexpr int kBarFullB = 7;        // [2] ring B slot landed
-constexpr int kBarEmptyB = 9;       // [2] dQ block: ring B slot read by its product
+constexpr int kBarEmptyB = 9;       // [2] ring B slot read by its product (dK/dV block: and its rows)
 constexpr int kBarSdP = 11;         // S and dP complete in TMEM (dK/dV block: S^T alone)
-constexpr int kBarPdS = 12;         // [step parity][2]: a column half of P / dS is in TMEM (one
-                                    // arrival per warp); the dK/dV block: [0][g] P^T, [1][g] dS^T
+constexpr int kBarPdS = 12;         // dQ block: [step parity][2]: a column half of dS is in TMEM
+                                    // (one arrival per warp of the group)
+constexpr int kBarPAll = 12;        // dK/dV block: P^T of every compute warp is in TMEM
+constexpr int kBarDSAll = 13;       // dK/dV block: dS^T of every compute warp is in TMEM
 constexpr int kBarAcc = 16;         // accumulators complete
 constexpr int kBarDPFree = 17;      // dQ block: every compute warp holds dP of the step in registers
 constexpr int kBarDPReady = 18;     // dK/dV block: dP^T complete in TMEM
@@ -185,15 +189,6 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&x)[32]) {
         "=r"(x[16]), "=r"(x[17]), "=r"(x[18]), "=r"(x[19]), "=r"(x[20]), "=r"(x[21]), "=r"(x[22]), "=r"(x[23]),
         "=r"(x[24]), "=r"(x[25]), "=r"(x[26]), "=r"(x[27]), "=r"(x[28]), "=r"(x[29]), "=r"(x[30]), "=r"(x[31])
       : "r"(taddr)
-      : "memory");
-}
-__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&x)[16]) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, "
-      "%14, %15, %16};\n\t"
-      "tcgen05.wait::st.sync.aligned;" ::"r"(taddr),
-      "r"(x[0]), "r"(x[1]), "r"(x[2]), "r"(x[3]), "r"(x[4]), "r"(x[5]), "r"(x[6]), "r"(x[7]), "r"(x[8]),
-      "r"(x[9]), "r"(x[10]), "r"(x[11]), "r"(x[12]), "r"(x[13]), "r"(x[14]), "r"(x[15])
       : "memory");
 }
 __device__ __forceinline__ void tmem_ld64(uint32_t taddr, uint32_t (&x)[64]) {
@@ -367,10 +362,17 @@ __device__ __forceinline__ void store_acc_half(uint32_t t_acc, int h, float mul,
 }
 
 // Block setup shared by both kernels: barrier init, TMEM allocation. Returns the TMEM base.
-__device__ __forceinline__ uint32_t block_setup(const Ctl& c, uint8_t* flags, uint32_t flags_u32, int warp) {
+__device__ __forceinline__ uint32_t block_setup(const Ctl& c, uint8_t* flags, uint32_t flags_u32, int warp,
+                                                bool dkdv) {
   if (threadIdx.x == 0) {
     for (int b = kBarFixed; b <= kBarSdP; ++b) mbar_init(c.bar(b), 1);   // fixed tiles, rings, S
-    for (int b = 0; b < 4; ++b) mbar_init(c.bar(kBarPdS + b), 4);   // one arrival per warp of a group
+    if (dkdv) {   // one arrival per compute warp
+      for (int b = 0; b < kSlotsB; ++b) mbar_init(c.bar(kBarEmptyB + b), 8);
+      mbar_init(c.bar(kBarPAll), 8);
+      mbar_init(c.bar(kBarDSAll), 8);
+    } else {
+      for (int b = 0; b < 4; ++b) mbar_init(c.bar(kBarPdS + b), 4);   // one arrival per warp of a group
+    }
     mbar_init(c.bar(kBarAcc), 1);
     mbar_init(c.bar(kBarDPFree), 8);    // one arrival per compute warp
     mbar_init(c.bar(kBarDPReady), 1);
@@ -458,7 +460,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   c.bars = base + kOffBar;
   c.abort = reinterpret_cast<volatile uint32_t*>(smem + kOffBar + kNumBars * 8 + 4);
   c.limit = p.wait_limit;
-  const uint32_t tmem = block_setup(c, smem + kOffBar, base + kOffBar, warp);
+  const uint32_t tmem = block_setup(c, smem + kOffBar, base + kOffBar, warp, true);
   const uint32_t tS = tmem, tdP = tmem + 128, tdV = tmem + 256, tdK = tmem + 384;
   const uint32_t sK = base + kOffFixed0, sV = base + kOffFixed1;
   // query tiles q0 .. q_tiles - 1; causal: from the first tile whose rows see this tile's
@@ -487,8 +489,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (p.withhold && j == 1) break;   // test hook: the consumers' waits for this tile run out
         mbar_arrive_expect_tx(c.bar(kBarFullA + a), kTileBytes);
         for (int h = 0; h < 2; ++h) tma_load_3d(sQ(j) + h * kBoxBytes, &tmQ, c.bar(kBarFullA + a), h * 64, (q0 + j) * kT, bh);
-        // dO_j's slot held dO_{j-2}: free once step j-2 has ended (its ring A commit)
-        if (j >= kSlotsB && !wait_phase(c, kBarEmptyA + (j - kSlotsB) % kSlotsA, ((j - kSlotsB) / kSlotsA) & 1, true)) {
+        // dO_j's slot held dO_{j-2} and its rows
+        if (j >= kSlotsB && !wait_phase(c, kBarEmptyB + b, (j / kSlotsB - 1) & 1, true)) {
           wait_phase(c, kBarFullA + a, (j / kSlotsA) & 1, false);   // that Q copy is in flight
           break;
         }
@@ -508,12 +510,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else if (warp == 1) {
     if (lane == 0) {
-      // Per query tile j: dV += P^T dO_j as each group hands its half of P^T over, then
+      // Per query tile j: dV += P^T dO_j once the compute warps have handed P^T over, then
       // S^T of tile j+1 into the columns P^T leaves (the compute warps hold S^T_j in
-      // registers by then), then dK += dS^T Q_j as the halves of dS^T arrive, then dP^T of
-      // tile j+1 into the columns dS^T leaves. The next tile's scores thus run on the tensor
-      // cores while the compute warps work on this tile's dS^T, and its dP^T while they
-      // compute its P^T.
+      // registers by then), then dK += dS^T Q_j once dS^T is handed over, then dP^T of tile
+      // j+1 into the columns dS^T leaves. The next tile's scores thus run on the tensor cores
+      // while the compute warps work on this tile's dS^T, and its dP^T while they compute
+      // its P^T. Per step this thread waits twice and commits twice: every other operation
+      // of it idles the tensor core (the MMA queue is shallow), so the compute warps check
+      // that Q_{j+1} and dO_{j+1} have landed before their hand-overs of step j, and free
+      // the ring slots themselves.
       bool ok = wait_phase(c, kBarFixed, 0, true);
       if (ok && nq > 0) ok = wait_phase(c, kBarFullA, 0, true) && wait_phase(c, kBarFullB, 0, true);
       if (ok && nq > 0) {
@@ -526,33 +531,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int j = 0; ok && j < nq; ++j) {
         const int j1 = j + 1;
         const bool more = j1 < nq;
-        for (int h = 0; ok && h < 2; ++h) {   // queries 64h .. 64h + 63, as each group hands them over
-          ok = wait_phase(c, kBarPdS + h, j & 1, true);
-          if (!ok) break;
-          tc_fence_after();
-          mma_tmem_by_rows_half(tdV, tS + 64 * h, sDO(j), h, j > 0 || h > 0);   // dV += P^T dO_j
-        }
-        if (!ok) break;
+        if (!wait_phase(c, kBarPAll, j & 1, true)) break;
+        tc_fence_after();
+        for (int h = 0; h < 2; ++h)   // queries 64h .. 64h + 63
+          mma_tmem_by_rows_half(tdV, tS + 64 * h, sDO(j), h, j > 0 || h > 0);     // dV += P^T dO_j
         if (more) {
-          if (!wait_phase(c, kBarFullA + j1 % kSlotsA, (j1 / kSlotsA) & 1, true)) break;
-          tc_fence_after();
           mma_rows_by_rows(tS, sK, sQ(j1));                               // S^T = K Q_{j+1}^T
           tc_commit(c.bar(kBarSdP));
         }
-        for (int h = 0; ok && h < 2; ++h) {
-          ok = wait_phase(c, kBarPdS + 2 + h, j & 1, true);
-          if (!ok) break;
-          tc_fence_after();
-          mma_tmem_by_rows_half(tdK, tdP + 64 * h, sQ(j), h, j > 0 || h > 0);    // dK += dS^T Q_j
-        }
-        if (!ok) break;
+        if (!wait_phase(c, kBarDSAll, j & 1, true)) break;
+        tc_fence_after();
+        for (int h = 0; h < 2; ++h)
+          mma_tmem_by_rows_half(tdK, tdP + 64 * h, sQ(j), h, j > 0 || h > 0);     // dK += dS^T Q_j
         if (more) {
-          if (!wait_phase(c, kBarFullB + j1 % kSlotsB, (j1 / kSlotsB) & 1, true)) break;
-          tc_fence_after();
           mma_rows_by_rows(tdP, sV, sDO(j1));                             // dP^T = V dO_{j+1}^T
           tc_commit(c.bar(kBarDPReady));
         }
-        tc_commit(c.bar(kBarEmptyA + j % kSlotsA));   // frees Q_j, and dO_j with its rows
       }
       tc_commit(c.bar(kBarAcc));   // also: every MMA this thread issued is done before TMEM is freed
       wait_phase(c, kBarAcc, 0, false);
@@ -562,14 +556,35 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int quarter = warp & 3;
     const int grp = (warp - 4) >> 2;   // query columns 64 grp .. 64 grp + 63
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+    // One thread checks, before the hand-overs of step j, that the ring tiles the MMA
+    // thread reads next (Q_{j+1} after P^T, dO_{j+1} after dS^T) have landed; another frees
+    // Q_j's slot once it sees dP^T_{j+1} complete.
+    const bool ringer = warp == 4 && lane == 0, releaser = warp == 8 && lane == 0;
     bool ok = true;
+    // Hands the step's P^T (or dS^T) over; false (warp-uniform) if the ring check gave up.
+    auto hand_over = [&](int bar, int ring_bar, uint32_t ring_parity, bool check) {
+      tc_fence_before();
+      __syncwarp();
+      bool landed = true;
+      if (ringer && check) landed = wait_phase(c, ring_bar, ring_parity, true);
+      landed = __shfl_sync(0xffffffffu, landed, 0);
+      if (landed && lane == 0) mbar_arrive(c.bar(bar));
+      __syncwarp();
+      return landed;
+    };
     for (int j = 0; j < nq; ++j) {
-      // the rows' (LSE, D) arrive with dO_j; S^T once its MMA is done
+      // the rows (-LSE, -D) arrive with dO_j; S^T once its MMA is done
       const int b = j % kSlotsB;
+      const int j1 = j + 1;
+      const bool more = j1 < nq;
       if (!wait_warp(c, kBarFullB + b, (j / kSlotsB) & 1) || !wait_warp(c, kBarSdP, j & 1)) {
         ok = false;
         break;
       }
+      // S^T_j complete: so is dV_{j-1}, the last reader of dO_{j-1}, and this warp is done
+      // with tile j-1's rows
+      if (j > 0 && lane == 0) mbar_arrive(c.bar(kBarEmptyB + (j - 1) % kSlotsB));
+      __syncwarp();
       tc_fence_after();
       // the tile's -LSE log2 e and -D, 128 query columns each (every lane reads the same words)
       const float* nl = reinterpret_cast<const float*>(smem + kOffRows + b * kRowsBytes) + 64 * grp;
@@ -603,14 +618,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tmem_st32(tS + lane_off + 64 * grp, pw);
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(c.bar(kBarPdS + grp));
-      __syncwarp();
-      if (!wait_warp(c, kBarDPReady, j & 1)) {
+      if (!hand_over(kBarPAll, kBarFullA + j1 % kSlotsA, (j1 / kSlotsA) & 1, more) ||
+          !wait_warp(c, kBarDPReady, j & 1)) {
         ok = false;
         break;
       }
+      // dP^T_j complete: so is dK_{j-1}, the last reader of Q_{j-1}
+      if (j > 0 && releaser) mbar_arrive(c.bar(kBarEmptyA + (j - 1) % kSlotsA));
+      __syncwarp();
       tc_fence_after();
       {
         // dS^T = P^T (dP^T - D), written over the first 32 of the group's dP^T columns
@@ -627,10 +642,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tmem_st32(tdP + lane_off + 64 * grp, dw);
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(c.bar(kBarPdS + 2 + grp));
-      __syncwarp();
+      if (!hand_over(kBarDSAll, kBarFullB + j1 % kSlotsB, (j1 / kSlotsB) & 1, more)) {
+        ok = false;
+        break;
+      }
     }
     if (ok && wait_warp(c, kBarAcc, 0)) {
       tc_fence_after();
@@ -666,7 +681,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   c.bars = base + kOffBarQ;
   c.abort = reinterpret_cast<volatile uint32_t*>(smem + kOffBarQ + kNumBars * 8 + 4);
   c.limit = p.wait_limit;
-  const uint32_t tmem = block_setup(c, smem + kOffBarQ, base + kOffBarQ, warp);
+  const uint32_t tmem = block_setup(c, smem + kOffBarQ, base + kOffBarQ, warp, false);
   const uint32_t sQ = base + kOffFixed0, sDO = base + kOffFixed1;
   // S is double-buffered (the fourth 128 columns), so S and dP of the next key tile are
   // computed while the compute warps work on this one; dP has one buffer, which the
