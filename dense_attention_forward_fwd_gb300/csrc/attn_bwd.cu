@@ -99,14 +99,16 @@ constexpr int kBarEmptyA = 4;       // [3] ring A slot read by its last product
 constexpr int kBarFullB = 7;        // [2] ring B slot landed
 constexpr int kBarEmptyB = 9;       // [2] ring B slot read by its product (dK/dV block: and its rows)
 constexpr int kBarSdP = 11;         // S and dP complete in TMEM (dK/dV block: S^T alone)
-constexpr int kBarPdS = 12;         // dQ block: [step parity][2]: a column half of dS is in TMEM
-                                    // (one arrival per warp of the group)
-constexpr int kBarPAll = 12;        // dK/dV block: P^T of every compute warp is in TMEM
-constexpr int kBarDSAll = 13;       // dK/dV block: dS^T of every compute warp is in TMEM
-constexpr int kBarAcc = 16;         // accumulators complete
-constexpr int kBarDPFree = 17;      // dQ block: every compute warp holds dP of the step in registers
-constexpr int kBarDPReady = 18;     // dK/dV block: dP^T complete in TMEM
-constexpr int kNumBars = 19;
+// hand-overs from the compute warps (one arrival per compute warp)
+constexpr int kBarPAll = 12;        // dK/dV block: P^T is in TMEM
+constexpr int kBarDSAll = 13;       // dK/dV block: dS^T is in TMEM
+constexpr int kBarDS = 12;          // dQ block: [step parity] dS is in TMEM (steps alternate
+                                    // between two barriers: the compute warps may finish step
+                                    // j + 1 before the MMA thread waits for step j)
+constexpr int kBarAcc = 14;         // accumulators complete
+constexpr int kBarDPFree = 15;      // dQ block: every compute warp holds dP of the step in registers
+constexpr int kBarDPReady = 16;     // dK/dV block: dP^T complete in TMEM
+constexpr int kNumBars = 17;
 constexpr int kFlagsBytes = kNumBars * 8 + 16;   // barriers, TMEM slot, abort flag
 
 constexpr int kSmemKV = kOffBar + kFlagsBytes;
@@ -366,13 +368,11 @@ __device__ __forceinline__ uint32_t block_setup(const Ctl& c, uint8_t* flags, ui
                                                 bool dkdv) {
   if (threadIdx.x == 0) {
     for (int b = kBarFixed; b <= kBarSdP; ++b) mbar_init(c.bar(b), 1);   // fixed tiles, rings, S
-    if (dkdv) {   // one arrival per compute warp
+    // one arrival per compute warp
+    if (dkdv)
       for (int b = 0; b < kSlotsB; ++b) mbar_init(c.bar(kBarEmptyB + b), 8);
-      mbar_init(c.bar(kBarPAll), 8);
-      mbar_init(c.bar(kBarDSAll), 8);
-    } else {
-      for (int b = 0; b < 4; ++b) mbar_init(c.bar(kBarPdS + b), 4);   // one arrival per warp of a group
-    }
+    mbar_init(c.bar(kBarPAll), 8);
+    mbar_init(c.bar(kBarDSAll), 8);
     mbar_init(c.bar(kBarAcc), 1);
     mbar_init(c.bar(kBarDPFree), 8);    // one arrival per compute warp
     mbar_init(c.bar(kBarDPReady), 1);
@@ -722,6 +722,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else if (warp == 1) {
     if (lane == 0) {
+      // Per key tile j: S(j+1) into the other S buffer (its dS(j-1) was read by the dQ MMAs
+      // issued before) and dP(j+1) once every compute warp holds dP(j) in registers, then
+      // dQ += dS K_j once dS is handed over. This thread waits twice and commits twice per
+      // step: the compute warps check that K_{j+1} and V_{j+1} have landed before their
+      // dP hand-over of step j, and free V_j's slot themselves (on seeing dP(j) complete).
       bool ok = wait_phase(c, kBarFixed, 0, true) && wait_phase(c, kBarFullA, 0, true) &&
                 wait_phase(c, kBarFullB, 0, true);
       if (ok) {
@@ -729,39 +734,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         mma_rows_by_rows(tS0, sQ, kslot(0));                   // S(0) = Q K_0^T
         mma_rows_by_rows(tdP, sDO, vslot(0));                  // dP(0) = dO V_0^T
         tc_commit(c.bar(kBarSdP));
-        tc_commit(c.bar(kBarEmptyB + 0));
       }
       for (int j = 0; ok && j < nk; ++j) {
         const int s = j & 1;
         const uint32_t tSj = s ? tS1 : tS0;
         if (j + 1 < nk) {
-          // S(j+1) into the other buffer (its dS(j-1) was read by the dQ MMAs issued before);
-          // dP(j+1) once every compute warp has taken dP(j) into registers
-          const int j1 = j + 1, s1 = s ^ 1;
-          if (!wait_phase(c, kBarFullA + j1 % kSlotsA, (j1 / kSlotsA) & 1, true)) break;
+          const int j1 = j + 1;
+          if (!wait_phase(c, kBarDPFree, j & 1, true)) break;
           tc_fence_after();
-          mma_rows_by_rows(s1 ? tS1 : tS0, sQ, kslot(j1));
-          if (!wait_phase(c, kBarDPFree, j & 1, true) ||
-              !wait_phase(c, kBarFullB + j1 % kSlotsB, (j1 / kSlotsB) & 1, true))
-            break;
-          tc_fence_after();
-          mma_rows_by_rows(tdP, sDO, vslot(j1));
+          mma_rows_by_rows(s ? tS0 : tS1, sQ, kslot(j1));      // S(j+1) = Q K_{j+1}^T
+          mma_rows_by_rows(tdP, sDO, vslot(j1));               // dP(j+1) = dO V_{j+1}^T
           tc_commit(c.bar(kBarSdP));
-          tc_commit(c.bar(kBarEmptyB + j1 % kSlotsB));   // V_{j+1} is free once dP(j+1) is done
         }
-        // The compute warps may finish step j + 1 before this thread gets here, so steps
-        // alternate between two sets of hand-off barriers: a set completes at most once
-        // more before it is waited on, which keeps its phase parity unambiguous.
-        for (int h = 0; ok && h < 2; ++h) {   // keys 64h .. 64h + 63
-          if (!wait_phase(c, kBarPdS + 2 * s + h, (j >> 1) & 1, true)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
+        if (!wait_phase(c, kBarDS + s, (j >> 1) & 1, true)) break;
+        tc_fence_after();
+        for (int h = 0; h < 2; ++h)   // keys 64h .. 64h + 63
           mma_tmem_by_rows_half(tdQ, tSj + 64 * h, kslot(j), h, j > 0 || h > 0);   // dQ += dS K_j
-        }
-        if (!ok) break;
-        tc_commit(c.bar(kBarEmptyA + j % kSlotsA));
+        tc_commit(c.bar(kBarEmptyA + j % kSlotsA));   // K_j is free once dQ(j) is done
       }
       tc_commit(c.bar(kBarAcc));
       wait_phase(c, kBarAcc, 0, false);
@@ -780,12 +769,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       nd = rt[kT + quarter * 32 + lane];
     }
     const float2 c2 = make_float2(p.scale_log2, p.scale_log2), nl2 = make_float2(nl, nl), nd2 = make_float2(nd, nd);
+    // One thread checks, before the dP hand-over of step j, that K_{j+1} and V_{j+1} (read
+    // by the MMAs that hand-over releases) have landed; another frees V_j's slot.
+    const bool ringer = warp == 4 && lane == 0, releaser = warp == 8 && lane == 0;
     bool ok = true;
     for (int j = 0; j < nk; ++j) {
+      const int j1 = j + 1;
       if (!wait_warp(c, kBarSdP, j & 1)) {
         ok = false;
         break;
       }
+      if (releaser) mbar_arrive(c.bar(kBarEmptyB + j % kSlotsB));   // dP(j) complete: V_j is free
+      __syncwarp();
       tc_fence_after();
       const uint32_t tSj = (j & 1) ? tS1 : tS0;
       // keys of this tile inside the sequence: columns < valid; causal: also <= c_hi
@@ -797,6 +792,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_ld64(tdP + lane_off + 64 * grp, xd);
       tc_fence_before();
       __syncwarp();
+      bool landed = true;
+      if (ringer && j1 < nk)
+        landed = wait_phase(c, kBarFullA + j1 % kSlotsA, (j1 / kSlotsA) & 1, true) &&
+                 wait_phase(c, kBarFullB + j1 % kSlotsB, (j1 / kSlotsB) & 1, true);
+      if (!__shfl_sync(0xffffffffu, landed, 0)) {
+        ok = false;
+        break;
+      }
       if (lane == 0) mbar_arrive(c.bar(kBarDPFree));   // dP may be overwritten now
       __syncwarp();
       {
@@ -823,7 +826,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(c.bar(kBarPdS + 2 * (j & 1) + grp));
+      if (lane == 0) mbar_arrive(c.bar(kBarDS + (j & 1)));
       __syncwarp();
     }
     if (ok && wait_warp(c, kBarAcc, 0)) {
