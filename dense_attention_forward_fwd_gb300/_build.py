@@ -8,8 +8,10 @@ import subprocess
 
 PKG = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(PKG)
-SOURCES = [os.path.join(PKG, "csrc", "attn_fwd.cu"), os.path.join(PKG, "csrc", "attn_bwd.cu")]
-HEADERS = [os.path.join(ROOT, "include", "attn_fwd.h"), os.path.join(ROOT, "include", "attn_bwd.h")]
+SOURCES = [os.path.join(PKG, "csrc", "attn_fwd.cu"), os.path.join(PKG, "csrc", "attn_fwd_wide.cu"),
+           os.path.join(PKG, "csrc", "attn_bwd.cu")]
+HEADERS = [os.path.join(ROOT, "include", "attn_fwd.h"), os.path.join(ROOT, "include", "attn_bwd.h"),
+           os.path.join(PKG, "csrc", "attn_wide.h"), os.path.join(PKG, "csrc", "tc_sm103.cuh")]
 LIB_PATH = os.path.join(PKG, "libattn_fwd.so")
 
 NVCC_FLAGS = [

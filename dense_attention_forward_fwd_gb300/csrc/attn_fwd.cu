@@ -75,6 +75,7 @@
 #include <utility>
 
 #include "attn_fwd.h"
+#include "attn_wide.h"
 
 namespace {
 
@@ -1820,6 +1821,22 @@ int forward(const void* q, const void* k, const void* v, const BiasArg* bias, vo
 
 extern "C" int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Nq,
                         int Nk, int d, float scale, void* stream) {
+  if (attn_wide::supported(d)) {
+    // head dimensions above 128: the one-Q-tile kernel (attn_fwd_wide.cu); the same checks
+    if (B < 0 || H < 0 || Nq < 0 || Nk < 0 || !std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
+    if (static_cast<long long>(B) * H == 0 || Nq == 0) return ATTN_OK;
+    if (Nk == 0 || !q || !k || !v || !o || !lse) return ATTN_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) | reinterpret_cast<uintptr_t>(v) |
+         reinterpret_cast<uintptr_t>(o)) & 15u)
+      return ATTN_ERR_MISALIGNED;
+    if (reinterpret_cast<uintptr_t>(lse) & 3u) return ATTN_ERR_MISALIGNED;
+    const long long max_rows = static_cast<long long>(Nq > Nk ? Nq : Nk);
+    if (static_cast<long long>(B) * H > (LLONG_MAX / (2 * d)) / max_rows) return ATTN_ERR_INVALID_ARG;
+    const int rc = attn_wide::forward(q, k, v, o, lse, B, H, Nq, Nk, d, scale, static_cast<cudaStream_t>(stream),
+                                      g_wait_limit.load(std::memory_order_relaxed));
+    if (rc == ATTN_OK) g_launches.fetch_add(1, std::memory_order_relaxed);
+    return rc;
+  }
   return forward(q, k, v, nullptr, o, lse, B, H, Nq, Nk, d, scale, stream);
 }
 
@@ -1937,7 +1954,9 @@ extern "C" int attn_fwd_status(void* stream) {
   if (cudaMemcpyFromSymbolAsync(&h, g_attn_status, sizeof h, 0, cudaMemcpyDeviceToHost, s) != cudaSuccess)
     return ATTN_ERR_CUDA;
   if (cudaStreamSynchronize(s) != cudaSuccess) return ATTN_ERR_CUDA;
-  if (h == 0) return ATTN_OK;
+  const int wide = attn_wide::take_status(s);   // the d > 128 kernel's own status word
+  if (wide < 0) return ATTN_ERR_CUDA;
+  if (h == 0) return wide ? ATTN_ERR_TIMEOUT : ATTN_OK;
   const unsigned int zero = 0;
   if (cudaMemcpyToSymbolAsync(g_attn_status, &zero, sizeof zero, 0, cudaMemcpyHostToDevice, s) != cudaSuccess ||
       cudaStreamSynchronize(s) != cudaSuccess)

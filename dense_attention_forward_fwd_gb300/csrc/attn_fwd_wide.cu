@@ -1,0 +1,560 @@
+// attn_fwd_wide.cu -- dense BF16 attention forward for head dimensions above 128 (192, 256)
+// on GB300 (sm_103a).
+//
+// The same computation as the d = 128 kernel (O = softmax(scale Q K^T) V with an online
+// softmax, "FlashAttention'ı Anlamak Bölüm 1", section 0.1; head dimensions above 128 are
+// what "Flash Attention на 5090 в CUDA C++" lists next, section "Что дальше"), laid out for
+// the larger d. TMEM holds 512 columns of 128 lanes: two Q tiles' S and O, as in the d = 128
+// kernel, would need 2 x (128 + d) columns, so a block here owns one 128-row Q tile, with
+// S double-buffered (2 x 128 columns) beside O (d columns). The next key tile's scores are
+// computed while the softmax works on this one, and P V of a step (d / 128 times the work
+// at d = 128) overlaps the next softmax: per 128-key step the tensor cores do 2 d / 128
+// times the work of one d = 128 tile step while the softmax's work is unchanged.
+//
+// Shared memory (224 KB at d = 256): Q as d / 64 boxes of 64 columns x 128 rows (16 KB
+// each); one key tile of K in the same boxes, a ring whose box c holds box c of successive
+// key tiles and is freed by a commit after the four K16 steps of Q K^T that read it; V in
+// a ring of three 64-key half tiles, each freed by a commit after the half of P V that
+// read it. Those early releases are what let the next tiles land a whole product ahead of
+// their use: with V as one 128-key tile, V_{j+1} could only be requested once all of
+// P_j V_j was done, and the first half of P_{j+1} waited for it every step.
+//
+// Roles (256 threads): warp 0 lane 0 issues TMA, warp 1 lane 0 issues tcgen05.mma and owns
+// TMEM, warps 4-7 run the softmax and the epilogue with one thread per query row (TMEM lane).
+// Per 128-key step j the MMA thread waits for each 64-key half of P_j and issues its half
+// of O += P_j V_j, then S_{j+2} = Q K_{j+2}^T into the S buffer P_j leaves. The softmax
+// thread that hands a half of P over has first checked that its V half has landed, so the
+// MMA thread waits only for P and for K_{j+2}'s boxes. Whole query tiles per block, no split
+// of the key range.
+//
+// Every wait is bounded (clock64 budget): on expiry the block raises an abort flag, sets
+// the status word and winds down; no trap, no fault.
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <atomic>
+#include <climits>
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include "attn_fwd.h"
+#include "attn_wide.h"
+#include "tc_sm103.cuh"
+
+namespace attn_wide {
+namespace {
+
+using namespace tc;
+
+constexpr int kBM = 128;                  // query rows per tile (= TMEM lanes)
+constexpr int kBN = 128;                  // keys per step
+constexpr int kBoxCols = 64;              // one TMA box: 64 BF16 columns (128 B) x 128 rows
+constexpr int kBoxBytes = kBoxCols * 2 * 128;
+constexpr int kVSlots = 3;                // V ring, in 64-key half tiles
+constexpr int kThreads = 256;
+constexpr float kRescaleLog2 = 32.0f;     // the running maximum moves when a tile's exceeds it by this
+constexpr int kTmemCols = 512;
+constexpr int kMaxChunks = 4;             // d <= 256
+
+// barriers
+constexpr int kBarQFull = 0;
+constexpr int kBarQEmpty = 1;                     // the tile's last Q K^T is done with Q
+constexpr int kBarKFull = 2;                      // [box]
+constexpr int kBarKFree = kBarKFull + kMaxChunks; // [box]: the Q K^T steps that read it are done
+constexpr int kBarVFull = kBarKFree + kMaxChunks; // [half-tile slot]
+constexpr int kBarVFree = kBarVFull + kVSlots;    // [half-tile slot]: its half of P V is done
+constexpr int kBarSFull = kBarVFree + kVSlots;    // [2 buffers]
+constexpr int kBarPFull = kBarSFull + 2;          // [step parity][half], one arrival per softmax warp
+constexpr int kBarOFull = kBarPFull + 4;
+constexpr int kBarOEmpty = kBarOFull + 1;         // the epilogue has read O out of TMEM
+constexpr int kBarDrain = kBarOEmpty + 1;
+constexpr int kNumBars = kBarDrain + 1;
+constexpr int kFlagsBytes = kNumBars * 8 + 8;     // barriers, TMEM slot, abort flag
+
+template <int D>
+struct Layout {
+  static constexpr int kChunks = D / kBoxCols;             // boxes per Q or K tile
+  static constexpr int kTileBytes = kChunks * kBoxBytes;
+  static constexpr int kHalfBytes = kChunks * kBoxBytes / 2;   // V: 64 keys x d
+  static constexpr int kOffQ = 0;
+  static constexpr int kOffK = kOffQ + kTileBytes;
+  static constexpr int kOffV = kOffK + kTileBytes;
+  static constexpr int kOffBar = kOffV + kVSlots * kHalfBytes;
+  static constexpr int kSmem = kOffBar + kFlagsBytes + 1024;   // + realignment of the base to 1024
+  static_assert(D % kBoxCols == 0 && kChunks <= kMaxChunks, "head dimension in whole boxes");
+  static_assert(kSmem <= 232448, "exceeds the 227 KB shared memory of one block");
+  static_assert(2 * kBN + D <= kTmemCols, "two S buffers and O must fit TMEM");
+};
+
+__device__ unsigned int g_wide_status;   // bit 0: a wait timed out
+
+struct Params {
+  uint16_t* o;
+  float* lse;
+  int Nq, Nk;
+  int q_tiles;        // 128-row query tiles per head
+  int n_kv;           // 128-key steps
+  int kv_tail;        // keys in the last step (1 .. 128)
+  int groups;         // B * H * q_tiles
+  float scale_log2;   // scale * log2(e)
+  unsigned long long wait_limit;
+};
+
+struct Ctl {
+  uint32_t bars;
+  volatile uint32_t* abort;
+  unsigned long long limit;
+  __device__ __forceinline__ uint32_t bar(int i) const { return bars + 8u * static_cast<uint32_t>(i); }
+};
+
+// true once the phase with this parity has completed; false on timeout, or (when
+// watch_abort) as soon as another role of the block has given up.
+__device__ __forceinline__ bool wait_phase(const Ctl& c, int idx, uint32_t parity, bool watch_abort) {
+  const uint32_t b = c.bar(idx);
+  if (mbar_try_wait(b, parity)) return true;
+  const long long t0 = clock64();
+  for (;;) {
+    if (mbar_try_wait(b, parity)) return true;
+    if (watch_abort && *c.abort) return false;
+    if (static_cast<unsigned long long>(clock64() - t0) > c.limit) {
+      *c.abort = 1u;
+      atomicOr(&g_wide_status, 1u);
+      return false;
+    }
+  }
+}
+__device__ __forceinline__ bool wait_warp(const Ctl& c, int idx, uint32_t parity) {
+  const bool ok = wait_phase(c, idx, parity, true);
+  return __all_sync(0xffffffffu, ok);
+}
+
+// Global counters (every role keeps them alike): step gs of the block's key stream (all its
+// query tiles' key tiles, in order) uses S buffer gs & 1 and K tile gs (box c in K slot c);
+// its V halves are half tiles 2 gs and 2 gs + 1, in V slots (2 gs + h) % kVSlots. A ring
+// barrier completes once per use of its slot, so the k-th use waits for parity k & 1.
+template <int D, bool kPos>
+__global__ void __launch_bounds__(kThreads, 1)
+    attn_fwd_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                         const __grid_constant__ CUtensorMap tmV, const Params p) {
+  using L = Layout<D>;
+  constexpr int kChunks = L::kChunks;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* smem = smem_raw + (base - raw);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  Ctl c;
+  c.bars = base + L::kOffBar;
+  c.abort = reinterpret_cast<volatile uint32_t*>(smem + L::kOffBar + kNumBars * 8 + 4);
+  c.limit = p.wait_limit;
+  const uint32_t sQ = base + L::kOffQ, sK = base + L::kOffK, sV = base + L::kOffV;
+  auto vslot = [&](int vi) { return sV + static_cast<uint32_t>(vi % kVSlots) * L::kHalfBytes; };
+
+  if (threadIdx.x == 0) {
+    for (int b = 0; b < kNumBars; ++b) mbar_init(c.bar(b), 1);
+    for (int b = 0; b < 4; ++b) mbar_init(c.bar(kBarPFull + b), 4);   // one arrival per softmax warp
+    mbar_init(c.bar(kBarOEmpty), 4);
+    *c.abort = 0u;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(c.bars + kNumBars * 8),
+                 "r"(kTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + L::kOffBar + kNumBars * 8);
+  const int n = p.n_kv;   // steps per query tile (the whole key range)
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // -------- TMA producer: per query tile Q, then K_0, and per step K_{t+1}, V_t --------
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmQ)) : "memory");
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmK)) : "memory");
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmV)) : "memory");
+      int u = 0, gj = 0;           // query tiles started, steps of earlier tiles
+      int k_loads[kMaxChunks] = {0, 0, 0, 0};   // loads requested into each K box
+      int v_halves = 0;                          // V halves requested
+      bool ok = true;
+      auto load_k = [&](int t, int bh) {   // key tile t of this query tile (global step gj + t)
+        const int gt = gj + t;
+        for (int cc = 0; ok && cc < kChunks; ++cc) {
+          if (gt > 0 && !wait_phase(c, kBarKFree + cc, static_cast<uint32_t>(gt - 1) & 1u, true)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(c.bar(kBarKFull + cc), kBoxBytes);
+          tma_load_3d(sK + cc * kBoxBytes, &tmK, c.bar(kBarKFull + cc), cc * kBoxCols, t * kBN, bh);
+          k_loads[cc] = gt + 1;
+        }
+      };
+      auto load_v = [&](int t, int bh) {   // both 64-key halves of V_t
+        for (int h = 0; ok && h < 2; ++h) {
+          const int vi = 2 * (gj + t) + h, slot = vi % kVSlots;
+          if (vi >= kVSlots && !wait_phase(c, kBarVFree + slot, static_cast<uint32_t>(vi / kVSlots - 1) & 1u, true)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(c.bar(kBarVFull + slot), L::kHalfBytes);
+          for (int cc = 0; cc < kChunks; ++cc)
+            tma_load_3d(vslot(vi) + cc * (kBoxBytes / 2), &tmV, c.bar(kBarVFull + slot), cc * kBoxCols,
+                        t * kBN + h * (kBN / 2), bh);
+          v_halves = vi + 1;
+        }
+      };
+      for (int g = blockIdx.x; ok && g < p.groups; g += gridDim.x) {
+        const int bh = g / p.q_tiles, qt = g % p.q_tiles;
+        if (u > 0 && !wait_phase(c, kBarQEmpty, (u - 1) & 1, true)) break;
+        mbar_arrive_expect_tx(c.bar(kBarQFull), L::kTileBytes);
+        for (int cc = 0; cc < kChunks; ++cc)
+          tma_load_3d(sQ + cc * kBoxBytes, &tmQ, c.bar(kBarQFull), cc * kBoxCols, qt * kBM, bh);
+        ++u;
+        load_k(0, bh);
+        for (int t = 0; ok && t < n; ++t) {
+          if (t + 1 < n) load_k(t + 1, bh);
+          load_v(t, bh);
+        }
+        gj += n;
+      }
+      // no copy into shared memory may be in flight when the block exits
+      if (u > 0) wait_phase(c, kBarQFull, (u - 1) & 1, false);
+      for (int cc = 0; cc < kChunks; ++cc)
+        if (k_loads[cc] > 0) wait_phase(c, kBarKFull + cc, static_cast<uint32_t>(k_loads[cc] - 1) & 1u, false);
+      for (int vi = v_halves > kVSlots ? v_halves - kVSlots : 0; vi < v_halves; ++vi)
+        wait_phase(c, kBarVFull + vi % kVSlots, static_cast<uint32_t>(vi / kVSlots) & 1u, false);
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // -------- MMA issuer --------
+      const uint32_t tS[2] = {tmem, tmem + kBN};
+      const uint32_t tO = tmem + 2 * kBN;
+      constexpr uint32_t kIdQK = idesc_bf16(kBM, kBN, false);
+      constexpr uint32_t kIdPV = idesc_bf16(kBM, D, true);
+      bool ok = true;
+      // S = Q K^T for the key tile of global step gt, box by box; each box is released as
+      // soon as the four K16 steps that read it are done
+      auto qk = [&](uint32_t d_tmem, int gt) {
+        for (int cc = 0; cc < kChunks; ++cc) {
+          if (!wait_phase(c, kBarKFull + cc, static_cast<uint32_t>(gt) & 1u, true)) {
+            ok = false;
+            return;
+          }
+          tc_fence_after();
+#pragma unroll
+          for (int k4 = 0; k4 < 4; ++k4) {
+            const uint32_t off = static_cast<uint32_t>(cc * kBoxBytes + k4 * 32);
+            mma_ss(d_tmem, sdesc_sw128(sQ + off, 16, 1024), sdesc_sw128(sK + off, 16, 1024), kIdQK, cc > 0 || k4 > 0);
+          }
+          tc_commit(c.bar(kBarKFree + cc));
+        }
+      };
+      int u = 0, gj = 0;
+      for (int g = blockIdx.x; ok && g < p.groups; g += gridDim.x) {
+        if (!wait_phase(c, kBarQFull, u & 1, true)) break;
+        tc_fence_after();
+        // the first two key tiles' scores; later ones follow each step's P V
+        for (int t = 0; ok && t < 2 && t < n; ++t) {
+          qk(tS[(gj + t) & 1], gj + t);
+          tc_commit(c.bar(kBarSFull + ((gj + t) & 1)));
+        }
+        if (!ok) break;
+        if (n <= 2) tc_commit(c.bar(kBarQEmpty));
+        // the first P V overwrites O: the previous tile's epilogue must have read it
+        if (u > 0 && !wait_phase(c, kBarOEmpty, (u - 1) & 1, true)) break;
+        for (int j = 0; ok && j < n; ++j) {
+          const int gs = gj + j, buf = gs & 1;
+          const uint32_t ph = static_cast<uint32_t>(gs >> 1) & 1u;
+          for (int h = 0; h < 2; ++h) {   // keys 64h .. 64h + 63: P columns 32h .., V half 2 gs + h
+            if (!wait_phase(c, kBarPFull + 2 * (gs & 1) + h, ph, true)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const int vi = 2 * gs + h;
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)   // 16 keys per MMA: 8 columns of packed P
+              mma_ts(tO, tS[buf] + (4 * h + kk) * 8, sdesc_sw128(vslot(vi) + kk * 16 * 128, kBoxBytes / 2, 1024),
+                     kIdPV, j > 0 || h > 0 || kk > 0);
+            tc_commit(c.bar(kBarVFree + vi % kVSlots));
+          }
+          if (!ok) break;
+          if (j + 2 < n) {
+            qk(tS[buf], gs + 2);
+            if (!ok) break;
+            tc_commit(c.bar(kBarSFull + buf));
+            if (j + 2 == n - 1) tc_commit(c.bar(kBarQEmpty));
+          }
+        }
+        if (!ok) break;
+        tc_commit(c.bar(kBarOFull));
+        gj += n;
+        ++u;
+      }
+      // every MMA this thread issued must finish before TMEM and shared memory are released
+      tc_commit(c.bar(kBarDrain));
+      wait_phase(c, kBarDrain, 0, false);
+    }
+    __syncwarp();
+  } else if (warp >= 4) {
+    // -------- softmax and epilogue: thread = query row --------
+    const int quarter = warp & 3;
+    const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+    const uint32_t tS[2] = {tmem + lane_off, tmem + lane_off + kBN};
+    const uint32_t tO = tmem + lane_off + 2 * kBN;
+    const float cs = kPos ? p.scale_log2 : 1.0f;
+    const bool ringer = warp == 4 && lane == 0;
+    int u = 0, gj = 0;
+    for (int g = blockIdx.x; g < p.groups; g += gridDim.x) {
+      const int bh = g / p.q_tiles, qt = g % p.q_tiles;
+      float m_used = -INFINITY, l = 0.0f, corr = 0.0f;
+      bool ok = true;
+      for (int j = 0; j < n; ++j) {
+        const int gs = gj + j, buf = gs & 1;
+        if (!wait_warp(c, kBarSFull + buf, static_cast<uint32_t>(gs >> 1) & 1u)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        float s[128];
+        {
+          uint32_t x[128];
+          tmem_ld<128>(tS[buf], x);
+#pragma unroll
+          for (int i = 0; i < 128; ++i) s[i] = kPos ? __uint_as_float(x[i]) : __uint_as_float(x[i]) * p.scale_log2;
+        }
+        if (j == n - 1 && p.kv_tail < kBN) {
+          const int valid = p.kv_tail;
+#pragma unroll
+          for (int i = 0; i < 128; ++i) s[i] = i < valid ? s[i] : -INFINITY;
+        }
+        // row max: eight independent three-input max chains
+        float mx[8];
+#pragma unroll
+        for (int t = 0; t < 8; ++t) mx[t] = fmaxf(s[t], s[t + 8]);
+#pragma unroll
+        for (int i = 16; i < 128; i += 16) {
+#pragma unroll
+          for (int t = 0; t < 8; ++t) mx[t] = max3(mx[t], s[i + t], s[i + 8 + t]);
+        }
+        const float m_raw =
+            fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])), fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+        const float m_tile = m_raw * cs;
+        bool rescale = false;
+        float alpha = 1.0f;
+        if (m_tile > m_used + kRescaleLog2) {
+          alpha = ex2(m_used - m_tile);   // 0 on a tile's first step
+          l *= alpha;
+          corr *= alpha;
+          m_used = m_tile;
+          rescale = j > 0;
+        }
+        if (__any_sync(0xffffffffu, rescale)) {
+          // O must hold the previous step's P V before it is rescaled (S_j's product was
+          // issued before that one), and be rescaled before this step's accumulates: wait
+          // for the commit of the previous step's second half (V half 2 gs - 1)
+          const int vi = 2 * gs - 1;
+          if (!wait_warp(c, kBarVFree + vi % kVSlots, static_cast<uint32_t>(vi / kVSlots) & 1u)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const float a = rescale ? alpha : 1.0f;
+#pragma unroll 1
+          for (int ch = 0; ch < D / 8; ++ch) {
+            uint32_t ov[8];
+            tmem_ld<8>(tO + ch * 8, ov);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * a);
+            tmem_st<8>(tO + ch * 8, ov);
+          }
+        }
+        const float neg_m = -m_used;
+        {
+          // the BF16 rounding error of the tile's largest weight, with the arithmetic that
+          // forms it below: l + corr is then the sum of the weights the tensor cores apply
+          const float pm = ex2(fmaf(m_raw, cs, neg_m));
+          corr += __uint_as_float(pack_bf16(pm, 0.0f) << 16) - pm;
+        }
+        float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        const float2 cs2 = make_float2(cs, cs), nm2 = make_float2(neg_m, neg_m);
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          uint32_t pk[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const int e = half * 64 + 2 * i;
+            const float2 a2 = ffma2(make_float2(s[e], s[e + 1]), cs2, nm2);
+            const float e0 = ex2(a2.x), e1 = ex2(a2.y);
+            pk[i] = pack_bf16(e0, e1);
+            const float2 t2 = fadd2(make_float2(acc[2 * (i & 3)], acc[2 * (i & 3) + 1]), make_float2(e0, e1));
+            acc[2 * (i & 3)] = t2.x;
+            acc[2 * (i & 3) + 1] = t2.y;
+          }
+          tmem_st<32>(tS[buf] + half * 32, pk);
+          tc_fence_before();
+          __syncwarp();
+          // the MMAs this hand-over releases read this half's V
+          bool landed = true;
+          if (ringer) {
+            const int vi = 2 * gs + half;
+            landed = wait_phase(c, kBarVFull + vi % kVSlots, static_cast<uint32_t>(vi / kVSlots) & 1u, true);
+          }
+          if (!__shfl_sync(0xffffffffu, landed, 0)) {
+            ok = false;
+            break;
+          }
+          if (lane == 0) mbar_arrive(c.bar(kBarPFull + 2 * (gs & 1) + half));
+          __syncwarp();
+        }
+        if (!ok) break;
+        l += ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
+      }
+      if (!ok || !wait_warp(c, kBarOFull, static_cast<uint32_t>(u) & 1u)) break;
+      tc_fence_after();
+      // epilogue: O / (l + corr) as BF16, each thread its own row; the natural-log LSE
+      const int row = qt * kBM + quarter * 32 + lane;
+      const bool live = row < p.Nq;
+      const float inv_l = 1.0f / (l + corr);
+      uint4* orow = reinterpret_cast<uint4*>(p.o + (static_cast<size_t>(bh) * p.Nq + (live ? row : 0)) * D);
+#pragma unroll 1
+      for (int ch = 0; ch < D / 32; ++ch) {
+        uint32_t x[32];
+        tmem_ld<32>(tO + ch * 32, x);
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          pk[i] = pack_bf16(__uint_as_float(x[2 * i]) * inv_l, __uint_as_float(x[2 * i + 1]) * inv_l);
+        if (live) {
+#pragma unroll
+          for (int v4 = 0; v4 < 4; ++v4)
+            orow[ch * 4 + v4] = make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2], pk[4 * v4 + 3]);
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(c.bar(kBarOEmpty));
+      __syncwarp();
+      if (live) p.lse[static_cast<size_t>(bh) * p.Nq + row] = (m_used + log2f(l)) * 0.69314718055994531f;
+      gj += n;
+      ++u;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
+  }
+}
+
+// ---------------------------------------------------------------------------------
+// Host side
+// ---------------------------------------------------------------------------------
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+PFN_cuTensorMapEncodeTiled_v12000 encoder() {
+  std::call_once(g_encode_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  return g_encode;
+}
+
+// [BH, rows, d] BF16 as a 3-D tensor (d innermost); box = 64 columns x box_rows rows x 1.
+bool make_map(CUtensorMap* map, const void* ptr, int rows, long long bh, int d, int box_rows) {
+  auto enc = encoder();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(bh)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2, static_cast<cuuint64_t>(rows) * d * 2};
+  cuuint32_t box[3] = {kBoxCols, static_cast<cuuint32_t>(box_rows), 1};
+  cuuint32_t elem[3] = {1, 1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, elem,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+constexpr int kMaxDevices = 64;
+std::atomic<int> g_attr_done[4][kMaxDevices];   // per instantiation (d, sign of the scale) and device
+
+template <int D, bool kPos>
+int launch(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, const Params& p, int grid, int dev,
+           cudaStream_t stream) {
+  auto kern = attn_fwd_wide_kernel<D, kPos>;
+  constexpr int kInst = (D == 256 ? 2 : 0) + (kPos ? 1 : 0);
+  if (dev < 0 || dev >= kMaxDevices || !g_attr_done[kInst][dev].load(std::memory_order_acquire)) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Layout<D>::kSmem) != cudaSuccess)
+      return ATTN_ERR_CUDA;
+    if (dev >= 0 && dev < kMaxDevices) g_attr_done[kInst][dev].store(1, std::memory_order_release);
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = Layout<D>::kSmem;
+  cfg.stream = stream;
+  return cudaLaunchKernelEx(&cfg, kern, mq, mk, mv, p) == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+}  // namespace
+
+int forward(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Nq, int Nk, int d,
+            float scale, cudaStream_t stream, unsigned long long wait_limit) {
+  if (!supported(d)) return ATTN_ERR_UNSUPPORTED;
+  const long long bh = static_cast<long long>(B) * H;
+  const long long q_tiles = (static_cast<long long>(Nq) + kBM - 1) / kBM;
+  if (bh > INT_MAX || bh * q_tiles > INT_MAX) return ATTN_ERR_UNSUPPORTED;
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
+    return ATTN_ERR_CUDA;
+  CUtensorMap mq, mk, mv;
+  if (!make_map(&mq, q, Nq, bh, d, kBM) || !make_map(&mk, k, Nk, bh, d, kBN) ||
+      !make_map(&mv, v, Nk, bh, d, kBN / 2))
+    return ATTN_ERR_CUDA;
+  Params p;
+  p.o = static_cast<uint16_t*>(o);
+  p.lse = lse;
+  p.Nq = Nq;
+  p.Nk = Nk;
+  p.q_tiles = static_cast<int>(q_tiles);
+  p.n_kv = (Nk + kBN - 1) / kBN;
+  p.kv_tail = Nk - (p.n_kv - 1) * kBN;
+  p.groups = static_cast<int>(bh * q_tiles);
+  p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+  p.wait_limit = wait_limit;
+  const int grid = std::min(sms, p.groups);
+  if (d == 256)
+    return scale > 0.0f ? launch<256, true>(mq, mk, mv, p, grid, dev, stream)
+                        : launch<256, false>(mq, mk, mv, p, grid, dev, stream);
+  return scale > 0.0f ? launch<192, true>(mq, mk, mv, p, grid, dev, stream)
+                      : launch<192, false>(mq, mk, mv, p, grid, dev, stream);
+}
+
+int take_status(cudaStream_t stream) {
+  unsigned int h = 0;
+  if (cudaMemcpyFromSymbolAsync(&h, g_wide_status, sizeof h, 0, cudaMemcpyDeviceToHost, stream) != cudaSuccess ||
+      cudaStreamSynchronize(stream) != cudaSuccess)
+    return -1;
+  if (h == 0) return 0;
+  const unsigned int zero = 0;
+  if (cudaMemcpyToSymbolAsync(g_wide_status, &zero, sizeof zero, 0, cudaMemcpyHostToDevice, stream) != cudaSuccess ||
+      cudaStreamSynchronize(stream) != cudaSuccess)
+    return -1;
+  return 1;
+}
+
+}  // namespace attn_wide

@@ -20,7 +20,8 @@
  *
  * Conventions shared by every entry point below:
  *   - Tensors are dense, C-ordered, [B, H, N, d] (batch, heads, sequence, head dim)
- *     with d = 128, in device memory reachable from the current CUDA device.
+ *     with d = 128 (attn_fwd also takes 192 and 256), in device memory reachable from
+ *     the current CUDA device.
  *   - BF16 is IEEE-style bfloat16 (1 sign, 8 exponent, 7 mantissa bits), passed as
  *     raw 16-bit storage (void*).
  *   - The caller owns every buffer it passes; the library keeps no pointer to them
@@ -45,7 +46,7 @@ extern "C" {
 /* Status codes. */
 #define ATTN_OK               0
 #define ATTN_ERR_INVALID_ARG (-1) /* null pointer, negative size, Nk == 0 with rows to compute, non-finite scale, size overflow */
-#define ATTN_ERR_UNSUPPORTED (-2) /* d != 128, or sizes beyond the kernel's index range */
+#define ATTN_ERR_UNSUPPORTED (-2) /* a head dimension the entry point does not take, or sizes beyond the kernel's index range */
 #define ATTN_ERR_MISALIGNED  (-3) /* q, k, v or o not 16-byte aligned, or lse not 4-byte aligned */
 #define ATTN_ERR_CUDA        (-4) /* a CUDA runtime or driver call failed (no device, launch failure, ...) */
 #define ATTN_ERR_TIMEOUT     (-5) /* a kernel gave up a pipeline wait after its time limit (see attn_fwd_status) */
@@ -63,7 +64,10 @@ extern "C" {
  *        written and ATTN_OK is returned. Otherwise Nk must be >= 1. Any Nq and Nk
  *        are accepted; a sequence that is not a multiple of 128 ends in a partial
  *        tile that the kernel masks.
- *   d    head dimension; must be 128.
+ *   d    head dimension: 128, 192 or 256. Head dimensions above 128 ("Flash Attention на
+ *        5090 в CUDA C++", section "Что дальше") run a kernel that gives each thread block
+ *        one 128-row query tile (TMEM holds its S twice and its O) and whole key ranges,
+ *        so they need no workspace.
  *   scale  any finite float, applied to the scores (1/sqrt(d) for standard attention).
  *   stream a cudaStream_t, or NULL.
  *

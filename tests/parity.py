@@ -111,10 +111,9 @@ def run_gpu(attn, q, k, v, scale: float, causal: bool = False, bias=None):
 
 
 def check_case(attn, B, H, Nq, Nk, seed=0, qk_mult=1.0, scale=None, rows=None, ulp_aware=False, qkv=None,
-               causal=False, bias=None):
+               causal=False, bias=None, d=128):
     """Full or row-sampled parity of one seeded case (causal: under the causal mask; bias: with
-    that additive bias); returns the Report."""
-    d = 128
+    that additive bias; d: the head dimension); returns the Report."""
     scale = float(np.float32(1 / np.sqrt(d))) if scale is None else scale
     q, k, v = qkv if qkv is not None else make_qkv(B, H, Nq, Nk, d=d, seed=seed, qk_mult=qk_mult)
     o_gpu, lse_gpu = run_gpu(attn, q, k, v, scale, causal, bias)
@@ -125,7 +124,7 @@ def check_case(attn, B, H, Nq, Nk, seed=0, qk_mult=1.0, scale=None, rows=None, u
     o_flat, l_flat = o_gpu.reshape(-1, d), lse_gpu.reshape(-1)
     if rows is not None:
         o_flat, l_flat = o_flat[rows], l_flat[rows]
-    if ulp_aware and not causal and bias is None:
+    if ulp_aware and not causal and bias is None and d == 128:
         # the same computation before the output's rounding: the literal bound, and the
         # BF16 output is exactly that FP32 output rounded
         o32, l32 = run_gpu_o32(attn, q, k, v, scale)

@@ -84,7 +84,16 @@ def test_o32_rejects_like_attn_fwd(kw, code):
     (dict(scale=math.inf), attn.ATTN_ERR_INVALID_ARG),
     (dict(scale=math.nan), attn.ATTN_ERR_INVALID_ARG),
     (dict(d=64), attn.ATTN_ERR_UNSUPPORTED),
-    (dict(d=256), attn.ATTN_ERR_UNSUPPORTED),
+    (dict(d=160), attn.ATTN_ERR_UNSUPPORTED),
+    (dict(d=320), attn.ATTN_ERR_UNSUPPORTED),
+    # head dimensions above 128 (the one-Q-tile kernel): the same checks, before any CUDA call
+    (dict(d=256, q=None), attn.ATTN_ERR_INVALID_ARG),
+    (dict(d=192, Nk=0), attn.ATTN_ERR_INVALID_ARG),
+    (dict(d=256, scale=math.nan), attn.ATTN_ERR_INVALID_ARG),
+    (dict(d=256, k=A + 8), attn.ATTN_ERR_MISALIGNED),
+    (dict(d=192, lse=A + 2), attn.ATTN_ERR_MISALIGNED),
+    (dict(d=256, B=1 << 16, H=1 << 16), attn.ATTN_ERR_UNSUPPORTED),
+    (dict(d=256, B=0, q=None, o=None), attn.ATTN_OK),
     (dict(q=A + 8), attn.ATTN_ERR_MISALIGNED),
     (dict(v=A + 2), attn.ATTN_ERR_MISALIGNED),
     (dict(o=A + 4), attn.ATTN_ERR_MISALIGNED),
