@@ -90,7 +90,13 @@ def parse():
                     help="time attn_fwd_fp8 (Q, K and V as FP8 E4M3 codes, P rounded to E4M3 for P V)")
     ap.add_argument("--mxfp8", action="store_true",
                     help="time attn_fwd_mxfp8 (Q, K and V in MXFP8, both products block-scaled)")
+    ap.add_argument("--head-dim", type=int, choices=[128, 192, 256], default=128,
+                    help="head dimension d of the workload's tensors (192 and 256: attn_fwd's one-Q-tile "
+                         "kernel; scale 1/sqrt(d))")
     args = ap.parse_args()
+    if args.head_dim != 128 and (args.causal or args.backward or args.bias != "none" or args.fp8_qk or args.fp8
+                                 or args.mxfp8):
+        ap.error("--head-dim 192 / 256 is attn_fwd's (dense, non-causal, BF16); use it alone")
     if (args.fp8_qk or args.fp8 or args.mxfp8) and (args.causal or args.backward or args.bias != "none"):
         ap.error("--fp8-qk, --fp8 and --mxfp8 have no causal, bias or backward entry point; use them alone")
     if args.fp8_qk + args.fp8 + args.mxfp8 > 1:
@@ -134,10 +140,13 @@ def job_tflops(flops_per_rank: float, world: int, ms: float) -> float:
     return flops_per_rank * world / (ms * 1e-3) / 1e12
 
 
-def kernel_hash(backward: bool = False) -> str:
+def kernel_hash(backward: bool = False, wide: bool = False) -> str:
     h = hashlib.sha256()
-    files = ((KERNEL_SRC.replace("attn_fwd.cu", "attn_bwd.cu"), os.path.join(ROOT, "include", "attn_bwd.h"))
-             if backward else (KERNEL_SRC, os.path.join(ROOT, "include", "attn_fwd.h")))
+    csrc = os.path.dirname(KERNEL_SRC)
+    files = ((os.path.join(csrc, "attn_bwd.cu"), os.path.join(ROOT, "include", "attn_bwd.h")) if backward else
+             (os.path.join(csrc, "attn_fwd_wide.cu"), os.path.join(csrc, "tc_sm103.cuh"),
+              os.path.join(ROOT, "include", "attn_fwd.h")) if wide else
+             (KERNEL_SRC, os.path.join(ROOT, "include", "attn_fwd.h")))
     for f in files:
         h.update(open(f, "rb").read())
     return h.hexdigest()[:16]
@@ -171,7 +180,8 @@ def traffic_key(w, args) -> str:
     """The profiles/traffic.json key of this run's kernel and workload."""
     return (w.name + ("-causal" if args.causal else "") + ("" if args.bias == "none" else "-bias-" + args.bias)
             + ("-backward" if args.backward else "") + ("-fp8qk" if args.fp8_qk else "")
-            + ("-fp8" if args.fp8 else "") + ("-mxfp8" if args.mxfp8 else ""))
+            + ("-fp8" if args.fp8 else "") + ("-mxfp8" if args.mxfp8 else "")
+            + ("" if w.d == 128 else f"-d{w.d}"))
 
 
 def host_cores() -> int:
@@ -597,7 +607,7 @@ def run_ours(args, w):
     if os.path.exists(TRAFFIC_FILE):
         key = traffic_key(w, args)
         rec = json.load(open(TRAFFIC_FILE)).get(key)
-        if rec and rec.get("kernel_hash") == kernel_hash(args.backward):
+        if rec and rec.get("kernel_hash") == kernel_hash(args.backward, w.d != 128):
             traffic = rec.get("bytes_per_launch")
 
     line = {
@@ -639,6 +649,9 @@ def run_ours(args, w):
 def main():
     args = parse()
     w = by_name(args.workload)
+    if args.head_dim != w.d:
+        import dataclasses
+        w = dataclasses.replace(w, d=args.head_dim)
     if args.impl == "reference":
         return run_reference(args, w)
     return run_ours(args, w)

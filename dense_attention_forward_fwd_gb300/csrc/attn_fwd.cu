@@ -76,6 +76,7 @@
 
 #include "attn_fwd.h"
 #include "attn_wide.h"
+#include "tc_sm103.cuh"
 
 namespace {
 
@@ -275,80 +276,34 @@ __device__ __forceinline__ int sk_block_of(long long x, long long sk_steps, int 
 __device__ unsigned int g_attn_status;   // per device; bit 0 = a wait timed out
 
 // ---------------------------------------------------------------------------------
-// PTX wrappers
+// PTX wrappers. The ones every kernel of the library uses (mbarrier, TMA tile loads,
+// tcgen05.mma / commit / fences, ex2, max3, BF16 packing, the shared-memory descriptor)
+// are in tc_sm103.cuh; this file's own follow.
 // ---------------------------------------------------------------------------------
-__device__ __forceinline__ uint32_t smem_u32(const void* p) {
-  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
+using tc::ex2;
+using tc::max3;
+using tc::mbar_arrive;
+using tc::mbar_arrive_expect_tx;
+using tc::mbar_init;
+using tc::mbar_test_wait;
+using tc::mbar_try_wait;
+using tc::mma_ss;
+using tc::mma_ts;
+using tc::pack_bf16;
+using tc::sdesc_sw128;
+using tc::smem_u32;
+using tc::tc_commit;
+using tc::tc_fence_after;
+using tc::tc_fence_before;
+using tc::tma_load_3d;
 
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-}
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
-}
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-
-// non-blocking: has the phase with this parity completed?
-__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-
-__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
-                                            int x, int y, int z) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "r"(z)
-      : "memory");
-}
 
 __device__ __forceinline__ unsigned int ld_acquire(const unsigned int* ptr) {
   unsigned int v;
   asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(ptr) : "memory");
   return v;
 }
-__device__ __forceinline__ void tc_fence_before() {
-  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-}
-__device__ __forceinline__ void tc_fence_after() {
-  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-}
-__device__ __forceinline__ void tc_commit(uint32_t bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
-               : "memory");
-}
 
-// D(tmem) (+)= A(smem desc) * B(smem desc)
-__device__ __forceinline__ void mma_ss(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, bool acc) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
-      "l"(a), "l"(b), "r"(idesc), "r"(static_cast<uint32_t>(acc))
-      : "memory");
-}
 // D(tmem) (+)= A(smem desc) * B(smem desc), 8-bit floating-point operands
 __device__ __forceinline__ void mma_ss_f8(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, bool acc) {
   asm volatile(
@@ -364,15 +319,6 @@ __device__ __forceinline__ void mma_ts_f8(uint32_t d, uint32_t a, uint64_t b, ui
       "{\n\t.reg .pred p;\n\t"
       "setp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d),
-      "r"(a), "l"(b), "r"(idesc), "r"(static_cast<uint32_t>(acc))
-      : "memory");
-}
-// D(tmem) (+)= A(tmem) * B(smem desc)
-__device__ __forceinline__ void mma_ts(uint32_t d, uint32_t a, uint64_t b, uint32_t idesc, bool acc) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d),
       "r"(a), "l"(b), "r"(idesc), "r"(static_cast<uint32_t>(acc))
       : "memory");
 }
@@ -468,16 +414,6 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&x)[32
       : "memory");
 }
 
-__device__ __forceinline__ float ex2(float x) {
-  float y;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
-__device__ __forceinline__ float max3(float a, float b, float c) {
-  float y;
-  asm("max.f32 %0, %1, %2, %3;" : "=f"(y) : "f"(a), "f"(b), "f"(c));
-  return y;
-}
 // (y0, y1) = (x0 * a + b, x1 * a + b) as one packed FP32x2 FMA
 __device__ __forceinline__ void fma2(float& y0, float& y1, float x0, float x1, float a, float b) {
   asm("{\n\t.reg .b64 x, a, b, y;\n\t"
@@ -605,12 +541,6 @@ __device__ __forceinline__ void add2(float& a0, float& a1, float x0, float x1) {
       : "+f"(a0), "+f"(a1)
       : "f"(x0), "f"(x1));
 }
-// two floats -> packed BF16x2 (round to nearest even), lo in the low half
-__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
-  uint32_t r;
-  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
-  return r;
-}
 // Four values rounded to E4M3 (nearest even, saturating), the first in the lowest byte.
 // As with the BF16 pair, cvt puts its first source in the upper half of the result.
 __device__ __forceinline__ uint32_t pack_e4m3x4(float a0, float a1, float a2, float a3) {
@@ -631,16 +561,9 @@ __device__ __forceinline__ float round_e4m3(float x) {
 }
 
 // ---------------------------------------------------------------------------------
-// Descriptors (tcgen05 shared-memory matrix descriptor and kind::f16 instruction
-// descriptor, field layouts per the PTX ISA)
+// Instruction descriptors (kind::f16, kind::f8f6f4, kind::mxf8f6f4; field layouts per the
+// PTX ISA)
 // ---------------------------------------------------------------------------------
-// 128B-swizzled operand: start address, leading/stride byte offsets, descriptor
-// version 1 (bits 46-48), swizzle mode 2 = 128B (bits 61-63).
-__device__ __forceinline__ uint64_t sdesc_sw128(uint32_t addr, uint32_t lbo, uint32_t sbo) {
-  return static_cast<uint64_t>((addr >> 4) & 0x3FFFu) |
-         (static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16) |
-         (static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
-}
 // BF16 x BF16 -> FP32, M = 128, N = 128, A K-major, B K-major (S = Q K^T) or
 // MN-major (O += P V, V stored key-major with d contiguous).
 __host__ __device__ constexpr uint32_t idesc_bf16(bool b_mn_major) {

@@ -2,6 +2,7 @@
 the host cores) prints one JSON line with every key of the contract for each variant, the
 flags that have no entry point together are refused, and the roofline arithmetic and
 traffic keys are the documented ones."""
+import dataclasses
 import json
 import os
 import subprocess
@@ -73,8 +74,12 @@ def test_traffic_keys_match_the_recorded_ones():
              "rect-4k-8k-mxfp8": ("rect-4k-8k", {"mxfp8": True}), "rect-4k-8k-fp8qk": ("rect-4k-8k", {"fp8_qk": True}),
              "rect-4k-8k-fp8": ("rect-4k-8k", {"fp8": True}), "square-4k-causal": ("square-4k", {"causal": True}),
              "rect-4k-8k-bias-shared": ("rect-4k-8k", {"bias": "shared"}),
-             "square-4k-backward": ("square-4k", {"backward": True})}
+             "square-4k-backward": ("square-4k", {"backward": True}),
+             "square-4k-d256": ("square-4k", {"d": 256})}
     recorded = json.load(open(os.path.join(ROOT, "profiles", "traffic.json")))
     assert set(recorded) <= set(cases)
     for key, (name, over) in cases.items():
-        assert bench.traffic_key(by_name(name), SimpleNamespace(**dict(base, **over))) == key
+        w = by_name(name)
+        if "d" in over:
+            w = dataclasses.replace(w, d=over.pop("d"))
+        assert bench.traffic_key(w, SimpleNamespace(**dict(base, **over))) == key

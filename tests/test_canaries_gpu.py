@@ -54,6 +54,16 @@ def test_forward_entry_points(gpu_lib, B, H, Nq, Nk):
         check(gpu_lib, ((fo, o), "bf16"), ((fl, lse), "f32"))
 
 
+@pytest.mark.parametrize("d", [192, 256])
+@pytest.mark.parametrize("B,H,Nq,Nk", SHAPES)
+def test_forward_wide_head_dims(gpu_lib, d, B, H, Nq, Nk):
+    # attn_fwd at d > 128 (the one-Q-tile kernel): each thread stores its own row of O
+    q, k, v = (to_device(a) for a in make_qkv(B, H, Nq, Nk, d=d, seed=17300 + Nq + Nk + d))
+    (fo, o), (fl, lse) = guarded((B, H, Nq, d), "bf16", "cuda"), guarded((B, H, Nq), "f32", "cuda")
+    gpu_lib.attn_fwd(q, k, v, o, lse, B, H, Nq, Nk, d, d ** -0.5)
+    check(gpu_lib, ((fo, o), "bf16"), ((fl, lse), "f32"))
+
+
 @pytest.mark.parametrize("B,H,Nq,Nk", SHAPES)
 def test_fp8_entry_points(gpu_lib, B, H, Nq, Nk):
     import torch
