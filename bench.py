@@ -91,12 +91,11 @@ def parse():
     ap.add_argument("--mxfp8", action="store_true",
                     help="time attn_fwd_mxfp8 (Q, K and V in MXFP8, both products block-scaled)")
     ap.add_argument("--head-dim", type=int, choices=[128, 192, 256], default=128,
-                    help="head dimension d of the workload's tensors (192 and 256: attn_fwd's one-Q-tile "
-                         "kernel; scale 1/sqrt(d))")
+                    help="head dimension d of the workload's tensors (192 and 256: the one-Q-tile kernel "
+                         "of attn_fwd and attn_fwd_causal; scale 1/sqrt(d))")
     args = ap.parse_args()
-    if args.head_dim != 128 and (args.causal or args.backward or args.bias != "none" or args.fp8_qk or args.fp8
-                                 or args.mxfp8):
-        ap.error("--head-dim 192 / 256 is attn_fwd's (dense, non-causal, BF16); use it alone")
+    if args.head_dim != 128 and (args.backward or args.bias != "none" or args.fp8_qk or args.fp8 or args.mxfp8):
+        ap.error("--head-dim 192 / 256 has the BF16 forward entry points only (attn_fwd, attn_fwd_causal)")
     if (args.fp8_qk or args.fp8 or args.mxfp8) and (args.causal or args.backward or args.bias != "none"):
         ap.error("--fp8-qk, --fp8 and --mxfp8 have no causal, bias or backward entry point; use them alone")
     if args.fp8_qk + args.fp8 + args.mxfp8 > 1:

@@ -1742,24 +1742,31 @@ int forward(const void* q, const void* k, const void* v, const BiasArg* bias, vo
 
 }  // namespace
 
+namespace {
+// Head dimensions above 128: the one-Q-tile kernel (attn_fwd_wide.cu), after the argument
+// checks of the d = 128 entry points (causal: also Nq <= Nk).
+int forward_wide(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Nq, int Nk,
+                 int d, float scale, bool causal, void* stream) {
+  if (B < 0 || H < 0 || Nq < 0 || Nk < 0 || !std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
+  if (static_cast<long long>(B) * H == 0 || Nq == 0) return ATTN_OK;
+  if (Nk == 0 || (causal && Nq > Nk) || !q || !k || !v || !o || !lse) return ATTN_ERR_INVALID_ARG;
+  if (causal && Nk > INT_MAX - 1024) return ATTN_ERR_UNSUPPORTED;   // row + causal_off + 2 * 128 stays in int
+  if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) | reinterpret_cast<uintptr_t>(v) |
+       reinterpret_cast<uintptr_t>(o)) & 15u)
+    return ATTN_ERR_MISALIGNED;
+  if (reinterpret_cast<uintptr_t>(lse) & 3u) return ATTN_ERR_MISALIGNED;
+  const long long max_rows = static_cast<long long>(Nq > Nk ? Nq : Nk);
+  if (static_cast<long long>(B) * H > (LLONG_MAX / (2 * d)) / max_rows) return ATTN_ERR_INVALID_ARG;
+  const int rc = attn_wide::forward(q, k, v, o, lse, B, H, Nq, Nk, d, scale, causal, static_cast<cudaStream_t>(stream),
+                                    g_wait_limit.load(std::memory_order_relaxed));
+  if (rc == ATTN_OK) g_launches.fetch_add(1, std::memory_order_relaxed);
+  return rc;
+}
+}  // namespace
+
 extern "C" int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Nq,
                         int Nk, int d, float scale, void* stream) {
-  if (attn_wide::supported(d)) {
-    // head dimensions above 128: the one-Q-tile kernel (attn_fwd_wide.cu); the same checks
-    if (B < 0 || H < 0 || Nq < 0 || Nk < 0 || !std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
-    if (static_cast<long long>(B) * H == 0 || Nq == 0) return ATTN_OK;
-    if (Nk == 0 || !q || !k || !v || !o || !lse) return ATTN_ERR_INVALID_ARG;
-    if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) | reinterpret_cast<uintptr_t>(v) |
-         reinterpret_cast<uintptr_t>(o)) & 15u)
-      return ATTN_ERR_MISALIGNED;
-    if (reinterpret_cast<uintptr_t>(lse) & 3u) return ATTN_ERR_MISALIGNED;
-    const long long max_rows = static_cast<long long>(Nq > Nk ? Nq : Nk);
-    if (static_cast<long long>(B) * H > (LLONG_MAX / (2 * d)) / max_rows) return ATTN_ERR_INVALID_ARG;
-    const int rc = attn_wide::forward(q, k, v, o, lse, B, H, Nq, Nk, d, scale, static_cast<cudaStream_t>(stream),
-                                      g_wait_limit.load(std::memory_order_relaxed));
-    if (rc == ATTN_OK) g_launches.fetch_add(1, std::memory_order_relaxed);
-    return rc;
-  }
+  if (attn_wide::supported(d)) return forward_wide(q, k, v, o, lse, B, H, Nq, Nk, d, scale, false, stream);
   return forward(q, k, v, nullptr, o, lse, B, H, Nq, Nk, d, scale, stream);
 }
 
@@ -1814,6 +1821,7 @@ extern "C" int attn_fwd_mxfp8(const void* q8, const void* sq, const void* k8, co
 extern "C" int attn_fwd_causal(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
                                int Nq, int Nk, int d, float scale, void* stream) {
   // the argument rules of attn_fwd, plus Nq <= Nk (every query row sees at least one key)
+  if (attn_wide::supported(d)) return forward_wide(q, k, v, o, lse, B, H, Nq, Nk, d, scale, true, stream);
   if (B < 0 || H < 0 || Nq < 0 || Nk < 0) return ATTN_ERR_INVALID_ARG;
   if (d != kD) return ATTN_ERR_UNSUPPORTED;
   if (!std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;

@@ -100,8 +100,40 @@ struct Params {
   int n_kv;           // 128-key steps
   int kv_tail;        // keys in the last step (1 .. 128)
   int groups;         // B * H * q_tiles
+  int bh_count;       // B * H
+  int causal;         // query i sees keys 0 .. i + causal_off only
+  int causal_off;     // Nk - Nq
   float scale_log2;   // scale * log2(e)
   unsigned long long wait_limit;
+};
+
+// The query tiles a block runs, in order; every role walks the same sequence. Plain: tile
+// g = blockIdx.x + r * gridDim.x of the list (bh, qt) with qt fastest (a head's tiles on
+// neighbouring blocks share its K and V in L2). Causal: the list sorted longest first (a
+// tile's key range ends at its last row's diagonal), every head's longest tile before any
+// head's second longest, dealt to the blocks in a snake (odd rounds in reverse block order)
+// to even out the rounds.
+struct TileIter {
+  const Params& p;
+  int r = 0;
+  __device__ explicit TileIter(const Params& pp) : p(pp) {}
+  __device__ bool next(int& bh, int& qt, int& n) {
+    const int grid = static_cast<int>(gridDim.x), b = static_cast<int>(blockIdx.x);
+    const long long pos = static_cast<long long>(r) * grid + ((p.causal && (r & 1)) ? grid - 1 - b : b);
+    ++r;
+    if (pos >= p.groups) return false;
+    if (p.causal) {
+      qt = p.q_tiles - 1 - static_cast<int>(pos / p.bh_count);
+      bh = static_cast<int>(pos % p.bh_count);
+      const int last_row = min(p.Nq, (qt + 1) * kBM) - 1;
+      n = (last_row + p.causal_off) / kBN + 1;   // key tiles up to its last row's diagonal
+    } else {
+      bh = static_cast<int>(pos / p.q_tiles);
+      qt = static_cast<int>(pos % p.q_tiles);
+      n = p.n_kv;
+    }
+    return true;
+  }
 };
 
 struct Ctl {
@@ -172,7 +204,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + L::kOffBar + kNumBars * 8);
-  const int n = p.n_kv;   // steps per query tile (the whole key range)
 
   if (warp == 0) {
     if (lane == 0) {
@@ -210,8 +241,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           v_halves = vi + 1;
         }
       };
-      for (int g = blockIdx.x; ok && g < p.groups; g += gridDim.x) {
-        const int bh = g / p.q_tiles, qt = g % p.q_tiles;
+      TileIter it(p);
+      int bh, qt, n;
+      while (ok && it.next(bh, qt, n)) {
         if (u > 0 && !wait_phase(c, kBarQEmpty, (u - 1) & 1, true)) break;
         mbar_arrive_expect_tx(c.bar(kBarQFull), L::kTileBytes);
         for (int cc = 0; cc < kChunks; ++cc)
@@ -258,7 +290,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       };
       int u = 0, gj = 0;
-      for (int g = blockIdx.x; ok && g < p.groups; g += gridDim.x) {
+      TileIter it(p);
+      int bh, qt, n;
+      while (ok && it.next(bh, qt, n)) {
         if (!wait_phase(c, kBarQFull, u & 1, true)) break;
         tc_fence_after();
         // the first two key tiles' scores; later ones follow each step's P V
@@ -313,8 +347,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float cs = kPos ? p.scale_log2 : 1.0f;
     const bool ringer = warp == 4 && lane == 0;
     int u = 0, gj = 0;
-    for (int g = blockIdx.x; g < p.groups; g += gridDim.x) {
-      const int bh = g / p.q_tiles, qt = g % p.q_tiles;
+    TileIter it(p);
+    int bh, qt, n;
+    while (it.next(bh, qt, n)) {
       float m_used = -INFINITY, l = 0.0f, corr = 0.0f;
       bool ok = true;
       for (int j = 0; j < n; ++j) {
@@ -331,10 +366,19 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int i = 0; i < 128; ++i) s[i] = kPos ? __uint_as_float(x[i]) : __uint_as_float(x[i]) * p.scale_log2;
         }
-        if (j == n - 1 && p.kv_tail < kBN) {
+        if (j == p.n_kv - 1 && p.kv_tail < kBN) {   // keys past the sequence
           const int valid = p.kv_tail;
 #pragma unroll
           for (int i = 0; i < 128; ++i) s[i] = i < valid ? s[i] : -INFINITY;
+        }
+        if (p.causal) {
+          // key j * 128 + i is visible to this row iff it is <= row + causal_off
+          const int lim_warp = qt * kBM + quarter * 32 + p.causal_off - j * kBN;   // the warp's first row
+          if (lim_warp < kBN - 1) {   // warp-uniform: some row of this warp has keys masked here
+            const int lim = lim_warp + lane;
+#pragma unroll
+            for (int i = 0; i < 128; ++i) s[i] = i <= lim ? s[i] : -INFINITY;
+          }
         }
         // row max: eight independent three-input max chains
         float mx[8];
@@ -512,7 +556,7 @@ int launch(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, 
 }  // namespace
 
 int forward(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Nq, int Nk, int d,
-            float scale, cudaStream_t stream, unsigned long long wait_limit) {
+            float scale, bool causal, cudaStream_t stream, unsigned long long wait_limit) {
   if (!supported(d)) return ATTN_ERR_UNSUPPORTED;
   const long long bh = static_cast<long long>(B) * H;
   const long long q_tiles = (static_cast<long long>(Nq) + kBM - 1) / kBM;
@@ -534,6 +578,9 @@ int forward(const void* q, const void* k, const void* v, void* o, float* lse, in
   p.n_kv = (Nk + kBN - 1) / kBN;
   p.kv_tail = Nk - (p.n_kv - 1) * kBN;
   p.groups = static_cast<int>(bh * q_tiles);
+  p.bh_count = static_cast<int>(bh);
+  p.causal = causal ? 1 : 0;
+  p.causal_off = causal ? Nk - Nq : 0;
   p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
   p.wait_limit = wait_limit;
   const int grid = std::min(sms, p.groups);

@@ -11,10 +11,11 @@ constexpr bool supported(int d) { return d == 192 || d == 256; }
 
 // O = softmax(scale Q K^T) V and the natural-log LSE for BF16 [B, H, N, d] tensors, d in
 // {192, 256}; arguments as attn_fwd (already validated by the caller: non-null, 16-byte
-// aligned, B*H, Nq, Nk >= 1, finite scale). wait_limit: clock64 budget of each of the
-// kernel's waits. Returns an attn_status code; ATTN_OK once the kernel is enqueued.
+// aligned, B*H, Nq, Nk >= 1, finite scale). causal: query i sees keys 0 .. i + Nk - Nq only
+// (the caller has checked Nq <= Nk). wait_limit: clock64 budget of each of the kernel's
+// waits. Returns an attn_status code; ATTN_OK once the kernel is enqueued.
 int forward(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Nq, int Nk,
-            int d, float scale, cudaStream_t stream, unsigned long long wait_limit);
+            int d, float scale, bool causal, cudaStream_t stream, unsigned long long wait_limit);
 
 // Reads and clears the kernel's device status word on `stream` (synchronising it): 1 if a
 // wait of a launch gave up since the last call, 0 if not, negative on a CUDA error.

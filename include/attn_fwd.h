@@ -20,8 +20,8 @@
  *
  * Conventions shared by every entry point below:
  *   - Tensors are dense, C-ordered, [B, H, N, d] (batch, heads, sequence, head dim)
- *     with d = 128 (attn_fwd also takes 192 and 256), in device memory reachable from
- *     the current CUDA device.
+ *     with d = 128 (attn_fwd and attn_fwd_causal also take 192 and 256), in device
+ *     memory reachable from the current CUDA device.
  *   - BF16 is IEEE-style bfloat16 (1 sign, 8 exponent, 7 mantissa bits), passed as
  *     raw 16-bit storage (void*).
  *   - The caller owns every buffer it passes; the library keeps no pointer to them
@@ -97,6 +97,8 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
  *   - lse is the log-sum-exp over the visible keys only.
  *   - The call allocates nothing: each block processes whole (b, h, 256-row) groups,
  *     longest first, over only the key tiles its rows can see.
+ *   - d = 192 and 256 are taken too (the kernel of attn_fwd at those head dimensions, with
+ *     whole 128-row query tiles, longest first).
  */
 int attn_fwd_causal(const void* q, const void* k, const void* v, void* o, float* lse,
                     int B, int H, int Nq, int Nk, int d, float scale, void* stream);

@@ -121,6 +121,11 @@ def call_causal(q=A, k=A, v=A, o=A, lse=A, B=1, H=1, Nq=128, Nk=128, d=128, scal
     (dict(B=1 << 16, H=1 << 16), attn.ATTN_ERR_UNSUPPORTED),
     (dict(Nq=0, Nk=0, lse=None), attn.ATTN_OK),
     (dict(B=0), attn.ATTN_OK),
+    # d > 128 (the one-Q-tile kernel): the same checks, before any CUDA call
+    (dict(Nq=129, Nk=128, d=256), attn.ATTN_ERR_INVALID_ARG),
+    (dict(d=192, o=A + 4), attn.ATTN_ERR_MISALIGNED),
+    (dict(d=256, k=None), attn.ATTN_ERR_INVALID_ARG),
+    (dict(d=320), attn.ATTN_ERR_UNSUPPORTED),
 ])
 def test_causal_argument_checks(kw, code):
     before = attn.attn_fwd_kernel_count()

@@ -83,3 +83,28 @@ def test_wide_unsupported_head_dims_rejected(gpu_lib):
         with pytest.raises(gpu_lib.AttnError) as e:
             gpu_lib.attn_fwd(q, q, q, o, lse, 1, 1, 128, 128, d, 0.1)
         assert e.value.status == gpu_lib.ATTN_ERR_UNSUPPORTED
+
+
+# ---- under the causal mask (attn_fwd_causal at d > 128): query i sees keys 0 .. i + Nk - Nq ----
+
+@pytest.mark.parametrize("d", [192, 256])
+@pytest.mark.parametrize("B,H,Nq,Nk", [
+    (1, 1, 128, 128),     # one tile on the diagonal
+    (1, 2, 256, 384),     # Nq < Nk: the mask starts at key Nk - Nq
+    (2, 3, 300, 1000),    # ragged, several tile lengths
+    (1, 1, 1, 129),
+    (1, 1, 129, 129),
+    (1, 2, 1000, 1000),
+])
+def test_wide_causal_parity(gpu_lib, d, B, H, Nq, Nk):
+    check_case(gpu_lib, B, H, Nq, Nk, seed=B * 100 + Nq + Nk + d, causal=True, d=d)
+
+
+@pytest.mark.parametrize("d", [192, 256])
+def test_wide_causal_many_tiles(gpu_lib, d):
+    # 2 * 8 * 16 = 256 tiles of 1 .. 16 key steps on at most 152 blocks (snake order)
+    check_case(gpu_lib, 2, 8, 2048, 2048, seed=21 + d, causal=True, d=d)
+
+
+def test_wide_causal_peaked(gpu_lib):
+    check_case(gpu_lib, 1, 2, 512, 1024, seed=4, qk_mult=3.0, ulp_aware=True, causal=True, d=256)
