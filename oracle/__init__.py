@@ -61,9 +61,13 @@ class Oracle:
         lib.attn_ref_rows_e4m3qk_f64.argtypes = [vp, vp, vp, i64, i64, i64, i64, i64, dbl, dbl, dbl, vp, i64, vp,
                                                  vp, ctypes.c_int]
         lib.attn_ref_rows_e4m3qk_f64.restype = ctypes.c_int
+        lib.attn_ref_rows_e4m3qk_causal_f64.argtypes = lib.attn_ref_rows_e4m3qk_f64.argtypes
+        lib.attn_ref_rows_e4m3qk_causal_f64.restype = ctypes.c_int
         lib.attn_ref_rows_e4m3_f64.argtypes = [vp, vp, vp, i64, i64, i64, i64, i64, dbl, dbl, dbl, dbl, vp, i64,
                                                vp, vp, ctypes.c_int]
         lib.attn_ref_rows_e4m3_f64.restype = ctypes.c_int
+        lib.attn_ref_rows_e4m3_causal_f64.argtypes = lib.attn_ref_rows_e4m3_f64.argtypes
+        lib.attn_ref_rows_e4m3_causal_f64.restype = ctypes.c_int
         lib.attn_ref_rows_mxfp8_f64.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, dbl, vp, i64, vp,
                                                 vp, ctypes.c_int]
         lib.attn_ref_rows_mxfp8_f64.restype = ctypes.c_int
@@ -167,9 +171,10 @@ class Oracle:
         return out
 
     def attention_rows_e4m3qk(self, q8, k8, v, scale: float, q_descale: float = 1.0, k_descale: float = 1.0,
-                              rows=None, nthreads: int = 0):
+                              rows=None, nthreads: int = 0, causal: bool = False):
         """As attention_rows with Q and K given as FP8 E4M3 codes (uint8 [B,H,N,d]) and their
-        per-tensor descale factors: the scores are scale * (q_descale Q8)(k_descale K8)^T."""
+        per-tensor descale factors: the scores are scale * (q_descale Q8)(k_descale K8)^T.
+        causal: under the causal mask of attention_rows_causal (needs Nq <= Nk)."""
         q8 = np.ascontiguousarray(q8)
         k8 = np.ascontiguousarray(k8)
         if q8.dtype != np.uint8 or k8.dtype != np.uint8:
@@ -184,17 +189,18 @@ class Oracle:
         rows = np.ascontiguousarray(rows, dtype=np.int64)
         o = np.empty((rows.size, dv), dtype=np.float64)
         lse = np.empty(rows.size, dtype=np.float64)
-        rc = self.lib.attn_ref_rows_e4m3qk_f64(_ptr(q8), _ptr(k8), _ptr(v), B * H, Nq, Nk, d, dv, float(scale),
-                                               float(q_descale), float(k_descale), _ptr(rows), rows.size,
-                                               _ptr(o), _ptr(lse), int(nthreads))
+        fn = self.lib.attn_ref_rows_e4m3qk_causal_f64 if causal else self.lib.attn_ref_rows_e4m3qk_f64
+        rc = fn(_ptr(q8), _ptr(k8), _ptr(v), B * H, Nq, Nk, d, dv, float(scale), float(q_descale), float(k_descale),
+                _ptr(rows), rows.size, _ptr(o), _ptr(lse), int(nthreads))
         if rc != 0:
             raise ValueError(f"attn_ref_rows_e4m3qk_f64 failed with status {rc}")
         return o, lse
 
     def attention_rows_e4m3(self, q8, k8, v8, scale: float, q_descale: float = 1.0, k_descale: float = 1.0,
-                            v_descale: float = 1.0, rows=None, nthreads: int = 0):
+                            v_descale: float = 1.0, rows=None, nthreads: int = 0, causal: bool = False):
         """As attention_rows_e4m3qk with V given as E4M3 codes too (uint8 [B,H,Nk,dv], real
-        values v_descale * V8); P is not rounded: this is the definition on the real inputs."""
+        values v_descale * V8); P is not rounded: this is the definition on the real inputs.
+        causal: under the causal mask of attention_rows_causal (needs Nq <= Nk)."""
         q8, k8, v8 = (np.ascontiguousarray(a) for a in (q8, k8, v8))
         if q8.dtype != np.uint8 or k8.dtype != np.uint8 or v8.dtype != np.uint8:
             raise TypeError("q8, k8 and v8 must be uint8 E4M3 codes")
@@ -207,9 +213,9 @@ class Oracle:
         rows = np.ascontiguousarray(rows, dtype=np.int64)
         o = np.empty((rows.size, dv), dtype=np.float64)
         lse = np.empty(rows.size, dtype=np.float64)
-        rc = self.lib.attn_ref_rows_e4m3_f64(_ptr(q8), _ptr(k8), _ptr(v8), B * H, Nq, Nk, d, dv, float(scale),
-                                             float(q_descale), float(k_descale), float(v_descale), _ptr(rows),
-                                             rows.size, _ptr(o), _ptr(lse), int(nthreads))
+        fn = self.lib.attn_ref_rows_e4m3_causal_f64 if causal else self.lib.attn_ref_rows_e4m3_f64
+        rc = fn(_ptr(q8), _ptr(k8), _ptr(v8), B * H, Nq, Nk, d, dv, float(scale), float(q_descale),
+                float(k_descale), float(v_descale), _ptr(rows), rows.size, _ptr(o), _ptr(lse), int(nthreads))
         if rc != 0:
             raise ValueError(f"attn_ref_rows_e4m3_f64 failed with status {rc}")
         return o, lse
@@ -357,13 +363,14 @@ def e4m3_to_f64(codes):
 
 
 def attention_rows_e4m3qk(q8, k8, v, scale: float, q_descale: float = 1.0, k_descale: float = 1.0, rows=None,
-                          nthreads: int = 0):
-    return default().attention_rows_e4m3qk(q8, k8, v, scale, q_descale, k_descale, rows, nthreads)
+                          nthreads: int = 0, causal: bool = False):
+    return default().attention_rows_e4m3qk(q8, k8, v, scale, q_descale, k_descale, rows, nthreads, causal)
 
 
 def attention_rows_e4m3(q8, k8, v8, scale: float, q_descale: float = 1.0, k_descale: float = 1.0,
-                        v_descale: float = 1.0, rows=None, nthreads: int = 0):
-    return default().attention_rows_e4m3(q8, k8, v8, scale, q_descale, k_descale, v_descale, rows, nthreads)
+                        v_descale: float = 1.0, rows=None, nthreads: int = 0, causal: bool = False):
+    return default().attention_rows_e4m3(q8, k8, v8, scale, q_descale, k_descale, v_descale, rows, nthreads,
+                                         causal)
 
 
 def e8m0_to_f64(codes):

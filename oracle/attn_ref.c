@@ -524,12 +524,12 @@ void attn_ref_e4m3_to_f64(const uint8_t *codes, int64_t n, double *out)
  *   q_descale, k_descale             the per-tensor factors of the real inputs
  * Other arguments and the return value as attn_ref_rows_f64.
  */
-int attn_ref_rows_e4m3qk_f64(const uint8_t *q8, const uint8_t *k8, const uint16_t *v,
-                             int64_t BH, int64_t Nq, int64_t Nk, int64_t d, int64_t dv,
-                             double scale, double q_descale, double k_descale,
-                             const int64_t *sel, int64_t nsel, double *o, double *lse, int nthreads)
+static int rows_e4m3qk(const uint8_t *q8, const uint8_t *k8, const uint16_t *v,
+                       int64_t BH, int64_t Nq, int64_t Nk, int64_t d, int64_t dv,
+                       double scale, double q_descale, double k_descale,
+                       const int64_t *sel, int64_t nsel, double *o, double *lse, int nthreads, int causal)
 {
-    if (BH < 0 || Nq < 0 || Nk < 1 || d < 1 || dv < 1 || nsel < 0) return REF_EINVAL;
+    if (BH < 0 || Nq < 0 || Nk < 1 || d < 1 || dv < 1 || nsel < 0 || (causal && Nq > Nk)) return REF_EINVAL;
     if (nsel == 0) return REF_OK;
     if (!q8 || !k8 || !v || !sel || !o || !lse) return REF_EINVAL;
     for (int64_t r = 0; r < nsel; r++)
@@ -556,8 +556,9 @@ int attn_ref_rows_e4m3qk_f64(const uint8_t *q8, const uint8_t *k8, const uint16_
             for (int64_t r = 0; r < nsel; r++) {
                 int64_t bh = sel[r] / Nq, i = sel[r] % Nq;
                 const uint8_t *qi = q8 + (bh * Nq + i) * d, *kh = k8 + bh * Nk * d;
+                const int64_t nk = causal ? i + (Nk - Nq) + 1 : Nk;   /* the row's keys */
                 /* step 1 on the real inputs q_descale * Q8 and k_descale * K8 */
-                for (int64_t j = 0; j < Nk; j++) {
+                for (int64_t j = 0; j < nk; j++) {
                     double acc = 0.0;
                     for (int64_t c = 0; c < d; c++)
                         acc += (q_descale * e4m3_to_f64(qi[c])) * (k_descale * e4m3_to_f64(kh[j * d + c]));
@@ -566,11 +567,11 @@ int attn_ref_rows_e4m3qk_f64(const uint8_t *q8, const uint8_t *k8, const uint16_
                 /* steps 2-5 with the head's BF16 value rows */
                 const uint16_t *vrows = v + bh * Nk * dv;
                 double *orow = o + r * dv;
-                double mx = row_max(s, Nk);
-                double den = row_exp_sum(s, Nk, mx);
+                double mx = row_max(s, nk);
+                double den = row_exp_sum(s, nk, mx);
                 for (int64_t c = 0; c < dv; c++) {
                     double num = 0.0;
-                    for (int64_t j = 0; j < Nk; j++)
+                    for (int64_t j = 0; j < nk; j++)
                         num += s[j] * bf16_to_f64(vrows[j * dv + c]);
                     orow[c] = num / den;
                 }
@@ -587,12 +588,12 @@ int attn_ref_rows_e4m3qk_f64(const uint8_t *q8, const uint8_t *k8, const uint16_
  * v8 [BH, Nk, dv] in C order with its descale factor: the real values are v_descale * V8,
  * and O is the definition's weighted sum of them (P is not rounded here).
  */
-int attn_ref_rows_e4m3_f64(const uint8_t *q8, const uint8_t *k8, const uint8_t *v8,
-                           int64_t BH, int64_t Nq, int64_t Nk, int64_t d, int64_t dv,
-                           double scale, double q_descale, double k_descale, double v_descale,
-                           const int64_t *sel, int64_t nsel, double *o, double *lse, int nthreads)
+static int rows_e4m3(const uint8_t *q8, const uint8_t *k8, const uint8_t *v8,
+                     int64_t BH, int64_t Nq, int64_t Nk, int64_t d, int64_t dv,
+                     double scale, double q_descale, double k_descale, double v_descale,
+                     const int64_t *sel, int64_t nsel, double *o, double *lse, int nthreads, int causal)
 {
-    if (BH < 0 || Nq < 0 || Nk < 1 || d < 1 || dv < 1 || nsel < 0) return REF_EINVAL;
+    if (BH < 0 || Nq < 0 || Nk < 1 || d < 1 || dv < 1 || nsel < 0 || (causal && Nq > Nk)) return REF_EINVAL;
     if (nsel == 0) return REF_OK;
     if (!q8 || !k8 || !v8 || !sel || !o || !lse) return REF_EINVAL;
     for (int64_t r = 0; r < nsel; r++)
@@ -619,19 +620,20 @@ int attn_ref_rows_e4m3_f64(const uint8_t *q8, const uint8_t *k8, const uint8_t *
             for (int64_t r = 0; r < nsel; r++) {
                 int64_t bh = sel[r] / Nq, i = sel[r] % Nq;
                 const uint8_t *qrow = q8 + (bh * Nq + i) * d, *khead = k8 + bh * Nk * d, *vhead = v8 + bh * Nk * dv;
+                const int64_t nk = causal ? i + (Nk - Nq) + 1 : Nk;   /* the row's keys */
                 /* step 1 on the real inputs */
-                for (int64_t j = 0; j < Nk; j++) {
+                for (int64_t j = 0; j < nk; j++) {
                     double dot = 0.0;
                     for (int64_t c = 0; c < d; c++)
                         dot += (q_descale * e4m3_to_f64(qrow[c])) * (k_descale * e4m3_to_f64(khead[j * d + c]));
                     w[j] = scale * dot;
                 }
                 /* steps 2-5 with the real values v_descale * V8 */
-                double top = row_max(w, Nk);
-                double sum = row_exp_sum(w, Nk, top);
+                double top = row_max(w, nk);
+                double sum = row_exp_sum(w, nk, top);
                 for (int64_t c = 0; c < dv; c++) {
                     double num = 0.0;
-                    for (int64_t j = 0; j < Nk; j++)
+                    for (int64_t j = 0; j < nk; j++)
                         num += w[j] * (v_descale * e4m3_to_f64(vhead[j * dv + c]));
                     o[r * dv + c] = num / sum;
                 }
@@ -641,6 +643,46 @@ int attn_ref_rows_e4m3_f64(const uint8_t *q8, const uint8_t *k8, const uint8_t *
         }
     }
     return failed ? REF_ENOMEM : REF_OK;
+}
+
+int attn_ref_rows_e4m3qk_f64(const uint8_t *q8, const uint8_t *k8, const uint16_t *v,
+                             int64_t BH, int64_t Nq, int64_t Nk, int64_t d, int64_t dv,
+                             double scale, double q_descale, double k_descale,
+                             const int64_t *sel, int64_t nsel, double *o, double *lse, int nthreads)
+{
+    return rows_e4m3qk(q8, k8, v, BH, Nq, Nk, d, dv, scale, q_descale, k_descale, sel, nsel, o, lse, nthreads, 0);
+}
+
+int attn_ref_rows_e4m3_f64(const uint8_t *q8, const uint8_t *k8, const uint8_t *v8,
+                           int64_t BH, int64_t Nq, int64_t Nk, int64_t d, int64_t dv,
+                           double scale, double q_descale, double k_descale, double v_descale,
+                           const int64_t *sel, int64_t nsel, double *o, double *lse, int nthreads)
+{
+    return rows_e4m3(q8, k8, v8, BH, Nq, Nk, d, dv, scale, q_descale, k_descale, v_descale, sel, nsel, o, lse,
+                     nthreads, 0);
+}
+
+/*
+ * The two FP8 functions above under the causal mask of attn_ref_rows_causal_f64 (the
+ * definition's optional mask B, "FlashAttention'ı Anlamak Bölüm 1", section 0.2, aligned to
+ * the bottom-right corner): row i uses keys 0 .. i + (Nk - Nq) only, every sum running over
+ * them. Requires Nq <= Nk.
+ */
+int attn_ref_rows_e4m3qk_causal_f64(const uint8_t *q8, const uint8_t *k8, const uint16_t *v,
+                                    int64_t BH, int64_t Nq, int64_t Nk, int64_t d, int64_t dv,
+                                    double scale, double q_descale, double k_descale,
+                                    const int64_t *sel, int64_t nsel, double *o, double *lse, int nthreads)
+{
+    return rows_e4m3qk(q8, k8, v, BH, Nq, Nk, d, dv, scale, q_descale, k_descale, sel, nsel, o, lse, nthreads, 1);
+}
+
+int attn_ref_rows_e4m3_causal_f64(const uint8_t *q8, const uint8_t *k8, const uint8_t *v8,
+                                  int64_t BH, int64_t Nq, int64_t Nk, int64_t d, int64_t dv,
+                                  double scale, double q_descale, double k_descale, double v_descale,
+                                  const int64_t *sel, int64_t nsel, double *o, double *lse, int nthreads)
+{
+    return rows_e4m3(q8, k8, v8, BH, Nq, Nk, d, dv, scale, q_descale, k_descale, v_descale, sel, nsel, o, lse,
+                     nthreads, 1);
 }
 
 /*

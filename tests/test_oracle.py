@@ -569,6 +569,36 @@ def pin_e4m3_constant_values_are_returned(orc):
     assert np.max(np.abs(o8 + 1.625)) < 1e-13
 
 
+def pin_e4m3_causal_scores_equal_the_bf16_causal_oracle(orc):
+    # under the causal mask too the E4M3-score oracle is the (pinned) BF16 causal oracle on
+    # the codes' values, the descale factors moved into the scale; Nq < Nk puts the mask's
+    # corner at key Nk - Nq
+    from dense_attention_forward_fwd_gb300.inputs import make_qk_e4m3
+    q8, k8, v, dq, dk = make_qk_e4m3(2, 1, 9, 23, d=16, seed=76, qk_mult=2.0)
+    qb, kb = bf16(orc.e4m3_to_f64(q8)), bf16(orc.e4m3_to_f64(k8))
+    o8, l8 = orc.attention_rows_e4m3qk(q8, k8, v, 0.3, dq, dk, causal=True)
+    ob, lb = orc.attention_rows_causal(qb, kb, v, 0.3 * dq * dk)
+    assert np.max(np.abs(o8 - ob)) < 1e-12 and np.max(np.abs(l8 - lb)) < 1e-12 * np.max(np.abs(lb))
+
+
+def pin_e4m3_causal_rows_are_the_unmasked_rows_over_the_visible_prefix(orc):
+    # row i of either FP8 oracle under the mask is its unmasked row over keys 0 .. i + Nk - Nq
+    from dense_attention_forward_fwd_gb300.inputs import make_qkv_e4m3
+    q8, k8, v8, dq, dk, dv = make_qkv_e4m3(1, 2, 6, 13, d=16, seed=77, qk_mult=2.0)
+    vb = bf16(orc.e4m3_to_f64(v8))
+    oq, lq = orc.attention_rows_e4m3qk(q8, k8, vb, 0.4, dq, dk, causal=True)
+    oa, la = orc.attention_rows_e4m3(q8, k8, v8, 0.4, dq, dk, dv, causal=True)
+    oq, lq, oa, la = oq.reshape(2, 6, 16), lq.reshape(2, 6), oa.reshape(2, 6, 16), la.reshape(2, 6)
+    for h in range(2):
+        for i in range(6):
+            n = i + 13 - 6 + 1
+            sl = (slice(None), slice(h, h + 1))
+            op, lp = orc.attention_rows_e4m3qk(q8[sl][:, :, i:i + 1], k8[sl][:, :, :n], vb[sl][:, :, :n], 0.4, dq, dk)
+            assert np.array_equal(oq[h, i], op[0]) and lq[h, i] == lp[0]
+            op, lp = orc.attention_rows_e4m3(q8[sl][:, :, i:i + 1], k8[sl][:, :, :n], v8[sl][:, :, :n], 0.4, dq, dk, dv)
+            assert np.array_equal(oa[h, i], op[0]) and la[h, i] == lp[0]
+
+
 # ---- MXFP8: E4M3 elements with E8M0 scales per 32 elements along each contraction ----------
 
 def pin_e8m0_decoder_closed_forms(orc):

@@ -56,6 +56,10 @@ MUTANTS = {
                                 "(1.0 * e4m3_to_f64(vh[j * dv + c]))"),
     "mx query scales of the first block only": ("(e8m0_to_f64(qs[c / 32]) * e4m3_to_f64(qi[c]))",
                                                 "(e8m0_to_f64(qs[0]) * e4m3_to_f64(qi[c]))"),
+    "e4m3 causal mask one key short": ("const int64_t nk = causal ? i + (Nk - Nq) + 1 : Nk;",
+                                       "const int64_t nk = causal ? i + (Nk - Nq) + (i > 0) : Nk;"),
+    "e4m3 causal mask aligned top-left": ("const int64_t nk = causal ? i + (Nk - Nq) + 1 : Nk;",
+                                          "const int64_t nk = causal ? i + 1 : Nk;"),
     "causal dense forward one key short": ("const int64_t nv = causal ? i + (Nk - Nq) + 1 : Nk;",
                                            "const int64_t nv = causal ? i + (Nk - Nq) + (i > 0) : Nk;"),
 }
