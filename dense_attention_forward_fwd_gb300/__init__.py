@@ -56,6 +56,10 @@ def load_library(build_if_stale: bool = True) -> ctypes.CDLL:
             lib.attn_fwd_fp8.argtypes = [vp, vp, vp, ctypes.c_longlong, vp, vp, i32, i32, i32, i32, i32, f32, f32, f32,
                                          f32, vp]
             lib.attn_fwd_fp8.restype = i32
+            lib.attn_fwd_fp8qk_causal.argtypes = lib.attn_fwd_fp8qk.argtypes
+            lib.attn_fwd_fp8qk_causal.restype = i32
+            lib.attn_fwd_fp8_causal.argtypes = lib.attn_fwd_fp8.argtypes
+            lib.attn_fwd_fp8_causal.restype = i32
             lib.attn_fwd_mxfp8.argtypes = [vp, vp, vp, vp, vp, ctypes.c_longlong, vp, ctypes.c_longlong, vp, vp, i32, i32,
                                            i32, i32, i32, f32, vp]
             lib.attn_fwd_mxfp8.restype = i32
@@ -157,29 +161,31 @@ def attn_fwd_causal(q, k, v, o, lse, B: int, H: int, Nq: int, Nk: int, d: int, s
 
 
 def attn_fwd_fp8qk(q8, k8, v, o, lse, B: int, H: int, Nq: int, Nk: int, d: int, scale: float,
-                   q_descale: float = 1.0, k_descale: float = 1.0, stream=None) -> None:
+                   q_descale: float = 1.0, k_descale: float = 1.0, stream=None, causal: bool = False) -> None:
     """Like :func:`attn_fwd`, with Q and K given as FP8 E4M3 codes (torch.float8_e4m3fn or
     uint8 CUDA tensors [B,H,N,d]) and one positive descale factor each:
-    S = scale * q_descale * k_descale * (Q8 K8^T); V, O and LSE as in attn_fwd."""
+    S = scale * q_descale * k_descale * (Q8 K8^T); V, O and LSE as in attn_fwd. causal: under
+    the causal mask of attn_fwd_causal (attn_fwd_fp8qk_causal)."""
     lib = load_library()
     args = (
         _ptr(q8, "q8", B * H * Nq * d, "e4m3"), _ptr(k8, "k8", B * H * Nk * d, "e4m3"),
         _ptr(v, "v", B * H * Nk * d, "bf16"), _ptr(o, "o", B * H * Nq * d, "bf16"),
         _ptr(lse, "lse", B * H * Nq, "f32"),
     )
-    rc = lib.attn_fwd_fp8qk(*args, int(B), int(H), int(Nq), int(Nk), int(d), float(scale), float(q_descale),
-                            float(k_descale), _stream_handle(stream, q8, k8, v, o, lse))
+    fn = lib.attn_fwd_fp8qk_causal if causal else lib.attn_fwd_fp8qk
+    rc = fn(*args, int(B), int(H), int(Nq), int(Nk), int(d), float(scale), float(q_descale), float(k_descale),
+            _stream_handle(stream, q8, k8, v, o, lse))
     if rc != ATTN_OK:
-        raise AttnError(rc, "attn_fwd_fp8qk")
+        raise AttnError(rc, "attn_fwd_fp8qk_causal" if causal else "attn_fwd_fp8qk")
 
 
 def attn_fwd_fp8(q8, k8, vt8, o, lse, B: int, H: int, Nq: int, Nk: int, d: int, scale: float,
                  q_descale: float = 1.0, k_descale: float = 1.0, v_descale: float = 1.0, stream=None,
-                 ldv: int | None = None) -> None:
+                 ldv: int | None = None, causal: bool = False) -> None:
     """Like :func:`attn_fwd_fp8qk`, with V as E4M3 codes too, passed transposed: ``vt8`` is
     [B,H,d,ldv] (keys innermost, ldv >= Nk a multiple of 16; a tensor's last dimension is
     taken as ldv). P is rounded to E4M3 for the P V product (see include/attn_fwd.h for the
-    accuracy this costs)."""
+    accuracy this costs). causal: under the causal mask (attn_fwd_fp8_causal)."""
     lib = load_library()
     if _is_tensor(vt8):
         if vt8.dim() != 4 or tuple(vt8.shape[:3]) != (B, H, d):
@@ -192,11 +198,11 @@ def attn_fwd_fp8(q8, k8, vt8, o, lse, B: int, H: int, Nq: int, Nk: int, d: int, 
         _ptr(vt8, "vt8", B * H * d * ldv, "e4m3"),
     )
     outs = (_ptr(o, "o", B * H * Nq * d, "bf16"), _ptr(lse, "lse", B * H * Nq, "f32"))
-    rc = lib.attn_fwd_fp8(*args, int(ldv), *outs, int(B), int(H), int(Nq), int(Nk), int(d), float(scale),
-                          float(q_descale), float(k_descale), float(v_descale),
-                          _stream_handle(stream, q8, k8, vt8, o, lse))
+    fn = lib.attn_fwd_fp8_causal if causal else lib.attn_fwd_fp8
+    rc = fn(*args, int(ldv), *outs, int(B), int(H), int(Nq), int(Nk), int(d), float(scale), float(q_descale),
+            float(k_descale), float(v_descale), _stream_handle(stream, q8, k8, vt8, o, lse))
     if rc != ATTN_OK:
-        raise AttnError(rc, "attn_fwd_fp8")
+        raise AttnError(rc, "attn_fwd_fp8_causal" if causal else "attn_fwd_fp8")
 
 
 def attn_fwd_mxfp8(q8, sq, k8, sk, vt8, svt, o, lse, B: int, H: int, Nq: int, Nk: int, d: int, scale: float,

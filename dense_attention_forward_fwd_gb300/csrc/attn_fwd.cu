@@ -1818,10 +1818,14 @@ extern "C" int attn_fwd_mxfp8(const void* q8, const void* sq, const void* k8, co
   return forward(q8, k8, vt8, nullptr, o, lse, B, H, Nq, Nk, d, scale, stream, 3, ldv, 1.0f, nullptr, &mx);
 }
 
-extern "C" int attn_fwd_causal(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
-                               int Nq, int Nk, int d, float scale, void* stream) {
+namespace {
+// The causal launches: whole (b, h, 256-row) groups, longest first, each over the key tiles
+// its rows can see (the causal order of SegIter): no workspace, no merge. f8: 0 BF16 inputs,
+// 1 Q and K as E4M3 codes, 2 V too (V^T rows of ldv bytes, v_scale its descale factor);
+// scale already holds any Q and K descale factors.
+int forward_causal(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Nq, int Nk,
+                   int d, float scale, void* stream, int f8 = 0, long long ldv = 0, float v_scale = 1.0f) {
   // the argument rules of attn_fwd, plus Nq <= Nk (every query row sees at least one key)
-  if (attn_wide::supported(d)) return forward_wide(q, k, v, o, lse, B, H, Nq, Nk, d, scale, true, stream);
   if (B < 0 || H < 0 || Nq < 0 || Nk < 0) return ATTN_ERR_INVALID_ARG;
   if (d != kD) return ATTN_ERR_UNSUPPORTED;
   if (!std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
@@ -1838,6 +1842,11 @@ extern "C" int attn_fwd_causal(const void* q, const void* k, const void* v, void
   if (bh > INT_MAX || bh * q_groups > INT_MAX) return ATTN_ERR_UNSUPPORTED;
   const long long max_rows = static_cast<long long>(Nk);
   if (bh > (LLONG_MAX / 256) / max_rows) return ATTN_ERR_INVALID_ARG;
+  if (f8 >= 2) {   // V^T rows: as attn_fwd_fp8
+    if (ldv < Nk) return ATTN_ERR_INVALID_ARG;
+    if (ldv % 16 != 0) return ATTN_ERR_MISALIGNED;
+    if (bh > (LLONG_MAX / kD) / ldv) return ATTN_ERR_INVALID_ARG;
+  }
 
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return ATTN_ERR_CUDA;
@@ -1845,10 +1854,10 @@ extern "C" int attn_fwd_causal(const void* q, const void* k, const void* v, void
   if (sms <= 0) return ATTN_ERR_CUDA;
 
   CUtensorMap mq, mk, mv;
-  if (!make_map(&mq, q, Nq, bh) || !make_map(&mk, k, Nk, bh) || !make_map(&mv, v, Nk, bh))
+  if (!make_map(&mq, q, Nq, bh, f8 >= 1) || !make_map(&mk, k, Nk, bh, f8 >= 1) ||
+      !(f8 >= 2 ? make_map_vt(&mv, v, Nk, ldv, bh) : make_map(&mv, v, Nk, bh)))
     return ATTN_ERR_CUDA;
 
-  // Whole groups only (the causal order of SegIter): no workspace, no merge.
   const long long n_groups = bh * q_groups;
   Params p;
   p.o = static_cast<uint16_t*>(o);
@@ -1874,9 +1883,52 @@ extern "C" int attn_fwd_causal(const void* q, const void* k, const void* v, void
   p.bias_sb = p.bias_sh = p.bias_sq = 0;
   p.H = H;
   p.scale = scale;
+  p.v_scale = v_scale;
   const int grid = static_cast<int>(n_groups < sms ? n_groups : sms);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (f8 == 2)
+    return scale > 0.0f ? launch<true, false, 2>(mq, mk, mv, p, grid, dev, s)
+                        : launch<false, false, 2>(mq, mk, mv, p, grid, dev, s);
+  if (f8 == 1)
+    return scale > 0.0f ? launch<true, false, 1>(mq, mk, mv, p, grid, dev, s)
+                        : launch<false, false, 1>(mq, mk, mv, p, grid, dev, s);
   return scale > 0.0f ? launch<true>(mq, mk, mv, p, grid, dev, s) : launch<false>(mq, mk, mv, p, grid, dev, s);
+}
+
+// The FP8 entry points' factor checks: the effective score scale, or 0 with *rc set.
+float fp8_scale(float scale, float q_descale, float k_descale, float v_descale, int* rc) {
+  *rc = ATTN_OK;
+  if (!std::isfinite(scale) || !std::isfinite(q_descale) || !std::isfinite(k_descale) ||
+      !std::isfinite(v_descale) || !(q_descale > 0.0f) || !(k_descale > 0.0f) || !(v_descale > 0.0f)) {
+    *rc = ATTN_ERR_INVALID_ARG;
+    return 0.0f;
+  }
+  const double eff = static_cast<double>(scale) * q_descale * k_descale;
+  if (!(std::fabs(eff) <= static_cast<double>(FLT_MAX))) *rc = ATTN_ERR_INVALID_ARG;
+  return static_cast<float>(eff);
+}
+}  // namespace
+
+extern "C" int attn_fwd_causal(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                               int Nq, int Nk, int d, float scale, void* stream) {
+  if (attn_wide::supported(d)) return forward_wide(q, k, v, o, lse, B, H, Nq, Nk, d, scale, true, stream);
+  return forward_causal(q, k, v, o, lse, B, H, Nq, Nk, d, scale, stream);
+}
+extern "C" int attn_fwd_fp8qk_causal(const void* q8, const void* k8, const void* v, void* o, float* lse, int B,
+                                     int H, int Nq, int Nk, int d, float scale, float q_descale, float k_descale,
+                                     void* stream) {
+  int rc = ATTN_OK;
+  const float eff = fp8_scale(scale, q_descale, k_descale, 1.0f, &rc);
+  if (rc != ATTN_OK) return rc;
+  return forward_causal(q8, k8, v, o, lse, B, H, Nq, Nk, d, eff, stream, 1);
+}
+extern "C" int attn_fwd_fp8_causal(const void* q8, const void* k8, const void* vt8, long long ldv, void* o,
+                                   float* lse, int B, int H, int Nq, int Nk, int d, float scale, float q_descale,
+                                   float k_descale, float v_descale, void* stream) {
+  int rc = ATTN_OK;
+  const float eff = fp8_scale(scale, q_descale, k_descale, v_descale, &rc);
+  if (rc != ATTN_OK) return rc;
+  return forward_causal(q8, k8, vt8, o, lse, B, H, Nq, Nk, d, eff, stream, 2, ldv, v_descale);
 }
 
 extern "C" int attn_fwd_status(void* stream) {

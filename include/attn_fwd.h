@@ -190,6 +190,22 @@ int attn_fwd_fp8(const void* q8, const void* k8, const void* vt8, long long ldv,
                  float v_descale, void* stream);
 
 /*
+ * attn_fwd_fp8qk_causal, attn_fwd_fp8_causal -- attn_fwd_fp8qk and attn_fwd_fp8 under the
+ * causal mask of attn_fwd_causal (query i sees keys 0 .. i + Nk - Nq).
+ *
+ * Arguments, layouts, accuracy and return values are those of the FP8 entry point of the
+ * same name, plus attn_fwd_causal's rules: Nq <= Nk is required (Nq > Nk returns
+ * ATTN_ERR_INVALID_ARG without touching the GPU), lse sums over the visible keys only, and
+ * the call allocates nothing (whole 256-row groups per block, longest first). d = 128.
+ */
+int attn_fwd_fp8qk_causal(const void* q8, const void* k8, const void* v, void* o, float* lse,
+                          int B, int H, int Nq, int Nk, int d, float scale, float q_descale,
+                          float k_descale, void* stream);
+int attn_fwd_fp8_causal(const void* q8, const void* k8, const void* vt8, long long ldv, void* o,
+                        float* lse, int B, int H, int Nq, int Nk, int d, float scale, float q_descale,
+                        float k_descale, float v_descale, void* stream);
+
+/*
  * attn_fwd_mxfp8 -- attention forward from MXFP8 inputs, both products block-scaled.
  *
  * The "MXFP8 MMA" that "Flash Attention на 5090 в CUDA C++" (section "Что дальше") names as

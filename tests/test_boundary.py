@@ -27,6 +27,7 @@ def declared_functions():
 def test_header_declares_the_entry_points():
     names = declared_functions()
     assert {"attn_fwd", "attn_fwd_causal", "attn_fwd_bias", "attn_fwd_fp8qk", "attn_fwd_fp8", "attn_fwd_o32", "attn_fwd_noalloc", "attn_bwd", "attn_bwd_causal",
+            "attn_fwd_fp8qk_causal", "attn_fwd_fp8_causal", "attn_fwd_mxfp8",
             "attn_bwd_status", "attn_bwd_set_wait_limit",
             "attn_bwd_kernel_count", "attn_fwd_status", "attn_status_string",
             "attn_fwd_set_wait_limit", "attn_fwd_kernel_count"} <= set(names)
@@ -157,8 +158,11 @@ def test_bias_argument_checks(kw, code):
     assert attn.attn_fwd_kernel_count() == before
 
 
-def call_fp8(q8=A, k8=A, v=A, o=A, lse=A, B=1, H=1, Nq=128, Nk=128, d=128, scale=0.125, dq=0.01, dk=0.02):
-    return attn.load_library().attn_fwd_fp8qk(q8, k8, v, o, lse, B, H, Nq, Nk, d, scale, dq, dk, None)
+def call_fp8(q8=A, k8=A, v=A, o=A, lse=A, B=1, H=1, Nq=128, Nk=128, d=128, scale=0.125, dq=0.01, dk=0.02,
+             causal=False):
+    lib = attn.load_library()
+    fn = lib.attn_fwd_fp8qk_causal if causal else lib.attn_fwd_fp8qk
+    return fn(q8, k8, v, o, lse, B, H, Nq, Nk, d, scale, dq, dk, None)
 
 
 @pytest.mark.parametrize("kw,code", [
@@ -175,10 +179,16 @@ def call_fp8(q8=A, k8=A, v=A, o=A, lse=A, B=1, H=1, Nq=128, Nk=128, d=128, scale
     (dict(B=0, q8=None), attn.ATTN_OK),
     (dict(Nq=0, lse=None), attn.ATTN_OK),
 ])
-def test_fp8qk_argument_checks(kw, code):
+@pytest.mark.parametrize("causal", [False, True])
+def test_fp8qk_argument_checks(kw, code, causal):
     before = attn.attn_fwd_kernel_count()
-    assert call_fp8(**kw) == code
+    assert call_fp8(causal=causal, **kw) == code
     assert attn.attn_fwd_kernel_count() == before
+
+
+def test_fp8_causal_rejects_more_queries_than_keys():
+    assert call_fp8(Nq=129, Nk=128, causal=True) == attn.ATTN_ERR_INVALID_ARG
+    assert call_fp8pv(Nq=129, Nk=128, causal=True) == attn.ATTN_ERR_INVALID_ARG
 
 
 def test_fp8qk_binding_checks_types():
@@ -190,8 +200,10 @@ def test_fp8qk_binding_checks_types():
 
 
 def call_fp8pv(q8=A, k8=A, vt8=A, ldv=128, o=A, lse=A, B=1, H=1, Nq=128, Nk=128, d=128, scale=0.125, dq=0.01,
-               dk=0.02, dv=0.03):
-    return attn.load_library().attn_fwd_fp8(q8, k8, vt8, ldv, o, lse, B, H, Nq, Nk, d, scale, dq, dk, dv, None)
+               dk=0.02, dv=0.03, causal=False):
+    lib = attn.load_library()
+    fn = lib.attn_fwd_fp8_causal if causal else lib.attn_fwd_fp8
+    return fn(q8, k8, vt8, ldv, o, lse, B, H, Nq, Nk, d, scale, dq, dk, dv, None)
 
 
 @pytest.mark.parametrize("kw,code", [
@@ -207,9 +219,10 @@ def call_fp8pv(q8=A, k8=A, vt8=A, ldv=128, o=A, lse=A, B=1, H=1, Nq=128, Nk=128,
     (dict(Nk=0), attn.ATTN_ERR_INVALID_ARG),
     (dict(B=0), attn.ATTN_OK),
 ])
-def test_fp8_argument_checks(kw, code):
+@pytest.mark.parametrize("causal", [False, True])
+def test_fp8_argument_checks(kw, code, causal):
     before = attn.attn_fwd_kernel_count()
-    assert call_fp8pv(**kw) == code
+    assert call_fp8pv(causal=causal, **kw) == code
     assert attn.attn_fwd_kernel_count() == before
 
 

@@ -21,7 +21,7 @@ pytestmark = pytest.mark.gpu
 SCALE = float(np.float32(1 / math.sqrt(128)))
 
 
-def run_fp8(attn, q8, k8, v, scale, dq, dk):
+def run_fp8(attn, q8, k8, v, scale, dq, dk, causal=False):
     import torch
     B, H, Nq, d = q8.shape
     Nk = k8.shape[2]
@@ -29,15 +29,15 @@ def run_fp8(attn, q8, k8, v, scale, dq, dk):
     lse = torch.full((B, H, Nq), float("nan"), dtype=torch.float32, device="cuda")
     q8d = torch.from_numpy(np.ascontiguousarray(q8)).cuda().view(torch.float8_e4m3fn)
     k8d = torch.from_numpy(np.ascontiguousarray(k8)).cuda()          # raw bytes are accepted too
-    attn.attn_fwd_fp8qk(q8d, k8d, to_device(v), o, lse, B, H, Nq, Nk, d, scale, dq, dk)
+    attn.attn_fwd_fp8qk(q8d, k8d, to_device(v), o, lse, B, H, Nq, Nk, d, scale, dq, dk, causal=causal)
     assert attn.attn_fwd_status() == attn.ATTN_OK
     return bf16_to_np(o), lse.cpu().numpy()
 
 
-def check_fp8(attn, B, H, Nq, Nk, seed, qk_mult=1.0, scale=SCALE, rows=None):
+def check_fp8(attn, B, H, Nq, Nk, seed, qk_mult=1.0, scale=SCALE, rows=None, causal=False):
     q8, k8, v, dq, dk = make_qk_e4m3(B, H, Nq, Nk, seed=seed, qk_mult=qk_mult)
-    o, lse = run_fp8(attn, q8, k8, v, scale, dq, dk)
-    o_ref, lse_ref = oracle.attention_rows_e4m3qk(q8, k8, v, scale, dq, dk, rows)
+    o, lse = run_fp8(attn, q8, k8, v, scale, dq, dk, causal)
+    o_ref, lse_ref = oracle.attention_rows_e4m3qk(q8, k8, v, scale, dq, dk, rows, causal=causal)
     o, lse = o.reshape(-1, 128), lse.reshape(-1)
     if rows is not None:
         o, lse = o[rows], lse[rows]
@@ -106,11 +106,14 @@ def test_fp8qk_is_deterministic(gpu_lib):
 # or V read from the wrong rows moves O by 1e-1 or more on average. The LSE does not depend
 # on P's rounding and keeps the forward's 1e-4.
 
-def fp8pv_tolerance(qk_mult):
+def fp8pv_tolerance(qk_mult, causal=False):
+    # under the causal mask rows near the diagonal average over few keys (tests/test_fp8_tolerance.py)
+    if causal:
+        return (7e-2, 7e-3) if qk_mult == 1.0 else (2e-1, 1e-2)
     return (4e-2, 5e-3) if qk_mult == 1.0 else (2e-1, 1e-2)
 
 
-def run_fp8pv(attn, q8, k8, v8, scale, dq, dk, dv, ldv=None, pad_code=0x7F):
+def run_fp8pv(attn, q8, k8, v8, scale, dq, dk, dv, ldv=None, pad_code=0x7F, causal=False):
     """v8 is key-major [B,H,Nk,d]; the kernel gets V^T [B,H,d,ldv] with the bytes past Nk of
     each row set to pad_code (NaN by default: a read of them would show in O)."""
     import torch
@@ -122,23 +125,24 @@ def run_fp8pv(attn, q8, k8, v8, scale, dq, dk, dv, ldv=None, pad_code=0x7F):
     o = torch.full((B, H, Nq, d), float("nan"), dtype=torch.bfloat16, device="cuda")
     lse = torch.full((B, H, Nq), float("nan"), dtype=torch.float32, device="cuda")
     attn.attn_fwd_fp8(torch.from_numpy(np.ascontiguousarray(q8)).cuda(), torch.from_numpy(np.ascontiguousarray(k8)).cuda(),
-                      torch.from_numpy(vt).cuda().view(torch.float8_e4m3fn), o, lse, B, H, Nq, Nk, d, scale, dq, dk, dv)
+                      torch.from_numpy(vt).cuda().view(torch.float8_e4m3fn), o, lse, B, H, Nq, Nk, d, scale, dq, dk, dv,
+                      causal=causal)
     assert attn.attn_fwd_status() == attn.ATTN_OK
     return bf16_to_np(o), lse.cpu().numpy()
 
 
-def check_fp8pv(attn, B, H, Nq, Nk, seed, qk_mult=1.0, scale=SCALE, rows=None, ldv=None):
+def check_fp8pv(attn, B, H, Nq, Nk, seed, qk_mult=1.0, scale=SCALE, rows=None, ldv=None, causal=False):
     from dense_attention_forward_fwd_gb300.inputs import make_qkv_e4m3
     q8, k8, v8, dq, dk, dv = make_qkv_e4m3(B, H, Nq, Nk, seed=seed, qk_mult=qk_mult)
-    o, lse = run_fp8pv(attn, q8, k8, v8, scale, dq, dk, dv, ldv)
-    o_ref, lse_ref = oracle.attention_rows_e4m3(q8, k8, v8, scale, dq, dk, dv, rows)
+    o, lse = run_fp8pv(attn, q8, k8, v8, scale, dq, dk, dv, ldv, causal=causal)
+    o_ref, lse_ref = oracle.attention_rows_e4m3(q8, k8, v8, scale, dq, dk, dv, rows, causal=causal)
     o, lse = o.reshape(-1, 128), lse.reshape(-1)
     if rows is not None:
         o, lse = o[rows], lse[rows]
     assert np.all(np.isfinite(o)) and np.all(np.isfinite(lse)), "non-finite output"
     err = np.abs(o.astype(np.float64) - o_ref)
     lse_err = np.abs(lse.astype(np.float64) - lse_ref) / np.maximum(1.0, np.abs(lse_ref))
-    t_max, t_mean = fp8pv_tolerance(qk_mult)
+    t_max, t_mean = fp8pv_tolerance(qk_mult, causal)
     assert err.max() <= t_max and err.mean() <= t_mean and lse_err.max() <= 1e-4, \
         f"max {err.max():.3e} mean {err.mean():.3e} lse {lse_err.max():.3e}"
     return err.max(), err.mean()
@@ -195,3 +199,44 @@ def test_fp8_is_deterministic(gpu_lib):
     a = run_fp8pv(gpu_lib, q8, k8, v8, SCALE, dq, dk, dv)
     b = run_fp8pv(gpu_lib, q8, k8, v8, SCALE, dq, dk, dv)
     assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+
+
+# ---- under the causal mask: attn_fwd_fp8qk_causal and attn_fwd_fp8_causal ----------------------
+
+@pytest.mark.parametrize("B,H,Nq,Nk", [
+    (1, 1, 128, 128),
+    (1, 2, 256, 384),      # Nq < Nk: the mask's corner at key Nk - Nq
+    (2, 3, 300, 1000),     # ragged
+    (1, 1, 1, 200),
+    (1, 2, 129, 129),
+    (1, 2, 1000, 1000),
+])
+def test_fp8qk_causal_parity(gpu_lib, B, H, Nq, Nk):
+    check_fp8(gpu_lib, B, H, Nq, Nk, seed=15000 + Nq + Nk, causal=True)
+
+
+def test_fp8qk_causal_peaked(gpu_lib):
+    check_fp8(gpu_lib, 1, 2, 512, 1024, seed=15100, qk_mult=3.0, causal=True)
+
+
+@pytest.mark.parametrize("B,H,Nq,Nk,seed", [
+    (1, 1, 128, 128, 16256),
+    (1, 2, 256, 384, 16640),
+    (1, 2, 129, 129, 16258),
+    (1, 2, 1000, 1000, 18000),
+])
+def test_fp8_causal_parity(gpu_lib, B, H, Nq, Nk, seed):
+    # the inputs tests/test_fp8_tolerance.py derives the causal bounds on
+    check_fp8pv(gpu_lib, B, H, Nq, Nk, seed=seed, causal=True)
+
+
+def test_fp8_causal_peaked(gpu_lib):
+    check_fp8pv(gpu_lib, 1, 2, 512, 1024, seed=16100, qk_mult=3.0, causal=True)
+
+
+@pytest.mark.parametrize("name", ["square-4k"])
+def test_fp8_causal_workload_sampled_rows(gpu_lib, name):
+    w = by_name(name)
+    rows = sample_rows(w.B, w.H, w.Nq, per_head=16)
+    check_fp8(gpu_lib, w.B, w.H, w.Nq, w.Nk, seed=w.seed, scale=w.scale, rows=rows, causal=True)
+    check_fp8pv(gpu_lib, w.B, w.H, w.Nq, w.Nk, seed=w.seed, scale=w.scale, rows=rows, causal=True)
