@@ -71,6 +71,8 @@ class Oracle:
         lib.attn_ref_rows_mxfp8_f64.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, dbl, vp, i64, vp,
                                                 vp, ctypes.c_int]
         lib.attn_ref_rows_mxfp8_f64.restype = ctypes.c_int
+        lib.attn_ref_rows_mxfp8_causal_f64.argtypes = lib.attn_ref_rows_mxfp8_f64.argtypes
+        lib.attn_ref_rows_mxfp8_causal_f64.restype = ctypes.c_int
         lib.attn_ref_e8m0_to_f64.argtypes = [vp, i64, vp]
         lib.attn_ref_e8m0_to_f64.restype = None
         lib.attn_ref_e4m3_to_f64.argtypes = [vp, i64, vp]
@@ -227,10 +229,12 @@ class Oracle:
         self.lib.attn_ref_e8m0_to_f64(_ptr(c), c.size, _ptr(out))
         return out
 
-    def attention_rows_mxfp8(self, q8, sq, k8, sk, v8, sv, scale: float, rows=None, nthreads: int = 0):
+    def attention_rows_mxfp8(self, q8, sq, k8, sk, v8, sv, scale: float, rows=None, nthreads: int = 0,
+                             causal: bool = False):
         """O and LSE (float64) of selected rows from MXFP8 inputs: E4M3 codes q8 [B,H,Nq,d],
         k8 [B,H,Nk,d], v8 [B,H,Nk,dv] with E8M0 block scales sq [B,H,Nq,d/32] and
-        sk [B,H,Nk,d/32] (32 elements along d) and sv [B,H,ceil(Nk/32),dv] (32 keys per column)."""
+        sk [B,H,Nk,d/32] (32 elements along d) and sv [B,H,ceil(Nk/32),dv] (32 keys per column).
+        causal: under the causal mask of attention_rows_causal (needs Nq <= Nk)."""
         arrs = [np.ascontiguousarray(a) for a in (q8, sq, k8, sk, v8, sv)]
         if any(a.dtype != np.uint8 for a in arrs):
             raise TypeError("MXFP8 codes and scales must be uint8")
@@ -247,9 +251,9 @@ class Oracle:
         rows = np.ascontiguousarray(rows, dtype=np.int64)
         o = np.empty((rows.size, dv), dtype=np.float64)
         lse = np.empty(rows.size, dtype=np.float64)
-        rc = self.lib.attn_ref_rows_mxfp8_f64(_ptr(q8), _ptr(sq), _ptr(k8), _ptr(sk), _ptr(v8), _ptr(sv), B * H, Nq,
-                                              Nk, d, dv, float(scale), _ptr(rows), rows.size, _ptr(o), _ptr(lse),
-                                              int(nthreads))
+        fn = self.lib.attn_ref_rows_mxfp8_causal_f64 if causal else self.lib.attn_ref_rows_mxfp8_f64
+        rc = fn(_ptr(q8), _ptr(sq), _ptr(k8), _ptr(sk), _ptr(v8), _ptr(sv), B * H, Nq, Nk, d, dv, float(scale),
+                _ptr(rows), rows.size, _ptr(o), _ptr(lse), int(nthreads))
         if rc != 0:
             raise ValueError(f"attn_ref_rows_mxfp8_f64 failed with status {rc}")
         return o, lse
@@ -377,8 +381,8 @@ def e8m0_to_f64(codes):
     return default().e8m0_to_f64(codes)
 
 
-def attention_rows_mxfp8(q8, sq, k8, sk, v8, sv, scale: float, rows=None, nthreads: int = 0):
-    return default().attention_rows_mxfp8(q8, sq, k8, sk, v8, sv, scale, rows, nthreads)
+def attention_rows_mxfp8(q8, sq, k8, sk, v8, sv, scale: float, rows=None, nthreads: int = 0, causal: bool = False):
+    return default().attention_rows_mxfp8(q8, sq, k8, sk, v8, sv, scale, rows, nthreads, causal)
 
 
 def attention(q, k, v, scale: float, nthreads: int = 0):

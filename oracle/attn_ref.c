@@ -716,12 +716,13 @@ void attn_ref_e8m0_to_f64(const uint8_t *codes, int64_t n, double *out)
  *   sv [BH, ceil(Nk/32), dv]                          E8M0 scales of 32 keys per column
  * d must be a multiple of 32. Other arguments and the return value as attn_ref_rows_f64.
  */
-int attn_ref_rows_mxfp8_f64(const uint8_t *q8, const uint8_t *sq, const uint8_t *k8, const uint8_t *sk,
-                            const uint8_t *v8, const uint8_t *sv,
-                            int64_t BH, int64_t Nq, int64_t Nk, int64_t d, int64_t dv, double scale,
-                            const int64_t *sel, int64_t nsel, double *o, double *lse, int nthreads)
+static int rows_mxfp8(const uint8_t *q8, const uint8_t *sq, const uint8_t *k8, const uint8_t *sk,
+                      const uint8_t *v8, const uint8_t *sv,
+                      int64_t BH, int64_t Nq, int64_t Nk, int64_t d, int64_t dv, double scale,
+                      const int64_t *sel, int64_t nsel, double *o, double *lse, int nthreads, int causal)
 {
-    if (BH < 0 || Nq < 0 || Nk < 1 || d < 32 || d % 32 != 0 || dv < 1 || nsel < 0) return REF_EINVAL;
+    if (BH < 0 || Nq < 0 || Nk < 1 || d < 32 || d % 32 != 0 || dv < 1 || nsel < 0 || (causal && Nq > Nk))
+        return REF_EINVAL;
     if (nsel == 0) return REF_OK;
     if (!q8 || !sq || !k8 || !sk || !v8 || !sv || !sel || !o || !lse) return REF_EINVAL;
     for (int64_t r = 0; r < nsel; r++)
@@ -751,8 +752,9 @@ int attn_ref_rows_mxfp8_f64(const uint8_t *q8, const uint8_t *sq, const uint8_t 
                 const uint8_t *qi = q8 + (bh * Nq + i) * d, *qs = sq + (bh * Nq + i) * db;
                 const uint8_t *kh = k8 + bh * Nk * d, *ks = sk + bh * Nk * db;
                 const uint8_t *vh = v8 + bh * Nk * dv, *vs = sv + bh * kb * dv;
+                const int64_t nk = causal ? i + (Nk - Nq) + 1 : Nk;   /* the row's keys */
                 /* step 1 on the real inputs */
-                for (int64_t j = 0; j < Nk; j++) {
+                for (int64_t j = 0; j < nk; j++) {
                     double dot = 0.0;
                     for (int64_t c = 0; c < d; c++)
                         dot += (e8m0_to_f64(qs[c / 32]) * e4m3_to_f64(qi[c])) *
@@ -760,11 +762,11 @@ int attn_ref_rows_mxfp8_f64(const uint8_t *q8, const uint8_t *sq, const uint8_t 
                     sc[j] = scale * dot;
                 }
                 /* steps 2-5 with the real values */
-                double top = row_max(sc, Nk);
-                double den = row_exp_sum(sc, Nk, top);
+                double top = row_max(sc, nk);
+                double den = row_exp_sum(sc, nk, top);
                 for (int64_t c = 0; c < dv; c++) {
                     double num = 0.0;
-                    for (int64_t j = 0; j < Nk; j++)
+                    for (int64_t j = 0; j < nk; j++)
                         num += sc[j] * (e8m0_to_f64(vs[(j / 32) * dv + c]) * e4m3_to_f64(vh[j * dv + c]));
                     o[r * dv + c] = num / den;
                 }
@@ -774,4 +776,24 @@ int attn_ref_rows_mxfp8_f64(const uint8_t *q8, const uint8_t *sq, const uint8_t 
         }
     }
     return failed ? REF_ENOMEM : REF_OK;
+}
+
+int attn_ref_rows_mxfp8_f64(const uint8_t *q8, const uint8_t *sq, const uint8_t *k8, const uint8_t *sk,
+                            const uint8_t *v8, const uint8_t *sv,
+                            int64_t BH, int64_t Nq, int64_t Nk, int64_t d, int64_t dv, double scale,
+                            const int64_t *sel, int64_t nsel, double *o, double *lse, int nthreads)
+{
+    return rows_mxfp8(q8, sq, k8, sk, v8, sv, BH, Nq, Nk, d, dv, scale, sel, nsel, o, lse, nthreads, 0);
+}
+
+/*
+ * attn_ref_rows_mxfp8_causal_f64: attn_ref_rows_mxfp8_f64 under the causal mask of
+ * attn_ref_rows_causal_f64 (row i uses keys 0 .. i + (Nk - Nq) only; needs Nq <= Nk).
+ */
+int attn_ref_rows_mxfp8_causal_f64(const uint8_t *q8, const uint8_t *sq, const uint8_t *k8, const uint8_t *sk,
+                                   const uint8_t *v8, const uint8_t *sv,
+                                   int64_t BH, int64_t Nq, int64_t Nk, int64_t d, int64_t dv, double scale,
+                                   const int64_t *sel, int64_t nsel, double *o, double *lse, int nthreads)
+{
+    return rows_mxfp8(q8, sq, k8, sk, v8, sv, BH, Nq, Nk, d, dv, scale, sel, nsel, o, lse, nthreads, 1);
 }

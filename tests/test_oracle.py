@@ -639,6 +639,31 @@ def pin_mxfp8_with_uniform_scales_is_per_tensor_fp8(orc):
     assert np.max(np.abs(om - oe)) < 1e-13 and np.max(np.abs(lm - le)) < 1e-13
 
 
+def pin_mxfp8_causal_equals_the_bf16_causal_oracle_on_the_scaled_values(orc):
+    # the MXFP8 oracle under the mask is the (pinned) BF16 causal oracle on the block-scaled
+    # values; Nq < Nk and a partial last key block of V's scales
+    from dense_attention_forward_fwd_gb300.inputs import make_qkv_mxfp8
+    q8, sq, k8, sk, v8, sv = make_qkv_mxfp8(1, 2, 9, 70, d=64, seed=78, qk_mult=2.0)
+    rng = np.random.default_rng(79)
+    sq, sk, sv = (np.ascontiguousarray(x + rng.integers(-3, 4, size=x.shape)).astype(np.uint8) for x in (sq, sk, sv))
+    qb, kb, vb = (bf16(_mx_real(orc, c, sc, ax)) for c, sc, ax in ((q8, sq, 3), (k8, sk, 3), (v8, sv, 2)))
+    om, lm = orc.attention_rows_mxfp8(q8, sq, k8, sk, v8, sv, 0.3, causal=True)
+    ob, lb = orc.attention_rows_causal(qb, kb, vb, 0.3)
+    assert np.max(np.abs(om - ob)) < 1e-12 * max(1.0, np.max(np.abs(ob)))
+    assert np.max(np.abs(lm - lb)) < 1e-12 * np.max(np.abs(lb))
+
+
+def pin_mxfp8_causal_rows_are_the_unmasked_rows_over_the_visible_prefix(orc):
+    from dense_attention_forward_fwd_gb300.inputs import make_qkv_mxfp8
+    q8, sq, k8, sk, v8, sv = make_qkv_mxfp8(1, 1, 5, 64, d=32, seed=80)
+    om, lm = orc.attention_rows_mxfp8(q8, sq, k8, sk, v8, sv, 0.25, causal=True)
+    for i in range(5):
+        n = i + 64 - 5 + 1   # a prefix of whole 32-key blocks plus part of the next: V's scales still apply
+        op, lp = orc.attention_rows_mxfp8(q8[:, :, i:i + 1], sq[:, :, i:i + 1], k8[:, :, :n], sk[:, :, :n],
+                                          v8[:, :, :n], np.ascontiguousarray(sv[:, :, :(n + 31) // 32]), 0.25)
+        assert np.array_equal(om[i], op[0]) and lm[i] == lp[0]
+
+
 PINS = [v for k_, v in sorted(globals().items()) if k_.startswith("pin_")]
 
 

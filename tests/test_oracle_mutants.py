@@ -60,6 +60,8 @@ MUTANTS = {
                                        "const int64_t nk = causal ? i + (Nk - Nq) + (i > 0) : Nk;"),
     "e4m3 causal mask aligned top-left": ("const int64_t nk = causal ? i + (Nk - Nq) + 1 : Nk;",
                                           "const int64_t nk = causal ? i + 1 : Nk;"),
+    "e4m3-value and mx causal masks ignored": ("const int64_t nk = causal ? i + (Nk - Nq) + 1 : Nk;   /* the row's keys */\n                /* step 1 on the real inputs */\n                for (int64_t j = 0; j < nk; j++) {\n                    double dot",
+                               "const int64_t nk = Nk;\n                /* step 1 on the real inputs */\n                for (int64_t j = 0; j < nk; j++) {\n                    double dot"),
     "causal dense forward one key short": ("const int64_t nv = causal ? i + (Nk - Nq) + 1 : Nk;",
                                            "const int64_t nv = causal ? i + (Nk - Nq) + (i > 0) : Nk;"),
 }
