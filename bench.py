@@ -98,8 +98,6 @@ def parse():
         ap.error("--head-dim 192 / 256 has the BF16 forward entry points only (attn_fwd, attn_fwd_causal)")
     if (args.fp8_qk or args.fp8 or args.mxfp8) and (args.backward or args.bias != "none"):
         ap.error("--fp8-qk, --fp8 and --mxfp8 have no bias or backward entry point")
-    if args.mxfp8 and args.causal:
-        ap.error("--mxfp8 has no causal entry point (--fp8-qk and --fp8 have)")
     if args.fp8_qk + args.fp8 + args.mxfp8 > 1:
         ap.error("--fp8-qk, --fp8 and --mxfp8 are different entry points; pick one")
     if args.bias != "none" and (args.causal or args.backward):
@@ -264,7 +262,8 @@ def oracle_rows_fn(oracle, w, causal: bool, bias_kind: str, H1: int, nq: int, fp
     if mxfp8:   # Q, K and V of the same draw in MXFP8
         from dense_attention_forward_fwd_gb300.inputs import make_qkv_mxfp8
         q8, sq, k8, sk, v8, sv = make_qkv_mxfp8(1, H1, nq, w.Nk, d=w.d, seed=w.seed, qk_mult=w.qk_mult)
-        return lambda q, k, v, scale, rows: oracle.attention_rows_mxfp8(q8, sq, k8, sk, v8, sv, scale, rows)
+        return lambda q, k, v, scale, rows: oracle.attention_rows_mxfp8(q8, sq, k8, sk, v8, sv, scale, rows,
+                                                                        causal=causal)
     if fp8:   # Q, K and V of the same draw as E4M3 codes
         from dense_attention_forward_fwd_gb300.inputs import make_qkv_e4m3
         q8, k8, v8, dq, dk, dv = make_qkv_e4m3(1, H1, nq, w.Nk, d=w.d, seed=w.seed, qk_mult=w.qk_mult)
@@ -494,7 +493,7 @@ def run_ours(args, w):
             attn.attn_fwd_fp8qk(*ins_, *outs_, w.B, w.H, w.Nq, w.Nk, w.d, w.scale, descale[0], descale[1], st,
                                 causal=args.causal)
         elif args.mxfp8:
-            attn.attn_fwd_mxfp8(*ins_, *outs_, w.B, w.H, w.Nq, w.Nk, w.d, w.scale, st)
+            attn.attn_fwd_mxfp8(*ins_, *outs_, w.B, w.H, w.Nq, w.Nk, w.d, w.scale, st, causal=args.causal)
         elif args.fp8:
             attn.attn_fwd_fp8(*ins_, *outs_, w.B, w.H, w.Nq, w.Nk, w.d, w.scale, descale[0], descale[1], descale[2],
                               st, causal=args.causal)

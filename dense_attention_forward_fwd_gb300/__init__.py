@@ -63,6 +63,8 @@ def load_library(build_if_stale: bool = True) -> ctypes.CDLL:
             lib.attn_fwd_mxfp8.argtypes = [vp, vp, vp, vp, vp, ctypes.c_longlong, vp, ctypes.c_longlong, vp, vp, i32, i32,
                                            i32, i32, i32, f32, vp]
             lib.attn_fwd_mxfp8.restype = i32
+            lib.attn_fwd_mxfp8_causal.argtypes = lib.attn_fwd_mxfp8.argtypes
+            lib.attn_fwd_mxfp8_causal.restype = i32
             i64 = ctypes.c_longlong
             lib.attn_fwd_bias.argtypes = [vp, vp, vp, vp, i64, i64, i64, vp, vp, i32, i32, i32, i32, i32, f32, vp]
             lib.attn_fwd_noalloc.restype = i32
@@ -206,12 +208,12 @@ def attn_fwd_fp8(q8, k8, vt8, o, lse, B: int, H: int, Nq: int, Nk: int, d: int, 
 
 
 def attn_fwd_mxfp8(q8, sq, k8, sk, vt8, svt, o, lse, B: int, H: int, Nq: int, Nk: int, d: int, scale: float,
-                   stream=None, ldv: int | None = None, ldsv: int | None = None) -> None:
+                   stream=None, ldv: int | None = None, ldsv: int | None = None, causal: bool = False) -> None:
     """Attention from MXFP8 inputs (see include/attn_fwd.h): E4M3 codes q8 [B,H,Nq,d] and
     k8 [B,H,Nk,d] with E8M0 scales sq [B,H,Nq,d/32] and sk [B,H,Nk,d/32] (32 elements along
     d), V transposed as codes vt8 [B,H,d,ldv] (keys innermost) with scales svt [B,H,d,ldsv]
     (byte t of a row: keys 32t .. 32t+31). A tensor's last dimension is taken as ldv / ldsv.
-    O (BF16) and LSE (FP32) as in attn_fwd."""
+    O (BF16) and LSE (FP32) as in attn_fwd. causal: under the causal mask (attn_fwd_mxfp8_causal)."""
     lib = load_library()
     for name, t, want in (("vt8", vt8, (B, H, d)), ("svt", svt, (B, H, d))):
         if _is_tensor(t) and (t.dim() != 4 or tuple(t.shape[:3]) != want):
@@ -228,10 +230,10 @@ def attn_fwd_mxfp8(q8, sq, k8, sk, vt8, svt, o, lse, B: int, H: int, Nq: int, Nk
         _ptr(vt8, "vt8", B * H * d * ldv, "e4m3"), int(ldv), _ptr(svt, "svt", B * H * d * ldsv, "e4m3"), int(ldsv),
         _ptr(o, "o", B * H * Nq * d, "bf16"), _ptr(lse, "lse", B * H * Nq, "f32"),
     )
-    rc = lib.attn_fwd_mxfp8(*args, int(B), int(H), int(Nq), int(Nk), int(d), float(scale),
-                            _stream_handle(stream, q8, k8, vt8, o, lse))
+    fn = lib.attn_fwd_mxfp8_causal if causal else lib.attn_fwd_mxfp8
+    rc = fn(*args, int(B), int(H), int(Nq), int(Nk), int(d), float(scale), _stream_handle(stream, q8, k8, vt8, o, lse))
     if rc != ATTN_OK:
-        raise AttnError(rc, "attn_fwd_mxfp8")
+        raise AttnError(rc, "attn_fwd_mxfp8_causal" if causal else "attn_fwd_mxfp8")
 
 
 def attn_fwd_bias(q, k, v, bias, o, lse, B: int, H: int, Nq: int, Nk: int, d: int, scale: float, stream=None,

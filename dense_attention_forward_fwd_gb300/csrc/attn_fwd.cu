@@ -1611,6 +1611,30 @@ struct MxArg {
   long long ldsv;
 };
 
+// The 8-bit entry points' own argument rules (f8 as forward's).
+int check_f8_args(int f8, long long ldv, const MxArg* mx, int Nk, long long bh) {
+  if (f8 >= 2) {
+    // V^T rows of ldv bytes: at least Nk, 16-byte multiples (TMA strides), and the last
+    // byte's offset, bh * 128 * ldv, must fit a signed 64-bit offset
+    if (ldv < Nk) return ATTN_ERR_INVALID_ARG;
+    if (ldv % 16 != 0) return ATTN_ERR_MISALIGNED;
+    if (bh > (LLONG_MAX / kD) / ldv) return ATTN_ERR_INVALID_ARG;
+  }
+  if (f8 == 3) {
+    // scale rows: 4 bytes per Q or K row (read as words); V^T scale rows of ldsv bytes, a
+    // word per key tile of 128, so at least 4 * ceil(Nk / 128) bytes (those past the last
+    // key block are read and replaced by 2^0)
+    if (mx == nullptr || !mx->sq || !mx->sk || !mx->svt) return ATTN_ERR_INVALID_ARG;
+    const long long n_kv = (static_cast<long long>(Nk) + kBN - 1) / kBN;
+    if (mx->ldsv < 4 * n_kv) return ATTN_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(mx->sq) | reinterpret_cast<uintptr_t>(mx->sk) |
+         reinterpret_cast<uintptr_t>(mx->svt)) & 3u || mx->ldsv % 16 != 0)
+      return ATTN_ERR_MISALIGNED;
+    if (bh > (LLONG_MAX / kD) / mx->ldsv) return ATTN_ERR_INVALID_ARG;
+  }
+  return ATTN_OK;
+}
+
 // attn_fwd, attn_fwd_bias (bias != nullptr), attn_fwd_fp8qk (f8 = 1: q and k hold FP8 E4M3
 // codes), attn_fwd_fp8 (f8 = 2: v too, as V^T with row stride ldv, descaled by v_scale) and
 // attn_fwd_o32 (o32 != nullptr: O in FP32 there, o unused): the argument rules, the plan,
@@ -1637,25 +1661,7 @@ int forward(const void* q, const void* k, const void* v, const BiasArg* bias, vo
   // element counts must fit a signed 64-bit byte offset
   const long long max_rows = static_cast<long long>(Nq > Nk ? Nq : Nk);
   if (bh > (LLONG_MAX / 256) / max_rows) return ATTN_ERR_INVALID_ARG;
-  if (f8 >= 2) {
-    // V^T rows of ldv bytes: at least Nk, 16-byte multiples (TMA strides), and the last
-    // byte's offset, bh * 128 * ldv, must fit a signed 64-bit offset
-    if (ldv < Nk) return ATTN_ERR_INVALID_ARG;
-    if (ldv % 16 != 0) return ATTN_ERR_MISALIGNED;
-    if (bh > (LLONG_MAX / kD) / ldv) return ATTN_ERR_INVALID_ARG;
-  }
-  if (f8 == 3) {
-    // scale rows: 4 bytes per Q or K row (read as words); V^T scale rows of ldsv bytes, a
-    // word per key tile of 128, so at least 4 * ceil(Nk / 128) bytes (those past the last
-    // key block are read and replaced by 2^0)
-    if (mx == nullptr || !mx->sq || !mx->sk || !mx->svt) return ATTN_ERR_INVALID_ARG;
-    const long long n_kv = (static_cast<long long>(Nk) + kBN - 1) / kBN;
-    if (mx->ldsv < 4 * n_kv) return ATTN_ERR_INVALID_ARG;
-    if ((reinterpret_cast<uintptr_t>(mx->sq) | reinterpret_cast<uintptr_t>(mx->sk) |
-         reinterpret_cast<uintptr_t>(mx->svt)) & 3u || mx->ldsv % 16 != 0)
-      return ATTN_ERR_MISALIGNED;
-    if (bh > (LLONG_MAX / kD) / mx->ldsv) return ATTN_ERR_INVALID_ARG;
-  }
+  if (const int rc = check_f8_args(f8, ldv, mx, Nk, bh); rc != ATTN_OK) return rc;
   if (bias != nullptr) {
     if (!bias->ptr || bias->sb < 0 || bias->sh < 0 || bias->sq < 0) return ATTN_ERR_INVALID_ARG;
     // the last element's offset, (B-1) sb + (H-1) sh + (Nq-1) sq + Nk - 1, in bytes must fit int64
@@ -1821,10 +1827,11 @@ extern "C" int attn_fwd_mxfp8(const void* q8, const void* sq, const void* k8, co
 namespace {
 // The causal launches: whole (b, h, 256-row) groups, longest first, each over the key tiles
 // its rows can see (the causal order of SegIter): no workspace, no merge. f8: 0 BF16 inputs,
-// 1 Q and K as E4M3 codes, 2 V too (V^T rows of ldv bytes, v_scale its descale factor);
-// scale already holds any Q and K descale factors.
+// 1 Q and K as E4M3 codes, 2 V too (V^T rows of ldv bytes, v_scale its descale factor),
+// 3 MXFP8 (mx: the block scales); scale already holds any Q and K descale factors.
 int forward_causal(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Nq, int Nk,
-                   int d, float scale, void* stream, int f8 = 0, long long ldv = 0, float v_scale = 1.0f) {
+                   int d, float scale, void* stream, int f8 = 0, long long ldv = 0, float v_scale = 1.0f,
+                   const MxArg* mx = nullptr) {
   // the argument rules of attn_fwd, plus Nq <= Nk (every query row sees at least one key)
   if (B < 0 || H < 0 || Nq < 0 || Nk < 0) return ATTN_ERR_INVALID_ARG;
   if (d != kD) return ATTN_ERR_UNSUPPORTED;
@@ -1842,11 +1849,7 @@ int forward_causal(const void* q, const void* k, const void* v, void* o, float* 
   if (bh > INT_MAX || bh * q_groups > INT_MAX) return ATTN_ERR_UNSUPPORTED;
   const long long max_rows = static_cast<long long>(Nk);
   if (bh > (LLONG_MAX / 256) / max_rows) return ATTN_ERR_INVALID_ARG;
-  if (f8 >= 2) {   // V^T rows: as attn_fwd_fp8
-    if (ldv < Nk) return ATTN_ERR_INVALID_ARG;
-    if (ldv % 16 != 0) return ATTN_ERR_MISALIGNED;
-    if (bh > (LLONG_MAX / kD) / ldv) return ATTN_ERR_INVALID_ARG;
-  }
+  if (const int rc = check_f8_args(f8, ldv, mx, Nk, bh); rc != ATTN_OK) return rc;
 
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return ATTN_ERR_CUDA;
@@ -1884,8 +1887,17 @@ int forward_causal(const void* q, const void* k, const void* v, void* o, float* 
   p.H = H;
   p.scale = scale;
   p.v_scale = v_scale;
+  if (mx != nullptr) {
+    p.sfq = static_cast<const uint32_t*>(mx->sq);
+    p.sfk = static_cast<const uint32_t*>(mx->sk);
+    p.sfv = static_cast<const uint8_t*>(mx->svt);
+    p.ldsv = mx->ldsv;
+  }
   const int grid = static_cast<int>(n_groups < sms ? n_groups : sms);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (f8 == 3)
+    return scale > 0.0f ? launch<true, false, 3>(mq, mk, mv, p, grid, dev, s)
+                        : launch<false, false, 3>(mq, mk, mv, p, grid, dev, s);
   if (f8 == 2)
     return scale > 0.0f ? launch<true, false, 2>(mq, mk, mv, p, grid, dev, s)
                         : launch<false, false, 2>(mq, mk, mv, p, grid, dev, s);
@@ -1929,6 +1941,13 @@ extern "C" int attn_fwd_fp8_causal(const void* q8, const void* k8, const void* v
   const float eff = fp8_scale(scale, q_descale, k_descale, v_descale, &rc);
   if (rc != ATTN_OK) return rc;
   return forward_causal(q8, k8, vt8, o, lse, B, H, Nq, Nk, d, eff, stream, 2, ldv, v_descale);
+}
+extern "C" int attn_fwd_mxfp8_causal(const void* q8, const void* sq, const void* k8, const void* sk,
+                                     const void* vt8, long long ldv, const void* svt, long long ldsv, void* o,
+                                     float* lse, int B, int H, int Nq, int Nk, int d, float scale, void* stream) {
+  if (!std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
+  const MxArg mx = {sq, sk, svt, ldsv};
+  return forward_causal(q8, k8, vt8, o, lse, B, H, Nq, Nk, d, scale, stream, 3, ldv, 1.0f, &mx);
 }
 
 extern "C" int attn_fwd_status(void* stream) {

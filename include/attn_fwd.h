@@ -240,6 +240,16 @@ int attn_fwd_mxfp8(const void* q8, const void* sq, const void* k8, const void* s
                    float scale, void* stream);
 
 /*
+ * attn_fwd_mxfp8_causal -- attn_fwd_mxfp8 under the causal mask of attn_fwd_causal (query i
+ * sees keys 0 .. i + Nk - Nq). Arguments, layouts, accuracy and return values are those of
+ * attn_fwd_mxfp8, plus attn_fwd_causal's rules (Nq <= Nk, LSE over the visible keys only, no
+ * allocation).
+ */
+int attn_fwd_mxfp8_causal(const void* q8, const void* sq, const void* k8, const void* sk, const void* vt8,
+                          long long ldv, const void* svt, long long ldsv, void* o, float* lse, int B, int H,
+                          int Nq, int Nk, int d, float scale, void* stream);
+
+/*
  * attn_fwd_o32 -- attn_fwd with O written in FP32, before its rounding to BF16.
  *
  * A diagnostic of the computation itself. The notes state that the tiled computation

@@ -27,7 +27,7 @@ def declared_functions():
 def test_header_declares_the_entry_points():
     names = declared_functions()
     assert {"attn_fwd", "attn_fwd_causal", "attn_fwd_bias", "attn_fwd_fp8qk", "attn_fwd_fp8", "attn_fwd_o32", "attn_fwd_noalloc", "attn_bwd", "attn_bwd_causal",
-            "attn_fwd_fp8qk_causal", "attn_fwd_fp8_causal", "attn_fwd_mxfp8",
+            "attn_fwd_fp8qk_causal", "attn_fwd_fp8_causal", "attn_fwd_mxfp8", "attn_fwd_mxfp8_causal",
             "attn_bwd_status", "attn_bwd_set_wait_limit",
             "attn_bwd_kernel_count", "attn_fwd_status", "attn_status_string",
             "attn_fwd_set_wait_limit", "attn_fwd_kernel_count"} <= set(names)
@@ -223,6 +223,42 @@ def call_fp8pv(q8=A, k8=A, vt8=A, ldv=128, o=A, lse=A, B=1, H=1, Nq=128, Nk=128,
 def test_fp8_argument_checks(kw, code, causal):
     before = attn.attn_fwd_kernel_count()
     assert call_fp8pv(causal=causal, **kw) == code
+    assert attn.attn_fwd_kernel_count() == before
+
+
+def call_mx(q8=A, sq=A, k8=A, sk=A, vt8=A, ldv=128, svt=A, ldsv=16, o=A, lse=A, B=1, H=1, Nq=128, Nk=128, d=128,
+            scale=0.125, causal=False):
+    lib = attn.load_library()
+    fn = lib.attn_fwd_mxfp8_causal if causal else lib.attn_fwd_mxfp8
+    return fn(q8, sq, k8, sk, vt8, ldv, svt, ldsv, o, lse, B, H, Nq, Nk, d, scale, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(sq=None), attn.ATTN_ERR_INVALID_ARG),
+    (dict(sk=None), attn.ATTN_ERR_INVALID_ARG),
+    (dict(svt=None), attn.ATTN_ERR_INVALID_ARG),
+    (dict(sq=A + 2), attn.ATTN_ERR_MISALIGNED),              # scale rows are read as words
+    (dict(ldsv=0), attn.ATTN_ERR_INVALID_ARG),               # under 4 bytes per key tile
+    (dict(ldsv=8), attn.ATTN_ERR_MISALIGNED),                # not a 16-byte multiple
+    (dict(ldsv=16, Nk=640, ldv=640), attn.ATTN_ERR_INVALID_ARG),   # 5 key tiles need 20 bytes
+    (dict(ldsv=24, Nk=640, ldv=640), attn.ATTN_ERR_MISALIGNED),
+    (dict(ldv=120), attn.ATTN_ERR_INVALID_ARG),
+    (dict(vt8=A + 8), attn.ATTN_ERR_MISALIGNED),
+    (dict(scale=math.nan), attn.ATTN_ERR_INVALID_ARG),
+    (dict(d=256), attn.ATTN_ERR_UNSUPPORTED),
+    (dict(Nk=0), attn.ATTN_ERR_INVALID_ARG),
+    (dict(B=0), attn.ATTN_OK),
+])
+@pytest.mark.parametrize("causal", [False, True])
+def test_mxfp8_argument_checks(kw, code, causal):
+    before = attn.attn_fwd_kernel_count()
+    assert call_mx(causal=causal, **kw) == code
+    assert attn.attn_fwd_kernel_count() == before
+
+
+def test_mxfp8_causal_rejects_more_queries_than_keys():
+    before = attn.attn_fwd_kernel_count()
+    assert call_mx(Nq=129, Nk=128, causal=True) == attn.ATTN_ERR_INVALID_ARG
     assert attn.attn_fwd_kernel_count() == before
 
 

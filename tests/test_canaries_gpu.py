@@ -11,7 +11,8 @@ import numpy as np
 import pytest
 
 from canary import fully_written, guarded, intact
-from dense_attention_forward_fwd_gb300.inputs import make_bias, make_qk_e4m3, make_qkv, make_qkv_e4m3
+from dense_attention_forward_fwd_gb300.inputs import (make_bias, make_qk_e4m3, make_qkv, make_qkv_e4m3, make_qkv_mxfp8,
+                                                      mx_value_layout)
 from parity import to_device
 
 pytestmark = pytest.mark.gpu
@@ -88,6 +89,21 @@ def test_fp8_entry_points(gpu_lib, B, H, Nq, Nk):
         gpu_lib.attn_fwd_fp8(torch.from_numpy(q8).cuda(), torch.from_numpy(k8).cuda(), torch.from_numpy(vt).cuda(), o,
                              lse, B, H, Nq, Nk, 128, SCALE, dq, dk, dv, causal=True)
         check(gpu_lib, ((fo, o), "bf16"), ((fl, lse), "f32"))
+
+
+@pytest.mark.parametrize("B,H,Nq,Nk", SHAPES)
+@pytest.mark.parametrize("causal", [False, True])
+def test_mxfp8_entry_points(gpu_lib, B, H, Nq, Nk, causal):
+    import torch
+    if causal and Nq > Nk:
+        pytest.skip("the causal mask needs Nq <= Nk")
+    q8, sq, k8, sk, v8, sv = make_qkv_mxfp8(B, H, Nq, Nk, seed=17500 + Nq + Nk)
+    vt8, svt = mx_value_layout(v8, sv)
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    (fo, o), (fl, lse) = outputs(B, H, Nq)
+    gpu_lib.attn_fwd_mxfp8(dev(q8), dev(sq), dev(k8), dev(sk), dev(vt8), dev(svt), o, lse, B, H, Nq, Nk, 128, SCALE,
+                           causal=causal)
+    check(gpu_lib, ((fo, o), "bf16"), ((fl, lse), "f32"))
 
 
 @pytest.mark.parametrize("B,H,Nq,Nk", SHAPES)

@@ -13,12 +13,15 @@ N(0,1) and peaked (x3) inputs of the shapes the GPU tests use. Under the causal 
 (attn_fwd_fp8_causal) rows near the diagonal average over few keys, so one weight's E4M3
 rounding weighs more in their O: the emulation with the mask gives up to 3.6e-2 (max) and
 3.6e-3 (mean) on N(0,1) inputs, and the causal GPU tests take their own bounds (CAUSAL_BOUNDS).
+attn_fwd_mxfp8 rounds P the same way (E4M3 under a block scale of 2^0) and its products of
+scaled E4M3 values are exact, so the same emulation on the decoded MXFP8 values (with a V
+descale of 1) gives its error too; the last test checks the MXFP8 GPU tests' inputs.
 """
 import numpy as np
 import pytest
 
 import oracle
-from dense_attention_forward_fwd_gb300.inputs import make_qkv_e4m3
+from dense_attention_forward_fwd_gb300.inputs import make_qkv_e4m3, make_qkv_mxfp8
 
 torch = pytest.importorskip("torch")
 
@@ -108,3 +111,35 @@ def test_the_emulation_without_p_rounding_matches_the_definition():
     finally:
         to_e4m3 = keep
     assert np.abs(o - o_ref).max() <= 1e-2 and np.abs(o - o_ref).mean() <= 1e-3
+
+
+def mx_decode(codes, scales, axis):
+    """E4M3 codes times their E8M0 block scales, the blocks of 32 along `axis`."""
+    n = codes.shape[axis]
+    f = np.repeat(oracle.e8m0_to_f64(scales), 32, axis=axis)
+    return oracle.e4m3_to_f64(codes) * np.take(f, np.arange(n), axis=axis)
+
+
+@pytest.mark.parametrize("B,H,Nq,Nk,qk_mult,seed,causal", [
+    (1, 2, 256, 384, 1.0, 15640, False),
+    (4, 2, 768, 768, 1.0, 16536, False),
+    (1, 2, 512, 2048, 3.0, 15100, False),
+    # the causal MXFP8 GPU tests' inputs (tests/test_mxfp8_gpu.py)
+    (1, 1, 128, 128, 1.0, 19256, True),
+    (1, 2, 256, 384, 1.0, 19640, True),
+    (2, 3, 300, 1000, 1.0, 20300, True),
+    (1, 2, 129, 129, 1.0, 19258, True),
+    (1, 2, 1000, 1000, 1.0, 21000, True),
+    (1, 2, 512, 1024, 3.0, 19100, True),
+])
+def test_mxfp8_bounds_cover_the_emulated_rounding_error(B, H, Nq, Nk, qk_mult, seed, causal):
+    q8, sq, k8, sk, v8, sv = make_qkv_mxfp8(B, H, Nq, Nk, seed=seed, qk_mult=qk_mult)
+    o_ref, _ = oracle.attention_rows_mxfp8(q8, sq, k8, sk, v8, sv, SCALE, causal=causal)
+    o_ref = o_ref.reshape(B, H, Nq, -1)
+    q, k, v = mx_decode(q8, sq, 3), mx_decode(k8, sk, 3), mx_decode(v8, sv, 2)
+    err = np.stack([np.abs(emulate_head(q[b, h], k[b, h], v[b, h], SCALE, 1.0, causal=causal) - o_ref[b, h])
+                    for b in range(B) for h in range(H)])
+    t_max, t_mean = (CAUSAL_BOUNDS if causal else BOUNDS)[qk_mult]
+    assert err.max() * 1.5 <= t_max, f"emulated max {err.max():.3e} leaves too little margin under {t_max}"
+    assert err.mean() * 1.5 <= t_mean, f"emulated mean {err.mean():.3e} leaves too little margin under {t_mean}"
+    assert err.max() * 20 >= t_max
