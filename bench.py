@@ -142,10 +142,11 @@ def job_tflops(flops_per_rank: float, world: int, ms: float) -> float:
 def kernel_hash(backward: bool = False, wide: bool = False) -> str:
     h = hashlib.sha256()
     csrc = os.path.dirname(KERNEL_SRC)
-    files = ((os.path.join(csrc, "attn_bwd.cu"), os.path.join(ROOT, "include", "attn_bwd.h")) if backward else
-             (os.path.join(csrc, "attn_fwd_wide.cu"), os.path.join(csrc, "tc_sm103.cuh"),
+    shared = os.path.join(csrc, "tc_sm103.cuh")   # the PTX wrappers every kernel file includes
+    files = ((os.path.join(csrc, "attn_bwd.cu"), shared, os.path.join(ROOT, "include", "attn_bwd.h")) if backward else
+             (os.path.join(csrc, "attn_fwd_wide.cu"), os.path.join(csrc, "attn_wide.h"), shared,
               os.path.join(ROOT, "include", "attn_fwd.h")) if wide else
-             (KERNEL_SRC, os.path.join(ROOT, "include", "attn_fwd.h")))
+             (KERNEL_SRC, shared, os.path.join(ROOT, "include", "attn_fwd.h")))
     for f in files:
         h.update(open(f, "rb").read())
     return h.hexdigest()[:16]
