@@ -68,6 +68,13 @@ class Oracle:
         lib.attn_ref_rows_e4m3_f64.restype = ctypes.c_int
         lib.attn_ref_rows_e4m3_causal_f64.argtypes = lib.attn_ref_rows_e4m3_f64.argtypes
         lib.attn_ref_rows_e4m3_causal_f64.restype = ctypes.c_int
+        bias_args = [vp, i64, i64, i64, i64]   # bias, H, sb, sh, sq after the three operands
+        lib.attn_ref_rows_e4m3qk_bias_f64.argtypes = (lib.attn_ref_rows_e4m3qk_f64.argtypes[:3] + bias_args
+                                                      + lib.attn_ref_rows_e4m3qk_f64.argtypes[3:])
+        lib.attn_ref_rows_e4m3qk_bias_f64.restype = ctypes.c_int
+        lib.attn_ref_rows_e4m3_bias_f64.argtypes = (lib.attn_ref_rows_e4m3_f64.argtypes[:3] + bias_args
+                                                    + lib.attn_ref_rows_e4m3_f64.argtypes[3:])
+        lib.attn_ref_rows_e4m3_bias_f64.restype = ctypes.c_int
         lib.attn_ref_rows_mxfp8_f64.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, dbl, vp, i64, vp,
                                                 vp, ctypes.c_int]
         lib.attn_ref_rows_mxfp8_f64.restype = ctypes.c_int
@@ -137,6 +144,16 @@ class Oracle:
             raise ValueError(f"attn_ref_rows_causal_f64 failed with status {rc}")
         return o, lse
 
+    @staticmethod
+    def _bias_strides(bias, B, H, Nq, Nk):
+        """(bias as uint16 [Bb,Hb,Nqb,Nk], sb, sh, sq) for a bias that broadcasts to [B,H,Nq,Nk]."""
+        bias = _u16(bias, 4)
+        Bb, Hb, Nqb, Nkb = bias.shape
+        if Bb not in (1, B) or Hb not in (1, H) or Nqb not in (1, Nq) or Nkb != Nk:
+            raise ValueError(f"bias shape {bias.shape} does not broadcast to {(B, H, Nq, Nk)}")
+        sb, sh, sq = (st // 2 if n > 1 else 0 for st, n in zip(bias.strides[:3], (Bb, Hb, Nqb)))
+        return bias, sb, sh, sq
+
     def attention_rows_bias(self, q, k, v, bias, scale: float, rows=None, nthreads: int = 0):
         """As attention_rows, with the additive bias B: S = scale * Q K^T + B.
 
@@ -173,10 +190,11 @@ class Oracle:
         return out
 
     def attention_rows_e4m3qk(self, q8, k8, v, scale: float, q_descale: float = 1.0, k_descale: float = 1.0,
-                              rows=None, nthreads: int = 0, causal: bool = False):
+                              rows=None, nthreads: int = 0, causal: bool = False, bias=None):
         """As attention_rows with Q and K given as FP8 E4M3 codes (uint8 [B,H,N,d]) and their
         per-tensor descale factors: the scores are scale * (q_descale Q8)(k_descale K8)^T.
-        causal: under the causal mask of attention_rows_causal (needs Nq <= Nk)."""
+        causal: under the causal mask of attention_rows_causal (needs Nq <= Nk). bias: the
+        additive B of attention_rows_bias (same shapes and broadcasting; not with causal)."""
         q8 = np.ascontiguousarray(q8)
         k8 = np.ascontiguousarray(k8)
         if q8.dtype != np.uint8 or k8.dtype != np.uint8:
@@ -191,18 +209,26 @@ class Oracle:
         rows = np.ascontiguousarray(rows, dtype=np.int64)
         o = np.empty((rows.size, dv), dtype=np.float64)
         lse = np.empty(rows.size, dtype=np.float64)
-        fn = self.lib.attn_ref_rows_e4m3qk_causal_f64 if causal else self.lib.attn_ref_rows_e4m3qk_f64
-        rc = fn(_ptr(q8), _ptr(k8), _ptr(v), B * H, Nq, Nk, d, dv, float(scale), float(q_descale), float(k_descale),
-                _ptr(rows), rows.size, _ptr(o), _ptr(lse), int(nthreads))
+        tail = (B * H, Nq, Nk, d, dv, float(scale), float(q_descale), float(k_descale), _ptr(rows), rows.size,
+                _ptr(o), _ptr(lse), int(nthreads))
+        if bias is not None:
+            if causal:
+                raise ValueError("bias and causal together are not supported (put the mask in the bias)")
+            bias, sb, sh, sq = self._bias_strides(bias, B, H, Nq, Nk)
+            rc = self.lib.attn_ref_rows_e4m3qk_bias_f64(_ptr(q8), _ptr(k8), _ptr(v), _ptr(bias), H, sb, sh, sq, *tail)
+        else:
+            fn = self.lib.attn_ref_rows_e4m3qk_causal_f64 if causal else self.lib.attn_ref_rows_e4m3qk_f64
+            rc = fn(_ptr(q8), _ptr(k8), _ptr(v), *tail)
         if rc != 0:
             raise ValueError(f"attn_ref_rows_e4m3qk_f64 failed with status {rc}")
         return o, lse
 
     def attention_rows_e4m3(self, q8, k8, v8, scale: float, q_descale: float = 1.0, k_descale: float = 1.0,
-                            v_descale: float = 1.0, rows=None, nthreads: int = 0, causal: bool = False):
+                            v_descale: float = 1.0, rows=None, nthreads: int = 0, causal: bool = False, bias=None):
         """As attention_rows_e4m3qk with V given as E4M3 codes too (uint8 [B,H,Nk,dv], real
         values v_descale * V8); P is not rounded: this is the definition on the real inputs.
-        causal: under the causal mask of attention_rows_causal (needs Nq <= Nk)."""
+        causal: under the causal mask of attention_rows_causal (needs Nq <= Nk). bias: the
+        additive B of attention_rows_bias (not with causal)."""
         q8, k8, v8 = (np.ascontiguousarray(a) for a in (q8, k8, v8))
         if q8.dtype != np.uint8 or k8.dtype != np.uint8 or v8.dtype != np.uint8:
             raise TypeError("q8, k8 and v8 must be uint8 E4M3 codes")
@@ -215,9 +241,16 @@ class Oracle:
         rows = np.ascontiguousarray(rows, dtype=np.int64)
         o = np.empty((rows.size, dv), dtype=np.float64)
         lse = np.empty(rows.size, dtype=np.float64)
-        fn = self.lib.attn_ref_rows_e4m3_causal_f64 if causal else self.lib.attn_ref_rows_e4m3_f64
-        rc = fn(_ptr(q8), _ptr(k8), _ptr(v8), B * H, Nq, Nk, d, dv, float(scale), float(q_descale),
-                float(k_descale), float(v_descale), _ptr(rows), rows.size, _ptr(o), _ptr(lse), int(nthreads))
+        tail = (B * H, Nq, Nk, d, dv, float(scale), float(q_descale), float(k_descale), float(v_descale),
+                _ptr(rows), rows.size, _ptr(o), _ptr(lse), int(nthreads))
+        if bias is not None:
+            if causal:
+                raise ValueError("bias and causal together are not supported (put the mask in the bias)")
+            bias, sb, sh, sq = self._bias_strides(bias, B, H, Nq, Nk)
+            rc = self.lib.attn_ref_rows_e4m3_bias_f64(_ptr(q8), _ptr(k8), _ptr(v8), _ptr(bias), H, sb, sh, sq, *tail)
+        else:
+            fn = self.lib.attn_ref_rows_e4m3_causal_f64 if causal else self.lib.attn_ref_rows_e4m3_f64
+            rc = fn(_ptr(q8), _ptr(k8), _ptr(v8), *tail)
         if rc != 0:
             raise ValueError(f"attn_ref_rows_e4m3_f64 failed with status {rc}")
         return o, lse
@@ -367,14 +400,14 @@ def e4m3_to_f64(codes):
 
 
 def attention_rows_e4m3qk(q8, k8, v, scale: float, q_descale: float = 1.0, k_descale: float = 1.0, rows=None,
-                          nthreads: int = 0, causal: bool = False):
-    return default().attention_rows_e4m3qk(q8, k8, v, scale, q_descale, k_descale, rows, nthreads, causal)
+                          nthreads: int = 0, causal: bool = False, bias=None):
+    return default().attention_rows_e4m3qk(q8, k8, v, scale, q_descale, k_descale, rows, nthreads, causal, bias)
 
 
 def attention_rows_e4m3(q8, k8, v8, scale: float, q_descale: float = 1.0, k_descale: float = 1.0,
-                        v_descale: float = 1.0, rows=None, nthreads: int = 0, causal: bool = False):
+                        v_descale: float = 1.0, rows=None, nthreads: int = 0, causal: bool = False, bias=None):
     return default().attention_rows_e4m3(q8, k8, v8, scale, q_descale, k_descale, v_descale, rows, nthreads,
-                                         causal)
+                                         causal, bias)
 
 
 def e8m0_to_f64(codes):

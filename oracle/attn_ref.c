@@ -527,9 +527,11 @@ void attn_ref_e4m3_to_f64(const uint8_t *codes, int64_t n, double *out)
 static int rows_e4m3qk(const uint8_t *q8, const uint8_t *k8, const uint16_t *v,
                        int64_t BH, int64_t Nq, int64_t Nk, int64_t d, int64_t dv,
                        double scale, double q_descale, double k_descale,
-                       const int64_t *sel, int64_t nsel, double *o, double *lse, int nthreads, int causal)
+                       const int64_t *sel, int64_t nsel, double *o, double *lse, int nthreads, int causal,
+                       const uint16_t *bias, int64_t H, int64_t sb, int64_t sh, int64_t sq)
 {
     if (BH < 0 || Nq < 0 || Nk < 1 || d < 1 || dv < 1 || nsel < 0 || (causal && Nq > Nk)) return REF_EINVAL;
+    if (bias && (H < 1 || BH % H != 0 || sb < 0 || sh < 0 || sq < 0)) return REF_EINVAL;
     if (nsel == 0) return REF_OK;
     if (!q8 || !k8 || !v || !sel || !o || !lse) return REF_EINVAL;
     for (int64_t r = 0; r < nsel; r++)
@@ -564,6 +566,10 @@ static int rows_e4m3qk(const uint8_t *q8, const uint8_t *k8, const uint16_t *v,
                         acc += (q_descale * e4m3_to_f64(qi[c])) * (k_descale * e4m3_to_f64(kh[j * d + c]));
                     s[j] = scale * acc;
                 }
+                if (bias) {   /* the optional B of the definition, one BF16 row per query */
+                    const uint16_t *brow = bias + (bh / H) * sb + (bh % H) * sh + i * sq;
+                    for (int64_t j = 0; j < nk; j++) s[j] += bf16_to_f64(brow[j]);
+                }
                 /* steps 2-5 with the head's BF16 value rows */
                 const uint16_t *vrows = v + bh * Nk * dv;
                 double *orow = o + r * dv;
@@ -591,9 +597,11 @@ static int rows_e4m3qk(const uint8_t *q8, const uint8_t *k8, const uint16_t *v,
 static int rows_e4m3(const uint8_t *q8, const uint8_t *k8, const uint8_t *v8,
                      int64_t BH, int64_t Nq, int64_t Nk, int64_t d, int64_t dv,
                      double scale, double q_descale, double k_descale, double v_descale,
-                     const int64_t *sel, int64_t nsel, double *o, double *lse, int nthreads, int causal)
+                     const int64_t *sel, int64_t nsel, double *o, double *lse, int nthreads, int causal,
+                     const uint16_t *bias, int64_t H, int64_t sb, int64_t sh, int64_t sq)
 {
     if (BH < 0 || Nq < 0 || Nk < 1 || d < 1 || dv < 1 || nsel < 0 || (causal && Nq > Nk)) return REF_EINVAL;
+    if (bias && (H < 1 || BH % H != 0 || sb < 0 || sh < 0 || sq < 0)) return REF_EINVAL;
     if (nsel == 0) return REF_OK;
     if (!q8 || !k8 || !v8 || !sel || !o || !lse) return REF_EINVAL;
     for (int64_t r = 0; r < nsel; r++)
@@ -628,6 +636,10 @@ static int rows_e4m3(const uint8_t *q8, const uint8_t *k8, const uint8_t *v8,
                         dot += (q_descale * e4m3_to_f64(qrow[c])) * (k_descale * e4m3_to_f64(khead[j * d + c]));
                     w[j] = scale * dot;
                 }
+                if (bias) {   /* the optional B of the definition */
+                    const uint16_t *bq = bias + (bh / H) * sb + (bh % H) * sh + i * sq;
+                    for (int64_t j = 0; j < nk; j++) w[j] += bf16_to_f64(bq[j]);
+                }
                 /* steps 2-5 with the real values v_descale * V8 */
                 double top = row_max(w, nk);
                 double sum = row_exp_sum(w, nk, top);
@@ -650,7 +662,8 @@ int attn_ref_rows_e4m3qk_f64(const uint8_t *q8, const uint8_t *k8, const uint16_
                              double scale, double q_descale, double k_descale,
                              const int64_t *sel, int64_t nsel, double *o, double *lse, int nthreads)
 {
-    return rows_e4m3qk(q8, k8, v, BH, Nq, Nk, d, dv, scale, q_descale, k_descale, sel, nsel, o, lse, nthreads, 0);
+    return rows_e4m3qk(q8, k8, v, BH, Nq, Nk, d, dv, scale, q_descale, k_descale, sel, nsel, o, lse, nthreads, 0,
+                       NULL, 1, 0, 0, 0);
 }
 
 int attn_ref_rows_e4m3_f64(const uint8_t *q8, const uint8_t *k8, const uint8_t *v8,
@@ -659,7 +672,7 @@ int attn_ref_rows_e4m3_f64(const uint8_t *q8, const uint8_t *k8, const uint8_t *
                            const int64_t *sel, int64_t nsel, double *o, double *lse, int nthreads)
 {
     return rows_e4m3(q8, k8, v8, BH, Nq, Nk, d, dv, scale, q_descale, k_descale, v_descale, sel, nsel, o, lse,
-                     nthreads, 0);
+                     nthreads, 0, NULL, 1, 0, 0, 0);
 }
 
 /*
@@ -673,7 +686,8 @@ int attn_ref_rows_e4m3qk_causal_f64(const uint8_t *q8, const uint8_t *k8, const 
                                     double scale, double q_descale, double k_descale,
                                     const int64_t *sel, int64_t nsel, double *o, double *lse, int nthreads)
 {
-    return rows_e4m3qk(q8, k8, v, BH, Nq, Nk, d, dv, scale, q_descale, k_descale, sel, nsel, o, lse, nthreads, 1);
+    return rows_e4m3qk(q8, k8, v, BH, Nq, Nk, d, dv, scale, q_descale, k_descale, sel, nsel, o, lse, nthreads, 1,
+                       NULL, 1, 0, 0, 0);
 }
 
 int attn_ref_rows_e4m3_causal_f64(const uint8_t *q8, const uint8_t *k8, const uint8_t *v8,
@@ -682,7 +696,36 @@ int attn_ref_rows_e4m3_causal_f64(const uint8_t *q8, const uint8_t *k8, const ui
                                   const int64_t *sel, int64_t nsel, double *o, double *lse, int nthreads)
 {
     return rows_e4m3(q8, k8, v8, BH, Nq, Nk, d, dv, scale, q_descale, k_descale, v_descale, sel, nsel, o, lse,
-                     nthreads, 1);
+                     nthreads, 1, NULL, 1, 0, 0, 0);
+}
+
+/*
+ * The two FP8 functions with the definition's optional additive bias B ("FlashAttention'ı
+ * Anlamak Bölüm 1", section 0.2: S = QK^T / sqrt(d) + B) added to each score after the
+ * scale, as attn_ref_rows_bias_f64 adds it: B_ij of head (b, h) = bias[b * sb + h * sh +
+ * i * sq + j] (BF16 bits, strides in elements, 0 repeats), H heads per batch. -inf removes
+ * a key; a row of only -inf has no softmax (NaN). No causal mask (the bias can carry one).
+ */
+int attn_ref_rows_e4m3qk_bias_f64(const uint8_t *q8, const uint8_t *k8, const uint16_t *v,
+                                  const uint16_t *bias, int64_t H, int64_t sb, int64_t sh, int64_t sq,
+                                  int64_t BH, int64_t Nq, int64_t Nk, int64_t d, int64_t dv,
+                                  double scale, double q_descale, double k_descale,
+                                  const int64_t *sel, int64_t nsel, double *o, double *lse, int nthreads)
+{
+    if (!bias) return REF_EINVAL;
+    return rows_e4m3qk(q8, k8, v, BH, Nq, Nk, d, dv, scale, q_descale, k_descale, sel, nsel, o, lse, nthreads, 0,
+                       bias, H, sb, sh, sq);
+}
+
+int attn_ref_rows_e4m3_bias_f64(const uint8_t *q8, const uint8_t *k8, const uint8_t *v8,
+                                const uint16_t *bias, int64_t H, int64_t sb, int64_t sh, int64_t sq,
+                                int64_t BH, int64_t Nq, int64_t Nk, int64_t d, int64_t dv,
+                                double scale, double q_descale, double k_descale, double v_descale,
+                                const int64_t *sel, int64_t nsel, double *o, double *lse, int nthreads)
+{
+    if (!bias) return REF_EINVAL;
+    return rows_e4m3(q8, k8, v8, BH, Nq, Nk, d, dv, scale, q_descale, k_descale, v_descale, sel, nsel, o, lse,
+                     nthreads, 0, bias, H, sb, sh, sq);
 }
 
 /*

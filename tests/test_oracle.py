@@ -599,6 +599,50 @@ def pin_e4m3_causal_rows_are_the_unmasked_rows_over_the_visible_prefix(orc):
             assert np.array_equal(oa[h, i], op[0]) and la[h, i] == lp[0]
 
 
+def pin_e4m3_bias_equals_the_bf16_bias_oracle_on_the_same_values(orc):
+    # with the optional B of the definition ("FlashAttention'ı Anlamak Bölüm 1", 0.2) the
+    # E4M3-score oracle is still the (pinned) BF16 bias oracle on the codes' values: a bias
+    # that differs by batch, head, row and key, and one shared by every head and batch
+    from dense_attention_forward_fwd_gb300.inputs import make_qk_e4m3
+    q8, k8, v, dq, dk = make_qk_e4m3(2, 3, 7, 19, d=16, seed=78, qk_mult=2.0)
+    qb, kb = bf16(orc.e4m3_to_f64(q8)), bf16(orc.e4m3_to_f64(k8))
+    rng = np.random.default_rng(79)
+    for shape in ((2, 3, 7, 19), (1, 1, 7, 19), (2, 1, 1, 19)):
+        bias = f32_to_bf16_bits(rng.normal(0.0, 2.0, size=shape).astype(np.float32))
+        o8, l8 = orc.attention_rows_e4m3qk(q8, k8, v, 0.3, dq, dk, bias=bias)
+        ob, lb = orc.attention_rows_bias(qb, kb, v, bias, 0.3 * dq * dk)
+        assert np.max(np.abs(o8 - ob)) < 1e-12 and np.max(np.abs(l8 - lb)) < 1e-12 * np.max(np.abs(lb))
+
+
+def pin_e4m3_bias_constant_per_row_moves_only_lse(orc):
+    # adding c_i to every score of row i leaves the softmax alone and adds c_i to the LSE, for
+    # both FP8 oracles (a bias row read from the wrong query fails the LSE)
+    from dense_attention_forward_fwd_gb300.inputs import make_qkv_e4m3
+    q8, k8, v8, dq, dk, dv = make_qkv_e4m3(1, 2, 6, 11, d=16, seed=80)
+    vb = bf16(orc.e4m3_to_f64(v8))
+    c = np.array([0.5, -3.0, 2.25, 0.0, 7.5, -0.125], dtype=np.float32)
+    bias = np.ascontiguousarray(np.broadcast_to(bf16(c)[None, None, :, None], (1, 1, 6, 11)))
+    shift = np.tile(c.astype(np.float64), 2)
+    o0, l0 = orc.attention_rows_e4m3qk(q8, k8, vb, 0.4, dq, dk)
+    o1, l1 = orc.attention_rows_e4m3qk(q8, k8, vb, 0.4, dq, dk, bias=bias)
+    assert np.max(np.abs(o1 - o0)) < 1e-13 and np.max(np.abs(l1 - (l0 + shift))) < 1e-12
+    o0, l0 = orc.attention_rows_e4m3(q8, k8, v8, 0.4, dq, dk, dv)
+    o1, l1 = orc.attention_rows_e4m3(q8, k8, v8, 0.4, dq, dk, dv, bias=bias)
+    assert np.max(np.abs(o1 - o0)) < 1e-13 and np.max(np.abs(l1 - (l0 + shift))) < 1e-12
+
+
+def pin_e4m3_values_with_bias_equal_the_scores_only_oracle_times_the_value_descale(orc):
+    # as without a bias: with V as codes, O = v_descale * (the E4M3-score oracle on the codes'
+    # values) under the same per-head bias, and the LSE does not involve V
+    from dense_attention_forward_fwd_gb300.inputs import make_qkv_e4m3
+    q8, k8, v8, dq, dk, dv = make_qkv_e4m3(2, 2, 5, 23, d=16, seed=81, qk_mult=2.0)
+    v8 = np.ascontiguousarray(v8[..., :8])
+    bias = f32_to_bf16_bits(np.random.default_rng(82).normal(size=(2, 2, 5, 23)).astype(np.float32))
+    o8, l8 = orc.attention_rows_e4m3(q8, k8, v8, 0.4, dq, dk, dv, bias=bias)
+    ob, lb = orc.attention_rows_e4m3qk(q8, k8, bf16(orc.e4m3_to_f64(v8)), 0.4, dq, dk, bias=bias)
+    assert np.max(np.abs(o8 - dv * ob)) < 1e-12 * max(1.0, np.max(np.abs(o8))) and np.array_equal(l8, lb)
+
+
 # ---- MXFP8: E4M3 elements with E8M0 scales per 32 elements along each contraction ----------
 
 def pin_e8m0_decoder_closed_forms(orc):

@@ -56,6 +56,15 @@ MUTANTS = {
                                 "(1.0 * e4m3_to_f64(vh[j * dv + c]))"),
     "mx query scales of the first block only": ("(e8m0_to_f64(qs[c / 32]) * e4m3_to_f64(qi[c]))",
                                                 "(e8m0_to_f64(qs[0]) * e4m3_to_f64(qi[c]))"),
+    "e4m3 bias ignored": ("for (int64_t j = 0; j < nk; j++) s[j] += bf16_to_f64(brow[j]);",
+                          "for (int64_t j = 0; j < nk; j++) s[j] += 0.0;"),
+    "e4m3 bias row stride dropped": ("(bh % H) * sh + i * sq;\n                    for (int64_t j = 0; j < nk; j++) s[j]",
+                                     "(bh % H) * sh;\n                    for (int64_t j = 0; j < nk; j++) s[j]"),
+    "e4m3 bias head and batch strides swapped": ("const uint16_t *brow = bias + (bh / H) * sb + (bh % H) * sh",
+                                                 "const uint16_t *brow = bias + (bh / H) * sh + (bh % H) * sb"),
+    "e4m3-value bias ignored": ("for (int64_t j = 0; j < nk; j++) w[j] += bf16_to_f64(bq[j]);",
+                                "for (int64_t j = 0; j < nk; j++) w[j] += 0.0;"),
+    "e4m3-value bias scaled": ("w[j] += bf16_to_f64(bq[j]);", "w[j] += scale * bf16_to_f64(bq[j]);"),
     "e4m3 causal mask one key short": ("const int64_t nk = causal ? i + (Nk - Nq) + 1 : Nk;",
                                        "const int64_t nk = causal ? i + (Nk - Nq) + (i > 0) : Nk;"),
     "e4m3 causal mask aligned top-left": ("const int64_t nk = causal ? i + (Nk - Nq) + 1 : Nk;",
