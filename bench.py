@@ -96,8 +96,10 @@ def parse():
     args = ap.parse_args()
     if args.head_dim != 128 and (args.backward or args.bias != "none" or args.fp8_qk or args.fp8 or args.mxfp8):
         ap.error("--head-dim 192 / 256 has the BF16 forward entry points only (attn_fwd, attn_fwd_causal)")
-    if (args.fp8_qk or args.fp8 or args.mxfp8) and (args.backward or args.bias != "none"):
-        ap.error("--fp8-qk, --fp8 and --mxfp8 have no bias or backward entry point")
+    if (args.fp8_qk or args.fp8 or args.mxfp8) and args.backward:
+        ap.error("--fp8-qk, --fp8 and --mxfp8 have no backward entry point")
+    if args.mxfp8 and args.bias != "none":
+        ap.error("--mxfp8 has no bias entry point (--fp8-qk and --fp8 have)")
     if args.fp8_qk + args.fp8 + args.mxfp8 > 1:
         ap.error("--fp8-qk, --fp8 and --mxfp8 are different entry points; pick one")
     if args.bias != "none" and (args.causal or args.backward):
@@ -265,19 +267,21 @@ def oracle_rows_fn(oracle, w, causal: bool, bias_kind: str, H1: int, nq: int, fp
         q8, sq, k8, sk, v8, sv = make_qkv_mxfp8(1, H1, nq, w.Nk, d=w.d, seed=w.seed, qk_mult=w.qk_mult)
         return lambda q, k, v, scale, rows: oracle.attention_rows_mxfp8(q8, sq, k8, sk, v8, sv, scale, rows,
                                                                         causal=causal)
+    bias = None
+    if bias_kind != "none":
+        from dense_attention_forward_fwd_gb300.inputs import make_bias
+        bias = make_bias((1, 1, nq, w.Nk) if bias_kind == "shared" else (1, H1, nq, w.Nk), seed=w.seed + 1)
     if fp8:   # Q, K and V of the same draw as E4M3 codes
         from dense_attention_forward_fwd_gb300.inputs import make_qkv_e4m3
         q8, k8, v8, dq, dk, dv = make_qkv_e4m3(1, H1, nq, w.Nk, d=w.d, seed=w.seed, qk_mult=w.qk_mult)
         return lambda q, k, v, scale, rows: oracle.attention_rows_e4m3(q8, k8, v8, scale, dq, dk, dv, rows,
-                                                                       causal=causal)
+                                                                       causal=causal, bias=bias)
     if fp8_qk:   # Q and K of the same draw (seed, shape) as E4M3 codes; V is make_qkv's V
         from dense_attention_forward_fwd_gb300.inputs import make_qk_e4m3
         q8, k8, _, dq, dk = make_qk_e4m3(1, H1, nq, w.Nk, d=w.d, seed=w.seed, qk_mult=w.qk_mult)
         return lambda q, k, v, scale, rows: oracle.attention_rows_e4m3qk(q8, k8, v, scale, dq, dk, rows,
-                                                                         causal=causal)
-    if bias_kind != "none":
-        from dense_attention_forward_fwd_gb300.inputs import make_bias
-        bias = make_bias((1, 1, nq, w.Nk) if bias_kind == "shared" else (1, H1, nq, w.Nk), seed=w.seed + 1)
+                                                                         causal=causal, bias=bias)
+    if bias is not None:
         return lambda q, k, v, scale, rows: oracle.attention_rows_bias(q, k, v, bias, scale, rows)
     return oracle.attention_rows_causal if causal else oracle.attention_rows
 
@@ -488,16 +492,16 @@ def run_ours(args, w):
     def call(ins_, outs_, st):
         if args.backward:
             attn.attn_bwd(*ins_, *outs_, w.B, w.H, w.Nq, w.Nk, w.d, w.scale, st, causal=args.causal)
+        elif args.fp8_qk:
+            attn.attn_fwd_fp8qk(*ins_[:3], *outs_, w.B, w.H, w.Nq, w.Nk, w.d, w.scale, descale[0], descale[1], st,
+                                causal=args.causal, bias=ins_[3] if args.bias != "none" else None)
+        elif args.fp8:
+            attn.attn_fwd_fp8(*ins_[:3], *outs_, w.B, w.H, w.Nq, w.Nk, w.d, w.scale, descale[0], descale[1],
+                              descale[2], st, causal=args.causal, bias=ins_[3] if args.bias != "none" else None)
         elif args.bias != "none":
             attn.attn_fwd_bias(ins_[0], ins_[1], ins_[2], ins_[3], *outs_, w.B, w.H, w.Nq, w.Nk, w.d, w.scale, st)
-        elif args.fp8_qk:
-            attn.attn_fwd_fp8qk(*ins_, *outs_, w.B, w.H, w.Nq, w.Nk, w.d, w.scale, descale[0], descale[1], st,
-                                causal=args.causal)
         elif args.mxfp8:
             attn.attn_fwd_mxfp8(*ins_, *outs_, w.B, w.H, w.Nq, w.Nk, w.d, w.scale, st, causal=args.causal)
-        elif args.fp8:
-            attn.attn_fwd_fp8(*ins_, *outs_, w.B, w.H, w.Nq, w.Nk, w.d, w.scale, descale[0], descale[1], descale[2],
-                              st, causal=args.causal)
         elif args.causal:
             attn.attn_fwd_causal(*ins_, *outs_, w.B, w.H, w.Nq, w.Nk, w.d, w.scale, st)
         else:

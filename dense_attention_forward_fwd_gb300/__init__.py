@@ -60,6 +60,13 @@ def load_library(build_if_stale: bool = True) -> ctypes.CDLL:
             lib.attn_fwd_fp8qk_causal.restype = i32
             lib.attn_fwd_fp8_causal.argtypes = lib.attn_fwd_fp8.argtypes
             lib.attn_fwd_fp8_causal.restype = i32
+            ll = ctypes.c_longlong
+            lib.attn_fwd_fp8qk_bias.argtypes = [vp, vp, vp, vp, ll, ll, ll, vp, vp, i32, i32, i32, i32, i32, f32, f32,
+                                                f32, vp]
+            lib.attn_fwd_fp8qk_bias.restype = i32
+            lib.attn_fwd_fp8_bias.argtypes = [vp, vp, vp, ll, vp, ll, ll, ll, vp, vp, i32, i32, i32, i32, i32, f32,
+                                              f32, f32, f32, vp]
+            lib.attn_fwd_fp8_bias.restype = i32
             lib.attn_fwd_mxfp8.argtypes = [vp, vp, vp, vp, vp, ctypes.c_longlong, vp, ctypes.c_longlong, vp, vp, i32, i32,
                                            i32, i32, i32, f32, vp]
             lib.attn_fwd_mxfp8.restype = i32
@@ -163,32 +170,44 @@ def attn_fwd_causal(q, k, v, o, lse, B: int, H: int, Nq: int, Nk: int, d: int, s
 
 
 def attn_fwd_fp8qk(q8, k8, v, o, lse, B: int, H: int, Nq: int, Nk: int, d: int, scale: float,
-                   q_descale: float = 1.0, k_descale: float = 1.0, stream=None, causal: bool = False) -> None:
+                   q_descale: float = 1.0, k_descale: float = 1.0, stream=None, causal: bool = False,
+                   bias=None, bias_strides=None) -> None:
     """Like :func:`attn_fwd`, with Q and K given as FP8 E4M3 codes (torch.float8_e4m3fn or
     uint8 CUDA tensors [B,H,N,d]) and one positive descale factor each:
     S = scale * q_descale * k_descale * (Q8 K8^T); V, O and LSE as in attn_fwd. causal: under
-    the causal mask of attn_fwd_causal (attn_fwd_fp8qk_causal)."""
+    the causal mask of attn_fwd_causal (attn_fwd_fp8qk_causal). bias: the additive bias of
+    :func:`attn_fwd_bias` (attn_fwd_fp8qk_bias; not with causal)."""
     lib = load_library()
+    if bias is not None and causal:
+        raise ValueError("bias and causal together are not supported (put the mask in the bias)")
     args = (
         _ptr(q8, "q8", B * H * Nq * d, "e4m3"), _ptr(k8, "k8", B * H * Nk * d, "e4m3"),
         _ptr(v, "v", B * H * Nk * d, "bf16"), _ptr(o, "o", B * H * Nq * d, "bf16"),
         _ptr(lse, "lse", B * H * Nq, "f32"),
     )
-    fn = lib.attn_fwd_fp8qk_causal if causal else lib.attn_fwd_fp8qk
-    rc = fn(*args, int(B), int(H), int(Nq), int(Nk), int(d), float(scale), float(q_descale), float(k_descale),
+    tail = (int(B), int(H), int(Nq), int(Nk), int(d), float(scale), float(q_descale), float(k_descale),
             _stream_handle(stream, q8, k8, v, o, lse))
+    if bias is not None:
+        name = "attn_fwd_fp8qk_bias"
+        rc = lib.attn_fwd_fp8qk_bias(*args[:3], *_bias_arg(bias, B, H, Nq, Nk, bias_strides), *args[3:], *tail)
+    else:
+        name = "attn_fwd_fp8qk_causal" if causal else "attn_fwd_fp8qk"
+        rc = getattr(lib, name)(*args, *tail)
     if rc != ATTN_OK:
-        raise AttnError(rc, "attn_fwd_fp8qk_causal" if causal else "attn_fwd_fp8qk")
+        raise AttnError(rc, name)
 
 
 def attn_fwd_fp8(q8, k8, vt8, o, lse, B: int, H: int, Nq: int, Nk: int, d: int, scale: float,
                  q_descale: float = 1.0, k_descale: float = 1.0, v_descale: float = 1.0, stream=None,
-                 ldv: int | None = None, causal: bool = False) -> None:
+                 ldv: int | None = None, causal: bool = False, bias=None, bias_strides=None) -> None:
     """Like :func:`attn_fwd_fp8qk`, with V as E4M3 codes too, passed transposed: ``vt8`` is
     [B,H,d,ldv] (keys innermost, ldv >= Nk a multiple of 16; a tensor's last dimension is
     taken as ldv). P is rounded to E4M3 for the P V product (see include/attn_fwd.h for the
-    accuracy this costs). causal: under the causal mask (attn_fwd_fp8_causal)."""
+    accuracy this costs). causal: under the causal mask (attn_fwd_fp8_causal). bias: the
+    additive bias of :func:`attn_fwd_bias` (attn_fwd_fp8_bias; not with causal)."""
     lib = load_library()
+    if bias is not None and causal:
+        raise ValueError("bias and causal together are not supported (put the mask in the bias)")
     if _is_tensor(vt8):
         if vt8.dim() != 4 or tuple(vt8.shape[:3]) != (B, H, d):
             raise ValueError(f"vt8 must be [B, H, d, ldv] = [{B}, {H}, {d}, ldv], got {tuple(vt8.shape)}")
@@ -200,11 +219,16 @@ def attn_fwd_fp8(q8, k8, vt8, o, lse, B: int, H: int, Nq: int, Nk: int, d: int, 
         _ptr(vt8, "vt8", B * H * d * ldv, "e4m3"),
     )
     outs = (_ptr(o, "o", B * H * Nq * d, "bf16"), _ptr(lse, "lse", B * H * Nq, "f32"))
-    fn = lib.attn_fwd_fp8_causal if causal else lib.attn_fwd_fp8
-    rc = fn(*args, int(ldv), *outs, int(B), int(H), int(Nq), int(Nk), int(d), float(scale), float(q_descale),
-            float(k_descale), float(v_descale), _stream_handle(stream, q8, k8, vt8, o, lse))
+    tail = (int(B), int(H), int(Nq), int(Nk), int(d), float(scale), float(q_descale), float(k_descale),
+            float(v_descale), _stream_handle(stream, q8, k8, vt8, o, lse))
+    if bias is not None:
+        name = "attn_fwd_fp8_bias"
+        rc = lib.attn_fwd_fp8_bias(*args, int(ldv), *_bias_arg(bias, B, H, Nq, Nk, bias_strides), *outs, *tail)
+    else:
+        name = "attn_fwd_fp8_causal" if causal else "attn_fwd_fp8"
+        rc = getattr(lib, name)(*args, int(ldv), *outs, *tail)
     if rc != ATTN_OK:
-        raise AttnError(rc, "attn_fwd_fp8_causal" if causal else "attn_fwd_fp8")
+        raise AttnError(rc, name)
 
 
 def attn_fwd_mxfp8(q8, sq, k8, sk, vt8, svt, o, lse, B: int, H: int, Nq: int, Nk: int, d: int, scale: float,
@@ -236,17 +260,8 @@ def attn_fwd_mxfp8(q8, sq, k8, sk, vt8, svt, o, lse, B: int, H: int, Nq: int, Nk
         raise AttnError(rc, "attn_fwd_mxfp8_causal" if causal else "attn_fwd_mxfp8")
 
 
-def attn_fwd_bias(q, k, v, bias, o, lse, B: int, H: int, Nq: int, Nk: int, d: int, scale: float, stream=None,
-                  bias_strides=None) -> None:
-    """Like :func:`attn_fwd`, with an additive bias: S = scale * Q K^T + bias.
-
-    ``bias`` is a BF16 CUDA tensor of shape (Bb, Hb, Nqb, Nk), Bb in {1, B}, Hb in {1, H},
-    Nqb in {1, Nq}, with unit stride over keys; a dimension of size 1 (or of stride 0, as
-    from ``expand``) is shared. Its element strides are passed as they are, or given as
-    ``bias_strides`` = (stride_b, stride_h, stride_q) when ``bias`` is an integer pointer.
-    Entries of -inf remove keys; see include/attn_fwd.h for the rules.
-    """
-    lib = load_library()
+def _bias_arg(bias, B: int, H: int, Nq: int, Nk: int, bias_strides):
+    """(device pointer, stride_b, stride_h, stride_q) of a bias argument (see attn_fwd_bias)."""
     if _is_tensor(bias):
         import torch
         if not bias.is_cuda or bias.dtype != torch.bfloat16:
@@ -266,6 +281,21 @@ def attn_fwd_bias(q, k, v, bias, o, lse, B: int, H: int, Nq: int, Nk: int, d: in
     else:
         raise TypeError(f"bias: expected a torch tensor or an integer device pointer, got {type(bias).__name__}")
     sb, sh, sq = (int(x) for x in bias_strides)
+    return bptr, sb, sh, sq
+
+
+def attn_fwd_bias(q, k, v, bias, o, lse, B: int, H: int, Nq: int, Nk: int, d: int, scale: float, stream=None,
+                  bias_strides=None) -> None:
+    """Like :func:`attn_fwd`, with an additive bias: S = scale * Q K^T + bias.
+
+    ``bias`` is a BF16 CUDA tensor of shape (Bb, Hb, Nqb, Nk), Bb in {1, B}, Hb in {1, H},
+    Nqb in {1, Nq}, with unit stride over keys; a dimension of size 1 (or of stride 0, as
+    from ``expand``) is shared. Its element strides are passed as they are, or given as
+    ``bias_strides`` = (stride_b, stride_h, stride_q) when ``bias`` is an integer pointer.
+    Entries of -inf remove keys; see include/attn_fwd.h for the rules.
+    """
+    lib = load_library()
+    bptr, sb, sh, sq = _bias_arg(bias, B, H, Nq, Nk, bias_strides)
     args = (
         _ptr(q, "q", B * H * Nq * d, "bf16"), _ptr(k, "k", B * H * Nk * d, "bf16"),
         _ptr(v, "v", B * H * Nk * d, "bf16"), bptr, sb, sh, sq, _ptr(o, "o", B * H * Nq * d, "bf16"),

@@ -1733,7 +1733,12 @@ int forward(const void* q, const void* k, const void* v, const BiasArg* bias, vo
     return scale > 0.0f ? launch<true, false, 0, true>(mq, mk, mv, p, pl.grid, dev, s)
                         : launch<false, false, 0, true>(mq, mk, mv, p, pl.grid, dev, s);
   // with a bias the scale is applied before the row max, so one instantiation serves any sign
-  if (bias != nullptr) return launch<true, true>(mq, mk, mv, p, pl.grid, dev, s);
+  if (bias != nullptr) {
+    if (f8 == 2) return launch<true, true, 2>(mq, mk, mv, p, pl.grid, dev, s);
+    if (f8 == 1) return launch<true, true, 1>(mq, mk, mv, p, pl.grid, dev, s);
+    if (f8 != 0) return ATTN_ERR_UNSUPPORTED;
+    return launch<true, true>(mq, mk, mv, p, pl.grid, dev, s);
+  }
   if (f8 == 3)
     return scale > 0.0f ? launch<true, false, 3>(mq, mk, mv, p, pl.grid, dev, s)
                         : launch<false, false, 3>(mq, mk, mv, p, pl.grid, dev, s);
@@ -1941,6 +1946,28 @@ extern "C" int attn_fwd_fp8_causal(const void* q8, const void* k8, const void* v
   const float eff = fp8_scale(scale, q_descale, k_descale, v_descale, &rc);
   if (rc != ATTN_OK) return rc;
   return forward_causal(q8, k8, vt8, o, lse, B, H, Nq, Nk, d, eff, stream, 2, ldv, v_descale);
+}
+extern "C" int attn_fwd_fp8qk_bias(const void* q8, const void* k8, const void* v, const void* bias,
+                                   long long bias_stride_b, long long bias_stride_h, long long bias_stride_q, void* o,
+                                   float* lse, int B, int H, int Nq, int Nk, int d, float scale, float q_descale,
+                                   float k_descale, void* stream) {
+  // S = scale * q_descale * k_descale * (Q8 K8^T) + B: attn_fwd_fp8qk's scores with
+  // attn_fwd_bias's bias, added after the (folded) scale
+  int rc = ATTN_OK;
+  const float eff = fp8_scale(scale, q_descale, k_descale, 1.0f, &rc);
+  if (rc != ATTN_OK) return rc;
+  const BiasArg ba = {bias, bias_stride_b, bias_stride_h, bias_stride_q};
+  return forward(q8, k8, v, &ba, o, lse, B, H, Nq, Nk, d, eff, stream, 1);
+}
+extern "C" int attn_fwd_fp8_bias(const void* q8, const void* k8, const void* vt8, long long ldv, const void* bias,
+                                 long long bias_stride_b, long long bias_stride_h, long long bias_stride_q, void* o,
+                                 float* lse, int B, int H, int Nq, int Nk, int d, float scale, float q_descale,
+                                 float k_descale, float v_descale, void* stream) {
+  int rc = ATTN_OK;
+  const float eff = fp8_scale(scale, q_descale, k_descale, v_descale, &rc);
+  if (rc != ATTN_OK) return rc;
+  const BiasArg ba = {bias, bias_stride_b, bias_stride_h, bias_stride_q};
+  return forward(q8, k8, vt8, &ba, o, lse, B, H, Nq, Nk, d, eff, stream, 2, ldv, v_descale);
 }
 extern "C" int attn_fwd_mxfp8_causal(const void* q8, const void* sq, const void* k8, const void* sk,
                                      const void* vt8, long long ldv, const void* svt, long long ldsv, void* o,

@@ -206,6 +206,23 @@ int attn_fwd_fp8_causal(const void* q8, const void* k8, const void* vt8, long lo
                         float k_descale, float v_descale, void* stream);
 
 /*
+ * attn_fwd_fp8qk_bias, attn_fwd_fp8_bias -- the two FP8 entry points with attn_fwd_bias's
+ * additive bias: S = scale * q_descale * k_descale * (Q8 K8^T) + B, the bias added after the
+ * scale as in attn_fwd_bias (the definition's optional B, "FlashAttention'ı Anlamak Bölüm 1",
+ * section 0.2 Notasyon). Arguments, layouts, accuracy and return values are those of
+ * attn_fwd_fp8qk / attn_fwd_fp8, with bias and its three strides as in attn_fwd_bias (and its
+ * argument checks). Not with the causal mask (a causal bias carries one).
+ */
+int attn_fwd_fp8qk_bias(const void* q8, const void* k8, const void* v, const void* bias,
+                        long long bias_stride_b, long long bias_stride_h, long long bias_stride_q,
+                        void* o, float* lse, int B, int H, int Nq, int Nk, int d, float scale,
+                        float q_descale, float k_descale, void* stream);
+int attn_fwd_fp8_bias(const void* q8, const void* k8, const void* vt8, long long ldv, const void* bias,
+                      long long bias_stride_b, long long bias_stride_h, long long bias_stride_q,
+                      void* o, float* lse, int B, int H, int Nq, int Nk, int d, float scale,
+                      float q_descale, float k_descale, float v_descale, void* stream);
+
+/*
  * attn_fwd_mxfp8 -- attention forward from MXFP8 inputs, both products block-scaled.
  *
  * The "MXFP8 MMA" that "Flash Attention на 5090 в CUDA C++" (section "Что дальше") names as

@@ -45,7 +45,8 @@ def test_reference_arm_prints_the_contract_line(flags):
         assert d["config"]["pass"] == "backward"
 
 
-@pytest.mark.parametrize("flags", [("--mxfp8", "--bias", "full"), ("--fp8-qk", "--bias", "shared"), ("--fp8", "--fp8-qk"),
+@pytest.mark.parametrize("flags", [("--mxfp8", "--bias", "full"), ("--fp8-qk", "--bias", "shared", "--causal"),
+                                   ("--fp8", "--fp8-qk"),
                                    ("--bias", "full", "--backward"), ("--head-dim", "256", "--backward"),
                                    ("--fp8", "--backward")])
 def test_flags_without_an_entry_point_are_refused(flags):

@@ -28,6 +28,7 @@ def test_header_declares_the_entry_points():
     names = declared_functions()
     assert {"attn_fwd", "attn_fwd_causal", "attn_fwd_bias", "attn_fwd_fp8qk", "attn_fwd_fp8", "attn_fwd_o32", "attn_fwd_noalloc", "attn_bwd", "attn_bwd_causal",
             "attn_fwd_fp8qk_causal", "attn_fwd_fp8_causal", "attn_fwd_mxfp8", "attn_fwd_mxfp8_causal",
+            "attn_fwd_fp8qk_bias", "attn_fwd_fp8_bias",
             "attn_bwd_status", "attn_bwd_set_wait_limit",
             "attn_bwd_kernel_count", "attn_fwd_status", "attn_status_string",
             "attn_fwd_set_wait_limit", "attn_fwd_kernel_count"} <= set(names)
@@ -224,6 +225,51 @@ def test_fp8_argument_checks(kw, code, causal):
     before = attn.attn_fwd_kernel_count()
     assert call_fp8pv(causal=causal, **kw) == code
     assert attn.attn_fwd_kernel_count() == before
+
+
+def call_fp8_bias(pv=False, q8=A, k8=A, v=A, ldv=128, bias=A, sb=0, sh=0, sq=128, o=A, lse=A, B=1, H=1, Nq=128,
+                  Nk=128, d=128, scale=0.125, dq=0.01, dk=0.02, dv=0.03):
+    lib = attn.load_library()
+    if pv:
+        return lib.attn_fwd_fp8_bias(q8, k8, v, ldv, bias, sb, sh, sq, o, lse, B, H, Nq, Nk, d, scale, dq, dk, dv, None)
+    return lib.attn_fwd_fp8qk_bias(q8, k8, v, bias, sb, sh, sq, o, lse, B, H, Nq, Nk, d, scale, dq, dk, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(bias=None), attn.ATTN_ERR_INVALID_ARG),
+    (dict(sq=-128), attn.ATTN_ERR_INVALID_ARG),
+    (dict(sb=1 << 62, B=2), attn.ATTN_ERR_INVALID_ARG),      # the last element's offset overflows
+    (dict(bias=A + 8), attn.ATTN_ERR_MISALIGNED),
+    (dict(sq=100), attn.ATTN_ERR_MISALIGNED),                # rows not on 16-byte boundaries
+    (dict(dq=0.0), attn.ATTN_ERR_INVALID_ARG),
+    (dict(dk=math.nan), attn.ATTN_ERR_INVALID_ARG),
+    (dict(scale=3e38, dq=10.0, dk=10.0), attn.ATTN_ERR_INVALID_ARG),
+    (dict(q8=None), attn.ATTN_ERR_INVALID_ARG),
+    (dict(d=64), attn.ATTN_ERR_UNSUPPORTED),
+    (dict(Nk=0), attn.ATTN_ERR_INVALID_ARG),
+    (dict(B=0), attn.ATTN_OK),
+])
+@pytest.mark.parametrize("pv", [False, True])
+def test_fp8_bias_argument_checks(kw, code, pv):
+    before = attn.attn_fwd_kernel_count()
+    assert call_fp8_bias(pv=pv, **kw) == code
+    assert attn.attn_fwd_kernel_count() == before
+
+
+def test_fp8_bias_value_operand_checks():
+    before = attn.attn_fwd_kernel_count()
+    assert call_fp8_bias(pv=True, dv=0.0) == attn.ATTN_ERR_INVALID_ARG
+    assert call_fp8_bias(pv=True, ldv=120) == attn.ATTN_ERR_INVALID_ARG
+    assert call_fp8_bias(pv=True, ldv=136, Nk=130, sq=136) == attn.ATTN_ERR_MISALIGNED
+    assert attn.attn_fwd_kernel_count() == before
+
+
+def test_fp8_bias_binding_refuses_causal():
+    with pytest.raises(ValueError):
+        attn.attn_fwd_fp8qk(A, A, A, A, A, 1, 1, 128, 128, 128, 0.1, causal=True, bias=A, bias_strides=(0, 0, 128))
+    with pytest.raises(ValueError):
+        attn.attn_fwd_fp8(A, A, A, A, A, 1, 1, 128, 128, 128, 0.1, ldv=128, causal=True, bias=A,
+                          bias_strides=(0, 0, 128))
 
 
 def call_mx(q8=A, sq=A, k8=A, sk=A, vt8=A, ldv=128, svt=A, ldsv=16, o=A, lse=A, B=1, H=1, Nq=128, Nk=128, d=128,

@@ -81,6 +81,15 @@ def test_fp8_entry_points(gpu_lib, B, H, Nq, Nk):
     gpu_lib.attn_fwd_fp8(torch.from_numpy(q8).cuda(), torch.from_numpy(k8).cuda(), torch.from_numpy(vt).cuda(), o, lse,
                          B, H, Nq, Nk, 128, SCALE, dq, dk, dv)
     check(gpu_lib, ((fo, o), "bf16"), ((fl, lse), "f32"))
+    if Nk % 8 == 0:   # the biased variants (bias rows on 16-byte boundaries)
+        bias = to_device(make_bias((B, H, Nq, Nk), seed=17350, std=1.0))
+        (fo, o), (fl, lse) = outputs(B, H, Nq)
+        gpu_lib.attn_fwd_fp8qk(q8d, k8d, to_device(v), o, lse, B, H, Nq, Nk, 128, SCALE, dq, dk, bias=bias)
+        check(gpu_lib, ((fo, o), "bf16"), ((fl, lse), "f32"))
+        (fo, o), (fl, lse) = outputs(B, H, Nq)
+        gpu_lib.attn_fwd_fp8(torch.from_numpy(q8).cuda(), torch.from_numpy(k8).cuda(), torch.from_numpy(vt).cuda(), o,
+                             lse, B, H, Nq, Nk, 128, SCALE, dq, dk, dv, bias=bias)
+        check(gpu_lib, ((fo, o), "bf16"), ((fl, lse), "f32"))
     if Nq <= Nk:   # the causal variants
         (fo, o), (fl, lse) = outputs(B, H, Nq)
         gpu_lib.attn_fwd_fp8qk(q8d, k8d, to_device(v), o, lse, B, H, Nq, Nk, 128, SCALE, dq, dk, causal=True)

@@ -21,7 +21,7 @@ pytestmark = pytest.mark.gpu
 SCALE = float(np.float32(1 / math.sqrt(128)))
 
 
-def run_fp8(attn, q8, k8, v, scale, dq, dk, causal=False):
+def run_fp8(attn, q8, k8, v, scale, dq, dk, causal=False, bias=None):
     import torch
     B, H, Nq, d = q8.shape
     Nk = k8.shape[2]
@@ -29,19 +29,22 @@ def run_fp8(attn, q8, k8, v, scale, dq, dk, causal=False):
     lse = torch.full((B, H, Nq), float("nan"), dtype=torch.float32, device="cuda")
     q8d = torch.from_numpy(np.ascontiguousarray(q8)).cuda().view(torch.float8_e4m3fn)
     k8d = torch.from_numpy(np.ascontiguousarray(k8)).cuda()          # raw bytes are accepted too
-    attn.attn_fwd_fp8qk(q8d, k8d, to_device(v), o, lse, B, H, Nq, Nk, d, scale, dq, dk, causal=causal)
+    attn.attn_fwd_fp8qk(q8d, k8d, to_device(v), o, lse, B, H, Nq, Nk, d, scale, dq, dk, causal=causal,
+                        bias=None if bias is None else to_device(bias))
     assert attn.attn_fwd_status() == attn.ATTN_OK
     return bf16_to_np(o), lse.cpu().numpy()
 
 
-def check_fp8(attn, B, H, Nq, Nk, seed, qk_mult=1.0, scale=SCALE, rows=None, causal=False):
+def check_fp8(attn, B, H, Nq, Nk, seed, qk_mult=1.0, scale=SCALE, rows=None, causal=False, bias=None):
     q8, k8, v, dq, dk = make_qk_e4m3(B, H, Nq, Nk, seed=seed, qk_mult=qk_mult)
-    o, lse = run_fp8(attn, q8, k8, v, scale, dq, dk, causal)
-    o_ref, lse_ref = oracle.attention_rows_e4m3qk(q8, k8, v, scale, dq, dk, rows, causal=causal)
+    o, lse = run_fp8(attn, q8, k8, v, scale, dq, dk, causal, bias)
+    o_ref, lse_ref = oracle.attention_rows_e4m3qk(q8, k8, v, scale, dq, dk, rows, causal=causal, bias=bias)
     o, lse = o.reshape(-1, 128), lse.reshape(-1)
     if rows is not None:
         o, lse = o[rows], lse[rows]
-    return compare(o, lse, o_ref, lse_ref, ulp_aware=qk_mult != 1.0)
+    # a sharp bias (std 8) concentrates rows on few keys, so |O| reaches the binade where
+    # half a BF16 ulp exceeds 1e-2, as with peaked scores
+    return compare(o, lse, o_ref, lse_ref, ulp_aware=qk_mult != 1.0 or bias is not None)
 
 
 @pytest.mark.parametrize("B,H,Nq,Nk", [
@@ -106,14 +109,17 @@ def test_fp8qk_is_deterministic(gpu_lib):
 # or V read from the wrong rows moves O by 1e-1 or more on average. The LSE does not depend
 # on P's rounding and keeps the forward's 1e-4.
 
-def fp8pv_tolerance(qk_mult, causal=False):
-    # under the causal mask rows near the diagonal average over few keys (tests/test_fp8_tolerance.py)
+def fp8pv_tolerance(qk_mult, causal=False, bias=False):
+    # under the causal mask rows near the diagonal average over few keys, and a bias sharpens
+    # the rows too (tests/test_fp8_tolerance.py derives both)
+    if bias:
+        return (1.2e-1, 8e-3)
     if causal:
         return (7e-2, 7e-3) if qk_mult == 1.0 else (2e-1, 1e-2)
     return (4e-2, 5e-3) if qk_mult == 1.0 else (2e-1, 1e-2)
 
 
-def run_fp8pv(attn, q8, k8, v8, scale, dq, dk, dv, ldv=None, pad_code=0x7F, causal=False):
+def run_fp8pv(attn, q8, k8, v8, scale, dq, dk, dv, ldv=None, pad_code=0x7F, causal=False, bias=None):
     """v8 is key-major [B,H,Nk,d]; the kernel gets V^T [B,H,d,ldv] with the bytes past Nk of
     each row set to pad_code (NaN by default: a read of them would show in O)."""
     import torch
@@ -126,23 +132,23 @@ def run_fp8pv(attn, q8, k8, v8, scale, dq, dk, dv, ldv=None, pad_code=0x7F, caus
     lse = torch.full((B, H, Nq), float("nan"), dtype=torch.float32, device="cuda")
     attn.attn_fwd_fp8(torch.from_numpy(np.ascontiguousarray(q8)).cuda(), torch.from_numpy(np.ascontiguousarray(k8)).cuda(),
                       torch.from_numpy(vt).cuda().view(torch.float8_e4m3fn), o, lse, B, H, Nq, Nk, d, scale, dq, dk, dv,
-                      causal=causal)
+                      causal=causal, bias=None if bias is None else to_device(bias))
     assert attn.attn_fwd_status() == attn.ATTN_OK
     return bf16_to_np(o), lse.cpu().numpy()
 
 
-def check_fp8pv(attn, B, H, Nq, Nk, seed, qk_mult=1.0, scale=SCALE, rows=None, ldv=None, causal=False):
+def check_fp8pv(attn, B, H, Nq, Nk, seed, qk_mult=1.0, scale=SCALE, rows=None, ldv=None, causal=False, bias=None):
     from dense_attention_forward_fwd_gb300.inputs import make_qkv_e4m3
     q8, k8, v8, dq, dk, dv = make_qkv_e4m3(B, H, Nq, Nk, seed=seed, qk_mult=qk_mult)
-    o, lse = run_fp8pv(attn, q8, k8, v8, scale, dq, dk, dv, ldv, causal=causal)
-    o_ref, lse_ref = oracle.attention_rows_e4m3(q8, k8, v8, scale, dq, dk, dv, rows, causal=causal)
+    o, lse = run_fp8pv(attn, q8, k8, v8, scale, dq, dk, dv, ldv, causal=causal, bias=bias)
+    o_ref, lse_ref = oracle.attention_rows_e4m3(q8, k8, v8, scale, dq, dk, dv, rows, causal=causal, bias=bias)
     o, lse = o.reshape(-1, 128), lse.reshape(-1)
     if rows is not None:
         o, lse = o[rows], lse[rows]
     assert np.all(np.isfinite(o)) and np.all(np.isfinite(lse)), "non-finite output"
     err = np.abs(o.astype(np.float64) - o_ref)
     lse_err = np.abs(lse.astype(np.float64) - lse_ref) / np.maximum(1.0, np.abs(lse_ref))
-    t_max, t_mean = fp8pv_tolerance(qk_mult, causal)
+    t_max, t_mean = fp8pv_tolerance(qk_mult, causal, bias is not None)
     assert err.max() <= t_max and err.mean() <= t_mean and lse_err.max() <= 1e-4, \
         f"max {err.max():.3e} mean {err.mean():.3e} lse {lse_err.max():.3e}"
     return err.max(), err.mean()
@@ -240,3 +246,57 @@ def test_fp8_causal_workload_sampled_rows(gpu_lib, name):
     rows = sample_rows(w.B, w.H, w.Nq, per_head=16)
     check_fp8(gpu_lib, w.B, w.H, w.Nq, w.Nk, seed=w.seed, scale=w.scale, rows=rows, causal=True)
     check_fp8pv(gpu_lib, w.B, w.H, w.Nq, w.Nk, seed=w.seed, scale=w.scale, rows=rows, causal=True)
+
+
+# ---- with the additive bias: attn_fwd_fp8qk_bias and attn_fwd_fp8_bias -------------------------
+
+def bias_shape(kind, B, H, Nq, Nk):
+    return {"full": (B, H, Nq, Nk), "shared": (1, 1, Nq, Nk), "key": (1, 1, 1, Nk)}[kind]
+
+
+@pytest.mark.parametrize("B,H,Nq,Nk,seed,kind,std", [
+    (1, 2, 256, 384, 22640, "full", 2.0),
+    (2, 3, 300, 1000, 23300, "shared", 2.0),   # ragged; one [Nq, Nk] bias for every head
+    (1, 2, 129, 136, 22265, "key", 2.0),       # one bias per key (a padding mask's shape)
+    (1, 2, 256, 5120, 27376, "full", 2.0),     # key steps split across blocks
+    (1, 2, 512, 1024, 22100, "full", 8.0),     # a sharp bias: late maxima and O rescales
+])
+def test_fp8_bias_parity(gpu_lib, B, H, Nq, Nk, seed, kind, std):
+    # the inputs tests/test_fp8_tolerance.py derives the biased bounds on; the FP8-score entry
+    # point (P in BF16) takes the forward's own bounds on the same shapes
+    from dense_attention_forward_fwd_gb300.inputs import make_bias
+    bias = make_bias(bias_shape(kind, B, H, Nq, Nk), seed=seed + 1, std=std)
+    check_fp8pv(gpu_lib, B, H, Nq, Nk, seed=seed, bias=bias)
+    check_fp8(gpu_lib, B, H, Nq, Nk, seed=seed, bias=bias)
+
+
+def test_fp8_bias_masks_keys(gpu_lib):
+    # -inf entries remove keys, whole key tiles of them included
+    from dense_attention_forward_fwd_gb300.inputs import BF16_NEG_INF, make_bias
+    bias = make_bias((1, 1, 1, 1024), seed=22700)
+    bias[..., :300] = BF16_NEG_INF
+    bias[..., 900:] = BF16_NEG_INF
+    check_fp8pv(gpu_lib, 1, 2, 384, 1024, seed=22701, bias=bias)
+    check_fp8(gpu_lib, 1, 2, 384, 1024, seed=22701, bias=bias)
+
+
+@pytest.mark.parametrize("kind", ["shared", "full"])
+def test_fp8_bias_workload_sampled_rows(gpu_lib, kind):
+    # rect-4k-8k with one bias for every head, or one per head, as `bench.py --bias` times them
+    from dense_attention_forward_fwd_gb300.inputs import make_bias
+    w = by_name("rect-4k-8k")
+    rows = sample_rows(w.B, w.H, w.Nq, per_head=16)
+    bias = make_bias(bias_shape(kind, w.B, w.H, w.Nq, w.Nk), seed=88, std=1.0)
+    check_fp8pv(gpu_lib, w.B, w.H, w.Nq, w.Nk, seed=w.seed, scale=w.scale, rows=rows, bias=bias)
+    check_fp8(gpu_lib, w.B, w.H, w.Nq, w.Nk, seed=w.seed, scale=w.scale, rows=rows, bias=bias)
+
+
+def test_fp8_bias_and_causal_together_are_refused(gpu_lib):
+    import torch
+    from dense_attention_forward_fwd_gb300.inputs import make_bias
+    q8, k8, v, dq, dk = make_qk_e4m3(1, 1, 128, 128, seed=22800)
+    o = torch.empty(1, 1, 128, 128, dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty(1, 1, 128, device="cuda")
+    with pytest.raises(ValueError):
+        gpu_lib.attn_fwd_fp8qk(torch.from_numpy(q8).cuda(), torch.from_numpy(k8).cuda(), to_device(v), o, lse, 1, 1, 128,
+                               128, 128, SCALE, dq, dk, causal=True, bias=to_device(make_bias((1, 1, 128, 128), seed=1)))

@@ -16,12 +16,15 @@ rounding weighs more in their O: the emulation with the mask gives up to 3.6e-2 
 attn_fwd_mxfp8 rounds P the same way (E4M3 under a block scale of 2^0) and its products of
 scaled E4M3 values are exact, so the same emulation on the decoded MXFP8 values (with a V
 descale of 1) gives its error too; the last test checks the MXFP8 GPU tests' inputs.
+With an additive bias (attn_fwd_fp8_bias) rows are sharper still: a bias of standard
+deviation 2 (8 on peaked rows) gives up to 7.0e-2 (max) and 4.3e-3 (mean), and those GPU
+tests take BIAS_BOUNDS.
 """
 import numpy as np
 import pytest
 
 import oracle
-from dense_attention_forward_fwd_gb300.inputs import make_qkv_e4m3, make_qkv_mxfp8
+from dense_attention_forward_fwd_gb300.inputs import bf16_bits_to_f32, make_bias, make_qkv_e4m3, make_qkv_mxfp8
 
 torch = pytest.importorskip("torch")
 
@@ -29,6 +32,7 @@ SCALE = float(np.float32(1 / np.sqrt(128)))
 # the GPU tests' bounds: (max, mean) for N(0,1) inputs and for peaked inputs
 BOUNDS = {1.0: (4e-2, 5e-3), 3.0: (2e-1, 1e-2)}
 CAUSAL_BOUNDS = {1.0: (7e-2, 7e-3), 3.0: (2e-1, 1e-2)}
+BIAS_BOUNDS = (1.2e-1, 8e-3)   # attn_fwd_fp8_bias, N(0,1) scores with a bias of std 2 to 8
 
 
 def to_e4m3(x):
@@ -39,10 +43,14 @@ def to_bf16(x):
     return torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32)).to(torch.bfloat16).to(torch.float32).numpy()
 
 
-def emulate_head(q, k, v8, scale, dv, tau=8.0, causal=False):
+def emulate_head(q, k, v8, scale, dv, tau=8.0, causal=False, bias=None):
     """q [Nq, d], k [Nk, d] real inputs (float64), v8 [Nk, d] E4M3 values; returns O [Nq, d].
-    causal: row i sees keys 0 .. i + Nk - Nq (a masked weight is exactly 0)."""
-    t = (q @ k.T).astype(np.float32) * np.float32(scale * 1.4426950408889634)
+    causal: row i sees keys 0 .. i + Nk - Nq (a masked weight is exactly 0). bias [Nq, Nk]
+    (float64): added to the scaled scores in FP32, then the whole scaled by log2 e."""
+    if bias is None:
+        t = (q @ k.T).astype(np.float32) * np.float32(scale * 1.4426950408889634)
+    else:
+        t = ((q @ k.T).astype(np.float32) * np.float32(scale) + bias.astype(np.float32)) * np.float32(1.4426950408889634)
     Nq, Nk = t.shape
     if causal:
         t[np.arange(Nk)[None, :] > np.arange(Nq)[:, None] + (Nk - Nq)] = -np.inf
@@ -140,6 +148,33 @@ def test_mxfp8_bounds_cover_the_emulated_rounding_error(B, H, Nq, Nk, qk_mult, s
     err = np.stack([np.abs(emulate_head(q[b, h], k[b, h], v[b, h], SCALE, 1.0, causal=causal) - o_ref[b, h])
                     for b in range(B) for h in range(H)])
     t_max, t_mean = (CAUSAL_BOUNDS if causal else BOUNDS)[qk_mult]
+    assert err.max() * 1.5 <= t_max, f"emulated max {err.max():.3e} leaves too little margin under {t_max}"
+    assert err.mean() * 1.5 <= t_mean, f"emulated mean {err.mean():.3e} leaves too little margin under {t_mean}"
+    assert err.max() * 20 >= t_max
+
+
+def bias_shape(kind, B, H, Nq, Nk):
+    return {"full": (B, H, Nq, Nk), "shared": (1, 1, Nq, Nk), "key": (1, 1, 1, Nk)}[kind]
+
+
+@pytest.mark.parametrize("B,H,Nq,Nk,seed,kind,std", [
+    # the biased FP8 GPU tests' inputs (tests/test_fp8_gpu.py)
+    (1, 2, 256, 384, 22640, "full", 2.0),
+    (2, 3, 300, 1000, 23300, "shared", 2.0),
+    (1, 2, 129, 136, 22265, "key", 2.0),
+    (1, 2, 256, 5120, 27376, "full", 2.0),
+    (1, 2, 512, 1024, 22100, "full", 8.0),
+])
+def test_bias_bounds_cover_the_emulated_rounding_error(B, H, Nq, Nk, seed, kind, std):
+    q8, k8, v8, dq, dk, dv = make_qkv_e4m3(B, H, Nq, Nk, seed=seed)
+    bias = make_bias(bias_shape(kind, B, H, Nq, Nk), seed=seed + 1, std=std)
+    o_ref, _ = oracle.attention_rows_e4m3(q8, k8, v8, SCALE, dq, dk, dv, bias=bias)
+    o_ref = o_ref.reshape(B, H, Nq, -1)
+    bf = np.broadcast_to(bf16_bits_to_f32(bias).astype(np.float64), (B, H, Nq, Nk))
+    err = np.stack([np.abs(emulate_head(oracle.e4m3_to_f64(q8[b, h]) * dq, oracle.e4m3_to_f64(k8[b, h]) * dk,
+                                        oracle.e4m3_to_f64(v8[b, h]), SCALE, dv, bias=bf[b, h]) - o_ref[b, h])
+                    for b in range(B) for h in range(H)])
+    t_max, t_mean = BIAS_BOUNDS
     assert err.max() * 1.5 <= t_max, f"emulated max {err.max():.3e} leaves too little margin under {t_max}"
     assert err.mean() * 1.5 <= t_mean, f"emulated mean {err.mean():.3e} leaves too little margin under {t_mean}"
     assert err.max() * 20 >= t_max
