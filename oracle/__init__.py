@@ -92,6 +92,13 @@ class Oracle:
         lib.attn_ref_dense_causal_f64.restype = ctypes.c_int
         lib.attn_ref_bwd_causal_f64.argtypes = lib.attn_ref_bwd_f64.argtypes
         lib.attn_ref_bwd_causal_f64.restype = ctypes.c_int
+        dense_bias = [vp, i64, i64, i64, i64]   # bias, H, sb, sh, sq
+        lib.attn_ref_dense_bias_f64.argtypes = lib.attn_ref_dense_f64.argtypes[:3] + dense_bias + \
+            lib.attn_ref_dense_f64.argtypes[3:]
+        lib.attn_ref_dense_bias_f64.restype = ctypes.c_int
+        lib.attn_ref_bwd_bias_f64.argtypes = lib.attn_ref_bwd_f64.argtypes[:4] + dense_bias + \
+            lib.attn_ref_bwd_f64.argtypes[4:]
+        lib.attn_ref_bwd_bias_f64.restype = ctypes.c_int
         lib.attn_ref_probs_f64.argtypes = [vp, vp, i64, i64, i64, i64, dbl, vp]
         lib.attn_ref_probs_f64.restype = ctypes.c_int
         lib.attn_ref_max_threads.argtypes = []
@@ -298,9 +305,21 @@ class Oracle:
         o, lse = self.attention_rows(q, k, v, scale, None, nthreads)
         return o.reshape(B, H, Nq, dv), lse.reshape(B, H, Nq)
 
-    def attention_dense(self, q, k, v, scale: float, causal: bool = False):
+    @staticmethod
+    def _dense_bias(bias, B, H, Nq, Nk):
+        """(float64 C-contiguous bias [Bb,Hb,Nqb,Nk], sb, sh, sq) for a float64 or BF16-bit bias
+        that broadcasts to [B,H,Nq,Nk] (a dimension of size 1 is shared)."""
+        bias = _f64(bias)
+        Bb, Hb, Nqb, Nkb = bias.shape
+        if Bb not in (1, B) or Hb not in (1, H) or Nqb not in (1, Nq) or Nkb != Nk:
+            raise ValueError(f"bias shape {bias.shape} does not broadcast to {(B, H, Nq, Nk)}")
+        sb, sh, sq = (st // 8 if n > 1 else 0 for st, n in zip(bias.strides[:3], (Bb, Hb, Nqb)))
+        return bias, sb, sh, sq
+
+    def attention_dense(self, q, k, v, scale: float, causal: bool = False, bias=None):
         """Forward on float64 (or BF16-bit uint16, widened exactly) inputs: (o [B,H,Nq,dv], lse [B,H,Nq]).
-        causal: the causal mask of attention_rows_causal (needs Nq <= Nk)."""
+        causal: the causal mask of attention_rows_causal (needs Nq <= Nk). bias: the additive
+        B of attention_rows_bias, float64 or BF16 bits (not with causal)."""
         q, k, v = _f64(q), _f64(k), _f64(v)
         B, H, Nq, d = q.shape
         Nk, dv = k.shape[2], v.shape[3]
@@ -308,17 +327,25 @@ class Oracle:
             raise ValueError(f"shape mismatch q{q.shape} k{k.shape} v{v.shape}")
         o = np.empty((B, H, Nq, dv), dtype=np.float64)
         lse = np.empty((B, H, Nq), dtype=np.float64)
-        fn = self.lib.attn_ref_dense_causal_f64 if causal else self.lib.attn_ref_dense_f64
-        rc = fn(_ptr(q), _ptr(k), _ptr(v), B * H, Nq, Nk, d, dv, float(scale), _ptr(o), _ptr(lse))
+        tail = (B * H, Nq, Nk, d, dv, float(scale), _ptr(o), _ptr(lse))
+        if bias is not None:
+            if causal:
+                raise ValueError("bias and causal together are not supported (put the mask in the bias)")
+            bias, sb, sh, sq = self._dense_bias(bias, B, H, Nq, Nk)
+            rc = self.lib.attn_ref_dense_bias_f64(_ptr(q), _ptr(k), _ptr(v), _ptr(bias), H, sb, sh, sq, *tail)
+        else:
+            fn = self.lib.attn_ref_dense_causal_f64 if causal else self.lib.attn_ref_dense_f64
+            rc = fn(_ptr(q), _ptr(k), _ptr(v), *tail)
         if rc != 0:
             raise ValueError(f"attn_ref_dense_f64 failed with status {rc}")
         return o, lse
 
-    def attention_bwd(self, q, k, v, dout, scale: float, nthreads: int = 0, causal: bool = False):
+    def attention_bwd(self, q, k, v, dout, scale: float, nthreads: int = 0, causal: bool = False, bias=None):
         """Gradients (dq, dk, dv) in float64 of the forward for upstream gradient dout [B,H,Nq,dv].
 
         Inputs are float64 arrays, or BF16 bits (uint16) widened exactly. causal: of the
-        causal forward (needs Nq <= Nk)."""
+        causal forward (needs Nq <= Nk). bias: of the biased forward (as attention_dense), the
+        bias held fixed."""
         q, k, v, dout = _f64(q), _f64(k), _f64(v), _f64(dout)
         B, H, Nq, d = q.shape
         Nk, dv = k.shape[2], v.shape[3]
@@ -327,9 +354,16 @@ class Oracle:
         dq = np.empty((B, H, Nq, d), dtype=np.float64)
         dk = np.empty((B, H, Nk, d), dtype=np.float64)
         dvv = np.empty((B, H, Nk, dv), dtype=np.float64)
-        fn = self.lib.attn_ref_bwd_causal_f64 if causal else self.lib.attn_ref_bwd_f64
-        rc = fn(_ptr(q), _ptr(k), _ptr(v), _ptr(dout), B * H, Nq, Nk, d, dv, float(scale), _ptr(dq), _ptr(dk),
-                _ptr(dvv), int(nthreads))
+        tail = (B * H, Nq, Nk, d, dv, float(scale), _ptr(dq), _ptr(dk), _ptr(dvv), int(nthreads))
+        if bias is not None:
+            if causal:
+                raise ValueError("bias and causal together are not supported (put the mask in the bias)")
+            bias, sb, sh, sq = self._dense_bias(bias, B, H, Nq, Nk)
+            rc = self.lib.attn_ref_bwd_bias_f64(_ptr(q), _ptr(k), _ptr(v), _ptr(dout), _ptr(bias), H, sb, sh, sq,
+                                                *tail)
+        else:
+            fn = self.lib.attn_ref_bwd_causal_f64 if causal else self.lib.attn_ref_bwd_f64
+            rc = fn(_ptr(q), _ptr(k), _ptr(v), _ptr(dout), *tail)
         if rc != 0:
             raise ValueError(f"attn_ref_bwd_f64 failed with status {rc}")
         return dq, dk, dvv
@@ -426,9 +460,9 @@ def probs(q, k, scale: float):
     return default().probs(q, k, scale)
 
 
-def attention_dense(q, k, v, scale: float, causal: bool = False):
-    return default().attention_dense(q, k, v, scale, causal)
+def attention_dense(q, k, v, scale: float, causal: bool = False, bias=None):
+    return default().attention_dense(q, k, v, scale, causal, bias)
 
 
-def attention_bwd(q, k, v, dout, scale: float, nthreads: int = 0, causal: bool = False):
-    return default().attention_bwd(q, k, v, dout, scale, nthreads, causal)
+def attention_bwd(q, k, v, dout, scale: float, nthreads: int = 0, causal: bool = False, bias=None):
+    return default().attention_bwd(q, k, v, dout, scale, nthreads, causal, bias)

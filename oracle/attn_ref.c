@@ -331,7 +331,24 @@ int attn_ref_max_threads(void)
  *
  * These take double inputs so that central differences of attn_ref_dense_f64 can check
  * them; BF16 inputs are widened exactly by the caller.
+ *
+ * With the definition's optional bias B (section 0.2: S = QK^T / sqrt(d) + B), held fixed,
+ * s_j = scale * q_i . k_j + B_ij and every formula above is unchanged: B enters the
+ * gradients only through p (a constant's derivative is zero), and dB = ds is not formed.
+ * The bias arrives as doubles, B_ij of head (b, h) = bias[b * sb + h * sh + i * sq + j].
  */
+struct dbias { const double *p; int64_t H, sb, sh, sq; };   /* p == NULL: no bias */
+
+/* row i of head bh's bias, or NULL */
+static const double *dbias_row(const struct dbias *b, int64_t bh, int64_t i)
+{
+    return b->p ? b->p + (bh / b->H) * b->sb + (bh % b->H) * b->sh + i * b->sq : NULL;
+}
+
+static int dbias_ok(const struct dbias *b, int64_t BH)
+{
+    return !b->p || (b->H >= 1 && BH % b->H == 0 && b->sb >= 0 && b->sh >= 0 && b->sq >= 0);
+}
 
 /*
  * The forward on double inputs: o [BH, Nq, dv], lse [BH, Nq] (same steps as above).
@@ -340,10 +357,10 @@ int attn_ref_max_threads(void)
  */
 static int dense_impl(const double *q, const double *k, const double *v,
                       int64_t BH, int64_t Nq, int64_t Nk, int64_t d, int64_t dv,
-                      double scale, double *o, double *lse, int causal)
+                      double scale, double *o, double *lse, int causal, const struct dbias *bias)
 {
     if (BH < 0 || Nq < 0 || Nk < 1 || d < 1 || dv < 1) return REF_EINVAL;
-    if (causal && Nq > Nk) return REF_EINVAL;
+    if ((causal && Nq > Nk) || !dbias_ok(bias, BH)) return REF_EINVAL;
     if (BH * Nq == 0) return REF_OK;
     if (!q || !k || !v || !o || !lse) return REF_EINVAL;
     double *s = (double *)malloc((size_t)Nk * sizeof(double));
@@ -358,6 +375,9 @@ static int dense_impl(const double *q, const double *k, const double *v,
                 for (int64_t c = 0; c < d; c++) acc += qi[c] * kh[j * d + c];
                 s[j] = scale * acc;
             }
+            const double *bi = dbias_row(bias, bh, i);
+            if (bi)
+                for (int64_t j = 0; j < nv; j++) s[j] += bi[j];
             double m = row_max(s, nv);
             double l = row_exp_sum(s, nv, m);
             double *oi = o + (bh * Nq + i) * dv;
@@ -377,14 +397,27 @@ int attn_ref_dense_f64(const double *q, const double *k, const double *v,
                        int64_t BH, int64_t Nq, int64_t Nk, int64_t d, int64_t dv,
                        double scale, double *o, double *lse)
 {
-    return dense_impl(q, k, v, BH, Nq, Nk, d, dv, scale, o, lse, 0);
+    const struct dbias none = {NULL, 1, 0, 0, 0};
+    return dense_impl(q, k, v, BH, Nq, Nk, d, dv, scale, o, lse, 0, &none);
 }
 
 int attn_ref_dense_causal_f64(const double *q, const double *k, const double *v,
                               int64_t BH, int64_t Nq, int64_t Nk, int64_t d, int64_t dv,
                               double scale, double *o, double *lse)
 {
-    return dense_impl(q, k, v, BH, Nq, Nk, d, dv, scale, o, lse, 1);
+    const struct dbias none = {NULL, 1, 0, 0, 0};
+    return dense_impl(q, k, v, BH, Nq, Nk, d, dv, scale, o, lse, 1, &none);
+}
+
+/* the forward on double inputs with the bias (no causal mask: a bias can carry one) */
+int attn_ref_dense_bias_f64(const double *q, const double *k, const double *v,
+                            const double *bias, int64_t H, int64_t sb, int64_t sh, int64_t sq,
+                            int64_t BH, int64_t Nq, int64_t Nk, int64_t d, int64_t dv,
+                            double scale, double *o, double *lse)
+{
+    if (!bias) return REF_EINVAL;
+    const struct dbias b = {bias, H, sb, sh, sq};
+    return dense_impl(q, k, v, BH, Nq, Nk, d, dv, scale, o, lse, 0, &b);
 }
 
 /*
@@ -395,10 +428,11 @@ int attn_ref_dense_causal_f64(const double *q, const double *k, const double *v,
  */
 static int bwd_impl(const double *q, const double *k, const double *v, const double *dout,
                     int64_t BH, int64_t Nq, int64_t Nk, int64_t d, int64_t dv,
-                    double scale, double *dq, double *dk, double *dvv, int nthreads, int causal)
+                    double scale, double *dq, double *dk, double *dvv, int nthreads, int causal,
+                    const struct dbias *bias)
 {
     if (BH < 0 || Nq < 0 || Nk < 1 || d < 1 || dv < 1) return REF_EINVAL;
-    if (causal && Nq > Nk) return REF_EINVAL;
+    if ((causal && Nq > Nk) || !dbias_ok(bias, BH)) return REF_EINVAL;
     if (BH == 0) return REF_OK;
     if (!q || !k || !v || !dout || !dq || !dk || !dvv) return REF_EINVAL;
     int failed = 0;
@@ -436,6 +470,9 @@ static int bwd_impl(const double *q, const double *k, const double *v, const dou
                         for (int64_t c = 0; c < d; c++) acc += qi[c] * kh[j * d + c];
                         p[j] = scale * acc;
                     }
+                    const double *brow = dbias_row(bias, bh, i);
+                    if (brow)
+                        for (int64_t j = 0; j < nvis; j++) p[j] += brow[j];
                     double m = row_max(p, nvis);
                     double l = row_exp_sum(p, nvis, m);
                     for (int64_t j = 0; j < nvis; j++) p[j] /= l;
@@ -472,14 +509,27 @@ int attn_ref_bwd_f64(const double *q, const double *k, const double *v, const do
                      int64_t BH, int64_t Nq, int64_t Nk, int64_t d, int64_t dv,
                      double scale, double *dq, double *dk, double *dvv, int nthreads)
 {
-    return bwd_impl(q, k, v, dout, BH, Nq, Nk, d, dv, scale, dq, dk, dvv, nthreads, 0);
+    const struct dbias none = {NULL, 1, 0, 0, 0};
+    return bwd_impl(q, k, v, dout, BH, Nq, Nk, d, dv, scale, dq, dk, dvv, nthreads, 0, &none);
 }
 
 int attn_ref_bwd_causal_f64(const double *q, const double *k, const double *v, const double *dout,
                             int64_t BH, int64_t Nq, int64_t Nk, int64_t d, int64_t dv,
                             double scale, double *dq, double *dk, double *dvv, int nthreads)
 {
-    return bwd_impl(q, k, v, dout, BH, Nq, Nk, d, dv, scale, dq, dk, dvv, nthreads, 1);
+    const struct dbias none = {NULL, 1, 0, 0, 0};
+    return bwd_impl(q, k, v, dout, BH, Nq, Nk, d, dv, scale, dq, dk, dvv, nthreads, 1, &none);
+}
+
+/* the gradient (dq, dk, dv) of the biased forward, the bias held fixed */
+int attn_ref_bwd_bias_f64(const double *q, const double *k, const double *v, const double *dout,
+                          const double *bias, int64_t H, int64_t sb, int64_t sh, int64_t sq,
+                          int64_t BH, int64_t Nq, int64_t Nk, int64_t d, int64_t dv,
+                          double scale, double *dq, double *dk, double *dvv, int nthreads)
+{
+    if (!bias) return REF_EINVAL;
+    const struct dbias b = {bias, H, sb, sh, sq};
+    return bwd_impl(q, k, v, dout, BH, Nq, Nk, d, dv, scale, dq, dk, dvv, nthreads, 0, &b);
 }
 
 /*

@@ -497,6 +497,73 @@ def pin_causal_bwd_keys_see_only_later_rows(orc):
     assert np.min(np.abs(dv[0, 0, :3]).max(axis=-1)) > 1e-3
 
 
+# ---- the backward of the biased forward (the bias held fixed) -------------------------------
+
+def pin_bias_dense_forward_equals_the_bf16_bias_oracle(orc):
+    # the double-input forward with a bias is the pinned BF16 bias oracle on the BF16 lattice,
+    # for a bias per (batch, head, row, key) and one shared by every head and batch
+    q, k, v = make_qkv(2, 3, 5, 7, d=8, seed=90)
+    rng = np.random.default_rng(91)
+    for shape in ((2, 3, 5, 7), (1, 1, 5, 7), (1, 3, 1, 7)):
+        bias = f32_to_bf16_bits(rng.normal(0.0, 2.0, size=shape).astype(np.float32))
+        o1, l1 = orc.attention_rows_bias(q, k, v, bias, 0.6)
+        o2, l2 = orc.attention_dense(q, k, v, 0.6, bias=bias)
+        assert np.max(np.abs(o1 - o2.reshape(-1, 8))) < 1e-15 and np.max(np.abs(l1 - l2.reshape(-1))) < 1e-13
+
+
+def pin_bias_bwd_matches_central_differences(orc):
+    # L = sum(dO * O) of the biased forward: dL/dx by central differences for every element of
+    # q, k, v, with a bias that differs by head, row and key; dv > d
+    rng = np.random.default_rng(92)
+    B, H, Nq, Nk, d, dv = 1, 2, 3, 4, 3, 5
+    q, k = rng.normal(size=(B, H, Nq, d)), rng.normal(size=(B, H, Nk, d))
+    v, dout = rng.normal(size=(B, H, Nk, dv)), rng.normal(size=(B, H, Nq, dv))
+    bias = rng.normal(0.0, 1.5, size=(B, H, Nq, Nk))
+    scale = 0.8
+    grads = dict(zip("qkv", orc.attention_bwd(q, k, v, dout, scale, bias=bias)))
+    h = 1e-6
+    for name in "qkv":
+        base = {"q": q, "k": k, "v": v}
+        x, g = base[name], grads[name]
+        fd = np.zeros_like(x)
+        for idx in np.ndindex(x.shape):
+            lo, hi = dict(base), dict(base)
+            hi[name] = x.copy()
+            hi[name][idx] += h
+            lo[name] = x.copy()
+            lo[name][idx] -= h
+            l_hi = np.sum(orc.attention_dense(hi["q"], hi["k"], hi["v"], scale, bias=bias)[0] * dout)
+            l_lo = np.sum(orc.attention_dense(lo["q"], lo["k"], lo["v"], scale, bias=bias)[0] * dout)
+            fd[idx] = (l_hi - l_lo) / (2 * h)
+        assert np.max(np.abs(fd - g)) < 1e-7 * max(1.0, np.max(np.abs(g))), name
+
+
+def pin_bias_bwd_causal_pattern_equals_the_causal_gradient(orc):
+    # 0 on and left of the bottom-right diagonal, -inf right of it: the (pinned) causal gradient
+    for Nq, Nk, seed in ((6, 6, 93), (4, 9, 94)):
+        q, k, v = make_qkv(2, 2, Nq, Nk, d=8, seed=seed)
+        dout = np.random.default_rng(seed + 100).normal(size=(2, 2, Nq, 8))
+        mask = np.zeros((1, 1, Nq, Nk))
+        for i in range(Nq):
+            mask[0, 0, i, i + Nk - Nq + 1:] = -np.inf
+        for gb, gc in zip(orc.attention_bwd(q, k, v, dout, 0.9, bias=mask),
+                          orc.attention_bwd(q, k, v, dout, 0.9, causal=True)):
+            assert np.max(np.abs(gb - gc)) < 1e-13
+
+
+def pin_bias_bwd_constant_per_row_changes_no_gradient(orc):
+    # adding c_i to every score of row i leaves every probability, hence every gradient, alone;
+    # and the key gradients of each head still sum to zero under a general bias
+    q, k, v = make_qkv(2, 2, 6, 9, d=8, seed=95, qk_mult=2.0)
+    dout = np.random.default_rng(96).normal(size=(2, 2, 6, 8))
+    c = np.broadcast_to(np.random.default_rng(97).normal(0.0, 3.0, size=(1, 1, 6, 1)), (1, 1, 6, 9)).copy()
+    for gb, g0 in zip(orc.attention_bwd(q, k, v, dout, 0.5, bias=c), orc.attention_bwd(q, k, v, dout, 0.5)):
+        assert np.max(np.abs(gb - g0)) < 1e-12 * max(1.0, np.max(np.abs(g0)))
+    b = np.random.default_rng(98).normal(0.0, 2.0, size=(2, 2, 6, 9))
+    _, dk, _ = orc.attention_bwd(q, k, v, dout, 0.5, bias=b)
+    assert np.max(np.abs(dk.sum(axis=2))) < 1e-12 * max(1.0, np.max(np.abs(dk))) and np.max(np.abs(dk)) > 1e-3
+
+
 # ---- FP8 E4M3 scores ------------------------------------------------------------------------
 # Q and K as E4M3 codes (the OCP 8-bit floating point format) with per-tensor descale factors.
 

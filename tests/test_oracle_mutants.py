@@ -56,6 +56,12 @@ MUTANTS = {
                                 "(1.0 * e4m3_to_f64(vh[j * dv + c]))"),
     "mx query scales of the first block only": ("(e8m0_to_f64(qs[c / 32]) * e4m3_to_f64(qi[c]))",
                                                 "(e8m0_to_f64(qs[0]) * e4m3_to_f64(qi[c]))"),
+    "bwd bias ignored": ("for (int64_t j = 0; j < nvis; j++) p[j] += brow[j];",
+                         "for (int64_t j = 0; j < nvis; j++) p[j] += 0.0;"),
+    "bwd bias rows transposed": ("const double *brow = dbias_row(bias, bh, i);", "const double *brow = dbias_row(bias, bh, 0);"),
+    "dense bias ignored": ("for (int64_t j = 0; j < nv; j++) s[j] += bi[j];", "for (int64_t j = 0; j < nv; j++) s[j] += 0.0;"),
+    "double bias head and batch strides swapped": ("(bh / b->H) * b->sb + (bh % b->H) * b->sh",
+                                                   "(bh / b->H) * b->sh + (bh % b->H) * b->sb"),
     "e4m3 bias ignored": ("for (int64_t j = 0; j < nk; j++) s[j] += bf16_to_f64(brow[j]);",
                           "for (int64_t j = 0; j < nk; j++) s[j] += 0.0;"),
     "e4m3 bias row stride dropped": ("(bh % H) * sh + i * sq;\n                    for (int64_t j = 0; j < nk; j++) s[j]",
