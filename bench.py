@@ -102,8 +102,8 @@ def parse():
         ap.error("--mxfp8 has no bias entry point (--fp8-qk and --fp8 have)")
     if args.fp8_qk + args.fp8 + args.mxfp8 > 1:
         ap.error("--fp8-qk, --fp8 and --mxfp8 are different entry points; pick one")
-    if args.bias != "none" and (args.causal or args.backward):
-        ap.error("--bias has no causal or backward entry point; use it alone")
+    if args.bias != "none" and args.causal:
+        ap.error("--bias has no causal entry point (a causal bias carries the mask)")
     return args
 
 
@@ -286,7 +286,7 @@ def oracle_rows_fn(oracle, w, causal: bool, bias_kind: str, H1: int, nq: int, fp
     return oracle.attention_rows_causal if causal else oracle.attention_rows
 
 
-def cpu_oracle_backward_sample(w, target_seconds: float, causal: bool = False):
+def cpu_oracle_backward_sample(w, target_seconds: float, causal: bool = False, bias_kind: str = "none"):
     """Time the FP64 backward oracle on one head with nq of the workload's query rows (all Nk
     keys, as dK and dV need every row); returns (TFLOPS at 2.5x forward FLOPs, rows, seconds,
     threads)."""
@@ -298,8 +298,12 @@ def cpu_oracle_backward_sample(w, target_seconds: float, causal: bool = False):
     def run(nq):
         q, k, v = make_qkv(1, 1, nq, w.Nk, d=w.d, seed=w.seed, qk_mult=w.qk_mult)
         do = np.random.Generator(np.random.PCG64(w.seed + 7)).standard_normal((1, 1, nq, w.d))
+        bias = None
+        if bias_kind != "none":   # one head's bias (shared or per head: the same work)
+            from dense_attention_forward_fwd_gb300.inputs import make_bias
+            bias = make_bias((1, 1, nq, w.Nk), seed=w.seed + 1)
         t = time.perf_counter()
-        oracle.attention_bwd(q, k, v, do, w.scale, causal=causal)
+        oracle.attention_bwd(q, k, v, do, w.scale, causal=causal, bias=bias)
         return time.perf_counter() - t
 
     nq = min(w.Nq, 32)
@@ -361,7 +365,7 @@ def run_reference(args, w):
     if args.backward:   # each step: the backward oracle on one head, sized to share ~2 minutes
         total, flops_sum = 0.0, 0.0
         for i in range(warm + steps):
-            tfl, n, dt, threads = cpu_oracle_backward_sample(w, 120.0 / (steps + warm), args.causal)
+            tfl, n, dt, threads = cpu_oracle_backward_sample(w, 120.0 / (steps + warm), args.causal, args.bias)
             if i >= warm:
                 total += dt
                 flops_sum += tfl * 1e12 * dt
@@ -482,16 +486,21 @@ def run_ours(args, w):
     if args.bias != "none":
         bshape = (1, 1, w.Nq, w.Nk) if args.bias == "shared" else (w.B, w.H, w.Nq, w.Nk)
         ins.append(torch.randn(bshape, device=dev, generator=g).to(torch.bfloat16))
-    if args.backward:   # the forward's O and LSE and an upstream gradient are the inputs
+    if args.backward:   # the forward's O and LSE and an upstream gradient (and the bias) are the inputs
         dout = torch.randn(w.B, w.H, w.Nq, w.d, device=dev, generator=g).to(torch.bfloat16)
-        (attn.attn_fwd_causal if args.causal else attn.attn_fwd)(q, k, v, o, lse, w.B, w.H, w.Nq, w.Nk, w.d,
-                                                                 w.scale, stream)
-        ins = [q, k, v, o, dout, lse]
+        if args.bias != "none":
+            attn.attn_fwd_bias(q, k, v, ins[3], o, lse, w.B, w.H, w.Nq, w.Nk, w.d, w.scale, stream)
+            ins = [q, k, v, o, dout, lse, ins[3]]
+        else:
+            (attn.attn_fwd_causal if args.causal else attn.attn_fwd)(q, k, v, o, lse, w.B, w.H, w.Nq, w.Nk, w.d,
+                                                                     w.scale, stream)
+            ins = [q, k, v, o, dout, lse]
         outs = [torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)]
 
     def call(ins_, outs_, st):
         if args.backward:
-            attn.attn_bwd(*ins_, *outs_, w.B, w.H, w.Nq, w.Nk, w.d, w.scale, st, causal=args.causal)
+            attn.attn_bwd(*ins_[:6], *outs_, w.B, w.H, w.Nq, w.Nk, w.d, w.scale, st, causal=args.causal,
+                          bias=ins_[6] if len(ins_) > 6 else None)
         elif args.fp8_qk:
             attn.attn_fwd_fp8qk(*ins_[:3], *outs_, w.B, w.H, w.Nq, w.Nk, w.d, w.scale, descale[0], descale[1], st,
                                 causal=args.causal, bias=ins_[3] if args.bias != "none" else None)
@@ -638,7 +647,7 @@ def run_ours(args, w):
     }
     if rank == 0 and not args.no_cpu_baseline:
         if args.backward:
-            tfl, n, dt, thr = cpu_oracle_backward_sample(w, args.cpu_seconds, args.causal)
+            tfl, n, dt, thr = cpu_oracle_backward_sample(w, args.cpu_seconds, args.causal, args.bias)
             sample = f"backward of one head with {n} query rows x {w.Nk} keys of {w.describe()}, FP64, {dt:.1f} s"
         else:
             tfl, n, dt, thr = cpu_oracle_sample(w, args.cpu_seconds, causal=args.causal, bias_kind=args.bias,

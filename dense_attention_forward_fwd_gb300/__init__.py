@@ -86,6 +86,8 @@ def load_library(build_if_stale: bool = True) -> ctypes.CDLL:
             lib.attn_bwd.argtypes = [vp] * 9 + [i32] * 5 + [f32, vp]
             lib.attn_bwd.restype = i32
             lib.attn_bwd_causal.argtypes = lib.attn_bwd.argtypes
+            lib.attn_bwd_bias.argtypes = [vp] * 7 + [ctypes.c_longlong] * 3 + [vp] * 3 + [i32] * 5 + [f32, vp]
+            lib.attn_bwd_bias.restype = i32
             lib.attn_bwd_causal.restype = i32
             lib.attn_bwd_status.argtypes = [vp]
             lib.attn_bwd_status.restype = i32
@@ -342,12 +344,15 @@ def attn_fwd_noalloc(q, k, v, o, lse, B: int, H: int, Nq: int, Nk: int, d: int, 
 
 
 def attn_bwd(q, k, v, o, dout, lse, dq, dk, dv, B: int, H: int, Nq: int, Nk: int, d: int, scale: float,
-             stream=None, causal: bool = False) -> None:
+             stream=None, causal: bool = False, bias=None, bias_strides=None) -> None:
     """Enqueue the gradients dQ, dK, dV of the forward for upstream gradient ``dout`` (see
     include/attn_bwd.h). q, o, dout, dq: BF16 [B,H,Nq,d]; k, v, dk, dv: BF16 [B,H,Nk,d];
     lse: the forward's FP32 [B,H,Nq]. CUDA tensors or integer device pointers. causal: of
-    the causal forward (attn_bwd_causal)."""
+    the causal forward (attn_bwd_causal). bias: of the biased forward (attn_bwd_bias; the
+    bias as in :func:`attn_fwd_bias`, held fixed; not with causal)."""
     lib = load_library()
+    if bias is not None and causal:
+        raise ValueError("bias and causal together are not supported (put the mask in the bias)")
     args = (
         _ptr(q, "q", B * H * Nq * d, "bf16"), _ptr(k, "k", B * H * Nk * d, "bf16"),
         _ptr(v, "v", B * H * Nk * d, "bf16"), _ptr(o, "o", B * H * Nq * d, "bf16"),
@@ -355,11 +360,16 @@ def attn_bwd(q, k, v, o, dout, lse, dq, dk, dv, B: int, H: int, Nq: int, Nk: int
         _ptr(dq, "dq", B * H * Nq * d, "bf16"), _ptr(dk, "dk", B * H * Nk * d, "bf16"),
         _ptr(dv, "dv", B * H * Nk * d, "bf16"),
     )
-    fn = lib.attn_bwd_causal if causal else lib.attn_bwd
-    rc = fn(*args, int(B), int(H), int(Nq), int(Nk), int(d), float(scale),
+    tail = (int(B), int(H), int(Nq), int(Nk), int(d), float(scale),
             _stream_handle(stream, q, k, v, o, dout, lse, dq, dk, dv))
+    if bias is not None:
+        name = "attn_bwd_bias"
+        rc = lib.attn_bwd_bias(*args[:6], *_bias_arg(bias, B, H, Nq, Nk, bias_strides), *args[6:], *tail)
+    else:
+        name = "attn_bwd_causal" if causal else "attn_bwd"
+        rc = getattr(lib, name)(*args, *tail)
     if rc != ATTN_OK:
-        raise AttnError(rc, "attn_bwd_causal" if causal else "attn_bwd")
+        raise AttnError(rc, name)
 
 
 def attn_bwd_causal(q, k, v, o, dout, lse, dq, dk, dv, B: int, H: int, Nq: int, Nk: int, d: int, scale: float,

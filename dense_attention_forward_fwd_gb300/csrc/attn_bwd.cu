@@ -273,7 +273,18 @@ struct BwdParams {
   int withhold;   // test hook: the dK/dV producer stops before its second query tile
   float scale, scale_log2;
   unsigned long long wait_limit;
+  // attn_bwd_bias: the forward's additive bias, B_ij of head (b, h) = bias[b * bias_sb + h * bias_sh
+  // + i * bias_sq + j] (BF16, strides in elements), H heads per batch
+  const uint16_t* bias;
+  long long bias_sb, bias_sh, bias_sq;
+  int H;
 };
+
+// The bias of head bh at query row `row` (nullptr-free: callers check the ranges).
+__device__ __forceinline__ const uint16_t* bias_row(const BwdParams& p, int bh, int row) {
+  return p.bias + static_cast<long long>(bh / p.H) * p.bias_sb + static_cast<long long>(bh % p.H) * p.bias_sh +
+         static_cast<long long>(row) * p.bias_sq;
+}
 
 // Stores one 64-column half of this warp's 32 rows (pk: the thread's own row, packed
 // BF16 pairs) through the warp's staging tile so that each global store instruction
@@ -390,11 +401,14 @@ __global__ void __launch_bounds__(256) bwd_rows_kernel(const uint16_t* __restric
 // ---------------------------------------------------------------------------------
 // dK / dV: one block per (b, h, key tile)
 // ---------------------------------------------------------------------------------
-template <bool kCausal>
+template <bool kCausal, bool kBias>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
                     const BwdParams p) {
+  // With a bias the Q ring keeps two of its three slots: the third holds each compute warp's
+  // 4 KB bias staging tile (below).
+  constexpr int kSlotsQ = kBias ? 2 : kSlotsA;
   extern __shared__ __align__(1024) uint8_t smem[];
   const uint32_t base = smem_u32(smem);
   if (base & 1023u) {   // every thread leaves before any barrier, copy or TMEM allocation
@@ -419,7 +433,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     q0 = first_row > 0 ? first_row / kT : 0;
   }
   const int nq = p.q_tiles - q0;
-  auto sQ = [&](int j) { return base + kOffRingA + (j % kSlotsA) * kTileBytes; };
+  auto sQ = [&](int j) { return base + kOffRingA + (j % kSlotsQ) * kTileBytes; };
   auto sDO = [&](int j) { return base + kOffRingB + (j % kSlotsB) * kTileBytes; };
 
   if (warp == 0) {
@@ -432,14 +446,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       int issued = 0;   // query tiles whose Q and dO were both requested
       for (int j = 0; j < nq; ++j, ++issued) {
-        const int a = j % kSlotsA, b = j % kSlotsB;
-        if (j >= kSlotsA && !wait_phase(c, kBarEmptyA + a, (j / kSlotsA - 1) & 1, true)) break;
+        const int a = j % kSlotsQ, b = j % kSlotsB;
+        if (j >= kSlotsQ && !wait_phase(c, kBarEmptyA + a, (j / kSlotsQ - 1) & 1, true)) break;
         if (p.withhold && j == 1) break;   // test hook: the consumers' waits for this tile run out
         mbar_arrive_expect_tx(c.bar(kBarFullA + a), kTileBytes);
         for (int h = 0; h < 2; ++h) tma_load_3d(sQ(j) + h * kBoxBytes, &tmQ, c.bar(kBarFullA + a), h * 64, (q0 + j) * kT, bh);
         // dO_j's slot held dO_{j-2} and its rows
         if (j >= kSlotsB && !wait_phase(c, kBarEmptyB + b, (j / kSlotsB - 1) & 1, true)) {
-          wait_phase(c, kBarFullA + a, (j / kSlotsA) & 1, false);   // that Q copy is in flight
+          wait_phase(c, kBarFullA + a, (j / kSlotsQ) & 1, false);   // that Q copy is in flight
           break;
         }
         mbar_arrive_expect_tx(c.bar(kBarFullB + b), kTileBytes + kRowsBytes);
@@ -450,8 +464,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       // no copy into shared memory may be in flight when the block exits
       wait_phase(c, kBarFixed, 0, false);
-      for (int j = issued - kSlotsA < 0 ? 0 : issued - kSlotsA; j < issued; ++j)
-        wait_phase(c, kBarFullA + j % kSlotsA, (j / kSlotsA) & 1, false);
+      for (int j = issued - kSlotsQ < 0 ? 0 : issued - kSlotsQ; j < issued; ++j)
+        wait_phase(c, kBarFullA + j % kSlotsQ, (j / kSlotsQ) & 1, false);
       for (int j = issued - kSlotsB < 0 ? 0 : issued - kSlotsB; j < issued; ++j)
         wait_phase(c, kBarFullB + j % kSlotsB, (j / kSlotsB) & 1, false);
     }
@@ -525,6 +539,31 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int b = j % kSlotsB;
       const int j1 = j + 1;
       const bool more = j1 < nq;
+      // bias: the warp's 64 query rows x 32 keys (4 KB), requested before the waits as eight
+      // 16-byte pieces per thread (load i: row 8i + lane/4, keys 8 (lane%4) .. + 7 of the
+      // warp's 32; rows past Nq and keys past Nk read nothing), held as loaded until S^T is
+      // in registers, then passed through the warp's staging tile so that each thread reads
+      // its own key's column
+      uint4 braw[kBias ? 8 : 1];
+      if constexpr (kBias) {
+        const int kc = kt * kT + quarter * 32 + 8 * (lane & 3);   // the piece's first key
+        const int row0 = (q0 + j) * kT + 64 * grp + (lane >> 2);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int row = row0 + 8 * i;
+          braw[i] = make_uint4(0u, 0u, 0u, 0u);
+          if (row < p.Nq) {
+            const uint16_t* src = bias_row(p, bh, row) + kc;
+            if (kc + 8 <= p.Nk) {
+              braw[i] = __ldg(reinterpret_cast<const uint4*>(src));
+            } else {
+              uint32_t w[4] = {0u, 0u, 0u, 0u};
+              for (int e = 0; e < 8 && kc + e < p.Nk; ++e) w[e >> 1] |= static_cast<uint32_t>(__ldg(src + e)) << (16 * (e & 1));
+              braw[i] = make_uint4(w[0], w[1], w[2], w[3]);
+            }
+          }
+        }
+      }
       if (!wait_warp(c, kBarFullB + b, (j / kSlotsB) & 1) || !wait_warp(c, kBarSdP, j & 1)) {
         ok = false;
         break;
@@ -544,16 +583,32 @@ __global__ void __launch_bounds__(kThreads, 1)
       // P^T of the group's 64 query columns, kept in registers for dS^T; written over the
       // first 32 of the group's S^T columns as BF16 pairs and handed over first
       const float2 c2 = make_float2(p.scale_log2, p.scale_log2);
+      const float2 lg2 = make_float2(1.4426950408889634f, 1.4426950408889634f);
       float pv[64];
       {
         uint32_t xs[64];
         tmem_ld64(tS + lane_off + 64 * grp, xs);
+        // the bias tile: rows of 32 keys (64 bytes), row-major; thread `lane` reads column lane
+        const uint16_t* bst = reinterpret_cast<const uint16_t*>(smem + kOffRingA + 2 * kTileBytes + (warp - 4) * 4096);
+        if constexpr (kBias) {
+          uint4* dst = reinterpret_cast<uint4*>(smem + kOffRingA + 2 * kTileBytes + (warp - 4) * 4096);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) dst[(8 * i + (lane >> 2)) * 4 + (lane & 3)] = braw[i];
+          __syncwarp();
+        }
         uint32_t pw[32];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {   // query columns 4i .. 4i + 3 of the group
           const float4 l4 = *reinterpret_cast<const float4*>(nl + 4 * i);
-          const float2 a0 = ffma2(f2(xs[4 * i], xs[4 * i + 1]), c2, make_float2(l4.x, l4.y));
-          const float2 a1 = ffma2(f2(xs[4 * i + 2], xs[4 * i + 3]), c2, make_float2(l4.z, l4.w));
+          float2 n0 = make_float2(l4.x, l4.y), n1 = make_float2(l4.z, l4.w);
+          if constexpr (kBias) {   // + B log2 e: the biased scores' exponent
+            const uint32_t b0 = bst[(4 * i) * 32 + lane], b1 = bst[(4 * i + 1) * 32 + lane];
+            const uint32_t b2 = bst[(4 * i + 2) * 32 + lane], b3 = bst[(4 * i + 3) * 32 + lane];
+            n0 = ffma2(f2(b0 << 16, b1 << 16), lg2, n0);
+            n1 = ffma2(f2(b2 << 16, b3 << 16), lg2, n1);
+          }
+          const float2 a0 = ffma2(f2(xs[4 * i], xs[4 * i + 1]), c2, n0);
+          const float2 a1 = ffma2(f2(xs[4 * i + 2], xs[4 * i + 3]), c2, n1);
           float q[4] = {ex2(a0.x), ex2(a0.y), ex2(a1.x), ex2(a1.y)};
           if (mask_warp) {
 #pragma unroll
@@ -566,13 +621,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tmem_st32(tS + lane_off + 64 * grp, pw);
       }
-      if (!hand_over(kBarPAll, kBarFullA + j1 % kSlotsA, (j1 / kSlotsA) & 1, more) ||
+      if (!hand_over(kBarPAll, kBarFullA + j1 % kSlotsQ, (j1 / kSlotsQ) & 1, more) ||
           !wait_warp(c, kBarDPReady, j & 1)) {
         ok = false;
         break;
       }
       // dP^T_j complete: so is dK_{j-1}, the last reader of Q_{j-1}
-      if (j > 0 && releaser) mbar_arrive(c.bar(kBarEmptyA + (j - 1) % kSlotsA));
+      if (j > 0 && releaser) mbar_arrive(c.bar(kBarEmptyA + (j - 1) % kSlotsQ));
       __syncwarp();
       tc_fence_after();
       {
@@ -611,7 +666,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 // ---------------------------------------------------------------------------------
 // dQ: one block per (b, h, query tile)
 // ---------------------------------------------------------------------------------
-template <bool kCausal>
+template <bool kCausal, bool kBias>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
@@ -721,8 +776,38 @@ __global__ void __launch_bounds__(kThreads, 1)
     // by the MMAs that hand-over releases) have landed; another frees V_j's slot.
     const bool ringer = warp == 4 && lane == 0, releaser = warp == 8 && lane == 0;
     bool ok = true;
+    const float2 lg2 = make_float2(1.4426950408889634f, 1.4426950408889634f);
     for (int j = 0; j < nk; ++j) {
       const int j1 = j + 1;
+      // bias: this thread's row over the group's 64 key columns, as BF16 pairs, requested
+      // before the waits: eight 16-byte loads when all 64 keys are inside Nk (strides are
+      // multiples of 8 elements), else key by key; nothing past Nq or Nk is read. (Staging
+      // them through shared memory, for loads that cover whole row pieces, needs one of the
+      // K ring's three slots: measured slower, 1.12 against 0.92 ms on square-4k.)
+      uint32_t bw[kBias ? 32 : 1];
+      if constexpr (kBias) {
+        const int k0 = j * kT + 64 * grp;
+        const int nvalid = p.Nk - k0;
+        if (qrow < p.Nq && nvalid >= 64) {
+          const uint4* src = reinterpret_cast<const uint4*>(bias_row(p, bh, qrow) + k0);
+#pragma unroll
+          for (int g = 0; g < 8; ++g) {
+            const uint4 t = __ldg(src + g);
+            bw[4 * g] = t.x;
+            bw[4 * g + 1] = t.y;
+            bw[4 * g + 2] = t.z;
+            bw[4 * g + 3] = t.w;
+          }
+        } else {
+          const uint16_t* src = qrow < p.Nq ? bias_row(p, bh, qrow) + k0 : nullptr;
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const uint32_t lo = src != nullptr && 2 * i < nvalid ? __ldg(src + 2 * i) : 0u;
+            const uint32_t hi = src != nullptr && 2 * i + 1 < nvalid ? __ldg(src + 2 * i + 1) : 0u;
+            bw[i] = lo | (hi << 16);
+          }
+        }
+      }
       if (!wait_warp(c, kBarSdP, j & 1)) {
         ok = false;
         break;
@@ -757,7 +842,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t dw[32];
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
-          const float2 a = ffma2(f2(xs[2 * i], xs[2 * i + 1]), c2, nl2);
+          float2 n = nl2;
+          if constexpr (kBias) n = ffma2(f2(bw[i] << 16, bw[i] & 0xffff0000u), lg2, nl2);   // + B log2 e
+          const float2 a = ffma2(f2(xs[2 * i], xs[2 * i + 1]), c2, n);
           float p0 = ex2(a.x), p1 = ex2(a.y);
           if (!full) {
             p0 = 2 * i < valid ? p0 : 0.0f;
@@ -841,36 +928,44 @@ int get_rows_workspace(int dev, cudaStream_t stream, size_t bytes, float** out) 
   return ATTN_OK;
 }
 
-std::atomic<int> g_attr_done[2] = {{0}, {0}};   // per instantiation (plain, causal)
+std::atomic<int> g_attr_done[3] = {{0}, {0}, {0}};   // per instantiation (plain, causal, bias)
 
-template <bool kCausal>
+template <bool kCausal, bool kBias = false>
 int launch_bwd(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, const CUtensorMap& mdo,
                const BwdParams& p, long long bh, long long k_tiles, long long q_tiles, cudaStream_t s) {
-  if (!g_attr_done[kCausal].load(std::memory_order_acquire)) {
-    if (cudaFuncSetAttribute(bwd_dkdv_kernel<kCausal>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemKV) !=
-            cudaSuccess ||
-        cudaFuncSetAttribute(bwd_dq_kernel<kCausal>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemQ) !=
+  constexpr int kInst = kBias ? 2 : (kCausal ? 1 : 0);
+  if (!g_attr_done[kInst].load(std::memory_order_acquire)) {
+    if (cudaFuncSetAttribute(bwd_dkdv_kernel<kCausal, kBias>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kSmemKV) != cudaSuccess ||
+        cudaFuncSetAttribute(bwd_dq_kernel<kCausal, kBias>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemQ) !=
             cudaSuccess)
       return ATTN_ERR_CUDA;
-    g_attr_done[kCausal].store(1, std::memory_order_release);
+    g_attr_done[kInst].store(1, std::memory_order_release);
   }
   cudaLaunchConfig_t cfg = {};
   cfg.blockDim = dim3(kThreads);
   cfg.stream = s;
   cfg.gridDim = dim3(static_cast<unsigned>(bh * k_tiles));
   cfg.dynamicSmemBytes = kSmemKV;
-  if (cudaLaunchKernelEx(&cfg, bwd_dkdv_kernel<kCausal>, mq, mk, mv, mdo, p) != cudaSuccess) return ATTN_ERR_CUDA;
+  if (cudaLaunchKernelEx(&cfg, bwd_dkdv_kernel<kCausal, kBias>, mq, mk, mv, mdo, p) != cudaSuccess)
+    return ATTN_ERR_CUDA;
   g_bwd_launches.fetch_add(1, std::memory_order_relaxed);
   cfg.gridDim = dim3(static_cast<unsigned>(bh * q_tiles));
   cfg.dynamicSmemBytes = kSmemQ;
-  if (cudaLaunchKernelEx(&cfg, bwd_dq_kernel<kCausal>, mq, mk, mv, mdo, p) != cudaSuccess) return ATTN_ERR_CUDA;
+  if (cudaLaunchKernelEx(&cfg, bwd_dq_kernel<kCausal, kBias>, mq, mk, mv, mdo, p) != cudaSuccess)
+    return ATTN_ERR_CUDA;
   g_bwd_launches.fetch_add(1, std::memory_order_relaxed);
   return ATTN_OK;
 }
 
+struct BwdBias {
+  const void* ptr;
+  long long sb, sh, sq;
+};
+
 int backward(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
              void* dq, void* dk, void* dv, int B, int H, int Nq, int Nk, int d, float scale, void* stream,
-             bool causal) {
+             bool causal, const BwdBias* bias = nullptr) {
   if (B < 0 || H < 0 || Nq < 0 || Nk < 0) return ATTN_ERR_INVALID_ARG;
   if (d != kD) return ATTN_ERR_UNSUPPORTED;
   if (!std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
@@ -890,6 +985,16 @@ int backward(const void* q, const void* k, const void* v, const void* o, const v
   if ((bh * q_tiles * kT + 7) / 8 > INT_MAX) return ATTN_ERR_UNSUPPORTED;   // the row pass's grid
   const long long max_rows = static_cast<long long>(Nq > Nk ? Nq : Nk);
   if (bh > (LLONG_MAX / 256) / max_rows) return ATTN_ERR_INVALID_ARG;
+  if (bias != nullptr) {   // the rules of attn_fwd_bias
+    if (!bias->ptr || bias->sb < 0 || bias->sh < 0 || bias->sq < 0) return ATTN_ERR_INVALID_ARG;
+    constexpr long long kCap = LLONG_MAX / 8;
+    const long long ext[3] = {B - 1LL, H - 1LL, Nq - 1LL};
+    const long long str[3] = {bias->sb, bias->sh, bias->sq};
+    for (int i = 0; i < 3; ++i)
+      if (str[i] > 0 && ext[i] > kCap / str[i]) return ATTN_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(bias->ptr) & 15u) || ((bias->sb | bias->sh | bias->sq) & 7))
+      return ATTN_ERR_MISALIGNED;
+  }
 
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return ATTN_ERR_CUDA;
@@ -914,6 +1019,11 @@ int backward(const void* q, const void* k, const void* v, const void* o, const v
   p.causal = causal ? 1 : 0;
   p.off = causal ? Nk - Nq : 0;
   p.withhold = g_bwd_withhold.load(std::memory_order_relaxed);
+  p.bias = bias ? static_cast<const uint16_t*>(bias->ptr) : nullptr;
+  p.bias_sb = bias ? bias->sb : 0;
+  p.bias_sh = bias ? bias->sh : 0;
+  p.bias_sq = bias ? bias->sq : 0;
+  p.H = H;
   float* rows = nullptr;
   {
     const int rc = get_rows_workspace(dev, s, static_cast<size_t>(bh) * p.q_pad * 2 * sizeof(float), &rows);
@@ -927,6 +1037,7 @@ int backward(const void* q, const void* k, const void* v, const void* o, const v
   if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
   g_bwd_launches.fetch_add(1, std::memory_order_relaxed);
 
+  if (bias != nullptr) return launch_bwd<false, true>(mq, mk, mv, mdo, p, bh, k_tiles, q_tiles, s);
   return causal ? launch_bwd<true>(mq, mk, mv, mdo, p, bh, k_tiles, q_tiles, s)
                 : launch_bwd<false>(mq, mk, mv, mdo, p, bh, k_tiles, q_tiles, s);
 }
@@ -943,6 +1054,14 @@ extern "C" int attn_bwd_causal(const void* q, const void* k, const void* v, cons
                                const float* lse, void* dq, void* dk, void* dv, int B, int H, int Nq, int Nk, int d,
                                float scale, void* stream) {
   return backward(q, k, v, o, dout, lse, dq, dk, dv, B, H, Nq, Nk, d, scale, stream, true);
+}
+
+extern "C" int attn_bwd_bias(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                             const float* lse, const void* bias, long long bias_stride_b, long long bias_stride_h,
+                             long long bias_stride_q, void* dq, void* dk, void* dv, int B, int H, int Nq, int Nk,
+                             int d, float scale, void* stream) {
+  const BwdBias ba = {bias, bias_stride_b, bias_stride_h, bias_stride_q};
+  return backward(q, k, v, o, dout, lse, dq, dk, dv, B, H, Nq, Nk, d, scale, stream, false, &ba);
 }
 
 extern "C" int attn_bwd_status(void* stream) {

@@ -64,6 +64,22 @@ int attn_bwd_causal(const void* q, const void* k, const void* v, const void* o, 
                     const float* lse, void* dq, void* dk, void* dv, int B, int H, int Nq, int Nk, int d,
                     float scale, void* stream);
 
+/*
+ * attn_bwd_bias -- gradients dQ, dK, dV of the biased forward (attn_fwd_bias: S = scale Q K^T
+ * + B, the definition's optional B, "FlashAttention'ı Anlamak Bölüm 1", section 0.2), the bias
+ * held fixed: it enters only through the recomputed P = exp(scale q.k + B - LSE), and its
+ * own gradient (dB = dS) is not formed. bias and its strides as in attn_fwd_bias (with its
+ * argument rules: non-null, non-negative strides whose last offset fits 64 bits, 16-byte
+ * aligned, strides multiples of 8 elements); o and lse from attn_fwd_bias with the same bias.
+ * Other arguments, layouts and return values are those of attn_bwd. Each block reads the
+ * bias of its tile pairs once per kernel (the dK/dV kernel by keys, the dQ kernel by rows).
+ * Not with the causal mask (a causal bias carries one).
+ */
+int attn_bwd_bias(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                  const float* lse, const void* bias, long long bias_stride_b, long long bias_stride_h,
+                  long long bias_stride_q, void* dq, void* dk, void* dv, int B, int H, int Nq, int Nk, int d,
+                  float scale, void* stream);
+
 /* Synchronises `stream`, then reads and clears the backward kernels' timeout status:
  * ATTN_OK, ATTN_ERR_TIMEOUT or ATTN_ERR_CUDA. */
 int attn_bwd_status(void* stream);

@@ -47,7 +47,7 @@ def test_reference_arm_prints_the_contract_line(flags):
 
 @pytest.mark.parametrize("flags", [("--mxfp8", "--bias", "full"), ("--fp8-qk", "--bias", "shared", "--causal"),
                                    ("--fp8", "--fp8-qk"),
-                                   ("--bias", "full", "--backward"), ("--head-dim", "256", "--backward"),
+                                   ("--bias", "full", "--causal"), ("--head-dim", "256", "--backward"),
                                    ("--fp8", "--backward")])
 def test_flags_without_an_entry_point_are_refused(flags):
     r = run_bench(*flags)

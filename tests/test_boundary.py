@@ -28,7 +28,7 @@ def test_header_declares_the_entry_points():
     names = declared_functions()
     assert {"attn_fwd", "attn_fwd_causal", "attn_fwd_bias", "attn_fwd_fp8qk", "attn_fwd_fp8", "attn_fwd_o32", "attn_fwd_noalloc", "attn_bwd", "attn_bwd_causal",
             "attn_fwd_fp8qk_causal", "attn_fwd_fp8_causal", "attn_fwd_mxfp8", "attn_fwd_mxfp8_causal",
-            "attn_fwd_fp8qk_bias", "attn_fwd_fp8_bias",
+            "attn_fwd_fp8qk_bias", "attn_fwd_fp8_bias", "attn_bwd_bias",
             "attn_bwd_status", "attn_bwd_set_wait_limit",
             "attn_bwd_kernel_count", "attn_fwd_status", "attn_status_string",
             "attn_fwd_set_wait_limit", "attn_fwd_kernel_count"} <= set(names)
@@ -371,3 +371,32 @@ def test_no_launch_without_gpu_calls():
     before = attn.attn_fwd_kernel_count()
     call(d=64)
     assert attn.attn_fwd_kernel_count() == before
+
+
+def call_bwd_bias(q=A, k=A, v=A, o=A, do=A, lse=A, bias=A, sb=0, sh=0, sq=128, dq=A, dk=A, dv=A, B=1, H=1, Nq=128,
+                  Nk=128, d=128, scale=0.125):
+    return attn.load_library().attn_bwd_bias(q, k, v, o, do, lse, bias, sb, sh, sq, dq, dk, dv, B, H, Nq, Nk, d, scale,
+                                             None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(bias=None), attn.ATTN_ERR_INVALID_ARG),
+    (dict(sh=-8), attn.ATTN_ERR_INVALID_ARG),
+    (dict(sb=1 << 62, B=2), attn.ATTN_ERR_INVALID_ARG),
+    (dict(bias=A + 8), attn.ATTN_ERR_MISALIGNED),
+    (dict(sq=100), attn.ATTN_ERR_MISALIGNED),
+    (dict(do=None), attn.ATTN_ERR_INVALID_ARG),
+    (dict(d=64), attn.ATTN_ERR_UNSUPPORTED),
+    (dict(Nk=0), attn.ATTN_ERR_INVALID_ARG),
+    (dict(B=0), attn.ATTN_OK),
+])
+def test_bwd_bias_argument_checks(kw, code):
+    before = attn.attn_bwd_kernel_count()
+    assert call_bwd_bias(**kw) == code
+    assert attn.attn_bwd_kernel_count() == before
+
+
+def test_bwd_bias_binding_refuses_causal():
+    with pytest.raises(ValueError):
+        attn.attn_bwd(A, A, A, A, A, A, A, A, A, 1, 1, 128, 128, 128, 0.1, causal=True, bias=A,
+                      bias_strides=(0, 0, 128))

@@ -33,7 +33,7 @@ def make_dout(B, H, Nq, seed):
     return f32_to_bf16_bits(rng.standard_normal((B, H, Nq, 128), dtype=np.float32))
 
 
-def run_fwd_bwd(attn, q, k, v, do, scale, stream=None, causal=False):
+def run_fwd_bwd(attn, q, k, v, do, scale, stream=None, causal=False, bias=None):
     import torch
     B, H, Nq, d = q.shape
     Nk = k.shape[2]
@@ -42,23 +42,27 @@ def run_fwd_bwd(attn, q, k, v, do, scale, stream=None, causal=False):
     lse = torch.empty((B, H, Nq), dtype=torch.float32, device="cuda")
     if stream is not None:
         stream.wait_stream(torch.cuda.current_stream())
-    (attn.attn_fwd_causal if causal else attn.attn_fwd)(qd, kd, vd, o, lse, B, H, Nq, Nk, d, scale, stream)
+    bd = None if bias is None else to_device(bias)
+    if bd is not None:
+        attn.attn_fwd_bias(qd, kd, vd, bd, o, lse, B, H, Nq, Nk, d, scale, stream)
+    else:
+        (attn.attn_fwd_causal if causal else attn.attn_fwd)(qd, kd, vd, o, lse, B, H, Nq, Nk, d, scale, stream)
     dq = torch.full((B, H, Nq, d), float("nan"), dtype=torch.bfloat16, device="cuda")
     dk = torch.full((B, H, Nk, d), float("nan"), dtype=torch.bfloat16, device="cuda")
     dv = torch.full((B, H, Nk, d), float("nan"), dtype=torch.bfloat16, device="cuda")
     if stream is not None:   # the inputs and outputs were made on the current stream
         stream.wait_stream(torch.cuda.current_stream())
-    attn.attn_bwd(qd, kd, vd, o, dod, lse, dq, dk, dv, B, H, Nq, Nk, d, scale, stream, causal=causal)
+    attn.attn_bwd(qd, kd, vd, o, dod, lse, dq, dk, dv, B, H, Nq, Nk, d, scale, stream, causal=causal, bias=bd)
     assert attn.attn_fwd_status(stream) == attn.ATTN_OK
     assert attn.attn_bwd_status(stream) == attn.ATTN_OK
     return bf16_to_np(dq), bf16_to_np(dk), bf16_to_np(dv)
 
 
-def check_bwd(attn, B, H, Nq, Nk, seed, qk_mult=1.0, scale=SCALE, causal=False):
+def check_bwd(attn, B, H, Nq, Nk, seed, qk_mult=1.0, scale=SCALE, causal=False, bias=None):
     q, k, v = make_qkv(B, H, Nq, Nk, seed=seed, qk_mult=qk_mult)
     do = make_dout(B, H, Nq, seed + 1)
-    got = run_fwd_bwd(attn, q, k, v, do, scale, causal=causal)
-    ref = oracle.attention_bwd(q, k, v, do, scale, causal=causal)
+    got = run_fwd_bwd(attn, q, k, v, do, scale, causal=causal, bias=bias)
+    ref = oracle.attention_bwd(q, k, v, do, scale, causal=causal, bias=bias)
     report = {}
     for name, g, r in zip(("dq", "dk", "dv"), got, ref):
         assert np.all(np.isfinite(g)), f"{name}: non-finite output"
@@ -183,3 +187,67 @@ def test_bwd_workload_sampled_heads(gpu_lib, name, causal, heads):
             err = np.abs(g.astype(np.float64) - r)
             assert err.max() <= MAX_REL * np.abs(r).max(), f"{gname} head ({b},{h}): max err {err.max():.3e}"
             assert err.mean() <= MEAN_REL * np.abs(r).mean(), f"{gname} head ({b},{h}): mean err {err.mean():.3e}"
+
+
+# ---- the backward of the biased forward (attn_bwd_bias), the bias held fixed ------------------
+
+def bias_shape(kind, B, H, Nq, Nk):
+    return {"full": (B, H, Nq, Nk), "shared": (1, 1, Nq, Nk), "key": (1, 1, 1, Nk)}[kind]
+
+
+@pytest.mark.parametrize("B,H,Nq,Nk,kind", [
+    (1, 1, 128, 128, "full"),
+    (1, 2, 256, 384, "full"),
+    (2, 3, 300, 1000, "shared"),   # ragged query and key tails; one [Nq, Nk] bias for every head
+    (1, 1, 1, 200, "full"),        # a single query row; keys end inside a 64-key group
+    (1, 2, 129, 136, "key"),       # one bias per key
+    (1, 4, 1024, 640, "full"),
+])
+def test_bwd_bias_parity(gpu_lib, B, H, Nq, Nk, kind):
+    from dense_attention_forward_fwd_gb300.inputs import make_bias
+    bias = make_bias(bias_shape(kind, B, H, Nq, Nk), seed=12500 + Nq + Nk, std=2.0)
+    check_bwd(gpu_lib, B, H, Nq, Nk, seed=12400 + Nq + Nk, bias=bias)
+
+
+def test_bwd_bias_peaked_and_negative_scale(gpu_lib):
+    from dense_attention_forward_fwd_gb300.inputs import make_bias
+    check_bwd(gpu_lib, 1, 2, 512, 768, seed=12600, qk_mult=3.0, bias=make_bias((1, 2, 512, 768), seed=12601, std=8.0))
+    check_bwd(gpu_lib, 1, 1, 256, 384, seed=12602, scale=-0.0883883461356163,
+              bias=make_bias((1, 1, 256, 384), seed=12603, std=2.0))
+
+
+def test_bwd_bias_masks(gpu_lib):
+    # -inf entries remove keys, two whole key tiles of them included, and a causal-pattern bias
+    # gives the causal backward's gradients
+    from dense_attention_forward_fwd_gb300.inputs import BF16_NEG_INF, make_bias
+    bias = make_bias((1, 1, 1, 1024), seed=12700)
+    bias[..., :300] = BF16_NEG_INF
+    bias[..., 900:] = BF16_NEG_INF
+    check_bwd(gpu_lib, 1, 2, 384, 1024, seed=12701, bias=bias)
+    Nq, Nk = 256, 384
+    mask = np.zeros((1, 1, Nq, Nk), dtype=np.uint16)
+    for i in range(Nq):
+        mask[0, 0, i, i + Nk - Nq + 1:] = BF16_NEG_INF
+    q, k, v = make_qkv(1, 2, Nq, Nk, seed=12702)
+    do = make_dout(1, 2, Nq, 12703)
+    gb = run_fwd_bwd(gpu_lib, q, k, v, do, SCALE, bias=mask)
+    gc = run_fwd_bwd(gpu_lib, q, k, v, do, SCALE, causal=True)
+    for a, b in zip(gb, gc):
+        assert np.max(np.abs(a - b)) <= 2e-2 * np.abs(b).max()
+
+
+def test_bwd_bias_zero_is_the_plain_gradient(gpu_lib):
+    q, k, v = make_qkv(1, 2, 256, 512, seed=12704)
+    do = make_dout(1, 2, 256, 12705)
+    gb = run_fwd_bwd(gpu_lib, q, k, v, do, SCALE, bias=np.zeros((1, 1, 1, 512), dtype=np.uint16))
+    g0 = run_fwd_bwd(gpu_lib, q, k, v, do, SCALE)
+    for a, b in zip(gb, g0):
+        assert np.max(np.abs(a - b)) <= 2e-2 * np.abs(b).max()
+
+
+@pytest.mark.parametrize("kind", ["shared", "full"])
+def test_bwd_bias_one_head_of_the_square_workload(gpu_lib, kind):
+    # square-4k's shape for one head, with a shared or per-head bias, as `bench.py --backward --bias` times it
+    from dense_attention_forward_fwd_gb300.inputs import make_bias
+    bias = make_bias(bias_shape(kind, 1, 1, 4096, 4096), seed=12706, std=1.0)
+    check_bwd(gpu_lib, 1, 1, 4096, 4096, seed=12707, bias=bias)

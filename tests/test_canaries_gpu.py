@@ -129,3 +129,11 @@ def test_backward(gpu_lib, B, H, Nq, Nk, causal):
     fv, dv = guarded((B, H, Nk, 128), "bf16", "cuda")
     gpu_lib.attn_bwd(q, k, v, o, do, lse, dq, dk, dv, B, H, Nq, Nk, 128, SCALE, causal=causal)
     check(gpu_lib, ((fq, dq), "bf16"), ((fk, dk), "bf16"), ((fv, dv), "bf16"))
+    if not causal and Nk % 8 == 0:   # the biased backward (bias rows on 16-byte boundaries)
+        bias = to_device(make_bias((B, H, Nq, Nk), seed=17450, std=1.0))
+        gpu_lib.attn_fwd_bias(q, k, v, bias, o, lse, B, H, Nq, Nk, 128, SCALE)
+        fq, dq = guarded((B, H, Nq, 128), "bf16", "cuda")
+        fk, dk = guarded((B, H, Nk, 128), "bf16", "cuda")
+        fv, dv = guarded((B, H, Nk, 128), "bf16", "cuda")
+        gpu_lib.attn_bwd(q, k, v, o, do, lse, dq, dk, dv, B, H, Nq, Nk, 128, SCALE, bias=bias)
+        check(gpu_lib, ((fq, dq), "bf16"), ((fk, dk), "bf16"), ((fv, dv), "bf16"))
