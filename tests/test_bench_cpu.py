@@ -77,6 +77,8 @@ def test_traffic_keys_match_the_recorded_ones():
              "rect-4k-8k-fp8": ("rect-4k-8k", {"fp8": True}), "square-4k-causal": ("square-4k", {"causal": True}),
              "rect-4k-8k-bias-shared": ("rect-4k-8k", {"bias": "shared"}),
              "square-4k-backward": ("square-4k", {"backward": True}),
+             "square-4k-bias-shared-backward": ("square-4k", {"bias": "shared", "backward": True}),
+             "rect-4k-8k-bias-shared-fp8qk": ("rect-4k-8k", {"bias": "shared", "fp8_qk": True}),
              "square-4k-d256": ("square-4k", {"d": 256})}
     recorded = json.load(open(os.path.join(ROOT, "profiles", "traffic.json")))
     assert set(recorded) <= set(cases)
