@@ -65,6 +65,7 @@
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <atomic>
 #include <cfloat>
 #include <climits>
@@ -72,6 +73,7 @@
 #include <cstdint>
 #include <map>
 #include <mutex>
+#include <vector>
 #include <utility>
 
 #include "attn_fwd.h"
@@ -195,15 +197,22 @@ struct Segment {
   int kv0, kv1;   // key steps [kv0, kv1) of the group
   int which;      // 0: first segment of this block's split share, 1: its last
   bool split;     // other blocks hold other key steps of this group
+  // split-region numbering (split groups only): the group's first key step, its number of
+  // key steps, and its index among the split region's groups (its merge counters)
+  long long x0;
+  int glen, cidx;
 };
 
 // The segments of one block, in processing order; every role of the block walks the
 // same sequence.
 //
 // Causal launches: a group needs only the keys up to its last row's diagonal, so groups
-// differ in length. They are processed whole (no split), longest first: list position x
-// holds diagonal position q_groups - 1 - x / (B*H) of head x % (B*H), and block b takes
-// position b of even waves and grid - 1 - b of odd ones, which evens out the waves.
+// differ in length. List position x holds diagonal position q_groups - 1 - x / (B*H) of
+// head x % (B*H) (longest first). With many groups they are processed whole: block b takes
+// position b of even waves and grid - 1 - b of odd ones, which evens out the waves. With
+// few (sk_steps > 0) the list's key steps are concatenated and cut into equal shares, as
+// the split region of a non-causal launch: a long group is then split between blocks and
+// merged like one.
 struct SegIter {
   int n_kv, dp_groups, grid, next_dp;
   long long sk_begin, sk_end, sk_pos;
@@ -223,7 +232,38 @@ struct SegIter {
     Nq = p.Nq;
     wave = 0;
   }
+  // causal split shares: the list level (diagonal position) holding sk_pos and its first step
+  int lvl = 0;
+  long long lvl_start = 0;
+  __device__ int level_len(int level) const {   // key steps of each group of a list level
+    const int qg = q_groups - 1 - level;
+    const int row_end = min(Nq, (qg + 1) * (kQTiles * kBM));
+    return (row_end + causal_off + kBN - 1) / kBN;
+  }
   __device__ bool next(Segment& sg) {
+    if (causal && sk_end > 0) {
+      if (sk_pos >= sk_end) return false;
+      int len = level_len(lvl);
+      while (sk_pos >= lvl_start + static_cast<long long>(bh_count) * len) {
+        lvl_start += static_cast<long long>(bh_count) * len;
+        len = level_len(++lvl);
+      }
+      const long long in_lvl = sk_pos - lvl_start;
+      const int h = static_cast<int>(div_floor(in_lvl, len));
+      const int kv0 = static_cast<int>(in_lvl - static_cast<long long>(h) * len);
+      const long long left = sk_end - sk_pos;
+      const int kv1 = left < len - kv0 ? kv0 + static_cast<int>(left) : len;
+      sg.group = h * q_groups + (q_groups - 1 - lvl);
+      sg.kv0 = kv0;
+      sg.kv1 = kv1;
+      sg.which = sk_pos == sk_begin ? 0 : 1;
+      sg.split = !(kv0 == 0 && kv1 == len);
+      sg.x0 = lvl_start + static_cast<long long>(h) * len;
+      sg.glen = len;
+      sg.cidx = lvl * bh_count + h;
+      sk_pos = sg.x0 + kv1;
+      return true;
+    }
     if (causal) {
       const int pos = (wave & 1) ? grid - 1 - static_cast<int>(blockIdx.x) : static_cast<int>(blockIdx.x);
       const long long x = static_cast<long long>(wave) * grid + pos;
@@ -258,6 +298,9 @@ struct SegIter {
       sg.kv1 = kv1;
       sg.which = sk_pos == sk_begin ? 0 : 1;
       sg.split = !(kv0 == 0 && kv1 == n_kv);
+      sg.x0 = g_rel * n_kv;
+      sg.glen = n_kv;
+      sg.cidx = static_cast<int>(g_rel);
       sk_pos = g_rel * n_kv + kv1;
       return true;
     }
@@ -1185,7 +1228,9 @@ __device__ void run_softmax(const Ctl& c, uint32_t tmem, uint8_t* stage, const P
           tmem_st8(tO + ch * 8, ov);
         }
       }
-      const float neg_m = (kBias && m_used == -INFINITY) ? 0.0f : -m_used;   // every p is 0 then
+      // every p is 0 then: a row that has seen only -inf (a bias, or keys past its diagonal
+      // in a causal share that starts after them)
+      const float neg_m = ((kBias || p.causal) && m_used == -INFINITY) ? 0.0f : -m_used;
       // The BF16 rounding of P matters most for the tile's largest term, which the stale
       // running max leaves anywhere in [1, 2^kRescaleLog2]. corr accumulates that term's
       // rounding error, so that l + corr is the sum of the weights the tensor core
@@ -1295,12 +1340,11 @@ __device__ void run_softmax(const Ctl& c, uint32_t tmem, uint8_t* stage, const P
     } else {
       // This block holds only some key steps of the group. Counters count, per 32 rows,
       // the shares that have left their record; the last share to finish merges.
-      const long long g_rel = sg.group - p.dp_groups;
-      const long long x0 = g_rel * p.n_kv;
+      const long long x0 = sg.x0;
       const int grid = static_cast<int>(gridDim.x);
       const int c_first = sk_block_of(x0, p.sk_steps, grid);
-      const int c_last = sk_block_of(x0 + p.n_kv - 1, p.sk_steps, grid);
-      unsigned int* ctr = p.cnt + (g_rel * kQTiles + tile) * 4 + quarter;
+      const int c_last = sk_block_of(x0 + sg.glen - 1, p.sk_steps, grid);
+      unsigned int* ctr = p.cnt + (static_cast<long long>(sg.cidx) * kQTiles + tile) * 4 + quarter;
       unsigned int arrived = 0;
       if (lane == 0) arrived = ld_acquire(ctr);
       __syncwarp();
@@ -1898,8 +1942,37 @@ int forward_causal(const void* q, const void* k, const void* v, void* o, float* 
     p.sfv = static_cast<const uint8_t*>(mx->svt);
     p.ldsv = mx->ldsv;
   }
-  const int grid = static_cast<int>(n_groups < sms ? n_groups : sms);
+  // Few groups (under two waves): the list's key steps are shared out evenly and long
+  // groups are split and merged (SegIter); otherwise whole groups in balanced waves.
+  int grid = static_cast<int>(n_groups < sms ? n_groups : sms);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (n_groups < 2LL * sms) {
+    // level l of the list (diagonal position q_groups - 1 - l) holds bh groups of len(l) steps
+    std::vector<long long> level_start(static_cast<size_t>(q_groups) + 1, 0);
+    for (long long l = 0; l < q_groups; ++l) {
+      const long long row_end = std::min<long long>(Nq, (q_groups - l) * (kQTiles * kBM));
+      level_start[l + 1] = level_start[l] + bh * ((row_end + p.causal_off + kBN - 1) / kBN);
+    }
+    const long long total = level_start[q_groups];
+    const long long g = total / kMinSegSteps;
+    grid = static_cast<int>(g < 1 ? 1 : (g > sms ? sms : g));
+    p.sk_steps = total;
+    // a share boundary inside a group needs the merge workspace
+    bool has_split = false;
+    for (int c = 1; c < grid && !has_split; ++c) {
+      const long long x = sk_share_start(c, total, grid);
+      long long l = 0;
+      while (level_start[l + 1] <= x) ++l;
+      const long long len = (level_start[l + 1] - level_start[l]) / bh;
+      if ((x - level_start[l]) % len != 0) has_split = true;
+    }
+    if (has_split) {
+      const size_t part_bytes = static_cast<size_t>(grid) * kPartBytesPerBlock;
+      const size_t cnt_bytes = static_cast<size_t>(n_groups) * kQTiles * 4 * sizeof(unsigned int);
+      const int rc = get_workspace(dev, s, part_bytes, cnt_bytes, &p.part, &p.cnt, &p.cnt_next, &p.cnt_len);
+      if (rc != ATTN_OK) return rc;
+    }
+  }
   if (f8 == 3)
     return scale > 0.0f ? launch<true, false, 3>(mq, mk, mv, p, grid, dev, s)
                         : launch<false, false, 3>(mq, mk, mv, p, grid, dev, s);
