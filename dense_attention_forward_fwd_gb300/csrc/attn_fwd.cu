@@ -142,6 +142,7 @@ constexpr int kPartFloatsPerTile = kD * kBM + 3 * kBM;
 constexpr size_t kPartBytesPerBlock = size_t(2) * kQTiles * kPartFloatsPerTile * sizeof(float);
 static_assert(kPartFloatsPerTile % 4 == 0, "each tile record must start on a 16-byte boundary");
 constexpr int kMinSegSteps = 8;   // smallest share of a group worth a block of its own
+constexpr int kMaxGrid = 160;     // blocks of a launch at most (one per SM)
 
 struct Params {
   uint16_t* o;            // BF16 bits [BH, Nq, 128]
@@ -151,7 +152,8 @@ struct Params {
   int n_kv;               // ceil(Nk / kBN)
   int kv_tail;            // valid keys in the last K/V tile, 1..128
   int dp_groups;          // groups [0, dp_groups) are processed whole, group g by block g % grid
-  long long sk_steps;     // key steps of groups [dp_groups, n_groups), split evenly over the blocks
+  long long sk_steps;     // key steps of groups [dp_groups, n_groups), shared out over the blocks
+  long long cuts[kMaxGrid + 1];   // block c's share of them: steps [cuts[c], cuts[c + 1])
   float* part;            // partial records, kPartBytesPerBlock per block (split groups only)
   unsigned int* cnt;      // [n_groups - dp_groups][kQTiles][4] arrival counters, zero at launch
   unsigned int* cnt_next; // the other bank: this launch zeroes it for the next one (or null)
@@ -222,8 +224,8 @@ struct SegIter {
     dp_groups = p.dp_groups;
     grid = static_cast<int>(gridDim.x);
     next_dp = static_cast<int>(blockIdx.x);
-    sk_begin = sk_share_start(blockIdx.x, p.sk_steps, grid);
-    sk_end = sk_share_start(static_cast<long long>(blockIdx.x) + 1, p.sk_steps, grid);
+    sk_begin = p.cuts[blockIdx.x];
+    sk_end = p.cuts[blockIdx.x + 1];
     sk_pos = sk_begin;
     causal = p.causal;
     causal_off = p.causal_off;
@@ -309,11 +311,13 @@ struct SegIter {
 };
 
 // The block whose share contains split-region key step x (every share is non-empty).
-__device__ __forceinline__ int sk_block_of(long long x, long long sk_steps, int grid) {
-  int c = static_cast<int>(div_floor(x * grid, sk_steps));
-  while (c + 1 < grid && sk_share_start(c + 1, sk_steps, grid) <= x) ++c;
-  while (c > 0 && sk_share_start(c, sk_steps, grid) > x) --c;
-  return c;
+__device__ __forceinline__ int sk_block_of(long long x, const Params& p, int grid) {
+  int lo = 0, hi = grid - 1;   // the last c with cuts[c] <= x
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (p.cuts[mid] <= x) lo = mid; else hi = mid - 1;
+  }
+  return lo;
 }
 
 __device__ unsigned int g_attn_status;   // per device; bit 0 = a wait timed out
@@ -945,11 +949,10 @@ __device__ void merge_split_row(const Params& p, int tile, int r, int c_first, i
                                 uint8_t* stage, uint16_t* o_row0, int valid_rows, float* lse_out, uint32_t own_tO,
                                 float own_m, float own_l, float own_corr, float o_scale, float* o32_row) {
   const int self = own_tO != 0 ? static_cast<int>(blockIdx.x) : -1;
-  const long long x0_grid = x0 * static_cast<long long>(gridDim.x);
-  // share cs's record: its first segment's slot when its share starts inside this group
-  // (sk_share_start(cs) >= x0, compared without dividing), else its last segment's
+  // share cs's record: its first segment's slot when its share starts inside this group,
+  // else its last segment's
   auto record = [&](int cs) -> const float* {
-    const int which = static_cast<long long>(cs) * p.sk_steps >= x0_grid ? 0 : 1;
+    const int which = p.cuts[cs] >= x0 ? 0 : 1;
     return p.part + (static_cast<size_t>(cs) * 2 + which) * kQTiles * kPartFloatsPerTile +
            static_cast<size_t>(tile) * kPartFloatsPerTile;
   };
@@ -1342,8 +1345,8 @@ __device__ void run_softmax(const Ctl& c, uint32_t tmem, uint8_t* stage, const P
       // the shares that have left their record; the last share to finish merges.
       const long long x0 = sg.x0;
       const int grid = static_cast<int>(gridDim.x);
-      const int c_first = sk_block_of(x0, p.sk_steps, grid);
-      const int c_last = sk_block_of(x0 + sg.glen - 1, p.sk_steps, grid);
+      const int c_first = sk_block_of(x0, p, grid);
+      const int c_last = sk_block_of(x0 + sg.glen - 1, p, grid);
       unsigned int* ctr = p.cnt + (static_cast<long long>(sg.cidx) * kQTiles + tile) * 4 + quarter;
       unsigned int arrived = 0;
       if (lane == 0) arrived = ld_acquire(ctr);
@@ -1551,13 +1554,33 @@ int sm_count(int dev) {
 struct Plan {
   int grid = 1;
   long long dp_groups = 0;   // processed whole, round-robin
-  long long sk_groups = 0;   // their key steps split evenly over the blocks
+  long long sk_groups = 0;   // their key steps shared out over the blocks
   long long sk_steps = 0;
+  std::vector<long long> cuts;   // grid + 1 share boundaries over the sk_steps
   bool has_split = false;    // some group's key steps end up in two or more blocks
 };
 
+// Share boundaries of a split region whose groups end at `bounds` (ascending, the last the
+// region's total): block c takes steps [floor(cT/G), floor((c+1)T/G)). (Shares balanced on a
+// cost that charges each further group a share enters about three steps, the start-up and
+// merge a per-block timeline measured, came out 2-3 % slower on rect-4k-8k: the grid shrank
+// and the shares that stay in one group grew.)
+std::vector<long long> share_cuts(const std::vector<long long>& bounds, int grid) {
+  const long long total = bounds.back();
+  std::vector<long long> cuts;
+  for (int c = 0; c <= grid; ++c) cuts.push_back(sk_share_start(c, total, grid));
+  return cuts;
+}
+
+bool cuts_split_a_group(const std::vector<long long>& cuts, const std::vector<long long>& bounds) {
+  for (size_t c = 1; c + 1 < cuts.size(); ++c)
+    if (!std::binary_search(bounds.begin(), bounds.end(), cuts[c])) return true;
+  return false;
+}
+
 Plan make_plan(long long n_groups, int n_kv, int sms) {
   Plan pl;
+  sms = std::min(sms, kMaxGrid);
   if (n_groups >= sms) {
     pl.grid = sms;
     const long long waves = n_groups / sms, rem = n_groups % sms;
@@ -1572,9 +1595,18 @@ Plan make_plan(long long n_groups, int n_kv, int sms) {
   }
   pl.sk_groups = n_groups - pl.dp_groups;
   pl.sk_steps = pl.sk_groups * n_kv;
-  for (int c = 1; c < pl.grid && pl.sk_steps > 0; ++c)
-    if (sk_share_start(c, pl.sk_steps, pl.grid) % n_kv != 0) pl.has_split = true;
+  if (pl.sk_steps > 0) {
+    std::vector<long long> bounds;
+    for (long long g = 1; g <= pl.sk_groups; ++g) bounds.push_back(g * n_kv);
+    pl.cuts = share_cuts(bounds, pl.grid);
+    pl.has_split = cuts_split_a_group(pl.cuts, bounds);
+  }
   return pl;
+}
+
+// the plan's share boundaries into the launch parameters
+void set_cuts(Params& p, const std::vector<long long>& cuts) {
+  for (int c = 0; c <= kMaxGrid; ++c) p.cuts[c] = c < static_cast<int>(cuts.size()) ? cuts[c] : 0;
 }
 
 // Workspace for split groups, cached per (device, stream) so that calls on different
@@ -1740,6 +1772,7 @@ int forward(const void* q, const void* k, const void* v, const BiasArg* bias, vo
   const Plan pl = make_plan(bh * q_groups, p.n_kv, sms);
   p.dp_groups = static_cast<int>(pl.dp_groups);
   p.sk_steps = pl.sk_steps;
+  set_cuts(p, pl.cuts);
   p.part = nullptr;
   p.cnt = nullptr;
   p.cnt_next = nullptr;
@@ -1921,6 +1954,7 @@ int forward_causal(const void* q, const void* k, const void* v, void* o, float* 
   p.kv_tail = Nk - (p.n_kv - 1) * kBN;
   p.dp_groups = 0;
   p.sk_steps = 0;
+  set_cuts(p, {});
   p.part = nullptr;
   p.cnt = nullptr;
   p.cnt_next = nullptr;
@@ -1944,29 +1978,26 @@ int forward_causal(const void* q, const void* k, const void* v, void* o, float* 
   }
   // Few groups (under two waves): the list's key steps are shared out evenly and long
   // groups are split and merged (SegIter); otherwise whole groups in balanced waves.
-  int grid = static_cast<int>(n_groups < sms ? n_groups : sms);
+  const int max_grid = std::min(sms, kMaxGrid);
+  int grid = static_cast<int>(n_groups < max_grid ? n_groups : max_grid);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (n_groups < 2LL * sms) {
-    // level l of the list (diagonal position q_groups - 1 - l) holds bh groups of len(l) steps
-    std::vector<long long> level_start(static_cast<size_t>(q_groups) + 1, 0);
+    // the list's group boundaries: level l (diagonal position q_groups - 1 - l) holds bh
+    // groups of len(l) steps
+    std::vector<long long> bounds;
+    long long total = 0;
     for (long long l = 0; l < q_groups; ++l) {
       const long long row_end = std::min<long long>(Nq, (q_groups - l) * (kQTiles * kBM));
-      level_start[l + 1] = level_start[l] + bh * ((row_end + p.causal_off + kBN - 1) / kBN);
+      const long long len = (row_end + p.causal_off + kBN - 1) / kBN;
+      for (long long h = 0; h < bh; ++h) bounds.push_back(total += len);
     }
-    const long long total = level_start[q_groups];
     const long long g = total / kMinSegSteps;
-    grid = static_cast<int>(g < 1 ? 1 : (g > sms ? sms : g));
+    grid = static_cast<int>(g < 1 ? 1 : (g > max_grid ? max_grid : g));
+    const std::vector<long long> cuts = share_cuts(bounds, grid);
     p.sk_steps = total;
+    set_cuts(p, cuts);
     // a share boundary inside a group needs the merge workspace
-    bool has_split = false;
-    for (int c = 1; c < grid && !has_split; ++c) {
-      const long long x = sk_share_start(c, total, grid);
-      long long l = 0;
-      while (level_start[l + 1] <= x) ++l;
-      const long long len = (level_start[l + 1] - level_start[l]) / bh;
-      if ((x - level_start[l]) % len != 0) has_split = true;
-    }
-    if (has_split) {
+    if (cuts_split_a_group(cuts, bounds)) {
       const size_t part_bytes = static_cast<size_t>(grid) * kPartBytesPerBlock;
       const size_t cnt_bytes = static_cast<size_t>(n_groups) * kQTiles * 4 * sizeof(unsigned int);
       const int rc = get_workspace(dev, s, part_bytes, cnt_bytes, &p.part, &p.cnt, &p.cnt_next, &p.cnt_len);
@@ -2086,6 +2117,17 @@ extern "C" int attn_fwd_set_wait_limit(unsigned long long cycles, int withhold_t
 
 extern "C" unsigned long long attn_fwd_kernel_count(void) { return g_launches.load(std::memory_order_relaxed); }
 
+extern "C" int attn_fwd_plan(long long n_groups, int n_kv, int sms, long long* dp_groups, long long* cuts, int* grid,
+                             int* has_split) {
+  if (n_groups < 1 || n_kv < 1 || sms < 1 || !dp_groups || !cuts || !grid || !has_split) return ATTN_ERR_INVALID_ARG;
+  const Plan pl = make_plan(n_groups, n_kv, sms);
+  *dp_groups = pl.dp_groups;
+  *grid = pl.grid;
+  *has_split = pl.has_split ? 1 : 0;
+  for (int c = 0; c <= kMaxGrid; ++c) cuts[c] = c < static_cast<int>(pl.cuts.size()) ? pl.cuts[c] : 0;
+  return ATTN_OK;
+}
+
 // ---------------------------------------------------------------------------------
 // Entry point that allocates nothing
 // ---------------------------------------------------------------------------------
@@ -2191,6 +2233,7 @@ extern "C" int attn_fwd_noalloc(const void* q, const void* k, const void* v, voi
   const Plan pl = make_plan(bh * q_groups, p.n_kv, sms);
   p.dp_groups = static_cast<int>(pl.dp_groups);
   p.sk_steps = pl.sk_steps;
+  set_cuts(p, pl.cuts);
   p.part = nullptr;
   p.cnt = nullptr;
   p.cnt_next = nullptr;   // the counters are cleared on the stream before each launch

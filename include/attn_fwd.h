@@ -348,6 +348,17 @@ int attn_fwd_set_wait_limit(unsigned long long cycles, int withhold_tile);
  */
 unsigned long long attn_fwd_kernel_count(void);
 
+/*
+ * attn_fwd_plan -- the work plan attn_fwd would use for n_groups groups (B*H*ceil(Nq/256)) of
+ * n_kv key steps (ceil(Nk/128)) on sms SMs, for inspection (host only, no device call):
+ * dp_groups groups processed whole, then the split region's key steps cut into grid shares,
+ * block c taking steps [cuts[c], cuts[c+1]); cuts must hold 161 values (unused ones are 0);
+ * has_split is 1 when a share boundary falls inside a group. Returns ATTN_OK, or
+ * ATTN_ERR_INVALID_ARG for a null pointer or a count below 1.
+ */
+int attn_fwd_plan(long long n_groups, int n_kv, int sms, long long* dp_groups, long long* cuts, int* grid,
+                  int* has_split);
+
 #ifdef __cplusplus
 }
 #endif

@@ -400,3 +400,42 @@ def test_bwd_bias_binding_refuses_causal():
     with pytest.raises(ValueError):
         attn.attn_bwd(A, A, A, A, A, A, A, A, A, 1, 1, 128, 128, 128, 0.1, causal=True, bias=A,
                       bias_strides=(0, 0, 128))
+
+
+def plan(n_groups, n_kv, sms=152):
+    lib = attn.load_library()
+    fn = lib.attn_fwd_plan
+    dp = ctypes.c_longlong()
+    cuts = (ctypes.c_longlong * 161)()
+    grid, split = ctypes.c_int(), ctypes.c_int()
+    assert fn(ctypes.c_longlong(n_groups), n_kv, sms, ctypes.byref(dp), cuts, ctypes.byref(grid), ctypes.byref(split)) == 0
+    return dp.value, list(cuts)[:grid.value + 1], grid.value, bool(split.value)
+
+
+@pytest.mark.parametrize("n_groups,n_kv", [(128, 64), (8, 8), (1, 1), (3, 40), (152, 32), (1024, 32), (300, 17),
+                                           (151, 128), (64, 128), (2, 3)])
+def test_plan_shares_cover_the_split_region(n_groups, n_kv):
+    # the shares partition the split region in order, every one non-empty
+    dp, cuts, grid, split = plan(n_groups, n_kv)
+    total = (n_groups - dp) * n_kv
+    assert 1 <= grid <= 152 and dp % 152 == 0 and dp <= n_groups
+    if total == 0:
+        return
+    assert cuts[0] == 0 and cuts[-1] == total and len(cuts) == grid + 1
+    assert all(b > a for a, b in zip(cuts, cuts[1:]))
+    assert split == any(c % n_kv != 0 for c in cuts[1:-1])
+    if dp > 0:
+        assert grid == 152
+
+
+def test_plan_shares_are_even():
+    # rect-4k-8k's 128 groups of 64 steps on 152 blocks: shares of 53 or 54 steps
+    dp, cuts, grid, split = plan(128, 64)
+    assert dp == 0 and split and grid == 152
+    sizes = [b - a for a, b in zip(cuts, cuts[1:])]
+    assert set(sizes) <= {53, 54}
+
+
+def test_plan_rejects_bad_arguments():
+    lib = attn.load_library()
+    assert lib.attn_fwd_plan(ctypes.c_longlong(0), 1, 152, None, None, None, None) == attn.ATTN_ERR_INVALID_ARG
