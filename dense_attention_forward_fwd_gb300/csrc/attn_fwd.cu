@@ -499,6 +499,8 @@ __device__ __forceinline__ uint4 ld_nc_v4(const void* ptr) {
 // lane's first piece (row row0 + (lane >> 3), keys from 8 (lane & 7)), `s4` is four rows.
 struct BiasRows {
   const uint16_t* piece;
+  const uint16_t* own_row;   // this lane's row (row0 + lane), for the L2 prefetch of the next step
+  bool own_in;               // that row lies inside the sequence
   long long sq, s4;
   int row0;
   bool rows_full;   // all 32 rows of the warp lie inside the sequence (warp-uniform)
@@ -1084,6 +1086,9 @@ __device__ void run_softmax(const Ctl& c, uint32_t tmem, uint8_t* stage, const P
       br.s4 = 4 * p.bias_sq;
       br.piece = p.bias + static_cast<long long>(bh / p.H) * p.bias_sb + static_cast<long long>(bh % p.H) * p.bias_sh +
                  static_cast<long long>(seg_row0 + (lane >> 3)) * p.bias_sq + 8 * (lane & 7);
+      br.own_row = p.bias + static_cast<long long>(bh / p.H) * p.bias_sb + static_cast<long long>(bh % p.H) * p.bias_sh +
+                   static_cast<long long>(seg_row0 + lane) * p.bias_sq;
+      br.own_in = seg_row0 + lane < p.Nq;
     }
     // MXFP8: the other tile's query scales for the whole segment; per step, the scales of
     // the key tile whose Q K^T the other tile computes next and of this step's V^T tile
@@ -1135,7 +1140,15 @@ __device__ void run_softmax(const Ctl& c, uint32_t tmem, uint8_t* stage, const P
       }
     }
     for (int j = 0; j < n; ++j) {
-      if constexpr (kBias) load_bias_pieces(bg, br, p.Nq, (sg.kv0 + j) * kBN, p.Nk);
+      if constexpr (kBias) {
+        load_bias_pieces(bg, br, p.Nq, (sg.kv0 + j) * kBN, p.Nk);
+        // the next step's bias of this lane's row (two 128-byte lines) into L2 meanwhile
+        const int k1 = (sg.kv0 + j + 1) * kBN;
+        if (j + 1 < n && br.own_in && k1 + kBN <= p.Nk) {
+          asm volatile("prefetch.global.L2 [%0];" ::"l"(br.own_row + k1));
+          asm volatile("prefetch.global.L2 [%0];" ::"l"(br.own_row + k1 + 64));
+        }
+      }
       if constexpr (kMX) {   // loads in flight while the step's scores are awaited
         mx_load_v(sg.kv0 + j);
         if (tile == 0 || j + 1 < n) mx_load_k(sg.kv0 + j + tile);
