@@ -1700,6 +1700,20 @@ struct MxArg {
   long long ldsv;
 };
 
+// attn_fwd_bias's rules for its bias argument.
+int check_bias(const BiasArg& bias, int B, int H, int Nq) {
+  if (!bias.ptr || bias.sb < 0 || bias.sh < 0 || bias.sq < 0) return ATTN_ERR_INVALID_ARG;
+  // the last element's offset, (B-1) sb + (H-1) sh + (Nq-1) sq + Nk - 1, in bytes must fit int64
+  constexpr long long kCap = LLONG_MAX / 8;
+  const long long ext[3] = {B - 1LL, H - 1LL, Nq - 1LL};
+  const long long str[3] = {bias.sb, bias.sh, bias.sq};
+  for (int i = 0; i < 3; ++i)
+    if (str[i] > 0 && ext[i] > kCap / str[i]) return ATTN_ERR_INVALID_ARG;
+  // 16-byte vector loads of each row's 8-key chunks
+  if ((reinterpret_cast<uintptr_t>(bias.ptr) & 15u) || ((bias.sb | bias.sh | bias.sq) & 7)) return ATTN_ERR_MISALIGNED;
+  return ATTN_OK;
+}
+
 // The 8-bit entry points' own argument rules (f8 as forward's).
 int check_f8_args(int f8, long long ldv, const MxArg* mx, int Nk, long long bh) {
   if (f8 >= 2) {
@@ -1751,18 +1765,8 @@ int forward(const void* q, const void* k, const void* v, const BiasArg* bias, vo
   const long long max_rows = static_cast<long long>(Nq > Nk ? Nq : Nk);
   if (bh > (LLONG_MAX / 256) / max_rows) return ATTN_ERR_INVALID_ARG;
   if (const int rc = check_f8_args(f8, ldv, mx, Nk, bh); rc != ATTN_OK) return rc;
-  if (bias != nullptr) {
-    if (!bias->ptr || bias->sb < 0 || bias->sh < 0 || bias->sq < 0) return ATTN_ERR_INVALID_ARG;
-    // the last element's offset, (B-1) sb + (H-1) sh + (Nq-1) sq + Nk - 1, in bytes must fit int64
-    constexpr long long kCap = LLONG_MAX / 8;
-    const long long ext[3] = {B - 1LL, H - 1LL, Nq - 1LL};
-    const long long str[3] = {bias->sb, bias->sh, bias->sq};
-    for (int i = 0; i < 3; ++i)
-      if (str[i] > 0 && ext[i] > kCap / str[i]) return ATTN_ERR_INVALID_ARG;
-    // 16-byte vector loads of each row's 8-key chunks
-    if ((reinterpret_cast<uintptr_t>(bias->ptr) & 15u) || ((bias->sb | bias->sh | bias->sq) & 7))
-      return ATTN_ERR_MISALIGNED;
-  }
+  if (bias != nullptr)
+    if (const int rc = check_bias(*bias, B, H, Nq); rc != ATTN_OK) return rc;
 
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return ATTN_ERR_CUDA;
@@ -1847,7 +1851,7 @@ namespace {
 // Head dimensions above 128: the one-Q-tile kernel (attn_fwd_wide.cu), after the argument
 // checks of the d = 128 entry points (causal: also Nq <= Nk).
 int forward_wide(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Nq, int Nk,
-                 int d, float scale, bool causal, void* stream) {
+                 int d, float scale, bool causal, void* stream, const BiasArg* bias = nullptr) {
   if (B < 0 || H < 0 || Nq < 0 || Nk < 0 || !std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
   if (static_cast<long long>(B) * H == 0 || Nq == 0) return ATTN_OK;
   if (Nk == 0 || (causal && Nq > Nk) || !q || !k || !v || !o || !lse) return ATTN_ERR_INVALID_ARG;
@@ -1858,8 +1862,13 @@ int forward_wide(const void* q, const void* k, const void* v, void* o, float* ls
   if (reinterpret_cast<uintptr_t>(lse) & 3u) return ATTN_ERR_MISALIGNED;
   const long long max_rows = static_cast<long long>(Nq > Nk ? Nq : Nk);
   if (static_cast<long long>(B) * H > (LLONG_MAX / (2 * d)) / max_rows) return ATTN_ERR_INVALID_ARG;
+  attn_wide::Bias wb{};
+  if (bias != nullptr) {
+    if (const int rc = check_bias(*bias, B, H, Nq); rc != ATTN_OK) return rc;
+    wb = {bias->ptr, bias->sb, bias->sh, bias->sq};
+  }
   const int rc = attn_wide::forward(q, k, v, o, lse, B, H, Nq, Nk, d, scale, causal, static_cast<cudaStream_t>(stream),
-                                    g_wait_limit.load(std::memory_order_relaxed));
+                                    g_wait_limit.load(std::memory_order_relaxed), bias != nullptr ? &wb : nullptr);
   if (rc == ATTN_OK) g_launches.fetch_add(1, std::memory_order_relaxed);
   return rc;
 }
@@ -1880,6 +1889,7 @@ extern "C" int attn_fwd_bias(const void* q, const void* k, const void* v, const 
                              long long bias_stride_h, long long bias_stride_q, void* o, float* lse, int B, int H,
                              int Nq, int Nk, int d, float scale, void* stream) {
   const BiasArg ba = {bias, bias_stride_b, bias_stride_h, bias_stride_q};
+  if (attn_wide::supported(d)) return forward_wide(q, k, v, o, lse, B, H, Nq, Nk, d, scale, false, stream, &ba);
   return forward(q, k, v, &ba, o, lse, B, H, Nq, Nk, d, scale, stream);
 }
 

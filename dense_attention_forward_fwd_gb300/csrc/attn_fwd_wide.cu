@@ -54,7 +54,8 @@ constexpr int kBM = 128;                  // query rows per tile (= TMEM lanes)
 constexpr int kBN = 128;                  // keys per step
 constexpr int kBoxCols = 64;              // one TMA box: 64 BF16 columns (128 B) x 128 rows
 constexpr int kBoxBytes = kBoxCols * 2 * 128;
-constexpr int kVSlots = 3;                // V ring, in 64-key half tiles
+constexpr int kMaxVSlots = 3;             // V ring, in 64-key half tiles (2 at d = 256 with a bias)
+constexpr int kStageWarpBytes = 32 * kBN * 2;   // a softmax warp's 32 bias rows of one step
 constexpr int kThreads = 256;
 constexpr float kRescaleLog2 = 32.0f;     // the running maximum moves when a tile's exceeds it by this
 constexpr int kTmemCols = 512;
@@ -66,8 +67,8 @@ constexpr int kBarQEmpty = 1;                     // the tile's last Q K^T is do
 constexpr int kBarKFull = 2;                      // [box]
 constexpr int kBarKFree = kBarKFull + kMaxChunks; // [box]: the Q K^T steps that read it are done
 constexpr int kBarVFull = kBarKFree + kMaxChunks; // [half-tile slot]
-constexpr int kBarVFree = kBarVFull + kVSlots;    // [half-tile slot]: its half of P V is done
-constexpr int kBarSFull = kBarVFree + kVSlots;    // [2 buffers]
+constexpr int kBarVFree = kBarVFull + kMaxVSlots; // [half-tile slot]: its half of P V is done
+constexpr int kBarSFull = kBarVFree + kMaxVSlots; // [2 buffers]
 constexpr int kBarPFull = kBarSFull + 2;          // [step parity][half], one arrival per softmax warp
 constexpr int kBarOFull = kBarPFull + 4;
 constexpr int kBarOEmpty = kBarOFull + 1;         // the epilogue has read O out of TMEM
@@ -75,15 +76,19 @@ constexpr int kBarDrain = kBarOEmpty + 1;
 constexpr int kNumBars = kBarDrain + 1;
 constexpr int kFlagsBytes = kNumBars * 8 + 8;     // barriers, TMEM slot, abort flag
 
-template <int D>
+// With a bias, each softmax warp stages its rows' bias in shared memory; at d = 256 that
+// room comes from one V slot.
+template <int D, bool kBias>
 struct Layout {
   static constexpr int kChunks = D / kBoxCols;             // boxes per Q or K tile
   static constexpr int kTileBytes = kChunks * kBoxBytes;
   static constexpr int kHalfBytes = kChunks * kBoxBytes / 2;   // V: 64 keys x d
+  static constexpr int kVSlots = (kBias && D == 256) ? 2 : kMaxVSlots;
   static constexpr int kOffQ = 0;
   static constexpr int kOffK = kOffQ + kTileBytes;
   static constexpr int kOffV = kOffK + kTileBytes;
-  static constexpr int kOffBar = kOffV + kVSlots * kHalfBytes;
+  static constexpr int kOffStage = kOffV + kVSlots * kHalfBytes;
+  static constexpr int kOffBar = kOffStage + (kBias ? 4 * kStageWarpBytes : 0);
   static constexpr int kSmem = kOffBar + kFlagsBytes + 1024;   // + realignment of the base to 1024
   static_assert(D % kBoxCols == 0 && kChunks <= kMaxChunks, "head dimension in whole boxes");
   static_assert(kSmem <= 232448, "exceeds the 227 KB shared memory of one block");
@@ -105,6 +110,12 @@ struct Params {
   int causal_off;     // Nk - Nq
   float scale_log2;   // scale * log2(e)
   unsigned long long wait_limit;
+  // additive bias (kBias): B_ij of head (b, h) = bias[b * bias_sb + h * bias_sh + i * bias_sq + j],
+  // BF16, strides in elements (multiples of 8), H heads per batch; scores become scale q.k + B
+  const uint16_t* bias;
+  long long bias_sb, bias_sh, bias_sq;
+  int H;
+  float scale;
 };
 
 // The query tiles a block runs, in order; every role walks the same sequence. Plain: tile
@@ -164,15 +175,24 @@ __device__ __forceinline__ bool wait_warp(const Ctl& c, int idx, uint32_t parity
   return __all_sync(0xffffffffu, ok);
 }
 
+// 16 bytes global -> shared without passing through registers; the bytes past src_bytes
+// (0 .. 16) are written as zeros and not read
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, int src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
 // Global counters (every role keeps them alike): step gs of the block's key stream (all its
 // query tiles' key tiles, in order) uses S buffer gs & 1 and K tile gs (box c in K slot c);
 // its V halves are half tiles 2 gs and 2 gs + 1, in V slots (2 gs + h) % kVSlots. A ring
 // barrier completes once per use of its slot, so the k-th use waits for parity k & 1.
-template <int D, bool kPos>
+template <int D, bool kPos, bool kBias>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                          const __grid_constant__ CUtensorMap tmV, const Params p) {
-  using L = Layout<D>;
+  using L = Layout<D, kBias>;
+  constexpr int kVSlots = L::kVSlots;
   constexpr int kChunks = L::kChunks;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -344,7 +364,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
     const uint32_t tS[2] = {tmem + lane_off, tmem + lane_off + kBN};
     const uint32_t tO = tmem + lane_off + 2 * kBN;
-    const float cs = kPos ? p.scale_log2 : 1.0f;
+    // the factor still to apply to a score: with a bias, s already holds scale q.k + B (natural units)
+    const float cs = kBias ? 1.4426950408889634f : (kPos ? p.scale_log2 : 1.0f);
     const bool ringer = warp == 4 && lane == 0;
     int u = 0, gj = 0;
     TileIter it(p);
@@ -352,6 +373,29 @@ __global__ void __launch_bounds__(kThreads, 1)
     while (it.next(bh, qt, n)) {
       float m_used = -INFINITY, l = 0.0f, corr = 0.0f;
       bool ok = true;
+      // bias: the warp's 32 rows x 128 keys of a step, staged in its own shared memory by
+      // 16-byte copies issued one step ahead. Copy i puts rows 2i and 2i + 1 (16 lanes each,
+      // 256 contiguous bytes per row, so four 128-byte lines per instruction); 16-byte chunk
+      // ch of staged row r sits at chunk ch ^ (r & 15), so neither the copies nor the
+      // row-per-lane reads meet a bank conflict. Rows past Nq and keys past Nk read nothing
+      // and are staged as 0 (those scores are never stored, or masked).
+      const int row0 = qt * kBM + quarter * 32;
+      const uint16_t* bbase = nullptr;
+      if constexpr (kBias)
+        bbase = p.bias + static_cast<long long>(bh / p.H) * p.bias_sb + static_cast<long long>(bh % p.H) * p.bias_sh;
+      const uint32_t stage = base + L::kOffStage + static_cast<uint32_t>(quarter * kStageWarpBytes);
+      auto stage_bias = [&](int j) {
+        const int k0 = j * kBN, ch = lane & 15;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const int r = 2 * i + (lane >> 4), row = row0 + r, key = k0 + 8 * ch;
+          const int valid = row < p.Nq ? max(0, min(8, p.Nk - key)) : 0;
+          const uint16_t* src = valid > 0 ? bbase + static_cast<long long>(row) * p.bias_sq + key : p.bias;
+          cp_async16(stage + static_cast<uint32_t>((r * 16 + (ch ^ (r & 15))) * 16), src, 2 * valid);
+        }
+        cp_async_commit();
+      };
+      if constexpr (kBias) stage_bias(0);
       for (int j = 0; j < n; ++j) {
         const int gs = gj + j, buf = gs & 1;
         if (!wait_warp(c, kBarSFull + buf, static_cast<uint32_t>(gs >> 1) & 1u)) {
@@ -363,8 +407,31 @@ __global__ void __launch_bounds__(kThreads, 1)
         {
           uint32_t x[128];
           tmem_ld<128>(tS[buf], x);
+          if constexpr (kBias) {   // scale q.k + B, B from the staged row
+            cp_async_wait_all();
+            __syncwarp();
+            const float2 sc2 = make_float2(p.scale, p.scale);
 #pragma unroll
-          for (int i = 0; i < 128; ++i) s[i] = kPos ? __uint_as_float(x[i]) : __uint_as_float(x[i]) * p.scale_log2;
+            for (int cc = 0; cc < 16; ++cc) {
+              uint4 b;
+              asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                           : "=r"(b.x), "=r"(b.y), "=r"(b.z), "=r"(b.w)
+                           : "r"(stage + static_cast<uint32_t>((lane * 16 + (cc ^ (lane & 15))) * 16)));
+              const uint32_t bw[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const int i = 4 * cc + e;
+                const float2 t = ffma2(f2(x[2 * i], x[2 * i + 1]), sc2, f2(bw[e] << 16, bw[e] & 0xffff0000u));
+                s[2 * i] = t.x;
+                s[2 * i + 1] = t.y;
+              }
+            }
+            __syncwarp();   // every lane has read the stage before the next step's copies land
+            if (j + 1 < n) stage_bias(j + 1);
+          } else {
+#pragma unroll
+            for (int i = 0; i < 128; ++i) s[i] = kPos ? __uint_as_float(x[i]) : __uint_as_float(x[i]) * p.scale_log2;
+          }
         }
         if (j == p.n_kv - 1 && p.kv_tail < kBN) {   // keys past the sequence
           const int valid = p.kv_tail;
@@ -421,11 +488,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_st<8>(tO + ch * 8, ov);
           }
         }
-        const float neg_m = -m_used;
+        // (with a bias a row may have seen only -inf so far: its weights are all 0 then)
+        const float neg_m = (kBias && m_used == -INFINITY) ? 0.0f : -m_used;
         {
           // the BF16 rounding error of the tile's largest weight, with the arithmetic that
           // forms it below: l + corr is then the sum of the weights the tensor cores apply
-          const float pm = ex2(fmaf(m_raw, cs, neg_m));
+          const float pm = (kBias && m_tile == -INFINITY) ? 0.0f : ex2(fmaf(m_raw, cs, neg_m));
           corr += __uint_as_float(pack_bf16(pm, 0.0f) << 16) - pm;
         }
         float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
@@ -491,6 +559,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       gj += n;
       ++u;
     }
+    if constexpr (kBias) cp_async_wait_all();   // (after an abort) no copy still lands in shared memory
   }
 
   tc_fence_before();
@@ -533,22 +602,22 @@ bool make_map(CUtensorMap* map, const void* ptr, int rows, long long bh, int d, 
 }
 
 constexpr int kMaxDevices = 64;
-std::atomic<int> g_attr_done[4][kMaxDevices];   // per instantiation (d, sign of the scale) and device
+std::atomic<int> g_attr_done[6][kMaxDevices];   // per instantiation (d, sign of the scale or bias) and device
 
-template <int D, bool kPos>
+template <int D, bool kPos, bool kBias = false>
 int launch(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, const Params& p, int grid, int dev,
            cudaStream_t stream) {
-  auto kern = attn_fwd_wide_kernel<D, kPos>;
-  constexpr int kInst = (D == 256 ? 2 : 0) + (kPos ? 1 : 0);
+  auto kern = attn_fwd_wide_kernel<D, kPos, kBias>;
+  constexpr int kInst = (D == 256 ? 3 : 0) + (kBias ? 2 : (kPos ? 1 : 0));
   if (dev < 0 || dev >= kMaxDevices || !g_attr_done[kInst][dev].load(std::memory_order_acquire)) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Layout<D>::kSmem) != cudaSuccess)
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Layout<D, kBias>::kSmem) != cudaSuccess)
       return ATTN_ERR_CUDA;
     if (dev >= 0 && dev < kMaxDevices) g_attr_done[kInst][dev].store(1, std::memory_order_release);
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(grid));
   cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = Layout<D>::kSmem;
+  cfg.dynamicSmemBytes = Layout<D, kBias>::kSmem;
   cfg.stream = stream;
   return cudaLaunchKernelEx(&cfg, kern, mq, mk, mv, p) == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
@@ -556,7 +625,7 @@ int launch(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, 
 }  // namespace
 
 int forward(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Nq, int Nk, int d,
-            float scale, bool causal, cudaStream_t stream, unsigned long long wait_limit) {
+            float scale, bool causal, cudaStream_t stream, unsigned long long wait_limit, const Bias* bias) {
   if (!supported(d)) return ATTN_ERR_UNSUPPORTED;
   const long long bh = static_cast<long long>(B) * H;
   const long long q_tiles = (static_cast<long long>(Nq) + kBM - 1) / kBM;
@@ -583,7 +652,17 @@ int forward(const void* q, const void* k, const void* v, void* o, float* lse, in
   p.causal_off = causal ? Nk - Nq : 0;
   p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
   p.wait_limit = wait_limit;
+  p.bias = bias ? static_cast<const uint16_t*>(bias->ptr) : nullptr;
+  p.bias_sb = bias ? bias->sb : 0;
+  p.bias_sh = bias ? bias->sh : 0;
+  p.bias_sq = bias ? bias->sq : 0;
+  p.H = H;
+  p.scale = scale;
   const int grid = std::min(sms, p.groups);
+  // with a bias the scale is applied before the row max: one instantiation serves any sign
+  if (bias != nullptr)
+    return d == 256 ? launch<256, true, true>(mq, mk, mv, p, grid, dev, stream)
+                    : launch<192, true, true>(mq, mk, mv, p, grid, dev, stream);
   if (d == 256)
     return scale > 0.0f ? launch<256, true>(mq, mk, mv, p, grid, dev, stream)
                         : launch<256, false>(mq, mk, mv, p, grid, dev, stream);

@@ -9,13 +9,22 @@ namespace attn_wide {
 // Head dimensions this kernel serves.
 constexpr bool supported(int d) { return d == 192 || d == 256; }
 
+// An additive bias as attn_fwd_bias takes it (BF16, element strides, already validated:
+// 16-byte aligned base, strides multiples of 8, offsets within 64 bits).
+struct Bias {
+  const void* ptr;
+  long long sb, sh, sq;
+};
+
 // O = softmax(scale Q K^T) V and the natural-log LSE for BF16 [B, H, N, d] tensors, d in
 // {192, 256}; arguments as attn_fwd (already validated by the caller: non-null, 16-byte
 // aligned, B*H, Nq, Nk >= 1, finite scale). causal: query i sees keys 0 .. i + Nk - Nq only
 // (the caller has checked Nq <= Nk). wait_limit: clock64 budget of each of the kernel's
-// waits. Returns an attn_status code; ATTN_OK once the kernel is enqueued.
+// waits. bias (or null): S = scale Q K^T + B as attn_fwd_bias (not with causal). Returns an
+// attn_status code; ATTN_OK once the kernel is enqueued.
 int forward(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Nq, int Nk,
-            int d, float scale, bool causal, cudaStream_t stream, unsigned long long wait_limit);
+            int d, float scale, bool causal, cudaStream_t stream, unsigned long long wait_limit,
+            const Bias* bias = nullptr);
 
 // Reads and clears the kernel's device status word on `stream` (synchronising it): 1 if a
 // wait of a launch gave up since the last call, 0 if not, negative on a CUDA error.

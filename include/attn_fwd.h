@@ -20,7 +20,7 @@
  *
  * Conventions shared by every entry point below:
  *   - Tensors are dense, C-ordered, [B, H, N, d] (batch, heads, sequence, head dim)
- *     with d = 128 (attn_fwd and attn_fwd_causal also take 192 and 256), in device
+ *     with d = 128 (attn_fwd, attn_fwd_causal and attn_fwd_bias also take 192 and 256), in device
  *     memory reachable from the current CUDA device.
  *   - BF16 is IEEE-style bfloat16 (1 sign, 8 exponent, 7 mantissa bits), passed as
  *     raw 16-bit storage (void*).
@@ -127,6 +127,8 @@ int attn_fwd_causal(const void* q, const void* k, const void* v, void* o, float*
  *   - lse is the log-sum-exp of the biased scores, in natural-log units.
  *   - The work split and workspace are those of attn_fwd (the bias adds no state). The
  *     bias is read once per (query row, key), from L2 when it is shared across heads.
+ *   - d = 192 and 256 are taken too: attn_fwd's one-query-tile kernel at those head
+ *     dimensions, each thread adding its own row's bias; no workspace.
  */
 int attn_fwd_bias(const void* q, const void* k, const void* v, const void* bias,
                   long long bias_stride_b, long long bias_stride_h, long long bias_stride_q,

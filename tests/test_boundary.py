@@ -152,6 +152,14 @@ def call_bias(q=A, k=A, v=A, bias=A, sb=0, sh=0, sq=128, o=A, lse=A, B=1, H=1, N
     (dict(Nk=0), attn.ATTN_ERR_INVALID_ARG),
     (dict(B=0), attn.ATTN_OK),
     (dict(Nq=0, bias=None), attn.ATTN_OK),
+    # d = 192 / 256 (the one-query-tile kernel) applies the same bias rules
+    (dict(d=256, bias=None), attn.ATTN_ERR_INVALID_ARG),
+    (dict(d=256, sq=-128), attn.ATTN_ERR_INVALID_ARG),
+    (dict(d=192, sh=1 << 62, H=4), attn.ATTN_ERR_INVALID_ARG),
+    (dict(d=256, bias=A + 8), attn.ATTN_ERR_MISALIGNED),
+    (dict(d=192, sq=130, Nk=130), attn.ATTN_ERR_MISALIGNED),
+    (dict(d=256, Nk=0), attn.ATTN_ERR_INVALID_ARG),
+    (dict(d=256, B=0, bias=None), attn.ATTN_OK),
 ])
 def test_bias_argument_checks(kw, code):
     before = attn.attn_fwd_kernel_count()

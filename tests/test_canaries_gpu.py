@@ -63,6 +63,11 @@ def test_forward_wide_head_dims(gpu_lib, d, B, H, Nq, Nk):
     (fo, o), (fl, lse) = guarded((B, H, Nq, d), "bf16", "cuda"), guarded((B, H, Nq), "f32", "cuda")
     gpu_lib.attn_fwd(q, k, v, o, lse, B, H, Nq, Nk, d, d ** -0.5)
     check(gpu_lib, ((fo, o), "bf16"), ((fl, lse), "f32"))
+    if Nk % 8 == 0:   # attn_fwd_bias at the same head dimension (bias rows on 16-byte boundaries)
+        bias = to_device(make_bias((B, H, Nq, Nk), seed=17400 + Nq + Nk + d, std=1.0))
+        (fo, o), (fl, lse) = guarded((B, H, Nq, d), "bf16", "cuda"), guarded((B, H, Nq), "f32", "cuda")
+        gpu_lib.attn_fwd_bias(q, k, v, bias, o, lse, B, H, Nq, Nk, d, d ** -0.5)
+        check(gpu_lib, ((fo, o), "bf16"), ((fl, lse), "f32"))
 
 
 @pytest.mark.parametrize("B,H,Nq,Nk", SHAPES)

@@ -9,7 +9,8 @@ those bounds.
 import numpy as np
 import pytest
 
-from dense_attention_forward_fwd_gb300.inputs import bf16_bits_to_f32, f32_to_bf16_bits, make_qkv, sample_rows
+from dense_attention_forward_fwd_gb300.inputs import (BF16_NEG_INF, bf16_bits_to_f32, f32_to_bf16_bits, make_bias,
+                                                  make_qkv, sample_rows)
 from parity import check_case, run_gpu
 
 pytestmark = pytest.mark.gpu
@@ -108,3 +109,85 @@ def test_wide_causal_many_tiles(gpu_lib, d):
 
 def test_wide_causal_peaked(gpu_lib):
     check_case(gpu_lib, 1, 2, 512, 1024, seed=4, qk_mult=3.0, ulp_aware=True, causal=True, d=256)
+
+
+# ---- with an additive bias (attn_fwd_bias at d > 128): S = scale * Q K^T + B ----
+
+def _bias_shape(kind, B, H, Nq, Nk):
+    return {"full": (B, H, Nq, Nk), "shared": (1, 1, Nq, Nk), "per_head": (1, H, Nq, Nk),
+            "per_key": (1, 1, 1, Nk)}[kind]
+
+
+@pytest.mark.parametrize("d", [192, 256])
+@pytest.mark.parametrize("B,H,Nq,Nk,kind", [
+    (1, 1, 128, 128, "full"),       # one tile, one key step
+    (2, 3, 300, 1000, "full"),      # ragged query and key tails
+    (1, 2, 384, 640, "shared"),
+    (1, 3, 1000, 1776, "per_key"),
+    (1, 1, 1, 200, "full"),
+    (1, 1, 129, 136, "per_head"),
+    (2, 8, 2048, 1024, "shared"),   # more query tiles than blocks
+])
+def test_wide_bias_parity(gpu_lib, d, B, H, Nq, Nk, kind):
+    bias = make_bias(_bias_shape(kind, B, H, Nq, Nk), seed=9500 + Nq + Nk + d, std=2.0)
+    check_case(gpu_lib, B, H, Nq, Nk, seed=8500 + Nq + Nk + d, bias=bias, d=d)
+
+
+@pytest.mark.parametrize("d", [192, 256])
+def test_wide_bias_padding_mask_hides_whole_key_tiles(gpu_lib, d):
+    # keys 0..299 and 900..999 removed for every row: the running maximum is still -inf when
+    # the first visible key arrives, two key steps in
+    Nk = 1000
+    bias = make_bias((1, 1, 1, Nk), seed=95, std=1.0)
+    bias[..., :300] = BF16_NEG_INF
+    bias[..., 900:] = BF16_NEG_INF
+    check_case(gpu_lib, 1, 2, 384, Nk, seed=96, bias=bias, d=d)
+
+
+def test_wide_bias_causal_pattern_agrees_with_the_causal_entry_point(gpu_lib):
+    d, Nq, Nk = 256, 384, 640
+    bias = np.zeros((1, 1, Nq, Nk), dtype=np.uint16)
+    for i in range(Nq):
+        bias[0, 0, i, i + Nk - Nq + 1:] = BF16_NEG_INF
+    q, k, v = make_qkv(1, 2, Nq, Nk, d=d, seed=97)
+    check_case(gpu_lib, 1, 2, Nq, Nk, qkv=(q, k, v), bias=bias, d=d)
+    ob, lb = run_gpu(gpu_lib, q, k, v, d ** -0.5, bias=bias)
+    oc, lc = run_gpu(gpu_lib, q, k, v, d ** -0.5, causal=True)
+    assert np.max(np.abs(ob - oc)) <= 2e-2 and np.max(np.abs(lb - lc)) <= 1e-4 * max(1.0, np.max(np.abs(lc)))
+
+
+@pytest.mark.parametrize("scale", [-0.0625, 0.0])
+def test_wide_bias_peaked_and_other_scales(gpu_lib, scale):
+    # a bias of standard deviation 8 on peaked scores (late maxima, O rescales; nearly one-hot
+    # rows, so |O| reaches 3 and O's own BF16 rounding is judged ulp-aware), and scales of the
+    # other sign and zero, where S is the bias alone
+    check_case(gpu_lib, 1, 2, 512, 2048, seed=98, qk_mult=3.0, ulp_aware=True, d=256,
+               bias=make_bias((1, 2, 512, 2048), seed=99, std=8.0))
+    check_case(gpu_lib, 1, 2, 200, 304, seed=100, scale=scale, d=256,
+               bias=make_bias((1, 1, 200, 304), seed=101, std=2.0))
+
+
+def test_wide_bias_of_zeros_matches_the_plain_entry_point(gpu_lib):
+    q, k, v = make_qkv(1, 2, 256, 512, d=256, seed=102)
+    ob, lb = run_gpu(gpu_lib, q, k, v, 0.0625, bias=np.zeros((1, 1, 1, 512), dtype=np.uint16))
+    o0, l0 = run_gpu(gpu_lib, q, k, v, 0.0625)
+    assert np.max(np.abs(ob - o0)) <= 1e-2 and np.max(np.abs(lb - l0)) <= 1e-5 * np.max(np.abs(l0))
+
+
+@pytest.mark.parametrize("kind", ["shared", "full"])
+def test_wide_bias_sampled_rows_square(gpu_lib, kind):
+    # the 4K x 4K shape at d = 256 as `bench.py --head-dim 256 --bias` times it
+    from dense_attention_forward_fwd_gb300.configs import by_name
+    w = by_name("square-4k")
+    d = 256
+    rows = sample_rows(w.B, w.H, w.Nq, per_head=8)
+    bias = make_bias(_bias_shape(kind, w.B, w.H, w.Nq, w.Nk), seed=103, std=1.0)
+    check_case(gpu_lib, w.B, w.H, w.Nq, w.Nk, seed=w.seed, rows=rows, bias=bias, d=d)
+
+
+def test_wide_bias_deterministic(gpu_lib):
+    q, k, v = make_qkv(1, 4, 1024, 2048, d=192, seed=104)
+    bias = make_bias((1, 4, 1024, 2048), seed=105, std=2.0)
+    o1, l1 = run_gpu(gpu_lib, q, k, v, 0.07, bias=bias)
+    o2, l2 = run_gpu(gpu_lib, q, k, v, 0.07, bias=bias)
+    assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
