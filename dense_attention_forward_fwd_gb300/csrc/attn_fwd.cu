@@ -2200,6 +2200,8 @@ unsigned long long current_context_id() {
 
 extern "C" int attn_fwd_noalloc(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
                                 int Nq, int Nk, int d, float scale, void* stream) {
+  // d = 192 / 256: the one-query-tile kernel, which never needs a workspace
+  if (attn_wide::supported(d)) return forward_wide(q, k, v, o, lse, B, H, Nq, Nk, d, scale, false, stream);
   // the same argument rules as attn_fwd
   if (B < 0 || H < 0 || Nq < 0 || Nk < 0) return ATTN_ERR_INVALID_ARG;
   if (d != kD) return ATTN_ERR_UNSUPPORTED;

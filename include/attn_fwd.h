@@ -303,6 +303,8 @@ int attn_fwd_o32(const void* q, const void* k, const void* v, float* o32, float*
  * Arguments, layouts and return values are those of attn_fwd, plus:
  *   - ATTN_ERR_UNSUPPORTED when the call would need more than the fixed 48 MiB (only on
  *     a device with more than 186 SMs).
+ *   - d = 192 and 256 run attn_fwd's one-query-tile kernel, which splits no work and
+ *     uses no workspace: the array below is not touched.
  *   - The first call in each CUDA context (on each device, and again after
  *     cudaDeviceReset or in another context made current by the caller) looks up the
  *     array's device address (cudaGetSymbolAddress, which allocates nothing) with that

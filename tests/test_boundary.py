@@ -167,6 +167,22 @@ def test_bias_argument_checks(kw, code):
     assert attn.attn_fwd_kernel_count() == before
 
 
+@pytest.mark.parametrize("d,kw,code", [
+    (256, dict(q=None), attn.ATTN_ERR_INVALID_ARG),
+    (192, dict(Nk=0), attn.ATTN_ERR_INVALID_ARG),
+    (256, dict(o=A + 8), attn.ATTN_ERR_MISALIGNED),
+    (192, dict(B=0), attn.ATTN_OK),
+    (64, dict(), attn.ATTN_ERR_UNSUPPORTED),
+])
+def test_noalloc_argument_checks(d, kw, code):
+    args = dict(q=A, k=A, v=A, o=A, lse=A, B=1, H=1, Nq=128, Nk=128)
+    args.update(kw)
+    before = attn.attn_fwd_kernel_count()
+    assert attn.load_library().attn_fwd_noalloc(args["q"], args["k"], args["v"], args["o"], args["lse"], args["B"],
+                                                args["H"], args["Nq"], args["Nk"], d, 0.1, None) == code
+    assert attn.attn_fwd_kernel_count() == before
+
+
 def call_fp8(q8=A, k8=A, v=A, o=A, lse=A, B=1, H=1, Nq=128, Nk=128, d=128, scale=0.125, dq=0.01, dk=0.02,
              causal=False):
     lib = attn.load_library()

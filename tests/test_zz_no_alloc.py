@@ -24,9 +24,6 @@ from parity import bf16_to_np, to_device
 
 pytestmark = pytest.mark.gpu
 
-SCALE = float(np.float32(1 / np.sqrt(128)))
-
-
 class Driver:
     """The few CUDA driver calls the allocation check needs, on the current context."""
     RESERVED_MEM_CURRENT, USED_MEM_CURRENT = 5, 7   # CUmemPool_attribute values
@@ -53,24 +50,24 @@ class Driver:
         return s.value
 
 
-def _prepare(shape):
+def _prepare(shape, d=128):
     """Seeded inputs and NaN-filled outputs on the device, ready before any timed or probed call."""
     import torch
     B, H, Nq, Nk = shape
-    q, k, v = make_qkv(B, H, Nq, Nk, seed=Nq + Nk)
-    o = torch.full((B, H, Nq, 128), float("nan"), dtype=torch.bfloat16, device="cuda")
+    q, k, v = make_qkv(B, H, Nq, Nk, d=d, seed=Nq + Nk)
+    o = torch.full((B, H, Nq, d), float("nan"), dtype=torch.bfloat16, device="cuda")
     lse = torch.full((B, H, Nq), float("nan"), dtype=torch.float32, device="cuda")
     bufs = (to_device(q), to_device(k), to_device(v), o, lse)
     torch.cuda.synchronize()   # a call on another stream must see the copies and fills done
     return bufs
 
 
-def _call(attn, fn_name, shape, bufs, stream=None):
+def _call(attn, fn_name, shape, bufs, stream=None, d=128):
     """One call of attn_fwd or attn_fwd_noalloc through the C ABI, waited for."""
     import torch
     B, H, Nq, Nk = shape
     st = torch.cuda.current_stream().cuda_stream if stream is None else stream
-    rc = getattr(attn.load_library(), fn_name)(*(t.data_ptr() for t in bufs), B, H, Nq, Nk, 128, SCALE, st)
+    rc = getattr(attn.load_library(), fn_name)(*(t.data_ptr() for t in bufs), B, H, Nq, Nk, d, d ** -0.5, st)
     assert rc == attn.ATTN_OK, attn.attn_status_string(rc)
     assert attn.attn_fwd_status(st) == attn.ATTN_OK   # synchronises the stream
 
@@ -79,9 +76,9 @@ def _result(bufs):
     return bf16_to_np(bufs[3]), bufs[4].cpu().numpy()
 
 
-def _run(attn, fn_name, shape, stream=None):
-    bufs = _prepare(shape)
-    _call(attn, fn_name, shape, bufs, stream)
+def _run(attn, fn_name, shape, stream=None, d=128):
+    bufs = _prepare(shape, d)
+    _call(attn, fn_name, shape, bufs, stream, d)
     return _result(bufs)
 
 
@@ -141,3 +138,22 @@ def test_noalloc_rejects_bad_arguments_like_attn_fwd(gpu_lib):
     assert lib.attn_fwd_noalloc(a + 2, a, a, a, a, 1, 1, 128, 128, 128, 0.1, None) == gpu_lib.ATTN_ERR_MISALIGNED
     assert lib.attn_fwd_noalloc(None, a, a, a, a, 1, 1, 128, 128, 128, 0.1, None) == gpu_lib.ATTN_ERR_INVALID_ARG
     assert lib.attn_fwd_noalloc(a, a, a, a, a, 0, 1, 128, 128, 128, 0.1, None) == gpu_lib.ATTN_OK
+
+
+@pytest.mark.parametrize("d", [192, 256])
+def test_noalloc_wide_head_dims(gpu_lib, d):
+    # d = 192 / 256: the kernel of attn_fwd at those head dimensions, bit for bit, and no
+    # change to the memory pool on a fresh stream
+    import torch
+    shape = (2, 3, 520, 1290)
+    want = _run(gpu_lib, "attn_fwd", shape, d=d)
+    bufs = _prepare(shape, d)
+    if torch.cuda.get_allocator_backend() == "native":
+        drv = Driver()
+        s1 = drv.new_stream()
+        before = drv.pool_bytes()
+        _call(gpu_lib, "attn_fwd_noalloc", shape, bufs, stream=s1, d=d)
+        assert drv.pool_bytes() == before, "attn_fwd_noalloc changed the memory pool"
+    else:
+        _call(gpu_lib, "attn_fwd_noalloc", shape, bufs, d=d)
+    _assert_same(_result(bufs), want, f"noalloc at d = {d}")
