@@ -69,7 +69,7 @@ def test_fp8qk_other_scales(gpu_lib, scale):
     check_fp8(gpu_lib, 1, 2, 256, 640, seed=13200, scale=scale)
 
 
-@pytest.mark.parametrize("name", ["rect-4k-8k", "square-4k"])
+@pytest.mark.parametrize("name", ["rect-4k-8k", "square-4k", "long-16k"])
 def test_fp8qk_workload_sampled_rows(gpu_lib, name):
     # the measured shapes at full size, in the launch configuration the benchmark times
     w = by_name(name)
@@ -181,7 +181,7 @@ def test_fp8_wide_value_rows(gpu_lib):
     check_fp8pv(gpu_lib, 1, 2, 256, 300, seed=14300, ldv=512)
 
 
-@pytest.mark.parametrize("name", ["rect-4k-8k", "square-4k"])
+@pytest.mark.parametrize("name", ["rect-4k-8k", "square-4k", "long-16k"])
 def test_fp8_workload_sampled_rows(gpu_lib, name):
     w = by_name(name)
     rows = sample_rows(w.B, w.H, w.Nq, per_head=16)

@@ -103,7 +103,7 @@ def test_mxfp8_scales_vary_per_block(gpu_lib):
     check_mx(gpu_lib, 1, 2, 256, 640, seed=0, inputs=inputs)
 
 
-@pytest.mark.parametrize("name", ["rect-4k-8k", "square-4k"])
+@pytest.mark.parametrize("name", ["rect-4k-8k", "square-4k", "long-16k"])
 def test_mxfp8_workload_sampled_rows(gpu_lib, name):
     # the measured shapes at full size, in the launch configuration the benchmark times
     w = by_name(name)

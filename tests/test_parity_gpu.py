@@ -176,11 +176,14 @@ def test_causal_peaked_and_other_scales(gpu_lib):
     check_case(gpu_lib, 1, 2, 512, 2048, seed=74, scale=2.0, ulp_aware=True, causal=True)
 
 
-@pytest.mark.parametrize("name", ["square-4k", "long-16k"])
+@pytest.mark.parametrize("name", ["square-4k", "long-16k", "rect-4k-8k", "peaked-8k"])
 def test_causal_workload_sampled_rows(gpu_lib, name):
+    # every workload under the causal mask as `bench.py --causal` launches it (rect-4k-8k:
+    # 128 groups, fewer than two per SM, so their key ranges are split between blocks)
     w = by_name(name)
     rows = sample_rows(w.B, w.H, w.Nq, per_head=16)
-    check_case(gpu_lib, w.B, w.H, w.Nq, w.Nk, seed=w.seed, scale=w.scale, rows=rows, causal=True)
+    check_case(gpu_lib, w.B, w.H, w.Nq, w.Nk, seed=w.seed, qk_mult=w.qk_mult, scale=w.scale, rows=rows, causal=True,
+               ulp_aware=w.qk_mult != 1.0)
 
 
 def test_causal_rejects_more_queries_than_keys(gpu_lib):
@@ -249,7 +252,7 @@ def test_bias_of_zeros_matches_the_plain_entry_point(gpu_lib):
     assert np.max(np.abs(ob - o0)) <= 1e-2 and np.max(np.abs(lb - l0)) <= 1e-5 * np.max(np.abs(l0))
 
 
-@pytest.mark.parametrize("name,kind", [("rect-4k-8k", "shared"), ("rect-4k-8k", "full")])
+@pytest.mark.parametrize("name,kind", [("rect-4k-8k", "shared"), ("rect-4k-8k", "full"), ("square-4k", "shared")])
 def test_bias_workload_sampled_rows(gpu_lib, name, kind):
     # the default benchmark shape with one [Nq, Nk] bias shared by every head, or one bias per
     # (batch, head) (537 MB of BF16 for this shape), as `bench.py --bias` times them

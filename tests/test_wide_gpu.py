@@ -191,3 +191,22 @@ def test_wide_bias_deterministic(gpu_lib):
     o1, l1 = run_gpu(gpu_lib, q, k, v, 0.07, bias=bias)
     o2, l2 = run_gpu(gpu_lib, q, k, v, 0.07, bias=bias)
     assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
+
+
+@pytest.mark.parametrize("d", [192, 256])
+@pytest.mark.parametrize("name", ["rect-4k-8k", "square-4k", "peaked-8k", "long-16k"])
+def test_wide_workload_sampled_rows(gpu_lib, d, name):
+    # the four workloads at d = 192 and 256 as `bench.py --head-dim` launches them
+    from dense_attention_forward_fwd_gb300.configs import by_name
+    w = by_name(name)
+    rows = sample_rows(w.B, w.H, w.Nq, per_head=8)
+    check_case(gpu_lib, w.B, w.H, w.Nq, w.Nk, seed=w.seed + d, qk_mult=w.qk_mult, rows=rows, d=d,
+               ulp_aware=w.qk_mult != 1.0)
+
+
+@pytest.mark.parametrize("name", ["rect-4k-8k", "long-16k"])
+def test_wide_causal_workload_sampled_rows(gpu_lib, name):
+    from dense_attention_forward_fwd_gb300.configs import by_name
+    w = by_name(name)
+    rows = sample_rows(w.B, w.H, w.Nq, per_head=8)
+    check_case(gpu_lib, w.B, w.H, w.Nq, w.Nk, seed=w.seed + 256, rows=rows, d=256, causal=True)
