@@ -60,12 +60,19 @@ constexpr int kThreads = 256;
 constexpr float kRescaleLog2 = 32.0f;     // the running maximum moves when a tile's exceeds it by this
 constexpr int kTmemCols = 512;
 constexpr int kMaxChunks = 4;             // d <= 256
+// K boxes that share one full and one free barrier. Each barrier operation of the MMA
+// thread leaves the tensor pipe idle for about 95 cycles, which sets the pace at d = 256,
+// where the tensor work of a step exceeds the softmax's: there boxes go in pairs (measured
+// +7 to +10 %; the whole tile at once loses on short key ranges). At d = 192 the softmax
+// sets the pace and each box keeps its own barriers, so the first Q K^T steps start early.
+template <int D>
+constexpr int kKGroupBoxesFor = D == 256 ? 2 : 1;
 
 // barriers
 constexpr int kBarQFull = 0;
 constexpr int kBarQEmpty = 1;                     // the tile's last Q K^T is done with Q
-constexpr int kBarKFull = 2;                      // [box]
-constexpr int kBarKFree = kBarKFull + kMaxChunks; // [box]: the Q K^T steps that read it are done
+constexpr int kBarKFull = 2;                      // [box group]
+constexpr int kBarKFree = kBarKFull + kMaxChunks; // [box group]: the Q K^T steps that read it are done
 constexpr int kBarVFull = kBarKFree + kMaxChunks; // [half-tile slot]
 constexpr int kBarVFree = kBarVFull + kMaxVSlots; // [half-tile slot]: its half of P V is done
 constexpr int kBarSFull = kBarVFree + kMaxVSlots; // [2 buffers]
@@ -194,6 +201,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   using L = Layout<D, kBias>;
   constexpr int kVSlots = L::kVSlots;
   constexpr int kChunks = L::kChunks;
+  constexpr int kKGroupBoxes = kKGroupBoxesFor<D>;
+  constexpr int kKGroups = (kChunks + kKGroupBoxes - 1) / kKGroupBoxes;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -232,19 +241,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmK)) : "memory");
       asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmV)) : "memory");
       int u = 0, gj = 0;           // query tiles started, steps of earlier tiles
-      int k_loads[kMaxChunks] = {0, 0, 0, 0};   // loads requested into each K box
+      int k_loads[kMaxChunks] = {0, 0, 0, 0};   // loads requested into each K box group
       int v_halves = 0;                          // V halves requested
       bool ok = true;
       auto load_k = [&](int t, int bh) {   // key tile t of this query tile (global step gj + t)
         const int gt = gj + t;
-        for (int cc = 0; ok && cc < kChunks; ++cc) {
-          if (gt > 0 && !wait_phase(c, kBarKFree + cc, static_cast<uint32_t>(gt - 1) & 1u, true)) {
+        for (int g = 0; ok && g < kKGroups; ++g) {
+          if (gt > 0 && !wait_phase(c, kBarKFree + g, static_cast<uint32_t>(gt - 1) & 1u, true)) {
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(c.bar(kBarKFull + cc), kBoxBytes);
-          tma_load_3d(sK + cc * kBoxBytes, &tmK, c.bar(kBarKFull + cc), cc * kBoxCols, t * kBN, bh);
-          k_loads[cc] = gt + 1;
+          const int c0 = g * kKGroupBoxes, c1 = min(kChunks, c0 + kKGroupBoxes);
+          mbar_arrive_expect_tx(c.bar(kBarKFull + g), (c1 - c0) * kBoxBytes);
+          for (int cc = c0; cc < c1; ++cc)
+            tma_load_3d(sK + cc * kBoxBytes, &tmK, c.bar(kBarKFull + g), cc * kBoxCols, t * kBN, bh);
+          k_loads[g] = gt + 1;
         }
       };
       auto load_v = [&](int t, int bh) {   // both 64-key halves of V_t
@@ -278,8 +289,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       // no copy into shared memory may be in flight when the block exits
       if (u > 0) wait_phase(c, kBarQFull, (u - 1) & 1, false);
-      for (int cc = 0; cc < kChunks; ++cc)
-        if (k_loads[cc] > 0) wait_phase(c, kBarKFull + cc, static_cast<uint32_t>(k_loads[cc] - 1) & 1u, false);
+      for (int g = 0; g < kKGroups; ++g)
+        if (k_loads[g] > 0) wait_phase(c, kBarKFull + g, static_cast<uint32_t>(k_loads[g] - 1) & 1u, false);
       for (int vi = v_halves > kVSlots ? v_halves - kVSlots : 0; vi < v_halves; ++vi)
         wait_phase(c, kBarVFull + vi % kVSlots, static_cast<uint32_t>(vi / kVSlots) & 1u, false);
     }
@@ -292,21 +303,25 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t kIdQK = idesc_bf16(kBM, kBN, false);
       constexpr uint32_t kIdPV = idesc_bf16(kBM, D, true);
       bool ok = true;
-      // S = Q K^T for the key tile of global step gt, box by box; each box is released as
-      // soon as the four K16 steps that read it are done
+      // S = Q K^T for the key tile of global step gt, group by group of boxes; each group
+      // is released as soon as the K16 steps that read it are done
       auto qk = [&](uint32_t d_tmem, int gt) {
-        for (int cc = 0; cc < kChunks; ++cc) {
-          if (!wait_phase(c, kBarKFull + cc, static_cast<uint32_t>(gt) & 1u, true)) {
+        for (int g = 0; g < kKGroups; ++g) {
+          if (!wait_phase(c, kBarKFull + g, static_cast<uint32_t>(gt) & 1u, true)) {
             ok = false;
             return;
           }
           tc_fence_after();
+          const int c0 = g * kKGroupBoxes, c1 = min(kChunks, c0 + kKGroupBoxes);
+          for (int cc = c0; cc < c1; ++cc) {
 #pragma unroll
-          for (int k4 = 0; k4 < 4; ++k4) {
-            const uint32_t off = static_cast<uint32_t>(cc * kBoxBytes + k4 * 32);
-            mma_ss(d_tmem, sdesc_sw128(sQ + off, 16, 1024), sdesc_sw128(sK + off, 16, 1024), kIdQK, cc > 0 || k4 > 0);
+            for (int k4 = 0; k4 < 4; ++k4) {
+              const uint32_t off = static_cast<uint32_t>(cc * kBoxBytes + k4 * 32);
+              mma_ss(d_tmem, sdesc_sw128(sQ + off, 16, 1024), sdesc_sw128(sK + off, 16, 1024), kIdQK,
+                     cc > 0 || k4 > 0);
+            }
           }
-          tc_commit(c.bar(kBarKFree + cc));
+          tc_commit(c.bar(kBarKFree + g));
         }
       };
       int u = 0, gj = 0;
