@@ -1851,7 +1851,7 @@ namespace {
 // Head dimensions above 128: the one-Q-tile kernel (attn_fwd_wide.cu), after the argument
 // checks of the d = 128 entry points (causal: also Nq <= Nk).
 int forward_wide(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Nq, int Nk,
-                 int d, float scale, bool causal, void* stream, const BiasArg* bias = nullptr) {
+                 int d, float scale, bool causal, void* stream, const BiasArg* bias = nullptr, bool qk8 = false) {
   if (B < 0 || H < 0 || Nq < 0 || Nk < 0 || !std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
   if (static_cast<long long>(B) * H == 0 || Nq == 0) return ATTN_OK;
   if (Nk == 0 || (causal && Nq > Nk) || !q || !k || !v || !o || !lse) return ATTN_ERR_INVALID_ARG;
@@ -1868,7 +1868,7 @@ int forward_wide(const void* q, const void* k, const void* v, void* o, float* ls
     wb = {bias->ptr, bias->sb, bias->sh, bias->sq};
   }
   const int rc = attn_wide::forward(q, k, v, o, lse, B, H, Nq, Nk, d, scale, causal, static_cast<cudaStream_t>(stream),
-                                    g_wait_limit.load(std::memory_order_relaxed), bias != nullptr ? &wb : nullptr);
+                                    g_wait_limit.load(std::memory_order_relaxed), bias != nullptr ? &wb : nullptr, qk8);
   if (rc == ATTN_OK) g_launches.fetch_add(1, std::memory_order_relaxed);
   return rc;
 }
@@ -1903,6 +1903,8 @@ extern "C" int attn_fwd_fp8qk(const void* q8, const void* k8, const void* v, voi
     return ATTN_ERR_INVALID_ARG;
   const double eff = static_cast<double>(scale) * q_descale * k_descale;
   if (!(std::fabs(eff) <= static_cast<double>(FLT_MAX))) return ATTN_ERR_INVALID_ARG;
+  if (attn_wide::supported(d))
+    return forward_wide(q8, k8, v, o, lse, B, H, Nq, Nk, d, static_cast<float>(eff), false, stream, nullptr, true);
   return forward(q8, k8, v, nullptr, o, lse, B, H, Nq, Nk, d, static_cast<float>(eff), stream, 1);
 }
 
@@ -2064,6 +2066,7 @@ extern "C" int attn_fwd_fp8qk_causal(const void* q8, const void* k8, const void*
   int rc = ATTN_OK;
   const float eff = fp8_scale(scale, q_descale, k_descale, 1.0f, &rc);
   if (rc != ATTN_OK) return rc;
+  if (attn_wide::supported(d)) return forward_wide(q8, k8, v, o, lse, B, H, Nq, Nk, d, eff, true, stream, nullptr, true);
   return forward_causal(q8, k8, v, o, lse, B, H, Nq, Nk, d, eff, stream, 1);
 }
 extern "C" int attn_fwd_fp8_causal(const void* q8, const void* k8, const void* vt8, long long ldv, void* o,
@@ -2084,6 +2087,7 @@ extern "C" int attn_fwd_fp8qk_bias(const void* q8, const void* k8, const void* v
   const float eff = fp8_scale(scale, q_descale, k_descale, 1.0f, &rc);
   if (rc != ATTN_OK) return rc;
   const BiasArg ba = {bias, bias_stride_b, bias_stride_h, bias_stride_q};
+  if (attn_wide::supported(d)) return forward_wide(q8, k8, v, o, lse, B, H, Nq, Nk, d, eff, false, stream, &ba, true);
   return forward(q8, k8, v, &ba, o, lse, B, H, Nq, Nk, d, eff, stream, 1);
 }
 extern "C" int attn_fwd_fp8_bias(const void* q8, const void* k8, const void* vt8, long long ldv, const void* bias,

@@ -68,6 +68,20 @@ constexpr int kMaxChunks = 4;             // d <= 256
 template <int D>
 constexpr int kKGroupBoxesFor = D == 256 ? 2 : 1;
 
+// kind::f8f6f4 instruction descriptor: E4M3 x E4M3 -> FP32 (format code 0 for A and B),
+// M = 128, N = 128, both K-major (S = Q K^T from FP8 codes)
+constexpr uint32_t kIdQK8 =
+    (1u << 4) | (static_cast<uint32_t>(128 >> 3) << 17) | (static_cast<uint32_t>(128 >> 4) << 24);
+// D (TMEM) (+)= A (shared memory) * B (shared memory), 8-bit floating-point operands
+__device__ __forceinline__ void mma_ss_e4m3(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, bool acc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
+      "l"(a), "l"(b), "r"(idesc), "r"(static_cast<uint32_t>(acc))
+      : "memory");
+}
+
 // barriers
 constexpr int kBarQFull = 0;
 constexpr int kBarQEmpty = 1;                     // the tile's last Q K^T is done with Q
@@ -84,13 +98,16 @@ constexpr int kNumBars = kBarDrain + 1;
 constexpr int kFlagsBytes = kNumBars * 8 + 8;     // barriers, TMEM slot, abort flag
 
 // With a bias, each softmax warp stages its rows' bias in shared memory; at d = 256 that
-// room comes from one V slot.
-template <int D, bool kBias>
+// room comes from one V slot. With Q and K as FP8 codes (kF8) a box holds 128 columns
+// (128 bytes) of the head dimension: two boxes per tile at d = 192 and 256 (at d = 192 the
+// second box's upper half lies past the tensor and is filled with zeros).
+template <int D, bool kBias, bool kF8 = false>
 struct Layout {
-  static constexpr int kChunks = D / kBoxCols;             // boxes per Q or K tile
-  static constexpr int kTileBytes = kChunks * kBoxBytes;
+  static constexpr int kChunks = D / kBoxCols;             // V boxes: 64 BF16 columns
+  static constexpr int kQKChunks = kF8 ? (D + 127) / 128 : kChunks;   // boxes per Q or K tile
+  static constexpr int kTileBytes = kQKChunks * kBoxBytes;  // one Q or K tile
   static constexpr int kHalfBytes = kChunks * kBoxBytes / 2;   // V: 64 keys x d
-  static constexpr int kVSlots = (kBias && D == 256) ? 2 : kMaxVSlots;
+  static constexpr int kVSlots = (kBias && D == 256 && !kF8) ? 2 : kMaxVSlots;
   static constexpr int kOffQ = 0;
   static constexpr int kOffK = kOffQ + kTileBytes;
   static constexpr int kOffV = kOffK + kTileBytes;
@@ -194,14 +211,16 @@ __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wai
 // query tiles' key tiles, in order) uses S buffer gs & 1 and K tile gs (box c in K slot c);
 // its V halves are half tiles 2 gs and 2 gs + 1, in V slots (2 gs + h) % kVSlots. A ring
 // barrier completes once per use of its slot, so the k-th use waits for parity k & 1.
-template <int D, bool kPos, bool kBias>
+template <int D, bool kPos, bool kBias, bool kF8>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                          const __grid_constant__ CUtensorMap tmV, const Params p) {
-  using L = Layout<D, kBias>;
+  using L = Layout<D, kBias, kF8>;
   constexpr int kVSlots = L::kVSlots;
-  constexpr int kChunks = L::kChunks;
-  constexpr int kKGroupBoxes = kKGroupBoxesFor<D>;
+  constexpr int kChunks = L::kQKChunks;   // Q and K boxes
+  constexpr int kVChunks = L::kChunks;    // V boxes
+  constexpr int kQKBoxCols = kF8 ? 128 : kBoxCols;   // head-dimension columns per Q or K box
+  constexpr int kKGroupBoxes = kF8 ? 1 : kKGroupBoxesFor<D>;
   constexpr int kKGroups = (kChunks + kKGroupBoxes - 1) / kKGroupBoxes;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -254,7 +273,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int c0 = g * kKGroupBoxes, c1 = min(kChunks, c0 + kKGroupBoxes);
           mbar_arrive_expect_tx(c.bar(kBarKFull + g), (c1 - c0) * kBoxBytes);
           for (int cc = c0; cc < c1; ++cc)
-            tma_load_3d(sK + cc * kBoxBytes, &tmK, c.bar(kBarKFull + g), cc * kBoxCols, t * kBN, bh);
+            tma_load_3d(sK + cc * kBoxBytes, &tmK, c.bar(kBarKFull + g), cc * kQKBoxCols, t * kBN, bh);
           k_loads[g] = gt + 1;
         }
       };
@@ -266,7 +285,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           mbar_arrive_expect_tx(c.bar(kBarVFull + slot), L::kHalfBytes);
-          for (int cc = 0; cc < kChunks; ++cc)
+          for (int cc = 0; cc < kVChunks; ++cc)
             tma_load_3d(vslot(vi) + cc * (kBoxBytes / 2), &tmV, c.bar(kBarVFull + slot), cc * kBoxCols,
                         t * kBN + h * (kBN / 2), bh);
           v_halves = vi + 1;
@@ -278,7 +297,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (u > 0 && !wait_phase(c, kBarQEmpty, (u - 1) & 1, true)) break;
         mbar_arrive_expect_tx(c.bar(kBarQFull), L::kTileBytes);
         for (int cc = 0; cc < kChunks; ++cc)
-          tma_load_3d(sQ + cc * kBoxBytes, &tmQ, c.bar(kBarQFull), cc * kBoxCols, qt * kBM, bh);
+          tma_load_3d(sQ + cc * kBoxBytes, &tmQ, c.bar(kBarQFull), cc * kQKBoxCols, qt * kBM, bh);
         ++u;
         load_k(0, bh);
         for (int t = 0; ok && t < n; ++t) {
@@ -314,11 +333,19 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_after();
           const int c0 = g * kKGroupBoxes, c1 = min(kChunks, c0 + kKGroupBoxes);
           for (int cc = c0; cc < c1; ++cc) {
+            // 32 bytes of each 128-byte row per MMA: 16 BF16 columns, or 32 FP8 columns (at
+            // d = 192 the second FP8 box holds 64 columns: two MMAs)
+            const int steps = kF8 ? min(4, (D - cc * 128) / 32) : 4;
 #pragma unroll
             for (int k4 = 0; k4 < 4; ++k4) {
+              if (k4 >= steps) break;
               const uint32_t off = static_cast<uint32_t>(cc * kBoxBytes + k4 * 32);
-              mma_ss(d_tmem, sdesc_sw128(sQ + off, 16, 1024), sdesc_sw128(sK + off, 16, 1024), kIdQK,
-                     cc > 0 || k4 > 0);
+              if constexpr (kF8)
+                mma_ss_e4m3(d_tmem, sdesc_sw128(sQ + off, 16, 1024), sdesc_sw128(sK + off, 16, 1024), kIdQK8,
+                            cc > 0 || k4 > 0);
+              else
+                mma_ss(d_tmem, sdesc_sw128(sQ + off, 16, 1024), sdesc_sw128(sK + off, 16, 1024), kIdQK,
+                       cc > 0 || k4 > 0);
             }
           }
           tc_commit(c.bar(kBarKFree + g));
@@ -604,43 +631,58 @@ PFN_cuTensorMapEncodeTiled_v12000 encoder() {
 }
 
 // [BH, rows, d] BF16 as a 3-D tensor (d innermost); box = 64 columns x box_rows rows x 1.
-bool make_map(CUtensorMap* map, const void* ptr, int rows, long long bh, int d, int box_rows) {
+// f8: E4M3 codes, one byte per element, boxes of 128 columns (128 bytes as for BF16).
+bool make_map(CUtensorMap* map, const void* ptr, int rows, long long bh, int d, int box_rows, bool f8 = false) {
   auto enc = encoder();
   if (!enc) return false;
+  const cuuint64_t es = f8 ? 1 : 2;
   cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(bh)};
-  cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2, static_cast<cuuint64_t>(rows) * d * 2};
-  cuuint32_t box[3] = {kBoxCols, static_cast<cuuint32_t>(box_rows), 1};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * es, static_cast<cuuint64_t>(rows) * d * es};
+  cuuint32_t box[3] = {f8 ? 128u : static_cast<cuuint32_t>(kBoxCols), static_cast<cuuint32_t>(box_rows), 1};
   cuuint32_t elem[3] = {1, 1, 1};
-  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, elem,
+  return enc(map, f8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr),
+             dims, strides, box, elem,
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 constexpr int kMaxDevices = 64;
-std::atomic<int> g_attr_done[6][kMaxDevices];   // per instantiation (d, sign of the scale or bias) and device
+// per instantiation (d, sign of the scale or bias, FP8 Q and K) and device
+std::atomic<int> g_attr_done[12][kMaxDevices];
 
-template <int D, bool kPos, bool kBias = false>
+template <int D, bool kPos, bool kBias, bool kF8>
 int launch(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, const Params& p, int grid, int dev,
            cudaStream_t stream) {
-  auto kern = attn_fwd_wide_kernel<D, kPos, kBias>;
-  constexpr int kInst = (D == 256 ? 3 : 0) + (kBias ? 2 : (kPos ? 1 : 0));
+  auto kern = attn_fwd_wide_kernel<D, kPos, kBias, kF8>;
+  constexpr int kInst = 2 * ((D == 256 ? 3 : 0) + (kBias ? 2 : (kPos ? 1 : 0))) + (kF8 ? 1 : 0);
+  constexpr int kSmem = Layout<D, kBias, kF8>::kSmem;
   if (dev < 0 || dev >= kMaxDevices || !g_attr_done[kInst][dev].load(std::memory_order_acquire)) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Layout<D, kBias>::kSmem) != cudaSuccess)
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem) != cudaSuccess)
       return ATTN_ERR_CUDA;
     if (dev >= 0 && dev < kMaxDevices) g_attr_done[kInst][dev].store(1, std::memory_order_release);
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(grid));
   cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = Layout<D, kBias>::kSmem;
+  cfg.dynamicSmemBytes = kSmem;
   cfg.stream = stream;
   return cudaLaunchKernelEx(&cfg, kern, mq, mk, mv, p) == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
 }  // namespace
 
+// One head dimension, scale sign, bias and Q/K format.
+template <int D, bool kF8>
+int launch_d(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, const Params& p, int grid, int dev,
+             cudaStream_t stream, bool bias, float scale) {
+  // with a bias the scale is applied before the row max: one instantiation serves any sign
+  if (bias) return launch<D, true, true, kF8>(mq, mk, mv, p, grid, dev, stream);
+  return scale > 0.0f ? launch<D, true, false, kF8>(mq, mk, mv, p, grid, dev, stream)
+                      : launch<D, false, false, kF8>(mq, mk, mv, p, grid, dev, stream);
+}
+
 int forward(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Nq, int Nk, int d,
-            float scale, bool causal, cudaStream_t stream, unsigned long long wait_limit, const Bias* bias) {
+            float scale, bool causal, cudaStream_t stream, unsigned long long wait_limit, const Bias* bias, bool qk8) {
   if (!supported(d)) return ATTN_ERR_UNSUPPORTED;
   const long long bh = static_cast<long long>(B) * H;
   const long long q_tiles = (static_cast<long long>(Nq) + kBM - 1) / kBM;
@@ -650,7 +692,7 @@ int forward(const void* q, const void* k, const void* v, void* o, float* lse, in
       cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
     return ATTN_ERR_CUDA;
   CUtensorMap mq, mk, mv;
-  if (!make_map(&mq, q, Nq, bh, d, kBM) || !make_map(&mk, k, Nk, bh, d, kBN) ||
+  if (!make_map(&mq, q, Nq, bh, d, kBM, qk8) || !make_map(&mk, k, Nk, bh, d, kBN, qk8) ||
       !make_map(&mv, v, Nk, bh, d, kBN / 2))
     return ATTN_ERR_CUDA;
   Params p;
@@ -674,15 +716,12 @@ int forward(const void* q, const void* k, const void* v, void* o, float* lse, in
   p.H = H;
   p.scale = scale;
   const int grid = std::min(sms, p.groups);
-  // with a bias the scale is applied before the row max: one instantiation serves any sign
-  if (bias != nullptr)
-    return d == 256 ? launch<256, true, true>(mq, mk, mv, p, grid, dev, stream)
-                    : launch<192, true, true>(mq, mk, mv, p, grid, dev, stream);
+  const bool b = bias != nullptr;
   if (d == 256)
-    return scale > 0.0f ? launch<256, true>(mq, mk, mv, p, grid, dev, stream)
-                        : launch<256, false>(mq, mk, mv, p, grid, dev, stream);
-  return scale > 0.0f ? launch<192, true>(mq, mk, mv, p, grid, dev, stream)
-                      : launch<192, false>(mq, mk, mv, p, grid, dev, stream);
+    return qk8 ? launch_d<256, true>(mq, mk, mv, p, grid, dev, stream, b, scale)
+               : launch_d<256, false>(mq, mk, mv, p, grid, dev, stream, b, scale);
+  return qk8 ? launch_d<192, true>(mq, mk, mv, p, grid, dev, stream, b, scale)
+             : launch_d<192, false>(mq, mk, mv, p, grid, dev, stream, b, scale);
 }
 
 int take_status(cudaStream_t stream) {

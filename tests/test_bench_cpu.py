@@ -23,7 +23,8 @@ def run_bench(*flags):
 
 
 @pytest.mark.parametrize("flags", [(), ("--causal",), ("--bias", "shared"), ("--backward",), ("--fp8-qk",),
-                                   ("--fp8",), ("--head-dim", "256", "--bias", "full")])
+                                   ("--fp8",), ("--head-dim", "256", "--bias", "full"),
+                                   ("--head-dim", "256", "--fp8-qk", "--causal")])
 def test_reference_arm_prints_the_contract_line(flags):
     r = run_bench(*flags)
     assert r.returncode == 0, r.stderr[-2000:]
@@ -48,7 +49,7 @@ def test_reference_arm_prints_the_contract_line(flags):
 @pytest.mark.parametrize("flags", [("--mxfp8", "--bias", "full"), ("--fp8-qk", "--bias", "shared", "--causal"),
                                    ("--fp8", "--fp8-qk"),
                                    ("--bias", "full", "--causal"), ("--head-dim", "256", "--backward"),
-                                   ("--head-dim", "256", "--fp8-qk"),
+                                   ("--head-dim", "256", "--fp8"),
                                    ("--fp8", "--backward")])
 def test_flags_without_an_entry_point_are_refused(flags):
     r = run_bench(*flags)
@@ -81,7 +82,8 @@ def test_traffic_keys_match_the_recorded_ones():
              "square-4k-bias-shared-backward": ("square-4k", {"bias": "shared", "backward": True}),
              "rect-4k-8k-bias-shared-fp8qk": ("rect-4k-8k", {"bias": "shared", "fp8_qk": True}),
              "square-4k-d256": ("square-4k", {"d": 256}),
-             "square-4k-bias-shared-d256": ("square-4k", {"bias": "shared", "d": 256})}
+             "square-4k-bias-shared-d256": ("square-4k", {"bias": "shared", "d": 256}),
+             "square-4k-fp8qk-d256": ("square-4k", {"fp8_qk": True, "d": 256})}
     recorded = json.load(open(os.path.join(ROOT, "profiles", "traffic.json")))
     assert set(recorded) <= set(cases)
     for key, (name, over) in cases.items():

@@ -205,9 +205,10 @@ def call_fp8(q8=A, k8=A, v=A, o=A, lse=A, B=1, H=1, Nq=128, Nk=128, d=128, scale
     (dict(Nq=0, lse=None), attn.ATTN_OK),
 ])
 @pytest.mark.parametrize("causal", [False, True])
-def test_fp8qk_argument_checks(kw, code, causal):
+@pytest.mark.parametrize("d", [128, 256])   # d = 256: the one-query-tile kernel's checks
+def test_fp8qk_argument_checks(kw, code, causal, d):
     before = attn.attn_fwd_kernel_count()
-    assert call_fp8(causal=causal, **kw) == code
+    assert call_fp8(causal=causal, **dict({"d": d}, **kw)) == code
     assert attn.attn_fwd_kernel_count() == before
 
 

@@ -68,6 +68,13 @@ def test_forward_wide_head_dims(gpu_lib, d, B, H, Nq, Nk):
         (fo, o), (fl, lse) = guarded((B, H, Nq, d), "bf16", "cuda"), guarded((B, H, Nq), "f32", "cuda")
         gpu_lib.attn_fwd_bias(q, k, v, bias, o, lse, B, H, Nq, Nk, d, d ** -0.5)
         check(gpu_lib, ((fo, o), "bf16"), ((fl, lse), "f32"))
+    # attn_fwd_fp8qk at the same head dimension (Q and K as E4M3 codes)
+    import torch
+    q8, k8, v8b, dq, dk = make_qk_e4m3(B, H, Nq, Nk, d=d, seed=17500 + Nq + Nk + d)
+    (fo, o), (fl, lse) = guarded((B, H, Nq, d), "bf16", "cuda"), guarded((B, H, Nq), "f32", "cuda")
+    gpu_lib.attn_fwd_fp8qk(torch.from_numpy(q8).cuda(), torch.from_numpy(k8).cuda(), to_device(v8b), o, lse, B, H,
+                           Nq, Nk, d, d ** -0.5, dq, dk)
+    check(gpu_lib, ((fo, o), "bf16"), ((fl, lse), "f32"))
 
 
 @pytest.mark.parametrize("B,H,Nq,Nk", SHAPES)

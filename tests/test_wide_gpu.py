@@ -210,3 +210,86 @@ def test_wide_causal_workload_sampled_rows(gpu_lib, name):
     w = by_name(name)
     rows = sample_rows(w.B, w.H, w.Nq, per_head=8)
     check_case(gpu_lib, w.B, w.H, w.Nq, w.Nk, seed=w.seed + 256, rows=rows, d=256, causal=True)
+
+
+# ---- Q and K as FP8 E4M3 codes (the attn_fwd_fp8qk family at d > 128): Q K^T on kind::f8f6f4 ----
+
+def run_fp8_wide(attn, q8, k8, v, scale, dq, dk, causal=False, bias=None):
+    import torch
+    from parity import bf16_to_np, to_device
+    B, H, Nq, d = q8.shape
+    Nk = k8.shape[2]
+    o = torch.full((B, H, Nq, d), float("nan"), dtype=torch.bfloat16, device="cuda")
+    lse = torch.full((B, H, Nq), float("nan"), dtype=torch.float32, device="cuda")
+    attn.attn_fwd_fp8qk(torch.from_numpy(q8).cuda(), torch.from_numpy(k8).cuda(), to_device(v), o, lse, B, H, Nq,
+                        Nk, d, scale, dq, dk, causal=causal, bias=None if bias is None else to_device(bias))
+    assert attn.attn_fwd_status() == attn.ATTN_OK
+    return bf16_to_np(o), lse.cpu().numpy()
+
+
+def check_fp8_wide(attn, B, H, Nq, Nk, d, seed, qk_mult=1.0, rows=None, causal=False, bias=None):
+    from dense_attention_forward_fwd_gb300.inputs import make_qk_e4m3
+    from parity import compare
+    import oracle
+    scale = d ** -0.5
+    q8, k8, v, dq, dk = make_qk_e4m3(B, H, Nq, Nk, d=d, seed=seed, qk_mult=qk_mult)
+    o, lse = run_fp8_wide(attn, q8, k8, v, scale, dq, dk, causal, bias)
+    o_ref, lse_ref = oracle.attention_rows_e4m3qk(q8, k8, v, scale, dq, dk, rows, causal=causal, bias=bias)
+    o, lse = o.reshape(-1, d), lse.reshape(-1)
+    if rows is not None:
+        o, lse = o[rows], lse[rows]
+    return compare(o, lse, o_ref, lse_ref, ulp_aware=qk_mult != 1.0 or bias is not None)
+
+
+@pytest.mark.parametrize("d", [192, 256])
+@pytest.mark.parametrize("B,H,Nq,Nk", [
+    (1, 1, 128, 128),
+    (1, 2, 300, 200),     # ragged Nq and Nk
+    (2, 3, 1000, 777),
+    (1, 1, 1, 129),
+    (1, 2, 128, 2176),    # 17 key steps
+    (2, 8, 2048, 1024),   # more query tiles than blocks
+])
+def test_wide_fp8qk_parity(gpu_lib, d, B, H, Nq, Nk):
+    check_fp8_wide(gpu_lib, B, H, Nq, Nk, d, seed=18000 + Nq + Nk + d)
+
+
+@pytest.mark.parametrize("d", [192, 256])
+@pytest.mark.parametrize("B,H,Nq,Nk", [(1, 2, 256, 384), (2, 3, 300, 1000)])
+def test_wide_fp8qk_causal_parity(gpu_lib, d, B, H, Nq, Nk):
+    check_fp8_wide(gpu_lib, B, H, Nq, Nk, d, seed=18100 + Nq + Nk + d, causal=True)
+
+
+@pytest.mark.parametrize("d", [192, 256])
+@pytest.mark.parametrize("B,H,Nq,Nk,kind", [(2, 3, 300, 1000, "full"), (1, 2, 384, 640, "shared")])
+def test_wide_fp8qk_bias_parity(gpu_lib, d, B, H, Nq, Nk, kind):
+    bias = make_bias(_bias_shape(kind, B, H, Nq, Nk), seed=18200 + Nq + Nk + d, std=2.0)
+    check_fp8_wide(gpu_lib, B, H, Nq, Nk, d, seed=18300 + Nq + Nk + d, bias=bias)
+
+
+def test_wide_fp8qk_peaked(gpu_lib):
+    check_fp8_wide(gpu_lib, 1, 2, 512, 2048, 256, seed=18400, qk_mult=3.0)
+
+
+@pytest.mark.parametrize("d", [192, 256])
+def test_wide_fp8qk_agrees_with_the_bf16_entry_point(gpu_lib, d):
+    # descale factors of 1: the codes' values are BF16 values, so attn_fwd sees the same inputs
+    torch = pytest.importorskip("torch")
+    from dense_attention_forward_fwd_gb300.inputs import make_qk_e4m3
+    q8, k8, v, _, _ = make_qk_e4m3(1, 2, 384, 640, d=d, seed=18500 + d)
+    widen = lambda c: torch.from_numpy(c).view(torch.float8_e4m3fn).to(torch.bfloat16).view(torch.int16).numpy() \
+        .view(np.uint16)
+    scale = 0.01
+    o8, l8 = run_fp8_wide(gpu_lib, q8, k8, v, scale, 1.0, 1.0)
+    ob, lb = run_gpu(gpu_lib, widen(q8), widen(k8), v, scale)
+    assert np.max(np.abs(o8 - ob)) <= 1e-2 and np.max(np.abs(l8 - lb)) <= 1e-4 * max(1.0, np.max(np.abs(lb)))
+
+
+@pytest.mark.parametrize("d", [192, 256])
+@pytest.mark.parametrize("name", ["square-4k", "long-16k"])
+def test_wide_fp8qk_workload_sampled_rows(gpu_lib, d, name):
+    # as `bench.py --head-dim d --fp8-qk` launches it
+    from dense_attention_forward_fwd_gb300.configs import by_name
+    w = by_name(name)
+    rows = sample_rows(w.B, w.H, w.Nq, per_head=8)
+    check_fp8_wide(gpu_lib, w.B, w.H, w.Nq, w.Nk, d, seed=w.seed + 8 * d, rows=rows)
