@@ -94,9 +94,9 @@ def parse():
                     help="head dimension d of the workload's tensors (192 and 256: the one-Q-tile kernel "
                          "of attn_fwd and attn_fwd_causal; scale 1/sqrt(d))")
     args = ap.parse_args()
-    if args.head_dim != 128 and (args.backward or args.fp8 or args.mxfp8):
-        ap.error("--head-dim 192 / 256 has the forward entry points with BF16 V only (attn_fwd, attn_fwd_causal, "
-                 "attn_fwd_bias and the attn_fwd_fp8qk family)")
+    if args.head_dim != 128 and (args.backward or args.mxfp8):
+        ap.error("--head-dim 192 / 256 has the forward entry points without block scales only (attn_fwd, "
+                 "attn_fwd_causal, attn_fwd_bias and the attn_fwd_fp8qk and attn_fwd_fp8 families)")
     if (args.fp8_qk or args.fp8 or args.mxfp8) and args.backward:
         ap.error("--fp8-qk, --fp8 and --mxfp8 have no backward entry point")
     if args.mxfp8 and args.bias != "none":

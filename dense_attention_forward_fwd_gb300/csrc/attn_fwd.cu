@@ -1851,7 +1851,8 @@ namespace {
 // Head dimensions above 128: the one-Q-tile kernel (attn_fwd_wide.cu), after the argument
 // checks of the d = 128 entry points (causal: also Nq <= Nk).
 int forward_wide(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Nq, int Nk,
-                 int d, float scale, bool causal, void* stream, const BiasArg* bias = nullptr, bool qk8 = false) {
+                 int d, float scale, bool causal, void* stream, const BiasArg* bias = nullptr, int f8 = 0,
+                 long long ldv = 0, float v_scale = 1.0f) {
   if (B < 0 || H < 0 || Nq < 0 || Nk < 0 || !std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
   if (static_cast<long long>(B) * H == 0 || Nq == 0) return ATTN_OK;
   if (Nk == 0 || (causal && Nq > Nk) || !q || !k || !v || !o || !lse) return ATTN_ERR_INVALID_ARG;
@@ -1862,13 +1863,21 @@ int forward_wide(const void* q, const void* k, const void* v, void* o, float* ls
   if (reinterpret_cast<uintptr_t>(lse) & 3u) return ATTN_ERR_MISALIGNED;
   const long long max_rows = static_cast<long long>(Nq > Nk ? Nq : Nk);
   if (static_cast<long long>(B) * H > (LLONG_MAX / (2 * d)) / max_rows) return ATTN_ERR_INVALID_ARG;
+  if (f8 == 2) {
+    // V^T rows of ldv bytes: at least Nk, 16-byte multiples (TMA strides), and the last
+    // byte's offset, B * H * d * ldv, must fit a signed 64-bit offset
+    if (ldv < Nk) return ATTN_ERR_INVALID_ARG;
+    if (ldv % 16 != 0) return ATTN_ERR_MISALIGNED;
+    if (static_cast<long long>(B) * H > (LLONG_MAX / d) / ldv) return ATTN_ERR_INVALID_ARG;
+  }
   attn_wide::Bias wb{};
   if (bias != nullptr) {
     if (const int rc = check_bias(*bias, B, H, Nq); rc != ATTN_OK) return rc;
     wb = {bias->ptr, bias->sb, bias->sh, bias->sq};
   }
   const int rc = attn_wide::forward(q, k, v, o, lse, B, H, Nq, Nk, d, scale, causal, static_cast<cudaStream_t>(stream),
-                                    g_wait_limit.load(std::memory_order_relaxed), bias != nullptr ? &wb : nullptr, qk8);
+                                    g_wait_limit.load(std::memory_order_relaxed), bias != nullptr ? &wb : nullptr, f8,
+                                    ldv, v_scale);
   if (rc == ATTN_OK) g_launches.fetch_add(1, std::memory_order_relaxed);
   return rc;
 }
@@ -1904,7 +1913,7 @@ extern "C" int attn_fwd_fp8qk(const void* q8, const void* k8, const void* v, voi
   const double eff = static_cast<double>(scale) * q_descale * k_descale;
   if (!(std::fabs(eff) <= static_cast<double>(FLT_MAX))) return ATTN_ERR_INVALID_ARG;
   if (attn_wide::supported(d))
-    return forward_wide(q8, k8, v, o, lse, B, H, Nq, Nk, d, static_cast<float>(eff), false, stream, nullptr, true);
+    return forward_wide(q8, k8, v, o, lse, B, H, Nq, Nk, d, static_cast<float>(eff), false, stream, nullptr, 1);
   return forward(q8, k8, v, nullptr, o, lse, B, H, Nq, Nk, d, static_cast<float>(eff), stream, 1);
 }
 
@@ -1918,6 +1927,9 @@ extern "C" int attn_fwd_fp8(const void* q8, const void* k8, const void* vt8, lon
     return ATTN_ERR_INVALID_ARG;
   const double eff = static_cast<double>(scale) * q_descale * k_descale;
   if (!(std::fabs(eff) <= static_cast<double>(FLT_MAX))) return ATTN_ERR_INVALID_ARG;
+  if (attn_wide::supported(d))
+    return forward_wide(q8, k8, vt8, o, lse, B, H, Nq, Nk, d, static_cast<float>(eff), false, stream, nullptr, 2,
+                        ldv, v_descale);
   return forward(q8, k8, vt8, nullptr, o, lse, B, H, Nq, Nk, d, static_cast<float>(eff), stream, 2, ldv, v_descale);
 }
 
@@ -2066,7 +2078,7 @@ extern "C" int attn_fwd_fp8qk_causal(const void* q8, const void* k8, const void*
   int rc = ATTN_OK;
   const float eff = fp8_scale(scale, q_descale, k_descale, 1.0f, &rc);
   if (rc != ATTN_OK) return rc;
-  if (attn_wide::supported(d)) return forward_wide(q8, k8, v, o, lse, B, H, Nq, Nk, d, eff, true, stream, nullptr, true);
+  if (attn_wide::supported(d)) return forward_wide(q8, k8, v, o, lse, B, H, Nq, Nk, d, eff, true, stream, nullptr, 1);
   return forward_causal(q8, k8, v, o, lse, B, H, Nq, Nk, d, eff, stream, 1);
 }
 extern "C" int attn_fwd_fp8_causal(const void* q8, const void* k8, const void* vt8, long long ldv, void* o,
@@ -2075,6 +2087,8 @@ extern "C" int attn_fwd_fp8_causal(const void* q8, const void* k8, const void* v
   int rc = ATTN_OK;
   const float eff = fp8_scale(scale, q_descale, k_descale, v_descale, &rc);
   if (rc != ATTN_OK) return rc;
+  if (attn_wide::supported(d))
+    return forward_wide(q8, k8, vt8, o, lse, B, H, Nq, Nk, d, eff, true, stream, nullptr, 2, ldv, v_descale);
   return forward_causal(q8, k8, vt8, o, lse, B, H, Nq, Nk, d, eff, stream, 2, ldv, v_descale);
 }
 extern "C" int attn_fwd_fp8qk_bias(const void* q8, const void* k8, const void* v, const void* bias,
@@ -2087,7 +2101,7 @@ extern "C" int attn_fwd_fp8qk_bias(const void* q8, const void* k8, const void* v
   const float eff = fp8_scale(scale, q_descale, k_descale, 1.0f, &rc);
   if (rc != ATTN_OK) return rc;
   const BiasArg ba = {bias, bias_stride_b, bias_stride_h, bias_stride_q};
-  if (attn_wide::supported(d)) return forward_wide(q8, k8, v, o, lse, B, H, Nq, Nk, d, eff, false, stream, &ba, true);
+  if (attn_wide::supported(d)) return forward_wide(q8, k8, v, o, lse, B, H, Nq, Nk, d, eff, false, stream, &ba, 1);
   return forward(q8, k8, v, &ba, o, lse, B, H, Nq, Nk, d, eff, stream, 1);
 }
 extern "C" int attn_fwd_fp8_bias(const void* q8, const void* k8, const void* vt8, long long ldv, const void* bias,
@@ -2098,6 +2112,8 @@ extern "C" int attn_fwd_fp8_bias(const void* q8, const void* k8, const void* vt8
   const float eff = fp8_scale(scale, q_descale, k_descale, v_descale, &rc);
   if (rc != ATTN_OK) return rc;
   const BiasArg ba = {bias, bias_stride_b, bias_stride_h, bias_stride_q};
+  if (attn_wide::supported(d))
+    return forward_wide(q8, k8, vt8, o, lse, B, H, Nq, Nk, d, eff, false, stream, &ba, 2, ldv, v_descale);
   return forward(q8, k8, vt8, &ba, o, lse, B, H, Nq, Nk, d, eff, stream, 2, ldv, v_descale);
 }
 extern "C" int attn_fwd_mxfp8_causal(const void* q8, const void* sq, const void* k8, const void* sk,

@@ -81,14 +81,56 @@ __device__ __forceinline__ void mma_ss_e4m3(uint32_t d, uint64_t a, uint64_t b, 
       "l"(a), "l"(b), "r"(idesc), "r"(static_cast<uint32_t>(acc))
       : "memory");
 }
+// D (TMEM) (+)= A (TMEM) * B (shared memory), 8-bit floating-point operands
+__device__ __forceinline__ void mma_ts_e4m3(uint32_t d, uint32_t a, uint64_t b, uint32_t idesc, bool acc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d),
+      "r"(a), "l"(b), "r"(idesc), "r"(static_cast<uint32_t>(acc))
+      : "memory");
+}
+// kind::f8f6f4 descriptor for O += P V with V as E4M3 codes: M = 128, N = d, A (P, in TMEM)
+// and B (V^T: d rows of keys) both K-major
+template <int D>
+constexpr uint32_t kIdPV8 =
+    (1u << 4) | (static_cast<uint32_t>(D >> 3) << 17) | (static_cast<uint32_t>(128 >> 4) << 24);
+// 16 columns of this warp's 32 TMEM lanes
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&x)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+      "%15, %16};\n\t"
+      "tcgen05.wait::st.sync.aligned;" ::"r"(taddr),
+      "r"(x[0]), "r"(x[1]), "r"(x[2]), "r"(x[3]), "r"(x[4]), "r"(x[5]), "r"(x[6]), "r"(x[7]), "r"(x[8]), "r"(x[9]),
+      "r"(x[10]), "r"(x[11]), "r"(x[12]), "r"(x[13]), "r"(x[14]), "r"(x[15])
+      : "memory");
+}
+// Four values rounded to E4M3 (nearest even, saturating), the first in the lowest byte
+// (cvt puts its first source in the upper half of its 16-bit result).
+__device__ __forceinline__ uint32_t pack_e4m3x4(float a0, float a1, float a2, float a3) {
+  uint16_t lo, hi;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(lo) : "f"(a1), "f"(a0));
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(hi) : "f"(a3), "f"(a2));
+  return static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
+}
+// x rounded to E4M3 as pack_e4m3x4 rounds it, widened back exactly (through FP16) to FP32
+__device__ __forceinline__ float round_e4m3(float x) {
+  uint16_t c;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(c) : "f"(0.0f), "f"(x));
+  uint32_t h2;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(c));
+  float r;
+  asm("cvt.f32.f16 %0, %1;" : "=f"(r) : "h"(static_cast<uint16_t>(h2 & 0xffffu)));
+  return r;
+}
 
 // barriers
 constexpr int kBarQFull = 0;
 constexpr int kBarQEmpty = 1;                     // the tile's last Q K^T is done with Q
 constexpr int kBarKFull = 2;                      // [box group]
 constexpr int kBarKFree = kBarKFull + kMaxChunks; // [box group]: the Q K^T steps that read it are done
-constexpr int kBarVFull = kBarKFree + kMaxChunks; // [half-tile slot]
-constexpr int kBarVFree = kBarVFull + kMaxVSlots; // [half-tile slot]: its half of P V is done
+constexpr int kBarVFull = kBarKFree + kMaxChunks; // [V slot]
+constexpr int kBarVFree = kBarVFull + kMaxVSlots; // [V slot]: the P V products that read it are done
 constexpr int kBarSFull = kBarVFree + kMaxVSlots; // [2 buffers]
 constexpr int kBarPFull = kBarSFull + 2;          // [step parity][half], one arrival per softmax warp
 constexpr int kBarOFull = kBarPFull + 4;
@@ -98,20 +140,23 @@ constexpr int kNumBars = kBarDrain + 1;
 constexpr int kFlagsBytes = kNumBars * 8 + 8;     // barriers, TMEM slot, abort flag
 
 // With a bias, each softmax warp stages its rows' bias in shared memory; at d = 256 that
-// room comes from one V slot. With Q and K as FP8 codes (kF8) a box holds 128 columns
+// room comes from one V slot. kF8 >= 1: Q and K as FP8 codes, a box holding 128 columns
 // (128 bytes) of the head dimension: two boxes per tile at d = 192 and 256 (at d = 192 the
-// second box's upper half lies past the tensor and is filled with zeros).
-template <int D, bool kBias, bool kF8 = false>
+// second box's upper half lies past the tensor and is filled with zeros). kF8 == 2: V too,
+// given as V^T codes (d rows of keys); a V slot then holds a whole key tile (d rows of 128
+// bytes), else one 64-key half of V.
+template <int D, bool kBias, int kF8 = 0>
 struct Layout {
   static constexpr int kChunks = D / kBoxCols;             // V boxes: 64 BF16 columns
-  static constexpr int kQKChunks = kF8 ? (D + 127) / 128 : kChunks;   // boxes per Q or K tile
+  static constexpr int kQKChunks = kF8 >= 1 ? (D + 127) / 128 : kChunks;   // boxes per Q or K tile
   static constexpr int kTileBytes = kQKChunks * kBoxBytes;  // one Q or K tile
   static constexpr int kHalfBytes = kChunks * kBoxBytes / 2;   // V: 64 keys x d
-  static constexpr int kVSlots = (kBias && D == 256 && !kF8) ? 2 : kMaxVSlots;
+  static constexpr int kVUnitBytes = kF8 == 2 ? D * kBN : kHalfBytes;   // one V slot
+  static constexpr int kVSlots = (kBias && D == 256 && kF8 == 0) ? 2 : kMaxVSlots;
   static constexpr int kOffQ = 0;
   static constexpr int kOffK = kOffQ + kTileBytes;
   static constexpr int kOffV = kOffK + kTileBytes;
-  static constexpr int kOffStage = kOffV + kVSlots * kHalfBytes;
+  static constexpr int kOffStage = kOffV + kVSlots * kVUnitBytes;
   static constexpr int kOffBar = kOffStage + (kBias ? 4 * kStageWarpBytes : 0);
   static constexpr int kSmem = kOffBar + kFlagsBytes + 1024;   // + realignment of the base to 1024
   static_assert(D % kBoxCols == 0 && kChunks <= kMaxChunks, "head dimension in whole boxes");
@@ -140,6 +185,7 @@ struct Params {
   long long bias_sb, bias_sh, bias_sq;
   int H;
   float scale;
+  float v_scale;   // V's descale factor (V as FP8 codes), applied with 1 / l
 };
 
 // The query tiles a block runs, in order; every role walks the same sequence. Plain: tile
@@ -211,16 +257,18 @@ __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wai
 // query tiles' key tiles, in order) uses S buffer gs & 1 and K tile gs (box c in K slot c);
 // its V halves are half tiles 2 gs and 2 gs + 1, in V slots (2 gs + h) % kVSlots. A ring
 // barrier completes once per use of its slot, so the k-th use waits for parity k & 1.
-template <int D, bool kPos, bool kBias, bool kF8>
+template <int D, bool kPos, bool kBias, int kF8>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                          const __grid_constant__ CUtensorMap tmV, const Params p) {
   using L = Layout<D, kBias, kF8>;
+  constexpr bool kQK8 = kF8 >= 1, kV8 = kF8 == 2;
   constexpr int kVSlots = L::kVSlots;
   constexpr int kChunks = L::kQKChunks;   // Q and K boxes
   constexpr int kVChunks = L::kChunks;    // V boxes
-  constexpr int kQKBoxCols = kF8 ? 128 : kBoxCols;   // head-dimension columns per Q or K box
-  constexpr int kKGroupBoxes = kF8 ? 1 : kKGroupBoxesFor<D>;
+  constexpr int kQKBoxCols = kQK8 ? 128 : kBoxCols;   // head-dimension columns per Q or K box
+  constexpr int kKGroupBoxes = kQK8 ? 1 : kKGroupBoxesFor<D>;
+  constexpr int kVUnits = kV8 ? 1 : 2;   // V slots per key tile
   constexpr int kKGroups = (kChunks + kKGroupBoxes - 1) / kKGroupBoxes;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -232,7 +280,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   c.abort = reinterpret_cast<volatile uint32_t*>(smem + L::kOffBar + kNumBars * 8 + 4);
   c.limit = p.wait_limit;
   const uint32_t sQ = base + L::kOffQ, sK = base + L::kOffK, sV = base + L::kOffV;
-  auto vslot = [&](int vi) { return sV + static_cast<uint32_t>(vi % kVSlots) * L::kHalfBytes; };
+  auto vslot = [&](int vi) { return sV + static_cast<uint32_t>(vi % kVSlots) * L::kVUnitBytes; };
 
   if (threadIdx.x == 0) {
     for (int b = 0; b < kNumBars; ++b) mbar_init(c.bar(b), 1);
@@ -277,17 +325,21 @@ __global__ void __launch_bounds__(kThreads, 1)
           k_loads[g] = gt + 1;
         }
       };
-      auto load_v = [&](int t, int bh) {   // both 64-key halves of V_t
-        for (int h = 0; ok && h < 2; ++h) {
-          const int vi = 2 * (gj + t) + h, slot = vi % kVSlots;
+      auto load_v = [&](int t, int bh) {   // both 64-key halves of V_t, or the V^T tile of step t
+        for (int h = 0; ok && h < kVUnits; ++h) {
+          const int vi = kVUnits * (gj + t) + h, slot = vi % kVSlots;
           if (vi >= kVSlots && !wait_phase(c, kBarVFree + slot, static_cast<uint32_t>(vi / kVSlots - 1) & 1u, true)) {
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(c.bar(kBarVFull + slot), L::kHalfBytes);
-          for (int cc = 0; cc < kVChunks; ++cc)
-            tma_load_3d(vslot(vi) + cc * (kBoxBytes / 2), &tmV, c.bar(kBarVFull + slot), cc * kBoxCols,
-                        t * kBN + h * (kBN / 2), bh);
+          mbar_arrive_expect_tx(c.bar(kBarVFull + slot), L::kVUnitBytes);
+          if constexpr (kV8) {   // keys t*128 .. t*128+127 of all d rows of V^T
+            tma_load_3d(vslot(vi), &tmV, c.bar(kBarVFull + slot), t * kBN, 0, bh);
+          } else {
+            for (int cc = 0; cc < kVChunks; ++cc)
+              tma_load_3d(vslot(vi) + cc * (kBoxBytes / 2), &tmV, c.bar(kBarVFull + slot), cc * kBoxCols,
+                          t * kBN + h * (kBN / 2), bh);
+          }
           v_halves = vi + 1;
         }
       };
@@ -335,12 +387,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int cc = c0; cc < c1; ++cc) {
             // 32 bytes of each 128-byte row per MMA: 16 BF16 columns, or 32 FP8 columns (at
             // d = 192 the second FP8 box holds 64 columns: two MMAs)
-            const int steps = kF8 ? min(4, (D - cc * 128) / 32) : 4;
+            const int steps = kQK8 ? min(4, (D - cc * 128) / 32) : 4;
 #pragma unroll
             for (int k4 = 0; k4 < 4; ++k4) {
               if (k4 >= steps) break;
               const uint32_t off = static_cast<uint32_t>(cc * kBoxBytes + k4 * 32);
-              if constexpr (kF8)
+              if constexpr (kQK8)
                 mma_ss_e4m3(d_tmem, sdesc_sw128(sQ + off, 16, 1024), sdesc_sw128(sK + off, 16, 1024), kIdQK8,
                             cc > 0 || k4 > 0);
               else
@@ -375,12 +427,22 @@ __global__ void __launch_bounds__(kThreads, 1)
               break;
             }
             tc_fence_after();
-            const int vi = 2 * gs + h;
+            if constexpr (kV8) {
+              // P as E4M3 (four keys per TMEM column: 32 keys = 8 columns per MMA) times V^T
+              // (d rows of the tile's 128 keys, K-major like K): 32 bytes of each row per MMA
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk)   // 16 keys per MMA: 8 columns of packed P
-              mma_ts(tO, tS[buf] + (4 * h + kk) * 8, sdesc_sw128(vslot(vi) + kk * 16 * 128, kBoxBytes / 2, 1024),
-                     kIdPV, j > 0 || h > 0 || kk > 0);
-            tc_commit(c.bar(kBarVFree + vi % kVSlots));
+              for (int kk = 2 * h; kk < 2 * h + 2; ++kk)
+                mma_ts_e4m3(tO, tS[buf] + kk * 8, sdesc_sw128(vslot(gs) + kk * 32, 16, 1024), kIdPV8<D>,
+                            j > 0 || kk > 0);
+              if (h == 1) tc_commit(c.bar(kBarVFree + gs % kVSlots));
+            } else {
+              const int vi = 2 * gs + h;
+#pragma unroll
+              for (int kk = 0; kk < 4; ++kk)   // 16 keys per MMA: 8 columns of packed P
+                mma_ts(tO, tS[buf] + (4 * h + kk) * 8, sdesc_sw128(vslot(vi) + kk * 16 * 128, kBoxBytes / 2, 1024),
+                       kIdPV, j > 0 || h > 0 || kk > 0);
+              tc_commit(c.bar(kBarVFree + vi % kVSlots));
+            }
           }
           if (!ok) break;
           if (j + 2 < n) {
@@ -503,7 +565,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float m_tile = m_raw * cs;
         bool rescale = false;
         float alpha = 1.0f;
-        if (m_tile > m_used + kRescaleLog2) {
+        // (P as E4M3 must stay below its largest finite value, 448: tau = 8)
+        if (m_tile > m_used + (kV8 ? 8.0f : kRescaleLog2)) {
           alpha = ex2(m_used - m_tile);   // 0 on a tile's first step
           l *= alpha;
           corr *= alpha;
@@ -514,7 +577,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           // O must hold the previous step's P V before it is rescaled (S_j's product was
           // issued before that one), and be rescaled before this step's accumulates: wait
           // for the commit of the previous step's second half (V half 2 gs - 1)
-          const int vi = 2 * gs - 1;
+          const int vi = kV8 ? gs - 1 : 2 * gs - 1;
           if (!wait_warp(c, kBarVFree + vi % kVSlots, static_cast<uint32_t>(vi / kVSlots) & 1u)) {
             ok = false;
             break;
@@ -536,30 +599,53 @@ __global__ void __launch_bounds__(kThreads, 1)
           // the BF16 rounding error of the tile's largest weight, with the arithmetic that
           // forms it below: l + corr is then the sum of the weights the tensor cores apply
           const float pm = (kBias && m_tile == -INFINITY) ? 0.0f : ex2(fmaf(m_raw, cs, neg_m));
-          corr += __uint_as_float(pack_bf16(pm, 0.0f) << 16) - pm;
+          if constexpr (kV8)
+            corr += round_e4m3(pm) - pm;
+          else
+            corr += __uint_as_float(pack_bf16(pm, 0.0f) << 16) - pm;
         }
         float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
         const float2 cs2 = make_float2(cs, cs), nm2 = make_float2(neg_m, neg_m);
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
-          uint32_t pk[32];
+          if constexpr (kV8) {   // 64 keys = 16 columns of four E4M3 values
+            uint32_t pk[16];
 #pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            const int e = half * 64 + 2 * i;
-            const float2 a2 = ffma2(make_float2(s[e], s[e + 1]), cs2, nm2);
-            const float e0 = ex2(a2.x), e1 = ex2(a2.y);
-            pk[i] = pack_bf16(e0, e1);
-            const float2 t2 = fadd2(make_float2(acc[2 * (i & 3)], acc[2 * (i & 3) + 1]), make_float2(e0, e1));
-            acc[2 * (i & 3)] = t2.x;
-            acc[2 * (i & 3) + 1] = t2.y;
+            for (int i = 0; i < 16; ++i) {
+              const int e = half * 64 + 4 * i;
+              const float2 a2 = ffma2(make_float2(s[e], s[e + 1]), cs2, nm2);
+              const float2 b2 = ffma2(make_float2(s[e + 2], s[e + 3]), cs2, nm2);
+              const float e0 = ex2(a2.x), e1 = ex2(a2.y), e2 = ex2(b2.x), e3 = ex2(b2.y);
+              pk[i] = pack_e4m3x4(e0, e1, e2, e3);
+              const int r = 2 * (i & 1);
+              const float2 t2 = fadd2(make_float2(acc[2 * r], acc[2 * r + 1]), make_float2(e0, e1));
+              const float2 t3 = fadd2(make_float2(acc[2 * r + 2], acc[2 * r + 3]), make_float2(e2, e3));
+              acc[2 * r] = t2.x;
+              acc[2 * r + 1] = t2.y;
+              acc[2 * r + 2] = t3.x;
+              acc[2 * r + 3] = t3.y;
+            }
+            tmem_st16(tS[buf] + half * 16, pk);
+          } else {
+            uint32_t pk[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              const int e = half * 64 + 2 * i;
+              const float2 a2 = ffma2(make_float2(s[e], s[e + 1]), cs2, nm2);
+              const float e0 = ex2(a2.x), e1 = ex2(a2.y);
+              pk[i] = pack_bf16(e0, e1);
+              const float2 t2 = fadd2(make_float2(acc[2 * (i & 3)], acc[2 * (i & 3) + 1]), make_float2(e0, e1));
+              acc[2 * (i & 3)] = t2.x;
+              acc[2 * (i & 3) + 1] = t2.y;
+            }
+            tmem_st<32>(tS[buf] + half * 32, pk);
           }
-          tmem_st<32>(tS[buf] + half * 32, pk);
           tc_fence_before();
           __syncwarp();
-          // the MMAs this hand-over releases read this half's V
+          // the MMAs this hand-over releases read this half's V (the step's V^T tile)
           bool landed = true;
           if (ringer) {
-            const int vi = 2 * gs + half;
+            const int vi = kV8 ? gs : 2 * gs + half;
             landed = wait_phase(c, kBarVFull + vi % kVSlots, static_cast<uint32_t>(vi / kVSlots) & 1u, true);
           }
           if (!__shfl_sync(0xffffffffu, landed, 0)) {
@@ -577,7 +663,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // epilogue: O / (l + corr) as BF16, each thread its own row; the natural-log LSE
       const int row = qt * kBM + quarter * 32 + lane;
       const bool live = row < p.Nq;
-      const float inv_l = 1.0f / (l + corr);
+      const float inv_l = (kV8 ? p.v_scale : 1.0f) / (l + corr);
       uint4* orow = reinterpret_cast<uint4*>(p.o + (static_cast<size_t>(bh) * p.Nq + (live ? row : 0)) * D);
 #pragma unroll 1
       for (int ch = 0; ch < D / 32; ++ch) {
@@ -647,14 +733,28 @@ bool make_map(CUtensorMap* map, const void* ptr, int rows, long long bh, int d, 
 }
 
 constexpr int kMaxDevices = 64;
-// per instantiation (d, sign of the scale or bias, FP8 Q and K) and device
-std::atomic<int> g_attr_done[12][kMaxDevices];
+// V^T as E4M3 codes, [BH, d, ldv] with keys innermost (Nk of each row of ldv used); box =
+// 128 keys x d rows x 1, one 128-byte swizzle span per row.
+bool make_map_vt(CUtensorMap* map, const void* ptr, int Nk, long long ldv, long long bh, int d) {
+  auto enc = encoder();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(Nk), static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(bh)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(ldv), static_cast<cuuint64_t>(ldv) * d};
+  cuuint32_t box[3] = {static_cast<cuuint32_t>(kBN), static_cast<cuuint32_t>(d), 1};
+  cuuint32_t elem[3] = {1, 1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(ptr), dims, strides, box, elem,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
 
-template <int D, bool kPos, bool kBias, bool kF8>
+// per instantiation (d, sign of the scale or bias, 8-bit inputs) and device
+std::atomic<int> g_attr_done[18][kMaxDevices];
+
+template <int D, bool kPos, bool kBias, int kF8>
 int launch(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, const Params& p, int grid, int dev,
            cudaStream_t stream) {
   auto kern = attn_fwd_wide_kernel<D, kPos, kBias, kF8>;
-  constexpr int kInst = 2 * ((D == 256 ? 3 : 0) + (kBias ? 2 : (kPos ? 1 : 0))) + (kF8 ? 1 : 0);
+  constexpr int kInst = 3 * ((D == 256 ? 3 : 0) + (kBias ? 2 : (kPos ? 1 : 0))) + kF8;
   constexpr int kSmem = Layout<D, kBias, kF8>::kSmem;
   if (dev < 0 || dev >= kMaxDevices || !g_attr_done[kInst][dev].load(std::memory_order_acquire)) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem) != cudaSuccess)
@@ -671,8 +771,8 @@ int launch(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, 
 
 }  // namespace
 
-// One head dimension, scale sign, bias and Q/K format.
-template <int D, bool kF8>
+// One head dimension, scale sign, bias and input format.
+template <int D, int kF8>
 int launch_d(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, const Params& p, int grid, int dev,
              cudaStream_t stream, bool bias, float scale) {
   // with a bias the scale is applied before the row max: one instantiation serves any sign
@@ -682,7 +782,8 @@ int launch_d(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv
 }
 
 int forward(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Nq, int Nk, int d,
-            float scale, bool causal, cudaStream_t stream, unsigned long long wait_limit, const Bias* bias, bool qk8) {
+            float scale, bool causal, cudaStream_t stream, unsigned long long wait_limit, const Bias* bias, int f8,
+            long long ldv, float v_scale) {
   if (!supported(d)) return ATTN_ERR_UNSUPPORTED;
   const long long bh = static_cast<long long>(B) * H;
   const long long q_tiles = (static_cast<long long>(Nq) + kBM - 1) / kBM;
@@ -692,8 +793,8 @@ int forward(const void* q, const void* k, const void* v, void* o, float* lse, in
       cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
     return ATTN_ERR_CUDA;
   CUtensorMap mq, mk, mv;
-  if (!make_map(&mq, q, Nq, bh, d, kBM, qk8) || !make_map(&mk, k, Nk, bh, d, kBN, qk8) ||
-      !make_map(&mv, v, Nk, bh, d, kBN / 2))
+  if (!make_map(&mq, q, Nq, bh, d, kBM, f8 >= 1) || !make_map(&mk, k, Nk, bh, d, kBN, f8 >= 1) ||
+      !(f8 == 2 ? make_map_vt(&mv, v, Nk, ldv, bh, d) : make_map(&mv, v, Nk, bh, d, kBN / 2)))
     return ATTN_ERR_CUDA;
   Params p;
   p.o = static_cast<uint16_t*>(o);
@@ -715,13 +816,16 @@ int forward(const void* q, const void* k, const void* v, void* o, float* lse, in
   p.bias_sq = bias ? bias->sq : 0;
   p.H = H;
   p.scale = scale;
+  p.v_scale = v_scale;
   const int grid = std::min(sms, p.groups);
   const bool b = bias != nullptr;
   if (d == 256)
-    return qk8 ? launch_d<256, true>(mq, mk, mv, p, grid, dev, stream, b, scale)
-               : launch_d<256, false>(mq, mk, mv, p, grid, dev, stream, b, scale);
-  return qk8 ? launch_d<192, true>(mq, mk, mv, p, grid, dev, stream, b, scale)
-             : launch_d<192, false>(mq, mk, mv, p, grid, dev, stream, b, scale);
+    return f8 == 2   ? launch_d<256, 2>(mq, mk, mv, p, grid, dev, stream, b, scale)
+           : f8 == 1 ? launch_d<256, 1>(mq, mk, mv, p, grid, dev, stream, b, scale)
+                     : launch_d<256, 0>(mq, mk, mv, p, grid, dev, stream, b, scale);
+  return f8 == 2   ? launch_d<192, 2>(mq, mk, mv, p, grid, dev, stream, b, scale)
+         : f8 == 1 ? launch_d<192, 1>(mq, mk, mv, p, grid, dev, stream, b, scale)
+                   : launch_d<192, 0>(mq, mk, mv, p, grid, dev, stream, b, scale);
 }
 
 int take_status(cudaStream_t stream) {

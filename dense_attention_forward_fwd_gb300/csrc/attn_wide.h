@@ -20,13 +20,15 @@ struct Bias {
 // {192, 256}; arguments as attn_fwd (already validated by the caller: non-null, 16-byte
 // aligned, B*H, Nq, Nk >= 1, finite scale). causal: query i sees keys 0 .. i + Nk - Nq only
 // (the caller has checked Nq <= Nk). wait_limit: clock64 budget of each of the kernel's
-// waits. bias (or null): S = scale Q K^T + B as attn_fwd_bias (not with causal). qk8: q and
-// k hold FP8 E4M3 codes [B, H, N, d] (one byte each), Q K^T runs on kind::f8f6f4 and
-// `scale` already includes both descale factors. Returns an attn_status code; ATTN_OK once
-// the kernel is enqueued.
+// waits. bias (or null): S = scale Q K^T + B as attn_fwd_bias (not with causal). f8 >= 1: q
+// and k hold FP8 E4M3 codes [B, H, N, d] (one byte each), Q K^T runs on kind::f8f6f4 and
+// `scale` already includes both descale factors. f8 == 2: v holds V^T as E4M3 codes
+// [B, H, d, ldv] (keys innermost, ldv >= Nk a multiple of 16, checked by the caller), P is
+// rounded to E4M3 for a kind::f8f6f4 P V and O is scaled by v_scale. Returns an
+// attn_status code; ATTN_OK once the kernel is enqueued.
 int forward(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Nq, int Nk,
             int d, float scale, bool causal, cudaStream_t stream, unsigned long long wait_limit,
-            const Bias* bias = nullptr, bool qk8 = false);
+            const Bias* bias = nullptr, int f8 = 0, long long ldv = 0, float v_scale = 1.0f);
 
 // Reads and clears the kernel's device status word on `stream` (synchronising it): 1 if a
 // wait of a launch gave up since the last call, 0 if not, negative on a CUDA error.

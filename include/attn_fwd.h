@@ -21,7 +21,7 @@
  * Conventions shared by every entry point below:
  *   - Tensors are dense, C-ordered, [B, H, N, d] (batch, heads, sequence, head dim)
  *     with d = 128 (attn_fwd, attn_fwd_causal, attn_fwd_bias, attn_fwd_noalloc and the
- *     attn_fwd_fp8qk family also take 192 and 256), in device
+ *     attn_fwd_fp8qk and attn_fwd_fp8 families also take 192 and 256), in device
  *     memory reachable from the current CUDA device.
  *   - BF16 is IEEE-style bfloat16 (1 sign, 8 exponent, 7 mantissa bits), passed as
  *     raw 16-bit storage (void*).
@@ -160,7 +160,8 @@ int attn_fwd_bias(const void* q, const void* k, const void* v, const void* bias,
  * workspace and return values are otherwise those of attn_fwd. NaN codes give
  * unspecified results for the rows they reach. d = 192 and 256 run attn_fwd's
  * one-query-tile kernel with Q K^T on kind::f8f6f4 (so do attn_fwd_fp8qk_causal and
- * attn_fwd_fp8qk_bias); the other 8-bit entry points take d = 128 only.
+ * attn_fwd_fp8qk_bias, and the attn_fwd_fp8 family with P V on kind::f8f6f4 too); the
+ * MXFP8 entry points take d = 128 only.
  */
 int attn_fwd_fp8qk(const void* q8, const void* k8, const void* v, void* o, float* lse,
                    int B, int H, int Nq, int Nk, int d, float scale, float q_descale, float k_descale,

@@ -49,7 +49,7 @@ def test_reference_arm_prints_the_contract_line(flags):
 @pytest.mark.parametrize("flags", [("--mxfp8", "--bias", "full"), ("--fp8-qk", "--bias", "shared", "--causal"),
                                    ("--fp8", "--fp8-qk"),
                                    ("--bias", "full", "--causal"), ("--head-dim", "256", "--backward"),
-                                   ("--head-dim", "256", "--fp8"),
+                                   ("--head-dim", "256", "--mxfp8"),
                                    ("--fp8", "--backward")])
 def test_flags_without_an_entry_point_are_refused(flags):
     r = run_bench(*flags)
@@ -83,7 +83,8 @@ def test_traffic_keys_match_the_recorded_ones():
              "rect-4k-8k-bias-shared-fp8qk": ("rect-4k-8k", {"bias": "shared", "fp8_qk": True}),
              "square-4k-d256": ("square-4k", {"d": 256}),
              "square-4k-bias-shared-d256": ("square-4k", {"bias": "shared", "d": 256}),
-             "square-4k-fp8qk-d256": ("square-4k", {"fp8_qk": True, "d": 256})}
+             "square-4k-fp8qk-d256": ("square-4k", {"fp8_qk": True, "d": 256}),
+             "square-4k-fp8-d256": ("square-4k", {"fp8": True, "d": 256})}
     recorded = json.load(open(os.path.join(ROOT, "profiles", "traffic.json")))
     assert set(recorded) <= set(cases)
     for key, (name, over) in cases.items():

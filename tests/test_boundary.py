@@ -246,9 +246,10 @@ def call_fp8pv(q8=A, k8=A, vt8=A, ldv=128, o=A, lse=A, B=1, H=1, Nq=128, Nk=128,
     (dict(B=0), attn.ATTN_OK),
 ])
 @pytest.mark.parametrize("causal", [False, True])
-def test_fp8_argument_checks(kw, code, causal):
+@pytest.mark.parametrize("d", [128, 256])   # d = 256: the one-query-tile kernel's checks
+def test_fp8_argument_checks(kw, code, causal, d):
     before = attn.attn_fwd_kernel_count()
-    assert call_fp8pv(causal=causal, **kw) == code
+    assert call_fp8pv(causal=causal, **dict({"d": d}, **kw)) == code
     assert attn.attn_fwd_kernel_count() == before
 
 

@@ -75,6 +75,15 @@ def test_forward_wide_head_dims(gpu_lib, d, B, H, Nq, Nk):
     gpu_lib.attn_fwd_fp8qk(torch.from_numpy(q8).cuda(), torch.from_numpy(k8).cuda(), to_device(v8b), o, lse, B, H,
                            Nq, Nk, d, d ** -0.5, dq, dk)
     check(gpu_lib, ((fo, o), "bf16"), ((fl, lse), "f32"))
+    # attn_fwd_fp8 at the same head dimension (V^T as E4M3 codes too)
+    q8, k8, v8, dq, dk, dv = make_qkv_e4m3(B, H, Nq, Nk, d=d, seed=17600 + Nq + Nk + d)
+    ldv = (Nk + 15) // 16 * 16
+    vt = np.zeros((B, H, d, ldv), dtype=np.uint8)
+    vt[..., :Nk] = np.swapaxes(v8, 2, 3)
+    (fo, o), (fl, lse) = guarded((B, H, Nq, d), "bf16", "cuda"), guarded((B, H, Nq), "f32", "cuda")
+    gpu_lib.attn_fwd_fp8(torch.from_numpy(q8).cuda(), torch.from_numpy(k8).cuda(), torch.from_numpy(vt).cuda(), o, lse,
+                         B, H, Nq, Nk, d, d ** -0.5, dq, dk, dv)
+    check(gpu_lib, ((fo, o), "bf16"), ((fl, lse), "f32"))
 
 
 @pytest.mark.parametrize("B,H,Nq,Nk", SHAPES)

@@ -293,3 +293,68 @@ def test_wide_fp8qk_workload_sampled_rows(gpu_lib, d, name):
     w = by_name(name)
     rows = sample_rows(w.B, w.H, w.Nq, per_head=8)
     check_fp8_wide(gpu_lib, w.B, w.H, w.Nq, w.Nk, d, seed=w.seed + 8 * d, rows=rows)
+
+
+# ---- V as FP8 too (the attn_fwd_fp8 family at d > 128): P rounded to E4M3, P V on kind::f8f6f4 ----
+# The tolerance is the d = 128 one (derived in tests/test_fp8_tolerance.py by emulating the
+# kernel's rounding of P): it bounds each element of O, an average over keys, whatever d is.
+
+def check_fp8pv_wide(attn, B, H, Nq, Nk, d, seed, qk_mult=1.0, rows=None, causal=False, bias=None, ldv=None):
+    from dense_attention_forward_fwd_gb300.inputs import make_qkv_e4m3
+    from test_fp8_gpu import fp8pv_tolerance, run_fp8pv
+    import oracle
+    scale = d ** -0.5
+    q8, k8, v8, dq, dk, dv = make_qkv_e4m3(B, H, Nq, Nk, d=d, seed=seed, qk_mult=qk_mult)
+    o, lse = run_fp8pv(attn, q8, k8, v8, scale, dq, dk, dv, ldv, causal=causal, bias=bias)
+    o_ref, lse_ref = oracle.attention_rows_e4m3(q8, k8, v8, scale, dq, dk, dv, rows, causal=causal, bias=bias)
+    o, lse = o.reshape(-1, d), lse.reshape(-1)
+    if rows is not None:
+        o, lse = o[rows], lse[rows]
+    assert np.all(np.isfinite(o)) and np.all(np.isfinite(lse)), "non-finite output"
+    err = np.abs(o.astype(np.float64) - o_ref)
+    lse_err = np.abs(lse.astype(np.float64) - lse_ref) / np.maximum(1.0, np.abs(lse_ref))
+    t_max, t_mean = fp8pv_tolerance(qk_mult, causal, bias is not None)
+    print(f"d={d} max {err.max():.3e} mean {err.mean():.3e} lse {lse_err.max():.3e}")
+    assert err.max() <= t_max and err.mean() <= t_mean and lse_err.max() <= 1e-4, \
+        f"max {err.max():.3e} mean {err.mean():.3e} lse {lse_err.max():.3e}"
+
+
+@pytest.mark.parametrize("d", [192, 256])
+@pytest.mark.parametrize("B,H,Nq,Nk", [
+    (1, 1, 128, 128),
+    (2, 3, 300, 1000),    # ragged tails; V^T rows padded to 1008 bytes (NaN codes past Nk)
+    (1, 1, 1, 200),
+    (1, 2, 129, 129),
+    (1, 2, 128, 2176),    # 17 key steps: the V^T ring wraps
+    (2, 8, 2048, 1024),   # more query tiles than blocks
+])
+def test_wide_fp8_parity(gpu_lib, d, B, H, Nq, Nk):
+    check_fp8pv_wide(gpu_lib, B, H, Nq, Nk, d, seed=19000 + Nq + Nk + d)
+
+
+@pytest.mark.parametrize("d", [192, 256])
+def test_wide_fp8_wide_row_stride(gpu_lib, d):
+    # V^T rows of 1,024 bytes for 640 keys
+    check_fp8pv_wide(gpu_lib, 1, 2, 384, 640, d, seed=19100 + d, ldv=1024)
+
+
+@pytest.mark.parametrize("d", [192, 256])
+def test_wide_fp8_causal_and_bias(gpu_lib, d):
+    check_fp8pv_wide(gpu_lib, 2, 3, 300, 1000, d, seed=19200 + d, causal=True)
+    bias = make_bias((1, 1, 384, 640), seed=19300 + d, std=2.0)
+    check_fp8pv_wide(gpu_lib, 1, 2, 384, 640, d, seed=19400 + d, bias=bias)
+
+
+def test_wide_fp8_peaked(gpu_lib):
+    # the running maximum moves late: with P in E4M3 the rescale threshold is 8 (P <= 256)
+    check_fp8pv_wide(gpu_lib, 1, 2, 512, 2048, 256, seed=19500, qk_mult=3.0)
+
+
+@pytest.mark.parametrize("d", [192, 256])
+@pytest.mark.parametrize("name", ["square-4k", "long-16k"])
+def test_wide_fp8_workload_sampled_rows(gpu_lib, d, name):
+    # as `bench.py --head-dim d --fp8` launches it
+    from dense_attention_forward_fwd_gb300.configs import by_name
+    w = by_name(name)
+    rows = sample_rows(w.B, w.H, w.Nq, per_head=8)
+    check_fp8pv_wide(gpu_lib, w.B, w.H, w.Nq, w.Nk, d, seed=w.seed + 16 * d, rows=rows)
