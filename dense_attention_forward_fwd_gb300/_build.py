@@ -17,7 +17,7 @@ LIB_PATH = os.path.join(PKG, "libattn_fwd.so")
 NVCC_FLAGS = [
     "-gencode", "arch=compute_103a,code=sm_103a",
     "-O3", "-lineinfo", "-std=c++17",
-    "-shared", "-Xcompiler", "-fPIC",
+    "-Xcompiler", "-fPIC",
 ]
 
 
@@ -43,9 +43,29 @@ def build_library(force: bool = False, extra_flags=(), out: str = LIB_PATH) -> s
         if not force and not _stale(out):
             return out
         tmp = out + f".tmp{os.getpid()}"
-        cmd = [nvcc_path(), *NVCC_FLAGS, *extra_flags, "-I", os.path.join(ROOT, "include"), "-o", tmp, *SOURCES]
-        res = subprocess.run(cmd, capture_output=True, text=True)
-        if res.returncode != 0:
-            raise RuntimeError(f"nvcc failed ({res.returncode}):\n{' '.join(cmd)}\n{res.stdout}\n{res.stderr}")
-        os.replace(tmp, out)
+        nvcc = nvcc_path()
+        # one nvcc per translation unit, all at once, then one link
+        objs = [f"{tmp}.{os.path.splitext(os.path.basename(src))[0]}.o" for src in SOURCES]
+        procs = []
+        for src, obj in zip(SOURCES, objs):
+            cmd = [nvcc, *NVCC_FLAGS, *extra_flags, "-I", os.path.join(ROOT, "include"), "-c", "-o", obj, src]
+            procs.append((cmd, subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.PIPE, text=True)))
+        try:
+            for cmd, proc in procs:
+                stdout, stderr = proc.communicate()
+                if proc.returncode != 0:
+                    raise RuntimeError(f"nvcc failed ({proc.returncode}):\n{' '.join(cmd)}\n{stdout}\n{stderr}")
+            cmd = [nvcc, "-gencode", "arch=compute_103a,code=sm_103a", "-shared", "-o", tmp, *objs]
+            res = subprocess.run(cmd, capture_output=True, text=True)
+            if res.returncode != 0:
+                raise RuntimeError(f"nvcc link failed ({res.returncode}):\n{' '.join(cmd)}\n{res.stdout}\n{res.stderr}")
+            os.replace(tmp, out)
+        finally:
+            for _, proc in procs:
+                if proc.poll() is None:
+                    proc.kill()
+                    proc.wait()
+            for obj in objs:
+                if os.path.exists(obj):
+                    os.remove(obj)
     return out
