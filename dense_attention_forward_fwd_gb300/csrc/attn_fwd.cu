@@ -1877,7 +1877,7 @@ int forward_wide(const void* q, const void* k, const void* v, void* o, float* ls
   }
   const int rc = attn_wide::forward(q, k, v, o, lse, B, H, Nq, Nk, d, scale, causal, static_cast<cudaStream_t>(stream),
                                     g_wait_limit.load(std::memory_order_relaxed), bias != nullptr ? &wb : nullptr, f8,
-                                    ldv, v_scale);
+                                    ldv, v_scale, g_withhold.load(std::memory_order_relaxed));
   if (rc == ATTN_OK) g_launches.fetch_add(1, std::memory_order_relaxed);
   return rc;
 }

@@ -186,6 +186,7 @@ struct Params {
   int H;
   float scale;
   float v_scale;   // V's descale factor (V as FP8 codes), applied with 1 / l
+  int withhold;    // test hook: never load a block's first V unit, so that a wait for it runs out
 };
 
 // The query tiles a block runs, in order; every role walks the same sequence. Plain: tile
@@ -328,6 +329,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       auto load_v = [&](int t, int bh) {   // both 64-key halves of V_t, or the V^T tile of step t
         for (int h = 0; ok && h < kVUnits; ++h) {
           const int vi = kVUnits * (gj + t) + h, slot = vi % kVSlots;
+          if (p.withhold && vi == 0) {   // (the test hook) the unit is never requested
+            v_halves = vi + 1;
+            continue;
+          }
           if (vi >= kVSlots && !wait_phase(c, kBarVFree + slot, static_cast<uint32_t>(vi / kVSlots - 1) & 1u, true)) {
             ok = false;
             break;
@@ -783,7 +788,7 @@ int launch_d(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv
 
 int forward(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Nq, int Nk, int d,
             float scale, bool causal, cudaStream_t stream, unsigned long long wait_limit, const Bias* bias, int f8,
-            long long ldv, float v_scale) {
+            long long ldv, float v_scale, int withhold) {
   if (!supported(d)) return ATTN_ERR_UNSUPPORTED;
   const long long bh = static_cast<long long>(B) * H;
   const long long q_tiles = (static_cast<long long>(Nq) + kBM - 1) / kBM;
@@ -817,6 +822,7 @@ int forward(const void* q, const void* k, const void* v, void* o, float* lse, in
   p.H = H;
   p.scale = scale;
   p.v_scale = v_scale;
+  p.withhold = withhold;
   const int grid = std::min(sms, p.groups);
   const bool b = bias != nullptr;
   if (d == 256)

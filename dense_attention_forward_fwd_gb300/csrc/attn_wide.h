@@ -24,11 +24,13 @@ struct Bias {
 // and k hold FP8 E4M3 codes [B, H, N, d] (one byte each), Q K^T runs on kind::f8f6f4 and
 // `scale` already includes both descale factors. f8 == 2: v holds V^T as E4M3 codes
 // [B, H, d, ldv] (keys innermost, ldv >= Nk a multiple of 16, checked by the caller), P is
-// rounded to E4M3 for a kind::f8f6f4 P V and O is scaled by v_scale. Returns an
-// attn_status code; ATTN_OK once the kernel is enqueued.
+// rounded to E4M3 for a kind::f8f6f4 P V and O is scaled by v_scale. withhold (a test
+// hook): each block skips the load of its first V unit, so that the wait for it runs out
+// and the launch takes its timeout exit. Returns an attn_status code; ATTN_OK once the
+// kernel is enqueued.
 int forward(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Nq, int Nk,
             int d, float scale, bool causal, cudaStream_t stream, unsigned long long wait_limit,
-            const Bias* bias = nullptr, int f8 = 0, long long ldv = 0, float v_scale = 1.0f);
+            const Bias* bias = nullptr, int f8 = 0, long long ldv = 0, float v_scale = 1.0f, int withhold = 0);
 
 // Reads and clears the kernel's device status word on `stream` (synchronising it): 1 if a
 // wait of a launch gave up since the last call, 0 if not, negative on a CUDA error.

@@ -343,8 +343,9 @@ const char* attn_status_string(int status);
  * attn_fwd_set_wait_limit -- test hook for the failure path. Sets, process-wide and for
  * launches enqueued after the call, the time limit of every in-kernel wait in SM clock
  * cycles (0 restores the default of 2^31 cycles, about one second) and whether launches
- * withhold one K/V tile load (withhold_tile != 0), so that the consumer's wait for it
- * runs out and the kernel takes its timeout exit. No GPU fault is involved: the kernel
+ * withhold one K/V tile load (withhold_tile != 0; at d = 192 and 256 the first V unit of
+ * each block), so that the consumer's wait for it runs out and the kernel takes its
+ * timeout exit. No GPU fault is involved: the kernel
  * returns normally and attn_fwd_status reports ATTN_ERR_TIMEOUT. Returns ATTN_OK.
  * No counterpart on the pages.
  */

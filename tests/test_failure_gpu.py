@@ -61,3 +61,26 @@ def test_backward_withheld_tile_times_out_cleanly(gpu_lib):
     assert status == attn.ATTN_ERR_TIMEOUT
     assert attn.attn_bwd_status() == attn.ATTN_OK
     check_bwd(attn, 1, 2, 512, 384, seed=24)
+
+
+@pytest.mark.parametrize("d", [192, 256])
+def test_wide_withheld_tile_times_out_cleanly(gpu_lib, d):
+    # d > 128 (the one-query-tile kernel): every block skips its first V unit; the softmax
+    # thread that checks V before handing P over gives up, the other roles see the abort
+    # flag, and the launch ends with ATTN_ERR_TIMEOUT
+    import torch
+    attn = gpu_lib
+    q, k, v = make_qkv(1, 2, 384, 640, d=d, seed=25 + d)
+    qd, kd, vd = to_device(q), to_device(k), to_device(v)
+    o = torch.zeros((1, 2, 384, d), dtype=torch.bfloat16, device="cuda")
+    lse = torch.zeros((1, 2, 384), dtype=torch.float32, device="cuda")
+    assert attn.attn_fwd_status() == attn.ATTN_OK
+    attn.attn_fwd_set_wait_limit(SHORT_LIMIT, withhold_tile=True)
+    try:
+        attn.attn_fwd(qd, kd, vd, o, lse, 1, 2, 384, 640, d, d ** -0.5)
+        status = attn.attn_fwd_status()
+    finally:
+        attn.attn_fwd_set_wait_limit(0, withhold_tile=False)
+    assert status == attn.ATTN_ERR_TIMEOUT
+    assert attn.attn_fwd_status() == attn.ATTN_OK
+    check_case(attn, 1, 2, 384, 640, seed=25 + d, d=d)
